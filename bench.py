@@ -1,0 +1,383 @@
+#!/usr/bin/env python
+"""Benchmark of the block-sparse (Splash) masked attention forward hot path.
+
+One step = one pass of the whole hot path on one batch of seeded synthetic
+input: the MaskInfo build (classification, compaction, pattern dedup) into a
+reused handle, then the attention forward.  The default workload is the
+dense-causal GQA configuration (B=2, Hq=32, Hkv=8, L=4096, d=128, 128x128
+blocks).  Inputs are resident in HBM when the timed region starts; L2 is
+flushed (a 256 MiB write) between timed steps, outside the timed events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (launched by torch.distributed.run) every rank runs the same
+workload on its own GPU (independent replicas, weak scaling); the timing is
+the max over ranks.  `--impl reference` times the CPU oracle (the plain f64
+implementation) on the host cores, on bounded samples of the same workload.
+Prints one JSON line on rank 0.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "masked attn fwd useful TFLOP/s & % of GB300 BF16 tensor peak; ms per call"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+# --------------------------------------------------------------------- accounting
+def flop_counts(w, counts, batch_rows):
+    """Useful FLOPs (unmasked (q, k) pairs only) and executed FLOPs (every
+    element of every active block) of one forward pass."""
+    per_pair = 2 * (w.dqk + w.dv)
+    rep = w.Hq * (w.B if batch_rows == 1 else 1)
+    useful = per_pair * counts["allowed_pairs"] * rep
+    executed = per_pair * w.bq * w.bk * counts["num_active"] * rep
+    return float(useful), float(executed)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def reduce_max(value, world, device=None):
+    """Max of a float over ranks (identity for one rank)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_throughput(flop_per_step_per_rank, world, ms_per_step_max):
+    """Aggregate over ranks: every rank processes its own copy of the workload."""
+    return world * flop_per_step_per_rank / (ms_per_step_max * 1e-3) / 1e12
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.device_index = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.device_index), "-lms", "50"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------- CPU oracle timing
+def oracle_sample_rate(w, inp, nrows, seed, nthreads=0):
+    """Times the oracle on `nrows` seeded random query rows of the workload;
+    returns (useful FLOP of those rows, seconds, threads)."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(w.B * w.Hq * w.L, size=min(nrows, w.B * w.Hq * w.L), replace=False))
+    seg = inp.segment_ids.numpy() if inp.segment_ids is not None else None
+    spec = oracle.MaskSpec(w.causal, w.window_left, w.window_right, seg, seg)
+    nth = nthreads or oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.attention(inp.q, inp.k, inp.v, spec, w.scale, w.softcap, rows=rows, nthreads=nth)
+    dt = time.perf_counter() - t0
+    # allowed keys of each sampled row (counted from the mask definition)
+    i = rows % w.L
+    b = rows // (w.Hq * w.L)
+    allowed = np.zeros(len(rows), dtype=np.int64)
+    for x in range(len(rows)):
+        j = np.arange(w.L)
+        ok = np.ones(w.L, dtype=bool)
+        if w.causal:
+            ok &= j <= i[x]
+        if w.window_left >= 0:
+            ok &= i[x] - j <= w.window_left
+        if w.window_right >= 0:
+            ok &= j - i[x] <= w.window_right
+        if seg is not None:
+            ok &= seg[b[x]] == seg[b[x], i[x]]
+        allowed[x] = int(ok.sum())
+    return 2.0 * (w.dqk + w.dv) * float(allowed.sum()), dt, nth, len(rows)
+
+
+def cpu_baseline(w, inp, target_s=12.0):
+    flop, dt, nth, n = oracle_sample_rate(w, inp, 256, 7)
+    rate = n / max(dt, 1e-6)
+    nrows = int(min(w.B * w.Hq * w.L, max(256, rate * target_s)))
+    flop, dt, nth, n = oracle_sample_rate(w, inp, nrows, 8)
+    return {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": nth, "kind": "oracle",
+            "sample": f"{n} seeded random query rows of the workload (all heads/batches), f64 oracle, "
+                      f"{dt:.1f} s wall; useful FLOPs of those rows / time"}
+
+
+# --------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import block_sparse_flash_gb300 as bsf
+    from block_sparse_flash_gb300 import build as libbuild
+    import workloads
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        libbuild.build()
+    if world > 1:
+        dist.barrier()
+    bsf.lib()
+
+    w = workloads.workload(args.workload)
+    inp = workloads.make_inputs(w)
+    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    seg = inp.segment_ids.to(dev) if inp.segment_ids is not None else None
+    spec = bsf.MaskSpec(w.causal, w.window_left, w.window_right, seg, seg)
+    mi = bsf.build_mask_info(spec, w.L, w.L, w.bq, w.bk)
+    counts = mi.counts()
+    batch_rows = mi.shape()["batch_rows"]
+    useful, executed = flop_counts(w, counts, batch_rows)
+    out = torch.empty((w.B, w.Hq, w.L, w.dv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Hq, w.L), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(attn_events=None):
+        mi.rebuild(spec, w.L, w.L, w.bq, w.bk)
+        if attn_events:
+            attn_events[0].record()
+        bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, out=out, lse=lse)
+        if attn_events:
+            attn_events[1].record()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    bsf.check_device_error()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    ea = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    launches0 = bsf.kernel_launches()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record()
+        step(ea[i])
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    launches = bsf.kernel_launches() - launches0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    bsf.check_device_error()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    attn_ms = [a.elapsed_time(b) for a, b in ea]
+    ms_step = reduce_max(statistics.mean(step_ms), world, dev)
+    ms_attn = reduce_max(statistics.mean(attn_ms), world, dev)
+    value = whole_job_throughput(useful, world, ms_step)
+
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = executed / (ms_attn * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "kernel": "splash_fwd_kernel", "peak_source": f"{peak_src} bf16 burst (cuBLAS)",
+                "achieved_is": "executed FLOPs of the active blocks per launch / mean launch time (CUDA events)"}
+    traffic_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(traffic_path):
+        with open(traffic_path) as f:
+            tr = json.load(f).get(f"workload{args.workload}")
+        if tr:
+            roofline["traffic"] = tr.get("bytes_per_launch")
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(bsf, w, inp, spec, mi, dev, K=max(3, min(K, 20)), world=world, useful=useful)
+
+    result = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, see workloads/)",
+        "config": {"workload": w.describe(), "step": "MaskInfo rebuild + attention forward",
+                   "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
+                   "active_blocks": counts["num_active"], "partial_blocks": counts["num_partial"],
+                   "patterns": counts["num_patterns"], "parallelism": f"replicas x{world}"},
+        "attention_ms": round(ms_attn, 5),
+        "mask_build_ms": round(ms_step - ms_attn, 5),
+        "attention_useful_tflops": round(useful / (ms_attn * 1e-3) / 1e12, 2),
+        "attention_executed_tflops": round(achieved, 2),
+        "pct_of_bf16_peak_useful": round(100 * useful / (ms_attn * 1e-3) / 1e12 / peak, 2),
+        "pct_of_bf16_peak_executed": round(100 * achieved / peak, 2),
+        "roofline": roofline,
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    if e2e:
+        result["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, inp)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    mi.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(bsf, w, inp, spec, mi, dev, K, world, useful):
+    """Same metric through the public API with host buffers: pinned host ->
+    device copies of the inputs, the step, device -> host copies of O and LSE,
+    all inside the timed region."""
+    import torch
+    qh, kh, vh = inp.q.pin_memory(), inp.k.pin_memory(), inp.v.pin_memory()
+    segh = inp.segment_ids.pin_memory() if inp.segment_ids is not None else None
+    q = torch.empty_like(qh, device=dev)
+    k = torch.empty_like(kh, device=dev)
+    v = torch.empty_like(vh, device=dev)
+    seg = spec.q_segment_ids
+    out = torch.empty((w.B, w.Hq, w.L, w.dv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Hq, w.L), dtype=torch.float32, device=dev)
+    outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lseh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = qh.numel() * 2 + kh.numel() * 2 + vh.numel() * 2 + (segh.numel() * 4 if segh is not None else 0)
+    d2h = outh.numel() * 2 + lseh.numel() * 4
+    times = []
+    for i in range(K + 2):
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        q.copy_(qh, non_blocking=True)
+        k.copy_(kh, non_blocking=True)
+        v.copy_(vh, non_blocking=True)
+        if segh is not None:
+            seg.copy_(segh, non_blocking=True)
+        mi.rebuild(spec, w.L, w.L, w.bq, w.bk)
+        bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, out=out, lse=lse)
+        outh.copy_(out, non_blocking=True)
+        lseh.copy_(lse, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        if i >= 2:
+            times.append(a.elapsed_time(b))
+    ms = reduce_max(statistics.mean(times), world, dev)
+    return {"value": round(whole_job_throughput(useful, world, ms), 3), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# --------------------------------------------------------------------- reference arm
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import workloads
+    w = workloads.workload(args.workload)
+    inp = workloads.make_inputs(w)
+    _, dt, nth, n = oracle_sample_rate(w, inp, 128, 3)
+    rate = n / max(dt, 1e-6)
+    per_step = int(min(8192, max(64, rate * 90.0 / max(1, args.steps + args.warmup))))
+    for i in range(args.warmup):
+        oracle_sample_rate(w, inp, per_step, 100 + i)
+    flops, secs = 0.0, 0.0
+    for i in range(args.steps):
+        f, dt, nth, n = oracle_sample_rate(w, inp, per_step, 1000 + i)
+        flops += f
+        secs += dt
+    value = flops / secs / 1e12
+    sample = (f"{per_step} seeded random query rows per step (all heads/batches) of the workload, f64 oracle "
+              f"on {nth} host threads; useful FLOPs of the rows / wall time")
+    res = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded N(0,1) bf16, see workloads/)",
+           "config": {"workload": w.describe(), "step": f"oracle on {per_step} sampled rows"},
+           "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nth, "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

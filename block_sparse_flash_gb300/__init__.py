@@ -1,0 +1,258 @@
+"""block_sparse_flash_gb300 -- Python binding of libsplash.so, the sm_103a
+block-sparse (Splash) masked attention forward library.
+
+This module only marshals arguments: torch tensors become device pointers,
+the current torch stream becomes the cudaStream_t.  Every step of the
+computation runs in the library's CUDA kernels; there is no CPU or PyTorch
+fallback.  If the library has not been built, importing works but every call
+raises SplashLibraryMissing.
+
+    spec = MaskSpec(causal=True, window_left=4095)
+    mi = build_mask_info(spec, L, L, 128, 128)
+    out, lse = attention_fwd(q, k, v, mi, scale=1 / 128 ** 0.5, softcap=30.0)
+
+C ABI: include/splash.h.
+"""
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libsplash.so")
+
+SPLASH_OK = 0
+_STATUS = {
+    0: "SPLASH_OK", 1: "SPLASH_ERR_INVALID_ARG", 2: "SPLASH_ERR_SHAPE", 3: "SPLASH_ERR_UNSUPPORTED",
+    4: "SPLASH_ERR_CUDA", 5: "SPLASH_ERR_DEVICE_TIMEOUT", 6: "SPLASH_ERR_OOM", 7: "SPLASH_ERR_DEVICE_CHECK",
+}
+
+
+class SplashLibraryMissing(RuntimeError):
+    pass
+
+
+class SplashError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__(f"{what}: {_status_string(status)}")
+
+
+class _Spec(ctypes.Structure):
+    _fields_ = [
+        ("causal", ctypes.c_int32),
+        ("window_left", ctypes.c_int64),
+        ("window_right", ctypes.c_int64),
+        ("q_segment_ids", ctypes.c_void_p),
+        ("kv_segment_ids", ctypes.c_void_p),
+        ("batch", ctypes.c_int32),
+    ]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libsplash.so (ctypes.CDLL); raises SplashLibraryMissing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise SplashLibraryMissing(
+            f"{LIB_PATH} is missing: build it with block_sparse_flash_gb300.build.build() "
+            "(there is no fallback implementation)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    P = ctypes.POINTER
+    L.splash_build_mask_info.argtypes = [P(_Spec), i64, i64, i32, i32, vp, P(vp)]
+    L.splash_mask_info_rebuild.argtypes = [vp, P(_Spec), i64, i64, i32, i32, vp]
+    L.splash_mask_info_shape.argtypes = [vp, P(i32), P(i64), P(i64), P(i32), P(i32)]
+    L.splash_mask_info_counts.argtypes = [vp, P(i64), P(i64), P(i64), P(i64)]
+    L.splash_mask_info_to_host.argtypes = [vp] + [vp] * 8
+    L.splash_mask_info_destroy.argtypes = [vp]
+    L.splash_mask_info_destroy.restype = None
+    L.splash_attention_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i64, i64, i32, i32, vp, vp, vp, f32, f32,
+                                       vp, vp, vp]
+    L.splash_last_device_error.argtypes = [vp]
+    L.splash_debug_wait_selftest.argtypes = [ctypes.c_uint64, vp]
+    L.splash_status_string.argtypes = [ctypes.c_int]
+    L.splash_status_string.restype = ctypes.c_char_p
+    L.splash_version.argtypes = []
+    L.splash_version.restype = ctypes.c_char_p
+    L.splash_kernel_launches.argtypes = []
+    L.splash_kernel_launches.restype = ctypes.c_uint64
+    for f in (L.splash_build_mask_info, L.splash_mask_info_rebuild, L.splash_mask_info_shape,
+              L.splash_mask_info_counts, L.splash_mask_info_to_host, L.splash_attention_fwd,
+              L.splash_last_device_error, L.splash_debug_wait_selftest):
+        f.restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _status_string(s):
+    try:
+        return lib().splash_status_string(int(s)).decode()
+    except SplashLibraryMissing:
+        return _STATUS.get(int(s), f"status {s}")
+
+
+def _check(status, what):
+    if status != SPLASH_OK:
+        raise SplashError(status, what)
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+@dataclass
+class MaskSpec:
+    """Joint mask = causal AND window AND segment equality (splash_mask_spec).
+
+    window_left / window_right: inclusive distances, -1 = unbounded.
+    q_segment_ids / kv_segment_ids: int32 CUDA tensors [batch, L] (or [L]) or None.
+    """
+    causal: bool = False
+    window_left: int = -1
+    window_right: int = -1
+    q_segment_ids: Optional[torch.Tensor] = None
+    kv_segment_ids: Optional[torch.Tensor] = None
+
+    def _c(self):
+        qs, kvs, batch = self.q_segment_ids, self.kv_segment_ids, 0
+        for t in (qs, kvs):
+            if t is not None and (t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous()):
+                raise ValueError("segment ids must be contiguous int32 CUDA tensors")
+        if qs is not None:
+            batch = 1 if qs.dim() == 1 else qs.shape[0]
+        return _Spec(int(bool(self.causal)), int(self.window_left), int(self.window_right),
+                     qs.data_ptr() if qs is not None else None,
+                     kvs.data_ptr() if kvs is not None else None, batch)
+
+
+class MaskInfo:
+    """Owner of a splash_mask_info handle (device memory freed on close)."""
+
+    def __init__(self, handle):
+        self._h = ctypes.c_void_p(handle)
+
+    @property
+    def handle(self):
+        if not self._h:
+            raise ValueError("MaskInfo is closed")
+        return self._h
+
+    def close(self):
+        if self._h:
+            lib().splash_mask_info_destroy(self._h)
+            self._h = ctypes.c_void_p(0)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def rebuild(self, spec: MaskSpec, Lq, Lk, bq, bk, stream=None):
+        s = spec._c()
+        _check(lib().splash_mask_info_rebuild(self.handle, ctypes.byref(s), Lq, Lk, bq, bk, _stream(stream)),
+               "splash_mask_info_rebuild")
+        return self
+
+    def shape(self):
+        bm, bq, bk = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        nq, nk = ctypes.c_int64(), ctypes.c_int64()
+        _check(lib().splash_mask_info_shape(self.handle, ctypes.byref(bm), ctypes.byref(nq), ctypes.byref(nk),
+                                            ctypes.byref(bq), ctypes.byref(bk)), "splash_mask_info_shape")
+        return dict(batch_rows=bm.value, nq=nq.value, nk=nk.value, bq=bq.value, bk=bk.value)
+
+    def counts(self):
+        a, p, n, u = (ctypes.c_int64() for _ in range(4))
+        _check(lib().splash_mask_info_counts(self.handle, ctypes.byref(a), ctypes.byref(p), ctypes.byref(n),
+                                             ctypes.byref(u)), "splash_mask_info_counts")
+        return dict(num_active=a.value, num_partial=p.value, num_patterns=n.value, allowed_pairs=u.value)
+
+    def to_host(self):
+        """All table arrays as numpy arrays (synchronous copy)."""
+        sh, c = self.shape(), self.counts()
+        R, A, P = sh["batch_rows"] * sh["nq"], c["num_active"], c["num_patterns"]
+        out = dict(
+            block_mask=np.zeros((sh["batch_rows"], sh["nq"], sh["nk"]), dtype=np.int8),
+            row_ptr=np.zeros(R + 1, dtype=np.int32),
+            active_rows=np.zeros(max(A, 1), dtype=np.int32),
+            active_cols=np.zeros(max(A, 1), dtype=np.int32),
+            mask_next=np.zeros(max(A, 1), dtype=np.int32),
+            bounds_start=np.zeros(max(A, 1), dtype=np.uint8),
+            bounds_end=np.zeros(max(A, 1), dtype=np.uint8),
+            partial_mask_blocks=np.zeros((max(P, 1), sh["bq"], sh["bk"]), dtype=np.uint8),
+        )
+        order = ["block_mask", "row_ptr", "active_rows", "active_cols", "mask_next", "bounds_start",
+                 "bounds_end", "partial_mask_blocks"]
+        _check(lib().splash_mask_info_to_host(self.handle, *[out[k].ctypes.data for k in order]),
+               "splash_mask_info_to_host")
+        for k in ("active_rows", "active_cols", "mask_next", "bounds_start", "bounds_end"):
+            out[k] = out[k][:A]
+        out["partial_mask_blocks"] = out["partial_mask_blocks"][:P]
+        out.update(c)
+        out.update(sh)
+        return out
+
+
+def build_mask_info(spec: MaskSpec, Lq: int, Lk: int, bq: int, bk: int, stream=None) -> MaskInfo:
+    h = ctypes.c_void_p()
+    s = spec._c()
+    _check(lib().splash_build_mask_info(ctypes.byref(s), Lq, Lk, bq, bk, _stream(stream), ctypes.byref(h)),
+           "splash_build_mask_info")
+    return MaskInfo(h.value)
+
+
+def attention_fwd(q, k, v, mask_info: MaskInfo, scale: float, softcap: float = 0.0, q_segment_ids=None,
+                  kv_segment_ids=None, out=None, lse=None, stream=None):
+    """out [B, Hq, Lq, dv] bf16 and lse [B, Hq, Lq] fp32 (allocated if not given)."""
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError("q, k, v must be contiguous 4-D bf16 CUDA tensors")
+    B, Hq, Lq, dqk = q.shape
+    Hkv, Lk, dv = k.shape[1], k.shape[2], v.shape[3]
+    if out is None:
+        out = torch.empty((B, Hq, Lq, dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
+    _check(lib().splash_attention_fwd(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Lq, Lk, dqk, dv,
+                                      _ptr(q_segment_ids), _ptr(kv_segment_ids), mask_info.handle,
+                                      float(scale), float(softcap), _ptr(out), _ptr(lse), _stream(stream)),
+           "splash_attention_fwd")
+    return out, lse
+
+
+def last_device_error(stream=None) -> int:
+    """Synchronises and returns (and clears) the device error status code."""
+    return lib().splash_last_device_error(_stream(stream))
+
+
+def check_device_error(stream=None):
+    _check(last_device_error(stream), "device")
+
+
+def debug_wait_selftest(timeout_ns: int, stream=None) -> int:
+    return lib().splash_debug_wait_selftest(int(timeout_ns), _stream(stream))
+
+
+def kernel_launches() -> int:
+    """Kernels launched by the library in this process so far."""
+    return int(lib().splash_kernel_launches())
+
+
+def version() -> str:
+    return lib().splash_version().decode()

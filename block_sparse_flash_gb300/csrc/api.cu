@@ -1,0 +1,232 @@
+// api.cu -- the extern "C" boundary of libsplash.so (declared in splash.h):
+// argument validation, MaskInfo handles, the device error word.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "internal.h"
+
+namespace {
+
+// The device error word: kernels atomicOr error bits into it.  One copy per
+// device (a __device__ variable); host code reaches it through
+// cudaGetSymbolAddress, resolved once per device.
+__device__ uint32_t g_error_word;
+
+constexpr int kMaxDevices = 64;
+uint32_t *g_error_addr[kMaxDevices];
+std::mutex g_error_mu;
+
+bool valid_block(int32_t b) { return b == 64 || b == 128; }
+
+splash_status check_spec(const splash_mask_spec *spec, int64_t Lq, int64_t Lk) {
+  if (spec == nullptr) return SPLASH_ERR_INVALID_ARG;
+  if (spec->causal != 0 && spec->causal != 1) return SPLASH_ERR_INVALID_ARG;
+  if (spec->window_left < -1 || spec->window_right < -1) return SPLASH_ERR_INVALID_ARG;
+  if (spec->q_segment_ids != nullptr) {
+    if (spec->batch <= 0) return SPLASH_ERR_INVALID_ARG;
+    if (spec->kv_segment_ids == nullptr && Lq != Lk) return SPLASH_ERR_SHAPE;
+  } else if (spec->kv_segment_ids != nullptr) {
+    return SPLASH_ERR_INVALID_ARG;
+  }
+  return SPLASH_OK;
+}
+
+splash_status check_geometry(int64_t Lq, int64_t Lk, int32_t bq, int32_t bk) {
+  if (Lq <= 0 || Lk <= 0 || bq <= 0 || bk <= 0) return SPLASH_ERR_INVALID_ARG;
+  if (!valid_block(bq) || !valid_block(bk)) return SPLASH_ERR_UNSUPPORTED;
+  if (Lq % bq != 0 || Lk % bk != 0) return SPLASH_ERR_UNSUPPORTED;  // ragged lengths: not in this build
+  if (Lq / bq > 65535 || Lk > (int64_t)1 << 30 || Lq > (int64_t)1 << 30) return SPLASH_ERR_UNSUPPORTED;
+  return SPLASH_OK;
+}
+
+}  // namespace
+
+static std::atomic<uint64_t> g_launches{0};
+
+void splash_count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+uint32_t *splash_device_error_word(int device) {
+  if (device < 0 || device >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_error_mu);
+  if (g_error_addr[device] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_error_addr[device] = static_cast<uint32_t *>(p);
+  }
+  return g_error_addr[device];
+}
+
+extern "C" {
+
+const char *splash_status_string(splash_status s) {
+  switch (s) {
+    case SPLASH_OK: return "SPLASH_OK";
+    case SPLASH_ERR_INVALID_ARG: return "SPLASH_ERR_INVALID_ARG: invalid argument";
+    case SPLASH_ERR_SHAPE: return "SPLASH_ERR_SHAPE: inconsistent shapes";
+    case SPLASH_ERR_UNSUPPORTED: return "SPLASH_ERR_UNSUPPORTED: shape or block size not supported by this build";
+    case SPLASH_ERR_CUDA: return "SPLASH_ERR_CUDA: a CUDA call failed";
+    case SPLASH_ERR_DEVICE_TIMEOUT: return "SPLASH_ERR_DEVICE_TIMEOUT: a kernel's bounded wait ran out";
+    case SPLASH_ERR_OOM: return "SPLASH_ERR_OOM: device allocation failed";
+    case SPLASH_ERR_DEVICE_CHECK: return "SPLASH_ERR_DEVICE_CHECK: a kernel rejected a table entry";
+  }
+  return "SPLASH_ERR_UNKNOWN";
+}
+
+const char *splash_version(void) { return "splash-gb300 0.1 sm_103a"; }
+
+uint64_t splash_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+splash_status splash_mask_info_rebuild(splash_mask_info *mi, const splash_mask_spec *spec, int64_t Lq,
+                                       int64_t Lk, int32_t bq, int32_t bk, void *cuda_stream) {
+  if (mi == nullptr) return SPLASH_ERR_INVALID_ARG;
+  splash_status st = check_spec(spec, Lq, Lk);
+  if (st != SPLASH_OK) return st;
+  if ((st = check_geometry(Lq, Lk, bq, bk)) != SPLASH_OK) return st;
+  int dev = 0;
+  SPLASH_CUDA_TRY(cudaGetDevice(&dev));
+  if (mi->device >= 0 && mi->device != dev) return SPLASH_ERR_INVALID_ARG;
+  mi->device = dev;
+  st = splash_mask_info_build_into(mi, spec, Lq, Lk, bq, bk, static_cast<cudaStream_t>(cuda_stream));
+  if (st != SPLASH_OK) {
+    mi->num_active = mi->num_partial = mi->num_patterns = mi->allowed_pairs = 0;
+    mi->nq = mi->nk = 0;
+  }
+  return st;
+}
+
+splash_status splash_build_mask_info(const splash_mask_spec *spec, int64_t Lq, int64_t Lk, int32_t bq,
+                                     int32_t bk, void *cuda_stream, splash_mask_info **out) {
+  if (out == nullptr) return SPLASH_ERR_INVALID_ARG;
+  *out = nullptr;
+  splash_status st = check_spec(spec, Lq, Lk);
+  if (st != SPLASH_OK) return st;
+  if ((st = check_geometry(Lq, Lk, bq, bk)) != SPLASH_OK) return st;
+  splash_mask_info *mi = new (std::nothrow) splash_mask_info();
+  if (mi == nullptr) return SPLASH_ERR_OOM;
+  st = splash_mask_info_rebuild(mi, spec, Lq, Lk, bq, bk, cuda_stream);
+  if (st != SPLASH_OK) {
+    splash_mask_info_free_buffers(mi);
+    delete mi;
+    return st;
+  }
+  *out = mi;
+  return SPLASH_OK;
+}
+
+splash_status splash_mask_info_shape(const splash_mask_info *mi, int32_t *batch_rows, int64_t *nq,
+                                     int64_t *nk, int32_t *bq, int32_t *bk) {
+  if (mi == nullptr) return SPLASH_ERR_INVALID_ARG;
+  if (batch_rows) *batch_rows = mi->batch_rows;
+  if (nq) *nq = mi->nq;
+  if (nk) *nk = mi->nk;
+  if (bq) *bq = mi->bq;
+  if (bk) *bk = mi->bk;
+  return SPLASH_OK;
+}
+
+splash_status splash_mask_info_counts(const splash_mask_info *mi, int64_t *num_active, int64_t *num_partial,
+                                      int64_t *num_patterns, int64_t *allowed_pairs) {
+  if (mi == nullptr) return SPLASH_ERR_INVALID_ARG;
+  if (num_active) *num_active = mi->num_active;
+  if (num_partial) *num_partial = mi->num_partial;
+  if (num_patterns) *num_patterns = mi->num_patterns;
+  if (allowed_pairs) *allowed_pairs = mi->allowed_pairs;
+  return SPLASH_OK;
+}
+
+splash_status splash_mask_info_to_host(const splash_mask_info *mi, int8_t *block_mask, int32_t *row_ptr,
+                                       int32_t *active_rows, int32_t *active_cols, int32_t *mask_next,
+                                       uint8_t *bounds_start, uint8_t *bounds_end,
+                                       uint8_t *partial_mask_blocks) {
+  if (mi == nullptr || mi->nq <= 0) return SPLASH_ERR_INVALID_ARG;
+  const int64_t R = (int64_t)mi->batch_rows * mi->nq, A = mi->num_active;
+  const int64_t P = mi->num_patterns;
+  if (block_mask) SPLASH_CUDA_TRY(cudaMemcpy(block_mask, mi->block_mask, R * mi->nk, cudaMemcpyDeviceToHost));
+  if (row_ptr) SPLASH_CUDA_TRY(cudaMemcpy(row_ptr, mi->row_ptr, 4 * (R + 1), cudaMemcpyDeviceToHost));
+  if (A > 0) {
+    if (active_rows) SPLASH_CUDA_TRY(cudaMemcpy(active_rows, mi->active_rows, 4 * A, cudaMemcpyDeviceToHost));
+    if (active_cols) SPLASH_CUDA_TRY(cudaMemcpy(active_cols, mi->active_cols, 4 * A, cudaMemcpyDeviceToHost));
+    if (mask_next) SPLASH_CUDA_TRY(cudaMemcpy(mask_next, mi->mask_next, 4 * A, cudaMemcpyDeviceToHost));
+    if (bounds_start) SPLASH_CUDA_TRY(cudaMemcpy(bounds_start, mi->bounds_start, A, cudaMemcpyDeviceToHost));
+    if (bounds_end) SPLASH_CUDA_TRY(cudaMemcpy(bounds_end, mi->bounds_end, A, cudaMemcpyDeviceToHost));
+  }
+  if (P > 0 && partial_mask_blocks)
+    SPLASH_CUDA_TRY(cudaMemcpy(partial_mask_blocks, mi->patterns, (size_t)P * mi->bq * mi->bk,
+                               cudaMemcpyDeviceToHost));
+  return SPLASH_OK;
+}
+
+void splash_mask_info_destroy(splash_mask_info *mi) {
+  if (mi == nullptr) return;
+  splash_mask_info_free_buffers(mi);
+  delete mi;
+}
+
+splash_status splash_attention_fwd(const void *q, const void *k, const void *v, int32_t B, int32_t Hq,
+                                   int32_t Hkv, int64_t Lq, int64_t Lk, int32_t dqk, int32_t dv,
+                                   const int32_t *q_segment_ids, const int32_t *kv_segment_ids,
+                                   const splash_mask_info *mi, float scale, float softcap, void *out,
+                                   float *lse, void *cuda_stream) {
+  (void)q_segment_ids;
+  (void)kv_segment_ids;
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || lse == nullptr || mi == nullptr)
+    return SPLASH_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lk <= 0 || dqk <= 0 || dv <= 0)
+    return SPLASH_ERR_INVALID_ARG;
+  if (!(scale == scale) || !(softcap == softcap)) return SPLASH_ERR_INVALID_ARG;  // NaN
+  if (Hq % Hkv != 0) return SPLASH_ERR_SHAPE;
+  if (mi->nq <= 0 || mi->Lq != Lq || mi->Lk != Lk) return SPLASH_ERR_SHAPE;
+  if (mi->batch_rows != 1 && mi->batch_rows != B) return SPLASH_ERR_SHAPE;
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
+  if (mis & 15u) return SPLASH_ERR_INVALID_ARG;
+  const bool shape_ok = ((dqk == 128 && dv == 128) || (dqk == 192 && dv == 128) || (dqk == 64 && dv == 64)) &&
+                        mi->bq == mi->bk;
+  if (!shape_ok) return SPLASH_ERR_UNSUPPORTED;
+  if (mi->bk == 64 && dqk == 192) return SPLASH_ERR_UNSUPPORTED;
+  if ((int64_t)B * Hq * Lq >= ((int64_t)1 << 31) || (int64_t)B * Hkv * Lk >= ((int64_t)1 << 31))
+    return SPLASH_ERR_UNSUPPORTED;
+  int dev = 0;
+  SPLASH_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev != mi->device) return SPLASH_ERR_INVALID_ARG;
+  uint32_t *err = splash_device_error_word(dev);
+  if (err == nullptr) return SPLASH_ERR_CUDA;
+  return splash_attention_fwd_launch(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, out, lse,
+                                     static_cast<cudaStream_t>(cuda_stream), err);
+}
+
+splash_status splash_last_device_error(void *cuda_stream) {
+  int dev = 0;
+  SPLASH_CUDA_TRY(cudaGetDevice(&dev));
+  SPLASH_CUDA_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)));
+  uint32_t *addr = splash_device_error_word(dev);
+  if (addr == nullptr) return SPLASH_ERR_CUDA;
+  uint32_t word = 0;
+  SPLASH_CUDA_TRY(cudaMemcpy(&word, addr, sizeof word, cudaMemcpyDeviceToHost));
+  if (word != 0) SPLASH_CUDA_TRY(cudaMemset(addr, 0, sizeof word));
+  if (word & (SPLASH_DEV_TIMEOUT_PRODUCER | SPLASH_DEV_TIMEOUT_MMA | SPLASH_DEV_TIMEOUT_SOFTMAX |
+              SPLASH_DEV_TIMEOUT_DRAIN | SPLASH_DEV_TIMEOUT_SELFTEST))
+    return SPLASH_ERR_DEVICE_TIMEOUT;
+  if (word & SPLASH_DEV_BAD_TABLE) return SPLASH_ERR_DEVICE_CHECK;
+  return SPLASH_OK;
+}
+
+splash_status splash_debug_wait_selftest(uint64_t timeout_ns, void *cuda_stream) {
+  if (timeout_ns == 0 || timeout_ns > 2000000000ull) return SPLASH_ERR_INVALID_ARG;
+  int dev = 0;
+  SPLASH_CUDA_TRY(cudaGetDevice(&dev));
+  uint32_t *err = splash_device_error_word(dev);
+  if (err == nullptr) return SPLASH_ERR_CUDA;
+  splash_status st = splash_wait_selftest_launch(timeout_ns, static_cast<cudaStream_t>(cuda_stream), err);
+  if (st != SPLASH_OK) return st;
+  return splash_last_device_error(cuda_stream);
+}
+
+}  // extern "C"

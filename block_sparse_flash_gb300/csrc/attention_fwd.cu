@@ -1,0 +1,677 @@
+// attention_fwd.cu -- block-sparse (Splash) masked attention, forward pass,
+// for sm_103a: TMA-staged Q/K/V tiles, QK^T and PV on tcgen05 tensor cores
+// with TMEM accumulators, warp-specialised online softmax.
+//
+// What it computes ("Pallas Kernels and Splash Attention", CMU 11-868
+// Lecture 13 notes):
+//   §5.1  online softmax: running max m and sum l, alpha = exp(m_old - m_new);
+//   §5.2  the Flash body per (head, q-block, kv-block): scores, mask + soft
+//         cap, m_next, exp, alpha, l and o updates, o / l once at the end
+//         (deferred normalisation); heads independent, GQA heads share K/V;
+//   §5.4  soft cap cap * tanh(x / cap);
+//   §6.3  only active blocks of a q-block row are visited (the row's range of
+//         the MaskInfo active list), partial blocks are masked from their
+//         pattern, and the residual LSE is written next to O.
+// "The maths and infra behind core LLM operations" (joto.ai), "Causal Mask":
+// empty blocks are neither loaded nor multiplied; "LSE and Online Softmax":
+// LSE = m + log l.
+//
+// GB300 design (differs from the TPU kernel on the pages):
+//   * one persistent CTA per SM; each work item is (batch, two query heads,
+//     one q-block row); the two heads are two 128-row query tiles that share
+//     the row's active list, and share K/V tiles when they are in the same
+//     GQA group;
+//   * warp roles: warps 0-3 / 4-7 run the softmax of tile 0 / tile 1 (one
+//     thread per query row = one TMEM lane), warp 8 issues TMA loads, warp 9
+//     issues tcgen05 MMAs;
+//   * TMEM (512 columns): S_t / P_t at column 128t (P, bf16 pairs, overwrites
+//     the first half of S after it is read), O_t at 256 + 128t;
+//   * the exponent is base 2 (log2 e folded into the scale); the output
+//     accumulator is only rescaled when a row's maximum grows by more than
+//     2^8 (the running reference stays exact: P <= 256 and l, O use the same
+//     reference);
+//   * every wait is bounded (mbar_wait): on timeout the CTA raises an error
+//     bit, stops all roles, drains its copies and MMAs and frees TMEM.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "sm103_ptx.cuh"
+
+namespace splash {
+namespace {
+
+constexpr int kThreads = 384;       // 12 warps
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int DQK, int DV, int BK>
+struct Cfg {
+  static constexpr int BM = 128;                      // MMA M (rows of a query tile)
+  static constexpr int QCH = DQK / 64;                // 64-column chunks of Q / K
+  static constexpr int VCH = DV / 64;                 // 64-column chunks of V
+  static constexpr int Q_CHUNK = BM * 128;            // bytes of a 128-row x 64-col bf16 box
+  static constexpr int KV_CHUNK = BK * 128;           // bytes of a BK-row x 64-col bf16 box
+  static constexpr int Q_BYTES = QCH * Q_CHUNK;
+  static constexpr int K_BYTES = QCH * KV_CHUNK;
+  static constexpr int V_BYTES = VCH * KV_CHUNK;
+  static constexpr int TILE_BUDGET = 227 * 1024 - 2048;
+  static constexpr int NK = (DQK >= 192) ? 2 : ((DQK >= 128) ? 2 : 4);
+  static constexpr int NV = (DQK >= 192) ? 1 : ((DQK >= 128) ? 2 : 4);
+  static constexpr int TILES = 2 * Q_BYTES + NK * K_BYTES + NV * V_BYTES;
+  static_assert(TILES <= TILE_BUDGET, "shared memory budget");
+  // barriers: q_full[2] q_empty[2] k_full[NK] k_empty[NK] v_full[NV] v_empty[NV]
+  //           s_full[2] p_full[2] o_done[2] drain
+  static constexpr int NBAR = 2 + 2 + 2 * NK + 2 * NV + 2 + 2 + 2 + 1;
+  static constexpr int SMEM = 1024 + TILES + NBAR * 8 + 16;
+  static constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, BK, false);
+  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, DV, true);
+};
+
+struct FwdParams {
+  int32_t B, Hq, Hkv, G;
+  int64_t Lq, Lk;
+  int32_t bq, nq, nk, nbm;
+  int32_t npairs;
+  int64_t num_items;
+  const int32_t *row_ptr;
+  const int32_t *active_cols;
+  const int32_t *mask_next;
+  const uint32_t *pattern_bits;
+  const int32_t *row_order;
+  int64_t num_patterns;
+  float scale_log2;   // scale * log2(e)             (no soft cap)
+  float cap_inner;    // scale / cap                 (soft cap)
+  float cap_log2;     // cap * log2(e)               (soft cap)
+  int32_t use_softcap;
+  __nv_bfloat16 *out;
+  float *lse;
+  uint32_t *err;
+  uint64_t timeout_ns;
+};
+
+struct Item {
+  int32_t b, h0, h1, kvh0, kvh1, qrow;
+  int32_t g0, nb;
+  bool act1, shared;
+};
+
+// Work item w: rows in longest-first order; for a table shared by the batch,
+// each row expands into B batches; each (row, batch) into npairs head pairs.
+__device__ __forceinline__ Item decode_item(const FwdParams &p, int64_t w) {
+  Item it;
+  int64_t k;
+  int32_t pair;
+  if (p.nbm == 1) {
+    const int64_t per = (int64_t)p.B * p.npairs;
+    k = w / per;
+    const int64_t rem = w - k * per;
+    it.b = (int32_t)(rem / p.npairs);
+    pair = (int32_t)(rem - (int64_t)it.b * p.npairs);
+  } else {
+    k = w / p.npairs;
+    pair = (int32_t)(w - k * p.npairs);
+    it.b = -1;
+  }
+  const int32_t mrow = p.row_order[k];
+  if (p.nbm != 1) it.b = mrow / p.nq;
+  it.qrow = mrow % p.nq;
+  it.g0 = p.row_ptr[mrow];
+  it.nb = p.row_ptr[mrow + 1] - it.g0;
+  it.h0 = 2 * pair;
+  it.h1 = 2 * pair + 1;
+  it.act1 = it.h1 < p.Hq;
+  it.kvh0 = it.h0 / p.G;
+  it.kvh1 = it.act1 ? it.h1 / p.G : it.kvh0;
+  it.shared = (it.kvh0 == it.kvh1);
+  return it;
+}
+
+__device__ __forceinline__ void raise_error(const FwdParams &p, volatile int *abort, uint32_t bits) {
+  atomicOr(p.err, bits);
+  *abort = 1;
+}
+
+template <int DQK, int DV, int BK>
+__global__ void __launch_bounds__(kThreads, 1)
+splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using C = Cfg<DQK, DV, BK>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  const uint32_t sQ = smem_u32(smem);
+  const uint32_t sK = sQ + 2 * C::Q_BYTES;
+  const uint32_t sV = sK + C::NK * C::K_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::TILES);
+  const uint32_t b0 = smem_u32(bars);
+  auto q_full = [&](int t) { return b0 + 8u * t; };
+  auto q_empty = [&](int t) { return b0 + 8u * (2 + t); };
+  auto k_full = [&](int s) { return b0 + 8u * (4 + s); };
+  auto k_empty = [&](int s) { return b0 + 8u * (4 + C::NK + s); };
+  auto v_full = [&](int s) { return b0 + 8u * (4 + 2 * C::NK + s); };
+  auto v_empty = [&](int s) { return b0 + 8u * (4 + 2 * C::NK + C::NV + s); };
+  auto s_full = [&](int t) { return b0 + 8u * (4 + 2 * C::NK + 2 * C::NV + t); };
+  auto p_full = [&](int t) { return b0 + 8u * (6 + 2 * C::NK + 2 * C::NV + t); };
+  auto o_done = [&](int t) { return b0 + 8u * (8 + 2 * C::NK + 2 * C::NV + t); };
+  const uint32_t drain_bar = b0 + 8u * (10 + 2 * C::NK + 2 * C::NV);
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::TILES + C::NBAR * 8);
+  volatile int *abort = reinterpret_cast<volatile int *>(smem + C::TILES + C::NBAR * 8 + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 32) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(q_full(t), 1);
+      mbar_init(q_empty(t), 1);
+      mbar_init(s_full(t), 1);
+      mbar_init(p_full(t), 128);
+      mbar_init(o_done(t), 1);
+    }
+    for (int s = 0; s < C::NK; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
+    }
+    for (int s = 0; s < C::NV; ++s) {
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
+    }
+    mbar_init(drain_bar, 1);
+    *abort = 0;
+    mbar_fence_init();
+  }
+  if (threadIdx.x == kProducerWarp * 32) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t kcnt = 0, vcnt = 0, qcnt[2] = {0, 0};
+      bool ok = true;
+      auto load_k = [&](int32_t b, int32_t kvh, int32_t col) -> bool {
+        const int s = kcnt % C::NK;
+        if (kcnt >= (uint32_t)C::NK && !mbar_wait(k_empty(s), ((kcnt / C::NK) - 1) & 1, abort, p.timeout_ns))
+          return false;
+        mbar_arrive_expect_tx(k_full(s), C::K_BYTES);
+        const int32_t y = (int32_t)(((int64_t)b * p.Hkv + kvh) * p.Lk + (int64_t)col * BK);
+        for (int ch = 0; ch < C::QCH; ++ch)
+          tma_load_2d(sK + s * C::K_BYTES + ch * C::KV_CHUNK, &tmK, ch * 64, y, k_full(s));
+        ++kcnt;
+        return true;
+      };
+      auto load_v = [&](int32_t b, int32_t kvh, int32_t col) -> bool {
+        const int s = vcnt % C::NV;
+        if (vcnt >= (uint32_t)C::NV && !mbar_wait(v_empty(s), ((vcnt / C::NV) - 1) & 1, abort, p.timeout_ns))
+          return false;
+        mbar_arrive_expect_tx(v_full(s), C::V_BYTES);
+        const int32_t y = (int32_t)(((int64_t)b * p.Hkv + kvh) * p.Lk + (int64_t)col * BK);
+        for (int ch = 0; ch < C::VCH; ++ch)
+          tma_load_2d(sV + s * C::V_BYTES + ch * C::KV_CHUNK, &tmV, ch * 64, y, v_full(s));
+        ++vcnt;
+        return true;
+      };
+      auto col_of = [&](const Item &it, int32_t g) -> int32_t {
+        int32_t c = p.active_cols[it.g0 + g];
+        if (c < 0 || c >= p.nk) {
+          atomicOr(p.err, SPLASH_DEV_BAD_TABLE);
+          c = 0;
+        }
+        return c;
+      };
+      for (int64_t w = blockIdx.x; w < p.num_items && ok; w += gridDim.x) {
+        const Item it = decode_item(p, w);
+        if (it.nb <= 0) continue;
+        for (int t = 0; t < (it.act1 ? 2 : 1) && ok; ++t) {
+          if (qcnt[t] > 0 && !mbar_wait(q_empty(t), (qcnt[t] - 1) & 1, abort, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(q_full(t), C::Q_BYTES);
+          const int32_t h = t ? it.h1 : it.h0;
+          const int32_t y = (int32_t)(((int64_t)it.b * p.Hq + h) * p.Lq + (int64_t)it.qrow * p.bq);
+          for (int ch = 0; ch < C::QCH; ++ch)
+            tma_load_2d(sQ + t * C::Q_BYTES + ch * C::Q_CHUNK, &tmQ, ch * 64, y, q_full(t));
+          ++qcnt[t];
+        }
+        if (!ok) break;
+        const bool two_kv = it.act1 && !it.shared;
+        int32_t c = col_of(it, 0);
+        ok = load_k(it.b, it.kvh0, c) && (!two_kv || load_k(it.b, it.kvh1, c));
+        for (int32_t g = 0; g < it.nb && ok; ++g) {
+          const int32_t cn = (g + 1 < it.nb) ? col_of(it, g + 1) : 0;
+          ok = load_v(it.b, it.kvh0, c);
+          if (ok && g + 1 < it.nb) ok = load_k(it.b, it.kvh0, cn);
+          if (ok && two_kv) ok = load_v(it.b, it.kvh1, c);
+          if (ok && two_kv && g + 1 < it.nb) ok = load_k(it.b, it.kvh1, cn);
+          c = cn;
+        }
+      }
+      if (!ok) raise_error(p, abort, SPLASH_DEV_TIMEOUT_PRODUCER);
+      // drain: the last load issued into every slot has landed
+      bool drained = true;
+      for (int s = 0; s < C::NK; ++s)
+        if (kcnt > (uint32_t)s) {
+          const uint32_t last = (kcnt - 1 - s) / C::NK;  // uses of slot s minus one
+          drained &= mbar_wait_drain(k_full(s), last & 1, p.timeout_ns);
+        }
+      for (int s = 0; s < C::NV; ++s)
+        if (vcnt > (uint32_t)s) {
+          const uint32_t last = (vcnt - 1 - s) / C::NV;
+          drained &= mbar_wait_drain(v_full(s), last & 1, p.timeout_ns);
+        }
+      for (int t = 0; t < 2; ++t)
+        if (qcnt[t] > 0) drained &= mbar_wait_drain(q_full(t), (qcnt[t] - 1) & 1, p.timeout_ns);
+      if (!drained) atomicOr(p.err, SPLASH_DEV_TIMEOUT_DRAIN);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t kcnt = 0, vcnt = 0, qcnt[2] = {0, 0}, pcnt[2] = {0, 0};
+      bool ok = true;
+      const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
+      const uint32_t tO[2] = {tmem + 256u, tmem + 384u};
+      auto issue_qk = [&](int t, int ks) {
+        const uint32_t qa = sQ + t * C::Q_BYTES, kb = sK + ks * C::K_BYTES;
+#pragma unroll
+        for (int ch = 0; ch < C::QCH; ++ch)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = sdesc_sw128(qa + ch * C::Q_CHUNK + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(kb + ch * C::KV_CHUNK + kk * 32, 16, 1024);
+            mma_ss(tS[t], ad, bd, C::IDESC_QK, (ch | kk) != 0);
+          }
+      };
+      auto issue_pv = [&](int t, int vs, bool first_block) {
+        const uint32_t vb = sV + vs * C::V_BYTES;
+#pragma unroll
+        for (int j = 0; j < BK / 16; ++j) {
+          const uint64_t bd = sdesc_sw128(vb + j * 2048, C::KV_CHUNK, 1024);
+          mma_ts(tO[t], tS[t] + j * 8, bd, C::IDESC_PV, (!first_block || j > 0) ? 1u : 0u);
+        }
+      };
+      auto wait_k = [&](int &slot) -> bool {
+        slot = kcnt % C::NK;
+        if (!mbar_wait(k_full(slot), (kcnt / C::NK) & 1, abort, p.timeout_ns)) return false;
+        tc_fence_after();
+        return true;
+      };
+      auto wait_v = [&](int &slot) -> bool {
+        slot = vcnt % C::NV;
+        if (!mbar_wait(v_full(slot), (vcnt / C::NV) & 1, abort, p.timeout_ns)) return false;
+        tc_fence_after();
+        return true;
+      };
+      for (int64_t w = blockIdx.x; w < p.num_items && ok; w += gridDim.x) {
+        const Item it = decode_item(p, w);
+        if (it.nb <= 0) continue;
+        const int nt = it.act1 ? 2 : 1;
+        const bool two_kv = it.act1 && !it.shared;
+        for (int t = 0; t < nt && ok; ++t) {
+          ok = mbar_wait(q_full(t), qcnt[t] & 1, abort, p.timeout_ns);
+          ++qcnt[t];
+        }
+        if (!ok) break;
+        tc_fence_after();
+        // S_t(0) = Q_t K(0)^T
+        int ks = 0;
+        if (!(ok = wait_k(ks))) break;
+        issue_qk(0, ks);
+        tc_commit(s_full(0));
+        if (!two_kv) {
+          if (nt == 2) {
+            issue_qk(1, ks);
+            tc_commit(s_full(1));
+          }
+          tc_commit(k_empty(ks));
+          ++kcnt;
+        } else {
+          tc_commit(k_empty(ks));
+          ++kcnt;
+          if (!(ok = wait_k(ks))) break;
+          issue_qk(1, ks);
+          tc_commit(s_full(1));
+          tc_commit(k_empty(ks));
+          ++kcnt;
+        }
+        if (it.nb == 1)
+          for (int t = 0; t < nt; ++t) tc_commit(q_empty(t));
+        for (int32_t g = 0; g < it.nb && ok; ++g) {
+          const bool more = g + 1 < it.nb;
+          // ---- tile 0
+          if (!(ok = mbar_wait(p_full(0), pcnt[0] & 1, abort, p.timeout_ns))) break;
+          ++pcnt[0];
+          tc_fence_after();
+          int vs0 = 0;
+          if (!(ok = wait_v(vs0))) break;
+          issue_pv(0, vs0, g == 0);
+          if (!more) tc_commit(o_done(0));
+          if (nt == 1 || two_kv) {
+            tc_commit(v_empty(vs0));
+            ++vcnt;
+          }
+          int ks0 = 0;
+          if (more) {
+            if (!(ok = wait_k(ks0))) break;
+            issue_qk(0, ks0);
+            tc_commit(s_full(0));
+            if (nt == 1 || two_kv) {
+              tc_commit(k_empty(ks0));
+              ++kcnt;
+            }
+            if (g + 2 == it.nb) tc_commit(q_empty(0));
+          }
+          if (nt == 1) continue;
+          // ---- tile 1
+          if (!(ok = mbar_wait(p_full(1), pcnt[1] & 1, abort, p.timeout_ns))) break;
+          ++pcnt[1];
+          tc_fence_after();
+          int vs1 = vs0;
+          if (two_kv && !(ok = wait_v(vs1))) break;
+          issue_pv(1, vs1, g == 0);
+          if (!more) tc_commit(o_done(1));
+          tc_commit(v_empty(vs1));
+          ++vcnt;
+          if (more) {
+            int ks1 = ks0;
+            if (two_kv && !(ok = wait_k(ks1))) break;
+            issue_qk(1, ks1);
+            tc_commit(s_full(1));
+            tc_commit(k_empty(ks1));
+            ++kcnt;
+            if (g + 2 == it.nb) tc_commit(q_empty(1));
+          }
+        }
+      }
+      if (!ok) raise_error(p, abort, SPLASH_DEV_TIMEOUT_MMA);
+      // drain: every MMA issued by this thread has completed
+      tc_commit(drain_bar);
+      if (!mbar_wait_drain(drain_bar, 0, p.timeout_ns)) atomicOr(p.err, SPLASH_DEV_TIMEOUT_DRAIN);
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;          // query tile
+    const int wq = warp & 3;          // TMEM lane quarter
+    const int row = wq * 32 + lane;   // query row within the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + 128u * t + lane_off;
+    const uint32_t tO = tmem + 256u + 128u * t + lane_off;
+    const bool row_valid = row < p.bq;
+    uint32_t scnt = 0, ocnt = 0;
+    bool ok = true;
+    for (int64_t w = blockIdx.x; w < p.num_items && ok; w += gridDim.x) {
+      const Item it = decode_item(p, w);
+      if (t == 1 && !it.act1) continue;
+      const int32_t h = t ? it.h1 : it.h0;
+      const int64_t orow = ((int64_t)it.b * p.Hq + h) * p.Lq + (int64_t)it.qrow * p.bq + row;
+      float m_ref = -INFINITY;  // running reference (log2 units)
+      float l = 0.f;
+      for (int32_t g = 0; g < it.nb && ok; ++g) {
+        int32_t mn = p.mask_next[it.g0 + g];
+        if (mn >= p.num_patterns) {
+          atomicOr(p.err, SPLASH_DEV_BAD_TABLE);
+          mn = -1;
+        }
+        uint32_t bits[BK / 32];
+        if (mn >= 0 && row_valid) {
+          const uint32_t *src = p.pattern_bits + ((int64_t)mn * p.bq + row) * (BK / 32);
+#pragma unroll
+          for (int x = 0; x < BK / 32; ++x) bits[x] = __ldg(src + x);
+        } else {
+#pragma unroll
+          for (int x = 0; x < BK / 32; ++x) bits[x] = row_valid ? 0xffffffffu : 0u;
+        }
+        // all lanes wait; the outcome is made warp-uniform before the
+        // warp-collective TMEM accesses
+        ok = __all_sync(0xffffffffu, mbar_wait(s_full(t), scnt & 1, abort, p.timeout_ns));
+        if (!ok) break;
+        ++scnt;
+        tc_fence_after();
+        float s[BK];
+        {
+          uint32_t r[32];
+#pragma unroll
+          for (int c = 0; c < BK / 32; ++c) {
+            tmem_ld32(tS + 32u * c, r);
+            tmem_wait_ld();
+            reg_fence32(r);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(r[x]);
+          }
+        }
+        // scores in log2 units, soft cap, element mask
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < BK; ++j) {
+          float x = p.use_softcap ? p.cap_log2 * tanhf(s[j] * p.cap_inner) : s[j] * p.scale_log2;
+          x = ((bits[j >> 5] >> (j & 31)) & 1u) ? x : -INFINITY;
+          s[j] = x;
+          mx = fmaxf(mx, x);
+        }
+        const float m_new = fmaxf(m_ref, mx);
+        float alpha = 1.f;
+        if (m_new != -INFINITY && (m_ref == -INFINITY || m_new > m_ref + kRescaleThreshold)) {
+          alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_new);
+          m_ref = m_new;
+        }
+        const float sub = (m_ref == -INFINITY) ? 0.f : m_ref;
+        float sum = 0.f;
+        uint32_t pk[BK / 2];
+#pragma unroll
+        for (int j = 0; j < BK; j += 2) {
+          const float p0 = ex2_approx(s[j] - sub);
+          const float p1 = ex2_approx(s[j + 1] - sub);
+          sum += p0 + p1;
+          pk[j >> 1] = pack_bf16x2(p0, p1);
+        }
+        l = l * alpha + sum;
+        // rescale the output accumulator (its previous PV has completed:
+        // S_t(g) was committed after it)
+        if (g > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          uint32_t r[32];
+#pragma unroll
+          for (int c = 0; c < DV / 32; ++c) {
+            tmem_ld32(tO + 32u * c, r);
+            tmem_wait_ld();
+            reg_fence32(r);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
+            tmem_st32(tO + 32u * c, r);
+          }
+        }
+        // P (bf16 pairs) into the first BK/2 columns of S_t
+#pragma unroll
+        for (int c = 0; c < BK / 64; ++c) {
+          uint32_t r[32];
+#pragma unroll
+          for (int x = 0; x < 32; ++x) r[x] = pk[c * 32 + x];
+          tmem_st32(tS + 32u * c, r);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_full(t));
+      }
+      if (!ok) break;
+      // ---- epilogue: O / l and the LSE
+      if (it.nb > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(o_done(t), ocnt & 1, abort, p.timeout_ns));
+        if (!ok) break;
+        ++ocnt;
+        tc_fence_after();
+      }
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16 *orow_ptr = p.out + orow * DV;
+#pragma unroll
+      for (int c = 0; c < DV / 32; ++c) {
+        uint32_t r[32];
+        if (it.nb > 0) {
+          tmem_ld32(tO + 32u * c, r);
+          tmem_wait_ld();
+          reg_fence32(r);
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) r[x] = 0u;
+        }
+        if (row_valid) {
+          uint32_t o[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x)
+            o[x] = pack_bf16x2(__uint_as_float(r[2 * x]) * inv, __uint_as_float(r[2 * x + 1]) * inv);
+          uint4 *dst = reinterpret_cast<uint4 *>(orow_ptr + c * 32);
+#pragma unroll
+          for (int x = 0; x < 4; ++x) dst[x] = make_uint4(o[4 * x], o[4 * x + 1], o[4 * x + 2], o[4 * x + 3]);
+        }
+      }
+      if (row_valid) p.lse[orow] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+    }
+    if (!ok) raise_error(p, abort, SPLASH_DEV_TIMEOUT_SOFTMAX);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// --------------------------------------------------------------- self test
+__global__ void wait_selftest_kernel(uint64_t timeout_ns, uint32_t *err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // nothing ever arrives on `bar`: the bounded wait must give up
+    if (!mbar_wait(smem_u32(&bar), 0, &abort_flag, timeout_ns)) atomicOr(err, SPLASH_DEV_TIMEOUT_SELFTEST);
+  }
+}
+
+// --------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+bool make_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t elem[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, elem,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int DQK, int DV, int BK>
+splash_status launch(const void *q, const void *k, const void *v, const FwdParams &prm, cudaStream_t stream) {
+  using C = Cfg<DQK, DV, BK>;
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, q, DQK, (uint64_t)prm.B * prm.Hq * prm.Lq, 128) ||
+      !make_map(&tk, k, DQK, (uint64_t)prm.B * prm.Hkv * prm.Lk, BK) ||
+      !make_map(&tv, v, DV, (uint64_t)prm.B * prm.Hkv * prm.Lk, BK))
+    return SPLASH_ERR_CUDA;
+  static int configured_device = -1;
+  int dev = 0;
+  SPLASH_CUDA_TRY(cudaGetDevice(&dev));
+  int sms = 148;
+  SPLASH_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  if (configured_device != dev) {
+    SPLASH_CUDA_TRY(cudaFuncSetAttribute(splash_fwd_kernel<DQK, DV, BK>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+    configured_device = dev;
+  }
+  const int64_t grid = prm.num_items < sms ? prm.num_items : sms;
+  if (grid <= 0) return SPLASH_OK;
+  splash_fwd_kernel<DQK, DV, BK><<<(unsigned)grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, prm);
+  SPLASH_CUDA_TRY(cudaGetLastError());
+  splash_count_launches(1);
+  return SPLASH_OK;
+}
+
+}  // namespace
+}  // namespace splash
+
+using namespace splash;
+
+splash_status splash_attention_fwd_launch(const void *q, const void *k, const void *v, int32_t B,
+                                          int32_t Hq, int32_t Hkv, int64_t Lq, int64_t Lk,
+                                          int32_t dqk, int32_t dv, const splash_mask_info *mi,
+                                          float scale, float softcap, void *out, float *lse,
+                                          cudaStream_t stream, uint32_t *err_word) {
+  FwdParams prm;
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.G = Hq / Hkv;
+  prm.Lq = Lq;
+  prm.Lk = Lk;
+  prm.bq = mi->bq;
+  prm.nq = (int32_t)mi->nq;
+  prm.nk = (int32_t)mi->nk;
+  prm.nbm = mi->batch_rows;
+  prm.npairs = (Hq + 1) / 2;
+  const int64_t rows = (int64_t)mi->batch_rows * mi->nq;
+  prm.num_items = (mi->batch_rows == 1 ? rows * B : rows) * prm.npairs;
+  prm.row_ptr = mi->row_ptr;
+  prm.active_cols = mi->active_cols;
+  prm.mask_next = mi->mask_next;
+  prm.pattern_bits = mi->pattern_bits;
+  prm.row_order = mi->row_order;
+  prm.num_patterns = mi->num_patterns;
+  prm.scale_log2 = scale * kLog2e;
+  prm.use_softcap = softcap > 0.f ? 1 : 0;
+  prm.cap_inner = softcap > 0.f ? scale / softcap : 0.f;
+  prm.cap_log2 = softcap > 0.f ? softcap * kLog2e : 0.f;
+  prm.out = reinterpret_cast<__nv_bfloat16 *>(out);
+  prm.lse = lse;
+  prm.err = err_word;
+  prm.timeout_ns = 1000000000ull;  // 1 s per wait
+  const int bk = mi->bk;
+  if (dqk == 128 && dv == 128 && bk == 128) return launch<128, 128, 128>(q, k, v, prm, stream);
+  if (dqk == 192 && dv == 128 && bk == 128) return launch<192, 128, 128>(q, k, v, prm, stream);
+  if (dqk == 64 && dv == 64 && bk == 64) return launch<64, 64, 64>(q, k, v, prm, stream);
+  if (dqk == 64 && dv == 64 && bk == 128) return launch<64, 64, 128>(q, k, v, prm, stream);
+  if (dqk == 128 && dv == 128 && bk == 64) return launch<128, 128, 64>(q, k, v, prm, stream);
+  return SPLASH_ERR_UNSUPPORTED;
+}
+
+splash_status splash_wait_selftest_launch(uint64_t timeout_ns, cudaStream_t stream, uint32_t *err_word) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(timeout_ns, err_word);
+  SPLASH_CUDA_TRY(cudaGetLastError());
+  splash_count_launches(1);
+  return SPLASH_OK;
+}

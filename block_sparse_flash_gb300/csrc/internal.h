@@ -1,0 +1,94 @@
+// internal.h -- declarations shared by the translation units of libsplash.so.
+// Not part of the public ABI (that is include/splash.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "splash.h"
+
+// Error bits of the device error word (set with atomicOr by kernels).
+enum : uint32_t {
+  SPLASH_DEV_TIMEOUT_PRODUCER = 1u << 0,
+  SPLASH_DEV_TIMEOUT_MMA = 1u << 1,
+  SPLASH_DEV_TIMEOUT_SOFTMAX = 1u << 2,
+  SPLASH_DEV_TIMEOUT_DRAIN = 1u << 3,
+  SPLASH_DEV_TIMEOUT_SELFTEST = 1u << 4,
+  SPLASH_DEV_BAD_TABLE = 1u << 8,
+};
+
+// The library-owned sparse execution table ("Pallas Kernels and Splash
+// Attention" §6.2).  All arrays are device memory of `device`.
+struct splash_mask_info {
+  int device = -1;
+  // geometry
+  int32_t batch_rows = 0;  // B_mask
+  int64_t Lq = 0, Lk = 0, nq = 0, nk = 0;
+  int32_t bq = 0, bk = 0;
+  // the mask it was built from (segment arrays are not retained)
+  int32_t causal = 0;
+  int64_t window_left = -1, window_right = -1;
+  int32_t has_segments = 0;
+  // totals (host copies)
+  int64_t num_active = 0, num_partial = 0, num_patterns = 0, allowed_pairs = 0;
+  int32_t max_row_blocks = 0;
+
+  // --- table arrays (public content) ---
+  int8_t *block_mask = nullptr;    // [R*nk]
+  int32_t *row_ptr = nullptr;      // [R+1]
+  int32_t *active_rows = nullptr;  // [cap_active]
+  int32_t *active_cols = nullptr;  // [cap_active]
+  int32_t *mask_next = nullptr;    // [cap_active]
+  uint8_t *bounds_start = nullptr; // [cap_active]
+  uint8_t *bounds_end = nullptr;   // [cap_active]
+  uint8_t *patterns = nullptr;     // [cap_patterns][bq][bk]
+  // --- derived arrays used by the attention kernel ---
+  uint32_t *pattern_bits = nullptr;  // [cap_patterns][bq][bk/32], bit dj of word dj/32 = allowed
+  int32_t *row_order = nullptr;      // [R] rows by descending active count (longest first)
+  // --- build scratch ---
+  int32_t *row_cnt = nullptr;      // [R]
+  int32_t *row_pcnt = nullptr;     // [R]
+  int32_t *prow_ptr = nullptr;     // [R+1]
+  int32_t *seg_summary = nullptr;  // [R*2 + B_mask*nk*2] (min, max) per q-block then per kv-block
+  int32_t *part_row = nullptr;     // [cap_active] global row (b_mask*nq + r) of the k-th partial block
+  int32_t *part_col = nullptr;     // [cap_active]
+  int32_t *part_g = nullptr;       // [cap_active] its active index
+  uint64_t *part_hash = nullptr;   // [cap_active]
+  int32_t *part_rep = nullptr;     // [cap_active] first partial with identical content
+  int32_t *part_pidx = nullptr;    // [cap_active] pattern index (valid for representatives)
+  int32_t *rep_list = nullptr;     // [cap_active] partial index of pattern u
+  int32_t *row_hist = nullptr;     // [nk+1] counting-sort bins
+  unsigned long long *counters = nullptr;  // [8]: A, A_p, P, allowed, max_row
+  // host staging
+  unsigned long long *h_counters = nullptr;  // pinned [8]
+
+  // capacities (elements)
+  int64_t cap_rows = 0, cap_blocks = 0, cap_seg = 0, cap_patterns = 0, cap_hist = 0;
+};
+
+// mask_info.cu
+splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mask_spec *spec,
+                                          int64_t Lq, int64_t Lk, int32_t bq, int32_t bk,
+                                          cudaStream_t stream);
+void splash_mask_info_free_buffers(splash_mask_info *mi);
+
+// api.cu
+uint32_t *splash_device_error_word(int device);  // device address of the error word (or NULL)
+
+// attention_fwd.cu
+splash_status splash_attention_fwd_launch(const void *q, const void *k, const void *v, int32_t B,
+                                          int32_t Hq, int32_t Hkv, int64_t Lq, int64_t Lk,
+                                          int32_t dqk, int32_t dv, const splash_mask_info *mi,
+                                          float scale, float softcap, void *out, float *lse,
+                                          cudaStream_t stream, uint32_t *err_word);
+splash_status splash_wait_selftest_launch(uint64_t timeout_ns, cudaStream_t stream,
+                                          uint32_t *err_word);
+
+// Counts kernel launches (splash_kernel_launches); call once per launch.
+void splash_count_launches(uint64_t n);
+
+#define SPLASH_CUDA_TRY(expr)                         \
+  do {                                                \
+    cudaError_t _e = (expr);                          \
+    if (_e != cudaSuccess) return SPLASH_ERR_CUDA;    \
+  } while (0)

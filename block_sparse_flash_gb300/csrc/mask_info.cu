@@ -1,0 +1,621 @@
+// mask_info.cu -- builds the sparse execution table (MaskInfo) on the GPU.
+//
+// "Pallas Kernels and Splash Attention" (CMU 11-868 Lecture 13 notes):
+//   §6.1  blocks of the mask are empty (skip), full (no element mask) or
+//         partial (element mask needed);
+//   §6.2  MaskInfo: block_mask, the active rows / columns, the deduplicated
+//         partial patterns and mask_next, bounds_start / bounds_end;
+//   §6.4  segment IDs (q_id == kv_id) joined with causal / local by AND.
+//
+// Pipeline (all kernels on the caller's stream, one host wait):
+//   K1 seg_summary   per q-block / kv-block min and max segment id
+//   K2 classify      exact allowed-element count of every block -> class,
+//                    per-row active / partial counts, allowed pairs
+//   K3 scan_rows     row_ptr (CSR) and partial offsets
+//      compact       active lists in row-major, kv-ascending order, bounds
+//   K4 partial_hash  a content hash of each partial block's element pattern
+//      dedup         first partial with identical content (hash prefilter,
+//                    exact word-by-word comparison)
+//      scan_reps     pattern index of each first occurrence
+//      finalize      mask_next
+//      row_order     rows by descending active count (work order of the
+//                    attention kernel)
+//      (host wait: read A, A_p, P)
+//      materialize   partial_mask_blocks (bytes) and their bit-packed copy
+#include <algorithm>
+#include <climits>
+
+#include "internal.h"
+
+namespace {
+
+struct DevMask {
+  int32_t causal;
+  int64_t wl, wr;
+  const int32_t *qseg, *kvseg;
+  int64_t Lq, Lk, nq, nk;
+  int32_t bq, bk, nbm;
+};
+
+// The band part of the joint mask for query i: allowed keys j lie in [lo, hi]
+// intersected with [c0, c1].
+__device__ __forceinline__ void band_range(const DevMask &m, int64_t i, int64_t c0, int64_t c1,
+                                           int64_t &lo, int64_t &hi) {
+  lo = c0;
+  hi = c1;
+  if (m.causal) hi = min(hi, i);
+  if (m.wl >= 0) lo = max(lo, i - m.wl);
+  if (m.wr >= 0) hi = min(hi, i + m.wr);
+}
+
+// 32 mask bits of query i against keys j0 .. j0+31 (bit t = key j0 + t).
+__device__ __forceinline__ uint32_t row_word(const DevMask &m, int32_t bm, int64_t i, int32_t sq,
+                                             int64_t j0) {
+  int64_t lo, hi;
+  band_range(m, i, j0, j0 + 31, lo, hi);
+  if (hi < lo) return 0u;
+  uint32_t bits = 0u;
+  if (m.qseg == nullptr) {
+    int64_t n = hi - lo + 1;  // 1..32 contiguous bits starting at lo - j0
+    uint32_t run = n >= 32 ? 0xffffffffu : ((1u << n) - 1u);
+    bits = run << (lo - j0);
+  } else {
+    const int32_t *kv = m.kvseg + (int64_t)bm * m.Lk;
+    for (int64_t j = lo; j <= hi; ++j)
+      if (kv[j] == sq) bits |= 1u << (j - j0);
+  }
+  return bits;
+}
+
+__device__ __forceinline__ int32_t q_segment(const DevMask &m, int32_t bm, int64_t i) {
+  return m.qseg ? m.qseg[(int64_t)bm * m.Lq + i] : 0;
+}
+
+// ---------------------------------------------------------------- K1
+__global__ void seg_summary_kernel(DevMask m, int32_t *qsum, int32_t *kvsum) {
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int32_t bm = blockIdx.y;
+  if (warp >= m.nq + m.nk) return;
+  const bool isq = warp < m.nq;
+  const int64_t blk = isq ? warp : warp - m.nq;
+  const int32_t n = isq ? m.bq : m.bk;
+  const int32_t *seg = isq ? m.qseg + (int64_t)bm * m.Lq + blk * m.bq
+                           : m.kvseg + (int64_t)bm * m.Lk + blk * m.bk;
+  int32_t mn = INT_MAX, mx = INT_MIN;
+  for (int32_t x = lane; x < n; x += 32) {
+    int32_t s = seg[x];
+    mn = min(mn, s);
+    mx = max(mx, s);
+  }
+  for (int off = 16; off; off >>= 1) {
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  }
+  if (lane == 0) {
+    int32_t *dst = isq ? qsum + ((int64_t)bm * m.nq + blk) * 2 : kvsum + ((int64_t)bm * m.nk + blk) * 2;
+    dst[0] = mn;
+    dst[1] = mx;
+  }
+}
+
+// ---------------------------------------------------------------- K2
+// One thread per block (bm, r, c); a CTA covers 128 blocks of one row.
+constexpr int kClassifyThreads = 128;
+
+__global__ void __launch_bounds__(kClassifyThreads)
+classify_kernel(DevMask m, const int32_t *qsum, const int32_t *kvsum, int8_t *block_mask,
+                int32_t *row_cnt, int32_t *row_pcnt, unsigned long long *counters) {
+  const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t r = blockIdx.y;
+  const int32_t bm = blockIdx.z;
+  const int64_t row = (int64_t)bm * m.nq + r;
+  int64_t cnt = 0;
+  int cls = 0;
+  if (c < m.nk) {
+    const int64_t c0 = c * m.bk, c1 = c0 + m.bk - 1;
+    for (int32_t di = 0; di < m.bq; ++di) {
+      int64_t lo, hi;
+      band_range(m, r * m.bq + di, c0, c1, lo, hi);
+      if (hi >= lo) cnt += hi - lo + 1;
+    }
+    if (cnt > 0 && m.qseg != nullptr) {
+      const int32_t qmn = qsum[row * 2], qmx = qsum[row * 2 + 1];
+      const int32_t kmn = kvsum[((int64_t)bm * m.nk + c) * 2], kmx = kvsum[((int64_t)bm * m.nk + c) * 2 + 1];
+      if (qmx < kmn || kmx < qmn) {
+        cnt = 0;  // no segment id in common
+      } else if (!(qmn == qmx && kmn == kmx && qmn == kmn)) {
+        // undecided by the summaries: count element by element
+        const int32_t *kv = m.kvseg + (int64_t)bm * m.Lk;
+        cnt = 0;
+        for (int32_t di = 0; di < m.bq; ++di) {
+          const int64_t i = r * m.bq + di;
+          const int32_t sq = q_segment(m, bm, i);
+          int64_t lo, hi;
+          band_range(m, i, c0, c1, lo, hi);
+          for (int64_t j = lo; j <= hi; ++j) cnt += (kv[j] == sq);
+        }
+      }
+      // (both constant and equal: the band count stands)
+    }
+    cls = cnt == 0 ? 0 : (cnt == (int64_t)m.bq * m.bk ? 2 : 1);
+    block_mask[row * m.nk + c] = (int8_t)cls;
+  }
+  // reduce within the CTA (all threads share the row)
+  int na = cls != 0, np = cls == 1;
+  unsigned long long ns = (unsigned long long)cnt;
+  for (int off = 16; off; off >>= 1) {
+    na += __shfl_xor_sync(0xffffffffu, na, off);
+    np += __shfl_xor_sync(0xffffffffu, np, off);
+    ns += __shfl_xor_sync(0xffffffffu, ns, off);
+  }
+  __shared__ int sa[kClassifyThreads / 32], sp[kClassifyThreads / 32];
+  __shared__ unsigned long long ss[kClassifyThreads / 32];
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    sa[w] = na;
+    sp[w] = np;
+    ss[w] = ns;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ta = 0, tp = 0;
+    unsigned long long ts = 0;
+    for (int x = 0; x < kClassifyThreads / 32; ++x) {
+      ta += sa[x];
+      tp += sp[x];
+      ts += ss[x];
+    }
+    if (ta) atomicAdd(&row_cnt[row], ta);
+    if (tp) atomicAdd(&row_pcnt[row], tp);
+    if (ts) atomicAdd(&counters[3], ts);
+  }
+}
+
+// ---------------------------------------------------------------- scans
+// Single-CTA exclusive scan of one or two int32 arrays (1024 threads).
+__device__ __forceinline__ int warp_incl_scan(int x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  return x;
+}
+
+// Returns the exclusive prefix of x within the CTA and the CTA total.
+__device__ __forceinline__ int block_excl_scan(int x, int &total, int *warp_buf) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int incl = warp_incl_scan(x);
+  if (lane == 31) warp_buf[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int v = lane < nw ? warp_buf[lane] : 0;
+    int vi = warp_incl_scan(v);
+    if (lane < nw) warp_buf[lane] = vi - v;
+    if (lane == 31) warp_buf[32] = vi;
+  }
+  __syncthreads();
+  int ex = warp_buf[w] + incl - x;
+  total = warp_buf[32];
+  __syncthreads();
+  return ex;
+}
+
+__global__ void __launch_bounds__(1024)
+scan_rows_kernel(int64_t R, const int32_t *row_cnt, const int32_t *row_pcnt, int32_t *row_ptr,
+                 int32_t *prow_ptr, unsigned long long *counters) {
+  __shared__ int buf_a[33], buf_p[33];
+  int carry_a = 0, carry_p = 0, mx = 0;
+  for (int64_t base = 0; base < R; base += blockDim.x) {
+    const int64_t x = base + threadIdx.x;
+    const int a = x < R ? row_cnt[x] : 0;
+    const int p = x < R ? row_pcnt[x] : 0;
+    mx = max(mx, a);
+    int ta, tp;
+    const int ea = block_excl_scan(a, ta, buf_a);
+    const int ep = block_excl_scan(p, tp, buf_p);
+    if (x < R) {
+      row_ptr[x] = carry_a + ea;
+      prow_ptr[x] = carry_p + ep;
+    }
+    carry_a += ta;
+    carry_p += tp;
+  }
+  for (int off = 16; off; off >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  __shared__ int smx[32];
+  if ((threadIdx.x & 31) == 0) smx[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t = max(t, smx[w]);
+    row_ptr[R] = carry_a;
+    prow_ptr[R] = carry_p;
+    counters[0] = (unsigned long long)carry_a;
+    counters[1] = (unsigned long long)carry_p;
+    counters[4] = (unsigned long long)t;
+  }
+}
+
+// ---------------------------------------------------------------- K3 compact
+// One warp per row (b_mask, r): columns in chunks of 32, ballots give each
+// active block its position.
+__global__ void compact_kernel(DevMask m, int64_t R, const int8_t *block_mask,
+                               const int32_t *row_ptr, const int32_t *prow_ptr,
+                               int32_t *active_rows, int32_t *active_cols, int32_t *mask_next,
+                               uint8_t *bounds_start, uint8_t *bounds_end, int32_t *part_row,
+                               int32_t *part_col, int32_t *part_g) {
+  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= R) return;
+  const int32_t r = (int32_t)(row % m.nq);
+  const int32_t g0 = row_ptr[row], gend = row_ptr[row + 1];
+  int32_t g = g0, k = prow_ptr[row];
+  const unsigned lt = (1u << lane) - 1u;
+  for (int64_t cb = 0; cb < m.nk; cb += 32) {
+    const int64_t c = cb + lane;
+    const int cls = c < m.nk ? block_mask[row * m.nk + c] : 0;
+    const unsigned act = __ballot_sync(0xffffffffu, cls != 0);
+    const unsigned par = __ballot_sync(0xffffffffu, cls == 1);
+    if (cls != 0) {
+      const int32_t pos = g + __popc(act & lt);
+      active_rows[pos] = r;
+      active_cols[pos] = (int32_t)c;
+      mask_next[pos] = -1;
+      bounds_start[pos] = (uint8_t)(pos == g0);
+      bounds_end[pos] = (uint8_t)(pos == gend - 1);
+      if (cls == 1) {
+        const int32_t kk = k + __popc(par & lt);
+        part_row[kk] = (int32_t)row;
+        part_col[kk] = (int32_t)c;
+        part_g[kk] = pos;
+      }
+    }
+    g += __popc(act);
+    k += __popc(par);
+  }
+}
+
+// ---------------------------------------------------------------- K4 patterns
+constexpr uint64_t kHashBasis = 0xcbf29ce484222325ull;
+constexpr uint64_t kHashPrime = 0x100000001b3ull;
+
+__device__ __forceinline__ uint64_t hash_step(uint64_t h, uint64_t x) { return (h ^ x) * kHashPrime; }
+
+// One CTA (bq threads, one per query row) per partial block, grid-stride.
+__global__ void partial_hash_kernel(DevMask m, const unsigned long long *counters,
+                                    const int32_t *part_row, const int32_t *part_col,
+                                    uint64_t *part_hash) {
+  __shared__ uint64_t rowh[128];
+  const int64_t Ap = (int64_t)counters[1];
+  const int di = threadIdx.x;
+  for (int64_t k = blockIdx.x; k < Ap; k += gridDim.x) {
+    const int64_t row = part_row[k];
+    const int32_t bm = (int32_t)(row / m.nq);
+    const int64_t r = row % m.nq, c = part_col[k];
+    const int64_t i = r * m.bq + di;
+    const int32_t sq = q_segment(m, bm, i);
+    uint64_t h = kHashBasis;
+    for (int32_t w = 0; w < m.bk / 32; ++w) h = hash_step(h, row_word(m, bm, i, sq, c * m.bk + w * 32));
+    rowh[di] = h;
+    __syncthreads();
+    if (di == 0) {
+      uint64_t H = kHashBasis;
+      for (int32_t x = 0; x < m.bq; ++x) H = hash_step(H, rowh[x]);
+      part_hash[k] = H;
+    }
+    __syncthreads();
+  }
+}
+
+// Warp-cooperative exact comparison of two partial blocks' patterns.
+__device__ bool patterns_equal(const DevMask &m, const int32_t *part_row, const int32_t *part_col,
+                               int64_t ka, int64_t kb) {
+  const int lane = threadIdx.x & 31;
+  const int64_t rowa = part_row[ka], rowb = part_row[kb];
+  const int32_t bma = (int32_t)(rowa / m.nq), bmb = (int32_t)(rowb / m.nq);
+  const int64_t ra = rowa % m.nq, rb = rowb % m.nq, ca = part_col[ka], cb = part_col[kb];
+  bool same = true;
+  for (int32_t di = lane; di < m.bq; di += 32) {
+    const int64_t ia = ra * m.bq + di, ib = rb * m.bq + di;
+    const int32_t sa = q_segment(m, bma, ia), sb = q_segment(m, bmb, ib);
+    for (int32_t w = 0; w < m.bk / 32 && same; ++w)
+      same = row_word(m, bma, ia, sa, ca * m.bk + w * 32) == row_word(m, bmb, ib, sb, cb * m.bk + w * 32);
+  }
+  return __all_sync(0xffffffffu, same);
+}
+
+// One warp per partial block k: rep[k] = the first k' <= k with identical content.
+__global__ void dedup_kernel(DevMask m, const unsigned long long *counters, const int32_t *part_row,
+                             const int32_t *part_col, const uint64_t *part_hash, int32_t *part_rep) {
+  const int64_t Ap = (int64_t)counters[1];
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t k = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; k < Ap; k += nwarps) {
+    const uint64_t h = part_hash[k];
+    int64_t rep = k;
+    for (int64_t base = 0; base < k && rep == k; base += 32) {
+      const int64_t kp = base + lane;
+      unsigned cand = __ballot_sync(0xffffffffu, kp < k && part_hash[kp] == h);
+      while (cand) {
+        const int t = __ffs(cand) - 1;
+        cand &= cand - 1u;
+        if (patterns_equal(m, part_row, part_col, k, base + t)) {
+          rep = base + t;
+          break;
+        }
+      }
+    }
+    if (lane == 0) part_rep[k] = (int32_t)rep;
+  }
+}
+
+__global__ void __launch_bounds__(1024)
+scan_reps_kernel(unsigned long long *counters, const int32_t *part_rep, int32_t *part_pidx) {
+  __shared__ int buf[33];
+  const int64_t Ap = (int64_t)counters[1];
+  int carry = 0;
+  for (int64_t base = 0; base < Ap; base += blockDim.x) {
+    const int64_t k = base + threadIdx.x;
+    const int f = (k < Ap && part_rep[k] == k) ? 1 : 0;
+    int tot;
+    const int ex = block_excl_scan(f, tot, buf);
+    if (k < Ap) part_pidx[k] = carry + ex;
+    carry += tot;
+  }
+  if (threadIdx.x == 0) counters[2] = (unsigned long long)carry;
+}
+
+__global__ void finalize_kernel(const unsigned long long *counters, const int32_t *part_g,
+                                const int32_t *part_rep, const int32_t *part_pidx,
+                                int32_t *mask_next, int32_t *rep_list) {
+  const int64_t Ap = (int64_t)counters[1];
+  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < Ap;
+       k += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t rep = part_rep[k];
+    const int32_t u = part_pidx[rep];
+    mask_next[part_g[k]] = u;
+    if (rep == k) rep_list[u] = (int32_t)k;
+  }
+}
+
+// One CTA (bq threads) per pattern: the bit-packed rows and the byte pattern.
+__global__ void materialize_kernel(DevMask m, int64_t P, const int32_t *rep_list,
+                                   const int32_t *part_row, const int32_t *part_col,
+                                   uint32_t *pattern_bits, uint8_t *patterns) {
+  const int di = threadIdx.x;
+  const int32_t words = m.bk / 32;
+  for (int64_t u = blockIdx.x; u < P; u += gridDim.x) {
+    const int64_t k = rep_list[u];
+    const int64_t row = part_row[k];
+    const int32_t bm = (int32_t)(row / m.nq);
+    const int64_t r = row % m.nq, c = part_col[k];
+    const int64_t i = r * m.bq + di;
+    const int32_t sq = q_segment(m, bm, i);
+    uint32_t *bits = pattern_bits + (u * m.bq + di) * words;
+    uchar4 *bytes = reinterpret_cast<uchar4 *>(patterns + (u * m.bq + di) * m.bk);
+    for (int32_t w = 0; w < words; ++w) {
+      const uint32_t word = row_word(m, bm, i, sq, c * m.bk + w * 32);
+      bits[w] = word;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const uint32_t nib = word >> (4 * t);
+        bytes[w * 8 + t] = make_uchar4(nib & 1u, (nib >> 1) & 1u, (nib >> 2) & 1u, (nib >> 3) & 1u);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- row order
+// Rows sorted by descending active-block count, ties in ascending row order
+// (a stable counting sort): the attention kernel takes its work longest row
+// first.  One CTA; `hist` is a global scratch array of nk+1 counters.
+__global__ void __launch_bounds__(1024)
+row_order_kernel(int64_t R, int64_t nk, const int32_t *row_cnt, int32_t *hist, int32_t *row_order) {
+  __shared__ int buf[33];
+  for (int64_t b = threadIdx.x; b <= nk; b += blockDim.x) hist[b] = 0;
+  __syncthreads();
+  for (int64_t x = threadIdx.x; x < R; x += blockDim.x) atomicAdd(&hist[row_cnt[x]], 1);
+  __syncthreads();
+  // exclusive scan over bins nk, nk-1, ..., 0 (descending counts first)
+  int carry = 0;
+  for (int64_t base = 0; base <= nk; base += blockDim.x) {
+    const int64_t x = base + threadIdx.x;
+    const int64_t bin = nk - x;
+    const int h = x <= nk ? hist[bin] : 0;
+    int tot;
+    const int ex = block_excl_scan(h, tot, buf);
+    if (x <= nk) hist[bin] = carry + ex;
+    carry += tot;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const unsigned lt = (1u << lane) - 1u;
+    for (int64_t base = 0; base < R; base += 32) {
+      const int64_t x = base + lane;
+      const bool valid = x < R;
+      const int c = valid ? row_cnt[x] : -1 - lane;  // invalid lanes get unique keys
+      const unsigned peers = __match_any_sync(0xffffffffu, c);
+      const int pos = valid ? hist[c] + __popc(peers & lt) : 0;
+      __syncwarp();
+      if (valid) {
+        row_order[pos] = (int32_t)x;
+        if ((peers & lt) == 0) hist[c] += __popc(peers);
+      }
+      __syncwarp();
+    }
+  }
+}
+
+// ---------------------------------------------------------------- host side
+template <typename T>
+cudaError_t grow(T *&p, int64_t have, int64_t need) {
+  if (p != nullptr && have >= need) return cudaSuccess;
+  if (p) cudaFree(p);
+  p = nullptr;
+  return cudaMalloc(&p, sizeof(T) * (size_t)std::max<int64_t>(need, 1));
+}
+
+template <typename T>
+cudaError_t grow_host(T *&p, int64_t have, int64_t need) {
+  if (p != nullptr && have >= need) return cudaSuccess;
+  if (p) cudaFreeHost(p);
+  p = nullptr;
+  return cudaMallocHost(&p, sizeof(T) * (size_t)std::max<int64_t>(need, 1));
+}
+
+splash_status map_alloc(cudaError_t e) {
+  if (e == cudaSuccess) return SPLASH_OK;
+  cudaGetLastError();
+  return e == cudaErrorMemoryAllocation ? SPLASH_ERR_OOM : SPLASH_ERR_CUDA;
+}
+
+}  // namespace
+
+void splash_mask_info_free_buffers(splash_mask_info *mi) {
+  void *dev[] = {mi->block_mask, mi->row_ptr, mi->active_rows, mi->active_cols, mi->mask_next,
+                 mi->bounds_start, mi->bounds_end, mi->patterns, mi->pattern_bits, mi->row_order,
+                 mi->row_cnt, mi->row_pcnt, mi->prow_ptr, mi->seg_summary, mi->part_row,
+                 mi->part_col, mi->part_g, mi->part_hash, mi->part_rep, mi->part_pidx,
+                 mi->rep_list, mi->counters, mi->row_hist};
+  for (void *p : dev)
+    if (p) cudaFree(p);
+  void *host[] = {mi->h_counters};
+  for (void *p : host)
+    if (p) cudaFreeHost(p);
+  const int device = mi->device;
+  *mi = splash_mask_info();
+  mi->device = device;
+}
+
+splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mask_spec *spec,
+                                          int64_t Lq, int64_t Lk, int32_t bq, int32_t bk,
+                                          cudaStream_t stream) {
+  const bool seg = spec->q_segment_ids != nullptr;
+  const int32_t nbm = seg ? spec->batch : 1;
+  const int64_t nq = Lq / bq, nk = Lk / bk, R = (int64_t)nbm * nq, NB = R * nk;
+
+  // -- buffers (reused when large enough) --
+  splash_status st;
+  if ((st = map_alloc(grow(mi->block_mask, mi->cap_blocks, NB))) != SPLASH_OK) return st;
+  if ((st = map_alloc(grow(mi->active_rows, mi->cap_blocks, NB))) != SPLASH_OK) return st;
+  if ((st = map_alloc(grow(mi->active_cols, mi->cap_blocks, NB))) != SPLASH_OK) return st;
+  if ((st = map_alloc(grow(mi->mask_next, mi->cap_blocks, NB))) != SPLASH_OK) return st;
+  if ((st = map_alloc(grow(mi->bounds_start, mi->cap_blocks, NB))) != SPLASH_OK) return st;
+  if ((st = map_alloc(grow(mi->bounds_end, mi->cap_blocks, NB))) != SPLASH_OK) return st;
+  if ((st = map_alloc(grow(mi->part_row, mi->cap_blocks, NB))) != SPLASH_OK) return st;
+  if ((st = map_alloc(grow(mi->part_col, mi->cap_blocks, NB))) != SPLASH_OK) return st;
+  if ((st = map_alloc(grow(mi->part_g, mi->cap_blocks, NB))) != SPLASH_OK) return st;
+  if ((st = map_alloc(grow(mi->part_hash, mi->cap_blocks, NB))) != SPLASH_OK) return st;
+  if ((st = map_alloc(grow(mi->part_rep, mi->cap_blocks, NB))) != SPLASH_OK) return st;
+  if ((st = map_alloc(grow(mi->part_pidx, mi->cap_blocks, NB))) != SPLASH_OK) return st;
+  if ((st = map_alloc(grow(mi->rep_list, mi->cap_blocks, NB))) != SPLASH_OK) return st;
+  mi->cap_blocks = std::max(mi->cap_blocks, NB);
+  if ((st = map_alloc(grow(mi->row_ptr, mi->cap_rows, R + 1))) != SPLASH_OK) return st;
+  if ((st = map_alloc(grow(mi->prow_ptr, mi->cap_rows, R + 1))) != SPLASH_OK) return st;
+  if ((st = map_alloc(grow(mi->row_cnt, mi->cap_rows, R + 1))) != SPLASH_OK) return st;
+  if ((st = map_alloc(grow(mi->row_pcnt, mi->cap_rows, R + 1))) != SPLASH_OK) return st;
+  if ((st = map_alloc(grow(mi->row_order, mi->cap_rows, R + 1))) != SPLASH_OK) return st;
+  mi->cap_rows = std::max(mi->cap_rows, R + 1);
+  if ((st = map_alloc(grow(mi->row_hist, mi->cap_hist, nk + 1))) != SPLASH_OK) return st;
+  mi->cap_hist = std::max(mi->cap_hist, nk + 1);
+  const int64_t nseg = seg ? 2 * (R + (int64_t)nbm * nk) : 2;
+  if ((st = map_alloc(grow(mi->seg_summary, mi->cap_seg, nseg))) != SPLASH_OK) return st;
+  mi->cap_seg = std::max(mi->cap_seg, nseg);
+  if ((st = map_alloc(grow(mi->counters, mi->counters ? 8 : 0, 8))) != SPLASH_OK) return st;
+  if ((st = map_alloc(grow_host(mi->h_counters, mi->h_counters ? 8 : 0, 8))) != SPLASH_OK) return st;
+
+  mi->batch_rows = nbm;
+  mi->Lq = Lq;
+  mi->Lk = Lk;
+  mi->nq = nq;
+  mi->nk = nk;
+  mi->bq = bq;
+  mi->bk = bk;
+  mi->causal = spec->causal;
+  mi->window_left = spec->window_left;
+  mi->window_right = spec->window_right;
+  mi->has_segments = seg;
+  mi->num_active = mi->num_partial = mi->num_patterns = mi->allowed_pairs = 0;
+
+  DevMask m;
+  m.causal = spec->causal;
+  m.wl = spec->window_left;
+  m.wr = spec->window_right;
+  m.qseg = spec->q_segment_ids;
+  m.kvseg = seg ? (spec->kv_segment_ids ? spec->kv_segment_ids : spec->q_segment_ids) : nullptr;
+  m.Lq = Lq;
+  m.Lk = Lk;
+  m.nq = nq;
+  m.nk = nk;
+  m.bq = bq;
+  m.bk = bk;
+  m.nbm = nbm;
+
+  int dev = 0, sms = 148;
+  SPLASH_CUDA_TRY(cudaGetDevice(&dev));
+  SPLASH_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+
+  SPLASH_CUDA_TRY(cudaMemsetAsync(mi->row_cnt, 0, sizeof(int32_t) * R, stream));
+  SPLASH_CUDA_TRY(cudaMemsetAsync(mi->row_pcnt, 0, sizeof(int32_t) * R, stream));
+  SPLASH_CUDA_TRY(cudaMemsetAsync(mi->counters, 0, sizeof(unsigned long long) * 8, stream));
+
+  int32_t *qsum = mi->seg_summary, *kvsum = mi->seg_summary + 2 * R;
+  if (seg) {
+    dim3 grid((unsigned)((nq + nk + 7) / 8), (unsigned)nbm);
+    seg_summary_kernel<<<grid, 256, 0, stream>>>(m, qsum, kvsum);
+  }
+  {
+    dim3 grid((unsigned)((nk + kClassifyThreads - 1) / kClassifyThreads), (unsigned)nq, (unsigned)nbm);
+    classify_kernel<<<grid, kClassifyThreads, 0, stream>>>(m, qsum, kvsum, mi->block_mask, mi->row_cnt,
+                                                          mi->row_pcnt, mi->counters);
+  }
+  scan_rows_kernel<<<1, 1024, 0, stream>>>(R, mi->row_cnt, mi->row_pcnt, mi->row_ptr, mi->prow_ptr,
+                                           mi->counters);
+  row_order_kernel<<<1, 1024, 0, stream>>>(R, nk, mi->row_cnt, mi->row_hist, mi->row_order);
+  compact_kernel<<<(unsigned)((R + 7) / 8), 256, 0, stream>>>(
+      m, R, mi->block_mask, mi->row_ptr, mi->prow_ptr, mi->active_rows, mi->active_cols,
+      mi->mask_next, mi->bounds_start, mi->bounds_end, mi->part_row, mi->part_col, mi->part_g);
+  partial_hash_kernel<<<sms * 4, bq, 0, stream>>>(m, mi->counters, mi->part_row, mi->part_col,
+                                                  mi->part_hash);
+  dedup_kernel<<<sms * 4, 256, 0, stream>>>(m, mi->counters, mi->part_row, mi->part_col,
+                                            mi->part_hash, mi->part_rep);
+  scan_reps_kernel<<<1, 1024, 0, stream>>>(mi->counters, mi->part_rep, mi->part_pidx);
+  finalize_kernel<<<sms * 4, 256, 0, stream>>>(mi->counters, mi->part_g, mi->part_rep,
+                                               mi->part_pidx, mi->mask_next, mi->rep_list);
+  SPLASH_CUDA_TRY(cudaGetLastError());
+  splash_count_launches(seg ? 10 : 9);
+
+  // -- the one host wait: the totals (P sizes the pattern buffer) --
+  SPLASH_CUDA_TRY(cudaMemcpyAsync(mi->h_counters, mi->counters, sizeof(unsigned long long) * 8,
+                                  cudaMemcpyDeviceToHost, stream));
+  SPLASH_CUDA_TRY(cudaStreamSynchronize(stream));
+  mi->num_active = (int64_t)mi->h_counters[0];
+  mi->num_partial = (int64_t)mi->h_counters[1];
+  mi->num_patterns = (int64_t)mi->h_counters[2];
+  mi->allowed_pairs = (int64_t)mi->h_counters[3];
+  mi->max_row_blocks = (int32_t)mi->h_counters[4];
+
+  const int64_t P = mi->num_patterns;
+  if (P > 0) {
+    if (mi->cap_patterns < P) {
+      if (mi->patterns) cudaFree(mi->patterns);
+      if (mi->pattern_bits) cudaFree(mi->pattern_bits);
+      mi->patterns = nullptr;
+      mi->pattern_bits = nullptr;
+      mi->cap_patterns = 0;
+      if ((st = map_alloc(cudaMalloc(&mi->patterns, (size_t)P * bq * bk))) != SPLASH_OK) return st;
+      if ((st = map_alloc(cudaMalloc(&mi->pattern_bits, (size_t)P * bq * (bk / 32) * 4))) != SPLASH_OK)
+        return st;
+      mi->cap_patterns = P;
+    }
+    const unsigned grid = (unsigned)std::min<int64_t>(P, 65535);
+    materialize_kernel<<<grid, bq, 0, stream>>>(m, P, mi->rep_list, mi->part_row, mi->part_col,
+                                                mi->pattern_bits, mi->patterns);
+    SPLASH_CUDA_TRY(cudaGetLastError());
+    splash_count_launches(1);
+  }
+  return SPLASH_OK;
+}

@@ -1,0 +1,233 @@
+/*
+ * splash.h -- C ABI of the GB300 (sm_103a) block-sparse masked attention
+ * library (libsplash.so).
+ *
+ * The operation is the forward pass of "Splash" attention: a mask made of a
+ * causal part, a local window and document segment IDs, joined by AND, is
+ * preprocessed into a sparse execution table (MaskInfo), and an attention
+ * kernel walks only the non-empty key/value blocks of each query block with an
+ * online softmax, writing O and the per-row log-sum-exp.
+ *
+ * Sources:
+ *   "Pallas Kernels and Splash Attention" (CMU 11-868 Lecture 13 notes):
+ *     §5.1 online softmax; §5.2 the Flash kernel body (m, l, o accumulators,
+ *     alpha rescale, deferred normalisation), MHA/GQA; §5.4 soft cap;
+ *     §6.1 empty / partial / full blocks; §6.2 MaskInfo (block_mask,
+ *     partial_mask_blocks, mask_next, bounds_start / bounds_end); §6.3 the
+ *     Splash grid over active blocks and the residual LSE; §6.4 segment IDs
+ *     and masks joined by AND.
+ *   "The maths and infra behind core LLM operations" (joto.ai): sections
+ *     "Causal Mask" (skip blocks above the diagonal, mask only the diagonal
+ *     ones) and "LSE and Online Softmax" (LSE = m + log l).
+ *
+ * Conventions that hold for every call:
+ *   - All tensors are caller-owned.  Pointers documented as "device" must be
+ *     device memory of the current CUDA device; "host" pointers are ordinary
+ *     host memory.  Nothing is retained after a call returns except inside a
+ *     splash_mask_info handle.
+ *   - `cuda_stream` is a cudaStream_t (NULL = the legacy default stream).
+ *     Kernels are launched asynchronously on it.
+ *   - No call throws, exits or traps.  Invalid arguments are detected on the
+ *     host before any launch and reported as a status; the output buffers are
+ *     then untouched.
+ *   - Tensor layouts are dense row-major (contiguous), innermost dimension
+ *     last.
+ */
+#ifndef SPLASH_H
+#define SPLASH_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SPLASH_OK = 0,
+    SPLASH_ERR_INVALID_ARG = 1,    /* NULL pointer, negative size, bad flag */
+    SPLASH_ERR_SHAPE = 2,          /* sizes inconsistent with each other or with the MaskInfo */
+    SPLASH_ERR_UNSUPPORTED = 3,    /* valid, but outside what this build implements */
+    SPLASH_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed */
+    SPLASH_ERR_DEVICE_TIMEOUT = 5, /* a kernel's bounded wait ran out (see splash_last_device_error) */
+    SPLASH_ERR_OOM = 6,            /* device allocation failed */
+    SPLASH_ERR_DEVICE_CHECK = 7    /* a kernel's bounds check rejected table contents */
+} splash_status;
+
+/*
+ * The joint mask (AND of the enabled parts), "Pallas Kernels and Splash
+ * Attention" §6.1 and §6.4.  Query position i and key position j are 0-based
+ * within their sequence; for batch row b the pair is allowed when
+ *     (!causal || j <= i)
+ *  && (window_left  < 0 || i - j <= window_left)
+ *  && (window_right < 0 || j - i <= window_right)
+ *  && (q_segment_ids == NULL || q_segment_ids[b][i] == kv_segment_ids[b][j]).
+ * A window of W keys including the query itself is window_left = W - 1.
+ */
+typedef struct {
+    int32_t causal;                 /* 0 or 1 */
+    int64_t window_left;            /* inclusive distance to the left; -1 = unbounded */
+    int64_t window_right;           /* inclusive distance to the right; -1 = unbounded */
+    const int32_t *q_segment_ids;   /* device int32 [batch][Lq], or NULL for no document mask */
+    const int32_t *kv_segment_ids;  /* device int32 [batch][Lk]; NULL means "same as q_segment_ids"
+                                       (then Lq must equal Lk) */
+    int32_t batch;                  /* rows of the segment arrays; ignored when q_segment_ids is NULL */
+} splash_mask_spec;
+
+/* Opaque, library-owned MaskInfo; freed by splash_mask_info_destroy. */
+typedef struct splash_mask_info splash_mask_info;
+
+/*
+ * splash_build_mask_info -- preprocess a mask into the sparse execution table
+ * ("Pallas Kernels and Splash Attention" §6.2, §6.3, §6.6).
+ *
+ * Every (bq x bk) block of the [Lq, Lk] mask is classified as empty (0),
+ * partial (1) or full (2) (block_mask).  Active (non-empty) blocks are listed
+ * in row-major order (q-block ascending, then kv-block ascending) as
+ * active_rows / active_cols, with row_ptr giving each q-block row's range
+ * (CSR) and bounds_start / bounds_end flagging the first / last active block
+ * of a row.  Each partial block's bq x bk element pattern (1 = allowed) is
+ * deduplicated by exact content in first-occurrence order into
+ * partial_mask_blocks; mask_next[g] is the pattern index of active block g, or
+ * -1 when the block is full.
+ *
+ * With segment IDs the table has B_mask = spec->batch batch rows (one per
+ * segment-array row); without them B_mask = 1 and it serves every batch row
+ * and head.  Rows are then ordered (b_mask, q-block).
+ *
+ *   spec        host pointer to the mask; its segment arrays are device memory
+ *               and are read on `cuda_stream` before this call returns.
+ *   Lq, Lk      sequence lengths (> 0); Lq % bq == 0 and Lk % bk == 0.
+ *   bq, bk      block sizes; this build supports bq, bk in {64, 128}.
+ *   cuda_stream stream for the build kernels.
+ *   out         receives a new handle (set to NULL on error).
+ *
+ * Synchronisation: the call waits once on `cuda_stream` to read the number of
+ * distinct patterns (it sizes the pattern buffer), so it is not capturable in
+ * a CUDA graph.  The returned table is complete when the call returns.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA, OOM; *out is NULL then.
+ */
+splash_status splash_build_mask_info(const splash_mask_spec *spec, int64_t Lq, int64_t Lk,
+                                     int32_t bq, int32_t bk, void *cuda_stream,
+                                     splash_mask_info **out);
+
+/*
+ * splash_mask_info_rebuild -- the same computation as splash_build_mask_info,
+ * written into an existing handle whose buffers are reused when they are large
+ * enough (no device allocation then).  The handle's previous contents are
+ * replaced; on error the handle is left empty but valid (destroy it or rebuild
+ * it).  Same synchronisation as splash_build_mask_info.
+ */
+splash_status splash_mask_info_rebuild(splash_mask_info *mi, const splash_mask_spec *spec,
+                                       int64_t Lq, int64_t Lk, int32_t bq, int32_t bk,
+                                       void *cuda_stream);
+
+/*
+ * splash_mask_info_shape -- host-side read of the table's geometry.
+ *   batch_rows = B_mask, nq = Lq/bq, nk = Lk/bk.  Any output may be NULL.
+ */
+splash_status splash_mask_info_shape(const splash_mask_info *mi, int32_t *batch_rows, int64_t *nq,
+                                     int64_t *nk, int32_t *bq, int32_t *bk);
+
+/*
+ * splash_mask_info_counts -- totals of the table (host values, no sync):
+ *   num_active    active blocks A (over all batch rows),
+ *   num_partial   partial blocks,
+ *   num_patterns  distinct partial patterns P,
+ *   allowed_pairs allowed (query, key) pairs summed over the batch rows (the
+ *                 "useful" entries of the score matrix).
+ * Any output may be NULL.
+ */
+splash_status splash_mask_info_counts(const splash_mask_info *mi, int64_t *num_active,
+                                      int64_t *num_partial, int64_t *num_patterns,
+                                      int64_t *allowed_pairs);
+
+/*
+ * splash_mask_info_to_host -- copy the table into caller-allocated HOST arrays
+ * (synchronous).  Sizes: block_mask [B_mask*nq*nk], row_ptr [B_mask*nq + 1],
+ * active_rows / active_cols / mask_next / bounds_start / bounds_end [A],
+ * partial_mask_blocks [P*bq*bk].  Any pointer may be NULL to skip that array.
+ */
+splash_status splash_mask_info_to_host(const splash_mask_info *mi, int8_t *block_mask,
+                                       int32_t *row_ptr, int32_t *active_rows,
+                                       int32_t *active_cols, int32_t *mask_next,
+                                       uint8_t *bounds_start, uint8_t *bounds_end,
+                                       uint8_t *partial_mask_blocks);
+
+/* Frees the handle and its device memory (NULL is a no-op).  Work queued on
+ * other streams that still reads the table must be complete first. */
+void splash_mask_info_destroy(splash_mask_info *mi);
+
+/*
+ * splash_attention_fwd -- block-sparse masked attention forward
+ * ("Pallas Kernels and Splash Attention" §5.1-§5.4, §6.3).
+ *
+ * For every batch b, query head h and query i, with kv head g = h / (Hq/Hkv):
+ *   s_j  = scale * q[b,h,i,:] . k[b,g,j,:]              (fp32 accumulation)
+ *   s_j  = softcap * tanh(s_j / softcap)                 (only if softcap > 0)
+ *   over the keys j allowed by the MaskInfo's mask:
+ *   out[b,h,i,:] = sum_j exp(s_j - m) v[b,g,j,:] / sum_j exp(s_j - m)
+ *   lse[b,h,i]   = m + ln(sum_j exp(s_j - m))            (natural log)
+ * Rows with no allowed key get out = 0 and lse = -inf.  Only the MaskInfo's
+ * active blocks are loaded or computed; partial blocks are masked element by
+ * element from partial_mask_blocks.
+ *
+ *   q    device bf16 [B][Hq][Lq][dqk]      k  device bf16 [B][Hkv][Lk][dqk]
+ *   v    device bf16 [B][Hkv][Lk][dv]      (all 16-byte aligned)
+ *   q_segment_ids, kv_segment_ids  the device arrays the MaskInfo was built
+ *        from, or NULL; accepted for interface symmetry (the stored patterns
+ *        already encode them).
+ *   mi   a MaskInfo built for (Lq, Lk) with B_mask == 1 or B_mask == B.
+ *   scale  multiplies q.k (e.g. 1/sqrt(dqk)); softcap <= 0 disables the cap.
+ *   out  device bf16 [B][Hq][Lq][dv]       lse device fp32 [B][Hq][Lq]
+ *
+ * Supported in this build: dqk in {64, 128, 192}, dv in {64, 128}, dv <= dqk
+ * when dqk = 192 is used with dv = 128, Hq % Hkv == 0, and the MaskInfo's
+ * blocks bq, bk in {64, 128} with bq == bk.  Other valid shapes return
+ * SPLASH_ERR_UNSUPPORTED.
+ * Errors are returned before any launch; kernel-side bounded waits and table
+ * checks are reported by splash_last_device_error.
+ */
+splash_status splash_attention_fwd(const void *q, const void *k, const void *v, int32_t B,
+                                   int32_t Hq, int32_t Hkv, int64_t Lq, int64_t Lk, int32_t dqk,
+                                   int32_t dv, const int32_t *q_segment_ids,
+                                   const int32_t *kv_segment_ids, const splash_mask_info *mi,
+                                   float scale, float softcap, void *out, float *lse,
+                                   void *cuda_stream);
+
+/*
+ * splash_last_device_error -- synchronises `cuda_stream`, then reads and
+ * clears the device error word that the library's kernels set when a bounded
+ * wait runs out (SPLASH_ERR_DEVICE_TIMEOUT) or a table entry fails a bounds
+ * check (SPLASH_ERR_DEVICE_CHECK).  Returns SPLASH_OK when no kernel
+ * reported anything, SPLASH_ERR_CUDA when the synchronisation itself fails.
+ */
+splash_status splash_last_device_error(void *cuda_stream);
+
+/*
+ * splash_debug_wait_selftest -- launches one tiny kernel whose mbarrier wait
+ * can never be satisfied (nothing arrives on it), bounded by timeout_ns
+ * nanoseconds, and returns what splash_last_device_error then reports
+ * (SPLASH_ERR_DEVICE_TIMEOUT when the bound works).  It exercises the same
+ * bounded-wait helper the attention kernel uses, without faulting or hanging
+ * the device.  timeout_ns must be in (0, 2e9].
+ */
+splash_status splash_debug_wait_selftest(uint64_t timeout_ns, void *cuda_stream);
+
+/*
+ * splash_kernel_launches -- number of kernels this library has launched in
+ * this process so far (all devices, all entry points).  Host-side counter,
+ * thread-safe; for accounting in benchmarks.
+ */
+uint64_t splash_kernel_launches(void);
+
+/* Static description of a status code (never NULL). */
+const char *splash_status_string(splash_status status);
+
+/* Library version string, e.g. "splash-gb300 0.1 sm_103a". */
+const char *splash_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPLASH_H */

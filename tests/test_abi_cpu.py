@@ -1,0 +1,85 @@
+"""The C ABI on the CPU: the library loads, exports every symbol include/splash.h
+declares, and rejects invalid arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "splash.h")
+
+
+@pytest.fixture(scope="module")
+def splash():
+    from block_sparse_flash_gb300 import build as b
+    b.build()
+    import block_sparse_flash_gb300 as bsf
+    return bsf
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(splash_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("splash_build_mask_info", "splash_attention_fwd", "splash_mask_info_counts",
+                     "splash_mask_info_to_host", "splash_mask_info_destroy", "splash_last_device_error",
+                     "splash_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(splash):
+    lib = splash.lib()
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libsplash.so does not export {name}"
+
+
+def test_status_strings_and_version(splash):
+    lib = splash.lib()
+    for code in range(8):
+        s = lib.splash_status_string(code).decode()
+        assert s.startswith("SPLASH_")
+    assert lib.splash_status_string(99).decode() == "SPLASH_ERR_UNKNOWN"
+    assert "sm_103a" in splash.version()
+
+
+def test_invalid_arguments_are_rejected_before_any_launch(splash):
+    lib = splash.lib()
+    out = ctypes.c_void_p()
+    spec = splash._Spec(1, -1, -1, None, None, 0)
+    null = ctypes.c_void_p(0)
+    # no output pointer / no spec
+    assert lib.splash_build_mask_info(ctypes.byref(spec), 256, 256, 64, 64, null, None) == 1
+    assert lib.splash_build_mask_info(None, 256, 256, 64, 64, null, ctypes.byref(out)) == 1
+    # bad sizes and unsupported blocks
+    assert lib.splash_build_mask_info(ctypes.byref(spec), 0, 256, 64, 64, null, ctypes.byref(out)) == 1
+    assert lib.splash_build_mask_info(ctypes.byref(spec), 256, 256, 32, 32, null, ctypes.byref(out)) == 3
+    assert lib.splash_build_mask_info(ctypes.byref(spec), 250, 256, 64, 64, null, ctypes.byref(out)) == 3
+    bad = splash._Spec(2, -1, -1, None, None, 0)
+    assert lib.splash_build_mask_info(ctypes.byref(bad), 256, 256, 64, 64, null, ctypes.byref(out)) == 1
+    bad = splash._Spec(1, -5, -1, None, None, 0)
+    assert lib.splash_build_mask_info(ctypes.byref(bad), 256, 256, 64, 64, null, ctypes.byref(out)) == 1
+    segs = splash._Spec(1, -1, -1, 16, None, 0)   # segment pointer with batch 0
+    assert lib.splash_build_mask_info(ctypes.byref(segs), 256, 256, 64, 64, null, ctypes.byref(out)) == 1
+    assert not out
+    # attention: NULL tensors / handle
+    f = lib.splash_attention_fwd
+    assert f(None, None, None, 1, 2, 2, 256, 256, 64, 64, None, None, None, 0.125, 0.0, None, None, null) == 1
+    # counts / shape / to_host on a NULL handle
+    assert lib.splash_mask_info_counts(None, None, None, None, None) == 1
+    assert lib.splash_mask_info_shape(None, None, None, None, None, None) == 1
+    lib.splash_mask_info_destroy(None)
+    assert lib.splash_debug_wait_selftest(0, null) == 1
+    assert lib.splash_debug_wait_selftest(3 * 10 ** 9, null) == 1
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, splash):
+    monkeypatch.setattr(splash, "_lib", None)
+    monkeypatch.setattr(splash, "LIB_PATH", "/nonexistent/libsplash.so")
+    with pytest.raises(splash.SplashLibraryMissing):
+        splash.lib()

@@ -1,0 +1,104 @@
+"""MaskInfo built on the GPU must equal the oracle's brute-force table
+bit for bit (every array), on the five workloads' masks and on fuzzed masks."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def bsf():
+    from block_sparse_flash_gb300 import build as b
+    b.build()
+    import block_sparse_flash_gb300 as m
+    return m
+
+
+def gpu_and_oracle(bsf, causal, wl, wr, seg_q, seg_kv, Lq, Lk, bq, bk):
+    q_dev = seg_q.cuda() if seg_q is not None else None
+    kv_dev = seg_kv.cuda() if seg_kv is not None else None
+    mi = bsf.build_mask_info(bsf.MaskSpec(causal, wl, wr, q_dev, kv_dev), Lq, Lk, bq, bk)
+    got = mi.to_host()
+    mi.close()
+    ref = oracle.mask_info(oracle.MaskSpec(causal, wl, wr,
+                                           seg_q.numpy() if seg_q is not None else None,
+                                           (seg_kv if seg_kv is not None else seg_q).numpy()
+                                           if seg_q is not None else None), Lq, Lk, bq, bk)
+    return got, ref
+
+
+def assert_same(got, ref, label):
+    np.testing.assert_array_equal(got["block_mask"], ref.block_mask, err_msg=label)
+    np.testing.assert_array_equal(got["row_ptr"], ref.row_ptr, err_msg=label)
+    np.testing.assert_array_equal(got["active_rows"], ref.active_rows, err_msg=label)
+    np.testing.assert_array_equal(got["active_cols"], ref.active_cols, err_msg=label)
+    np.testing.assert_array_equal(got["mask_next"], ref.mask_next, err_msg=label)
+    np.testing.assert_array_equal(got["bounds_start"], ref.bounds_start, err_msg=label)
+    np.testing.assert_array_equal(got["bounds_end"], ref.bounds_end, err_msg=label)
+    np.testing.assert_array_equal(got["partial_mask_blocks"], ref.partial_mask_blocks, err_msg=label)
+    assert got["num_active"] == ref.num_active, label
+    assert got["num_partial"] == ref.num_partial, label
+    assert got["num_patterns"] == ref.num_patterns, label
+    assert got["allowed_pairs"] == ref.allowed_pairs, label
+
+
+@pytest.mark.parametrize("index", [1, 2, 3, 4, 5])
+def test_workload_masks_bit_exact(bsf, index):
+    w = workloads.workload(index)
+    seg = workloads.make_inputs(w, with_values=False).segment_ids
+    got, ref = gpu_and_oracle(bsf, w.causal, w.window_left, w.window_right, seg, seg, w.L, w.L, w.bq, w.bk)
+    assert_same(got, ref, w.name)
+
+
+def fuzz_cases():
+    rng = np.random.default_rng(1234)
+    cases = []
+    for n in range(40):
+        L = int(rng.choice([128, 256, 512, 1024]))
+        bq = int(rng.choice([64, 128]))
+        bk = int(rng.choice([64, 128]))
+        causal = bool(rng.integers(2))
+        wl = int(rng.choice([-1, 0, 1, 63, 64, 100, 300]))
+        wr = int(rng.choice([-1, 0, 5, 64, 200]))
+        kind = int(rng.integers(4))  # 0 none, 1 sorted docs, 2 non-monotone ids, 3 batch of 2 with q != kv
+        cases.append((n, L, bq, bk, causal, wl, wr, kind, int(rng.integers(1 << 30))))
+    return cases
+
+
+@pytest.mark.parametrize("n,L,bq,bk,causal,wl,wr,kind,seed", fuzz_cases())
+def test_fuzzed_masks_bit_exact(bsf, n, L, bq, bk, causal, wl, wr, kind, seed):
+    seg_q = seg_kv = None
+    if kind == 1:
+        seg_q = seg_kv = workloads.random_segment_ids(1, L, seed, 6, True)
+    elif kind == 2:
+        seg_q = seg_kv = workloads.random_segment_ids(1, L, seed, 3, False)
+    elif kind == 3:
+        seg_q = workloads.random_segment_ids(2, L, seed, 4, True)
+        seg_kv = workloads.random_segment_ids(2, L, seed + 1, 4, True)
+    got, ref = gpu_and_oracle(bsf, causal, wl, wr, seg_q, seg_kv, L, L, bq, bk)
+    assert_same(got, ref, f"case {n}")
+
+
+def test_rebuild_reuses_the_handle(bsf):
+    seg = workloads.random_segment_ids(1, 1024, 5, 5, True).cuda()
+    mi = bsf.build_mask_info(bsf.MaskSpec(True), 4096, 4096, 128, 128)
+    a = mi.counts()
+    mi.rebuild(bsf.MaskSpec(False, 10, 10, seg, seg), 1024, 1024, 64, 64)
+    got = mi.to_host()
+    ref = oracle.mask_info(oracle.MaskSpec(False, 10, 10, seg.cpu().numpy(), seg.cpu().numpy()), 1024, 1024, 64, 64)
+    assert_same(got, ref, "rebuilt")
+    mi.rebuild(bsf.MaskSpec(True), 4096, 4096, 128, 128)
+    assert mi.counts() == a
+    mi.close()
+
+
+def test_everything_masked_gives_an_empty_table(bsf):
+    q = torch.zeros(1, 256, dtype=torch.int32)
+    kv = torch.ones(1, 256, dtype=torch.int32)
+    got, ref = gpu_and_oracle(bsf, True, -1, -1, q, kv, 256, 256, 64, 64)
+    assert got["num_active"] == 0
+    assert_same(got, ref, "empty")
