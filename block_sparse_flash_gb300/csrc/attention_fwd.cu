@@ -21,9 +21,10 @@
 //     one q-block row); the two heads are two 128-row query tiles that share
 //     the row's active list, and share K/V tiles when they are in the same
 //     GQA group;
-//   * warp roles: warps 0-3 / 4-7 run the softmax of tile 0 / tile 1 (one
-//     thread per query row = one TMEM lane), warp 8 issues TMA loads, warp 9
-//     issues tcgen05 MMAs;
+//   * warp roles (384 threads): warps 0-3 / 4-7 run the softmax of tile 0 /
+//     tile 1 (one thread per query row = one TMEM lane), warp 8 issues TMA
+//     loads, warp 9 issues tcgen05 MMAs, warps 10-11 only hand their
+//     registers to the softmax warpgroups;
 //   * TMEM (512 columns): S_t / P_t at column 128t (P, bf16 pairs, overwrites
 //     the first half of S after it is read), O_t at 256 + 128t;
 //   * the exponent is base 2 (log2 e folded into the scale); the output
@@ -44,7 +45,12 @@
 namespace splash {
 namespace {
 
-constexpr int kThreads = 384;       // 12 warps
+constexpr int kThreads = 384;       // 12 warps = 3 warpgroups
+// Register split (setmaxnreg): the launch gives 384 x 168; the two softmax
+// warpgroups take 216 each and the producer / MMA warpgroup keeps 72:
+// 2*128*216 + 128*72 = 64512 = 384*168.
+constexpr int kSoftmaxRegs = 192;
+constexpr int kControlRegs = 104;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kTmemCols = 512;
@@ -139,6 +145,280 @@ __device__ __forceinline__ void raise_error(const FwdParams &p, volatile int *ab
   *abort = 1;
 }
 
+// Maximum of BK values with eight independent chains (short dependency path).
+template <int N>
+__device__ __forceinline__ float max_tree(const float (&v)[N]) {
+  float m[8];
+#pragma unroll
+  for (int x = 0; x < 8; ++x) m[x] = v[x];
+#pragma unroll
+  for (int j = 8; j < N; ++j) m[j & 7] = fmaxf(m[j & 7], v[j]);
+  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+}
+
+// tanh for the soft cap, two ways, both from the mathematics of tanh (not
+// from any library implementation):
+//  * |t| <= 0.25: the Maclaurin series t - t^3/3 + 2t^5/15 - 17t^7/315; the
+//    first omitted term, 62 t^9 / 2835, is below 8.4e-8 there;
+//  * otherwise the identity tanh|t| = 1 - 2 / (1 + e^(2|t|)) with the sign
+//    restored (absolute error ~1e-7 from ex2 / division rounding).
+constexpr float kTanhSeriesLimit = 0.25f;
+
+__device__ __forceinline__ float tanh_identity(float t) {
+  const float a = fminf(fabsf(t), 16.f);  // tanh(16) rounds to 1 in fp32
+  const float e = ex2_approx(2.8853900817779268f * a);  // e^(2a)
+  return copysignf(1.f - __fdividef(2.f, e + 1.f), t);
+}
+
+// cap*log2e*tanh(s*k) by the series, with k = scale/cap and kc = cap*log2e*k.
+__device__ __forceinline__ float tanh_series_scaled(float s, float k, float kc) {
+  const float a = s * k;
+  const float t2 = a * a;
+  float poly = fmaf(t2, -17.f / 315.f, 2.f / 15.f);
+  poly = fmaf(poly, t2, -1.f / 3.f);
+  const float q = fmaf(t2, poly, 1.f);
+  return (s * kc) * q;
+}
+
+// Shared-memory addresses of the CTA's mbarriers:
+//   q_full[2] q_empty[2] k_full[NK] k_empty[NK] v_full[NV] v_empty[NV]
+//   s_full[2] p_full[2] o_done[2] drain
+template <class C>
+struct Bars {
+  uint32_t base;
+  __device__ __forceinline__ uint32_t q_full(int t) const { return base + 8u * t; }
+  __device__ __forceinline__ uint32_t q_empty(int t) const { return base + 8u * (2 + t); }
+  __device__ __forceinline__ uint32_t k_full(int s) const { return base + 8u * (4 + s); }
+  __device__ __forceinline__ uint32_t k_empty(int s) const { return base + 8u * (4 + C::NK + s); }
+  __device__ __forceinline__ uint32_t v_full(int s) const { return base + 8u * (4 + 2 * C::NK + s); }
+  __device__ __forceinline__ uint32_t v_empty(int s) const { return base + 8u * (4 + 2 * C::NK + C::NV + s); }
+  __device__ __forceinline__ uint32_t s_full(int t) const { return base + 8u * (4 + 2 * C::NK + 2 * C::NV + t); }
+  __device__ __forceinline__ uint32_t p_full(int t) const { return base + 8u * (6 + 2 * C::NK + 2 * C::NV + t); }
+  __device__ __forceinline__ uint32_t o_done(int t) const { return base + 8u * (8 + 2 * C::NK + 2 * C::NV + t); }
+  __device__ __forceinline__ uint32_t drain() const { return base + 8u * (10 + 2 * C::NK + 2 * C::NV); }
+};
+
+// Loads one K or V tile (CH boxes of 64 columns x BK rows) into the next slot
+// of a ring of NS slots of BYTES bytes; waits (bounded) for the slot to be
+// released by the MMAs that read its previous contents.
+template <int NS, int BYTES, int CH, int CHUNK>
+__device__ __forceinline__ bool produce_tile(const FwdParams &p, const CUtensorMap *tm, uint32_t ring,
+                                             uint32_t full0, uint32_t empty0, uint32_t &cnt, int32_t y,
+                                             volatile int *abort) {
+  const uint32_t s = cnt % NS;
+  if (cnt >= (uint32_t)NS && !mbar_wait(empty0 + 8u * s, ((cnt / NS) - 1u) & 1u, abort, p.timeout_ns))
+    return false;
+  mbar_arrive_expect_tx(full0 + 8u * s, BYTES);
+#pragma unroll
+  for (int ch = 0; ch < CH; ++ch) tma_load_2d(ring + s * BYTES + ch * CHUNK, tm, ch * 64, y, full0 + 8u * s);
+  ++cnt;
+  return true;
+}
+
+__device__ __forceinline__ int32_t checked_col(const FwdParams &p, int32_t g) {
+  int32_t c = p.active_cols[g];
+  if (c < 0 || c >= p.nk) {
+    atomicOr(p.err, SPLASH_DEV_BAD_TABLE);
+    c = 0;
+  }
+  return c;
+}
+
+// The TMA producer (one thread): per work item the two Q tiles, then K and V
+// tiles in exactly the order the MMA issuer consumes them:
+//   K0(0) [K1(0)], then per block g: V0(g) K0(g+1) [V1(g) K1(g+1)]
+// (the bracketed loads only when the two query heads use different KV heads).
+template <class C, int BK>
+__device__ __noinline__ void run_producer(const FwdParams &p, const CUtensorMap *tmQ, const CUtensorMap *tmK,
+                                          const CUtensorMap *tmV, uint32_t sQ, uint32_t sK, uint32_t sV,
+                                          const Bars<C> bar, volatile int *abort) {
+  uint32_t kcnt = 0, vcnt = 0, q0 = 0, q1 = 0;
+  bool ok = true;
+  for (int64_t w = blockIdx.x; w < p.num_items && ok; w += gridDim.x) {
+    const Item it = decode_item(p, w);
+    if (it.nb <= 0) continue;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if (t == 1 && !it.act1) break;
+      uint32_t &qc = t ? q1 : q0;
+      if (qc > 0 && !mbar_wait(bar.q_empty(t), (qc - 1) & 1, abort, p.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(bar.q_full(t), C::Q_BYTES);
+      const int32_t y = (int32_t)(((int64_t)it.b * p.Hq + (t ? it.h1 : it.h0)) * p.Lq + (int64_t)it.qrow * p.bq);
+#pragma unroll
+      for (int ch = 0; ch < C::QCH; ++ch)
+        tma_load_2d(sQ + t * C::Q_BYTES + ch * C::Q_CHUNK, tmQ, ch * 64, y, bar.q_full(t));
+      ++qc;
+    }
+    if (!ok) break;
+    const bool two_kv = it.act1 && !it.shared;
+    const int64_t kv0 = ((int64_t)it.b * p.Hkv + it.kvh0) * p.Lk;
+    const int64_t kv1 = ((int64_t)it.b * p.Hkv + it.kvh1) * p.Lk;
+    int32_t c = checked_col(p, it.g0);
+    ok = produce_tile<C::NK, C::K_BYTES, C::QCH, C::KV_CHUNK>(p, tmK, sK, bar.k_full(0), bar.k_empty(0), kcnt,
+                                                              (int32_t)(kv0 + (int64_t)c * BK), abort);
+    if (ok && two_kv)
+      ok = produce_tile<C::NK, C::K_BYTES, C::QCH, C::KV_CHUNK>(p, tmK, sK, bar.k_full(0), bar.k_empty(0), kcnt,
+                                                                (int32_t)(kv1 + (int64_t)c * BK), abort);
+    for (int32_t g = 0; g < it.nb && ok; ++g) {
+      const bool more = g + 1 < it.nb;
+      const int32_t cn = more ? checked_col(p, it.g0 + g + 1) : 0;
+      ok = produce_tile<C::NV, C::V_BYTES, C::VCH, C::KV_CHUNK>(p, tmV, sV, bar.v_full(0), bar.v_empty(0), vcnt,
+                                                                (int32_t)(kv0 + (int64_t)c * BK), abort);
+      if (ok && more)
+        ok = produce_tile<C::NK, C::K_BYTES, C::QCH, C::KV_CHUNK>(p, tmK, sK, bar.k_full(0), bar.k_empty(0), kcnt,
+                                                                  (int32_t)(kv0 + (int64_t)cn * BK), abort);
+      if (ok && two_kv)
+        ok = produce_tile<C::NV, C::V_BYTES, C::VCH, C::KV_CHUNK>(p, tmV, sV, bar.v_full(0), bar.v_empty(0),
+                                                                  vcnt, (int32_t)(kv1 + (int64_t)c * BK), abort);
+      if (ok && two_kv && more)
+        ok = produce_tile<C::NK, C::K_BYTES, C::QCH, C::KV_CHUNK>(p, tmK, sK, bar.k_full(0), bar.k_empty(0),
+                                                                  kcnt, (int32_t)(kv1 + (int64_t)cn * BK), abort);
+      c = cn;
+    }
+  }
+  if (!ok) raise_error(p, abort, SPLASH_DEV_TIMEOUT_PRODUCER);
+  // drain: the last load issued into every slot has landed
+  bool drained = true;
+  for (int s = 0; s < C::NK; ++s)
+    if (kcnt > (uint32_t)s) drained &= mbar_wait_drain(bar.k_full(s), ((kcnt - 1 - s) / C::NK) & 1, p.timeout_ns);
+  for (int s = 0; s < C::NV; ++s)
+    if (vcnt > (uint32_t)s) drained &= mbar_wait_drain(bar.v_full(s), ((vcnt - 1 - s) / C::NV) & 1, p.timeout_ns);
+  if (q0 > 0) drained &= mbar_wait_drain(bar.q_full(0), (q0 - 1) & 1, p.timeout_ns);
+  if (q1 > 0) drained &= mbar_wait_drain(bar.q_full(1), (q1 - 1) & 1, p.timeout_ns);
+  if (!drained) atomicOr(p.err, SPLASH_DEV_TIMEOUT_DRAIN);
+}
+
+// S_t = Q_t K^T: QCH chunks x 4 MMAs of K = 16 (K-major A and B, 128B swizzle;
+// the k-step advances the start address by 32 bytes inside the swizzle atom).
+template <class C>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr) {
+  const uint64_t qd = sdesc_sw128(q_addr, 16, 1024), kd = sdesc_sw128(k_addr, 16, 1024);
+#pragma unroll
+  for (int ch = 0; ch < C::QCH; ++ch)
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_ss(d_tmem, qd + (uint64_t)((ch * C::Q_CHUNK + kk * 32) >> 4),
+             kd + (uint64_t)((ch * C::KV_CHUNK + kk * 32) >> 4), C::IDESC_QK, (ch | kk) != 0);
+}
+
+// O_t (+)= P_t V: P read from TMEM (bf16 pairs, 8 columns per K = 16 step),
+// V MN-major with 128B swizzle (K step = 16 rows = 2048 bytes; the 64-column
+// chunks of V are KV_CHUNK bytes apart).
+template <class C, int BK>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr, bool first_block) {
+  const uint64_t vd = sdesc_sw128(v_addr, C::KV_CHUNK, 1024);
+#pragma unroll
+  for (int j = 0; j < BK / 16; ++j)
+    mma_ts(d_tmem, p_tmem + 8u * j, vd + (uint64_t)((j * 2048) >> 4), C::IDESC_PV,
+           (!first_block || j > 0) ? 1u : 0u);
+}
+
+__device__ __forceinline__ bool wait_ring(uint32_t full0, uint32_t cnt, int ns, volatile int *abort,
+                                          uint64_t timeout_ns, uint32_t &slot) {
+  slot = cnt % (uint32_t)ns;
+  if (!mbar_wait(full0 + 8u * slot, (cnt / (uint32_t)ns) & 1u, abort, timeout_ns)) return false;
+  tc_fence_after();
+  return true;
+}
+
+// The MMA issuer (one thread).  Per item: S_0(0), S_1(0); then per block g:
+//   wait P_0(g): O_0 += P_0 V(g); S_0(g+1) = Q_0 K(g+1)^T;
+//   wait P_1(g): O_1 += P_1 V(g); S_1(g+1) = Q_1 K(g+1)^T.
+// Commits: s_full after each S, o_done after the last PV, slot releases
+// after the last MMA that reads a slot, q_empty after a tile's last S.
+template <class C, int BK>
+__device__ __noinline__ void run_mma(const FwdParams &p, uint32_t tmem, uint32_t sQ, uint32_t sK, uint32_t sV,
+                                     const Bars<C> bar, volatile int *abort) {
+  uint32_t kcnt = 0, vcnt = 0, q0 = 0, q1 = 0, p0 = 0, p1 = 0;
+  bool ok = true;
+  const uint32_t tS0 = tmem, tS1 = tmem + 128u, tO0 = tmem + 256u, tO1 = tmem + 384u;
+  for (int64_t w = blockIdx.x; w < p.num_items && ok; w += gridDim.x) {
+    const Item it = decode_item(p, w);
+    if (it.nb <= 0) continue;
+    const bool two = it.act1;
+    const bool two_kv = it.act1 && !it.shared;
+    if (!(ok = mbar_wait(bar.q_full(0), q0 & 1, abort, p.timeout_ns))) break;
+    ++q0;
+    if (two) {
+      if (!(ok = mbar_wait(bar.q_full(1), q1 & 1, abort, p.timeout_ns))) break;
+      ++q1;
+    }
+    tc_fence_after();
+    uint32_t ks;
+    if (!(ok = wait_ring(bar.k_full(0), kcnt, C::NK, abort, p.timeout_ns, ks))) break;
+    issue_qk<C>(tS0, sQ, sK + ks * C::K_BYTES);
+    tc_commit(bar.s_full(0));
+    if (two_kv) {
+      tc_commit(bar.k_empty(ks));
+      ++kcnt;
+      if (!(ok = wait_ring(bar.k_full(0), kcnt, C::NK, abort, p.timeout_ns, ks))) break;
+    }
+    if (two) {
+      issue_qk<C>(tS1, sQ + C::Q_BYTES, sK + ks * C::K_BYTES);
+      tc_commit(bar.s_full(1));
+    }
+    tc_commit(bar.k_empty(ks));
+    ++kcnt;
+    if (it.nb == 1) {
+      tc_commit(bar.q_empty(0));
+      if (two) tc_commit(bar.q_empty(1));
+    }
+    for (int32_t g = 0; g < it.nb && ok; ++g) {
+      const bool more = g + 1 < it.nb;
+      // ---- tile 0
+      if (!(ok = mbar_wait(bar.p_full(0), p0 & 1, abort, p.timeout_ns))) break;
+      ++p0;
+      tc_fence_after();
+      uint32_t vs0;
+      if (!(ok = wait_ring(bar.v_full(0), vcnt, C::NV, abort, p.timeout_ns, vs0))) break;
+      issue_pv<C, BK>(tO0, tS0, sV + vs0 * C::V_BYTES, g == 0);
+      if (!more) tc_commit(bar.o_done(0));
+      if (!two || two_kv) {
+        tc_commit(bar.v_empty(vs0));
+        ++vcnt;
+      }
+      uint32_t ks0 = 0;
+      if (more) {
+        if (!(ok = wait_ring(bar.k_full(0), kcnt, C::NK, abort, p.timeout_ns, ks0))) break;
+        issue_qk<C>(tS0, sQ, sK + ks0 * C::K_BYTES);
+        tc_commit(bar.s_full(0));
+        if (!two || two_kv) {
+          tc_commit(bar.k_empty(ks0));
+          ++kcnt;
+        }
+        if (g + 2 == it.nb) tc_commit(bar.q_empty(0));
+      }
+      if (!two) continue;
+      // ---- tile 1
+      if (!(ok = mbar_wait(bar.p_full(1), p1 & 1, abort, p.timeout_ns))) break;
+      ++p1;
+      tc_fence_after();
+      uint32_t vs1 = vs0;
+      if (two_kv && !(ok = wait_ring(bar.v_full(0), vcnt, C::NV, abort, p.timeout_ns, vs1))) break;
+      issue_pv<C, BK>(tO1, tS1, sV + vs1 * C::V_BYTES, g == 0);
+      if (!more) tc_commit(bar.o_done(1));
+      tc_commit(bar.v_empty(vs1));
+      ++vcnt;
+      if (more) {
+        uint32_t ks1 = ks0;
+        if (two_kv && !(ok = wait_ring(bar.k_full(0), kcnt, C::NK, abort, p.timeout_ns, ks1))) break;
+        issue_qk<C>(tS1, sQ + C::Q_BYTES, sK + ks1 * C::K_BYTES);
+        tc_commit(bar.s_full(1));
+        tc_commit(bar.k_empty(ks1));
+        ++kcnt;
+        if (g + 2 == it.nb) tc_commit(bar.q_empty(1));
+      }
+    }
+  }
+  if (!ok) raise_error(p, abort, SPLASH_DEV_TIMEOUT_MMA);
+  // drain: every MMA issued by this thread has completed
+  tc_commit(bar.drain());
+  if (!mbar_wait_drain(bar.drain(), 0, p.timeout_ns)) atomicOr(p.err, SPLASH_DEV_TIMEOUT_DRAIN);
+}
+
 template <int DQK, int DV, int BK>
 __global__ void __launch_bounds__(kThreads, 1)
 splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -151,17 +431,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   const uint32_t sK = sQ + 2 * C::Q_BYTES;
   const uint32_t sV = sK + C::NK * C::K_BYTES;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::TILES);
-  const uint32_t b0 = smem_u32(bars);
-  auto q_full = [&](int t) { return b0 + 8u * t; };
-  auto q_empty = [&](int t) { return b0 + 8u * (2 + t); };
-  auto k_full = [&](int s) { return b0 + 8u * (4 + s); };
-  auto k_empty = [&](int s) { return b0 + 8u * (4 + C::NK + s); };
-  auto v_full = [&](int s) { return b0 + 8u * (4 + 2 * C::NK + s); };
-  auto v_empty = [&](int s) { return b0 + 8u * (4 + 2 * C::NK + C::NV + s); };
-  auto s_full = [&](int t) { return b0 + 8u * (4 + 2 * C::NK + 2 * C::NV + t); };
-  auto p_full = [&](int t) { return b0 + 8u * (6 + 2 * C::NK + 2 * C::NV + t); };
-  auto o_done = [&](int t) { return b0 + 8u * (8 + 2 * C::NK + 2 * C::NV + t); };
-  const uint32_t drain_bar = b0 + 8u * (10 + 2 * C::NK + 2 * C::NV);
+  const Bars<C> bar{smem_u32(bars)};
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::TILES + C::NBAR * 8);
   volatile int *abort = reinterpret_cast<volatile int *>(smem + C::TILES + C::NBAR * 8 + 4);
 
@@ -174,21 +444,21 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   }
   if (threadIdx.x == 32) {
     for (int t = 0; t < 2; ++t) {
-      mbar_init(q_full(t), 1);
-      mbar_init(q_empty(t), 1);
-      mbar_init(s_full(t), 1);
-      mbar_init(p_full(t), 128);
-      mbar_init(o_done(t), 1);
+      mbar_init(bar.q_full(t), 1);
+      mbar_init(bar.q_empty(t), 1);
+      mbar_init(bar.s_full(t), 1);
+      mbar_init(bar.p_full(t), 128);
+      mbar_init(bar.o_done(t), 1);
     }
     for (int s = 0; s < C::NK; ++s) {
-      mbar_init(k_full(s), 1);
-      mbar_init(k_empty(s), 1);
+      mbar_init(bar.k_full(s), 1);
+      mbar_init(bar.k_empty(s), 1);
     }
     for (int s = 0; s < C::NV; ++s) {
-      mbar_init(v_full(s), 1);
-      mbar_init(v_empty(s), 1);
+      mbar_init(bar.v_full(s), 1);
+      mbar_init(bar.v_empty(s), 1);
     }
-    mbar_init(drain_bar, 1);
+    mbar_init(bar.drain(), 1);
     *abort = 0;
     mbar_fence_init();
   }
@@ -202,211 +472,18 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
+  if (warp >= 8) {
+  // ============================================================ warpgroup 2
+  regs_decrease<kControlRegs>();
   if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t kcnt = 0, vcnt = 0, qcnt[2] = {0, 0};
-      bool ok = true;
-      auto load_k = [&](int32_t b, int32_t kvh, int32_t col) -> bool {
-        const int s = kcnt % C::NK;
-        if (kcnt >= (uint32_t)C::NK && !mbar_wait(k_empty(s), ((kcnt / C::NK) - 1) & 1, abort, p.timeout_ns))
-          return false;
-        mbar_arrive_expect_tx(k_full(s), C::K_BYTES);
-        const int32_t y = (int32_t)(((int64_t)b * p.Hkv + kvh) * p.Lk + (int64_t)col * BK);
-        for (int ch = 0; ch < C::QCH; ++ch)
-          tma_load_2d(sK + s * C::K_BYTES + ch * C::KV_CHUNK, &tmK, ch * 64, y, k_full(s));
-        ++kcnt;
-        return true;
-      };
-      auto load_v = [&](int32_t b, int32_t kvh, int32_t col) -> bool {
-        const int s = vcnt % C::NV;
-        if (vcnt >= (uint32_t)C::NV && !mbar_wait(v_empty(s), ((vcnt / C::NV) - 1) & 1, abort, p.timeout_ns))
-          return false;
-        mbar_arrive_expect_tx(v_full(s), C::V_BYTES);
-        const int32_t y = (int32_t)(((int64_t)b * p.Hkv + kvh) * p.Lk + (int64_t)col * BK);
-        for (int ch = 0; ch < C::VCH; ++ch)
-          tma_load_2d(sV + s * C::V_BYTES + ch * C::KV_CHUNK, &tmV, ch * 64, y, v_full(s));
-        ++vcnt;
-        return true;
-      };
-      auto col_of = [&](const Item &it, int32_t g) -> int32_t {
-        int32_t c = p.active_cols[it.g0 + g];
-        if (c < 0 || c >= p.nk) {
-          atomicOr(p.err, SPLASH_DEV_BAD_TABLE);
-          c = 0;
-        }
-        return c;
-      };
-      for (int64_t w = blockIdx.x; w < p.num_items && ok; w += gridDim.x) {
-        const Item it = decode_item(p, w);
-        if (it.nb <= 0) continue;
-        for (int t = 0; t < (it.act1 ? 2 : 1) && ok; ++t) {
-          if (qcnt[t] > 0 && !mbar_wait(q_empty(t), (qcnt[t] - 1) & 1, abort, p.timeout_ns)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(q_full(t), C::Q_BYTES);
-          const int32_t h = t ? it.h1 : it.h0;
-          const int32_t y = (int32_t)(((int64_t)it.b * p.Hq + h) * p.Lq + (int64_t)it.qrow * p.bq);
-          for (int ch = 0; ch < C::QCH; ++ch)
-            tma_load_2d(sQ + t * C::Q_BYTES + ch * C::Q_CHUNK, &tmQ, ch * 64, y, q_full(t));
-          ++qcnt[t];
-        }
-        if (!ok) break;
-        const bool two_kv = it.act1 && !it.shared;
-        int32_t c = col_of(it, 0);
-        ok = load_k(it.b, it.kvh0, c) && (!two_kv || load_k(it.b, it.kvh1, c));
-        for (int32_t g = 0; g < it.nb && ok; ++g) {
-          const int32_t cn = (g + 1 < it.nb) ? col_of(it, g + 1) : 0;
-          ok = load_v(it.b, it.kvh0, c);
-          if (ok && g + 1 < it.nb) ok = load_k(it.b, it.kvh0, cn);
-          if (ok && two_kv) ok = load_v(it.b, it.kvh1, c);
-          if (ok && two_kv && g + 1 < it.nb) ok = load_k(it.b, it.kvh1, cn);
-          c = cn;
-        }
-      }
-      if (!ok) raise_error(p, abort, SPLASH_DEV_TIMEOUT_PRODUCER);
-      // drain: the last load issued into every slot has landed
-      bool drained = true;
-      for (int s = 0; s < C::NK; ++s)
-        if (kcnt > (uint32_t)s) {
-          const uint32_t last = (kcnt - 1 - s) / C::NK;  // uses of slot s minus one
-          drained &= mbar_wait_drain(k_full(s), last & 1, p.timeout_ns);
-        }
-      for (int s = 0; s < C::NV; ++s)
-        if (vcnt > (uint32_t)s) {
-          const uint32_t last = (vcnt - 1 - s) / C::NV;
-          drained &= mbar_wait_drain(v_full(s), last & 1, p.timeout_ns);
-        }
-      for (int t = 0; t < 2; ++t)
-        if (qcnt[t] > 0) drained &= mbar_wait_drain(q_full(t), (qcnt[t] - 1) & 1, p.timeout_ns);
-      if (!drained) atomicOr(p.err, SPLASH_DEV_TIMEOUT_DRAIN);
-    }
+    if (lane == 0) run_producer<C, BK>(p, &tmQ, &tmK, &tmV, sQ, sK, sV, bar, abort);
   } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      uint32_t kcnt = 0, vcnt = 0, qcnt[2] = {0, 0}, pcnt[2] = {0, 0};
-      bool ok = true;
-      const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
-      const uint32_t tO[2] = {tmem + 256u, tmem + 384u};
-      auto issue_qk = [&](int t, int ks) {
-        const uint32_t qa = sQ + t * C::Q_BYTES, kb = sK + ks * C::K_BYTES;
-#pragma unroll
-        for (int ch = 0; ch < C::QCH; ++ch)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = sdesc_sw128(qa + ch * C::Q_CHUNK + kk * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(kb + ch * C::KV_CHUNK + kk * 32, 16, 1024);
-            mma_ss(tS[t], ad, bd, C::IDESC_QK, (ch | kk) != 0);
-          }
-      };
-      auto issue_pv = [&](int t, int vs, bool first_block) {
-        const uint32_t vb = sV + vs * C::V_BYTES;
-#pragma unroll
-        for (int j = 0; j < BK / 16; ++j) {
-          const uint64_t bd = sdesc_sw128(vb + j * 2048, C::KV_CHUNK, 1024);
-          mma_ts(tO[t], tS[t] + j * 8, bd, C::IDESC_PV, (!first_block || j > 0) ? 1u : 0u);
-        }
-      };
-      auto wait_k = [&](int &slot) -> bool {
-        slot = kcnt % C::NK;
-        if (!mbar_wait(k_full(slot), (kcnt / C::NK) & 1, abort, p.timeout_ns)) return false;
-        tc_fence_after();
-        return true;
-      };
-      auto wait_v = [&](int &slot) -> bool {
-        slot = vcnt % C::NV;
-        if (!mbar_wait(v_full(slot), (vcnt / C::NV) & 1, abort, p.timeout_ns)) return false;
-        tc_fence_after();
-        return true;
-      };
-      for (int64_t w = blockIdx.x; w < p.num_items && ok; w += gridDim.x) {
-        const Item it = decode_item(p, w);
-        if (it.nb <= 0) continue;
-        const int nt = it.act1 ? 2 : 1;
-        const bool two_kv = it.act1 && !it.shared;
-        for (int t = 0; t < nt && ok; ++t) {
-          ok = mbar_wait(q_full(t), qcnt[t] & 1, abort, p.timeout_ns);
-          ++qcnt[t];
-        }
-        if (!ok) break;
-        tc_fence_after();
-        // S_t(0) = Q_t K(0)^T
-        int ks = 0;
-        if (!(ok = wait_k(ks))) break;
-        issue_qk(0, ks);
-        tc_commit(s_full(0));
-        if (!two_kv) {
-          if (nt == 2) {
-            issue_qk(1, ks);
-            tc_commit(s_full(1));
-          }
-          tc_commit(k_empty(ks));
-          ++kcnt;
-        } else {
-          tc_commit(k_empty(ks));
-          ++kcnt;
-          if (!(ok = wait_k(ks))) break;
-          issue_qk(1, ks);
-          tc_commit(s_full(1));
-          tc_commit(k_empty(ks));
-          ++kcnt;
-        }
-        if (it.nb == 1)
-          for (int t = 0; t < nt; ++t) tc_commit(q_empty(t));
-        for (int32_t g = 0; g < it.nb && ok; ++g) {
-          const bool more = g + 1 < it.nb;
-          // ---- tile 0
-          if (!(ok = mbar_wait(p_full(0), pcnt[0] & 1, abort, p.timeout_ns))) break;
-          ++pcnt[0];
-          tc_fence_after();
-          int vs0 = 0;
-          if (!(ok = wait_v(vs0))) break;
-          issue_pv(0, vs0, g == 0);
-          if (!more) tc_commit(o_done(0));
-          if (nt == 1 || two_kv) {
-            tc_commit(v_empty(vs0));
-            ++vcnt;
-          }
-          int ks0 = 0;
-          if (more) {
-            if (!(ok = wait_k(ks0))) break;
-            issue_qk(0, ks0);
-            tc_commit(s_full(0));
-            if (nt == 1 || two_kv) {
-              tc_commit(k_empty(ks0));
-              ++kcnt;
-            }
-            if (g + 2 == it.nb) tc_commit(q_empty(0));
-          }
-          if (nt == 1) continue;
-          // ---- tile 1
-          if (!(ok = mbar_wait(p_full(1), pcnt[1] & 1, abort, p.timeout_ns))) break;
-          ++pcnt[1];
-          tc_fence_after();
-          int vs1 = vs0;
-          if (two_kv && !(ok = wait_v(vs1))) break;
-          issue_pv(1, vs1, g == 0);
-          if (!more) tc_commit(o_done(1));
-          tc_commit(v_empty(vs1));
-          ++vcnt;
-          if (more) {
-            int ks1 = ks0;
-            if (two_kv && !(ok = wait_k(ks1))) break;
-            issue_qk(1, ks1);
-            tc_commit(s_full(1));
-            tc_commit(k_empty(ks1));
-            ++kcnt;
-            if (g + 2 == it.nb) tc_commit(q_empty(1));
-          }
-        }
-      }
-      if (!ok) raise_error(p, abort, SPLASH_DEV_TIMEOUT_MMA);
-      // drain: every MMA issued by this thread has completed
-      tc_commit(drain_bar);
-      if (!mbar_wait_drain(drain_bar, 0, p.timeout_ns)) atomicOr(p.err, SPLASH_DEV_TIMEOUT_DRAIN);
-    }
-  } else if (warp < 8) {
+    if (lane == 0) run_mma<C, BK>(p, tmem, sQ, sK, sV, bar, abort);
+  }
+  } else {
+  // ============================================================ warpgroups 0, 1
+  regs_increase<kSoftmaxRegs>();
+  {
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;          // query tile
     const int wq = warp & 3;          // TMEM lane quarter
@@ -430,8 +507,10 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
           atomicOr(p.err, SPLASH_DEV_BAD_TABLE);
           mn = -1;
         }
+        const bool partial = mn >= 0;
+        const bool need_mask = partial || !row_valid;
         uint32_t bits[BK / 32];
-        if (mn >= 0 && row_valid) {
+        if (partial && row_valid) {
           const uint32_t *src = p.pattern_bits + ((int64_t)mn * p.bq + row) * (BK / 32);
 #pragma unroll
           for (int x = 0; x < BK / 32; ++x) bits[x] = __ldg(src + x);
@@ -441,30 +520,54 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         }
         // all lanes wait; the outcome is made warp-uniform before the
         // warp-collective TMEM accesses
-        ok = __all_sync(0xffffffffu, mbar_wait(s_full(t), scnt & 1, abort, p.timeout_ns));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar.s_full(t), scnt & 1, abort, p.timeout_ns));
         if (!ok) break;
         ++scnt;
         tc_fence_after();
         float s[BK];
         {
-          uint32_t r[32];
+          uint32_t r[BK / 32][32];
+#pragma unroll
+          for (int c = 0; c < BK / 32; ++c) tmem_ld32(tS + 32u * c, r[c]);
+          tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < BK / 32; ++c) {
-            tmem_ld32(tS + 32u * c, r);
-            tmem_wait_ld();
-            reg_fence32(r);
+            reg_fence32(r[c]);
 #pragma unroll
-            for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(r[x]);
+            for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(r[c][x]);
           }
         }
-        // scores in log2 units, soft cap, element mask
-        float mx = -INFINITY;
+        // s_j in log2 units: s*scale*log2e (folded into the exponent's FFMA
+        // below) or, with the soft cap, cap*log2e*tanh(s*scale/cap) computed
+        // here.  Masked entries become -inf.
+        float mx;
+        if (!p.use_softcap) {
+          if (need_mask) {
 #pragma unroll
-        for (int j = 0; j < BK; ++j) {
-          float x = p.use_softcap ? p.cap_log2 * tanhf(s[j] * p.cap_inner) : s[j] * p.scale_log2;
-          x = ((bits[j >> 5] >> (j & 31)) & 1u) ? x : -INFINITY;
-          s[j] = x;
-          mx = fmaxf(mx, x);
+            for (int j = 0; j < BK; ++j) s[j] = ((bits[j >> 5] >> (j & 31)) & 1u) ? s[j] : -INFINITY;
+          }
+          mx = max_tree<BK>(s) * p.scale_log2;  // scale > 0
+        } else {
+          float am[8];
+#pragma unroll
+          for (int x = 0; x < 8; ++x) am[x] = fabsf(s[x]);
+#pragma unroll
+          for (int j = 8; j < BK; ++j) am[j & 7] = fmaxf(am[j & 7], fabsf(s[j]));
+          const float amax = fmaxf(fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3])),
+                                   fmaxf(fmaxf(am[4], am[5]), fmaxf(am[6], am[7]))) * p.cap_inner;
+          if (__any_sync(0xffffffffu, amax > kTanhSeriesLimit)) {
+#pragma unroll
+            for (int j = 0; j < BK; ++j) s[j] = p.cap_log2 * tanh_identity(s[j] * p.cap_inner);
+          } else {
+            const float kc = p.cap_log2 * p.cap_inner;
+#pragma unroll
+            for (int j = 0; j < BK; ++j) s[j] = tanh_series_scaled(s[j], p.cap_inner, kc);
+          }
+          if (need_mask) {
+#pragma unroll
+            for (int j = 0; j < BK; ++j) s[j] = ((bits[j >> 5] >> (j & 31)) & 1u) ? s[j] : -INFINITY;
+          }
+          mx = max_tree<BK>(s);
         }
         const float m_new = fmaxf(m_ref, mx);
         float alpha = 1.f;
@@ -473,15 +576,26 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
           m_ref = m_new;
         }
         const float sub = (m_ref == -INFINITY) ? 0.f : m_ref;
-        float sum = 0.f;
-        uint32_t pk[BK / 2];
+        const float mul = p.use_softcap ? 1.f : p.scale_log2;
+        // P = 2^(s - m_ref) as bf16 pairs into the first BK/2 columns of S_t
+        // (S is already in registers), 32 columns per store
+        float sum8[8];
 #pragma unroll
-        for (int j = 0; j < BK; j += 2) {
-          const float p0 = ex2_approx(s[j] - sub);
-          const float p1 = ex2_approx(s[j + 1] - sub);
-          sum += p0 + p1;
-          pk[j >> 1] = pack_bf16x2(p0, p1);
+        for (int x = 0; x < 8; ++x) sum8[x] = 0.f;
+#pragma unroll
+        for (int c = 0; c < BK / 64; ++c) {
+          uint32_t r[32];
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            const int j = c * 64 + 2 * x;
+            const float p0 = ex2_approx(fmaf(s[j], mul, -sub));
+            const float p1 = ex2_approx(fmaf(s[j + 1], mul, -sub));
+            sum8[x & 7] += p0 + p1;
+            r[x] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(tS + 32u * c, r);
         }
+        const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
         l = l * alpha + sum;
         // rescale the output accumulator (its previous PV has completed:
         // S_t(g) was committed after it)
@@ -497,22 +611,14 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             tmem_st32(tO + 32u * c, r);
           }
         }
-        // P (bf16 pairs) into the first BK/2 columns of S_t
-#pragma unroll
-        for (int c = 0; c < BK / 64; ++c) {
-          uint32_t r[32];
-#pragma unroll
-          for (int x = 0; x < 32; ++x) r[x] = pk[c * 32 + x];
-          tmem_st32(tS + 32u * c, r);
-        }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(p_full(t));
+        mbar_arrive(bar.p_full(t));
       }
       if (!ok) break;
       // ---- epilogue: O / l and the LSE
       if (it.nb > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(o_done(t), ocnt & 1, abort, p.timeout_ns));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar.o_done(t), ocnt & 1, abort, p.timeout_ns));
         if (!ok) break;
         ++ocnt;
         tc_fence_after();
@@ -543,6 +649,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       if (row_valid) p.lse[orow] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
     }
     if (!ok) raise_error(p, abort, SPLASH_DEV_TIMEOUT_SOFTMAX);
+  }
   }
 
   tc_fence_before();

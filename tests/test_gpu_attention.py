@@ -62,6 +62,8 @@ SMALL = [
     ("bidirectional window", 1, 2, 2, 640, 640, 128, 128, 128, dict(causal=False, wl=70, wr=130)),
     ("softcap 30 large logits", 1, 4, 2, 512, 512, 128, 128, 128, dict(softcap=30.0, q_gain=6.0)),
     ("softcap + window", 1, 2, 1, 768, 768, 128, 128, 128, dict(softcap=20.0, wl=255, q_gain=3.0)),
+    ("softcap small logits (series path)", 2, 4, 2, 512, 512, 128, 128, 128, dict(softcap=50.0)),
+    ("softcap mixed rows", 1, 2, 2, 512, 512, 64, 64, 64, dict(softcap=8.0, q_gain=1.5)),
     ("Lq < Lk causal", 1, 2, 2, 256, 512, 128, 128, 128, {}),
     ("long row many blocks", 1, 2, 2, 2048, 2048, 128, 128, 128, dict(q_gain=2.0)),
 ]
