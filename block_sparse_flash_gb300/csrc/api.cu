@@ -202,6 +202,16 @@ splash_status splash_attention_fwd(const void *q, const void *k, const void *v, 
                                      static_cast<cudaStream_t>(cuda_stream), err);
 }
 
+splash_status splash_classify_blocks_noalloc(const splash_mask_spec *spec, int64_t Lq, int64_t Lk, int32_t bq,
+                                             int32_t bk, int8_t *block_mask, int64_t *totals, void *cuda_stream) {
+  if (block_mask == nullptr || totals == nullptr) return SPLASH_ERR_INVALID_ARG;
+  splash_status st = check_spec(spec, Lq, Lk);
+  if (st != SPLASH_OK) return st;
+  if ((st = check_geometry(Lq, Lk, bq, bk)) != SPLASH_OK) return st;
+  return splash_classify_blocks_noalloc_impl(spec, Lq, Lk, bq, bk, block_mask, totals,
+                                             static_cast<cudaStream_t>(cuda_stream));
+}
+
 splash_status splash_last_device_error(void *cuda_stream) {
   int dev = 0;
   SPLASH_CUDA_TRY(cudaGetDevice(&dev));

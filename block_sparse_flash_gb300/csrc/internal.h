@@ -71,6 +71,9 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
                                           int64_t Lq, int64_t Lk, int32_t bq, int32_t bk,
                                           cudaStream_t stream);
 void splash_mask_info_free_buffers(splash_mask_info *mi);
+splash_status splash_classify_blocks_noalloc_impl(const splash_mask_spec *spec, int64_t Lq, int64_t Lk,
+                                                  int32_t bq, int32_t bk, int8_t *block_mask,
+                                                  int64_t *totals, cudaStream_t stream);
 
 // api.cu
 uint32_t *splash_device_error_word(int device);  // device address of the error word (or NULL)

@@ -619,3 +619,139 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
   }
   return SPLASH_OK;
 }
+
+// ---------------------------------------------------------------- no-allocation variant
+// Block classification (the classify step above, with its per-row counters
+// and segment summaries) for callers that must not allocate device memory --
+// for example a serving process whose device memory is owned by its own pool
+// allocator under a fixed budget, where a cudaMalloc behind the pool's back
+// can fail or break its accounting.  The scratch lives in the fixed array
+// below instead: it is part of the module image, so every GPU that loads the
+// library holds it until the process exits.
+//
+// Limits: B_mask * nq <= kNoAllocMaxRows and B_mask * nk <= kNoAllocMaxCols.
+// All calls share the array (it keeps the last call's contents; the counters
+// are cleared at the start of every call), so calls that overlap on the GPU
+// -- on different streams, or from different host threads -- race.
+namespace {
+constexpr int64_t kNoAllocMaxRows = 16384;
+constexpr int64_t kNoAllocMaxCols = 16384;
+struct NoAllocScratch {
+  int32_t row_cnt[kNoAllocMaxRows];
+  int32_t row_pcnt[kNoAllocMaxRows];
+  int32_t qsum[2 * kNoAllocMaxRows];
+  int32_t kvsum[2 * kNoAllocMaxCols];
+  unsigned long long counters[8];
+  unsigned long long totals[4];
+};
+}  // namespace
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[sizeof(NoAllocScratch)];
+
+namespace {
+
+constexpr int kMaxNoAllocDevices = 64;
+NoAllocScratch *g_noalloc_addr[kMaxNoAllocDevices];
+
+// Device address of the scratch array on the current device; resolved once
+// per device (the first call on a device does it).
+splash_status noalloc_scratch(NoAllocScratch **out) {
+  int dev = 0;
+  SPLASH_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxNoAllocDevices) return SPLASH_ERR_UNSUPPORTED;
+  if (g_noalloc_addr[dev] == nullptr) {
+    void *ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return SPLASH_ERR_CUDA;
+    }
+    g_noalloc_addr[dev] = static_cast<NoAllocScratch *>(ptr);
+  }
+  *out = g_noalloc_addr[dev];
+  return SPLASH_OK;
+}
+
+// Sums the per-row counters: totals = {active, partial, allowed pairs, max row}.
+__global__ void __launch_bounds__(256) noalloc_totals_kernel(int64_t R, NoAllocScratch *s) {
+  unsigned long long a = 0, p = 0, mx = 0;
+  for (int64_t x = threadIdx.x; x < R; x += blockDim.x) {
+    a += (unsigned long long)s->row_cnt[x];
+    p += (unsigned long long)s->row_pcnt[x];
+    mx = max(mx, (unsigned long long)s->row_cnt[x]);
+  }
+  for (int off = 16; off; off >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, off);
+    p += __shfl_xor_sync(0xffffffffu, p, off);
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  }
+  __shared__ unsigned long long sa[8], sp[8], sm[8];
+  if ((threadIdx.x & 31) == 0) {
+    sa[threadIdx.x >> 5] = a;
+    sp[threadIdx.x >> 5] = p;
+    sm[threadIdx.x >> 5] = mx;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long ta = 0, tp = 0, tm = 0;
+    for (int w = 0; w < 8; ++w) {
+      ta += sa[w];
+      tp += sp[w];
+      tm = max(tm, sm[w]);
+    }
+    s->totals[0] = ta;
+    s->totals[1] = tp;
+    s->totals[2] = s->counters[3];
+    s->totals[3] = tm;
+  }
+}
+
+}  // namespace
+
+splash_status splash_classify_blocks_noalloc_impl(const splash_mask_spec *spec, int64_t Lq, int64_t Lk,
+                                                  int32_t bq, int32_t bk, int8_t *block_mask,
+                                                  int64_t *totals, cudaStream_t stream) {
+  const bool seg = spec->q_segment_ids != nullptr;
+  const int32_t nbm = seg ? spec->batch : 1;
+  const int64_t nq = Lq / bq, nk = Lk / bk, R = (int64_t)nbm * nq;
+  if (R > kNoAllocMaxRows || (int64_t)nbm * nk > kNoAllocMaxCols) return SPLASH_ERR_UNSUPPORTED;
+  NoAllocScratch *s = nullptr;
+  splash_status st = noalloc_scratch(&s);
+  if (st != SPLASH_OK) return st;
+
+  DevMask m;
+  m.causal = spec->causal;
+  m.wl = spec->window_left;
+  m.wr = spec->window_right;
+  m.qseg = spec->q_segment_ids;
+  m.kvseg = seg ? (spec->kv_segment_ids ? spec->kv_segment_ids : spec->q_segment_ids) : nullptr;
+  m.Lq = Lq;
+  m.Lk = Lk;
+  m.nq = nq;
+  m.nk = nk;
+  m.bq = bq;
+  m.bk = bk;
+  m.nbm = nbm;
+
+  // the counters must start at zero: the array keeps the previous call's values
+  SPLASH_CUDA_TRY(cudaMemsetAsync(s->row_cnt, 0, sizeof(int32_t) * R, stream));
+  SPLASH_CUDA_TRY(cudaMemsetAsync(s->row_pcnt, 0, sizeof(int32_t) * R, stream));
+  SPLASH_CUDA_TRY(cudaMemsetAsync(s->counters, 0, sizeof(s->counters), stream));
+  if (seg) {
+    dim3 grid((unsigned)((nq + nk + 7) / 8), (unsigned)nbm);
+    seg_summary_kernel<<<grid, 256, 0, stream>>>(m, s->qsum, s->kvsum);
+  }
+  {
+    dim3 grid((unsigned)((nk + kClassifyThreads - 1) / kClassifyThreads), (unsigned)nq, (unsigned)nbm);
+    classify_kernel<<<grid, kClassifyThreads, 0, stream>>>(m, s->qsum, s->kvsum, block_mask, s->row_cnt,
+                                                          s->row_pcnt, s->counters);
+  }
+  noalloc_totals_kernel<<<1, 256, 0, stream>>>(R, s);
+  SPLASH_CUDA_TRY(cudaGetLastError());
+  splash_count_launches(seg ? 3 : 2);
+  unsigned long long t[4];
+  SPLASH_CUDA_TRY(cudaMemcpyAsync(t, s->totals, sizeof t, cudaMemcpyDeviceToHost, stream));
+  SPLASH_CUDA_TRY(cudaStreamSynchronize(stream));
+  for (int x = 0; x < 4; ++x) totals[x] = (int64_t)t[x];
+  return SPLASH_OK;
+}

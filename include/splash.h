@@ -195,6 +195,36 @@ splash_status splash_attention_fwd(const void *q, const void *k, const void *v, 
                                    void *cuda_stream);
 
 /*
+ * splash_classify_blocks_noalloc -- the block classification of a mask
+ * (block_mask and its totals), computed without allocating any device memory.
+ * The pages have no counterpart: this exists for callers that must not call
+ * cudaMalloc, such as a process whose device memory is owned by its own pool
+ * allocator under a fixed budget, where an allocation outside the pool can fail
+ * or break the pool's accounting.
+ *
+ * It runs the same classification as splash_build_mask_info, but its working
+ * memory (per-row counters, segment summaries, totals) is a fixed array inside
+ * the library's module, present on every GPU that loads the library until the
+ * process exits.  The first call on a device looks that array up (once per
+ * device), so make the first call on each device before any stream capture.
+ *
+ *   spec, Lq, Lk, bq, bk  as for splash_build_mask_info.
+ *   block_mask  device int8 [B_mask][nq][nk], caller-allocated: 0 empty,
+ *               1 partial, 2 full (identical to the MaskInfo's block_mask).
+ *   totals      host int64 [4]: active blocks, partial blocks, allowed
+ *               (query, key) pairs, and the largest active-block count of a
+ *               q-block row.
+ * Limits: B_mask * nq <= 16384 and B_mask * nk <= 16384; larger masks return
+ * SPLASH_ERR_UNSUPPORTED.  The call waits on `cuda_stream` for the totals.
+ * All calls share the one array (its counters are cleared at the start of each
+ * call), so calls that overlap on the GPU -- other streams or other host
+ * threads -- race and must be serialised by the caller.
+ */
+splash_status splash_classify_blocks_noalloc(const splash_mask_spec *spec, int64_t Lq, int64_t Lk,
+                                             int32_t bq, int32_t bk, int8_t *block_mask,
+                                             int64_t *totals, void *cuda_stream);
+
+/*
  * splash_last_device_error -- synchronises `cuda_stream`, then reads and
  * clears the device error word that the library's kernels set when a bounded
  * wait runs out (SPLASH_ERR_DEVICE_TIMEOUT) or a table entry fails a bounds
