@@ -66,6 +66,23 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def recorded_traffic(workload_index):
+    """DRAM bytes per attention launch from the committed ncu summary, or None
+    when the kernel source has changed since those counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "block_sparse_flash_gb300", "csrc", "attention_fwd.cu")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(f"workload{workload_index}")
+    if not rec:
+        return None
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    return rec.get("bytes_per_launch") if sha == rec.get("kernel_sha256_prefix") else None
+
+
 def reduce_max(value, world, device=None):
     """Max of a float over ranks (identity for one rank)."""
     if world <= 1:
@@ -259,12 +276,7 @@ def run_ours(args):
                 "frac": round(achieved / peak, 4), "traffic": None,
                 "kernel": "splash_fwd_kernel", "peak_source": f"{peak_src} bf16 burst (cuBLAS)",
                 "achieved_is": "executed FLOPs of the active blocks per launch / mean launch time (CUDA events)"}
-    traffic_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(traffic_path):
-        with open(traffic_path) as f:
-            tr = json.load(f).get(f"workload{args.workload}")
-        if tr:
-            roofline["traffic"] = tr.get("bytes_per_launch")
+    roofline["traffic"] = recorded_traffic(args.workload)
 
     e2e = None
     if not args.no_e2e:

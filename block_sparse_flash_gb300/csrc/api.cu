@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -180,7 +181,8 @@ splash_status splash_attention_fwd(const void *q, const void *k, const void *v, 
     return SPLASH_ERR_INVALID_ARG;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lk <= 0 || dqk <= 0 || dv <= 0)
     return SPLASH_ERR_INVALID_ARG;
-  if (!(scale == scale) || !(softcap == softcap)) return SPLASH_ERR_INVALID_ARG;  // NaN
+  if (!(scale > 0.f) || !(scale < INFINITY) || !(softcap == softcap) || softcap == INFINITY)
+    return SPLASH_ERR_INVALID_ARG;  // scale must be positive and finite; NaN / inf cap rejected
   if (Hq % Hkv != 0) return SPLASH_ERR_SHAPE;
   if (mi->nq <= 0 || mi->Lq != Lq || mi->Lk != Lk) return SPLASH_ERR_SHAPE;
   if (mi->batch_rows != 1 && mi->batch_rows != B) return SPLASH_ERR_SHAPE;

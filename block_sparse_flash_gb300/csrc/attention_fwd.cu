@@ -20,11 +20,13 @@
 //   * one persistent CTA per SM; each work item is (batch, two query heads,
 //     one q-block row); the two heads are two 128-row query tiles that share
 //     the row's active list, and share K/V tiles when they are in the same
-//     GQA group;
+//     GQA group; items are sorted longest row first and dealt to the CTAs in
+//     serpentine order;
 //   * warp roles (384 threads): warps 0-3 / 4-7 run the softmax of tile 0 /
 //     tile 1 (one thread per query row = one TMEM lane), warp 8 issues TMA
-//     loads, warp 9 issues tcgen05 MMAs, warps 10-11 only hand their
-//     registers to the softmax warpgroups;
+//     loads; warp 9 issues the tcgen05 MMAs of both tiles when they share
+//     K/V (GQA), or warps 9 / 10 issue those of tile 0 / tile 1 (MHA);
+//     warp 11 only hands its registers to the softmax warpgroups;
 //   * TMEM (512 columns): S_t / P_t at column 128t (P, bf16 pairs, overwrites
 //     the first half of S after it is read), O_t at 256 + 128t;
 //   * the exponent is base 2 (log2 e folded into the scale); the output
@@ -49,8 +51,8 @@ constexpr int kThreads = 384;       // 12 warps = 3 warpgroups
 // Register split (setmaxnreg): the launch gives 384 x 168; the two softmax
 // warpgroups take 216 each and the producer / MMA warpgroup keeps 72:
 // 2*128*216 + 128*72 = 64512 = 384*168.
-constexpr int kSoftmaxRegs = 192;
-constexpr int kControlRegs = 104;
+constexpr int kSoftmaxRegs = 200;
+constexpr int kControlRegs = 96;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kTmemCols = 512;
@@ -97,6 +99,7 @@ struct FwdParams {
   float cap_inner;    // scale / cap                 (soft cap)
   float cap_log2;     // cap * log2(e)               (soft cap)
   int32_t use_softcap;
+  int32_t dual_issuer;  // one MMA issuer per tile (pairs with different KV heads)
   __nv_bfloat16 *out;
   float *lse;
   uint32_t *err;
@@ -140,20 +143,30 @@ __device__ __forceinline__ Item decode_item(const FwdParams &p, int64_t w) {
   return it;
 }
 
+// Serpentine static schedule: round k of the CTA's items visits the CTAs in
+// alternating directions, so that the rows (sorted longest first) spread
+// evenly over the grid.  Returns the item index of round k, or -1 when done.
+__device__ __forceinline__ int64_t item_of_round(const FwdParams &p, int64_t k) {
+  const int64_t G = gridDim.x;
+  const int64_t c = (k & 1) ? (G - 1 - blockIdx.x) : blockIdx.x;
+  const int64_t w = k * G + c;
+  return w < p.num_items ? w : -1;
+}
+
 __device__ __forceinline__ void raise_error(const FwdParams &p, volatile int *abort, uint32_t bits) {
   atomicOr(p.err, bits);
   *abort = 1;
 }
 
-// Maximum of BK values with eight independent chains (short dependency path).
+// Maximum of N values: four independent chains of three-input maxima.
 template <int N>
 __device__ __forceinline__ float max_tree(const float (&v)[N]) {
-  float m[8];
+  float m[4];
 #pragma unroll
-  for (int x = 0; x < 8; ++x) m[x] = v[x];
+  for (int x = 0; x < 4; ++x) m[x] = fmaxf(v[2 * x], v[2 * x + 1]);
 #pragma unroll
-  for (int j = 8; j < N; ++j) m[j & 7] = fmaxf(m[j & 7], v[j]);
-  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+  for (int j = 8; j < N; j += 2) m[(j >> 1) & 3] = fmax3(m[(j >> 1) & 3], v[j], v[j + 1]);
+  return fmax3(m[0], m[1], fmaxf(m[2], m[3]));
 }
 
 // tanh for the soft cap, two ways, both from the mathematics of tanh (not
@@ -234,7 +247,9 @@ __device__ __noinline__ void run_producer(const FwdParams &p, const CUtensorMap 
                                           const Bars<C> bar, volatile int *abort) {
   uint32_t kcnt = 0, vcnt = 0, q0 = 0, q1 = 0;
   bool ok = true;
-  for (int64_t w = blockIdx.x; w < p.num_items && ok; w += gridDim.x) {
+  for (int64_t k = 0; ok; ++k) {
+    const int64_t w = item_of_round(p, k);
+    if (w < 0) break;
     const Item it = decode_item(p, w);
     if (it.nb <= 0) continue;
 #pragma unroll
@@ -324,18 +339,156 @@ __device__ __forceinline__ bool wait_ring(uint32_t full0, uint32_t cnt, int ns, 
   return true;
 }
 
-// The MMA issuer (one thread).  Per item: S_0(0), S_1(0); then per block g:
+// Per-ring bookkeeping of one MMA issuer.  Uses of the ring are numbered in
+// the producer's order; the empty barrier of a slot counts two releases per
+// use, one from each issuer: a commit from the issuer whose MMAs read the slot
+// (it arrives when they complete), a plain arrive from the other one, given
+// only after the use's data has landed.  An issuer never waits on a use while
+// an earlier use of the same ring is unreleased by it; issuer 0 defers its
+// release of tile 1's use (always the later of a pair) to its next step.
+struct RingState {
+  uint32_t cnt;      // next use
+  uint32_t pending;  // a deferred plain release, valid when has_pending
+  bool has_pending;
+};
+
+__device__ __forceinline__ bool plain_release(uint32_t full0, uint32_t empty0, uint32_t use, int ns,
+                                              volatile int *abort, uint64_t timeout_ns) {
+  const uint32_t slot = use % (uint32_t)ns;
+  if (!mbar_wait(full0 + 8u * slot, (use / (uint32_t)ns) & 1u, abort, timeout_ns)) return false;
+  mbar_arrive(empty0 + 8u * slot);
+  return true;
+}
+
+__device__ __forceinline__ bool flush_pending(RingState &r, uint32_t full0, uint32_t empty0, int ns,
+                                              volatile int *abort, uint64_t timeout_ns) {
+  if (!r.has_pending) return true;
+  r.has_pending = false;
+  return plain_release(full0, empty0, r.pending, ns, abort, timeout_ns);
+}
+
+// One step of a ring: the tile-0 and tile-1 uses of one K or V tile (one use
+// when both tiles share it).  Waits for this issuer's use, and returns its
+// slot in `slot` (use_it = false when this issuer has no MMA on it).
+__device__ __forceinline__ bool ring_step_acquire(RingState &r, uint32_t full0, uint32_t empty0, int ns, int t,
+                                                  bool two_kv, bool mine, volatile int *abort, uint64_t timeout_ns,
+                                                  uint32_t &slot, uint32_t &use) {
+  if (!flush_pending(r, full0, empty0, ns, abort, timeout_ns)) return false;
+  if (two_kv && t == 1) {
+    // tile 0's use comes first in the ring: release it before waiting on ours
+    if (!plain_release(full0, empty0, r.cnt, ns, abort, timeout_ns)) return false;
+  }
+  use = (two_kv && t == 1) ? r.cnt + 1 : r.cnt;
+  slot = use % (uint32_t)ns;
+  if (!mine) return plain_release(full0, empty0, use, ns, abort, timeout_ns);
+  if (!mbar_wait(full0 + 8u * slot, (use / (uint32_t)ns) & 1u, abort, timeout_ns)) return false;
+  tc_fence_after();
+  return true;
+}
+
+// After this issuer's MMAs on the step's slot: commit its release, defer or
+// skip the other tile's, advance the ring.
+__device__ __forceinline__ void ring_step_release(RingState &r, uint32_t empty0, int ns, int t, bool two_kv,
+                                                  bool mine, uint32_t use) {
+  if (mine) tc_commit(empty0 + 8u * (use % (uint32_t)ns));
+  if (two_kv && t == 0) {
+    r.pending = r.cnt + 1;
+    r.has_pending = true;
+  }
+  r.cnt += two_kv ? 2u : 1u;
+}
+
+// An MMA issuer (one thread per query tile t).  Per item: S_t(0) = Q_t K(0)^T;
+// then per block g: wait P_t(g): O_t += P_t V(g); S_t(g+1) = Q_t K(g+1)^T.
+// Both issuers walk the same K / V ring sequence (the producer's order:
+// K0(0) [K1(0)], then per block V0(g) K0(g+1) [V1(g) K1(g+1)]).  Commits:
+// s_full after each S, o_done after the last PV, q_empty after the tile's
+// last S.  Two issuers keep one tile's MMA burst from waiting behind the
+// other's in the tensor pipe's queue.
+template <class C, int BK>
+__device__ __noinline__ void run_mma(const FwdParams &p, uint32_t tmem, uint32_t sQ, uint32_t sK, uint32_t sV,
+                                     const Bars<C> bar, volatile int *abort, const int t) {
+  RingState kr{0u, 0u, false}, vr{0u, 0u, false};
+  uint32_t qc = 0, pc = 0;
+  bool ok = true;
+  const uint32_t tS = tmem + 128u * t, tO = tmem + 256u + 128u * t;
+  const uint32_t sQt = sQ + t * C::Q_BYTES;
+  for (int64_t k = 0; ok; ++k) {
+    const int64_t w = item_of_round(p, k);
+    if (w < 0) break;
+    const Item it = decode_item(p, w);
+    if (it.nb <= 0) continue;
+    const bool mine = (t == 0) || it.act1;
+    const bool two_kv = it.act1 && !it.shared;
+    if (mine) {
+      if (!(ok = mbar_wait(bar.q_full(t), qc & 1, abort, p.timeout_ns))) break;
+      ++qc;
+      tc_fence_after();
+    }
+    uint32_t slot, use;
+    // S_t(0)
+    if (!(ok = ring_step_acquire(kr, bar.k_full(0), bar.k_empty(0), C::NK, t, two_kv, mine, abort, p.timeout_ns,
+                                 slot, use)))
+      break;
+    if (mine) {
+      issue_qk<C>(tS, sQt, sK + slot * C::K_BYTES);
+      tc_commit(bar.s_full(t));
+      if (it.nb == 1) tc_commit(bar.q_empty(t));
+    }
+    ring_step_release(kr, bar.k_empty(0), C::NK, t, two_kv, mine, use);
+    for (int32_t g = 0; g < it.nb && ok; ++g) {
+      const bool more = g + 1 < it.nb;
+      // O_t += P_t V(g)
+      if (mine) {
+        if (!(ok = mbar_wait(bar.p_full(t), pc & 1, abort, p.timeout_ns))) break;
+        ++pc;
+        tc_fence_after();
+      }
+      if (!(ok = ring_step_acquire(vr, bar.v_full(0), bar.v_empty(0), C::NV, t, two_kv, mine, abort,
+                                   p.timeout_ns, slot, use)))
+        break;
+      if (mine) {
+        issue_pv<C, BK>(tO, tS, sV + slot * C::V_BYTES, g == 0);
+        if (!more) tc_commit(bar.o_done(t));
+      }
+      ring_step_release(vr, bar.v_empty(0), C::NV, t, two_kv, mine, use);
+      if (!more) break;
+      // S_t(g+1) = Q_t K(g+1)^T
+      if (!(ok = ring_step_acquire(kr, bar.k_full(0), bar.k_empty(0), C::NK, t, two_kv, mine, abort,
+                                   p.timeout_ns, slot, use)))
+        break;
+      if (mine) {
+        issue_qk<C>(tS, sQt, sK + slot * C::K_BYTES);
+        tc_commit(bar.s_full(t));
+        if (g + 2 == it.nb) tc_commit(bar.q_empty(t));
+      }
+      ring_step_release(kr, bar.k_empty(0), C::NK, t, two_kv, mine, use);
+    }
+  }
+  if (ok) ok = flush_pending(kr, bar.k_full(0), bar.k_empty(0), C::NK, abort, p.timeout_ns) &&
+               flush_pending(vr, bar.v_full(0), bar.v_empty(0), C::NV, abort, p.timeout_ns);
+  if (!ok) raise_error(p, abort, SPLASH_DEV_TIMEOUT_MMA);
+  // drain: every MMA issued by this thread has completed (the barrier counts
+  // both issuers)
+  tc_commit(bar.drain());
+  if (!mbar_wait_drain(bar.drain(), 0, p.timeout_ns)) atomicOr(p.err, SPLASH_DEV_TIMEOUT_DRAIN);
+}
+
+// The single MMA issuer (one thread for both tiles), used when the tiles share
+// their K / V tiles (GQA heads of one group).  Per item: S_0(0), S_1(0); then per block g:
 //   wait P_0(g): O_0 += P_0 V(g); S_0(g+1) = Q_0 K(g+1)^T;
 //   wait P_1(g): O_1 += P_1 V(g); S_1(g+1) = Q_1 K(g+1)^T.
 // Commits: s_full after each S, o_done after the last PV, slot releases
 // after the last MMA that reads a slot, q_empty after a tile's last S.
 template <class C, int BK>
-__device__ __noinline__ void run_mma(const FwdParams &p, uint32_t tmem, uint32_t sQ, uint32_t sK, uint32_t sV,
+__device__ __noinline__ void run_mma_pair(const FwdParams &p, uint32_t tmem, uint32_t sQ, uint32_t sK, uint32_t sV,
                                      const Bars<C> bar, volatile int *abort) {
   uint32_t kcnt = 0, vcnt = 0, q0 = 0, q1 = 0, p0 = 0, p1 = 0;
   bool ok = true;
   const uint32_t tS0 = tmem, tS1 = tmem + 128u, tO0 = tmem + 256u, tO1 = tmem + 384u;
-  for (int64_t w = blockIdx.x; w < p.num_items && ok; w += gridDim.x) {
+  for (int64_t k = 0; ok; ++k) {
+    const int64_t w = item_of_round(p, k);
+    if (w < 0) break;
     const Item it = decode_item(p, w);
     if (it.nb <= 0) continue;
     const bool two = it.act1;
@@ -419,6 +572,54 @@ __device__ __noinline__ void run_mma(const FwdParams &p, uint32_t tmem, uint32_t
   if (!mbar_wait_drain(bar.drain(), 0, p.timeout_ns)) atomicOr(p.err, SPLASH_DEV_TIMEOUT_DRAIN);
 }
 
+// Packed form of tanh_series_scaled for two scores.
+__device__ __forceinline__ f32x2 tanh_series_scaled2(f32x2 s, f32x2 k, f32x2 kc) {
+  const f32x2 a = fmul2(s, k);
+  const f32x2 t2 = fmul2(a, a);
+  f32x2 poly = ffma2(t2, f32x2{-17.f / 315.f, -17.f / 315.f}, f32x2{2.f / 15.f, 2.f / 15.f});
+  poly = ffma2(poly, t2, f32x2{-1.f / 3.f, -1.f / 3.f});
+  const f32x2 q = ffma2(t2, poly, f32x2{1.f, 1.f});
+  return fmul2(fmul2(s, kc), q);
+}
+
+// s_j <- 2^(s_j * mul - sub) in place (packed argument), returns the row sum
+// (eight independent partial sums).
+template <int N>
+__device__ __forceinline__ float exp2_block(float (&s)[N], float mul, float sub) {
+  const f32x2 m2{mul, mul}, n2{-sub, -sub};
+  f32x2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+  for (int j = 0; j < N; j += 2) {
+    const f32x2 a = ffma2(f32x2{s[j], s[j + 1]}, m2, n2);
+    s[j] = ex2_approx(a.x);
+    s[j + 1] = ex2_approx(a.y);
+    acc[(j >> 1) & 3] = fadd2(acc[(j >> 1) & 3], f32x2{s[j], s[j + 1]});
+  }
+  const f32x2 t = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+  return t.x + t.y;
+}
+
+// The same, also returning the maximum of the inputs in `mx`: the max rides
+// along the exponentials (whose special-function unit paces the loop) instead
+// of being a dense pass of its own.
+template <int N>
+__device__ __forceinline__ float exp2_block_max(float (&s)[N], float mul, float sub, float &mx) {
+  const f32x2 m2{mul, mul}, n2{-sub, -sub};
+  f32x2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int j = 0; j < N; j += 2) {
+    m[(j >> 1) & 3] = fmax3(m[(j >> 1) & 3], s[j], s[j + 1]);
+    const f32x2 a = ffma2(f32x2{s[j], s[j + 1]}, m2, n2);
+    s[j] = ex2_approx(a.x);
+    s[j + 1] = ex2_approx(a.y);
+    acc[(j >> 1) & 3] = fadd2(acc[(j >> 1) & 3], f32x2{s[j], s[j + 1]});
+  }
+  mx = fmax3(m[0], m[1], fmaxf(m[2], m[3]));
+  const f32x2 t = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+  return t.x + t.y;
+}
+
 template <int DQK, int DV, int BK>
 __global__ void __launch_bounds__(kThreads, 1)
 splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -452,13 +653,13 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     }
     for (int s = 0; s < C::NK; ++s) {
       mbar_init(bar.k_full(s), 1);
-      mbar_init(bar.k_empty(s), 1);
+      mbar_init(bar.k_empty(s), p.dual_issuer ? 2 : 1);  // one release per MMA issuer
     }
     for (int s = 0; s < C::NV; ++s) {
       mbar_init(bar.v_full(s), 1);
-      mbar_init(bar.v_empty(s), 1);
+      mbar_init(bar.v_empty(s), p.dual_issuer ? 2 : 1);
     }
-    mbar_init(bar.drain(), 1);
+    mbar_init(bar.drain(), p.dual_issuer ? 2 : 1);
     *abort = 0;
     mbar_fence_init();
   }
@@ -477,8 +678,13 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   regs_decrease<kControlRegs>();
   if (warp == kProducerWarp) {
     if (lane == 0) run_producer<C, BK>(p, &tmQ, &tmK, &tmV, sQ, sK, sV, bar, abort);
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) run_mma<C, BK>(p, tmem, sQ, sK, sV, bar, abort);
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    if (lane == 0) {
+      if (p.dual_issuer)
+        run_mma<C, BK>(p, tmem, sQ, sK, sV, bar, abort, warp - kMmaWarp);
+      else if (warp == kMmaWarp)
+        run_mma_pair<C, BK>(p, tmem, sQ, sK, sV, bar, abort);
+    }
   }
   } else {
   // ============================================================ warpgroups 0, 1
@@ -494,7 +700,9 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     const bool row_valid = row < p.bq;
     uint32_t scnt = 0, ocnt = 0;
     bool ok = true;
-    for (int64_t w = blockIdx.x; w < p.num_items && ok; w += gridDim.x) {
+    for (int64_t k = 0; ok; ++k) {
+      const int64_t w = item_of_round(p, k);
+      if (w < 0) break;
       const Item it = decode_item(p, w);
       if (t == 1 && !it.act1) continue;
       const int32_t h = t ? it.h1 : it.h0;
@@ -538,64 +746,103 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
           }
         }
         // s_j in log2 units: s*scale*log2e (folded into the exponent's FFMA
-        // below) or, with the soft cap, cap*log2e*tanh(s*scale/cap) computed
-        // here.  Masked entries become -inf.
-        float mx;
-        if (!p.use_softcap) {
-          if (need_mask) {
+        // through `mul`) or, with the soft cap, cap*log2e*tanh(s*scale/cap)
+        // computed here.  Masked entries become -inf.
+        const float mul = p.use_softcap ? 1.f : p.scale_log2;
+        if (p.use_softcap) {
+          float am[4];
 #pragma unroll
-            for (int j = 0; j < BK; ++j) s[j] = ((bits[j >> 5] >> (j & 31)) & 1u) ? s[j] : -INFINITY;
-          }
-          mx = max_tree<BK>(s) * p.scale_log2;  // scale > 0
-        } else {
-          float am[8];
+          for (int x = 0; x < 4; ++x) am[x] = fmaxf(fabsf(s[2 * x]), fabsf(s[2 * x + 1]));
 #pragma unroll
-          for (int x = 0; x < 8; ++x) am[x] = fabsf(s[x]);
-#pragma unroll
-          for (int j = 8; j < BK; ++j) am[j & 7] = fmaxf(am[j & 7], fabsf(s[j]));
-          const float amax = fmaxf(fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3])),
-                                   fmaxf(fmaxf(am[4], am[5]), fmaxf(am[6], am[7]))) * p.cap_inner;
+          for (int j = 8; j < BK; j += 2) am[(j >> 1) & 3] = fmax3(am[(j >> 1) & 3], fabsf(s[j]), fabsf(s[j + 1]));
+          const float amax = fmax3(am[0], am[1], fmaxf(am[2], am[3])) * p.cap_inner;
           if (__any_sync(0xffffffffu, amax > kTanhSeriesLimit)) {
 #pragma unroll
             for (int j = 0; j < BK; ++j) s[j] = p.cap_log2 * tanh_identity(s[j] * p.cap_inner);
           } else {
-            const float kc = p.cap_log2 * p.cap_inner;
+            const f32x2 k2{p.cap_inner, p.cap_inner};
+            const f32x2 kc2{p.cap_log2 * p.cap_inner, p.cap_log2 * p.cap_inner};
 #pragma unroll
-            for (int j = 0; j < BK; ++j) s[j] = tanh_series_scaled(s[j], p.cap_inner, kc);
+            for (int j = 0; j < BK; j += 2) {
+              const f32x2 r2 = tanh_series_scaled2(f32x2{s[j], s[j + 1]}, k2, kc2);
+              s[j] = r2.x;
+              s[j + 1] = r2.y;
+            }
           }
-          if (need_mask) {
-#pragma unroll
-            for (int j = 0; j < BK; ++j) s[j] = ((bits[j >> 5] >> (j & 31)) & 1u) ? s[j] : -INFINITY;
-          }
-          mx = max_tree<BK>(s);
         }
-        const float m_new = fmaxf(m_ref, mx);
+        if (need_mask) {
+#pragma unroll
+          for (int j = 0; j < BK; ++j) s[j] = ((bits[j >> 5] >> (j & 31)) & 1u) ? s[j] : -INFINITY;
+        }
         float alpha = 1.f;
-        if (m_new != -INFINITY && (m_ref == -INFINITY || m_new > m_ref + kRescaleThreshold)) {
-          alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_new);
-          m_ref = m_new;
-        }
-        const float sub = (m_ref == -INFINITY) ? 0.f : m_ref;
-        const float mul = p.use_softcap ? 1.f : p.scale_log2;
-        // P = 2^(s - m_ref) as bf16 pairs into the first BK/2 columns of S_t
-        // (S is already in registers), 32 columns per store
-        float sum8[8];
+        float sum;
+        bool redo = false;  // this lane's exponentials must be recomputed (rare)
+        if (m_ref == -INFINITY) {
+          // first block with an allowed key: the reference is this block's max
+          const float mx = max_tree<BK>(s) * mul;  // scale > 0
+          if (mx != -INFINITY) {
+            alpha = 0.f;
+            m_ref = mx;
+          }
+          sum = exp2_block<BK>(s, mul, m_ref == -INFINITY ? 0.f : m_ref);
+        } else {
+          // exponentiate against the current reference while the block's max
+          // is reduced alongside; the reference moves only when the max grows
+          // by more than 2^8, and then the exponentials are rescaled
+          float mx;
+          sum = exp2_block_max<BK>(s, mul, m_ref, mx);
+          mx *= mul;
+          if (mx > m_ref + kRescaleThreshold) {
+            const float m_old = m_ref;
+            alpha = ex2_approx(m_old - mx);
+            m_ref = mx;
+            if (mx - m_old < 64.f) {
 #pragma unroll
-        for (int x = 0; x < 8; ++x) sum8[x] = 0.f;
+              for (int j = 0; j < BK; ++j) s[j] *= alpha;
+              sum *= alpha;
+            } else {
+              redo = true;  // the exponentials may have overflowed
+            }
+          }
+        }
+        // (lanes of a warp can be in different branches above: rows with no
+        // allowed key so far take the first one; the vote below is after
+        // they reconverge)
+        if (__any_sync(0xffffffffu, redo)) {
+          {
+            // rare: reload S (warp-collective) and redo this lane's row
+#pragma unroll
+            for (int c = 0; c < BK / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32(tS + 32u * c, r);
+              tmem_wait_ld();
+              reg_fence32(r);
+              if (redo) {
+#pragma unroll
+                for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(r[x]);
+              }
+            }
+            if (redo) {
+              if (p.use_softcap) {
+#pragma unroll
+                for (int j = 0; j < BK; ++j) s[j] = p.cap_log2 * tanh_identity(s[j] * p.cap_inner);
+              }
+              if (need_mask) {
+#pragma unroll
+                for (int j = 0; j < BK; ++j) s[j] = ((bits[j >> 5] >> (j & 31)) & 1u) ? s[j] : -INFINITY;
+              }
+              sum = exp2_block<BK>(s, mul, m_ref);
+            }
+          }
+        }
+        // P (bf16 pairs) into the first BK/2 columns of S_t, 32 columns per store
 #pragma unroll
         for (int c = 0; c < BK / 64; ++c) {
           uint32_t r[32];
 #pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            const int j = c * 64 + 2 * x;
-            const float p0 = ex2_approx(fmaf(s[j], mul, -sub));
-            const float p1 = ex2_approx(fmaf(s[j + 1], mul, -sub));
-            sum8[x & 7] += p0 + p1;
-            r[x] = pack_bf16x2(p0, p1);
-          }
+          for (int x = 0; x < 32; ++x) r[x] = pack_bf16x2(s[c * 64 + 2 * x], s[c * 64 + 2 * x + 1]);
           tmem_st32(tS + 32u * c, r);
         }
-        const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
         l = l * alpha + sum;
         // rescale the output accumulator (its previous PV has completed:
         // S_t(g) was committed after it)
@@ -639,8 +886,10 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         if (row_valid) {
           uint32_t o[16];
 #pragma unroll
-          for (int x = 0; x < 16; ++x)
-            o[x] = pack_bf16x2(__uint_as_float(r[2 * x]) * inv, __uint_as_float(r[2 * x + 1]) * inv);
+          for (int x = 0; x < 16; ++x) {
+            const f32x2 y = fmul2(f32x2{__uint_as_float(r[2 * x]), __uint_as_float(r[2 * x + 1])}, f32x2{inv, inv});
+            o[x] = pack_bf16x2(y.x, y.y);
+          }
           uint4 *dst = reinterpret_cast<uint4 *>(orow_ptr + c * 32);
 #pragma unroll
           for (int x = 0; x < 4; ++x) dst[x] = make_uint4(o[4 * x], o[4 * x + 1], o[4 * x + 2], o[4 * x + 3]);
@@ -761,6 +1010,9 @@ splash_status splash_attention_fwd_launch(const void *q, const void *k, const vo
   prm.num_patterns = mi->num_patterns;
   prm.scale_log2 = scale * kLog2e;
   prm.use_softcap = softcap > 0.f ? 1 : 0;
+  // one issuer per tile only when the two query heads of an item read
+  // different KV heads (MHA); shared K/V keeps one issuer for both tiles
+  prm.dual_issuer = (prm.G == 1) ? 1 : 0;
   prm.cap_inner = softcap > 0.f ? scale / softcap : 0.f;
   prm.cap_log2 = softcap > 0.f ? softcap * kLog2e : 0.f;
   prm.out = reinterpret_cast<__nv_bfloat16 *>(out);

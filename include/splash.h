@@ -177,7 +177,8 @@ void splash_mask_info_destroy(splash_mask_info *mi);
  *        from, or NULL; accepted for interface symmetry (the stored patterns
  *        already encode them).
  *   mi   a MaskInfo built for (Lq, Lk) with B_mask == 1 or B_mask == B.
- *   scale  multiplies q.k (e.g. 1/sqrt(dqk)); softcap <= 0 disables the cap.
+ *   scale  multiplies q.k (e.g. 1/sqrt(dqk)); must be positive and finite.
+ *   softcap <= 0 disables the cap (NaN or +inf is rejected).
  *   out  device bf16 [B][Hq][Lq][dv]       lse device fp32 [B][Hq][Lq]
  *
  * Supported in this build: dqk in {64, 128, 192}, dv in {64, 128}, dv <= dqk

@@ -70,6 +70,10 @@ def test_invalid_arguments_are_rejected_before_any_launch(splash):
     # attention: NULL tensors / handle
     f = lib.splash_attention_fwd
     assert f(None, None, None, 1, 2, 2, 256, 256, 64, 64, None, None, None, 0.125, 0.0, None, None, null) == 1
+    # non-positive / NaN scale (checked before the handle is touched)
+    fake = ctypes.c_void_p(16)
+    assert f(fake, fake, fake, 1, 2, 2, 256, 256, 64, 64, None, None, fake, 0.0, 0.0, fake, fake, null) == 1
+    assert f(fake, fake, fake, 1, 2, 2, 256, 256, 64, 64, None, None, fake, float("nan"), 0.0, fake, fake, null) == 1
     # counts / shape / to_host on a NULL handle
     assert lib.splash_mask_info_counts(None, None, None, None, None) == 1
     assert lib.splash_mask_info_shape(None, None, None, None, None, None) == 1

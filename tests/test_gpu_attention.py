@@ -56,6 +56,8 @@ SMALL = [
     ("causal GQA d128", 2, 4, 2, 512, 512, 128, 128, 128, {}),
     ("odd heads G=3 causal window", 1, 3, 1, 512, 512, 128, 128, 128, dict(wl=100)),
     ("MHA pairs d192/128", 2, 2, 2, 384, 384, 192, 128, 128, {}),
+    ("MHA pairs d128, odd heads", 1, 3, 3, 512, 512, 128, 128, 128, dict(wl=200)),
+    ("GQA G=3 pairs straddle groups", 1, 6, 2, 512, 512, 128, 128, 128, {}),
     ("d64 blocks 128", 1, 4, 4, 512, 512, 64, 64, 128, {}),
     ("d128 blocks 64", 1, 4, 2, 512, 512, 128, 128, 64, {}),
     ("no mask", 1, 2, 1, 256, 256, 128, 128, 128, dict(causal=False)),
@@ -65,6 +67,8 @@ SMALL = [
     ("softcap small logits (series path)", 2, 4, 2, 512, 512, 128, 128, 128, dict(softcap=50.0)),
     ("softcap mixed rows", 1, 2, 2, 512, 512, 64, 64, 64, dict(softcap=8.0, q_gain=1.5)),
     ("Lq < Lk causal", 1, 2, 2, 256, 512, 128, 128, 128, {}),
+    ("huge logits (reference jumps)", 1, 4, 2, 1024, 1024, 128, 128, 128, dict(q_gain=40.0)),
+    ("huge logits soft-capped", 1, 2, 2, 512, 512, 64, 64, 64, dict(q_gain=40.0, softcap=100.0)),
     ("long row many blocks", 1, 2, 2, 2048, 2048, 128, 128, 128, dict(q_gain=2.0)),
 ]
 
