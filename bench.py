@@ -165,22 +165,27 @@ def oracle_sample_rate(w, inp, nrows, seed, nthreads=0):
     t0 = time.perf_counter()
     oracle.attention(inp.q, inp.k, inp.v, spec, w.scale, w.softcap, rows=rows, nthreads=nth)
     dt = time.perf_counter() - t0
-    # allowed keys of each sampled row (counted from the mask definition)
-    i = rows % w.L
-    b = rows // (w.Hq * w.L)
-    allowed = np.zeros(len(rows), dtype=np.int64)
-    for x in range(len(rows)):
-        j = np.arange(w.L)
-        ok = np.ones(w.L, dtype=bool)
-        if w.causal:
-            ok &= j <= i[x]
-        if w.window_left >= 0:
-            ok &= i[x] - j <= w.window_left
-        if w.window_right >= 0:
-            ok &= j - i[x] <= w.window_right
-        if seg is not None:
-            ok &= seg[b[x]] == seg[b[x], i[x]]
-        allowed[x] = int(ok.sum())
+    # allowed keys of each sampled row, counted from the mask definition: the
+    # band [lo, hi] of the causal / window part, intersected with the row's
+    # document when segment IDs are given (contiguous documents)
+    i = (rows % w.L).astype(np.int64)
+    b = (rows // (w.Hq * w.L)).astype(np.int64)
+    lo = np.maximum(0, i - w.window_left) if w.window_left >= 0 else np.zeros_like(i)
+    hi = i.copy() if w.causal else np.full_like(i, w.L - 1)
+    if w.window_right >= 0:
+        hi = np.minimum(hi, i + w.window_right)
+    if seg is not None:
+        starts = np.zeros_like(seg, dtype=np.int64)
+        ends = np.zeros_like(seg, dtype=np.int64)
+        for r in range(seg.shape[0]):
+            change = np.flatnonzero(np.diff(seg[r]) != 0) + 1
+            bounds = np.concatenate([[0], change, [seg.shape[1]]])
+            doc = np.repeat(np.arange(len(bounds) - 1), np.diff(bounds))
+            starts[r] = bounds[doc]
+            ends[r] = bounds[doc + 1] - 1
+        lo = np.maximum(lo, starts[b, i])
+        hi = np.minimum(hi, ends[b, i])
+    allowed = np.maximum(hi - lo + 1, 0)
     return 2.0 * (w.dqk + w.dv) * float(allowed.sum()), dt, nth, len(rows)
 
 
