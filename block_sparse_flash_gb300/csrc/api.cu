@@ -135,6 +135,8 @@ splash_status splash_mask_info_shape(const splash_mask_info *mi, int32_t *batch_
 splash_status splash_mask_info_counts(const splash_mask_info *mi, int64_t *num_active, int64_t *num_partial,
                                       int64_t *num_patterns, int64_t *allowed_pairs) {
   if (mi == nullptr) return SPLASH_ERR_INVALID_ARG;
+  const splash_status st = splash_mask_info_sync_counts(const_cast<splash_mask_info *>(mi));
+  if (st != SPLASH_OK) return st;
   if (num_active) *num_active = mi->num_active;
   if (num_partial) *num_partial = mi->num_partial;
   if (num_patterns) *num_patterns = mi->num_patterns;
@@ -147,6 +149,8 @@ splash_status splash_mask_info_to_host(const splash_mask_info *mi, int8_t *block
                                        uint8_t *bounds_start, uint8_t *bounds_end,
                                        uint8_t *partial_mask_blocks) {
   if (mi == nullptr || mi->nq <= 0) return SPLASH_ERR_INVALID_ARG;
+  const splash_status st = splash_mask_info_sync_counts(const_cast<splash_mask_info *>(mi));
+  if (st != SPLASH_OK) return st;
   const int64_t R = (int64_t)mi->batch_rows * mi->nq, A = mi->num_active;
   const int64_t P = mi->num_patterns;
   if (block_mask) SPLASH_CUDA_TRY(cudaMemcpy(block_mask, mi->block_mask, R * mi->nk, cudaMemcpyDeviceToHost));

@@ -1007,7 +1007,9 @@ splash_status splash_attention_fwd_launch(const void *q, const void *k, const vo
   prm.mask_next = mi->mask_next;
   prm.pattern_bits = mi->pattern_bits;
   prm.row_order = mi->row_order;
-  prm.num_patterns = mi->num_patterns;
+  // bound for the kernel's check of mask_next (the true count may still be in
+  // flight after an asynchronous build; it never exceeds the buffer capacity)
+  prm.num_patterns = mi->counts_pending ? mi->cap_patterns : mi->num_patterns;
   prm.scale_log2 = scale * kLog2e;
   prm.use_softcap = softcap > 0.f ? 1 : 0;
   // one issuer per tile only when the two query heads of an item read

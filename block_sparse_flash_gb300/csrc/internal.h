@@ -61,6 +61,10 @@ struct splash_mask_info {
   unsigned long long *counters = nullptr;  // [8]: A, A_p, P, allowed, max_row
   // host staging
   unsigned long long *h_counters = nullptr;  // pinned [8]
+  // counts of an asynchronous build: h_counters is valid once `counts_ready`
+  // (recorded after its copy) has completed
+  cudaEvent_t counts_ready = nullptr;
+  bool counts_pending = false;
 
   // capacities (elements)
   int64_t cap_rows = 0, cap_blocks = 0, cap_seg = 0, cap_patterns = 0, cap_hist = 0;
@@ -71,6 +75,8 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
                                           int64_t Lq, int64_t Lk, int32_t bq, int32_t bk,
                                           cudaStream_t stream);
 void splash_mask_info_free_buffers(splash_mask_info *mi);
+// Makes the host totals current (waits for an asynchronous build's copy).
+splash_status splash_mask_info_sync_counts(splash_mask_info *mi);
 splash_status splash_classify_blocks_noalloc_impl(const splash_mask_spec *spec, int64_t Lq, int64_t Lk,
                                                   int32_t bq, int32_t bk, int8_t *block_mask,
                                                   int64_t *totals, cudaStream_t stream);

@@ -381,11 +381,19 @@ __global__ void finalize_kernel(const unsigned long long *counters, const int32_
 }
 
 // One CTA (bq threads) per pattern: the bit-packed rows and the byte pattern.
-__global__ void materialize_kernel(DevMask m, int64_t P, const int32_t *rep_list,
-                                   const int32_t *part_row, const int32_t *part_col,
-                                   uint32_t *pattern_bits, uint8_t *patterns) {
+// The pattern count is read on the device (counters[2]) and never exceeds the
+// buffer capacity `cap` (a count above it is reported and clipped).
+__global__ void materialize_kernel(DevMask m, const unsigned long long *counters, int64_t cap,
+                                   const int32_t *rep_list, const int32_t *part_row,
+                                   const int32_t *part_col, uint32_t *pattern_bits, uint8_t *patterns,
+                                   uint32_t *err) {
   const int di = threadIdx.x;
   const int32_t words = m.bk / 32;
+  int64_t P = (int64_t)counters[2];
+  if (P > cap) {
+    if (blockIdx.x == 0 && di == 0 && err) atomicOr(err, SPLASH_DEV_BAD_TABLE);
+    P = cap;
+  }
   for (int64_t u = blockIdx.x; u < P; u += gridDim.x) {
     const int64_t k = rep_list[u];
     const int64_t row = part_row[k];
@@ -485,6 +493,7 @@ void splash_mask_info_free_buffers(splash_mask_info *mi) {
   void *host[] = {mi->h_counters};
   for (void *p : host)
     if (p) cudaFreeHost(p);
+  if (mi->counts_ready) cudaEventDestroy(mi->counts_ready);
   const int device = mi->device;
   *mi = splash_mask_info();
   mi->device = device;
@@ -558,6 +567,9 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
   SPLASH_CUDA_TRY(cudaGetDevice(&dev));
   SPLASH_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
 
+  // a previous asynchronous build (possibly on another stream) copies its
+  // totals into h_counters: keep that copy ordered before this build's
+  if (mi->counts_pending && mi->counts_ready) SPLASH_CUDA_TRY(cudaStreamWaitEvent(stream, mi->counts_ready, 0));
   SPLASH_CUDA_TRY(cudaMemsetAsync(mi->row_cnt, 0, sizeof(int32_t) * R, stream));
   SPLASH_CUDA_TRY(cudaMemsetAsync(mi->row_pcnt, 0, sizeof(int32_t) * R, stream));
   SPLASH_CUDA_TRY(cudaMemsetAsync(mi->counters, 0, sizeof(unsigned long long) * 8, stream));
@@ -588,35 +600,69 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
   SPLASH_CUDA_TRY(cudaGetLastError());
   splash_count_launches(seg ? 10 : 9);
 
-  // -- the one host wait: the totals (P sizes the pattern buffer) --
-  SPLASH_CUDA_TRY(cudaMemcpyAsync(mi->h_counters, mi->counters, sizeof(unsigned long long) * 8,
-                                  cudaMemcpyDeviceToHost, stream));
-  SPLASH_CUDA_TRY(cudaStreamSynchronize(stream));
+  uint32_t *err = splash_device_error_word(mi->device);
+  // -- pattern buffer.  Without segment IDs a q-block row has at most
+  // 2 * (ceil((bq-1)/bk) + 1) partial blocks (a block is partial only if one of
+  // the two band edges sweeps through it), so P has a bound known here and the
+  // build runs without a host wait; the totals are read lazily.  With segment
+  // IDs the build waits once for P.
+  const int64_t per_row = 2 * ((bq - 1 + bk - 1) / bk + 1);
+  const int64_t p_bound = std::min<int64_t>(R * per_row, NB);
+  const bool async = !seg && p_bound * (int64_t)bq * bk <= ((int64_t)256 << 20);
+  int64_t P_cap;
+  if (async) {
+    P_cap = p_bound;
+  } else {
+    SPLASH_CUDA_TRY(cudaMemcpyAsync(mi->h_counters, mi->counters, sizeof(unsigned long long) * 8,
+                                    cudaMemcpyDeviceToHost, stream));
+    SPLASH_CUDA_TRY(cudaStreamSynchronize(stream));
+    P_cap = (int64_t)mi->h_counters[2];
+  }
+  if (P_cap > 0 && mi->cap_patterns < P_cap) {
+    if (mi->patterns) cudaFree(mi->patterns);
+    if (mi->pattern_bits) cudaFree(mi->pattern_bits);
+    mi->patterns = nullptr;
+    mi->pattern_bits = nullptr;
+    mi->cap_patterns = 0;
+    if ((st = map_alloc(cudaMalloc(&mi->patterns, (size_t)P_cap * bq * bk))) != SPLASH_OK) return st;
+    if ((st = map_alloc(cudaMalloc(&mi->pattern_bits, (size_t)P_cap * bq * (bk / 32) * 4))) != SPLASH_OK)
+      return st;
+    mi->cap_patterns = P_cap;
+  }
+  if (P_cap > 0) {
+    const unsigned grid = (unsigned)std::min<int64_t>(P_cap, async ? sms * 4 : 65535);
+    materialize_kernel<<<grid, bq, 0, stream>>>(m, mi->counters, mi->cap_patterns, mi->rep_list, mi->part_row,
+                                                mi->part_col, mi->pattern_bits, mi->patterns, err);
+    SPLASH_CUDA_TRY(cudaGetLastError());
+    splash_count_launches(1);
+  }
+  if (async) {
+    SPLASH_CUDA_TRY(cudaMemcpyAsync(mi->h_counters, mi->counters, sizeof(unsigned long long) * 8,
+                                    cudaMemcpyDeviceToHost, stream));
+    if (mi->counts_ready == nullptr)
+      SPLASH_CUDA_TRY(cudaEventCreateWithFlags(&mi->counts_ready, cudaEventDisableTiming));
+    SPLASH_CUDA_TRY(cudaEventRecord(mi->counts_ready, stream));
+    mi->counts_pending = true;
+  } else {
+    mi->counts_pending = false;
+    mi->num_active = (int64_t)mi->h_counters[0];
+    mi->num_partial = (int64_t)mi->h_counters[1];
+    mi->num_patterns = (int64_t)mi->h_counters[2];
+    mi->allowed_pairs = (int64_t)mi->h_counters[3];
+    mi->max_row_blocks = (int32_t)mi->h_counters[4];
+  }
+  return SPLASH_OK;
+}
+
+splash_status splash_mask_info_sync_counts(splash_mask_info *mi) {
+  if (!mi->counts_pending) return SPLASH_OK;
+  SPLASH_CUDA_TRY(cudaEventSynchronize(mi->counts_ready));
   mi->num_active = (int64_t)mi->h_counters[0];
   mi->num_partial = (int64_t)mi->h_counters[1];
   mi->num_patterns = (int64_t)mi->h_counters[2];
   mi->allowed_pairs = (int64_t)mi->h_counters[3];
   mi->max_row_blocks = (int32_t)mi->h_counters[4];
-
-  const int64_t P = mi->num_patterns;
-  if (P > 0) {
-    if (mi->cap_patterns < P) {
-      if (mi->patterns) cudaFree(mi->patterns);
-      if (mi->pattern_bits) cudaFree(mi->pattern_bits);
-      mi->patterns = nullptr;
-      mi->pattern_bits = nullptr;
-      mi->cap_patterns = 0;
-      if ((st = map_alloc(cudaMalloc(&mi->patterns, (size_t)P * bq * bk))) != SPLASH_OK) return st;
-      if ((st = map_alloc(cudaMalloc(&mi->pattern_bits, (size_t)P * bq * (bk / 32) * 4))) != SPLASH_OK)
-        return st;
-      mi->cap_patterns = P;
-    }
-    const unsigned grid = (unsigned)std::min<int64_t>(P, 65535);
-    materialize_kernel<<<grid, bq, 0, stream>>>(m, P, mi->rep_list, mi->part_row, mi->part_col,
-                                                mi->pattern_bits, mi->patterns);
-    SPLASH_CUDA_TRY(cudaGetLastError());
-    splash_count_launches(1);
-  }
+  mi->counts_pending = false;
   return SPLASH_OK;
 }
 

@@ -102,3 +102,26 @@ def test_everything_masked_gives_an_empty_table(bsf):
     got, ref = gpu_and_oracle(bsf, True, -1, -1, q, kv, 256, 256, 64, 64)
     assert got["num_active"] == 0
     assert_same(got, ref, "empty")
+
+
+def test_async_build_then_attention_then_counts(bsf):
+    # without segment IDs the build does not wait on the host; the attention
+    # call may follow at once and the totals are read afterwards
+    L = 2048
+    q = workloads.normal_bf16((1, 2, L, 128), 11).cuda()
+    k = workloads.normal_bf16((1, 2, L, 128), 12).cuda()
+    v = workloads.normal_bf16((1, 2, L, 128), 13).cuda()
+    mi = bsf.build_mask_info(bsf.MaskSpec(True, 300, 0), L, L, 128, 128)
+    out, lse = bsf.attention_fwd(q, k, v, mi, 128 ** -0.5)
+    mi.rebuild(bsf.MaskSpec(True), L, L, 128, 128)
+    out2, lse2 = bsf.attention_fwd(q, k, v, mi, 128 ** -0.5)
+    ref = oracle.mask_info(oracle.MaskSpec(True), L, L, 128, 128)
+    c = mi.counts()
+    assert (c["num_active"], c["num_partial"], c["num_patterns"], c["allowed_pairs"]) == \
+        (ref.num_active, ref.num_partial, ref.num_patterns, ref.allowed_pairs)
+    assert bsf.last_device_error() == 0
+    O, Lr = oracle.attention(q.cpu(), k.cpu(), v.cpu(), oracle.MaskSpec(True), 128 ** -0.5, rows=np.arange(0, 2 * L, 7))
+    from tests.parity import compare_rows, gather_rows
+    o, l = gather_rows(out2, lse2, np.arange(0, 2 * L, 7))
+    compare_rows(o, l, O, Lr, "async rebuild")
+    mi.close()
