@@ -66,21 +66,27 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def kernel_source_sha():
+    """sha256 prefix of the attention kernel's sources (kernel + PTX header)."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("attention_fwd.cu", "sm103_ptx.cuh"):
+        with open(os.path.join(ROOT, "block_sparse_flash_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def recorded_traffic(workload_index):
     """DRAM bytes per attention launch from the committed ncu summary, or None
     when the kernel source has changed since those counters were taken."""
-    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    src = os.path.join(ROOT, "block_sparse_flash_gb300", "csrc", "attention_fwd.cu")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f).get(f"workload{workload_index}")
     if not rec:
         return None
-    with open(src, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()[:16]
-    return rec.get("bytes_per_launch") if sha == rec.get("kernel_sha256_prefix") else None
+    return rec.get("bytes_per_launch") if kernel_source_sha() == rec.get("kernel_sha256_prefix") else None
 
 
 def reduce_max(value, world, device=None):

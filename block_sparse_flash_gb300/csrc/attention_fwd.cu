@@ -24,8 +24,9 @@
 //     serpentine order;
 //   * warp roles (384 threads): warps 0-3 / 4-7 run the softmax of tile 0 /
 //     tile 1 (one thread per query row = one TMEM lane), warp 8 issues TMA
-//     loads; warp 9 issues the tcgen05 MMAs of both tiles when they share
-//     K/V (GQA), or warps 9 / 10 issue those of tile 0 / tile 1 (MHA);
+//     loads; warp 9 (as a whole warp, one elected lane issuing) issues the
+//     tcgen05 MMAs of both tiles when they share K/V (GQA), or lane 0 of
+//     warps 9 / 10 issues those of tile 0 / tile 1 (MHA);
 //     warp 11 only hands its registers to the softmax warpgroups;
 //   * TMEM (512 columns): S_t / P_t at column 128t (P, bf16 pairs, overwrites
 //     the first half of S after it is read), O_t at 256 + 128t;
@@ -49,10 +50,10 @@ namespace {
 
 constexpr int kThreads = 384;       // 12 warps = 3 warpgroups
 // Register split (setmaxnreg): the launch gives 384 x 168; the two softmax
-// warpgroups take 216 each and the producer / MMA warpgroup keeps 72:
-// 2*128*216 + 128*72 = 64512 = 384*168.
+// warpgroups take 200 each and the producer / MMA warpgroup keeps 104:
+// 2*128*200 + 128*104 = 64512 = 384*168.
 constexpr int kSoftmaxRegs = 200;
-constexpr int kControlRegs = 96;
+constexpr int kControlRegs = 104;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kTmemCols = 512;
@@ -308,27 +309,32 @@ __device__ __noinline__ void run_producer(const FwdParams &p, const CUtensorMap 
 
 // S_t = Q_t K^T: QCH chunks x 4 MMAs of K = 16 (K-major A and B, 128B swizzle;
 // the k-step advances the start address by 32 bytes inside the swizzle atom).
+// Descriptors are passed as their low halves; the high halves are constants.
+// Only the lane with `leader` != 0 issues (mma_ss_lhp / mma_ts_lhp).
 template <class C>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr) {
-  const uint64_t qd = sdesc_sw128(q_addr, 16, 1024), kd = sdesc_sw128(k_addr, 16, 1024);
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr, uint32_t leader) {
+  constexpr uint32_t HI = sdesc_hi_sw128(1024);
+  const uint32_t qd = sdesc_lo(q_addr, 16), kd = sdesc_lo(k_addr, 16);
 #pragma unroll
   for (int ch = 0; ch < C::QCH; ++ch)
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
-      mma_ss(d_tmem, qd + (uint64_t)((ch * C::Q_CHUNK + kk * 32) >> 4),
-             kd + (uint64_t)((ch * C::KV_CHUNK + kk * 32) >> 4), C::IDESC_QK, (ch | kk) != 0);
+      mma_ss_lhp(leader, d_tmem, qd + (uint32_t)((ch * C::Q_CHUNK + kk * 32) >> 4), HI,
+                 kd + (uint32_t)((ch * C::KV_CHUNK + kk * 32) >> 4), HI, C::IDESC_QK, (ch | kk) != 0);
 }
 
 // O_t (+)= P_t V: P read from TMEM (bf16 pairs, 8 columns per K = 16 step),
 // V MN-major with 128B swizzle (K step = 16 rows = 2048 bytes; the 64-column
 // chunks of V are KV_CHUNK bytes apart).
 template <class C, int BK>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr, bool first_block) {
-  const uint64_t vd = sdesc_sw128(v_addr, C::KV_CHUNK, 1024);
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr, bool first_block,
+                                         uint32_t leader) {
+  constexpr uint32_t HI = sdesc_hi_sw128(1024);
+  const uint32_t vd = sdesc_lo(v_addr, C::KV_CHUNK);
 #pragma unroll
   for (int j = 0; j < BK / 16; ++j)
-    mma_ts(d_tmem, p_tmem + 8u * j, vd + (uint64_t)((j * 2048) >> 4), C::IDESC_PV,
-           (!first_block || j > 0) ? 1u : 0u);
+    mma_ts_lhp(leader, d_tmem, p_tmem + 8u * j, vd + (uint32_t)((j * 2048) >> 4), HI, C::IDESC_PV,
+               (!first_block || j > 0) ? 1u : 0u);
 }
 
 __device__ __forceinline__ bool wait_ring(uint32_t full0, uint32_t cnt, int ns, volatile int *abort,
@@ -431,7 +437,7 @@ __device__ __noinline__ void run_mma(const FwdParams &p, uint32_t tmem, uint32_t
                                  slot, use)))
       break;
     if (mine) {
-      issue_qk<C>(tS, sQt, sK + slot * C::K_BYTES);
+      issue_qk<C>(tS, sQt, sK + slot * C::K_BYTES, 1u);
       tc_commit(bar.s_full(t));
       if (it.nb == 1) tc_commit(bar.q_empty(t));
     }
@@ -448,7 +454,7 @@ __device__ __noinline__ void run_mma(const FwdParams &p, uint32_t tmem, uint32_t
                                    p.timeout_ns, slot, use)))
         break;
       if (mine) {
-        issue_pv<C, BK>(tO, tS, sV + slot * C::V_BYTES, g == 0);
+        issue_pv<C, BK>(tO, tS, sV + slot * C::V_BYTES, g == 0, 1u);
         if (!more) tc_commit(bar.o_done(t));
       }
       ring_step_release(vr, bar.v_empty(0), C::NV, t, two_kv, mine, use);
@@ -458,7 +464,7 @@ __device__ __noinline__ void run_mma(const FwdParams &p, uint32_t tmem, uint32_t
                                    p.timeout_ns, slot, use)))
         break;
       if (mine) {
-        issue_qk<C>(tS, sQt, sK + slot * C::K_BYTES);
+        issue_qk<C>(tS, sQt, sK + slot * C::K_BYTES, 1u);
         tc_commit(bar.s_full(t));
         if (g + 2 == it.nb) tc_commit(bar.q_empty(t));
       }
@@ -474,15 +480,43 @@ __device__ __noinline__ void run_mma(const FwdParams &p, uint32_t tmem, uint32_t
   if (!mbar_wait_drain(bar.drain(), 0, p.timeout_ns)) atomicOr(p.err, SPLASH_DEV_TIMEOUT_DRAIN);
 }
 
-// The single MMA issuer (one thread for both tiles), used when the tiles share
-// their K / V tiles (GQA heads of one group).  Per item: S_0(0), S_1(0); then per block g:
+// Waits for the phase `pph` of barrier `pb` and, when needed, for the ring
+// tiles (V slot, K slot) the MMAs after it read.  The barriers are first
+// polled together, so that one poll's latency covers all of them; the bounded
+// waits one by one are the fallback.
+__device__ __forceinline__ bool wait_ready(uint32_t pb, uint32_t pph, bool need_v, uint32_t vb, uint32_t vph,
+                                           bool need_k, uint32_t kb, uint32_t kph, volatile int *abort,
+                                           uint64_t timeout_ns) {
+  bool r;
+  if (need_v && need_k)
+    r = mbar_try_wait3(pb, pph, vb, vph, kb, kph);
+  else if (need_v)
+    r = mbar_try_wait2(pb, pph, vb, vph);
+  else if (need_k)
+    r = mbar_try_wait2(pb, pph, kb, kph);
+  else
+    r = mbar_try_wait(pb, pph);
+  if (r) return true;
+  return mbar_wait(pb, pph, abort, timeout_ns) && (!need_v || mbar_wait(vb, vph, abort, timeout_ns)) &&
+         (!need_k || mbar_wait(kb, kph, abort, timeout_ns));
+}
+
+// The single MMA issuer for both tiles, used when the tiles share their K / V
+// tiles (GQA heads of one group).  It runs as a whole, converged warp: every
+// lane waits and computes the same (warp-uniform) ring state and descriptors,
+// and the elected lane `leader` issues the MMAs and commits.  (Measured on
+// GB300: a burst of MMAs issued this way costs ~17 cycles per MMA, against
+// ~50 from one lane of a diverged warp and ~68 when softmax warps share the
+// sub-partition; a 128x128x16 MMA executes in ~64.)
+// Per item: S_0(0), S_1(0); then per block g:
 //   wait P_0(g): O_0 += P_0 V(g); S_0(g+1) = Q_0 K(g+1)^T;
 //   wait P_1(g): O_1 += P_1 V(g); S_1(g+1) = Q_1 K(g+1)^T.
 // Commits: s_full after each S, o_done after the last PV, slot releases
 // after the last MMA that reads a slot, q_empty after a tile's last S.
 template <class C, int BK>
-__device__ __noinline__ void run_mma_pair(const FwdParams &p, uint32_t tmem, uint32_t sQ, uint32_t sK, uint32_t sV,
-                                     const Bars<C> bar, volatile int *abort) {
+__device__ __forceinline__ void run_mma_pair(const FwdParams &p, uint32_t tmem, uint32_t sQ, uint32_t sK, uint32_t sV,
+                                     const Bars<C> bar, volatile int *abort, const uint32_t leader) {
+  const uint64_t tmo = p.timeout_ns;
   uint32_t kcnt = 0, vcnt = 0, q0 = 0, q1 = 0, p0 = 0, p1 = 0;
   bool ok = true;
   const uint32_t tS0 = tmem, tS1 = tmem + 128u, tO0 = tmem + 256u, tO1 = tmem + 384u;
@@ -493,83 +527,80 @@ __device__ __noinline__ void run_mma_pair(const FwdParams &p, uint32_t tmem, uin
     if (it.nb <= 0) continue;
     const bool two = it.act1;
     const bool two_kv = it.act1 && !it.shared;
-    if (!(ok = mbar_wait(bar.q_full(0), q0 & 1, abort, p.timeout_ns))) break;
+    // S_0(0) [and S_1(0)]: Q tiles and the first K tile
+    uint32_t ks = kcnt % C::NK;
+    if (!(ok = wait_ready(bar.q_full(0), q0 & 1u, two, bar.q_full(1), q1 & 1u, true, bar.k_full(ks),
+                          (kcnt / C::NK) & 1u, abort, tmo)))
+      break;
     ++q0;
-    if (two) {
-      if (!(ok = mbar_wait(bar.q_full(1), q1 & 1, abort, p.timeout_ns))) break;
-      ++q1;
-    }
+    if (two) ++q1;
     tc_fence_after();
-    uint32_t ks;
-    if (!(ok = wait_ring(bar.k_full(0), kcnt, C::NK, abort, p.timeout_ns, ks))) break;
-    issue_qk<C>(tS0, sQ, sK + ks * C::K_BYTES);
-    tc_commit(bar.s_full(0));
+    issue_qk<C>(tS0, sQ, sK + ks * C::K_BYTES, leader);
+    tc_commit_p(leader, bar.s_full(0));
     if (two_kv) {
-      tc_commit(bar.k_empty(ks));
+      tc_commit_p(leader, bar.k_empty(ks));
       ++kcnt;
-      if (!(ok = wait_ring(bar.k_full(0), kcnt, C::NK, abort, p.timeout_ns, ks))) break;
+      if (!(ok = wait_ring(bar.k_full(0), kcnt, C::NK, abort, tmo, ks))) break;
     }
     if (two) {
-      issue_qk<C>(tS1, sQ + C::Q_BYTES, sK + ks * C::K_BYTES);
-      tc_commit(bar.s_full(1));
+      issue_qk<C>(tS1, sQ + C::Q_BYTES, sK + ks * C::K_BYTES, leader);
+      tc_commit_p(leader, bar.s_full(1));
     }
-    tc_commit(bar.k_empty(ks));
+    tc_commit_p(leader, bar.k_empty(ks));
     ++kcnt;
     if (it.nb == 1) {
-      tc_commit(bar.q_empty(0));
-      if (two) tc_commit(bar.q_empty(1));
+      tc_commit_p(leader, bar.q_empty(0));
+      if (two) tc_commit_p(leader, bar.q_empty(1));
     }
     for (int32_t g = 0; g < it.nb && ok; ++g) {
       const bool more = g + 1 < it.nb;
-      // ---- tile 0
-      if (!(ok = mbar_wait(bar.p_full(0), p0 & 1, abort, p.timeout_ns))) break;
+      // ---- tile 0: P_0(g), V(g) and K(g+1)
+      const uint32_t vs0 = vcnt % C::NV, ks0 = kcnt % C::NK;
+      if (!(ok = wait_ready(bar.p_full(0), p0 & 1u, true, bar.v_full(vs0), (vcnt / C::NV) & 1u, more,
+                            bar.k_full(ks0), (kcnt / C::NK) & 1u, abort, tmo)))
+        break;
       ++p0;
       tc_fence_after();
-      uint32_t vs0;
-      if (!(ok = wait_ring(bar.v_full(0), vcnt, C::NV, abort, p.timeout_ns, vs0))) break;
-      issue_pv<C, BK>(tO0, tS0, sV + vs0 * C::V_BYTES, g == 0);
-      if (!more) tc_commit(bar.o_done(0));
+      issue_pv<C, BK>(tO0, tS0, sV + vs0 * C::V_BYTES, g == 0, leader);
+      if (!more) tc_commit_p(leader, bar.o_done(0));
       if (!two || two_kv) {
-        tc_commit(bar.v_empty(vs0));
+        tc_commit_p(leader, bar.v_empty(vs0));
         ++vcnt;
       }
-      uint32_t ks0 = 0;
       if (more) {
-        if (!(ok = wait_ring(bar.k_full(0), kcnt, C::NK, abort, p.timeout_ns, ks0))) break;
-        issue_qk<C>(tS0, sQ, sK + ks0 * C::K_BYTES);
-        tc_commit(bar.s_full(0));
+        issue_qk<C>(tS0, sQ, sK + ks0 * C::K_BYTES, leader);
+        tc_commit_p(leader, bar.s_full(0));
         if (!two || two_kv) {
-          tc_commit(bar.k_empty(ks0));
+          tc_commit_p(leader, bar.k_empty(ks0));
           ++kcnt;
         }
-        if (g + 2 == it.nb) tc_commit(bar.q_empty(0));
+        if (g + 2 == it.nb) tc_commit_p(leader, bar.q_empty(0));
       }
       if (!two) continue;
-      // ---- tile 1
-      if (!(ok = mbar_wait(bar.p_full(1), p1 & 1, abort, p.timeout_ns))) break;
+      // ---- tile 1: P_1(g) [and its own V(g), K(g+1)]
+      const uint32_t vs1 = two_kv ? vcnt % C::NV : vs0, ks1 = two_kv ? kcnt % C::NK : ks0;
+      if (!(ok = wait_ready(bar.p_full(1), p1 & 1u, two_kv, bar.v_full(vs1), (vcnt / C::NV) & 1u,
+                            two_kv && more, bar.k_full(ks1), (kcnt / C::NK) & 1u, abort, tmo)))
+        break;
       ++p1;
       tc_fence_after();
-      uint32_t vs1 = vs0;
-      if (two_kv && !(ok = wait_ring(bar.v_full(0), vcnt, C::NV, abort, p.timeout_ns, vs1))) break;
-      issue_pv<C, BK>(tO1, tS1, sV + vs1 * C::V_BYTES, g == 0);
-      if (!more) tc_commit(bar.o_done(1));
-      tc_commit(bar.v_empty(vs1));
+      issue_pv<C, BK>(tO1, tS1, sV + vs1 * C::V_BYTES, g == 0, leader);
+      if (!more) tc_commit_p(leader, bar.o_done(1));
+      tc_commit_p(leader, bar.v_empty(vs1));
       ++vcnt;
       if (more) {
-        uint32_t ks1 = ks0;
-        if (two_kv && !(ok = wait_ring(bar.k_full(0), kcnt, C::NK, abort, p.timeout_ns, ks1))) break;
-        issue_qk<C>(tS1, sQ + C::Q_BYTES, sK + ks1 * C::K_BYTES);
-        tc_commit(bar.s_full(1));
-        tc_commit(bar.k_empty(ks1));
+        issue_qk<C>(tS1, sQ + C::Q_BYTES, sK + ks1 * C::K_BYTES, leader);
+        tc_commit_p(leader, bar.s_full(1));
+        tc_commit_p(leader, bar.k_empty(ks1));
         ++kcnt;
-        if (g + 2 == it.nb) tc_commit(bar.q_empty(1));
+        if (g + 2 == it.nb) tc_commit_p(leader, bar.q_empty(1));
       }
     }
   }
-  if (!ok) raise_error(p, abort, SPLASH_DEV_TIMEOUT_MMA);
+  if (!ok && leader) raise_error(p, abort, SPLASH_DEV_TIMEOUT_MMA);
   // drain: every MMA issued by this thread has completed
-  tc_commit(bar.drain());
-  if (!mbar_wait_drain(bar.drain(), 0, p.timeout_ns)) atomicOr(p.err, SPLASH_DEV_TIMEOUT_DRAIN);
+  tc_commit_p(leader, bar.drain());
+  if (!mbar_wait_drain(bar.drain(), 0, tmo) && leader) atomicOr(p.err, SPLASH_DEV_TIMEOUT_DRAIN);
 }
 
 // Packed form of tanh_series_scaled for two scores.
@@ -679,11 +710,10 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   if (warp == kProducerWarp) {
     if (lane == 0) run_producer<C, BK>(p, &tmQ, &tmK, &tmV, sQ, sK, sV, bar, abort);
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-    if (lane == 0) {
-      if (p.dual_issuer)
-        run_mma<C, BK>(p, tmem, sQ, sK, sV, bar, abort, warp - kMmaWarp);
-      else if (warp == kMmaWarp)
-        run_mma_pair<C, BK>(p, tmem, sQ, sK, sV, bar, abort);
+    if (p.dual_issuer) {
+      if (lane == 0) run_mma<C, BK>(p, tmem, sQ, sK, sV, bar, abort, warp - kMmaWarp);
+    } else if (warp == kMmaWarp) {
+      run_mma_pair<C, BK>(p, tmem, sQ, sK, sV, bar, abort, elect_one_sync());
     }
   }
   } else {
@@ -809,31 +839,37 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         // allowed key so far take the first one; the vote below is after
         // they reconverge)
         if (__any_sync(0xffffffffu, redo)) {
+          // rare: some lane's exponentials may have overflowed.  The warp
+          // reloads S (warp-collective) and every lane recomputes its row
+          // against its current reference (for the other lanes this gives
+          // the values they already have, up to rounding); nothing from the
+          // main path stays live across this branch.
           {
-            // rare: reload S (warp-collective) and redo this lane's row
+            uint32_t r[BK / 32][32];
+#pragma unroll
+            for (int c = 0; c < BK / 32; ++c) tmem_ld32(tS + 32u * c, r[c]);
+            tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < BK / 32; ++c) {
-              uint32_t r[32];
-              tmem_ld32(tS + 32u * c, r);
-              tmem_wait_ld();
-              reg_fence32(r);
-              if (redo) {
+              reg_fence32(r[c]);
 #pragma unroll
-                for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(r[x]);
-              }
-            }
-            if (redo) {
-              if (p.use_softcap) {
-#pragma unroll
-                for (int j = 0; j < BK; ++j) s[j] = p.cap_log2 * tanh_identity(s[j] * p.cap_inner);
-              }
-              if (need_mask) {
-#pragma unroll
-                for (int j = 0; j < BK; ++j) s[j] = ((bits[j >> 5] >> (j & 31)) & 1u) ? s[j] : -INFINITY;
-              }
-              sum = exp2_block<BK>(s, mul, m_ref);
+              for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(r[c][x]);
             }
           }
+          if (p.use_softcap) {
+#pragma unroll
+            for (int j = 0; j < BK; ++j) s[j] = p.cap_log2 * tanh_identity(s[j] * p.cap_inner);
+          }
+          if (need_mask) {
+            const uint32_t *src = p.pattern_bits + ((int64_t)mn * p.bq + row) * (BK / 32);
+#pragma unroll
+            for (int x = 0; x < BK / 32; ++x) {
+              const uint32_t b = (partial && row_valid) ? __ldg(src + x) : (row_valid ? 0xffffffffu : 0u);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) s[x * 32 + j] = ((b >> j) & 1u) ? s[x * 32 + j] : -INFINITY;
+            }
+          }
+          sum = exp2_block<BK>(s, mul, m_ref == -INFINITY ? 0.f : m_ref);
         }
         // P (bf16 pairs) into the first BK/2 columns of S_t, 32 columns per store
 #pragma unroll

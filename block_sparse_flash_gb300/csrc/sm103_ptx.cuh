@@ -58,6 +58,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// Tests two (three) barrier phases with the try_waits issued back to back, so
+// that their latencies overlap; true only when every phase has completed.
+__device__ __forceinline__ bool mbar_try_wait2(uint32_t b0, uint32_t ph0, uint32_t b1, uint32_t ph1) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p0, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p1, [%3], %4;\n\t"
+      "and.pred p0, p0, p1;\n\t"
+      "selp.b32 %0, 1, 0, p0;\n\t}"
+      : "=r"(done)
+      : "r"(b0), "r"(ph0), "r"(b1), "r"(ph1)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ bool mbar_try_wait3(uint32_t b0, uint32_t ph0, uint32_t b1, uint32_t ph1,
+                                               uint32_t b2, uint32_t ph2) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p0, p1, p2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p0, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p1, [%3], %4;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p2, [%5], %6;\n\t"
+      "and.pred p0, p0, p1;\n\t"
+      "and.pred p0, p0, p2;\n\t"
+      "selp.b32 %0, 1, 0, p0;\n\t}"
+      : "=r"(done)
+      : "r"(b0), "r"(ph0), "r"(b1), "r"(ph1), "r"(b2), "r"(ph2)
+      : "memory");
+  return done != 0;
+}
+
 // Waits until the phase of parity `parity` of the barrier has completed.
 // Bounded: gives up (returns false) once `timeout_ns` of wall-clock time has
 // passed or another role of the CTA has raised *abort.  Never traps.
@@ -131,26 +163,78 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                : "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16 (bf16 in, f32 accumulate).
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16 (bf16 in, f32
+// accumulate).  Each shared-memory descriptor is given as its two 32-bit
+// halves (sdesc_lo / sdesc_hi_sw128), so that an offset inside a tile is one
+// 32-bit add on the low half.  No "memory" clobber: the MMA reads only shared
+// and tensor memory that mbarrier waits (asm volatile, ordered) guard.
+__device__ __forceinline__ void mma_ss_lh(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                          uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %2};\n\t"
+      "mov.b64 db, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate));
 }
 
 // D[tmem] (+)= A[tmem] * B[smem desc], A read from tensor memory.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
+__device__ __forceinline__ void mma_ts_lh(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate));
+}
+
+// Forms for an issuer that runs as a whole, converged warp: every lane
+// executes the instruction with the same operands and only the lane with
+// `pred` != 0 issues it.  Issuing from a converged warp is several times
+// cheaper per MMA than issuing from one lane of a diverged warp.
+__device__ __forceinline__ void mma_ss_lhp(uint32_t pred, uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                           uint32_t b_lo, uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 e, %7, 0;\n\t"
+      "mov.b64 da, {%1, %2};\n\t"
+      "mov.b64 db, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate), "r"(pred));
+}
+
+__device__ __forceinline__ void mma_ts_lhp(uint32_t pred, uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                           uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 db;\n\t"
+      "setp.ne.b32 e, %6, 0;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate), "r"(pred));
+}
+
+__device__ __forceinline__ void tc_commit_p(uint32_t pred, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "setp.ne.b32 e, %1, 0;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+      "r"(pred)
       : "memory");
+}
+
+// 1 in exactly one lane of the converged warp, 0 in the others.
+__device__ __forceinline__ uint32_t elect_one_sync() {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "selp.b32 %0, 1, 0, e;\n\t}"
+      : "=r"(r));
+  return r;
 }
 
 // Instruction descriptor, kind::f16 with f32 accumulation and bf16 A/B:
@@ -162,19 +246,21 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// Shared-memory matrix descriptor with 128-byte swizzling:
+// Shared-memory matrix descriptor with 128-byte swizzling (64 bits):
 //   bits 0-13 start address >> 4, 16-29 leading byte offset >> 4,
 //   32-45 stride byte offset >> 4, 46-47 version (1), 61-63 layout (2 = 128B).
 // K-major operands: 8-row groups of 128-byte rows, SBO = 1024, LBO unused.
 // MN-major operands: LBO = distance between 64-element MN chunks, SBO =
 // distance between groups of 8 K rows (1024).
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-  d |= 1ull << 46;
-  d |= 2ull << 61;
-  return d;
+// Low half: start address >> 4 (shared memory addresses stay below 2^18, so
+// adding a tile offset never carries out of the field) and LBO >> 4.
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+// High half: SBO >> 4, version 1 (bit 46 = bit 14 of the half), layout 2
+// (bits 61-63 = bits 29-31 of the half).
+__host__ __device__ constexpr uint32_t sdesc_hi_sw128(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
 }
 
 // 32 lanes x 32 columns of 32-bit TMEM words: thread t of the warp receives
