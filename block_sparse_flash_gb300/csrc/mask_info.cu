@@ -22,6 +22,9 @@
 //                    attention kernel)
 //      (host wait: read A, A_p, P)
 //      materialize   partial_mask_blocks (bytes) and their bit-packed copy
+// Band-only masks (no segment IDs) take the classes in closed form, need no
+// host wait (the pattern count has a bound), and small tables run the whole
+// pipeline as one single-CTA kernel (build_small_kernel).
 #include <algorithm>
 #include <climits>
 
@@ -71,6 +74,34 @@ __device__ __forceinline__ int32_t q_segment(const DevMask &m, int32_t bm, int64
   return m.qseg ? m.qseg[(int64_t)bm * m.Lq + i] : 0;
 }
 
+// The band part in closed form: key j is allowed for query i iff
+// i - W <= j <= i + A, with A = 0 for causal (and min with the right window)
+// and W the left window; an unbounded side is kBandInf.
+constexpr int64_t kBandInf = (int64_t)1 << 60;
+
+__device__ __forceinline__ void band_limits(const DevMask &m, int64_t &A, int64_t &W) {
+  A = kBandInf;
+  if (m.causal) A = 0;
+  if (m.wr >= 0) A = min(A, m.wr);
+  W = m.wl >= 0 ? m.wl : kBandInf;
+}
+
+// Class of block (r, c) under the band alone (0 empty, 1 partial, 2 full).
+// Rows i in [r0, r1] and keys j in [c0, c1]: the block holds an allowed pair
+// iff some row i has i + A >= c0 and i - W <= c1; it is full iff every row has
+// lo(i) = max(c0, i - W) = c0 and hi(i) = min(c1, i + A) = c1, i.e. iff
+// r1 - W <= c0 and r0 + A >= c1 (lo and hi are nondecreasing in i).
+__device__ __forceinline__ int band_block_class(const DevMask &m, int64_t A, int64_t W, int64_t r, int64_t c) {
+  const int64_t r0 = r * m.bq, r1 = r0 + m.bq - 1, c0 = c * m.bk, c1 = c0 + m.bk - 1;
+  if (max(r0, c0 - A) > min(r1, c1 + W)) return 0;
+  return (r1 - W <= c0 && r0 + A >= c1) ? 2 : 1;
+}
+
+// Allowed keys of query i under the band alone.
+__device__ __forceinline__ int64_t band_row_count(const DevMask &m, int64_t A, int64_t W, int64_t i) {
+  return max((int64_t)0, min(m.Lk - 1, i + A) - max((int64_t)0, i - W) + 1);
+}
+
 // ---------------------------------------------------------------- K1
 __global__ void seg_summary_kernel(DevMask m, int32_t *qsum, int32_t *kvsum) {
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -112,7 +143,17 @@ classify_kernel(DevMask m, const int32_t *qsum, const int32_t *kvsum, int8_t *bl
   const int64_t row = (int64_t)bm * m.nq + r;
   int64_t cnt = 0;
   int cls = 0;
-  if (c < m.nk) {
+  if (m.qseg == nullptr) {
+    // band only: classes in closed form; the allowed pairs are counted per
+    // query row by the first CTA of the row (cnt is then a row count)
+    int64_t A, W;
+    band_limits(m, A, W);
+    if (c < m.nk) {
+      cls = band_block_class(m, A, W, r, c);
+      block_mask[row * m.nk + c] = (int8_t)cls;
+    }
+    if (blockIdx.x == 0 && (int)threadIdx.x < m.bq) cnt = band_row_count(m, A, W, r * m.bq + threadIdx.x);
+  } else if (c < m.nk) {
     const int64_t c0 = c * m.bk, c1 = c0 + m.bk - 1;
     for (int32_t di = 0; di < m.bq; ++di) {
       int64_t lo, hi;
@@ -283,26 +324,50 @@ constexpr uint64_t kHashPrime = 0x100000001b3ull;
 
 __device__ __forceinline__ uint64_t hash_step(uint64_t h, uint64_t x) { return (h ^ x) * kHashPrime; }
 
+// Content hash of a partial block: an FNV hash per row (over the row's mask
+// words), mixed with the row index by the splitmix64 finalizer (Steele, Lea
+// and Flood, 2014) and summed over the rows.  A sum reduces in parallel (a
+// sequential fold over 128 rows costs ~10k cycles); equal contents give equal
+// hashes, and the hash only pre-filters the exact comparison.
+__device__ __forceinline__ uint64_t row_hash_term(uint64_t rowh, int32_t di) {
+  uint64_t z = rowh + (uint64_t)(di + 1) * 0x9e3779b97f4a7c15ull;
+  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+  z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+  return z ^ (z >> 31);
+}
+
+__device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
+  for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
 // One CTA (bq threads, one per query row) per partial block, grid-stride.
 __global__ void partial_hash_kernel(DevMask m, const unsigned long long *counters,
                                     const int32_t *part_row, const int32_t *part_col,
                                     uint64_t *part_hash) {
-  __shared__ uint64_t rowh[128];
+  __shared__ uint64_t wsum[4];
   const int64_t Ap = (int64_t)counters[1];
   const int di = threadIdx.x;
   for (int64_t k = blockIdx.x; k < Ap; k += gridDim.x) {
     const int64_t row = part_row[k];
     const int32_t bm = (int32_t)(row / m.nq);
     const int64_t r = row % m.nq, c = part_col[k];
+    if (m.qseg == nullptr) {
+      // band only: the diagonal offset identifies the content exactly (see
+      // build_small_kernel), and serves as the "hash"
+      if (di == 0) part_hash[k] = (uint64_t)(c * m.bk - r * m.bq);
+      continue;
+    }
     const int64_t i = r * m.bq + di;
     const int32_t sq = q_segment(m, bm, i);
     uint64_t h = kHashBasis;
     for (int32_t w = 0; w < m.bk / 32; ++w) h = hash_step(h, row_word(m, bm, i, sq, c * m.bk + w * 32));
-    rowh[di] = h;
+    const uint64_t t = warp_sum_u64(row_hash_term(h, di));
+    if ((di & 31) == 0) wsum[di >> 5] = t;
     __syncthreads();
     if (di == 0) {
-      uint64_t H = kHashBasis;
-      for (int32_t x = 0; x < m.bq; ++x) H = hash_step(H, rowh[x]);
+      uint64_t H = 0;
+      for (int x = 0; x < m.bq / 32; ++x) H += wsum[x];
       part_hash[k] = H;
     }
     __syncthreads();
@@ -338,6 +403,10 @@ __global__ void dedup_kernel(DevMask m, const unsigned long long *counters, cons
     for (int64_t base = 0; base < k && rep == k; base += 32) {
       const int64_t kp = base + lane;
       unsigned cand = __ballot_sync(0xffffffffu, kp < k && part_hash[kp] == h);
+      if (cand && m.qseg == nullptr) {
+        rep = base + __ffs(cand) - 1;  // equal diagonal offsets: equal content
+        break;
+      }
       while (cand) {
         const int t = __ffs(cand) - 1;
         cand &= cand - 1u;
@@ -457,6 +526,257 @@ row_order_kernel(int64_t R, int64_t nk, const int32_t *row_cnt, int32_t *hist, i
   }
 }
 
+// ---------------------------------------------------------------- fused build
+// The whole pipeline above in one CTA, for band-only masks (no segment IDs)
+// with a small table.  Every phase is a loop over the CTA's 1024 threads with
+// __syncthreads between phases; the block classes come from the closed form,
+// and every intermediate (row counts and offsets, row-order bins, the partial
+// blocks' coordinates, hashes, representatives and pattern indices) stays in
+// shared memory (global memory is only written: the table itself).  Partial
+// blocks are deduplicated by their diagonal offset d = c*bk - r*bq: under a
+// band mask the pattern of a block is {(i', j'): L <= j' - i' <= U} with L, U
+// shifted by -d, and for partial blocks (neither empty nor full) the clipped
+// interval of diagonals is strictly monotone in d, so equal content <=> equal
+// d — the content comparison of the general pipeline is not needed.
+constexpr int kSmallThreads = 1024;
+constexpr int64_t kSmallMaxRows = 2048;      // R
+constexpr int64_t kSmallMaxCols = 2048;      // nk
+constexpr int64_t kSmallMaxBlocks = 65536;   // R * nk
+constexpr int64_t kSmallMaxPartials = 2048;  // bound on the partial blocks
+
+struct SmallOut {
+  int8_t *block_mask;
+  int32_t *row_ptr, *row_order;
+  int32_t *active_rows, *active_cols, *mask_next;
+  uint8_t *bounds_start, *bounds_end;
+  unsigned long long *counters;
+  uint32_t *pattern_bits;
+  uint8_t *patterns;
+  int64_t cap_patterns;
+  uint32_t *err;
+  int32_t max_partials;  // capacity of the shared partial arrays
+};
+
+// Dynamic shared memory of build_small_kernel for R rows, nk columns and up to
+// max_partials partial blocks.
+inline size_t small_smem_bytes(int64_t R, int64_t nk, int64_t max_partials) {
+  return sizeof(int32_t) * (size_t)(2 * R + 2 * (R + 1) + (nk + 1)) +
+         (sizeof(int64_t) + 5 * sizeof(int32_t)) * (size_t)max_partials + 64;
+}
+
+__global__ void __launch_bounds__(kSmallThreads) build_small_kernel(DevMask m, SmallOut o) {
+  extern __shared__ __align__(16) uint8_t s_dyn[];
+  const int64_t R = m.nq, nk = m.nk, PM = o.max_partials;
+  int64_t *s_pd = reinterpret_cast<int64_t *>(s_dyn);                      // [PM] diagonal offsets
+  int32_t *s_cnt = reinterpret_cast<int32_t *>(s_pd + PM);                // [R]
+  int32_t *s_pcnt = s_cnt + R;                                             // [R]
+  int32_t *s_rp = s_pcnt + R;                                              // [R+1]
+  int32_t *s_prp = s_rp + R + 1;                                           // [R+1]
+  int32_t *s_hist = s_prp + R + 1;                                         // [nk+1]
+  int32_t *s_prow = s_hist + nk + 1;                                       // [PM]
+  int32_t *s_pcol = s_prow + PM;                                           // [PM]
+  int32_t *s_pg = s_pcol + PM;                                             // [PM]
+  int32_t *s_prep = s_pg + PM;                                             // [PM]
+  int32_t *s_ppidx = s_prep + PM;                                          // [PM]
+  __shared__ int buf_a[33], buf_p[33], s_mx[32];
+  __shared__ unsigned long long s_allowed;
+  __shared__ int64_t s_tot[3];  // A, A_p, P
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int64_t A, W;
+  band_limits(m, A, W);
+
+  // classes, per-row counts, allowed pairs
+  for (int64_t x = tid; x < R; x += kSmallThreads) {
+    s_cnt[x] = 0;
+    s_pcnt[x] = 0;
+  }
+  if (tid == 0) s_allowed = 0;
+  __syncthreads();
+  const int32_t nk32 = (int32_t)nk, nb32 = (int32_t)(R * nk);
+  for (int32_t idx = tid; idx < nb32; idx += kSmallThreads) {
+    const int32_t r = idx / nk32, c = idx - r * nk32;
+    const int cls = band_block_class(m, A, W, r, c);
+    o.block_mask[idx] = (int8_t)cls;
+    if (cls != 0) atomicAdd(&s_cnt[r], 1);
+    if (cls == 1) atomicAdd(&s_pcnt[r], 1);
+  }
+  unsigned long long allowed = 0;
+  for (int64_t i = tid; i < m.Lq; i += kSmallThreads) allowed += (unsigned long long)band_row_count(m, A, W, i);
+  for (int off = 16; off; off >>= 1) allowed += __shfl_xor_sync(0xffffffffu, allowed, off);
+  if (lane == 0 && allowed) atomicAdd(&s_allowed, allowed);
+  __syncthreads();
+
+  // row_ptr (CSR), partial offsets and the longest row
+  int carry_a = 0, carry_p = 0, mx = 0;
+  for (int64_t base = 0; base < R; base += kSmallThreads) {
+    const int64_t x = base + tid;
+    const int a = x < R ? s_cnt[x] : 0, pc = x < R ? s_pcnt[x] : 0;
+    mx = max(mx, a);
+    int ta, tp;
+    const int ea = block_excl_scan(a, ta, buf_a);
+    const int ep = block_excl_scan(pc, tp, buf_p);
+    if (x < R) {
+      s_rp[x] = carry_a + ea;
+      s_prp[x] = carry_p + ep;
+      o.row_ptr[x] = carry_a + ea;
+    }
+    carry_a += ta;
+    carry_p += tp;
+  }
+  for (int off = 16; off; off >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if (lane == 0) s_mx[warp] = mx;
+  for (int64_t b = tid; b <= nk; b += kSmallThreads) s_hist[b] = 0;
+  __syncthreads();
+  if (tid == 0) {
+    int t = 0;
+    for (int x = 0; x < kSmallThreads / 32; ++x) t = max(t, s_mx[x]);
+    s_rp[R] = carry_a;
+    s_prp[R] = carry_p;
+    o.row_ptr[R] = carry_a;
+    o.counters[0] = (unsigned long long)carry_a;
+    o.counters[1] = (unsigned long long)carry_p;
+    o.counters[3] = s_allowed;
+    o.counters[4] = (unsigned long long)t;
+    s_tot[0] = carry_a;
+    s_tot[1] = carry_p;
+  }
+  // row order: bins of a stable counting sort, descending counts first
+  for (int64_t x = tid; x < R; x += kSmallThreads) atomicAdd(&s_hist[s_cnt[x]], 1);
+  __syncthreads();
+  int carry = 0;
+  for (int64_t base = 0; base <= nk; base += kSmallThreads) {
+    const int64_t x = base + tid;
+    const int64_t bin = nk - x;
+    const int h = x <= nk ? s_hist[bin] : 0;
+    int tot;
+    const int ex = block_excl_scan(h, tot, buf_a);
+    if (x <= nk) s_hist[bin] = carry + ex;
+    carry += tot;
+  }
+  __syncthreads();
+  const int64_t Ap = s_tot[1];
+  if (Ap > PM) {
+    // cannot happen (the host bounds the partial blocks); report, do nothing
+    if (tid == 0 && o.err) atomicOr(o.err, SPLASH_DEV_BAD_TABLE);
+    return;
+  }
+  if (warp == 0) {
+    // placement in row order (ties in ascending row order)
+    const unsigned lt = (1u << lane) - 1u;
+    for (int64_t base = 0; base < R; base += 32) {
+      const int64_t x = base + lane;
+      const bool valid = x < R;
+      const int c = valid ? s_cnt[x] : -1 - lane;
+      const unsigned peers = __match_any_sync(0xffffffffu, c);
+      const int pos = valid ? s_hist[c] + __popc(peers & lt) : 0;
+      __syncwarp();
+      if (valid) {
+        o.row_order[pos] = (int32_t)x;
+        if ((peers & lt) == 0) s_hist[c] += __popc(peers);
+      }
+      __syncwarp();
+    }
+  } else {
+    // active lists (warps 1..31, one row at a time); classes recomputed
+    const unsigned lt = (1u << lane) - 1u;
+    for (int64_t row = warp - 1; row < R; row += kSmallThreads / 32 - 1) {
+      const int32_t g0 = s_rp[row], gend = s_rp[row + 1];
+      int32_t g = g0, k = s_prp[row];
+      for (int64_t cb = 0; cb < nk; cb += 32) {
+        const int64_t c = cb + lane;
+        const int cls = c < nk ? band_block_class(m, A, W, row, c) : 0;
+        const unsigned act = __ballot_sync(0xffffffffu, cls != 0);
+        const unsigned par = __ballot_sync(0xffffffffu, cls == 1);
+        if (cls != 0) {
+          const int32_t pos = g + __popc(act & lt);
+          o.active_rows[pos] = (int32_t)row;
+          o.active_cols[pos] = (int32_t)c;
+          o.bounds_start[pos] = (uint8_t)(pos == g0);
+          o.bounds_end[pos] = (uint8_t)(pos == gend - 1);
+          if (cls == 1) {
+            const int32_t kk = k + __popc(par & lt);
+            s_prow[kk] = (int32_t)row;
+            s_pcol[kk] = (int32_t)c;
+            s_pg[kk] = pos;
+            s_pd[kk] = c * m.bk - row * m.bq;
+          } else {
+            o.mask_next[pos] = -1;
+          }
+        }
+        g += __popc(act);
+        k += __popc(par);
+      }
+    }
+  }
+  __syncthreads();
+
+  // first partial with the same diagonal offset (one warp per partial)
+  for (int32_t k = warp; k < (int32_t)Ap; k += kSmallThreads / 32) {
+    const int64_t d = s_pd[k];
+    int32_t rep = k;
+    for (int32_t base = 0; base < k; base += 32) {
+      const int32_t kp = base + lane;
+      const unsigned hit = __ballot_sync(0xffffffffu, kp < k && s_pd[kp] == d);
+      if (hit) {
+        rep = base + __ffs(hit) - 1;
+        break;
+      }
+    }
+    if (lane == 0) s_prep[k] = rep;
+  }
+  __syncthreads();
+  // pattern indices of the first occurrences
+  carry = 0;
+  for (int64_t base = 0; base < Ap; base += kSmallThreads) {
+    const int64_t k = base + tid;
+    const int f = (k < Ap && s_prep[k] == k) ? 1 : 0;
+    int tot;
+    const int ex = block_excl_scan(f, tot, buf_a);
+    if (k < Ap) s_ppidx[k] = carry + ex;
+    carry += tot;
+  }
+  if (tid == 0) {
+    o.counters[2] = (unsigned long long)carry;
+    s_tot[2] = carry;
+  }
+  __syncthreads();
+  // mask_next of the partial blocks, then the pattern list (partial index of
+  // pattern u) in the place of s_pg, which is not read again
+  for (int64_t k = tid; k < Ap; k += kSmallThreads) {
+    const int32_t rep = s_prep[k];
+    o.mask_next[s_pg[k]] = s_ppidx[rep];
+  }
+  __syncthreads();
+  for (int64_t k = tid; k < Ap; k += kSmallThreads)
+    if (s_prep[k] == k) s_pg[s_ppidx[k]] = (int32_t)k;  // s_pg becomes the pattern list
+  __syncthreads();
+  // partial_mask_blocks and their bit-packed copy (groups of bq threads)
+  int64_t P = s_tot[2];
+  if (P > o.cap_patterns) {
+    if (tid == 0 && o.err) atomicOr(o.err, SPLASH_DEV_BAD_TABLE);
+    P = o.cap_patterns;
+  }
+  const int32_t words = m.bk / 32;
+  const int G = kSmallThreads / m.bq, grp = tid / m.bq, di = tid - grp * m.bq;
+  for (int64_t u0 = 0; u0 < P; u0 += G) {
+    const int64_t u = u0 + grp;
+    if (u >= P) break;
+    const int64_t k = s_pg[u];
+    const int64_t i = (int64_t)s_prow[k] * m.bq + di, c = s_pcol[k];
+    uint32_t *bits = o.pattern_bits + (u * m.bq + di) * words;
+    uchar4 *bytes = reinterpret_cast<uchar4 *>(o.patterns + (u * m.bq + di) * m.bk);
+    for (int32_t w = 0; w < words; ++w) {
+      const uint32_t word = row_word(m, 0, i, 0, c * m.bk + w * 32);
+      bits[w] = word;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const uint32_t nib = word >> (4 * t);
+        bytes[w * 8 + t] = make_uchar4(nib & 1u, (nib >> 1) & 1u, (nib >> 2) & 1u, (nib >> 3) & 1u);
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- host side
 template <typename T>
 cudaError_t grow(T *&p, int64_t have, int64_t need) {
@@ -570,6 +890,69 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
   // a previous asynchronous build (possibly on another stream) copies its
   // totals into h_counters: keep that copy ordered before this build's
   if (mi->counts_pending && mi->counts_ready) SPLASH_CUDA_TRY(cudaStreamWaitEvent(stream, mi->counts_ready, 0));
+
+  uint32_t *err = splash_device_error_word(mi->device);
+  // -- pattern buffer.  Without segment IDs a q-block row has at most
+  // 2 * (ceil((bq-1)/bk) + 1) partial blocks (a block is partial only if one of
+  // the two band edges sweeps through it), so P has a bound known here and the
+  // build runs without a host wait; the totals are read lazily.  With segment
+  // IDs the build waits once for P.
+  const int64_t per_row = 2 * ((bq - 1 + bk - 1) / bk + 1);
+  const int64_t p_bound = std::min<int64_t>(R * per_row, NB);
+  const bool async = !seg && p_bound * (int64_t)bq * bk <= ((int64_t)256 << 20);
+  auto reserve_patterns = [&](int64_t P_cap) -> splash_status {
+    if (P_cap <= 0 || mi->cap_patterns >= P_cap) return SPLASH_OK;
+    if (mi->patterns) cudaFree(mi->patterns);
+    if (mi->pattern_bits) cudaFree(mi->pattern_bits);
+    mi->patterns = nullptr;
+    mi->pattern_bits = nullptr;
+    mi->cap_patterns = 0;
+    splash_status s2;
+    if ((s2 = map_alloc(cudaMalloc(&mi->patterns, (size_t)P_cap * bq * bk))) != SPLASH_OK) return s2;
+    if ((s2 = map_alloc(cudaMalloc(&mi->pattern_bits, (size_t)P_cap * bq * (bk / 32) * 4))) != SPLASH_OK)
+      return s2;
+    mi->cap_patterns = P_cap;
+    return SPLASH_OK;
+  };
+  auto finish_async = [&]() -> splash_status {
+    SPLASH_CUDA_TRY(cudaMemcpyAsync(mi->h_counters, mi->counters, sizeof(unsigned long long) * 8,
+                                    cudaMemcpyDeviceToHost, stream));
+    if (mi->counts_ready == nullptr)
+      SPLASH_CUDA_TRY(cudaEventCreateWithFlags(&mi->counts_ready, cudaEventDisableTiming));
+    SPLASH_CUDA_TRY(cudaEventRecord(mi->counts_ready, stream));
+    mi->counts_pending = true;
+    return SPLASH_OK;
+  };
+
+  if (async && R <= kSmallMaxRows && nk <= kSmallMaxCols && NB <= kSmallMaxBlocks &&
+      p_bound <= kSmallMaxPartials) {
+    // small band-only table: the whole build is one single-CTA kernel
+    if ((st = reserve_patterns(p_bound)) != SPLASH_OK) return st;
+    SmallOut o;
+    o.block_mask = mi->block_mask;
+    o.row_ptr = mi->row_ptr;
+    o.row_order = mi->row_order;
+    o.active_rows = mi->active_rows;
+    o.active_cols = mi->active_cols;
+    o.mask_next = mi->mask_next;
+    o.bounds_start = mi->bounds_start;
+    o.bounds_end = mi->bounds_end;
+    o.counters = mi->counters;
+    o.pattern_bits = mi->pattern_bits;
+    o.patterns = mi->patterns;
+    o.cap_patterns = mi->cap_patterns;
+    o.err = err;
+    o.max_partials = (int32_t)p_bound;
+    const size_t smem = small_smem_bytes(R, nk, p_bound);
+    if (smem > 48 * 1024)
+      SPLASH_CUDA_TRY(cudaFuncSetAttribute(build_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)small_smem_bytes(kSmallMaxRows, kSmallMaxCols, kSmallMaxPartials)));
+    build_small_kernel<<<1, kSmallThreads, smem, stream>>>(m, o);
+    SPLASH_CUDA_TRY(cudaGetLastError());
+    splash_count_launches(1);
+    return finish_async();
+  }
+
   SPLASH_CUDA_TRY(cudaMemsetAsync(mi->row_cnt, 0, sizeof(int32_t) * R, stream));
   SPLASH_CUDA_TRY(cudaMemsetAsync(mi->row_pcnt, 0, sizeof(int32_t) * R, stream));
   SPLASH_CUDA_TRY(cudaMemsetAsync(mi->counters, 0, sizeof(unsigned long long) * 8, stream));
@@ -600,15 +983,6 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
   SPLASH_CUDA_TRY(cudaGetLastError());
   splash_count_launches(seg ? 10 : 9);
 
-  uint32_t *err = splash_device_error_word(mi->device);
-  // -- pattern buffer.  Without segment IDs a q-block row has at most
-  // 2 * (ceil((bq-1)/bk) + 1) partial blocks (a block is partial only if one of
-  // the two band edges sweeps through it), so P has a bound known here and the
-  // build runs without a host wait; the totals are read lazily.  With segment
-  // IDs the build waits once for P.
-  const int64_t per_row = 2 * ((bq - 1 + bk - 1) / bk + 1);
-  const int64_t p_bound = std::min<int64_t>(R * per_row, NB);
-  const bool async = !seg && p_bound * (int64_t)bq * bk <= ((int64_t)256 << 20);
   int64_t P_cap;
   if (async) {
     P_cap = p_bound;
@@ -618,17 +992,7 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
     SPLASH_CUDA_TRY(cudaStreamSynchronize(stream));
     P_cap = (int64_t)mi->h_counters[2];
   }
-  if (P_cap > 0 && mi->cap_patterns < P_cap) {
-    if (mi->patterns) cudaFree(mi->patterns);
-    if (mi->pattern_bits) cudaFree(mi->pattern_bits);
-    mi->patterns = nullptr;
-    mi->pattern_bits = nullptr;
-    mi->cap_patterns = 0;
-    if ((st = map_alloc(cudaMalloc(&mi->patterns, (size_t)P_cap * bq * bk))) != SPLASH_OK) return st;
-    if ((st = map_alloc(cudaMalloc(&mi->pattern_bits, (size_t)P_cap * bq * (bk / 32) * 4))) != SPLASH_OK)
-      return st;
-    mi->cap_patterns = P_cap;
-  }
+  if ((st = reserve_patterns(P_cap)) != SPLASH_OK) return st;
   if (P_cap > 0) {
     const unsigned grid = (unsigned)std::min<int64_t>(P_cap, async ? sms * 4 : 65535);
     materialize_kernel<<<grid, bq, 0, stream>>>(m, mi->counters, mi->cap_patterns, mi->rep_list, mi->part_row,
@@ -637,12 +1001,7 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
     splash_count_launches(1);
   }
   if (async) {
-    SPLASH_CUDA_TRY(cudaMemcpyAsync(mi->h_counters, mi->counters, sizeof(unsigned long long) * 8,
-                                    cudaMemcpyDeviceToHost, stream));
-    if (mi->counts_ready == nullptr)
-      SPLASH_CUDA_TRY(cudaEventCreateWithFlags(&mi->counts_ready, cudaEventDisableTiming));
-    SPLASH_CUDA_TRY(cudaEventRecord(mi->counts_ready, stream));
-    mi->counts_pending = true;
+    if ((st = finish_async()) != SPLASH_OK) return st;
   } else {
     mi->counts_pending = false;
     mi->num_active = (int64_t)mi->h_counters[0];

@@ -83,6 +83,28 @@ def test_fuzzed_masks_bit_exact(bsf, n, L, bq, bk, causal, wl, wr, kind, seed):
     assert_same(got, ref, f"case {n}")
 
 
+# Band-only masks (no segment IDs) are built either by one single-CTA kernel
+# (tables up to 2048 q-block rows, 2048 kv-blocks and 65536 blocks) or by the
+# multi-kernel pipeline; both take the block classes in closed form.  Shapes on
+# both sides of each limit, square and rectangular.
+BAND_CASES = [
+    # Lq, Lk, bq, bk, causal, wl, wr
+    (131072, 2048, 64, 64, True, -1, -1),      # single CTA: 2048 rows x 32 (row limit)
+    (2048, 131072, 128, 64, False, 700, 3000),  # single CTA: 16 rows x 2048 (column limit)
+    (16384, 16384, 64, 64, True, 4095, 0),      # single CTA: 256 x 256 = 65536 blocks
+    (16384, 16384, 64, 128, False, 100, 100),   # single CTA, bq != bk
+    (20480, 20480, 64, 64, True, -1, -1),       # multi-kernel: 320 x 320 blocks
+    (8192, 139264, 64, 64, True, 2000, -1),     # multi-kernel: 2176 kv-blocks
+    (3000 * 64, 128, 64, 64, False, 10, 10),    # multi-kernel: 3000 rows
+]
+
+
+@pytest.mark.parametrize("Lq,Lk,bq,bk,causal,wl,wr", BAND_CASES)
+def test_band_masks_both_build_paths(bsf, Lq, Lk, bq, bk, causal, wl, wr):
+    got, ref = gpu_and_oracle(bsf, causal, wl, wr, None, None, Lq, Lk, bq, bk)
+    assert_same(got, ref, f"{Lq}x{Lk} {bq}x{bk} causal={causal} window=({wl},{wr})")
+
+
 def test_rebuild_reuses_the_handle(bsf):
     seg = workloads.random_segment_ids(1, 1024, 5, 5, True).cuda()
     mi = bsf.build_mask_info(bsf.MaskSpec(True), 4096, 4096, 128, 128)
