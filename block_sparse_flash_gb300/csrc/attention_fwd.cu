@@ -50,16 +50,18 @@ namespace {
 
 constexpr int kThreads = 384;       // 12 warps = 3 warpgroups
 // Register split (setmaxnreg): the launch gives 384 x 168; the two softmax
-// warpgroups take 200 each and the producer / MMA warpgroup keeps 104:
-// 2*128*200 + 128*104 = 64512 = 384*168.
-constexpr int kSoftmaxRegs = 200;
-constexpr int kControlRegs = 104;
+// warpgroups take 192 each and the producer / MMA warpgroup keeps 120:
+// 2*128*192 + 128*120 = 64512 = 384*168.
+constexpr int kSoftmaxRegs = 192;
+constexpr int kControlRegs = 120;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Upper bound on a block row's sum of exponentials (2^64): reaching it moves
+// the row's reference (no overflow in P, l or O).
+constexpr float kPMax = 1.8446744e19f;
 
 template <int DQK, int DV, int BK>
 struct Cfg {
@@ -172,26 +174,20 @@ __device__ __forceinline__ float max_tree(const float (&v)[N]) {
 
 // tanh for the soft cap, two ways, both from the mathematics of tanh (not
 // from any library implementation):
-//  * |t| <= 0.25: the Maclaurin series t - t^3/3 + 2t^5/15 - 17t^7/315; the
-//    first omitted term, 62 t^9 / 2835, is below 8.4e-8 there;
+//  * |t| <= 0.25: t * (1 + u (c1 + c2 u)), u = t^2, with c1, c2 a minimax fit
+//    of tanh(t)/t on [0, 0.25] (Lawson-weighted least squares, q(0) = 1 held
+//    fixed); max relative error 4.8e-7, like the Maclaurin series to t^7
+//    (3.3e-7) with one multiply-add less;
 //  * otherwise the identity tanh|t| = 1 - 2 / (1 + e^(2|t|)) with the sign
 //    restored (absolute error ~1e-7 from ex2 / division rounding).
+constexpr float kTanhC1 = -0.33324610f;
+constexpr float kTanhC2 = 0.12877172f;
 constexpr float kTanhSeriesLimit = 0.25f;
 
 __device__ __forceinline__ float tanh_identity(float t) {
   const float a = fminf(fabsf(t), 16.f);  // tanh(16) rounds to 1 in fp32
   const float e = ex2_approx(2.8853900817779268f * a);  // e^(2a)
   return copysignf(1.f - __fdividef(2.f, e + 1.f), t);
-}
-
-// cap*log2e*tanh(s*k) by the series, with k = scale/cap and kc = cap*log2e*k.
-__device__ __forceinline__ float tanh_series_scaled(float s, float k, float kc) {
-  const float a = s * k;
-  const float t2 = a * a;
-  float poly = fmaf(t2, -17.f / 315.f, 2.f / 15.f);
-  poly = fmaf(poly, t2, -1.f / 3.f);
-  const float q = fmaf(t2, poly, 1.f);
-  return (s * kc) * q;
 }
 
 // Shared-memory addresses of the CTA's mbarriers:
@@ -603,14 +599,13 @@ __device__ __forceinline__ void run_mma_pair(const FwdParams &p, uint32_t tmem, 
   if (!mbar_wait_drain(bar.drain(), 0, tmo) && leader) atomicOr(p.err, SPLASH_DEV_TIMEOUT_DRAIN);
 }
 
-// Packed form of tanh_series_scaled for two scores.
-__device__ __forceinline__ f32x2 tanh_series_scaled2(f32x2 s, f32x2 k, f32x2 kc) {
+// tanh(s*k) for two scores by the series (|s*k| <= 0.25), packed fp32x2:
+// a = s*k, then a + a*u*(c1 + c2*u) with u = a*a.
+__device__ __forceinline__ f32x2 tanh_series2(f32x2 s, f32x2 k) {
   const f32x2 a = fmul2(s, k);
-  const f32x2 t2 = fmul2(a, a);
-  f32x2 poly = ffma2(t2, f32x2{-17.f / 315.f, -17.f / 315.f}, f32x2{2.f / 15.f, 2.f / 15.f});
-  poly = ffma2(poly, t2, f32x2{-1.f / 3.f, -1.f / 3.f});
-  const f32x2 q = ffma2(t2, poly, f32x2{1.f, 1.f});
-  return fmul2(fmul2(s, kc), q);
+  const f32x2 u = fmul2(a, a);
+  const f32x2 p1 = ffma2(u, f32x2{kTanhC2, kTanhC2}, f32x2{kTanhC1, kTanhC1});
+  return ffma2(fmul2(a, u), p1, a);
 }
 
 // s_j <- 2^(s_j * mul - sub) in place (packed argument), returns the row sum
@@ -626,27 +621,6 @@ __device__ __forceinline__ float exp2_block(float (&s)[N], float mul, float sub)
     s[j + 1] = ex2_approx(a.y);
     acc[(j >> 1) & 3] = fadd2(acc[(j >> 1) & 3], f32x2{s[j], s[j + 1]});
   }
-  const f32x2 t = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
-  return t.x + t.y;
-}
-
-// The same, also returning the maximum of the inputs in `mx`: the max rides
-// along the exponentials (whose special-function unit paces the loop) instead
-// of being a dense pass of its own.
-template <int N>
-__device__ __forceinline__ float exp2_block_max(float (&s)[N], float mul, float sub, float &mx) {
-  const f32x2 m2{mul, mul}, n2{-sub, -sub};
-  f32x2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-  for (int j = 0; j < N; j += 2) {
-    m[(j >> 1) & 3] = fmax3(m[(j >> 1) & 3], s[j], s[j + 1]);
-    const f32x2 a = ffma2(f32x2{s[j], s[j + 1]}, m2, n2);
-    s[j] = ex2_approx(a.x);
-    s[j + 1] = ex2_approx(a.y);
-    acc[(j >> 1) & 3] = fadd2(acc[(j >> 1) & 3], f32x2{s[j], s[j + 1]});
-  }
-  mx = fmax3(m[0], m[1], fmaxf(m[2], m[3]));
   const f32x2 t = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
   return t.x + t.y;
 }
@@ -679,7 +653,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       mbar_init(bar.q_full(t), 1);
       mbar_init(bar.q_empty(t), 1);
       mbar_init(bar.s_full(t), 1);
-      mbar_init(bar.p_full(t), 128);
+      mbar_init(bar.p_full(t), 4);  // the four warps of the tile's softmax
       mbar_init(bar.o_done(t), 1);
     }
     for (int s = 0; s < C::NK; ++s) {
@@ -775,10 +749,10 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(r[c][x]);
           }
         }
-        // s_j in log2 units: s*scale*log2e (folded into the exponent's FFMA
-        // through `mul`) or, with the soft cap, cap*log2e*tanh(s*scale/cap)
-        // computed here.  Masked entries become -inf.
-        const float mul = p.use_softcap ? 1.f : p.scale_log2;
+        // Scores in log2 units are s*mul: mul = scale*log2e, or with the soft
+        // cap s <- tanh(s*scale/cap) here and mul = cap*log2e (the exponent's
+        // FFMA applies it).  Masked entries become -inf.
+        const float mul = p.use_softcap ? p.cap_log2 : p.scale_log2;
         if (p.use_softcap) {
           float am[4];
 #pragma unroll
@@ -788,13 +762,12 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
           const float amax = fmax3(am[0], am[1], fmaxf(am[2], am[3])) * p.cap_inner;
           if (__any_sync(0xffffffffu, amax > kTanhSeriesLimit)) {
 #pragma unroll
-            for (int j = 0; j < BK; ++j) s[j] = p.cap_log2 * tanh_identity(s[j] * p.cap_inner);
+            for (int j = 0; j < BK; ++j) s[j] = tanh_identity(s[j] * p.cap_inner);
           } else {
             const f32x2 k2{p.cap_inner, p.cap_inner};
-            const f32x2 kc2{p.cap_log2 * p.cap_inner, p.cap_log2 * p.cap_inner};
 #pragma unroll
             for (int j = 0; j < BK; j += 2) {
-              const f32x2 r2 = tanh_series_scaled2(f32x2{s[j], s[j + 1]}, k2, kc2);
+              const f32x2 r2 = tanh_series2(f32x2{s[j], s[j + 1]}, k2);
               s[j] = r2.x;
               s[j + 1] = r2.y;
             }
@@ -804,46 +777,30 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
 #pragma unroll
           for (int j = 0; j < BK; ++j) s[j] = ((bits[j >> 5] >> (j & 31)) & 1u) ? s[j] : -INFINITY;
         }
+        // Exponentials against the row's running reference m_ref, which
+        // moves only (i) to the first allowed keys' maximum and (ii) when a
+        // block's sum of exponentials would reach 2^64 (then the block is
+        // recomputed against its own maximum): between those events the max
+        // is not needed at all.  P, l and O stay far from overflow (P < 2^64),
+        // and O / l is independent of the reference.
         float alpha = 1.f;
-        float sum;
-        bool redo = false;  // this lane's exponentials must be recomputed (rare)
-        if (m_ref == -INFINITY) {
-          // first block with an allowed key: the reference is this block's max
+        if (__any_sync(0xffffffffu, m_ref == -INFINITY)) {
+          // a row's first block with allowed keys: its reference is their max
           const float mx = max_tree<BK>(s) * mul;  // scale > 0
-          if (mx != -INFINITY) {
+          if (m_ref == -INFINITY && mx != -INFINITY) {
             alpha = 0.f;
             m_ref = mx;
           }
-          sum = exp2_block<BK>(s, mul, m_ref == -INFINITY ? 0.f : m_ref);
-        } else {
-          // exponentiate against the current reference while the block's max
-          // is reduced alongside; the reference moves only when the max grows
-          // by more than 2^8, and then the exponentials are rescaled
-          float mx;
-          sum = exp2_block_max<BK>(s, mul, m_ref, mx);
-          mx *= mul;
-          if (mx > m_ref + kRescaleThreshold) {
-            const float m_old = m_ref;
-            alpha = ex2_approx(m_old - mx);
-            m_ref = mx;
-            if (mx - m_old < 64.f) {
-#pragma unroll
-              for (int j = 0; j < BK; ++j) s[j] *= alpha;
-              sum *= alpha;
-            } else {
-              redo = true;  // the exponentials may have overflowed
-            }
-          }
         }
-        // (lanes of a warp can be in different branches above: rows with no
-        // allowed key so far take the first one; the vote below is after
-        // they reconverge)
+        float sum = exp2_block<BK>(s, mul, m_ref == -INFINITY ? 0.f : m_ref);
+        const bool redo = !(sum < kPMax);
         if (__any_sync(0xffffffffu, redo)) {
-          // rare: some lane's exponentials may have overflowed.  The warp
-          // reloads S (warp-collective) and every lane recomputes its row
-          // against its current reference (for the other lanes this gives
-          // the values they already have, up to rounding); nothing from the
-          // main path stays live across this branch.
+          // rare: exponentials above 2^64 for some lane.  The warp reloads S
+          // (warp-collective; P has not been written yet); those lanes move
+          // their reference to the block's maximum, and every lane
+          // recomputes its row (for the others this gives the values they
+          // already have, up to rounding); nothing from the main path stays
+          // live across this branch but the references.
           {
             uint32_t r[BK / 32][32];
 #pragma unroll
@@ -858,7 +815,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
           }
           if (p.use_softcap) {
 #pragma unroll
-            for (int j = 0; j < BK; ++j) s[j] = p.cap_log2 * tanh_identity(s[j] * p.cap_inner);
+            for (int j = 0; j < BK; ++j) s[j] = tanh_identity(s[j] * p.cap_inner);
           }
           if (need_mask) {
             const uint32_t *src = p.pattern_bits + ((int64_t)mn * p.bq + row) * (BK / 32);
@@ -868,6 +825,11 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
 #pragma unroll
               for (int j = 0; j < 32; ++j) s[x * 32 + j] = ((b >> j) & 1u) ? s[x * 32 + j] : -INFINITY;
             }
+          }
+          if (redo) {
+            const float mx = max_tree<BK>(s) * mul;
+            alpha *= ex2_approx(m_ref - mx);
+            m_ref = mx;
           }
           sum = exp2_block<BK>(s, mul, m_ref == -INFINITY ? 0.f : m_ref);
         }
@@ -896,7 +858,8 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar.p_full(t));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar.p_full(t));  // one arrival per warp
       }
       if (!ok) break;
       // ---- epilogue: O / l and the LSE
