@@ -78,10 +78,15 @@ struct Cfg {
   static constexpr int NV = (DQK >= 192) ? 1 : ((DQK >= 128) ? 2 : 4);
   static constexpr int TILES = 2 * Q_BYTES + NK * K_BYTES + NV * V_BYTES;
   static_assert(TILES <= TILE_BUDGET, "shared memory budget");
+  // O staging for the epilogue's TMA stores: per softmax warp, 32 rows x 64
+  // columns of bf16 (128B-swizzled), when it fits next to the tiles
+  static constexpr int STAGE_WARP = 32 * 128;
+  static constexpr bool STAGE = TILES + 8 * STAGE_WARP <= TILE_BUDGET;
+  static constexpr int STAGE_BYTES = STAGE ? 8 * STAGE_WARP : 0;
   // barriers: q_full[2] q_empty[2] k_full[NK] k_empty[NK] v_full[NV] v_empty[NV]
   //           s_full[2] p_full[2] o_done[2] drain
   static constexpr int NBAR = 2 + 2 + 2 * NK + 2 * NV + 2 + 2 + 2 + 1;
-  static constexpr int SMEM = 1024 + TILES + NBAR * 8 + 16;
+  static constexpr int SMEM = 1024 + TILES + STAGE_BYTES + NBAR * 8 + 16;
   static constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, BK, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, DV, true);
 };
@@ -628,7 +633,8 @@ __device__ __forceinline__ float exp2_block(float (&s)[N], float mul, float sub)
 template <int DQK, int DV, int BK>
 __global__ void __launch_bounds__(kThreads, 1)
 splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const FwdParams p) {
   using C = Cfg<DQK, DV, BK>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -636,10 +642,11 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   const uint32_t sQ = smem_u32(smem);
   const uint32_t sK = sQ + 2 * C::Q_BYTES;
   const uint32_t sV = sK + C::NK * C::K_BYTES;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::TILES);
+  const uint32_t sStage = sV + C::NV * C::V_BYTES;  // C::STAGE_BYTES of O staging
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::TILES + C::STAGE_BYTES);
   const Bars<C> bar{smem_u32(bars)};
-  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::TILES + C::NBAR * 8);
-  volatile int *abort = reinterpret_cast<volatile int *>(smem + C::TILES + C::NBAR * 8 + 4);
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::TILES + C::STAGE_BYTES + C::NBAR * 8);
+  volatile int *abort = reinterpret_cast<volatile int *>(smem + C::TILES + C::STAGE_BYTES + C::NBAR * 8 + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -672,6 +679,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    if (C::STAGE) tma_prefetch_desc(&tmO);
   }
   tc_fence_before();
   __syncthreads();
@@ -870,6 +878,49 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         tc_fence_after();
       }
       const float inv = l > 0.f ? 1.f / l : 0.f;
+      if (C::STAGE) {
+        // O rows to the warp's 128B-swizzled staging box (32 rows x 64
+        // columns), one TMA store per box: whole-line global writes instead
+        // of 32 rows' scattered pieces per store instruction
+        const uint32_t stage = sStage + (uint32_t)warp * C::STAGE_WARP;
+        const bool warp_rows = wq * 32 < p.bq;  // rows beyond bq belong to no output
+#pragma unroll
+        for (int hh = 0; hh < DV / 64; ++hh) {
+          uint32_t r0[32], r1[32];
+          if (it.nb > 0) {
+            tmem_ld32(tO + 64u * hh, r0);
+            tmem_ld32(tO + 64u * hh + 32u, r1);
+            tmem_wait_ld();
+            reg_fence32(r0);
+            reg_fence32(r1);
+          } else {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) r0[x] = r1[x] = 0u;
+          }
+          uint32_t o[32];
+#pragma unroll
+          for (int x = 0; x < 16; ++x) {
+            const f32x2 y0 = fmul2(f32x2{__uint_as_float(r0[2 * x]), __uint_as_float(r0[2 * x + 1])}, f32x2{inv, inv});
+            const f32x2 y1 = fmul2(f32x2{__uint_as_float(r1[2 * x]), __uint_as_float(r1[2 * x + 1])}, f32x2{inv, inv});
+            o[x] = pack_bf16x2(y0.x, y0.y);
+            o[16 + x] = pack_bf16x2(y1.x, y1.y);
+          }
+          if (warp_rows) {
+            if (lane == 0) bulk_wait_read_all();  // the previous box has been read
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              st_shared_v4(stage + (uint32_t)lane * 128u + (uint32_t)((j ^ (lane & 7)) * 16), o[4 * j], o[4 * j + 1],
+                           o[4 * j + 2], o[4 * j + 3]);
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmO, stage, 64 * hh, (int32_t)(orow - lane));
+              bulk_commit_group();
+            }
+          }
+        }
+      } else {
       __nv_bfloat16 *orow_ptr = p.out + orow * DV;
 #pragma unroll
       for (int c = 0; c < DV / 32; ++c) {
@@ -889,14 +940,16 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             const f32x2 y = fmul2(f32x2{__uint_as_float(r[2 * x]), __uint_as_float(r[2 * x + 1])}, f32x2{inv, inv});
             o[x] = pack_bf16x2(y.x, y.y);
           }
-          uint4 *dst = reinterpret_cast<uint4 *>(orow_ptr + c * 32);
-#pragma unroll
-          for (int x = 0; x < 4; ++x) dst[x] = make_uint4(o[4 * x], o[4 * x + 1], o[4 * x + 2], o[4 * x + 3]);
+          // two 32-byte stores (whole sectors) per 32 columns
+          st_global_v8(orow_ptr + c * 32, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
+          st_global_v8(orow_ptr + c * 32 + 16, o[8], o[9], o[10], o[11], o[12], o[13], o[14], o[15]);
         }
+      }
       }
       if (row_valid) p.lse[orow] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
     }
     if (!ok) raise_error(p, abort, SPLASH_DEV_TIMEOUT_SOFTMAX);
+    if (C::STAGE && lane == 0) bulk_wait_all();  // this warp's O stores have completed
   }
   }
 
@@ -954,11 +1007,13 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, 
 template <int DQK, int DV, int BK>
 splash_status launch(const void *q, const void *k, const void *v, const FwdParams &prm, cudaStream_t stream) {
   using C = Cfg<DQK, DV, BK>;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (!make_map(&tq, q, DQK, (uint64_t)prm.B * prm.Hq * prm.Lq, 128) ||
       !make_map(&tk, k, DQK, (uint64_t)prm.B * prm.Hkv * prm.Lk, BK) ||
-      !make_map(&tv, v, DV, (uint64_t)prm.B * prm.Hkv * prm.Lk, BK))
+      !make_map(&tv, v, DV, (uint64_t)prm.B * prm.Hkv * prm.Lk, BK) ||
+      (C::STAGE && !make_map(&to, prm.out, DV, (uint64_t)prm.B * prm.Hq * prm.Lq, 32)))
     return SPLASH_ERR_CUDA;
+  if (!C::STAGE) to = tq;  // unused
   static int configured_device = -1;
   int dev = 0;
   SPLASH_CUDA_TRY(cudaGetDevice(&dev));
@@ -971,7 +1026,7 @@ splash_status launch(const void *q, const void *k, const void *v, const FwdParam
   }
   const int64_t grid = prm.num_items < sms ? prm.num_items : sms;
   if (grid <= 0) return SPLASH_OK;
-  splash_fwd_kernel<DQK, DV, BK><<<(unsigned)grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, prm);
+  splash_fwd_kernel<DQK, DV, BK><<<(unsigned)grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, to, prm);
   SPLASH_CUDA_TRY(cudaGetLastError());
   splash_count_launches(1);
   return SPLASH_OK;
