@@ -43,6 +43,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--splits", type=int, default=1,
+                    help="split-KV forward with this many splits per row, then the LSE merge")
     return ap.parse_args(argv)
 
 
@@ -164,7 +166,8 @@ def oracle_sample_rate(w, inp, nrows, seed, nthreads=0):
     import numpy as np
     import oracle
     rng = np.random.default_rng(seed)
-    rows = np.sort(rng.choice(w.B * w.Hq * w.L, size=min(nrows, w.B * w.Hq * w.L), replace=False))
+    nq_rows = w.B * w.Hq * w.q_len
+    rows = np.sort(rng.choice(nq_rows, size=min(nrows, nq_rows), replace=False))
     seg = inp.segment_ids.numpy() if inp.segment_ids is not None else None
     spec = oracle.MaskSpec(w.causal, w.window_left, w.window_right, seg, seg)
     nth = nthreads or oracle.default_threads()
@@ -174,8 +177,8 @@ def oracle_sample_rate(w, inp, nrows, seed, nthreads=0):
     # allowed keys of each sampled row, counted from the mask definition: the
     # band [lo, hi] of the causal / window part, intersected with the row's
     # document when segment IDs are given (contiguous documents)
-    i = (rows % w.L).astype(np.int64)
-    b = (rows // (w.Hq * w.L)).astype(np.int64)
+    i = (rows % w.q_len).astype(np.int64)
+    b = (rows // (w.Hq * w.q_len)).astype(np.int64)
     lo = np.maximum(0, i - w.window_left) if w.window_left >= 0 else np.zeros_like(i)
     hi = i.copy() if w.causal else np.full_like(i, w.L - 1)
     if w.window_right >= 0:
@@ -198,7 +201,7 @@ def oracle_sample_rate(w, inp, nrows, seed, nthreads=0):
 def cpu_baseline(w, inp, target_s=12.0):
     flop, dt, nth, n = oracle_sample_rate(w, inp, 256, 7)
     rate = n / max(dt, 1e-6)
-    nrows = int(min(w.B * w.Hq * w.L, max(256, rate * target_s)))
+    nrows = int(min(w.B * w.Hq * w.q_len, max(256, rate * target_s)))
     flop, dt, nth, n = oracle_sample_rate(w, inp, nrows, 8)
     return {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": nth, "kind": "oracle",
             "sample": f"{n} seeded random query rows of the workload (all heads/batches), f64 oracle, "
@@ -232,19 +235,32 @@ def run_ours(args):
     q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
     seg = inp.segment_ids.to(dev) if inp.segment_ids is not None else None
     spec = bsf.MaskSpec(w.causal, w.window_left, w.window_right, seg, seg)
-    mi = bsf.build_mask_info(spec, w.L, w.L, w.bq, w.bk)
+    mi = bsf.build_mask_info(spec, w.q_len, w.L, w.bq, w.bk)
     counts = mi.counts()
     batch_rows = mi.shape()["batch_rows"]
     useful, executed = flop_counts(w, counts, batch_rows)
-    out = torch.empty((w.B, w.Hq, w.L, w.dv), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((w.B, w.Hq, w.L), dtype=torch.float32, device=dev)
+    out = torch.empty((w.B, w.Hq, w.q_len, w.dv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Hq, w.q_len), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    def step(attn_events=None):
-        mi.rebuild(spec, w.L, w.L, w.bq, w.bk)
+    S = args.splits
+    if S > 1:
+        o_part = torch.empty((S, w.B, w.Hq, w.q_len, w.dv), dtype=torch.float32, device=dev)
+        lse_part = torch.empty((S, w.B, w.Hq, w.q_len), dtype=torch.float32, device=dev)
+
+    def step(attn_events=None, merge_events=None):
+        mi.rebuild(spec, w.q_len, w.L, w.bq, w.bk)
         if attn_events:
             attn_events[0].record()
-        bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, out=out, lse=lse)
+        if S > 1:
+            bsf.attention_fwd_split(q, k, v, mi, w.scale, w.softcap, S, o_part=o_part, lse_part=lse_part)
+            if merge_events:
+                merge_events[0].record()
+            bsf.attention_merge(o_part, lse_part, out=out, lse=lse)
+            if merge_events:
+                merge_events[1].record()
+        else:
+            bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, out=out, lse=lse)
         if attn_events:
             attn_events[1].record()
 
@@ -257,6 +273,7 @@ def run_ours(args):
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     ea = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    em = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -266,7 +283,7 @@ def run_ours(args):
     for i in range(K):
         flush.zero_()
         ev[i][0].record()
-        step(ea[i])
+        step(ea[i], em[i] if S > 1 else None)
         ev[i][1].record()
     torch.cuda.synchronize()
     launches = bsf.kernel_launches() - launches0
@@ -282,7 +299,8 @@ def run_ours(args):
 
     peaks, peak_src = measured_peaks()
     peak = float(peaks["bf16_tflops"])
-    achieved = executed / (ms_attn * 1e-3) / 1e12
+    ms_merge = reduce_max(statistics.mean([a.elapsed_time(b) for a, b in em]), world, dev) if S > 1 else 0.0
+    achieved = executed / ((ms_attn - ms_merge) * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": None,
                 "kernel": "splash_fwd_kernel", "peak_source": f"{peak_src} bf16 burst (cuBLAS)",
@@ -311,6 +329,16 @@ def run_ours(args):
         "gpu_launches": int(launches),
         "clocks": clk,
     }
+    if S > 1:
+        rows = w.B * w.Hq * w.q_len
+        mbytes = S * rows * (4 * w.dv + 4) + rows * (2 * w.dv + 4)
+        gbs = mbytes / (ms_merge * 1e-3) / 1e9
+        hbm = float(peaks.get("hbm_gbs", 6800.0))
+        result["split_kv"] = {
+            "splits": S, "split_kernel_ms": round(ms_attn - ms_merge, 5), "merge_ms": round(ms_merge, 5),
+            "merge_roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                               "frac": round(gbs / hbm, 4), "bytes": int(mbytes)},
+            "note": "attention_ms = split kernel + merge; roofline.achieved uses the split kernel alone"}
     if e2e:
         result["e2e"] = e2e
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -333,8 +361,8 @@ def run_e2e(bsf, w, inp, spec, mi, dev, K, world, useful):
     k = torch.empty_like(kh, device=dev)
     v = torch.empty_like(vh, device=dev)
     seg = spec.q_segment_ids
-    out = torch.empty((w.B, w.Hq, w.L, w.dv), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((w.B, w.Hq, w.L), dtype=torch.float32, device=dev)
+    out = torch.empty((w.B, w.Hq, w.q_len, w.dv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Hq, w.q_len), dtype=torch.float32, device=dev)
     outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lseh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     h2d = qh.numel() * 2 + kh.numel() * 2 + vh.numel() * 2 + (segh.numel() * 4 if segh is not None else 0)
@@ -349,7 +377,7 @@ def run_e2e(bsf, w, inp, spec, mi, dev, K, world, useful):
         v.copy_(vh, non_blocking=True)
         if segh is not None:
             seg.copy_(segh, non_blocking=True)
-        mi.rebuild(spec, w.L, w.L, w.bq, w.bk)
+        mi.rebuild(spec, w.q_len, w.L, w.bq, w.bk)
         bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, out=out, lse=lse)
         outh.copy_(out, non_blocking=True)
         lseh.copy_(lse, non_blocking=True)

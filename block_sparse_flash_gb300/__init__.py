@@ -76,6 +76,9 @@ def lib():
     L.splash_mask_info_destroy.restype = None
     L.splash_attention_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i64, i64, i32, i32, vp, vp, vp, f32, f32,
                                        vp, vp, vp]
+    L.splash_attention_fwd_split.argtypes = [vp, vp, vp, i32, i32, i32, i64, i64, i32, i32, vp, vp, vp, f32, f32,
+                                             i32, vp, vp, vp]
+    L.splash_attention_merge.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp]
     L.splash_last_device_error.argtypes = [vp]
     L.splash_debug_wait_selftest.argtypes = [ctypes.c_uint64, vp]
     L.splash_status_string.argtypes = [ctypes.c_int]
@@ -86,6 +89,7 @@ def lib():
     L.splash_kernel_launches.restype = ctypes.c_uint64
     for f in (L.splash_build_mask_info, L.splash_mask_info_rebuild, L.splash_mask_info_shape,
               L.splash_mask_info_counts, L.splash_mask_info_to_host, L.splash_attention_fwd,
+              L.splash_attention_fwd_split, L.splash_attention_merge,
               L.splash_last_device_error, L.splash_debug_wait_selftest):
         f.restype = ctypes.c_int
     _lib = L
@@ -217,22 +221,65 @@ def build_mask_info(spec: MaskSpec, Lq: int, Lk: int, bq: int, bk: int, stream=N
     return MaskInfo(h.value)
 
 
-def attention_fwd(q, k, v, mask_info: MaskInfo, scale: float, softcap: float = 0.0, q_segment_ids=None,
-                  kv_segment_ids=None, out=None, lse=None, stream=None):
-    """out [B, Hq, Lq, dv] bf16 and lse [B, Hq, Lq] fp32 (allocated if not given)."""
+def _qkv_shapes(q, k, v):
     for t in (q, k, v):
         if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
             raise ValueError("q, k, v must be contiguous 4-D bf16 CUDA tensors")
     B, Hq, Lq, dqk = q.shape
-    Hkv, Lk, dv = k.shape[1], k.shape[2], v.shape[3]
+    return B, Hq, Lq, dqk, k.shape[1], k.shape[2], v.shape[3]
+
+
+def attention_fwd(q, k, v, mask_info: MaskInfo, scale: float, softcap: float = 0.0, q_segment_ids=None,
+                  kv_segment_ids=None, out=None, lse=None, stream=None, num_splits: int = 1):
+    """out [B, Hq, Lq, dv] bf16 and lse [B, Hq, Lq] fp32 (allocated if not given).
+
+    num_splits > 1 runs the split-KV forward into fp32 workspace allocated
+    here, then the LSE merge (same result)."""
+    B, Hq, Lq, dqk, Hkv, Lk, dv = _qkv_shapes(q, k, v)
     if out is None:
         out = torch.empty((B, Hq, Lq, dv), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
+    if num_splits > 1:
+        o_part, lse_part = attention_fwd_split(q, k, v, mask_info, scale, softcap, num_splits, q_segment_ids,
+                                               kv_segment_ids, stream=stream)
+        return attention_merge(o_part, lse_part, out=out, lse=lse, stream=stream)
     _check(lib().splash_attention_fwd(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Lq, Lk, dqk, dv,
                                       _ptr(q_segment_ids), _ptr(kv_segment_ids), mask_info.handle,
                                       float(scale), float(softcap), _ptr(out), _ptr(lse), _stream(stream)),
            "splash_attention_fwd")
+    return out, lse
+
+
+def attention_fwd_split(q, k, v, mask_info: MaskInfo, scale: float, softcap: float, num_splits: int,
+                        q_segment_ids=None, kv_segment_ids=None, o_part=None, lse_part=None, stream=None):
+    """Split-KV partials: o_part [S, B, Hq, Lq, dv] fp32 and lse_part [S, B, Hq, Lq] fp32."""
+    B, Hq, Lq, dqk, Hkv, Lk, dv = _qkv_shapes(q, k, v)
+    if o_part is None:
+        o_part = torch.empty((num_splits, B, Hq, Lq, dv), dtype=torch.float32, device=q.device)
+    if lse_part is None:
+        lse_part = torch.empty((num_splits, B, Hq, Lq), dtype=torch.float32, device=q.device)
+    _check(lib().splash_attention_fwd_split(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Lq, Lk, dqk, dv,
+                                            _ptr(q_segment_ids), _ptr(kv_segment_ids), mask_info.handle,
+                                            float(scale), float(softcap), int(num_splits), _ptr(o_part),
+                                            _ptr(lse_part), _stream(stream)),
+           "splash_attention_fwd_split")
+    return o_part, lse_part
+
+
+def attention_merge(o_part, lse_part, out=None, lse=None, stream=None):
+    """Merges split-KV partials [S, ..., dv] / [S, ...] into bf16 out [..., dv] and fp32 lse [...]."""
+    if o_part.dtype != torch.float32 or lse_part.dtype != torch.float32 or not o_part.is_contiguous() \
+            or not lse_part.is_contiguous():
+        raise ValueError("o_part and lse_part must be contiguous fp32 tensors")
+    S, dv = o_part.shape[0], o_part.shape[-1]
+    rows = lse_part[0].numel()
+    if out is None:
+        out = torch.empty(o_part.shape[1:], dtype=torch.bfloat16, device=o_part.device)
+    if lse is None:
+        lse = torch.empty(lse_part.shape[1:], dtype=torch.float32, device=o_part.device)
+    _check(lib().splash_attention_merge(_ptr(o_part), _ptr(lse_part), int(S), int(rows), int(dv), _ptr(out),
+                                        _ptr(lse), _stream(stream)), "splash_attention_merge")
     return out, lse
 
 

@@ -174,13 +174,13 @@ void splash_mask_info_destroy(splash_mask_info *mi) {
   delete mi;
 }
 
-splash_status splash_attention_fwd(const void *q, const void *k, const void *v, int32_t B, int32_t Hq,
-                                   int32_t Hkv, int64_t Lq, int64_t Lk, int32_t dqk, int32_t dv,
-                                   const int32_t *q_segment_ids, const int32_t *kv_segment_ids,
-                                   const splash_mask_info *mi, float scale, float softcap, void *out,
-                                   float *lse, void *cuda_stream) {
-  (void)q_segment_ids;
-  (void)kv_segment_ids;
+namespace {
+
+// Argument checks shared by the attention entry points; on success *err is
+// the device's error word.
+splash_status check_attention(const void *q, const void *k, const void *v, int32_t B, int32_t Hq, int32_t Hkv,
+                              int64_t Lq, int64_t Lk, int32_t dqk, int32_t dv, const splash_mask_info *mi,
+                              float scale, float softcap, const void *out, const void *lse, uint32_t **err) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || lse == nullptr || mi == nullptr)
     return SPLASH_ERR_INVALID_ARG;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lk <= 0 || dqk <= 0 || dv <= 0)
@@ -202,10 +202,53 @@ splash_status splash_attention_fwd(const void *q, const void *k, const void *v, 
   int dev = 0;
   SPLASH_CUDA_TRY(cudaGetDevice(&dev));
   if (dev != mi->device) return SPLASH_ERR_INVALID_ARG;
-  uint32_t *err = splash_device_error_word(dev);
-  if (err == nullptr) return SPLASH_ERR_CUDA;
-  return splash_attention_fwd_launch(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, out, lse,
-                                     static_cast<cudaStream_t>(cuda_stream), err);
+  *err = splash_device_error_word(dev);
+  if (*err == nullptr) return SPLASH_ERR_CUDA;
+  return SPLASH_OK;
+}
+
+}  // namespace
+
+splash_status splash_attention_fwd(const void *q, const void *k, const void *v, int32_t B, int32_t Hq,
+                                   int32_t Hkv, int64_t Lq, int64_t Lk, int32_t dqk, int32_t dv,
+                                   const int32_t *q_segment_ids, const int32_t *kv_segment_ids,
+                                   const splash_mask_info *mi, float scale, float softcap, void *out,
+                                   float *lse, void *cuda_stream) {
+  (void)q_segment_ids;
+  (void)kv_segment_ids;
+  uint32_t *err = nullptr;
+  splash_status st = check_attention(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, out, lse, &err);
+  if (st != SPLASH_OK) return st;
+  return splash_attention_fwd_launch(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, out, lse, 1,
+                                     nullptr, nullptr, static_cast<cudaStream_t>(cuda_stream), err);
+}
+
+splash_status splash_attention_fwd_split(const void *q, const void *k, const void *v, int32_t B, int32_t Hq,
+                                         int32_t Hkv, int64_t Lq, int64_t Lk, int32_t dqk, int32_t dv,
+                                         const int32_t *q_segment_ids, const int32_t *kv_segment_ids,
+                                         const splash_mask_info *mi, float scale, float softcap,
+                                         int32_t num_splits, float *o_part, float *lse_part, void *cuda_stream) {
+  (void)q_segment_ids;
+  (void)kv_segment_ids;
+  if (num_splits < 1 || num_splits > SPLASH_MAX_SPLITS) return SPLASH_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(o_part) & 31u) != 0) return SPLASH_ERR_INVALID_ARG;
+  uint32_t *err = nullptr;
+  splash_status st =
+      check_attention(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, o_part, lse_part, &err);
+  if (st != SPLASH_OK) return st;
+  return splash_attention_fwd_launch(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, nullptr, nullptr,
+                                     num_splits, o_part, lse_part, static_cast<cudaStream_t>(cuda_stream), err);
+}
+
+splash_status splash_attention_merge(const float *o_part, const float *lse_part, int32_t num_splits, int64_t rows,
+                                     int32_t dv, void *out, float *lse, void *cuda_stream) {
+  if (o_part == nullptr || lse_part == nullptr || out == nullptr || lse == nullptr) return SPLASH_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > SPLASH_MAX_SPLITS || rows < 0) return SPLASH_ERR_INVALID_ARG;
+  if (dv != 64 && dv != 128) return SPLASH_ERR_UNSUPPORTED;
+  if (((reinterpret_cast<uintptr_t>(o_part) | reinterpret_cast<uintptr_t>(out)) & 15u) != 0)
+    return SPLASH_ERR_INVALID_ARG;
+  return splash_attention_merge_launch(o_part, lse_part, num_splits, rows, dv, out, lse,
+                                       static_cast<cudaStream_t>(cuda_stream));
 }
 
 splash_status splash_classify_blocks_noalloc(const splash_mask_spec *spec, int64_t Lq, int64_t Lk, int32_t bq,

@@ -40,6 +40,7 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "internal.h"
@@ -110,22 +111,38 @@ struct FwdParams {
   int32_t dual_issuer;  // one MMA issuer per tile (pairs with different KV heads)
   __nv_bfloat16 *out;
   float *lse;
+  // split-KV: each q-block row's active list is cut into nsplit consecutive
+  // ranges (separate work items); split s writes its normalized partial O
+  // (fp32) and LSE at o_part / lse_part + s * part_rows rows (out / lse unused)
+  int32_t nsplit;
+  float *o_part;
+  float *lse_part;
+  int64_t part_rows;  // B * Hq * Lq
   uint32_t *err;
   uint64_t timeout_ns;
 };
 
 struct Item {
   int32_t b, h0, h1, kvh0, kvh1, qrow;
-  int32_t g0, nb;
+  int32_t g0, nb;  // this item's range of the row's active list
+  int32_t split;
   bool act1, shared;
 };
 
 // Work item w: rows in longest-first order; for a table shared by the batch,
-// each row expands into B batches; each (row, batch) into npairs head pairs.
+// each row expands into B batches; each (row, batch) into npairs head pairs;
+// each of those into nsplit consecutive ranges of the row's active blocks
+// (split s of nb blocks: [nb*s/nsplit, nb*(s+1)/nsplit)).
 __device__ __forceinline__ Item decode_item(const FwdParams &p, int64_t w) {
   Item it;
   int64_t k;
   int32_t pair;
+  it.split = 0;
+  if (p.nsplit > 1) {
+    const int64_t base = w / p.nsplit;
+    it.split = (int32_t)(w - base * p.nsplit);
+    w = base;
+  }
   if (p.nbm == 1) {
     const int64_t per = (int64_t)p.B * p.npairs;
     k = w / per;
@@ -142,6 +159,12 @@ __device__ __forceinline__ Item decode_item(const FwdParams &p, int64_t w) {
   it.qrow = mrow % p.nq;
   it.g0 = p.row_ptr[mrow];
   it.nb = p.row_ptr[mrow + 1] - it.g0;
+  if (p.nsplit > 1) {
+    const int32_t lo = (int32_t)((int64_t)it.nb * it.split / p.nsplit);
+    const int32_t hi = (int32_t)((int64_t)it.nb * (it.split + 1) / p.nsplit);
+    it.g0 += lo;
+    it.nb = hi - lo;
+  }
   it.h0 = 2 * pair;
   it.h1 = 2 * pair + 1;
   it.act1 = it.h1 < p.Hq;
@@ -878,7 +901,30 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         tc_fence_after();
       }
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      if (C::STAGE) {
+      if (p.o_part != nullptr) {
+        // split-KV partial: the split's normalized O in fp32 (32-byte stores)
+        float *dst = p.o_part + ((int64_t)it.split * p.part_rows + orow) * DV;
+#pragma unroll
+        for (int c = 0; c < DV / 32; ++c) {
+          uint32_t r[32];
+          if (it.nb > 0) {
+            tmem_ld32(tO + 32u * c, r);
+            tmem_wait_ld();
+            reg_fence32(r);
+          } else {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) r[x] = 0u;
+          }
+          if (row_valid) {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * inv);
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+              st_global_v8(dst + c * 32 + 8 * x, r[8 * x], r[8 * x + 1], r[8 * x + 2], r[8 * x + 3], r[8 * x + 4],
+                           r[8 * x + 5], r[8 * x + 6], r[8 * x + 7]);
+          }
+        }
+      } else if (C::STAGE) {
         // O rows to the warp's 128B-swizzled staging box (32 rows x 64
         // columns), one TMA store per box: whole-line global writes instead
         // of 32 rows' scattered pieces per store instruction
@@ -946,7 +992,13 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         }
       }
       }
-      if (row_valid) p.lse[orow] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+      if (row_valid) {
+        const float lse_v = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+        if (p.o_part != nullptr)
+          p.lse_part[(int64_t)it.split * p.part_rows + orow] = lse_v;
+        else
+          p.lse[orow] = lse_v;
+      }
     }
     if (!ok) raise_error(p, abort, SPLASH_DEV_TIMEOUT_SOFTMAX);
     if (C::STAGE && lane == 0) bulk_wait_all();  // this warp's O stores have completed
@@ -1011,9 +1063,9 @@ splash_status launch(const void *q, const void *k, const void *v, const FwdParam
   if (!make_map(&tq, q, DQK, (uint64_t)prm.B * prm.Hq * prm.Lq, 128) ||
       !make_map(&tk, k, DQK, (uint64_t)prm.B * prm.Hkv * prm.Lk, BK) ||
       !make_map(&tv, v, DV, (uint64_t)prm.B * prm.Hkv * prm.Lk, BK) ||
-      (C::STAGE && !make_map(&to, prm.out, DV, (uint64_t)prm.B * prm.Hq * prm.Lq, 32)))
+      (C::STAGE && prm.o_part == nullptr && !make_map(&to, prm.out, DV, (uint64_t)prm.B * prm.Hq * prm.Lq, 32)))
     return SPLASH_ERR_CUDA;
-  if (!C::STAGE) to = tq;  // unused
+  if (!C::STAGE || prm.o_part != nullptr) to = tq;  // unused (no staging, or split partials)
   static int configured_device = -1;
   int dev = 0;
   SPLASH_CUDA_TRY(cudaGetDevice(&dev));
@@ -1041,6 +1093,7 @@ splash_status splash_attention_fwd_launch(const void *q, const void *k, const vo
                                           int32_t Hq, int32_t Hkv, int64_t Lq, int64_t Lk,
                                           int32_t dqk, int32_t dv, const splash_mask_info *mi,
                                           float scale, float softcap, void *out, float *lse,
+                                          int32_t nsplit, float *o_part, float *lse_part,
                                           cudaStream_t stream, uint32_t *err_word) {
   FwdParams prm;
   prm.B = B;
@@ -1055,7 +1108,11 @@ splash_status splash_attention_fwd_launch(const void *q, const void *k, const vo
   prm.nbm = mi->batch_rows;
   prm.npairs = (Hq + 1) / 2;
   const int64_t rows = (int64_t)mi->batch_rows * mi->nq;
-  prm.num_items = (mi->batch_rows == 1 ? rows * B : rows) * prm.npairs;
+  prm.nsplit = nsplit > 1 ? nsplit : 1;
+  prm.num_items = (mi->batch_rows == 1 ? rows * B : rows) * prm.npairs * prm.nsplit;
+  prm.o_part = o_part;
+  prm.lse_part = lse_part;
+  prm.part_rows = (int64_t)B * Hq * Lq;
   prm.row_ptr = mi->row_ptr;
   prm.active_cols = mi->active_cols;
   prm.mask_next = mi->mask_next;
@@ -1086,6 +1143,85 @@ splash_status splash_attention_fwd_launch(const void *q, const void *k, const vo
 
 splash_status splash_wait_selftest_launch(uint64_t timeout_ns, cudaStream_t stream, uint32_t *err_word) {
   wait_selftest_kernel<<<1, 32, 0, stream>>>(timeout_ns, err_word);
+  SPLASH_CUDA_TRY(cudaGetLastError());
+  splash_count_launches(1);
+  return SPLASH_OK;
+}
+
+// ------------------------------------------------------------------ merge
+namespace splash {
+namespace {
+
+// LSE merge of split-KV partials ("The maths and infra behind core LLM
+// operations" (joto.ai), "LSE and Online Softmax": softmax segments combine
+// through their log-sum-exp): per row, lse = m + ln sum_s exp(lse_s - m) with
+// m = max_s lse_s, and out = sum_s exp(lse_s - lse) o_s.  One warp per row;
+// each lane holds DV / 32 consecutive columns (vector loads of the fp32
+// partials, one 8- or 4-byte store of the bf16 result).
+template <int DV>
+__global__ void __launch_bounds__(256) splash_merge_kernel(const float *o_part, const float *lse_part, int32_t nsplit,
+                                                           int64_t rows, __nv_bfloat16 *out, float *lse) {
+  constexpr int PER = DV / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < rows; row += nwarps) {
+    float m = -INFINITY;
+    for (int32_t sp = 0; sp < nsplit; ++sp) m = fmaxf(m, __ldg(lse_part + sp * rows + row));
+    float acc[PER];
+#pragma unroll
+    for (int x = 0; x < PER; ++x) acc[x] = 0.f;
+    float den = 0.f;
+    if (m != -INFINITY) {
+      for (int32_t sp = 0; sp < nsplit; ++sp) {
+        const float ls = __ldg(lse_part + sp * rows + row);
+        if (ls == -INFINITY) continue;
+        const float wgt = __expf(ls - m);
+        den += wgt;
+        const float *src = o_part + (sp * rows + row) * DV + lane * PER;
+        if constexpr (PER == 4) {
+          const float4 v = __ldg(reinterpret_cast<const float4 *>(src));
+          acc[0] += wgt * v.x;
+          acc[1] += wgt * v.y;
+          acc[2] += wgt * v.z;
+          acc[3] += wgt * v.w;
+        } else {
+          const float2 v = __ldg(reinterpret_cast<const float2 *>(src));
+          acc[0] += wgt * v.x;
+          acc[1] += wgt * v.y;
+        }
+      }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    __nv_bfloat16 *dst = out + row * DV + lane * PER;
+    if constexpr (PER == 4) {
+      const uint32_t a = pack_bf16x2(acc[0] * inv, acc[1] * inv), b = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+      *reinterpret_cast<uint2 *>(dst) = make_uint2(a, b);
+    } else {
+      *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    }
+    if (lane == 0) lse[row] = den > 0.f ? m + __logf(den) : -INFINITY;
+  }
+}
+
+}  // namespace
+}  // namespace splash
+
+splash_status splash_attention_merge_launch(const float *o_part, const float *lse_part, int32_t nsplit, int64_t rows,
+                                            int32_t dv, void *out, float *lse, cudaStream_t stream) {
+  using namespace splash;
+  if (rows <= 0) return SPLASH_OK;
+  int dev = 0, sms = 148;
+  SPLASH_CUDA_TRY(cudaGetDevice(&dev));
+  SPLASH_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int64_t want = (rows + 7) / 8;  // 8 rows (warps) per CTA
+  const unsigned grid = (unsigned)std::min<int64_t>(want, (int64_t)sms * 16);
+  __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(out);
+  if (dv == 128)
+    splash_merge_kernel<128><<<grid, 256, 0, stream>>>(o_part, lse_part, nsplit, rows, o, lse);
+  else if (dv == 64)
+    splash_merge_kernel<64><<<grid, 256, 0, stream>>>(o_part, lse_part, nsplit, rows, o, lse);
+  else
+    return SPLASH_ERR_UNSUPPORTED;
   SPLASH_CUDA_TRY(cudaGetLastError());
   splash_count_launches(1);
   return SPLASH_OK;

@@ -85,11 +85,16 @@ splash_status splash_classify_blocks_noalloc_impl(const splash_mask_spec *spec, 
 uint32_t *splash_device_error_word(int device);  // device address of the error word (or NULL)
 
 // attention_fwd.cu
+// nsplit > 1: split-KV partials into o_part / lse_part (out / lse unused).
 splash_status splash_attention_fwd_launch(const void *q, const void *k, const void *v, int32_t B,
                                           int32_t Hq, int32_t Hkv, int64_t Lq, int64_t Lk,
                                           int32_t dqk, int32_t dv, const splash_mask_info *mi,
                                           float scale, float softcap, void *out, float *lse,
+                                          int32_t nsplit, float *o_part, float *lse_part,
                                           cudaStream_t stream, uint32_t *err_word);
+splash_status splash_attention_merge_launch(const float *o_part, const float *lse_part, int32_t nsplit,
+                                            int64_t rows, int32_t dv, void *out, float *lse,
+                                            cudaStream_t stream);
 splash_status splash_wait_selftest_launch(uint64_t timeout_ns, cudaStream_t stream,
                                           uint32_t *err_word);
 

@@ -195,6 +195,50 @@ splash_status splash_attention_fwd(const void *q, const void *k, const void *v, 
                                    float scale, float softcap, void *out, float *lse,
                                    void *cuda_stream);
 
+/* Largest num_splits accepted by the split-KV entry points. */
+#define SPLASH_MAX_SPLITS 256
+
+/*
+ * splash_attention_fwd_split -- the same forward with each q-block row's
+ * active list cut into num_splits consecutive ranges ("split-KV"), each a
+ * separate work item, so that rows with many active blocks and few rows in
+ * total (long keys, few queries) still fill the GPU.  For split s (blocks
+ * [nb*s/num_splits, nb*(s+1)/num_splits) of a row with nb active blocks), with
+ * J_s its allowed keys and R = B*Hq*Lq:
+ *   o_part[s][b][h][i][:]  = sum_{j in J_s} exp(s_j - lse_s) v[b,g,j,:]   (fp32)
+ *   lse_part[s][b][h][i]   = ln sum_{j in J_s} exp(s_j)
+ * with o_part = 0 and lse_part = -inf where J_s is empty.  splash_attention_merge
+ * turns them into out / lse equal to splash_attention_fwd's: this is the merge
+ * of softmax segments through their log-sum-exp ("The maths and infra behind
+ * core LLM operations" (joto.ai), "LSE and Online Softmax"; "Pallas Kernels
+ * and Splash Attention" §5.1).
+ *
+ *   num_splits  1 .. SPLASH_MAX_SPLITS (splits beyond a row's block count are
+ *               empty)
+ *   o_part      device fp32 [num_splits][B][Hq][Lq][dv], 32-byte aligned
+ *   lse_part    device fp32 [num_splits][B][Hq][Lq]
+ * Both are caller-owned workspace, fully overwritten.  Other arguments,
+ * supported shapes and errors as for splash_attention_fwd.
+ */
+splash_status splash_attention_fwd_split(const void *q, const void *k, const void *v, int32_t B,
+                                         int32_t Hq, int32_t Hkv, int64_t Lq, int64_t Lk, int32_t dqk,
+                                         int32_t dv, const int32_t *q_segment_ids,
+                                         const int32_t *kv_segment_ids, const splash_mask_info *mi,
+                                         float scale, float softcap, int32_t num_splits, float *o_part,
+                                         float *lse_part, void *cuda_stream);
+
+/*
+ * splash_attention_merge -- combines split-KV partials (layout above, rows =
+ * B*Hq*Lq):  m = max_s lse_part[s][r];  lse[r] = m + ln sum_s exp(lse_part[s][r] - m);
+ * out[r][:] = sum_s exp(lse_part[s][r] - lse[r]) o_part[s][r][:]  (bf16);
+ * rows whose splits are all empty get out = 0, lse = -inf.
+ *   o_part  device fp32, 16-byte aligned     lse_part  device fp32
+ *   dv      64 or 128 (else SPLASH_ERR_UNSUPPORTED)
+ *   out     device bf16 [rows][dv], 16-byte aligned    lse  device fp32 [rows]
+ */
+splash_status splash_attention_merge(const float *o_part, const float *lse_part, int32_t num_splits,
+                                     int64_t rows, int32_t dv, void *out, float *lse, void *cuda_stream);
+
 /*
  * splash_classify_blocks_noalloc -- the block classification of a mask
  * (block_mask and its totals), computed without allocating any device memory.

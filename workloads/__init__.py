@@ -36,6 +36,11 @@ class Workload:
     window_right: int = -1
     documents: bool = False   # segment IDs from seeded document lengths
     softcap: float = 0.0
+    Lq: int = 0               # query length when it differs from L (L is then the key length)
+
+    @property
+    def q_len(self) -> int:
+        return self.Lq or self.L
 
     @property
     def scale(self) -> float:
@@ -47,7 +52,8 @@ class Workload:
         return 1000 * c + 1, 1000 * c + 2, 1000 * c + 3, 1000 * c + 4
 
     def describe(self) -> str:
-        parts = [f"B={self.B}", f"Hq={self.Hq}", f"Hkv={self.Hkv}", f"L={self.L}",
+        lens = f"L={self.L}" if not self.Lq else f"Lq={self.Lq}, Lk={self.L}"
+        parts = [f"B={self.B}", f"Hq={self.Hq}", f"Hkv={self.Hkv}", lens,
                  f"dqk={self.dqk}", f"dv={self.dv}", f"blocks={self.bq}x{self.bk}"]
         mask = []
         if self.documents:
@@ -72,8 +78,18 @@ WORKLOADS: List[Workload] = [
 ]
 
 
+# Workloads beyond the five above, for the split-KV forward: few query rows
+# against long keys (the shape where one item per q-block row leaves most of
+# the GPU idle).  Not one of the five configurations.
+EXTRA_WORKLOADS: List[Workload] = [
+    Workload(6, "few queries, long keys GQA", 1, 32, 8, 65536, 128, 128, 128, 128, causal=False, Lq=512),
+]
+
+
 def workload(index: int) -> Workload:
-    return WORKLOADS[index - 1]
+    if index <= len(WORKLOADS):
+        return WORKLOADS[index - 1]
+    return EXTRA_WORKLOADS[index - len(WORKLOADS) - 1]
 
 
 def normal_bf16(shape, seed: int) -> torch.Tensor:
@@ -135,7 +151,7 @@ class Inputs:
 def make_inputs(w: Workload, with_values: bool = True) -> Inputs:
     sq, sk, sv, ss = w.seeds
     if with_values:
-        q = normal_bf16((w.B, w.Hq, w.L, w.dqk), sq)
+        q = normal_bf16((w.B, w.Hq, w.q_len, w.dqk), sq)
         k = normal_bf16((w.B, w.Hkv, w.L, w.dqk), sk)
         v = normal_bf16((w.B, w.Hkv, w.L, w.dv), sv)
     else:
