@@ -1,5 +1,6 @@
 """The oracle: a plain, slow, obviously correct CPU implementation of
-block-sparse masked attention (forward) and of its sparse execution table.
+block-sparse masked attention (forward and backward) and of its sparse
+execution table.
 
 TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
 CPU-baseline / reference legs of bench.py may import this package.  It
@@ -23,7 +24,8 @@ from typing import Optional
 import numpy as np
 
 from . import build as _build
-from .softmax_ref import merge, online_softmax_trace, partial_state, safe_softmax  # noqa: F401
+from .softmax_ref import (exp_limits, merge, mle_safe_range, mle_softmax, online_softmax_trace,  # noqa: F401
+                          partial_state, safe_softmax)
 
 _lib = None
 
@@ -53,7 +55,11 @@ def lib():
                                        ctypes.POINTER(_Spec), ctypes.c_double, ctypes.c_double,
                                        vp, i64, i32, vp, vp]
         L.oracle_allowed.argtypes = [ctypes.POINTER(_Spec), i64, i64, i64, i64, i64]
-        for f in (L.oracle_mask_classify, L.oracle_mask_table, L.oracle_attention, L.oracle_allowed):
+        L.oracle_attention_bwd_head.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                                ctypes.POINTER(_Spec), ctypes.c_double, ctypes.c_double,
+                                                i32, vp, vp, vp, vp, vp]
+        for f in (L.oracle_mask_classify, L.oracle_mask_table, L.oracle_attention, L.oracle_allowed,
+                  L.oracle_attention_bwd_head):
             f.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -218,3 +224,59 @@ def attention(q, k, v, spec: MaskSpec, scale: float, softcap: float = 0.0, rows=
     if rows is None:
         return out.reshape(B, Hq, Lq, dv), lse.reshape(B, Hq, Lq)
     return out, lse
+
+
+def _f64(x) -> np.ndarray:
+    """float64 copy of a torch tensor (bf16 widens exactly) or an array."""
+    if hasattr(x, "dtype") and str(x.dtype).startswith("torch."):
+        import torch  # torch CPU only: widening the caller's tensor
+        return np.ascontiguousarray(x.detach().to(torch.float64).cpu().numpy())
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def attention_bwd(q, k, v, dout, spec: MaskSpec, scale: float, softcap: float = 0.0, heads=None,
+                  nthreads: int = 0):
+    """Backward attention in f64 (gradients of the forward with respect to q,
+    k and v for the upstream gradient dout).
+
+    q [B, Hq, Lq, dqk], k [B, Hkv, Lk, dqk], v [B, Hkv, Lk, dv],
+    dout [B, Hq, Lq, dv]: torch tensors (bf16 widens exactly) or float64
+    arrays.  heads: optional list of (b, h) pairs; only those query heads are
+    differentiated (dq of the others stays 0 and dk / dv then hold the listed
+    heads' contributions).  Returns dict(dq, dk, dv, lse, delta) of f64 arrays
+    shaped like q, k, v, [B, Hq, Lq], [B, Hq, Lq]."""
+    qf, kf, vf, gf = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, Hq, Lq, dqk = qf.shape
+    _, Hkv, Lk, _ = kf.shape
+    dv = vf.shape[3]
+    if Hq % Hkv or gf.shape != (B, Hq, Lq, dv):
+        raise ValueError("shape mismatch")
+    G = Hq // Hkv
+    s, keep = spec._c()
+    dq = np.zeros_like(qf)
+    dk = np.zeros_like(kf)
+    dvv = np.zeros_like(vf)
+    lse = np.full((B, Hq, Lq), -np.inf)
+    delta = np.zeros((B, Hq, Lq))
+    if heads is None:
+        heads = [(b, h) for b in range(B) for h in range(Hq)]
+    tdk = np.zeros((Lk, dqk))
+    tdv = np.zeros((Lk, dv))
+    for b, h in heads:
+        g = h // G
+        qh, gh = np.ascontiguousarray(qf[b, h]), np.ascontiguousarray(gf[b, h])
+        kh, vh = np.ascontiguousarray(kf[b, g]), np.ascontiguousarray(vf[b, g])
+        dqh = np.zeros((Lq, dqk))
+        lh = np.zeros(Lq)
+        dh = np.zeros(Lq)
+        _check(lib().oracle_attention_bwd_head(qh.ctypes.data, kh.ctypes.data, vh.ctypes.data, gh.ctypes.data,
+                                               b, Lq, Lk, dqk, dv, ctypes.byref(s), float(scale), float(softcap),
+                                               nthreads or default_threads(), dqh.ctypes.data, tdk.ctypes.data,
+                                               tdv.ctypes.data, lh.ctypes.data, dh.ctypes.data),
+               "attention_bwd")
+        dq[b, h] = dqh
+        dk[b, g] += tdk
+        dvv[b, g] += tdv
+        lse[b, h] = lh
+        delta[b, h] = dh
+    return dict(dq=dq, dk=dk, dv=dvv, lse=lse, delta=delta)

@@ -1,6 +1,6 @@
 /*
  * splash_oracle.c -- the CPU oracle for block-sparse (Splash-style) masked
- * attention, forward pass.
+ * attention: mask tables, forward pass and backward pass.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls
  * this file; only the tests, __graft_entry__.smoke() and the CPU-baseline leg
@@ -367,6 +367,156 @@ int oracle_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, in
     jb.next = 0;
     pthread_mutex_init(&jb.mu, NULL);
     run_threads(attention_worker, &jb, nthreads);
+    pthread_mutex_destroy(&jb.mu);
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Backward pass of one (batch b, query head h): the gradients of
+ *   out_i = sum_j P_ij v_j,  P_ij = exp(s_ij) / sum_j' exp(s_ij')  (allowed j)
+ * with respect to q, k and v, for an upstream gradient dout.  Plain calculus
+ * on the forward's definition (the softmax Jacobian):
+ *   dP_ij = dout_i . v_j,  D_i = sum_j P_ij dP_ij,  dS_ij = P_ij (dP_ij - D_i),
+ *   with the soft cap s = cap tanh(u/cap), u = scale q.k: dU_ij = dS_ij (1 - t_ij^2),
+ *   t = tanh(u/cap) (without it dU = dS);
+ *   dq_i = scale sum_j dU_ij k_j,  dk_j = scale sum_i dU_ij q_i,  dv_j = sum_i P_ij dout_i.
+ * P is recomputed from the row's log-sum-exp, P_ij = exp(s_ij - LSE_i) -- the
+ * residual the forward keeps for its backward ([L13] §6.3; [OPS] "LSE and
+ * Online Softmax": the backward rebuilds the probabilities from LSE instead
+ * of storing them).  Pass A runs over query rows (LSE, D, dq); pass B over key
+ * rows (dk, dv), each row owned by one thread. */
+
+typedef struct {
+    const double *q, *k, *v, *dout;
+    int64_t b, Lq, Lk, dqk, dv;
+    const oracle_mask_spec *sp;
+    double scale, softcap;
+    double *dq, *dk, *dvo, *lse, *delta;
+    int64_t next, total;
+    pthread_mutex_t mu;
+} bwd_job;
+
+static int64_t bwd_take(bwd_job *jb)
+{
+    pthread_mutex_lock(&jb->mu);
+    int64_t x = jb->next++;
+    pthread_mutex_unlock(&jb->mu);
+    return x < jb->total ? x : -1;
+}
+
+/* score s and tanh value t of (i, j); returns 0 when the pair is masked */
+static int bwd_score(const bwd_job *jb, int64_t i, int64_t j, double *s, double *t)
+{
+    if (!allowed(jb->sp, jb->b, jb->Lq, jb->Lk, i, j)) return 0;
+    const double *qi = jb->q + i * jb->dqk, *kj = jb->k + j * jb->dqk;
+    double dot = 0.0;
+    for (int64_t d = 0; d < jb->dqk; ++d) dot += qi[d] * kj[d];
+    double u = jb->scale * dot;
+    if (jb->softcap > 0.0) {
+        *t = tanh(u / jb->softcap);
+        *s = jb->softcap * *t;
+    } else {
+        *t = 0.0;
+        *s = u;
+    }
+    return 1;
+}
+
+static double bwd_dp(const bwd_job *jb, int64_t i, int64_t j)
+{
+    const double *g = jb->dout + i * jb->dv, *vj = jb->v + j * jb->dv;
+    double acc = 0.0;
+    for (int64_t d = 0; d < jb->dv; ++d) acc += g[d] * vj[d];
+    return acc;
+}
+
+static void *bwd_rows_worker(void *arg)
+{
+    bwd_job *jb = (bwd_job *)arg;
+    double *s = (double *)malloc(sizeof(double) * (size_t)jb->Lk);
+    double *t = (double *)malloc(sizeof(double) * (size_t)jb->Lk);
+    unsigned char *ok = (unsigned char *)malloc((size_t)jb->Lk);
+    if (!s || !t || !ok) { free(s); free(t); free(ok); return NULL; }
+    for (int64_t i; (i = bwd_take(jb)) >= 0;) {
+        double *dqi = jb->dq + i * jb->dqk;
+        for (int64_t d = 0; d < jb->dqk; ++d) dqi[d] = 0.0;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < jb->Lk; ++j) {
+            ok[j] = (unsigned char)bwd_score(jb, i, j, &s[j], &t[j]);
+            if (ok[j] && s[j] > m) m = s[j];
+        }
+        if (m == -INFINITY) { /* no allowed key: no gradient flows */
+            jb->lse[i] = -INFINITY;
+            jb->delta[i] = 0.0;
+            continue;
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < jb->Lk; ++j)
+            if (ok[j]) l += exp(s[j] - m);
+        double lse = m + log(l), D = 0.0;
+        for (int64_t j = 0; j < jb->Lk; ++j)
+            if (ok[j]) D += exp(s[j] - lse) * bwd_dp(jb, i, j);
+        jb->lse[i] = lse;
+        jb->delta[i] = D;
+        for (int64_t j = 0; j < jb->Lk; ++j) {
+            if (!ok[j]) continue;
+            double p = exp(s[j] - lse);
+            double du = p * (bwd_dp(jb, i, j) - D);
+            if (jb->softcap > 0.0) du *= 1.0 - t[j] * t[j];
+            const double *kj = jb->k + j * jb->dqk;
+            for (int64_t d = 0; d < jb->dqk; ++d) dqi[d] += jb->scale * du * kj[d];
+        }
+    }
+    free(s); free(t); free(ok);
+    return NULL;
+}
+
+static void *bwd_keys_worker(void *arg)
+{
+    bwd_job *jb = (bwd_job *)arg;
+    for (int64_t j; (j = bwd_take(jb)) >= 0;) {
+        double *dkj = jb->dk + j * jb->dqk, *dvj = jb->dvo + j * jb->dv;
+        for (int64_t d = 0; d < jb->dqk; ++d) dkj[d] = 0.0;
+        for (int64_t d = 0; d < jb->dv; ++d) dvj[d] = 0.0;
+        for (int64_t i = 0; i < jb->Lq; ++i) {
+            double s, t;
+            if (jb->lse[i] == -INFINITY || !bwd_score(jb, i, j, &s, &t)) continue;
+            double p = exp(s - jb->lse[i]);
+            double du = p * (bwd_dp(jb, i, j) - jb->delta[i]);
+            if (jb->softcap > 0.0) du *= 1.0 - t * t;
+            const double *g = jb->dout + i * jb->dv, *qi = jb->q + i * jb->dqk;
+            for (int64_t d = 0; d < jb->dv; ++d) dvj[d] += p * g[d];
+            for (int64_t d = 0; d < jb->dqk; ++d) dkj[d] += jb->scale * du * qi[d];
+        }
+    }
+    return NULL;
+}
+
+/* q [Lq][dqk] and dout [Lq][dv] are head h's rows of batch b; k [Lk][dqk] and
+ * v [Lk][dv] those of its key/value head; all f64.  b selects the segment-ID
+ * batch row (ignored without segment IDs).  Writes dq [Lq][dqk], this head's
+ * contributions dk [Lk][dqk] and dv [Lk][dv] (a GQA group sums them), the
+ * row log-sum-exp lse [Lq] and D = delta [Lq]. */
+int oracle_attention_bwd_head(const double *q, const double *k, const double *v, const double *dout,
+                              int64_t b, int64_t Lq, int64_t Lk, int64_t dqk, int64_t dv,
+                              const oracle_mask_spec *sp, double scale, double softcap, int nthreads,
+                              double *dq, double *dk, double *dvo, double *lse, double *delta)
+{
+    if (!q || !k || !v || !dout || !sp || !dq || !dk || !dvo || !lse || !delta || Lq <= 0 || Lk <= 0 ||
+        dqk <= 0 || dv <= 0 || b < 0)
+        return ORACLE_ERR_ARG;
+    if (sp->q_seg != NULL && (sp->kv_seg == NULL || b >= sp->batch)) return ORACLE_ERR_ARG;
+    bwd_job jb;
+    jb.q = q; jb.k = k; jb.v = v; jb.dout = dout;
+    jb.b = sp->q_seg != NULL ? b : 0;
+    jb.Lq = Lq; jb.Lk = Lk; jb.dqk = dqk; jb.dv = dv;
+    jb.sp = sp; jb.scale = scale; jb.softcap = softcap;
+    jb.dq = dq; jb.dk = dk; jb.dvo = dvo; jb.lse = lse; jb.delta = delta;
+    pthread_mutex_init(&jb.mu, NULL);
+    jb.next = 0; jb.total = Lq;
+    run_threads(bwd_rows_worker, &jb, nthreads);
+    jb.next = 0; jb.total = Lk;
+    run_threads(bwd_keys_worker, &jb, nthreads);
     pthread_mutex_destroy(&jb.mu);
     return ORACLE_OK;
 }
