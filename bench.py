@@ -45,6 +45,11 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--splits", type=int, default=1,
                     help="split-KV forward with this many splits per row, then the LSE merge")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (MaskInfo rebuild + gradients) instead of the forward")
+    ap.add_argument("--max-logit", type=float, default=None,
+                    help="Max Logit Estimate: fix every row's softmax reference at this constant "
+                         "(e.g. the workload's soft cap)")
     return ap.parse_args(argv)
 
 
@@ -244,6 +249,8 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     S = args.splits
+    if S > 1 and args.max_logit is not None:
+        raise SystemExit("--max-logit applies to the one-pass forward only")
     if S > 1:
         o_part = torch.empty((S, w.B, w.Hq, w.q_len, w.dv), dtype=torch.float32, device=dev)
         lse_part = torch.empty((S, w.B, w.Hq, w.q_len), dtype=torch.float32, device=dev)
@@ -260,7 +267,7 @@ def run_ours(args):
             if merge_events:
                 merge_events[1].record()
         else:
-            bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, out=out, lse=lse)
+            bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, out=out, lse=lse, max_logit=args.max_logit)
         if attn_events:
             attn_events[1].record()
 
@@ -309,7 +316,8 @@ def run_ours(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(bsf, w, inp, spec, mi, dev, K=max(3, min(K, 20)), world=world, useful=useful)
+        e2e = run_e2e(bsf, w, inp, spec, mi, dev, K=max(3, min(K, 20)), world=world, useful=useful,
+                      max_logit=args.max_logit)
 
     result = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
@@ -339,6 +347,8 @@ def run_ours(args):
             "merge_roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                                "frac": round(gbs / hbm, 4), "bytes": int(mbytes)},
             "note": "attention_ms = split kernel + merge; roofline.achieved uses the split kernel alone"}
+    if args.max_logit is not None:
+        result["config"]["max_logit"] = args.max_logit
     if e2e:
         result["e2e"] = e2e
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -350,7 +360,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(bsf, w, inp, spec, mi, dev, K, world, useful):
+def run_e2e(bsf, w, inp, spec, mi, dev, K, world, useful, max_logit=None):
     """Same metric through the public API with host buffers: pinned host ->
     device copies of the inputs, the step, device -> host copies of O and LSE,
     all inside the timed region."""
@@ -378,7 +388,7 @@ def run_e2e(bsf, w, inp, spec, mi, dev, K, world, useful):
         if segh is not None:
             seg.copy_(segh, non_blocking=True)
         mi.rebuild(spec, w.q_len, w.L, w.bq, w.bk)
-        bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, out=out, lse=lse)
+        bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, out=out, lse=lse, max_logit=max_logit)
         outh.copy_(out, non_blocking=True)
         lseh.copy_(lse, non_blocking=True)
         b.record()
@@ -422,10 +432,105 @@ def run_reference(args):
     print(json.dumps(res), flush=True)
 
 
+# --------------------------------------------------------------------- backward
+def bwd_flop_counts(w, counts, batch_rows):
+    """Backward FLOPs: per (query, key) pair five products of the forward's
+    size class: S, dP, dV, dK, dQ = 2 * (3 * dqk + 2 * dv)."""
+    per_pair = 2 * (3 * w.dqk + 2 * w.dv)
+    rep = w.Hq * (w.B if batch_rows == 1 else 1)
+    return (float(per_pair * counts["allowed_pairs"] * rep),
+            float(per_pair * w.bq * w.bk * counts["num_active"] * rep))
+
+
+def run_backward(args):
+    """One step = MaskInfo rebuild + the backward call (transposed table, D,
+    main kernel, dq conversion) for the workload's forward outputs, which are
+    computed once before timing; dout is seeded N(0, 1) bf16."""
+    import torch
+
+    import block_sparse_flash_gb300 as bsf
+    from block_sparse_flash_gb300 import build as libbuild
+    import workloads
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    libbuild.build()
+    w = workloads.workload(args.workload)
+    inp = workloads.make_inputs(w)
+    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    dout = workloads.normal_bf16((w.B, w.Hq, w.q_len, w.dv), 1000 * w.index + 5).to(dev)
+    seg = inp.segment_ids.to(dev) if inp.segment_ids is not None else None
+    spec = bsf.MaskSpec(w.causal, w.window_left, w.window_right, seg, seg)
+    mi = bsf.build_mask_info(spec, w.q_len, w.L, w.bq, w.bk)
+    counts = mi.counts()
+    useful, executed = bwd_flop_counts(w, counts, mi.shape()["batch_rows"])
+    out, lse = bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(bsf.attention_bwd_workspace_size(w.B, w.Hq, w.q_len, w.dqk), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(ev=None):
+        mi.rebuild(spec, w.q_len, w.L, w.bq, w.bk)
+        if ev:
+            ev[0].record()
+        bsf.attention_bwd(q, k, v, out, lse, dout, mi, w.scale, w.softcap, dq=dq, dk=dk, dv=dv, workspace=ws)
+        if ev:
+            ev[1].record()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    bsf.check_device_error()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    eb = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0)
+    clocks.start()
+    launches0 = bsf.kernel_launches()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record()
+        step(eb[i])
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    launches = bsf.kernel_launches() - launches0
+    clk = clocks.stop()
+    bsf.check_device_error()
+    ms_step = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    ms_bwd = statistics.mean(a.elapsed_time(b) for a, b in eb)
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = executed / (ms_bwd * 1e-3) / 1e12
+    result = {
+        "metric": "masked attn bwd useful TFLOP/s & % of GB300 BF16 tensor peak; ms per call",
+        "value": round(useful / (ms_step * 1e-3) / 1e12, 3), "unit": "TFLOP/s", "n_gpus": 1, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, see workloads/)",
+        "config": {"workload": w.describe(), "step": "MaskInfo rebuild + attention backward",
+                   "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
+                   "active_blocks": counts["num_active"], "parallelism": "replicas x1"},
+        "backward_ms": round(ms_bwd, 5),
+        "backward_useful_tflops": round(useful / (ms_bwd * 1e-3) / 1e12, 2),
+        "backward_executed_tflops": round(achieved, 2),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None, "kernel": "whole backward call",
+                     "peak_source": f"{peak_src} bf16 burst (cuBLAS)",
+                     "achieved_is": "executed backward FLOPs of the active blocks / mean time of the whole "
+                                    "backward call (its 7 kernels, CUDA events)"},
+        "gpu_launches": int(launches), "clocks": clk,
+    }
+    print(json.dumps(result), flush=True)
+    mi.close()
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.backward:
+        run_backward(args)
     else:
         run_ours(args)
 

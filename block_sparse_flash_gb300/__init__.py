@@ -78,6 +78,11 @@ def lib():
                                        vp, vp, vp]
     L.splash_attention_fwd_split.argtypes = [vp, vp, vp, i32, i32, i32, i64, i64, i32, i32, vp, vp, vp, f32, f32,
                                              i32, vp, vp, vp]
+    L.splash_attention_fwd_mle.argtypes = [vp, vp, vp, i32, i32, i32, i64, i64, i32, i32, vp, vp, vp, f32, f32,
+                                           f32, vp, vp, vp]
+    L.splash_attention_bwd_workspace_size.argtypes = [i32, i32, i64, i32, P(ctypes.c_size_t)]
+    L.splash_attention_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i64, i64, i32, i32, vp, vp, vp,
+                                       f32, f32, vp, vp, vp, vp, ctypes.c_size_t, vp]
     L.splash_attention_merge.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp]
     L.splash_last_device_error.argtypes = [vp]
     L.splash_debug_wait_selftest.argtypes = [ctypes.c_uint64, vp]
@@ -230,16 +235,28 @@ def _qkv_shapes(q, k, v):
 
 
 def attention_fwd(q, k, v, mask_info: MaskInfo, scale: float, softcap: float = 0.0, q_segment_ids=None,
-                  kv_segment_ids=None, out=None, lse=None, stream=None, num_splits: int = 1):
+                  kv_segment_ids=None, out=None, lse=None, stream=None, num_splits: int = 1,
+                  max_logit=None):
     """out [B, Hq, Lq, dv] bf16 and lse [B, Hq, Lq] fp32 (allocated if not given).
 
     num_splits > 1 runs the split-KV forward into fp32 workspace allocated
-    here, then the LSE merge (same result)."""
+    here, then the LSE merge (same result).  max_logit = c runs the Max Logit
+    Estimate variant (the softmax reference fixed at c; same result while c
+    is in the safe range, e.g. c = softcap)."""
     B, Hq, Lq, dqk, Hkv, Lk, dv = _qkv_shapes(q, k, v)
     if out is None:
         out = torch.empty((B, Hq, Lq, dv), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
+    if max_logit is not None:
+        if num_splits > 1:
+            raise ValueError("max_logit is supported by the one-pass forward only (num_splits == 1)")
+        _check(lib().splash_attention_fwd_mle(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Lq, Lk, dqk, dv,
+                                              _ptr(q_segment_ids), _ptr(kv_segment_ids), mask_info.handle,
+                                              float(scale), float(softcap), float(max_logit), _ptr(out),
+                                              _ptr(lse), _stream(stream)),
+               "splash_attention_fwd_mle")
+        return out, lse
     if num_splits > 1:
         o_part, lse_part = attention_fwd_split(q, k, v, mask_info, scale, softcap, num_splits, q_segment_ids,
                                                kv_segment_ids, stream=stream)
@@ -281,6 +298,43 @@ def attention_merge(o_part, lse_part, out=None, lse=None, stream=None):
     _check(lib().splash_attention_merge(_ptr(o_part), _ptr(lse_part), int(S), int(rows), int(dv), _ptr(out),
                                         _ptr(lse), _stream(stream)), "splash_attention_merge")
     return out, lse
+
+
+def attention_bwd(q, k, v, out, lse, dout, mask_info: MaskInfo, scale: float, softcap: float = 0.0,
+                  q_segment_ids=None, kv_segment_ids=None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of attention_fwd for the upstream gradient dout,
+    from the forward's out and lse (bf16 tensors shaped like q, k, v; allocated
+    if not given).  workspace: optional uint8 device tensor of at least
+    attention_bwd_workspace_size(...) bytes."""
+    B, Hq, Lq, dqk, Hkv, Lk, dvd = _qkv_shapes(q, k, v)
+    for name, t, shape, dt in (("out", out, (B, Hq, Lq, dvd), torch.bfloat16),
+                               ("dout", dout, (B, Hq, Lq, dvd), torch.bfloat16),
+                               ("lse", lse, (B, Hq, Lq), torch.float32)):
+        if tuple(t.shape) != shape or t.dtype != dt or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {dt} tensor of shape {shape}")
+    if dq is None:
+        dq = torch.empty_like(q)
+    if dk is None:
+        dk = torch.empty_like(k)
+    if dv is None:
+        dv = torch.empty_like(v)
+    need = attention_bwd_workspace_size(B, Hq, Lq, dqk)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(lib().splash_attention_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), B, Hq, Hkv,
+                                      Lq, Lk, dqk, dvd, _ptr(q_segment_ids), _ptr(kv_segment_ids),
+                                      mask_info.handle, float(scale), float(softcap), _ptr(dq), _ptr(dk), _ptr(dv),
+                                      _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+                                      _stream(stream)),
+           "splash_attention_bwd")
+    return dq, dk, dv
+
+
+def attention_bwd_workspace_size(B: int, Hq: int, Lq: int, dqk: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().splash_attention_bwd_workspace_size(int(B), int(Hq), int(Lq), int(dqk), ctypes.byref(n)),
+           "splash_attention_bwd_workspace_size")
+    return int(n.value)
 
 
 def last_device_error(stream=None) -> int:

@@ -219,8 +219,52 @@ splash_status splash_attention_fwd(const void *q, const void *k, const void *v, 
   uint32_t *err = nullptr;
   splash_status st = check_attention(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, out, lse, &err);
   if (st != SPLASH_OK) return st;
-  return splash_attention_fwd_launch(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, out, lse, 1,
-                                     nullptr, nullptr, static_cast<cudaStream_t>(cuda_stream), err);
+  return splash_attention_fwd_launch(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, NAN, out, lse,
+                                     1, nullptr, nullptr, static_cast<cudaStream_t>(cuda_stream), err);
+}
+
+splash_status splash_attention_fwd_mle(const void *q, const void *k, const void *v, int32_t B, int32_t Hq,
+                                       int32_t Hkv, int64_t Lq, int64_t Lk, int32_t dqk, int32_t dv,
+                                       const int32_t *q_segment_ids, const int32_t *kv_segment_ids,
+                                       const splash_mask_info *mi, float scale, float softcap, float max_logit,
+                                       void *out, float *lse, void *cuda_stream) {
+  (void)q_segment_ids;
+  (void)kv_segment_ids;
+  if (!std::isfinite(max_logit)) return SPLASH_ERR_INVALID_ARG;
+  uint32_t *err = nullptr;
+  splash_status st = check_attention(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, out, lse, &err);
+  if (st != SPLASH_OK) return st;
+  return splash_attention_fwd_launch(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, max_logit, out,
+                                     lse, 1, nullptr, nullptr, static_cast<cudaStream_t>(cuda_stream), err);
+}
+
+splash_status splash_attention_bwd_workspace_size(int32_t B, int32_t Hq, int64_t Lq, int32_t dqk, size_t *bytes) {
+  if (bytes == nullptr || B <= 0 || Hq <= 0 || Lq <= 0 || dqk <= 0) return SPLASH_ERR_INVALID_ARG;
+  *bytes = splash_attention_bwd_workspace_bytes(B, Hq, Lq, dqk);
+  return SPLASH_OK;
+}
+
+splash_status splash_attention_bwd(const void *q, const void *k, const void *v, const void *out, const float *lse,
+                                   const void *dout, int32_t B, int32_t Hq, int32_t Hkv, int64_t Lq, int64_t Lk,
+                                   int32_t dqk, int32_t dv, const int32_t *q_segment_ids,
+                                   const int32_t *kv_segment_ids, splash_mask_info *mi, float scale, float softcap,
+                                   void *dq, void *dk, void *dv_out, void *workspace, size_t workspace_bytes,
+                                   void *cuda_stream) {
+  (void)q_segment_ids;
+  (void)kv_segment_ids;
+  if (dout == nullptr || dq == nullptr || dk == nullptr || dv_out == nullptr || workspace == nullptr)
+    return SPLASH_ERR_INVALID_ARG;
+  uint32_t *err = nullptr;
+  splash_status st = check_attention(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, out, lse, &err);
+  if (st != SPLASH_OK) return st;
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq) |
+                        reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv_out) |
+                        reinterpret_cast<uintptr_t>(lse) | reinterpret_cast<uintptr_t>(workspace);
+  if (mis & 15u) return SPLASH_ERR_INVALID_ARG;
+  if (workspace_bytes < splash_attention_bwd_workspace_bytes(B, Hq, Lq, dqk)) return SPLASH_ERR_INVALID_ARG;
+  if (dqk != dv || (dqk != 64 && dqk != 128) || mi->bq != 128 || mi->bk != 128) return SPLASH_ERR_UNSUPPORTED;
+  return splash_attention_bwd_launch(q, k, v, out, lse, dout, B, Hq, Hkv, Lq, Lk, dqk, mi, scale, softcap, dq, dk,
+                                     dv_out, workspace, static_cast<cudaStream_t>(cuda_stream), err);
 }
 
 splash_status splash_attention_fwd_split(const void *q, const void *k, const void *v, int32_t B, int32_t Hq,
@@ -236,8 +280,9 @@ splash_status splash_attention_fwd_split(const void *q, const void *k, const voi
   splash_status st =
       check_attention(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, o_part, lse_part, &err);
   if (st != SPLASH_OK) return st;
-  return splash_attention_fwd_launch(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, nullptr, nullptr,
-                                     num_splits, o_part, lse_part, static_cast<cudaStream_t>(cuda_stream), err);
+  return splash_attention_fwd_launch(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, NAN, nullptr,
+                                     nullptr, num_splits, o_part, lse_part, static_cast<cudaStream_t>(cuda_stream),
+                                     err);
 }
 
 splash_status splash_attention_merge(const float *o_part, const float *lse_part, int32_t num_splits, int64_t rows,

@@ -41,6 +41,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "internal.h"
@@ -108,6 +109,10 @@ struct FwdParams {
   float cap_inner;    // scale / cap                 (soft cap)
   float cap_log2;     // cap * log2(e)               (soft cap)
   int32_t use_softcap;
+  // Max Logit Estimate: every row's reference starts at this constant (log2
+  // units, c * log2(e)) instead of its first allowed keys' maximum
+  int32_t use_mle;
+  float mle_ref;
   int32_t dual_issuer;  // one MMA issuer per tile (pairs with different KV heads)
   __nv_bfloat16 *out;
   float *lse;
@@ -742,7 +747,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       if (t == 1 && !it.act1) continue;
       const int32_t h = t ? it.h1 : it.h0;
       const int64_t orow = ((int64_t)it.b * p.Hq + h) * p.Lq + (int64_t)it.qrow * p.bq + row;
-      float m_ref = -INFINITY;  // running reference (log2 units)
+      float m_ref = p.use_mle ? p.mle_ref : -INFINITY;  // running reference (log2 units)
       float l = 0.f;
       for (int32_t g = 0; g < it.nb && ok; ++g) {
         int32_t mn = p.mask_next[it.g0 + g];
@@ -1092,8 +1097,8 @@ using namespace splash;
 splash_status splash_attention_fwd_launch(const void *q, const void *k, const void *v, int32_t B,
                                           int32_t Hq, int32_t Hkv, int64_t Lq, int64_t Lk,
                                           int32_t dqk, int32_t dv, const splash_mask_info *mi,
-                                          float scale, float softcap, void *out, float *lse,
-                                          int32_t nsplit, float *o_part, float *lse_part,
+                                          float scale, float softcap, float max_logit, void *out,
+                                          float *lse, int32_t nsplit, float *o_part, float *lse_part,
                                           cudaStream_t stream, uint32_t *err_word) {
   FwdParams prm;
   prm.B = B;
@@ -1123,6 +1128,8 @@ splash_status splash_attention_fwd_launch(const void *q, const void *k, const vo
   prm.num_patterns = mi->counts_pending ? mi->cap_patterns : mi->num_patterns;
   prm.scale_log2 = scale * kLog2e;
   prm.use_softcap = softcap > 0.f ? 1 : 0;
+  prm.use_mle = std::isnan(max_logit) ? 0 : 1;  // NaN: off
+  prm.mle_ref = prm.use_mle ? max_logit * kLog2e : 0.f;
   // one issuer per tile only when the two query heads of an item read
   // different KV heads (MHA); shared K/V keeps one issuer for both tiles
   prm.dual_issuer = (prm.G == 1) ? 1 : 0;

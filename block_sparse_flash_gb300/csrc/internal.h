@@ -68,6 +68,15 @@ struct splash_mask_info {
 
   // capacities (elements)
   int64_t cap_rows = 0, cap_blocks = 0, cap_seg = 0, cap_patterns = 0, cap_hist = 0;
+
+  // --- column-major (transposed) table for the backward pass, rebuilt by
+  // each backward call; allocated on first use ---
+  int32_t *t_col_cnt = nullptr;       // [B_mask*nk]
+  int32_t *t_col_ptr = nullptr;       // [B_mask*nk + 1]
+  int32_t *t_col_rows = nullptr;      // [cap_blocks] q-block of each active block, by column
+  int32_t *t_col_next = nullptr;      // [cap_blocks] its pattern index or -1
+  uint32_t *t_pattern_bits = nullptr; // [cap_patterns][bk][bq/32], bit of (query, key) by key row
+  int64_t t_cap_cols = 0, t_cap_active = 0, t_cap_patterns = 0;
 };
 
 // mask_info.cu
@@ -75,6 +84,7 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
                                           int64_t Lq, int64_t Lk, int32_t bq, int32_t bk,
                                           cudaStream_t stream);
 void splash_mask_info_free_buffers(splash_mask_info *mi);
+void splash_mask_info_free_transposed(splash_mask_info *mi);
 // Makes the host totals current (waits for an asynchronous build's copy).
 splash_status splash_mask_info_sync_counts(splash_mask_info *mi);
 splash_status splash_classify_blocks_noalloc_impl(const splash_mask_spec *spec, int64_t Lq, int64_t Lk,
@@ -89,12 +99,19 @@ uint32_t *splash_device_error_word(int device);  // device address of the error 
 splash_status splash_attention_fwd_launch(const void *q, const void *k, const void *v, int32_t B,
                                           int32_t Hq, int32_t Hkv, int64_t Lq, int64_t Lk,
                                           int32_t dqk, int32_t dv, const splash_mask_info *mi,
-                                          float scale, float softcap, void *out, float *lse,
-                                          int32_t nsplit, float *o_part, float *lse_part,
+                                          float scale, float softcap, float max_logit, void *out,
+                                          float *lse, int32_t nsplit, float *o_part, float *lse_part,
                                           cudaStream_t stream, uint32_t *err_word);
 splash_status splash_attention_merge_launch(const float *o_part, const float *lse_part, int32_t nsplit,
                                             int64_t rows, int32_t dv, void *out, float *lse,
                                             cudaStream_t stream);
+// attention_bwd.cu (bq = bk = 128, dqk = dv = d in {64, 128})
+size_t splash_attention_bwd_workspace_bytes(int32_t B, int32_t Hq, int64_t Lq, int32_t dqk);
+splash_status splash_attention_bwd_launch(const void *q, const void *k, const void *v, const void *out,
+                                          const float *lse, const void *dout, int32_t B, int32_t Hq, int32_t Hkv,
+                                          int64_t Lq, int64_t Lk, int32_t d, splash_mask_info *mi, float scale,
+                                          float softcap, void *dq, void *dk, void *dv, void *workspace,
+                                          cudaStream_t stream, uint32_t *err_word);
 splash_status splash_wait_selftest_launch(uint64_t timeout_ns, cudaStream_t stream,
                                           uint32_t *err_word);
 

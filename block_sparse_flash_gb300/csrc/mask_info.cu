@@ -802,7 +802,17 @@ splash_status map_alloc(cudaError_t e) {
 
 }  // namespace
 
+void splash_mask_info_free_transposed(splash_mask_info *mi) {
+  void *dev[] = {mi->t_col_cnt, mi->t_col_ptr, mi->t_col_rows, mi->t_col_next, mi->t_pattern_bits};
+  for (void *p : dev)
+    if (p) cudaFree(p);
+  mi->t_col_cnt = mi->t_col_ptr = mi->t_col_rows = mi->t_col_next = nullptr;
+  mi->t_pattern_bits = nullptr;
+  mi->t_cap_cols = mi->t_cap_active = mi->t_cap_patterns = 0;
+}
+
 void splash_mask_info_free_buffers(splash_mask_info *mi) {
+  splash_mask_info_free_transposed(mi);
   void *dev[] = {mi->block_mask, mi->row_ptr, mi->active_rows, mi->active_cols, mi->mask_next,
                  mi->bounds_start, mi->bounds_end, mi->patterns, mi->pattern_bits, mi->row_order,
                  mi->row_cnt, mi->row_pcnt, mi->prow_ptr, mi->seg_summary, mi->part_row,

@@ -195,6 +195,33 @@ splash_status splash_attention_fwd(const void *q, const void *k, const void *v, 
                                    float scale, float softcap, void *out, float *lse,
                                    void *cuda_stream);
 
+/*
+ * splash_attention_fwd_mle -- the same forward with the Max Logit Estimate
+ * ("Pallas Kernels and Splash Attention" §5.4): every row's softmax reference
+ * is the constant max_logit (natural-log units, the same units as s_j after
+ * scale and soft cap) instead of a running maximum, so no block maximum is
+ * taken and the accumulator is never rescaled (alpha = 1):
+ *   out = sum_j exp(s_j - c) v_j / sum_j exp(s_j - c),  lse = c + ln sum_j exp(s_j - c)
+ * which equals splash_attention_fwd's result (c cancels) while c is in the
+ * safe range of §5.4 / exercise 10: with a soft cap, c = softcap always is.
+ * Outside it:
+ *   - a block whose sum of exponentials (base 2, fp32) would reach 2^64
+ *     (scores some 40 or more above c) moves that row's reference to the
+ *     block's maximum (the overflow guard of the plain kernel), so too small a
+ *     c costs time, not accuracy;
+ *   - a row whose scores all lie more than about 87 below c underflows: its
+ *     sum flushes to 0 and it gets out = 0, lse = -inf, like a fully masked
+ *     row (the underflow the lecture warns about; not detected).
+ *   max_logit  finite (else SPLASH_ERR_INVALID_ARG)
+ * Other arguments, supported shapes and errors as for splash_attention_fwd.
+ */
+splash_status splash_attention_fwd_mle(const void *q, const void *k, const void *v, int32_t B,
+                                       int32_t Hq, int32_t Hkv, int64_t Lq, int64_t Lk, int32_t dqk,
+                                       int32_t dv, const int32_t *q_segment_ids,
+                                       const int32_t *kv_segment_ids, const splash_mask_info *mi,
+                                       float scale, float softcap, float max_logit, void *out,
+                                       float *lse, void *cuda_stream);
+
 /* Largest num_splits accepted by the split-KV entry points. */
 #define SPLASH_MAX_SPLITS 256
 
@@ -238,6 +265,47 @@ splash_status splash_attention_fwd_split(const void *q, const void *k, const voi
  */
 splash_status splash_attention_merge(const float *o_part, const float *lse_part, int32_t num_splits,
                                      int64_t rows, int32_t dv, void *out, float *lse, void *cuda_stream);
+
+/*
+ * splash_attention_bwd -- gradients of splash_attention_fwd with respect to
+ * q, k and v for an upstream gradient dout, from the forward's out and lse
+ * ("Pallas Kernels and Splash Attention" §6.3: the forward's residual outputs
+ * serve the backward; "The maths and infra behind core LLM operations"
+ * (joto.ai), "LSE and Online Softmax": the probabilities are recomputed from
+ * the scores and LSE, P_ij = exp(s_ij - lse_i), instead of being stored).
+ * With dP_ij = dout_i . v_j, D_i = dout_i . out_i and
+ *   dS_ij = P_ij (dP_ij - D_i)  (times 1 - tanh^2(scale q.k / softcap) with a cap):
+ *   dv[b,g,j,:] = sum over heads h of group g, allowed i: P_ij dout[b,h,i,:]
+ *   dk[b,g,j,:] = scale * sum over h, i: dS_ij q[b,h,i,:]
+ *   dq[b,h,i,:] = scale * sum over allowed j: dS_ij k[b,g,j,:]
+ * (masked pairs contribute nothing; a key no query sees gets dk = dv = 0).
+ * Only the MaskInfo's active blocks are computed, visited column by column:
+ * the call rebuilds a column-major copy of the table inside the MaskInfo
+ * (device memory it allocates on first use, hence the non-const handle).
+ *
+ *   q, k, v, mi, scale, softcap   exactly as given to the forward
+ *   out  device bf16 [B][Hq][Lq][dv], lse device fp32 [B][Hq][Lq]: the forward's outputs
+ *   dout device bf16 [B][Hq][Lq][dv]
+ *   dq   device bf16 [B][Hq][Lq][dqk]   dk device bf16 [B][Hkv][Lk][dqk]
+ *   dv_out device bf16 [B][Hkv][Lk][dv]   (all fully overwritten)
+ *   workspace  device, 16-byte aligned, at least
+ *              splash_attention_bwd_workspace_size(B, Hq, Lq, dqk) bytes
+ *              (an fp32 dq accumulator and D); caller-owned, overwritten.
+ * All device pointers 16-byte aligned.  Supported: dqk == dv in {64, 128}
+ * and MaskInfo blocks bq = bk = 128 (other valid shapes return
+ * SPLASH_ERR_UNSUPPORTED).  dq is accumulated with fp32 atomic additions, so
+ * its last bits may differ between runs; dk and dv are deterministic.
+ * Errors as for splash_attention_fwd.
+ */
+splash_status splash_attention_bwd_workspace_size(int32_t B, int32_t Hq, int64_t Lq, int32_t dqk,
+                                                  size_t *bytes);
+splash_status splash_attention_bwd(const void *q, const void *k, const void *v, const void *out,
+                                   const float *lse, const void *dout, int32_t B, int32_t Hq,
+                                   int32_t Hkv, int64_t Lq, int64_t Lk, int32_t dqk, int32_t dv,
+                                   const int32_t *q_segment_ids, const int32_t *kv_segment_ids,
+                                   splash_mask_info *mi, float scale, float softcap, void *dq,
+                                   void *dk, void *dv_out, void *workspace, size_t workspace_bytes,
+                                   void *cuda_stream);
 
 /*
  * splash_classify_blocks_noalloc -- the block classification of a mask

@@ -74,6 +74,21 @@ def test_invalid_arguments_are_rejected_before_any_launch(splash):
     fake = ctypes.c_void_p(16)
     assert f(fake, fake, fake, 1, 2, 2, 256, 256, 64, 64, None, None, fake, 0.0, 0.0, fake, fake, null) == 1
     assert f(fake, fake, fake, 1, 2, 2, 256, 256, 64, 64, None, None, fake, float("nan"), 0.0, fake, fake, null) == 1
+    # the Max Logit Estimate variant and the backward: NULL tensors, bad scale
+    fm = lib.splash_attention_fwd_mle
+    assert fm(None, None, None, 1, 2, 2, 256, 256, 64, 64, None, None, None, 0.125, 0.0, 1.0, None, None,
+              null) == 1
+    assert fm(fake, fake, fake, 1, 2, 2, 256, 256, 64, 64, None, None, fake, 0.125, 0.0, float("inf"), fake,
+              fake, null) == 1
+    fb = lib.splash_attention_bwd
+    assert fb(None, None, None, None, None, None, 1, 2, 2, 256, 256, 64, 64, None, None, None, 0.125, 0.0,
+              None, None, None, None, 0, null) == 1
+    assert fb(fake, fake, fake, fake, fake, fake, 1, 2, 2, 256, 256, 64, 64, None, None, fake, -1.0, 0.0,
+              fake, fake, fake, fake, 1 << 20, null) == 1
+    n = ctypes.c_size_t(0)
+    assert lib.splash_attention_bwd_workspace_size(2, 4, 1024, 128, ctypes.byref(n)) == 0
+    assert n.value == 2 * 4 * 1024 * 128 * 4 + 2 * 4 * 1024 * 4   # fp32 dq accumulator + D
+    assert lib.splash_attention_bwd_workspace_size(2, 4, 1024, 128, None) == 1
     # counts / shape / to_host on a NULL handle
     assert lib.splash_mask_info_counts(None, None, None, None, None) == 1
     assert lib.splash_mask_info_shape(None, None, None, None, None, None) == 1

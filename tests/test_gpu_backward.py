@@ -1,0 +1,149 @@
+"""Backward pass on the GPU against the f64 backward oracle.
+
+The GPU backward is fed the GPU forward's out and lse (its own product
+path); the oracle differentiates the forward's definition from q, k, v and
+dout, taking D_i = dout_i . out_i from its own forward output rounded to
+bf16 (the backward's interface receives the stored bf16 output and defines D
+from it; the exact D differs from it by that rounding, which moves small dq
+rows by several per cent).  Gradients are compared per tensor with the tolerances of the
+forward's output (bf16 results of fp32 arithmetic on bf16 operands):
+max |error| <= 2e-2 * max |reference| and, per row (one query's dq, one
+key's dk / dv), ||error|| <= 2e-2 * max(||reference row||, 1e-2 * the
+largest reference row norm)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+GRAD_ABS = 2e-2   # relative to the tensor's largest |reference| entry
+GRAD_ROW = 2e-2   # per-row relative norm
+
+
+@pytest.fixture(scope="module")
+def bsf():
+    from block_sparse_flash_gb300 import build as b
+    b.build()
+    import block_sparse_flash_gb300 as m
+    return m
+
+
+def compare_grad(got, ref, label, extra=None):
+    """extra: optional per-row absolute allowance added to the row bound."""
+    g = got.float().cpu().numpy().astype(np.float64).reshape(-1, got.shape[-1])
+    r = ref.reshape(-1, ref.shape[-1])
+    assert np.all(np.isfinite(g)), f"{label}: non-finite"
+    scale = max(float(np.abs(r).max()), 1e-30)
+    err = np.abs(g - r)
+    assert float(err.max()) <= GRAD_ABS * scale, f"{label}: max abs err {err.max():.3e} (max |ref| {scale:.3e})"
+    rn = np.linalg.norm(r, axis=1)
+    bound = GRAD_ROW * np.maximum(rn, 1e-2 * max(float(rn.max()), 1e-30))
+    if extra is not None:
+        bound = bound + extra.reshape(-1)
+    ratio = float((np.linalg.norm(g - r, axis=1) / bound).max())
+    assert ratio <= 1.0, f"{label}: row error {ratio:.3f} x its bound"
+    return float(err.max()) / scale, ratio
+
+
+CASES = [
+    # label, B, Hq, Hkv, L, d, softcap, mask kwargs
+    ("causal MHA d128", 1, 2, 2, 512, 128, 0.0, dict(causal=True)),
+    ("causal GQA d128 softcap 30", 2, 4, 2, 1024, 128, 30.0, dict(causal=True)),
+    ("window 300 + causal d64", 1, 4, 1, 1024, 64, 0.0, dict(causal=True, wl=299)),
+    ("documents + causal, batch 2", 2, 2, 1, 768, 128, 0.0, dict(causal=True, docs=True)),
+    ("two-sided window, no causal", 1, 2, 2, 640, 128, 20.0, dict(causal=False, wl=200, wr=150)),
+]
+
+
+def make(bsf, B, Hq, Hkv, L, d, causal=True, wl=-1, wr=-1, docs=False, seed=0, kv_seg=None):
+    q = workloads.normal_bf16((B, Hq, L, d), seed + 1)
+    k = workloads.normal_bf16((B, Hkv, L, d), seed + 2)
+    v = workloads.normal_bf16((B, Hkv, L, d), seed + 3)
+    g = workloads.normal_bf16((B, Hq, L, d), seed + 5)
+    qs = workloads.random_segment_ids(B, L, seed + 4, 4, True) if docs else None
+    ks = kv_seg if kv_seg is not None else qs
+    mi = bsf.build_mask_info(bsf.MaskSpec(causal, wl, wr, qs.cuda() if qs is not None else None,
+                                          ks.cuda() if ks is not None else None), L, L, 128, 128)
+    ospec = oracle.MaskSpec(causal, wl, wr, qs.numpy() if qs is not None else None,
+                            ks.numpy() if ks is not None else None)
+    return q, k, v, g, mi, ospec
+
+
+def run_both(bsf, q, k, v, g, mi, ospec, scale, cap):
+    qd, kd, vd, gd = q.cuda(), k.cuda(), v.cuda(), g.cuda()
+    out, lse = bsf.attention_fwd(qd, kd, vd, mi, scale, cap)
+    dq, dk, dv = bsf.attention_bwd(qd, kd, vd, out, lse, gd, mi, scale, cap)
+    torch.cuda.synchronize()
+    assert bsf.last_device_error() == 0, "device error"
+    # the reference takes D_i = dout_i . out_i from a stored bf16 output, as
+    # the backward's interface defines it: the oracle's own forward output,
+    # rounded to bf16 (never the GPU's)
+    O, _ = oracle.attention(q, k, v, ospec, scale, cap)
+    out_bf16 = torch.from_numpy(O).to(torch.bfloat16)
+    ref = oracle.attention_bwd(q, k, v, g, ospec, scale, cap, out=out_bf16)
+    return (dq, dk, dv), ref
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_backward_matches_the_oracle(bsf, case):
+    label, B, Hq, Hkv, L, d, cap, kw = case
+    q, k, v, g, mi, ospec = make(bsf, B, Hq, Hkv, L, d, seed=13 * CASES.index(case), **kw)
+    scale = 1.0 / math.sqrt(d)
+    (dq, dk, dv), ref = run_both(bsf, q, k, v, g, mi, ospec, scale, cap)
+    errs = [compare_grad(dq, ref["dq"], f"{label}: dq"), compare_grad(dk, ref["dk"], f"{label}: dk"),
+            compare_grad(dv, ref["dv"], f"{label}: dv")]
+    print(label, errs)
+    mi.close()
+
+
+def test_keys_no_query_sees_get_zero_gradients(bsf):
+    # key block 2 carries a segment ID no query has: its column of the table is
+    # empty, and dk = dv = 0 there
+    B, Hq, Hkv, L, d = 1, 2, 1, 512, 128
+    qs = torch.zeros((B, L), dtype=torch.int32)
+    ks = torch.zeros((B, L), dtype=torch.int32)
+    ks[:, 256:384] = 7
+    q = workloads.normal_bf16((B, Hq, L, d), 91)
+    k = workloads.normal_bf16((B, Hkv, L, d), 92)
+    v = workloads.normal_bf16((B, Hkv, L, d), 93)
+    g = workloads.normal_bf16((B, Hq, L, d), 94)
+    mi = bsf.build_mask_info(bsf.MaskSpec(False, -1, -1, qs.cuda(), ks.cuda()), L, L, 128, 128)
+    ospec = oracle.MaskSpec(False, -1, -1, qs.numpy(), ks.numpy())
+    (dq, dk, dv), ref = run_both(bsf, q, k, v, g, mi, ospec, d ** -0.5, 0.0)
+    assert torch.all(dk[:, :, 256:384] == 0) and torch.all(dv[:, :, 256:384] == 0)
+    compare_grad(dq, ref["dq"], "dq")
+    compare_grad(dk, ref["dk"], "dk")
+    compare_grad(dv, ref["dv"], "dv")
+    mi.close()
+
+
+def test_dk_dv_are_deterministic_and_dq_nearly(bsf):
+    q, k, v, g, mi, _ = make(bsf, 1, 4, 2, 1024, 128, seed=40)
+    qd, kd, vd, gd = q.cuda(), k.cuda(), v.cuda(), g.cuda()
+    out, lse = bsf.attention_fwd(qd, kd, vd, mi, 128 ** -0.5, 0.0)
+    a = bsf.attention_bwd(qd, kd, vd, out, lse, gd, mi, 128 ** -0.5, 0.0)
+    b = bsf.attention_bwd(qd, kd, vd, out, lse, gd, mi, 128 ** -0.5, 0.0)
+    torch.cuda.synchronize()
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    # dq: fp32 atomic additions in varying order, then one bf16 rounding
+    assert (a[0].float() - b[0].float()).abs().max().item() <= 1e-2 * a[0].float().abs().max().item()
+    mi.close()
+
+
+def test_backward_rejects_unsupported_shapes(bsf):
+    q, k, v, g, mi, _ = make(bsf, 1, 2, 2, 256, 128)
+    qd, kd, vd, gd = q.cuda(), k.cuda(), v.cuda(), g.cuda()
+    out, lse = bsf.attention_fwd(qd, kd, vd, mi, 0.1, 0.0)
+    with pytest.raises(bsf.SplashError):  # workspace too small
+        bsf.attention_bwd(qd, kd, vd, out, lse, gd, mi, 0.1, 0.0,
+                          workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    mi.close()
+    mi64 = bsf.build_mask_info(bsf.MaskSpec(True, -1, -1, None, None), 256, 256, 64, 64)
+    with pytest.raises(bsf.SplashError):  # 64 x 64 blocks: unsupported by the backward
+        bsf.attention_bwd(qd, kd, vd, out, lse, gd, mi64, 0.1, 0.0)
+    mi64.close()

@@ -181,3 +181,22 @@ def test_head_subset_gives_the_same_rows():
     # one head's key contribution: the full dk minus the other heads' equals it
     others = oracle.attention_bwd(q, k, v, g, spec, 0.5, heads=[(1, 0), (1, 1), (1, 3)])
     np.testing.assert_allclose(part["dk"][1] + others["dk"][1], full["dk"][1], rtol=1e-12, atol=1e-13)
+
+
+def test_delta_from_the_exact_output_is_the_exact_delta():
+    # D_i = dout_i . out_i equals sum_j P_ij dP_ij when out is the exact
+    # forward output; a rounded output moves only D (and through it dq, dk)
+    B, Hq, Hkv, L, d = 1, 2, 1, 128, 32
+    q = workloads.normal_bf16((B, Hq, L, d), 81)
+    k = workloads.normal_bf16((B, Hkv, L, d), 82)
+    v = workloads.normal_bf16((B, Hkv, L, d), 83)
+    g = workloads.normal_bf16((B, Hq, L, d), 84)
+    spec = MaskSpec(True, 40, -1)
+    O, _ = oracle.attention(q, k, v, spec, 0.2, 5.0)
+    exact = oracle.attention_bwd(q, k, v, g, spec, 0.2, 5.0)
+    given = oracle.attention_bwd(q, k, v, g, spec, 0.2, 5.0, out=O)
+    for name in ("dq", "dk", "dv", "delta"):
+        np.testing.assert_allclose(given[name], exact[name], rtol=1e-11, atol=1e-12)
+    rounded = oracle.attention_bwd(q, k, v, g, spec, 0.2, 5.0, out=torch.from_numpy(O).to(torch.bfloat16))
+    np.testing.assert_array_equal(rounded["dv"], exact["dv"])
+    assert not np.array_equal(rounded["dq"], exact["dq"])

@@ -69,6 +69,81 @@ def test_merge_is_order_independent_over_many_segments():
 
 
 # ---------------------------------------------------------------------------
+# Max Logit Estimate ("Pallas Kernels and Splash Attention" §5.4, exercise 10).
+# ---------------------------------------------------------------------------
+
+
+def test_mle_exp_limits_are_the_printed_ones_and_numpys():
+    g = read_golden("exercise10_mle_safe_range.txt")
+    over, sub = oracle.exp_limits(np.float32)
+    assert over == pytest.approx(float(g["overflow_limit"]), abs=0.05)
+    assert sub == pytest.approx(float(g["subnormal_limit"]), abs=0.05)
+    # brute force on float32 exp itself: finite just below, inf just above;
+    # normal just above the subnormal bound, subnormal just below it
+    with np.errstate(over="ignore", under="ignore"):
+        assert np.isfinite(np.exp(np.float32(over - 0.01)))
+        assert np.isinf(np.exp(np.float32(over + 0.01)))
+        tiny = np.finfo(np.float32).tiny
+        assert np.exp(np.float32(sub + 0.01)) >= tiny
+        assert 0 < np.exp(np.float32(sub - 0.01)) < tiny
+
+
+def test_mle_safe_range_matches_exercise10():
+    g = read_golden("exercise10_mle_safe_range.txt")
+    lo, hi = oracle.mle_safe_range(float(g["score_max"]), float(g["row_max_floor"]), np.float32)
+    tol = float(g["tolerance"])
+    assert lo == pytest.approx(float(g["c_low"]), abs=tol)
+    assert hi == pytest.approx(float(g["c_high"]), abs=tol)
+
+
+def test_mle_constant_cancels_inside_the_range_and_fails_outside():
+    # scores spanning the exercise's [-30, 40]: one row reaching 40, one whose
+    # maximum is -30
+    rng = np.random.default_rng(10)
+    top = np.concatenate([[40.0], rng.uniform(-30, 40, size=255)])
+    low = np.concatenate([[-30.0], rng.uniform(-60, -30, size=255)])
+    lo, hi = oracle.mle_safe_range(40.0, -30.0, np.float32, n_terms=256)
+    for c in np.linspace(lo + 0.5, hi - 0.5, 9):
+        for row in (top, low):
+            w, l, lse = oracle.mle_softmax(row, c, np.float32)
+            assert np.all(np.isfinite(w)) and l > 0
+            # terms far below the row's maximum may flush; they weigh < 1e-6
+            np.testing.assert_allclose(w, oracle.safe_softmax(row), rtol=2e-4, atol=1e-6)
+            m = np.max(row)
+            assert float(lse) == pytest.approx(m + np.log(np.sum(np.exp(row - m))), abs=2e-4)
+    # in float64 any moderate constant gives the same weights (c cancels)
+    for c in (-200.0, 0.0, 40.0, 300.0):
+        w, _, _ = oracle.mle_softmax(top, c, np.float64)
+        np.testing.assert_allclose(w, oracle.safe_softmax(top), rtol=1e-12, atol=0)
+    # below the range the top row overflows; far above it the low row's
+    # exponentials all underflow to zero
+    w, l, _ = oracle.mle_softmax(top, lo - 2.0 - np.log(256), np.float32)
+    assert not np.all(np.isfinite(w))
+    # the sum's own bound: 256 equal maxima overflow the sum (not the terms)
+    # just below c = 40 - ln(FLT_MAX) + ln(256), and not just above it
+    flat = np.full(256, 40.0)
+    w, l, _ = oracle.mle_softmax(flat, lo - 0.05, np.float32)
+    assert np.isinf(l) and np.all(w == 0)
+    w, l, _ = oracle.mle_softmax(flat, lo + 0.05, np.float32)
+    assert np.isfinite(l)
+    np.testing.assert_allclose(w, 1 / 256, rtol=1e-6)
+    w, l, _ = oracle.mle_softmax(low, hi + 20.0, np.float32)
+    assert l == 0 and not np.any(np.isfinite(w))
+
+
+def test_mle_softcap_constant_is_always_safe():
+    # with scores cap * tanh(.) in (-cap, cap) and c = cap, exp(s - c) <= 1
+    # never overflows, and a row keeps normal exponentials while 2 cap < 87
+    for cap in (10.0, 30.0, 43.0):
+        s = cap * np.tanh(np.random.default_rng(int(cap)).normal(scale=5.0, size=512) / 1.0)
+        s[0] = -cap * (1 - 1e-7)
+        lo, hi = oracle.mle_safe_range(cap, -cap, np.float32)
+        assert lo < cap < hi
+        w, l, _ = oracle.mle_softmax(s, cap, np.float32)
+        np.testing.assert_allclose(w, oracle.safe_softmax(s), rtol=2e-4, atol=1e-6)
+
+
+# ---------------------------------------------------------------------------
 # MaskInfo: the pages' worked examples (§6.1, §6.2, §6.6, exercises 11, 12).
 # ---------------------------------------------------------------------------
 
