@@ -24,7 +24,8 @@
 //   * kernels per call: the transposed table (column counts, scan, fill,
 //     pattern transpose), a prep kernel (D, dq accumulator cleared), the main
 //     kernel and a conversion of the fp32 dq accumulator to bf16;
-//   * main kernel: one persistent CTA per SM, 384 threads; warps 0-7 (two
+//   * main kernel: one persistent CTA per SM, items dealt longest column
+//     first in serpentine order; 384 threads; warps 0-7 (two
 //     warpgroups) do the elementwise work: a thread owns one key (TMEM lane)
 //     and half of the block's 128 queries; warp 8 issues TMA loads; warp 9
 //     issues the MMAs from one elected lane of the converged warp; warps
@@ -35,8 +36,9 @@
 //       dK  += dS^T Q   (A = dS^T from shared memory, K-major)
 //       dQ   = dS K     (A = the same shared buffer read MN-major)
 //     dQ reuses the dP^T columns once dS is formed; it is added to an fp32
-//     accumulator in global memory with vector reductions.  dK and dV stay in
-//     TMEM for the whole item;
+//     accumulator in global memory with vector reductions, transposed through
+//     shared memory first so that each reduction covers whole 128-byte rows.
+//     dK and dV stay in TMEM for the whole item;
 //   * Q is double-buffered, dO single-buffered (it is first needed by dP one
 //     MMA group after Q);
 //   * every wait is bounded: on timeout the CTA raises an error bit, stops,
@@ -133,6 +135,17 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdParams &p, int64_t w) {
   return it;
 }
 
+// Work item of this CTA's round k: items are ordered longest column first
+// (kv block ascending) and dealt in serpentine order (CTA c takes item
+// k*G + c on even rounds, k*G + G-1-c on odd ones); -1 past the end, -2 for
+// a slot of the last round that has no item.
+__device__ __forceinline__ int64_t bwd_item_of_round(const BwdParams &p, int64_t k) {
+  const int64_t g = gridDim.x;
+  if (k * g >= p.num_items) return -1;
+  const int64_t w = k * g + ((k & 1) ? g - 1 - blockIdx.x : blockIdx.x);
+  return w < p.num_items ? w : -2;
+}
+
 // (query head, q-block, pattern) of the item's iteration t: heads outermost
 __device__ __forceinline__ void bwd_step(const BwdParams &p, const BwdItem &it, int32_t t, int32_t &h,
                                          int32_t &i, int32_t &mn) {
@@ -208,7 +221,10 @@ __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const C
   using C = BwdCfg<D>;
   uint32_t n = 0, kv = 0;
   bool ok = true;
-  for (int64_t w = blockIdx.x; w < p.num_items && ok; w += gridDim.x) {
+  for (int64_t k = 0; ok; ++k) {
+    const int64_t w = bwd_item_of_round(p, k);
+    if (w == -1) break;
+    if (w < 0) continue;
     const BwdItem it = bwd_item(p, w);
     const int32_t N = p.G * it.cnt;
     if (N == 0) continue;
@@ -313,7 +329,10 @@ __device__ void bwd_mma(const BwdParams &p, uint32_t tmem, uint32_t s0, const Bw
   const uint32_t tS = tmem + C::T_S, tDP = tmem + C::T_DP, tDV = tmem + C::T_DV, tDK = tmem + C::T_DK;
   uint32_t n = 0, kv = 0;
   bool ok = true;
-  for (int64_t w = blockIdx.x; w < p.num_items && ok; w += gridDim.x) {
+  for (int64_t k = 0; ok; ++k) {
+    const int64_t w = bwd_item_of_round(p, k);
+    if (w == -1) break;
+    if (w < 0) continue;
     const BwdItem it = bwd_item(p, w);
     const int32_t N = p.G * it.cnt;
     if (N == 0) continue;
@@ -359,14 +378,21 @@ __device__ void bwd_mma(const BwdParams &p, uint32_t tmem, uint32_t s0, const Bw
 }
 
 // ------------------------------------------------------------ elementwise warps
-// dQ(m) from TMEM (lane = query, this warpgroup's half of the D columns) added
-// to the fp32 accumulator row.
+// dQ(m) from TMEM (lane = query, this warpgroup's half of the D columns)
+// added to the fp32 accumulator.  Each 32 x 32 piece is transposed through
+// this warp's own 4 KB of the dS^T buffer (its dS^T rows, free once the
+// MMAs of iteration m have completed): written row per lane (128B swizzle),
+// read back so that eight lanes cover one row's 128 contiguous bytes, so each
+// vector reduction of the warp touches 4 rows' lines instead of 32.
+// base: accumulator row of the warp's first query, at this half's columns.
 template <int D>
-__device__ __forceinline__ bool bwd_readout(const BwdParams &p, uint32_t tDQ, uint32_t m, float *dst,
-                                            volatile int *abort, uint32_t bars_dq_full, uint32_t bars_dq_empty,
-                                            int lane) {
+__device__ __forceinline__ bool bwd_readout(const BwdParams &p, uint32_t tDQ, uint32_t m, float *base,
+                                            uint32_t stage, volatile int *abort, uint32_t bars_dq_full,
+                                            uint32_t bars_dq_empty, int lane) {
   if (!__all_sync(0xffffffffu, mbar_wait(bars_dq_full, m & 1u, abort, p.timeout_ns))) return false;
   tc_fence_after();
+  const uint32_t wrow = stage + (uint32_t)lane * 128u;
+  const int rsub = lane >> 3, x = lane & 7;
 #pragma unroll
   for (int c = 0; c < D / 64; ++c) {
     uint32_t r[32];
@@ -374,12 +400,18 @@ __device__ __forceinline__ bool bwd_readout(const BwdParams &p, uint32_t tDQ, ui
     tmem_wait_ld();
     reg_fence32(r);
 #pragma unroll
-    for (int x = 0; x < 32; x += 4)
-      red_add_v4(dst + 32 * c + x, __uint_as_float(r[x]), __uint_as_float(r[x + 1]), __uint_as_float(r[x + 2]),
-                 __uint_as_float(r[x + 3]));
+    for (int y = 0; y < 8; ++y)
+      st_shared_v4(wrow + (uint32_t)(((y ^ (lane & 7)) << 4)), r[4 * y], r[4 * y + 1], r[4 * y + 2], r[4 * y + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int row = it * 4 + rsub;
+      const float4 v = ld_shared_f4(stage + (uint32_t)row * 128u + (uint32_t)((x ^ (row & 7)) << 4));
+      red_add_v4(base + (int64_t)row * D + 32 * c + 4 * x, v.x, v.y, v.z, v.w);
+    }
+    __syncwarp();
   }
   tc_fence_before();
-  __syncwarp();
   if (lane == 0) mbar_arrive(bars_dq_empty);
   return true;
 }
@@ -400,8 +432,13 @@ __device__ void bwd_work(const BwdParams &p, uint32_t tmem, uint32_t s0, const B
   const float mul = CAP ? p.cap_log2 : p.scale_log2;
   uint32_t n = 0;
   bool ok = true;
-  float *prev_dst = nullptr;  // dq accumulator row of the previous iteration
-  for (int64_t w = blockIdx.x; w < p.num_items && ok; w += gridDim.x) {
+  float *prev_dst = nullptr;  // dq accumulator: the previous iteration's first row of this warp
+  // this warp's 32 rows of its half of the dS^T buffer (staging for the dQ readout)
+  const uint32_t stage = s0 + C::OFF_DS + wg * C::CHUNK + (uint32_t)(wq * 32) * 128u;
+  for (int64_t k = 0; ok; ++k) {
+    const int64_t w = bwd_item_of_round(p, k);
+    if (w == -1) break;
+    if (w < 0) continue;
     const BwdItem it = bwd_item(p, w);
     const int32_t N = p.G * it.cnt;
     const int64_t krow = ((int64_t)it.b * p.Hkv + it.kvh) * p.Lk + (int64_t)it.j * 128 + jj;
@@ -465,7 +502,8 @@ __device__ void bwd_work(const BwdParams &p, uint32_t tmem, uint32_t s0, const B
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.p_ready());
       // ---- dQ(n-1) out of TMEM (its MMAs ran while P(n) was formed)
-      if (t > 0 && !(ok = bwd_readout<D>(p, tDQ, n - 1, prev_dst, abort, bar.dq_full(), bar.dq_empty(), lane)))
+      if (t > 0 &&
+          !(ok = bwd_readout<D>(p, tDQ, n - 1, prev_dst, stage, abort, bar.dq_full(), bar.dq_empty(), lane)))
         break;
       // ---- dS^T(n) = P^T (dP^T - D) [(1 - t^2)], bf16 into the swizzled dS^T buffer
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar.dp_full(), n & 1u, abort, p.timeout_ns)))) break;
@@ -504,11 +542,12 @@ __device__ void bwd_work(const BwdParams &p, uint32_t tmem, uint32_t s0, const B
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.ds_ready());
-      prev_dst = p.dq_acc + (((int64_t)it.b * p.Hq + h) * p.Lq + (int64_t)i * 128 + jj) * D + wg * (D / 2);
+      prev_dst = p.dq_acc + (((int64_t)it.b * p.Hq + h) * p.Lq + (int64_t)i * 128 + wq * 32) * D + wg * (D / 2);
     }
     if (!ok) break;
     // ---- the item's last dQ, then dK, dV (complete once that dQ has landed)
-    if (!(ok = bwd_readout<D>(p, tDQ, n - 1, prev_dst, abort, bar.dq_full(), bar.dq_empty(), lane))) break;
+    if (!(ok = bwd_readout<D>(p, tDQ, n - 1, prev_dst, stage, abort, bar.dq_full(), bar.dq_empty(), lane)))
+      break;
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) {
       uint32_t rk[32], rv[32];

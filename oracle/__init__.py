@@ -235,20 +235,20 @@ def _f64(x) -> np.ndarray:
 
 
 def attention_bwd(q, k, v, dout, spec: MaskSpec, scale: float, softcap: float = 0.0, heads=None,
-                  nthreads: int = 0, out=None):
+                  nthreads: int = 0, delta=None):
     """Backward attention in f64 (gradients of the forward with respect to q,
     k and v for the upstream gradient dout).
 
     q [B, Hq, Lq, dqk], k [B, Hkv, Lk, dqk], v [B, Hkv, Lk, dv],
     dout [B, Hq, Lq, dv]: torch tensors (bf16 widens exactly) or float64
-    arrays.  out (optional, shaped like dout): a stored forward output from
-    which D_i = dout_i . out_i is taken; without it D is exact.  heads:
+    arrays.  delta (optional, [B, Hq, Lq]): D_i to use instead of the exact
+    sum_j P_ij dP_ij (for instance dout_i . out_i of a stored output).  heads:
     optional list of (b, h) pairs; only those query heads are differentiated
     (dq of the others stays 0 and dk / dv then hold the listed heads'
     contributions).  Returns dict(dq, dk, dv, lse, delta) of f64 arrays shaped
     like q, k, v, [B, Hq, Lq], [B, Hq, Lq]."""
     qf, kf, vf, gf = _f64(q), _f64(k), _f64(v), _f64(dout)
-    of = _f64(out) if out is not None else None
+    df = _f64(delta) if delta is not None else None
     B, Hq, Lq, dqk = qf.shape
     _, Hkv, Lk, _ = kf.shape
     dv = vf.shape[3]
@@ -268,13 +268,13 @@ def attention_bwd(q, k, v, dout, spec: MaskSpec, scale: float, softcap: float = 
     for b, h in heads:
         g = h // G
         qh, gh = np.ascontiguousarray(qf[b, h]), np.ascontiguousarray(gf[b, h])
-        oh = np.ascontiguousarray(of[b, h]) if of is not None else None
+        dh_in = np.ascontiguousarray(df[b, h]) if df is not None else None
         kh, vh = np.ascontiguousarray(kf[b, g]), np.ascontiguousarray(vf[b, g])
         dqh = np.zeros((Lq, dqk))
         lh = np.zeros(Lq)
         dh = np.zeros(Lq)
         _check(lib().oracle_attention_bwd_head(qh.ctypes.data, kh.ctypes.data, vh.ctypes.data, gh.ctypes.data,
-                                               oh.ctypes.data if oh is not None else None, b, Lq, Lk, dqk, dv, ctypes.byref(s), float(scale), float(softcap),
+                                               dh_in.ctypes.data if dh_in is not None else None, b, Lq, Lk, dqk, dv, ctypes.byref(s), float(scale), float(softcap),
                                                nthreads or default_threads(), dqh.ctypes.data, tdk.ctypes.data,
                                                tdv.ctypes.data, lh.ctypes.data, dh.ctypes.data),
                "attention_bwd")

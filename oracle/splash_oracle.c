@@ -387,7 +387,7 @@ int oracle_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, in
  * rows (dk, dv), each row owned by one thread. */
 
 typedef struct {
-    const double *q, *k, *v, *dout, *out;
+    const double *q, *k, *v, *dout, *delta_in;
     int64_t b, Lq, Lk, dqk, dv;
     const oracle_mask_spec *sp;
     double scale, softcap;
@@ -454,8 +454,8 @@ static void *bwd_rows_worker(void *arg)
         for (int64_t j = 0; j < jb->Lk; ++j)
             if (ok[j]) l += exp(s[j] - m);
         double lse = m + log(l), D = 0.0;
-        if (jb->out) { /* D from a given forward output: dout_i . out_i */
-            for (int64_t d = 0; d < jb->dv; ++d) D += jb->dout[i * jb->dv + d] * jb->out[i * jb->dv + d];
+        if (jb->delta_in) { /* D given (e.g. dout_i . out_i of a stored output) */
+            D = jb->delta_in[i];
         } else {
             for (int64_t j = 0; j < jb->Lk; ++j)
                 if (ok[j]) D += exp(s[j] - lse) * bwd_dp(jb, i, j);
@@ -498,14 +498,14 @@ static void *bwd_keys_worker(void *arg)
 
 /* q [Lq][dqk] and dout [Lq][dv] are head h's rows of batch b; k [Lk][dqk] and
  * v [Lk][dv] those of its key/value head; all f64.  b selects the segment-ID
- * batch row (ignored without segment IDs).  out [Lq][dv] is optional: when
- * given, D_i = dout_i . out_i is taken from it (the form a backward that
- * receives the stored forward output uses); when NULL, D_i = sum_j P_ij dP_ij
- * exactly.  Writes dq [Lq][dqk], this head's contributions dk [Lk][dqk] and
+ * batch row (ignored without segment IDs).  delta_in [Lq] is optional: when
+ * given, D_i is taken from it (for instance dout_i . out_i of a stored
+ * forward output); when NULL, D_i = sum_j P_ij dP_ij exactly.  Writes
+ * dq [Lq][dqk], this head's contributions dk [Lk][dqk] and
  * dv [Lk][dv] (a GQA group sums them), the row log-sum-exp lse [Lq] and
  * D = delta [Lq]. */
 int oracle_attention_bwd_head(const double *q, const double *k, const double *v, const double *dout,
-                              const double *out, int64_t b, int64_t Lq, int64_t Lk, int64_t dqk, int64_t dv,
+                              const double *delta_in, int64_t b, int64_t Lq, int64_t Lk, int64_t dqk, int64_t dv,
                               const oracle_mask_spec *sp, double scale, double softcap, int nthreads,
                               double *dq, double *dk, double *dvo, double *lse, double *delta)
 {
@@ -514,7 +514,7 @@ int oracle_attention_bwd_head(const double *q, const double *k, const double *v,
         return ORACLE_ERR_ARG;
     if (sp->q_seg != NULL && (sp->kv_seg == NULL || b >= sp->batch)) return ORACLE_ERR_ARG;
     bwd_job jb;
-    jb.q = q; jb.k = k; jb.v = v; jb.dout = dout; jb.out = out;
+    jb.q = q; jb.k = k; jb.v = v; jb.dout = dout; jb.delta_in = delta_in;
     jb.b = sp->q_seg != NULL ? b : 0;
     jb.Lq = Lq; jb.Lk = Lk; jb.dqk = dqk; jb.dv = dv;
     jb.sp = sp; jb.scale = scale; jb.softcap = softcap;

@@ -2,10 +2,10 @@
 
 The GPU backward is fed the GPU forward's out and lse (its own product
 path); the oracle differentiates the forward's definition from q, k, v and
-dout, taking D_i = dout_i . out_i from its own forward output rounded to
-bf16 (the backward's interface receives the stored bf16 output and defines D
-from it; the exact D differs from it by that rounding, which moves small dq
-rows by several per cent).  Gradients are compared per tensor with the tolerances of the
+dout (exact D).  The GPU forms D_i = dout_i . out_i from the stored bf16
+output, which moves small dq rows by several per cent; each dq row's bound
+therefore adds an allowance derived from that rounding (d_term_allowance).
+Gradients are compared per tensor with the tolerances of the
 forward's output (bf16 results of fp32 arithmetic on bf16 operands):
 max |error| <= 2e-2 * max |reference| and, per row (one query's dq, one
 key's dk / dv), ||error|| <= 2e-2 * max(||reference row||, 1e-2 * the
@@ -80,13 +80,26 @@ def run_both(bsf, q, k, v, g, mi, ospec, scale, cap):
     dq, dk, dv = bsf.attention_bwd(qd, kd, vd, out, lse, gd, mi, scale, cap)
     torch.cuda.synchronize()
     assert bsf.last_device_error() == 0, "device error"
-    # the reference takes D_i = dout_i . out_i from a stored bf16 output, as
-    # the backward's interface defines it: the oracle's own forward output,
-    # rounded to bf16 (never the GPU's)
-    O, _ = oracle.attention(q, k, v, ospec, scale, cap)
-    out_bf16 = torch.from_numpy(O).to(torch.bfloat16)
-    ref = oracle.attention_bwd(q, k, v, g, ospec, scale, cap, out=out_bf16)
+    ref = oracle.attention_bwd(q, k, v, g, ospec, scale, cap)
     return (dq, dk, dv), ref
+
+
+def d_term_allowance(q, k, v, g, ospec, scale, cap):
+    """Per-row allowance for dq from D_i = dout_i . out_i being formed from
+    the stored bf16 output instead of the exact one.  Each element of that
+    output is within 2^-9 |O_id| (its bf16 rounding) plus 2^-9 sum_j P_ij
+    |v_jd| (the bf16 rounding of P before the PV product) of the exact O, so
+    |dD_i| <= 2^-9 sum_d |dout_id| (|O_id| + sum_j P_ij |v_jd|).  A change
+    dD_i of D moves dq_i by exactly dD_i times the dq_i of a backward with
+    dout = 0 and D = 1 (pinned in the oracle tests), so the allowance is
+    |dD_i| * ||that row||.  The weighted sums are the oracle's own forward
+    with other values (|v|)."""
+    O, _ = oracle.attention(q, k, v, ospec, scale, cap)
+    A, _ = oracle.attention(q, k, v.abs(), ospec, scale, cap)
+    dD = 2.0 ** -9 * np.sum(np.abs(g.double().numpy()) * (np.abs(O) + A), axis=-1)
+    B, Hq, Lq, _ = q.shape
+    unit = oracle.attention_bwd(q, k, v, torch.zeros_like(g), ospec, scale, cap, delta=np.ones((B, Hq, Lq)))
+    return dD * np.linalg.norm(unit["dq"], axis=-1)
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
@@ -95,7 +108,8 @@ def test_backward_matches_the_oracle(bsf, case):
     q, k, v, g, mi, ospec = make(bsf, B, Hq, Hkv, L, d, seed=13 * CASES.index(case), **kw)
     scale = 1.0 / math.sqrt(d)
     (dq, dk, dv), ref = run_both(bsf, q, k, v, g, mi, ospec, scale, cap)
-    errs = [compare_grad(dq, ref["dq"], f"{label}: dq"), compare_grad(dk, ref["dk"], f"{label}: dk"),
+    extra = d_term_allowance(q, k, v, g, ospec, scale, cap)
+    errs = [compare_grad(dq, ref["dq"], f"{label}: dq", extra), compare_grad(dk, ref["dk"], f"{label}: dk"),
             compare_grad(dv, ref["dv"], f"{label}: dv")]
     print(label, errs)
     mi.close()

@@ -183,9 +183,10 @@ def test_head_subset_gives_the_same_rows():
     np.testing.assert_allclose(part["dk"][1] + others["dk"][1], full["dk"][1], rtol=1e-12, atol=1e-13)
 
 
-def test_delta_from_the_exact_output_is_the_exact_delta():
+def test_given_delta_from_the_exact_output_is_the_exact_delta():
     # D_i = dout_i . out_i equals sum_j P_ij dP_ij when out is the exact
-    # forward output; a rounded output moves only D (and through it dq, dk)
+    # forward output; another D moves only dq and dk, linearly:
+    # dq_i changes by -scale (D'_i - D_i) sum_j P_ij (1 - t_ij^2) k_j
     B, Hq, Hkv, L, d = 1, 2, 1, 128, 32
     q = workloads.normal_bf16((B, Hq, L, d), 81)
     k = workloads.normal_bf16((B, Hkv, L, d), 82)
@@ -194,9 +195,11 @@ def test_delta_from_the_exact_output_is_the_exact_delta():
     spec = MaskSpec(True, 40, -1)
     O, _ = oracle.attention(q, k, v, spec, 0.2, 5.0)
     exact = oracle.attention_bwd(q, k, v, g, spec, 0.2, 5.0)
-    given = oracle.attention_bwd(q, k, v, g, spec, 0.2, 5.0, out=O)
+    given = oracle.attention_bwd(q, k, v, g, spec, 0.2, 5.0, delta=np.sum(g.double().numpy() * O, axis=-1))
     for name in ("dq", "dk", "dv", "delta"):
         np.testing.assert_allclose(given[name], exact[name], rtol=1e-11, atol=1e-12)
-    rounded = oracle.attention_bwd(q, k, v, g, spec, 0.2, 5.0, out=torch.from_numpy(O).to(torch.bfloat16))
-    np.testing.assert_array_equal(rounded["dv"], exact["dv"])
-    assert not np.array_equal(rounded["dq"], exact["dq"])
+    shift = np.random.default_rng(5).normal(size=(B, Hq, L))
+    moved = oracle.attention_bwd(q, k, v, g, spec, 0.2, 5.0, delta=exact["delta"] + shift)
+    unit = oracle.attention_bwd(q, k, v, torch.zeros_like(g), spec, 0.2, 5.0, delta=np.ones((B, Hq, L)))
+    np.testing.assert_array_equal(moved["dv"], exact["dv"])
+    np.testing.assert_allclose(moved["dq"], exact["dq"] + shift[..., None] * unit["dq"], rtol=1e-9, atol=1e-11)
