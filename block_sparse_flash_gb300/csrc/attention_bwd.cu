@@ -36,8 +36,8 @@
 //       dK  += dS^T Q   (A = dS^T from shared memory, K-major)
 //       dQ   = dS K     (A = the same shared buffer read MN-major)
 //     dQ reuses the dP^T columns once dS is formed; it is added to an fp32
-//     accumulator in global memory with vector reductions, transposed through
-//     shared memory first so that each reduction covers whole 128-byte rows.
+//     accumulator in global memory by asynchronous TMA tile reductions staged
+//     in shared memory, so the columns are free again as soon as they are read.
 //     dK and dV stay in TMEM for the whole item;
 //   * Q is double-buffered, dO single-buffered (it is first needed by dP one
 //     MMA group after Q);
@@ -192,8 +192,12 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
                : "memory");
 }
 
-__device__ __forceinline__ void red_add_v4(float *dst, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d)
+// Tiled TMA reduction: the box at (x, y) of the tensor map += the shared
+// memory tile at src (fp32 add, bulk-group completion).
+__device__ __forceinline__ void tma_reduce_add_2d(const void *tmap, uint32_t src, int32_t x, int32_t y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(src), "r"(x), "r"(y)
                : "memory");
 }
 
@@ -379,46 +383,49 @@ __device__ void bwd_mma(const BwdParams &p, uint32_t tmem, uint32_t s0, const Bw
 
 // ------------------------------------------------------------ elementwise warps
 // dQ(m) from TMEM (lane = query, this warpgroup's half of the D columns)
-// added to the fp32 accumulator.  Each 32 x 32 piece is transposed through
-// this warp's own 4 KB of the dS^T buffer (its dS^T rows, free once the
-// MMAs of iteration m have completed): written row per lane (128B swizzle),
-// read back so that eight lanes cover one row's 128 contiguous bytes, so each
-// vector reduction of the warp touches 4 rows' lines instead of 32.
-// base: accumulator row of the warp's first query, at this half's columns.
+// added to the fp32 accumulator by TMA tile reductions: each 32 x 32 piece
+// is staged in this warp's own 4 KB of the dS^T buffer (its dS^T rows, free
+// once the MMAs of iteration m have completed; 128B-swizzled, as the tensor
+// map expects) and reduced into global memory asynchronously.  TMEM is
+// released as soon as the pieces are in registers; a later staging (or dS
+// store) into the same 4 KB first waits until the reduction has read it.
+// row0: accumulator row of the warp's first query.
 template <int D>
-__device__ __forceinline__ bool bwd_readout(const BwdParams &p, uint32_t tDQ, uint32_t m, float *base,
-                                            uint32_t stage, volatile int *abort, uint32_t bars_dq_full,
-                                            uint32_t bars_dq_empty, int lane) {
+__device__ __forceinline__ bool bwd_readout(const BwdParams &p, const CUtensorMap *tmDQ, uint32_t tDQ, uint32_t m,
+                                            int32_t row0, int32_t col0, uint32_t stage, volatile int *abort,
+                                            uint32_t bars_dq_full, uint32_t bars_dq_empty, int lane) {
   if (!__all_sync(0xffffffffu, mbar_wait(bars_dq_full, m & 1u, abort, p.timeout_ns))) return false;
   tc_fence_after();
   const uint32_t wrow = stage + (uint32_t)lane * 128u;
-  const int rsub = lane >> 3, x = lane & 7;
 #pragma unroll
   for (int c = 0; c < D / 64; ++c) {
     uint32_t r[32];
     tmem_ld32(tDQ + 32u * c, r);
     tmem_wait_ld();
     reg_fence32(r);
+    if (c + 1 == D / 64) {  // TMEM fully read: the columns may take the next dP^T
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars_dq_empty);
+    }
+    if (lane == 0) bulk_wait_read_all();  // the previous reduction has read the staging
+    __syncwarp();
 #pragma unroll
     for (int y = 0; y < 8; ++y)
       st_shared_v4(wrow + (uint32_t)(((y ^ (lane & 7)) << 4)), r[4 * y], r[4 * y + 1], r[4 * y + 2], r[4 * y + 3]);
+    fence_proxy_async_shared();
     __syncwarp();
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-      const int row = it * 4 + rsub;
-      const float4 v = ld_shared_f4(stage + (uint32_t)row * 128u + (uint32_t)((x ^ (row & 7)) << 4));
-      red_add_v4(base + (int64_t)row * D + 32 * c + 4 * x, v.x, v.y, v.z, v.w);
+    if (lane == 0) {
+      tma_reduce_add_2d(tmDQ, stage, col0 + 32 * c, row0);
+      bulk_commit_group();
     }
-    __syncwarp();
   }
-  tc_fence_before();
-  if (lane == 0) mbar_arrive(bars_dq_empty);
   return true;
 }
 
 template <int D, bool CAP>
-__device__ void bwd_work(const BwdParams &p, uint32_t tmem, uint32_t s0, const BwdBars &bar, volatile int *abort,
-                         int warp, int lane) {
+__device__ void bwd_work(const BwdParams &p, const CUtensorMap *tmDQ, uint32_t tmem, uint32_t s0, const BwdBars &bar,
+                         volatile int *abort, int warp, int lane) {
   using C = BwdCfg<D>;
   const int wg = warp >> 2;   // which 64 queries of the block
   const int wq = warp & 3;    // TMEM lane quarter
@@ -432,7 +439,8 @@ __device__ void bwd_work(const BwdParams &p, uint32_t tmem, uint32_t s0, const B
   const float mul = CAP ? p.cap_log2 : p.scale_log2;
   uint32_t n = 0;
   bool ok = true;
-  float *prev_dst = nullptr;  // dq accumulator: the previous iteration's first row of this warp
+  int32_t prev_row = 0;  // dq accumulator row of the previous iteration's first query of this warp
+  const int32_t col0 = wg * (D / 2);
   // this warp's 32 rows of its half of the dS^T buffer (staging for the dQ readout)
   const uint32_t stage = s0 + C::OFF_DS + wg * C::CHUNK + (uint32_t)(wq * 32) * 128u;
   for (int64_t k = 0; ok; ++k) {
@@ -502,8 +510,8 @@ __device__ void bwd_work(const BwdParams &p, uint32_t tmem, uint32_t s0, const B
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.p_ready());
       // ---- dQ(n-1) out of TMEM (its MMAs ran while P(n) was formed)
-      if (t > 0 &&
-          !(ok = bwd_readout<D>(p, tDQ, n - 1, prev_dst, stage, abort, bar.dq_full(), bar.dq_empty(), lane)))
+      if (t > 0 && !(ok = bwd_readout<D>(p, tmDQ, tDQ, n - 1, prev_row, col0, stage, abort, bar.dq_full(),
+                                         bar.dq_empty(), lane)))
         break;
       // ---- dS^T(n) = P^T (dP^T - D) [(1 - t^2)], bf16 into the swizzled dS^T buffer
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar.dp_full(), n & 1u, abort, p.timeout_ns)))) break;
@@ -515,6 +523,8 @@ __device__ void bwd_work(const BwdParams &p, uint32_t tmem, uint32_t s0, const B
         tmem_wait_ld();
         reg_fence32(r0);
         reg_fence32(r1);
+        if (lane == 0) bulk_wait_read_all();  // dQ staging in these rows has been read
+        __syncwarp();
         const uint32_t row = s0 + C::OFF_DS + wg * C::CHUNK + jj * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {  // 8 queries = one 16-byte chunk
@@ -542,11 +552,12 @@ __device__ void bwd_work(const BwdParams &p, uint32_t tmem, uint32_t s0, const B
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.ds_ready());
-      prev_dst = p.dq_acc + (((int64_t)it.b * p.Hq + h) * p.Lq + (int64_t)i * 128 + wq * 32) * D + wg * (D / 2);
+      prev_row = (int32_t)(((int64_t)it.b * p.Hq + h) * p.Lq + (int64_t)i * 128 + wq * 32);
     }
     if (!ok) break;
     // ---- the item's last dQ, then dK, dV (complete once that dQ has landed)
-    if (!(ok = bwd_readout<D>(p, tDQ, n - 1, prev_dst, stage, abort, bar.dq_full(), bar.dq_empty(), lane)))
+    if (!(ok = bwd_readout<D>(p, tmDQ, tDQ, n - 1, prev_row, col0, stage, abort, bar.dq_full(), bar.dq_empty(),
+                              lane)))
       break;
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) {
@@ -574,13 +585,14 @@ __device__ void bwd_work(const BwdParams &p, uint32_t tmem, uint32_t s0, const B
     tc_fence_before();
   }
   if (!ok && lane == 0) bwd_raise(p, abort, SPLASH_DEV_TIMEOUT_SOFTMAX);
+  if (lane == 0) bulk_wait_all();  // this warp's dq reductions have completed
 }
 
 template <int D, bool CAP>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 splash_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                  const BwdParams p) {
+                  const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -620,6 +632,7 @@ splash_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmDO);
+    tma_prefetch_desc(&tmDQ);
   }
   tc_fence_before();
   __syncthreads();
@@ -635,7 +648,7 @@ splash_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     }
   } else {
     regs_increase<kBwdWorkRegs>();
-    bwd_work<D, CAP>(p, tmem, s0, bar, abort, warp, lane);
+    bwd_work<D, CAP>(p, &tmDQ, tmem, s0, bar, abort, warp, lane);
   }
 
   tc_fence_before();
@@ -785,7 +798,7 @@ __global__ void pattern_transpose_kernel(const uint32_t *pattern_bits, const uns
   }
 }
 
-bool make_bwd_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows) {
+PFN_cuTensorMapEncodeTiled_v12000 bwd_encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -796,6 +809,12 @@ bool make_bwd_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t ro
         q == cudaDriverEntryPointSuccess)
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
   });
+  return fn;
+}
+
+// bf16 [rows][cols] tiles of 128 rows x 64 columns (128B swizzle)
+bool make_bwd_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows) {
+  auto fn = bwd_encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols * 2};
@@ -806,15 +825,30 @@ bool make_bwd_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t ro
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [rows][cols] tiles of 32 rows x 32 columns (128B swizzle), for the dq
+// accumulator's reductions
+bool make_bwd_map_f32(CUtensorMap *map, void *base, uint64_t cols, uint64_t rows) {
+  auto fn = bwd_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 4};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t elem[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D, bool CAP>
 splash_status launch_bwd(const void *q, const void *k, const void *v, const void *dout, const BwdParams &prm,
                          int sms, cudaStream_t stream) {
   using C = BwdCfg<D>;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   if (!make_bwd_map(&tq, q, D, (uint64_t)prm.B * prm.Hq * prm.Lq) ||
       !make_bwd_map(&tk, k, D, (uint64_t)prm.B * prm.Hkv * prm.Lk) ||
       !make_bwd_map(&tv, v, D, (uint64_t)prm.B * prm.Hkv * prm.Lk) ||
-      !make_bwd_map(&tdo, dout, D, (uint64_t)prm.B * prm.Hq * prm.Lq))
+      !make_bwd_map(&tdo, dout, D, (uint64_t)prm.B * prm.Hq * prm.Lq) ||
+      !make_bwd_map_f32(&tdq, prm.dq_acc, D, (uint64_t)prm.B * prm.Hq * prm.Lq))
     return SPLASH_ERR_CUDA;
   static int configured_device = -1;
   int dev = 0;
@@ -826,7 +860,7 @@ splash_status launch_bwd(const void *q, const void *k, const void *v, const void
   }
   const int64_t grid = prm.num_items < sms ? prm.num_items : sms;
   if (grid <= 0) return SPLASH_OK;
-  splash_bwd_kernel<D, CAP><<<(unsigned)grid, kBwdThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, prm);
+  splash_bwd_kernel<D, CAP><<<(unsigned)grid, kBwdThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, prm);
   SPLASH_CUDA_TRY(cudaGetLastError());
   splash_count_launches(1);
   return SPLASH_OK;
