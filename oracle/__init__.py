@@ -152,11 +152,13 @@ class MaskInfo:
 
 
 def mask_info(spec: MaskSpec, Lq: int, Lk: int, bq: int, bk: int, nthreads: int = 0) -> MaskInfo:
-    """Builds MaskInfo by brute-force classification of every element."""
+    """Builds MaskInfo by brute-force classification of every element.  When
+    Lq or Lk is not a multiple of the block, the grid is padded to whole blocks
+    and padding positions are masked."""
     L = lib()
     s, keep = spec._c()
     nbm = spec.batch_rows
-    nq, nk = Lq // bq, Lk // bk
+    nq, nk = -(-Lq // bq), -(-Lk // bk)  # padded grid: the last blocks may be ragged
     bm = np.zeros((nbm, nq, nk), dtype=np.int8)
     A, Ap, npairs = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
     _check(L.oracle_mask_classify(ctypes.byref(s), Lq, Lk, bq, bk, nthreads or default_threads(),

@@ -32,6 +32,9 @@
  *   - LSE is the natural-log log-sum-exp of the scaled (and capped) scores,
  *     LSE = m + ln(l) [OPS] "LSE and Online Softmax";
  *   - a GQA query head h reads key/value head h / (Hq/Hkv) [L13 §5.2];
+ *   - lengths that are not a multiple of the block: the block grid is padded
+ *     to whole blocks and padding positions are masked [L13 §2.3], so a block
+ *     with padding is never full;
  *   - MaskInfo: block class 0 = empty, 1 = partial, 2 = full; active blocks in
  *     row-major order (q-block ascending, then kv-block ascending); bounds
  *     flags mark the first and last active block of each q-block row; partial
@@ -82,6 +85,22 @@ int oracle_allowed(const oracle_mask_spec *sp, int64_t b, int64_t Lq, int64_t Lk
     return allowed(sp, b, Lq, Lk, i, j);
 }
 
+/* The predicate on the padded block grid: when Lq or Lk is not a multiple of
+ * the block, the last q-block / kv-block extends past the sequence and its
+ * padding positions are masked ([L13 §2.3]: ragged edges are padded so that
+ * every block has the same size; padding contributes nothing). */
+static int allowed_padded(const oracle_mask_spec *sp, int64_t b, int64_t Lq, int64_t Lk,
+                          int64_t i, int64_t j)
+{
+    if (i >= Lq || j >= Lk) return 0;
+    return allowed(sp, b, Lq, Lk, i, j);
+}
+
+static int64_t ceil_div(int64_t a, int64_t b)
+{
+    return (a + b - 1) / b;
+}
+
 static int64_t batch_rows_of(const oracle_mask_spec *sp)
 {
     return sp->q_seg != NULL ? sp->batch : 1;
@@ -114,7 +133,7 @@ static void *classify_worker(void *arg)
             int64_t n = 0;
             for (int64_t i = r * jb->bq; i < (r + 1) * jb->bq; ++i)
                 for (int64_t j = c * jb->bk; j < (c + 1) * jb->bk; ++j)
-                    n += allowed(jb->sp, bm, jb->Lq, jb->Lk, i, j);
+                    n += allowed_padded(jb->sp, bm, jb->Lq, jb->Lk, i, j);
             int8_t cls = (n == 0) ? 0 : (n == jb->bq * jb->bk ? 2 : 1);
             jb->block_mask[row * jb->nk + c] = cls;
             jb->block_count[row * jb->nk + c] = n;
@@ -144,11 +163,11 @@ int oracle_mask_classify(const oracle_mask_spec *sp, int64_t Lq, int64_t Lk, int
                          int64_t bk, int nthreads, int8_t *block_mask,
                          int64_t *num_active, int64_t *num_partial, int64_t *allowed_pairs)
 {
-    if (!sp || !block_mask || bq <= 0 || bk <= 0 || Lq % bq || Lk % bk) return ORACLE_ERR_ARG;
+    if (!sp || !block_mask || bq <= 0 || bk <= 0 || Lq <= 0 || Lk <= 0) return ORACLE_ERR_ARG;
     if (sp->q_seg != NULL && (sp->kv_seg == NULL || sp->batch <= 0)) return ORACLE_ERR_ARG;
     classify_job jb;
     jb.sp = sp; jb.Lq = Lq; jb.Lk = Lk; jb.bq = bq; jb.bk = bk;
-    jb.nq = Lq / bq; jb.nk = Lk / bk; jb.nbm = batch_rows_of(sp);
+    jb.nq = ceil_div(Lq, bq); jb.nk = ceil_div(Lk, bk); jb.nbm = batch_rows_of(sp);
     jb.block_mask = block_mask;
     jb.block_count = (int64_t *)malloc(sizeof(int64_t) * (size_t)(jb.nbm * jb.nq * jb.nk));
     if (!jb.block_count) return ORACLE_ERR_NOMEM;
@@ -188,9 +207,9 @@ int oracle_mask_table(const oracle_mask_spec *sp, int64_t Lq, int64_t Lk, int64_
                       uint8_t *bounds_end, uint8_t *patterns, int64_t pattern_capacity,
                       int64_t *num_patterns)
 {
-    if (!sp || !block_mask || !row_ptr || bq <= 0 || bk <= 0 || Lq % bq || Lk % bk)
+    if (!sp || !block_mask || !row_ptr || bq <= 0 || bk <= 0 || Lq <= 0 || Lk <= 0)
         return ORACLE_ERR_ARG;
-    int64_t nq = Lq / bq, nk = Lk / bk, nbm = batch_rows_of(sp);
+    int64_t nq = ceil_div(Lq, bq), nk = ceil_div(Lk, bk), nbm = batch_rows_of(sp);
     size_t pbytes = (size_t)(bq * bk);
     uint8_t *cand = (uint8_t *)malloc(pbytes);
     uint64_t *hashes = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)(pattern_capacity > 0 ? pattern_capacity : 1));
@@ -212,7 +231,7 @@ int oracle_mask_table(const oracle_mask_spec *sp, int64_t Lq, int64_t Lk, int64_
                     for (int64_t di = 0; di < bq; ++di)
                         for (int64_t dj = 0; dj < bk; ++dj)
                             cand[di * bk + dj] =
-                                (uint8_t)allowed(sp, bm, Lq, Lk, r * bq + di, c * bk + dj);
+                                (uint8_t)allowed_padded(sp, bm, Lq, Lk, r * bq + di, c * bk + dj);
                     uint64_t h = fnv1a(cand, pbytes);
                     int64_t found = -1;
                     for (int64_t u = 0; u < P; ++u)

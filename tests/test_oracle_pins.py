@@ -298,7 +298,9 @@ def dense_mask(spec, Lq, Lk):
 
 def brute_maskinfo(spec, Lq, Lk, bq, bk):
     dm = dense_mask(spec, Lq, Lk)
-    nbm, nq, nk = dm.shape[0], Lq // bq, Lk // bk
+    nbm, nq, nk = dm.shape[0], -(-Lq // bq), -(-Lk // bk)
+    # ragged lengths: pad the dense mask to whole blocks with masked entries
+    dm = np.pad(dm, ((0, 0), (0, nq * bq - Lq), (0, nk * bk - Lk)))
     blocks = dm.reshape(nbm, nq, bq, nk, bk).transpose(0, 1, 3, 2, 4)
     cnt = blocks.sum(axis=(3, 4))
     cls = np.where(cnt == 0, 0, np.where(cnt == bq * bk, 2, 1)).astype(np.int8)
@@ -343,10 +345,47 @@ def tiny_specs():
 
 
 @pytest.mark.parametrize("L,spec", tiny_specs())
-@pytest.mark.parametrize("bq,bk", [(4, 4), (8, 8), (16, 16), (8, 16), (16, 4)])
+@pytest.mark.parametrize("bq,bk", [(4, 4), (8, 8), (16, 16), (8, 16), (16, 4), (5, 7), (16, 12)])
 def test_maskinfo_matches_dense_brute_force(L, spec, bq, bk):
-    mi = oracle.mask_info(spec, L, L, bq, bk)
-    ref = brute_maskinfo(spec, L, L, bq, bk)
+    check_against_brute_force(spec, L, L, bq, bk)
+
+
+def ragged_specs():
+    rng = np.random.default_rng(77)
+    out = []
+    for Lq, Lk in ((30, 30), (37, 37), (45, 29), (21, 50)):
+        for causal in (False, True):
+            for wl, wr in ((-1, -1), (3, -1), (7, 2)):
+                out.append((Lq, Lk, MaskSpec(causal=causal, window_left=wl, window_right=wr)))
+        qs = workloads.random_segment_ids(2, Lq, int(rng.integers(1 << 30)), 3, True).numpy()
+        ks = workloads.random_segment_ids(2, Lk, int(rng.integers(1 << 30)), 3, True).numpy()
+        out.append((Lq, Lk, MaskSpec(causal=True, q_segment_ids=qs, kv_segment_ids=ks)))
+    return out
+
+
+@pytest.mark.parametrize("Lq,Lk,spec", ragged_specs())
+@pytest.mark.parametrize("bq,bk", [(8, 8), (16, 16), (8, 16)])
+def test_ragged_maskinfo_matches_dense_brute_force(Lq, Lk, spec, bq, bk):
+    check_against_brute_force(spec, Lq, Lk, bq, bk)
+
+
+def test_ragged_grid_worked_example():
+    g = read_golden("ragged_1000_256.txt")
+    L, b = int(g["L"]), int(g["block"])
+    mi = oracle.mask_info(MaskSpec(), L, L, b, b)
+    computed = mi.num_active * b * b
+    assert computed == int(g["computed_elements"])
+    assert mi.allowed_pairs == L * L
+    assert round(100 * mi.allowed_pairs / computed, 1) == float(g["useful_percent"])
+    # the 7 blocks on the ragged edge are partial (padding masked); the last
+    # row's, the last column's and the corner's patterns are the three
+    assert mi.num_partial == 7 and mi.num_patterns == 3
+    assert int(np.count_nonzero(mi.block_mask == 2)) == 9
+
+
+def check_against_brute_force(spec, Lq, Lk, bq, bk):
+    mi = oracle.mask_info(spec, Lq, Lk, bq, bk)
+    ref = brute_maskinfo(spec, Lq, Lk, bq, bk)
     np.testing.assert_array_equal(mi.block_mask, ref["block_mask"])
     assert mi.row_ptr.tolist() == ref["row_ptr"]
     assert mi.active_rows.tolist() == ref["active_rows"]
