@@ -39,8 +39,8 @@ splash_status check_spec(const splash_mask_spec *spec, int64_t Lq, int64_t Lk) {
 splash_status check_geometry(int64_t Lq, int64_t Lk, int32_t bq, int32_t bk) {
   if (Lq <= 0 || Lk <= 0 || bq <= 0 || bk <= 0) return SPLASH_ERR_INVALID_ARG;
   if (!valid_block(bq) || !valid_block(bk)) return SPLASH_ERR_UNSUPPORTED;
-  if (Lq % bq != 0 || Lk % bk != 0) return SPLASH_ERR_UNSUPPORTED;  // ragged lengths: not in this build
-  if (Lq / bq > 65535 || Lk > (int64_t)1 << 30 || Lq > (int64_t)1 << 30) return SPLASH_ERR_UNSUPPORTED;
+  // ragged lengths are padded to whole blocks (the padding is masked)
+  if ((Lq + bq - 1) / bq > 65535 || Lk > (int64_t)1 << 30 || Lq > (int64_t)1 << 30) return SPLASH_ERR_UNSUPPORTED;
   return SPLASH_OK;
 }
 
@@ -263,6 +263,7 @@ splash_status splash_attention_bwd(const void *q, const void *k, const void *v, 
   if (mis & 15u) return SPLASH_ERR_INVALID_ARG;
   if (workspace_bytes < splash_attention_bwd_workspace_bytes(B, Hq, Lq, dqk)) return SPLASH_ERR_INVALID_ARG;
   if (dqk != dv || (dqk != 64 && dqk != 128) || mi->bq != 128 || mi->bk != 128) return SPLASH_ERR_UNSUPPORTED;
+  if (Lq % 128 != 0 || Lk % 128 != 0) return SPLASH_ERR_UNSUPPORTED;  // the backward takes whole blocks
   return splash_attention_bwd_launch(q, k, v, out, lse, dout, B, Hq, Hkv, Lq, Lk, dqk, mi, scale, softcap, dq, dk,
                                      dv_out, workspace, static_cast<cudaStream_t>(cuda_stream), err);
 }

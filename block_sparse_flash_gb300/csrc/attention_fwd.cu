@@ -30,10 +30,14 @@
 //     warp 11 only hands its registers to the softmax warpgroups;
 //   * TMEM (512 columns): S_t / P_t at column 128t (P, bf16 pairs, overwrites
 //     the first half of S after it is read), O_t at 256 + 128t;
-//   * the exponent is base 2 (log2 e folded into the scale); the output
-//     accumulator is only rescaled when a row's maximum grows by more than
-//     2^8 (the running reference stays exact: P <= 256 and l, O use the same
-//     reference);
+//   * the exponent is base 2 (log2 e folded into the scale); a row's
+//     reference moves only to its first allowed keys' maximum and when a
+//     block's sum of exponentials would reach 2^64 (so the steady state takes
+//     no running maximum and the accumulator is rarely rescaled; l and O use
+//     the same reference, and O / l does not depend on it);
+//   * ragged lengths: the last q-block / kv-block may extend past Lq / Lk;
+//     its padding is masked by the block's pattern and padding rows are
+//     never stored;
 //   * every wait is bounded (mbar_wait): on timeout the CTA raises an error
 //     bit, stops all roles, drains its copies and MMAs and frees TMEM.
 #include <cuda.h>
@@ -747,6 +751,8 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       if (t == 1 && !it.act1) continue;
       const int32_t h = t ? it.h1 : it.h0;
       const int64_t orow = ((int64_t)it.b * p.Hq + h) * p.Lq + (int64_t)it.qrow * p.bq + row;
+      // rows past a ragged Lq are padding: computed (all masked), never stored
+      const bool row_out = row_valid && (int64_t)it.qrow * p.bq + row < p.Lq;
       float m_ref = p.use_mle ? p.mle_ref : -INFINITY;  // running reference (log2 units)
       float l = 0.f;
       for (int32_t g = 0; g < it.nb && ok; ++g) {
@@ -920,7 +926,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
 #pragma unroll
             for (int x = 0; x < 32; ++x) r[x] = 0u;
           }
-          if (row_valid) {
+          if (row_out) {
 #pragma unroll
             for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * inv);
 #pragma unroll
@@ -966,7 +972,9 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             fence_proxy_async_shared();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tmO, stage, 64 * hh, (int32_t)(orow - lane));
+              // O viewed as [B*Hq][Lq][DV]: rows past a ragged Lq fall outside
+              // the tensor and the store clips them
+              tma_store_3d(&tmO, stage, 64 * hh, it.qrow * p.bq + wq * 32, it.b * p.Hq + h);
               bulk_commit_group();
             }
           }
@@ -984,7 +992,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
 #pragma unroll
           for (int x = 0; x < 32; ++x) r[x] = 0u;
         }
-        if (row_valid) {
+        if (row_out) {
           uint32_t o[16];
 #pragma unroll
           for (int x = 0; x < 16; ++x) {
@@ -997,7 +1005,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         }
       }
       }
-      if (row_valid) {
+      if (row_out) {
         const float lse_v = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
         if (p.o_part != nullptr)
           p.lse_part[(int64_t)it.split * p.part_rows + orow] = lse_v;
@@ -1061,6 +1069,20 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [planes][rows][cols] bf16 with 64-column x box_rows x 1 boxes (128B swizzle)
+bool make_map_3d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint64_t planes,
+                 uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {cols, rows, planes};
+  const cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
+  const cuuint32_t box[3] = {64, box_rows, 1};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, elem,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int DQK, int DV, int BK>
 splash_status launch(const void *q, const void *k, const void *v, const FwdParams &prm, cudaStream_t stream) {
   using C = Cfg<DQK, DV, BK>;
@@ -1068,7 +1090,8 @@ splash_status launch(const void *q, const void *k, const void *v, const FwdParam
   if (!make_map(&tq, q, DQK, (uint64_t)prm.B * prm.Hq * prm.Lq, 128) ||
       !make_map(&tk, k, DQK, (uint64_t)prm.B * prm.Hkv * prm.Lk, BK) ||
       !make_map(&tv, v, DV, (uint64_t)prm.B * prm.Hkv * prm.Lk, BK) ||
-      (C::STAGE && prm.o_part == nullptr && !make_map(&to, prm.out, DV, (uint64_t)prm.B * prm.Hq * prm.Lq, 32)))
+      (C::STAGE && prm.o_part == nullptr &&
+       !make_map_3d(&to, prm.out, DV, (uint64_t)prm.Lq, (uint64_t)prm.B * prm.Hq, 32)))
     return SPLASH_ERR_CUDA;
   if (!C::STAGE || prm.o_part != nullptr) to = tq;  // unused (no staging, or split partials)
   static int configured_device = -1;

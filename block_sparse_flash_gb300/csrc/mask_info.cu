@@ -38,17 +38,21 @@ struct DevMask {
   const int32_t *qseg, *kvseg;
   int64_t Lq, Lk, nq, nk;
   int32_t bq, bk, nbm;
+  int32_t ragged;  // Lq or Lk is not a multiple of its block: the grid is padded
 };
 
 // The band part of the joint mask for query i: allowed keys j lie in [lo, hi]
-// intersected with [c0, c1].
+// intersected with [c0, c1].  Padding of a ragged grid (queries i >= Lq, keys
+// j >= Lk) is masked ("Pallas Kernels and Splash Attention" §2.3: ragged
+// edges are padded so that every block has the same size).
 __device__ __forceinline__ void band_range(const DevMask &m, int64_t i, int64_t c0, int64_t c1,
                                            int64_t &lo, int64_t &hi) {
   lo = c0;
-  hi = c1;
+  hi = min(c1, m.Lk - 1);
   if (m.causal) hi = min(hi, i);
   if (m.wl >= 0) lo = max(lo, i - m.wl);
   if (m.wr >= 0) hi = min(hi, i + m.wr);
+  if (i >= m.Lq) hi = lo - 1;
 }
 
 // 32 mask bits of query i against keys j0 .. j0+31 (bit t = key j0 + t).
@@ -71,7 +75,7 @@ __device__ __forceinline__ uint32_t row_word(const DevMask &m, int32_t bm, int64
 }
 
 __device__ __forceinline__ int32_t q_segment(const DevMask &m, int32_t bm, int64_t i) {
-  return m.qseg ? m.qseg[(int64_t)bm * m.Lq + i] : 0;
+  return (m.qseg && i < m.Lq) ? m.qseg[(int64_t)bm * m.Lq + i] : 0;  // padding rows: unused
 }
 
 // The band part in closed form: key j is allowed for query i iff
@@ -90,15 +94,19 @@ __device__ __forceinline__ void band_limits(const DevMask &m, int64_t &A, int64_
 // Rows i in [r0, r1] and keys j in [c0, c1]: the block holds an allowed pair
 // iff some row i has i + A >= c0 and i - W <= c1; it is full iff every row has
 // lo(i) = max(c0, i - W) = c0 and hi(i) = min(c1, i + A) = c1, i.e. iff
-// r1 - W <= c0 and r0 + A >= c1 (lo and hi are nondecreasing in i).
+// r1 - W <= c0 and r0 + A >= c1 (lo and hi are nondecreasing in i).  On a
+// ragged grid the rows and keys are first clipped to the sequences, and a
+// block with padding is never full.
 __device__ __forceinline__ int band_block_class(const DevMask &m, int64_t A, int64_t W, int64_t r, int64_t c) {
   const int64_t r0 = r * m.bq, r1 = r0 + m.bq - 1, c0 = c * m.bk, c1 = c0 + m.bk - 1;
-  if (max(r0, c0 - A) > min(r1, c1 + W)) return 0;
-  return (r1 - W <= c0 && r0 + A >= c1) ? 2 : 1;
+  const int64_t r1v = min(r1, m.Lq - 1), c1v = min(c1, m.Lk - 1);
+  if (max(r0, c0 - A) > min(r1v, c1v + W)) return 0;
+  return (r1v == r1 && c1v == c1 && r1 - W <= c0 && r0 + A >= c1) ? 2 : 1;
 }
 
 // Allowed keys of query i under the band alone.
 __device__ __forceinline__ int64_t band_row_count(const DevMask &m, int64_t A, int64_t W, int64_t i) {
+  if (i >= m.Lq) return 0;
   return max((int64_t)0, min(m.Lk - 1, i + A) - max((int64_t)0, i - W) + 1);
 }
 
@@ -110,7 +118,8 @@ __global__ void seg_summary_kernel(DevMask m, int32_t *qsum, int32_t *kvsum) {
   if (warp >= m.nq + m.nk) return;
   const bool isq = warp < m.nq;
   const int64_t blk = isq ? warp : warp - m.nq;
-  const int32_t n = isq ? m.bq : m.bk;
+  // the last block of a ragged sequence holds fewer positions
+  const int32_t n = (int32_t)(isq ? min((int64_t)m.bq, m.Lq - blk * m.bq) : min((int64_t)m.bk, m.Lk - blk * m.bk));
   const int32_t *seg = isq ? m.qseg + (int64_t)bm * m.Lq + blk * m.bq
                            : m.kvseg + (int64_t)bm * m.Lk + blk * m.bk;
   int32_t mn = INT_MAX, mx = INT_MIN;
@@ -352,7 +361,7 @@ __global__ void partial_hash_kernel(DevMask m, const unsigned long long *counter
     const int64_t row = part_row[k];
     const int32_t bm = (int32_t)(row / m.nq);
     const int64_t r = row % m.nq, c = part_col[k];
-    if (m.qseg == nullptr) {
+    if (m.qseg == nullptr && !m.ragged) {
       // band only: the diagonal offset identifies the content exactly (see
       // build_small_kernel), and serves as the "hash"
       if (di == 0) part_hash[k] = (uint64_t)(c * m.bk - r * m.bq);
@@ -403,7 +412,7 @@ __global__ void dedup_kernel(DevMask m, const unsigned long long *counters, cons
     for (int64_t base = 0; base < k && rep == k; base += 32) {
       const int64_t kp = base + lane;
       unsigned cand = __ballot_sync(0xffffffffu, kp < k && part_hash[kp] == h);
-      if (cand && m.qseg == nullptr) {
+      if (cand && m.qseg == nullptr && !m.ragged) {
         rep = base + __ffs(cand) - 1;  // equal diagonal offsets: equal content
         break;
       }
@@ -834,7 +843,8 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
                                           cudaStream_t stream) {
   const bool seg = spec->q_segment_ids != nullptr;
   const int32_t nbm = seg ? spec->batch : 1;
-  const int64_t nq = Lq / bq, nk = Lk / bk, R = (int64_t)nbm * nq, NB = R * nk;
+  const int64_t nq = (Lq + bq - 1) / bq, nk = (Lk + bk - 1) / bk, R = (int64_t)nbm * nq, NB = R * nk;
+  const bool ragged = (Lq % bq) != 0 || (Lk % bk) != 0;
 
   // -- buffers (reused when large enough) --
   splash_status st;
@@ -892,6 +902,7 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
   m.bq = bq;
   m.bk = bk;
   m.nbm = nbm;
+  m.ragged = ragged ? 1 : 0;
 
   int dev = 0, sms = 148;
   SPLASH_CUDA_TRY(cudaGetDevice(&dev));
@@ -906,9 +917,10 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
   // 2 * (ceil((bq-1)/bk) + 1) partial blocks (a block is partial only if one of
   // the two band edges sweeps through it), so P has a bound known here and the
   // build runs without a host wait; the totals are read lazily.  With segment
-  // IDs the build waits once for P.
+  // IDs the build waits once for P.  A ragged grid adds at most the last
+  // column's block of every row and the whole last row.
   const int64_t per_row = 2 * ((bq - 1 + bk - 1) / bk + 1);
-  const int64_t p_bound = std::min<int64_t>(R * per_row, NB);
+  const int64_t p_bound = std::min<int64_t>(R * per_row + (ragged ? R + nk : 0), NB);
   const bool async = !seg && p_bound * (int64_t)bq * bk <= ((int64_t)256 << 20);
   auto reserve_patterns = [&](int64_t P_cap) -> splash_status {
     if (P_cap <= 0 || mi->cap_patterns >= P_cap) return SPLASH_OK;
@@ -934,9 +946,10 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
     return SPLASH_OK;
   };
 
-  if (async && R <= kSmallMaxRows && nk <= kSmallMaxCols && NB <= kSmallMaxBlocks &&
+  if (async && !ragged && R <= kSmallMaxRows && nk <= kSmallMaxCols && NB <= kSmallMaxBlocks &&
       p_bound <= kSmallMaxPartials) {
-    // small band-only table: the whole build is one single-CTA kernel
+    // small band-only table on whole blocks: the whole build is one
+    // single-CTA kernel (its diagonal-offset dedup needs whole blocks)
     if ((st = reserve_patterns(p_bound)) != SPLASH_OK) return st;
     SmallOut o;
     o.block_mask = mi->block_mask;
@@ -1128,7 +1141,7 @@ splash_status splash_classify_blocks_noalloc_impl(const splash_mask_spec *spec, 
                                                   int64_t *totals, cudaStream_t stream) {
   const bool seg = spec->q_segment_ids != nullptr;
   const int32_t nbm = seg ? spec->batch : 1;
-  const int64_t nq = Lq / bq, nk = Lk / bk, R = (int64_t)nbm * nq;
+  const int64_t nq = (Lq + bq - 1) / bq, nk = (Lk + bk - 1) / bk, R = (int64_t)nbm * nq;
   if (R > kNoAllocMaxRows || (int64_t)nbm * nk > kNoAllocMaxCols) return SPLASH_ERR_UNSUPPORTED;
   NoAllocScratch *s = nullptr;
   splash_status st = noalloc_scratch(&s);
@@ -1147,6 +1160,7 @@ splash_status splash_classify_blocks_noalloc_impl(const splash_mask_spec *spec, 
   m.bq = bq;
   m.bk = bk;
   m.nbm = nbm;
+  m.ragged = (Lq % bq) != 0 || (Lk % bk) != 0;
 
   // the counters must start at zero: the array keeps the previous call's values
   SPLASH_CUDA_TRY(cudaMemsetAsync(s->row_cnt, 0, sizeof(int32_t) * R, stream));

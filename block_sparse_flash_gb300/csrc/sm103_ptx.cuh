@@ -141,6 +141,14 @@ __device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int
                "r"(x), "r"(y), "r"(src)
                : "memory");
 }
+// 3-D tiled store of the box at (x, y, z); rows past the tensor's extent in
+// any dimension are not written.
+__device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int32_t x, int32_t y, int32_t z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y), "r"(z), "r"(src)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // this thread's bulk stores have finished reading their shared-memory source
 __device__ __forceinline__ void bulk_wait_read_all() {

@@ -96,7 +96,11 @@ typedef struct splash_mask_info splash_mask_info;
  *
  *   spec        host pointer to the mask; its segment arrays are device memory
  *               and are read on `cuda_stream` before this call returns.
- *   Lq, Lk      sequence lengths (> 0); Lq % bq == 0 and Lk % bk == 0.
+ *   Lq, Lk      sequence lengths (> 0).  When one is not a multiple of its
+ *               block, the grid is padded to nq = ceil(Lq/bq) by
+ *               nk = ceil(Lk/bk) whole blocks and the padding positions are
+ *               masked (§2.3: ragged edges are padded so that every block has
+ *               the same size); a block holding padding is never full.
  *   bq, bk      block sizes; this build supports bq, bk in {64, 128}.
  *   cuda_stream stream for the build kernels.
  *   out         receives a new handle (set to NULL on error).

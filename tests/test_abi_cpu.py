@@ -59,7 +59,7 @@ def test_invalid_arguments_are_rejected_before_any_launch(splash):
     # bad sizes and unsupported blocks
     assert lib.splash_build_mask_info(ctypes.byref(spec), 0, 256, 64, 64, null, ctypes.byref(out)) == 1
     assert lib.splash_build_mask_info(ctypes.byref(spec), 256, 256, 32, 32, null, ctypes.byref(out)) == 3
-    assert lib.splash_build_mask_info(ctypes.byref(spec), 250, 256, 64, 64, null, ctypes.byref(out)) == 3
+    assert lib.splash_build_mask_info(ctypes.byref(spec), 256, 256, 64, 96, null, ctypes.byref(out)) == 3
     bad = splash._Spec(2, -1, -1, None, None, 0)
     assert lib.splash_build_mask_info(ctypes.byref(bad), 256, 256, 64, 64, null, ctypes.byref(out)) == 1
     bad = splash._Spec(1, -5, -1, None, None, 0)
