@@ -47,6 +47,8 @@ def parse_args(argv=None):
                     help="split-KV forward with this many splits per row, then the LSE merge")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (MaskInfo rebuild + gradients) instead of the forward")
+    ap.add_argument("--pattern-source", choices=["stored", "positions"], default="stored",
+                    help="partial-block masks from the stored patterns or computed from positions")
     ap.add_argument("--max-logit", type=float, default=None,
                     help="Max Logit Estimate: fix every row's softmax reference at this constant "
                          "(e.g. the workload's soft cap)")
@@ -241,6 +243,8 @@ def run_ours(args):
     seg = inp.segment_ids.to(dev) if inp.segment_ids is not None else None
     spec = bsf.MaskSpec(w.causal, w.window_left, w.window_right, seg, seg)
     mi = bsf.build_mask_info(spec, w.q_len, w.L, w.bq, w.bk)
+    if args.pattern_source != "stored":
+        mi.set_pattern_source(args.pattern_source)
     counts = mi.counts()
     batch_rows = mi.shape()["batch_rows"]
     useful, executed = flop_counts(w, counts, batch_rows)
@@ -349,6 +353,8 @@ def run_ours(args):
             "note": "attention_ms = split kernel + merge; roofline.achieved uses the split kernel alone"}
     if args.max_logit is not None:
         result["config"]["max_logit"] = args.max_logit
+    if args.pattern_source != "stored":
+        result["config"]["pattern_source"] = args.pattern_source
     if e2e:
         result["e2e"] = e2e
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -83,6 +83,7 @@ def lib():
     L.splash_attention_bwd_workspace_size.argtypes = [i32, i32, i64, i32, P(ctypes.c_size_t)]
     L.splash_attention_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i64, i64, i32, i32, vp, vp, vp,
                                        f32, f32, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    L.splash_mask_info_set_pattern_source.argtypes = [vp, i32]
     L.splash_attention_merge.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp]
     L.splash_last_device_error.argtypes = [vp]
     L.splash_debug_wait_selftest.argtypes = [ctypes.c_uint64, vp]
@@ -185,6 +186,12 @@ class MaskInfo:
         _check(lib().splash_mask_info_shape(self.handle, ctypes.byref(bm), ctypes.byref(nq), ctypes.byref(nk),
                                             ctypes.byref(bq), ctypes.byref(bk)), "splash_mask_info_shape")
         return dict(batch_rows=bm.value, nq=nq.value, nk=nk.value, bq=bq.value, bk=bk.value)
+
+    def set_pattern_source(self, source: str):
+        """'stored' (default) or 'positions': the forward computes partial
+        blocks' masks from positions (tables without segment IDs)."""
+        code = {"stored": 0, "positions": 1}[source]
+        _check(lib().splash_mask_info_set_pattern_source(self.handle, code), "splash_mask_info_set_pattern_source")
 
     def counts(self):
         a, p, n, u = (ctypes.c_int64() for _ in range(4))

@@ -144,6 +144,14 @@ splash_status splash_mask_info_counts(const splash_mask_info *mi, int64_t *num_a
   return SPLASH_OK;
 }
 
+splash_status splash_mask_info_set_pattern_source(splash_mask_info *mi, int32_t source) {
+  if (mi == nullptr || (source != SPLASH_PATTERNS_STORED && source != SPLASH_PATTERNS_FROM_POSITIONS))
+    return SPLASH_ERR_INVALID_ARG;
+  if (source == SPLASH_PATTERNS_FROM_POSITIONS && mi->has_segments) return SPLASH_ERR_UNSUPPORTED;
+  mi->patterns_from_positions = source == SPLASH_PATTERNS_FROM_POSITIONS ? 1 : 0;
+  return SPLASH_OK;
+}
+
 splash_status splash_mask_info_to_host(const splash_mask_info *mi, int8_t *block_mask, int32_t *row_ptr,
                                        int32_t *active_rows, int32_t *active_cols, int32_t *mask_next,
                                        uint8_t *bounds_start, uint8_t *bounds_end,

@@ -108,6 +108,10 @@ struct FwdParams {
   const int32_t *mask_next;
   const uint32_t *pattern_bits;
   const int32_t *row_order;
+  // partial blocks' element masks computed from positions instead of read
+  // from pattern_bits (masks without segment IDs): causal / window bounds
+  int32_t band_bits, band_causal;
+  int64_t band_wl, band_wr;
   int64_t num_patterns;
   float scale_log2;   // scale * log2(e)             (no soft cap)
   float cap_inner;    // scale / cap                 (soft cap)
@@ -645,6 +649,35 @@ __device__ __forceinline__ f32x2 tanh_series2(f32x2 s, f32x2 k) {
   return ffma2(fmul2(a, u), p1, a);
 }
 
+// Element mask of a partial block for query position qpos (row `row` of the
+// tile; active block g_idx, pattern mn): read from the stored bit-packed
+// pattern, or computed from positions when the table allows it (the band part
+// of the mask: causal and window bounds, and the padding of ragged lengths --
+// "Pallas Kernels and Splash Attention" §6.6: masks can be computed in the
+// kernel from q / kv positions instead of stored patterns).
+template <int BK>
+__device__ __forceinline__ void partial_bits(const FwdParams &p, int32_t mn, int row, int64_t qpos, int32_t g_idx,
+                                             uint32_t (&bits)[BK / 32]) {
+  if (p.band_bits) {
+    const int64_t c0 = (int64_t)__ldg(p.active_cols + g_idx) * BK;
+    int64_t lo = c0, hi = min(c0 + BK - 1, p.Lk - 1);
+    if (p.band_causal) hi = min(hi, qpos);
+    if (p.band_wl >= 0) lo = max(lo, qpos - p.band_wl);
+    if (p.band_wr >= 0) hi = min(hi, qpos + p.band_wr);
+    if (qpos >= p.Lq) hi = lo - 1;
+#pragma unroll
+    for (int x = 0; x < BK / 32; ++x) {
+      const int64_t w0 = c0 + 32 * x, a = max(lo, w0), b = min(hi, w0 + 31);
+      const int32_t n = (int32_t)(b - a + 1);
+      bits[x] = n <= 0 ? 0u : ((n >= 32 ? 0xffffffffu : ((1u << n) - 1u)) << (int32_t)(a - w0));
+    }
+  } else {
+    const uint32_t *src = p.pattern_bits + ((int64_t)mn * p.bq + row) * (BK / 32);
+#pragma unroll
+    for (int x = 0; x < BK / 32; ++x) bits[x] = __ldg(src + x);
+  }
+}
+
 // s_j <- 2^(s_j * mul - sub) in place (packed argument), returns the row sum
 // (eight independent partial sums).
 template <int N>
@@ -765,9 +798,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         const bool need_mask = partial || !row_valid;
         uint32_t bits[BK / 32];
         if (partial && row_valid) {
-          const uint32_t *src = p.pattern_bits + ((int64_t)mn * p.bq + row) * (BK / 32);
-#pragma unroll
-          for (int x = 0; x < BK / 32; ++x) bits[x] = __ldg(src + x);
+          partial_bits<BK>(p, mn, row, (int64_t)it.qrow * p.bq + row, it.g0 + g, bits);
         } else {
 #pragma unroll
           for (int x = 0; x < BK / 32; ++x) bits[x] = row_valid ? 0xffffffffu : 0u;
@@ -860,12 +891,17 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             for (int j = 0; j < BK; ++j) s[j] = tanh_identity(s[j] * p.cap_inner);
           }
           if (need_mask) {
-            const uint32_t *src = p.pattern_bits + ((int64_t)mn * p.bq + row) * (BK / 32);
+            uint32_t rb[BK / 32];
+            if (partial && row_valid) {
+              partial_bits<BK>(p, mn, row, (int64_t)it.qrow * p.bq + row, it.g0 + g, rb);
+            } else {
+#pragma unroll
+              for (int x = 0; x < BK / 32; ++x) rb[x] = row_valid ? 0xffffffffu : 0u;
+            }
 #pragma unroll
             for (int x = 0; x < BK / 32; ++x) {
-              const uint32_t b = (partial && row_valid) ? __ldg(src + x) : (row_valid ? 0xffffffffu : 0u);
 #pragma unroll
-              for (int j = 0; j < 32; ++j) s[x * 32 + j] = ((b >> j) & 1u) ? s[x * 32 + j] : -INFINITY;
+              for (int j = 0; j < 32; ++j) s[x * 32 + j] = ((rb[x] >> j) & 1u) ? s[x * 32 + j] : -INFINITY;
             }
           }
           if (redo) {
@@ -1145,6 +1181,10 @@ splash_status splash_attention_fwd_launch(const void *q, const void *k, const vo
   prm.active_cols = mi->active_cols;
   prm.mask_next = mi->mask_next;
   prm.pattern_bits = mi->pattern_bits;
+  prm.band_bits = (mi->patterns_from_positions && !mi->has_segments) ? 1 : 0;
+  prm.band_causal = mi->causal;
+  prm.band_wl = mi->window_left;
+  prm.band_wr = mi->window_right;
   prm.row_order = mi->row_order;
   // bound for the kernel's check of mask_next (the true count may still be in
   // flight after an asynchronous build; it never exceeds the buffer capacity)

@@ -29,6 +29,9 @@ struct splash_mask_info {
   int32_t causal = 0;
   int64_t window_left = -1, window_right = -1;
   int32_t has_segments = 0;
+  // the forward computes partial blocks' masks from positions instead of
+  // reading the stored patterns (masks without segment IDs only)
+  int32_t patterns_from_positions = 0;
   // totals (host copies)
   int64_t num_active = 0, num_partial = 0, num_patterns = 0, allowed_pairs = 0;
   int32_t max_row_blocks = 0;

@@ -157,6 +157,23 @@ splash_status splash_mask_info_to_host(const splash_mask_info *mi, int8_t *block
                                        uint8_t *bounds_start, uint8_t *bounds_end,
                                        uint8_t *partial_mask_blocks);
 
+/*
+ * splash_mask_info_set_pattern_source -- where the attention forward takes the
+ * element masks of partial blocks from:
+ *   SPLASH_PATTERNS_STORED (default): the deduplicated partial_mask_blocks;
+ *   SPLASH_PATTERNS_FROM_POSITIONS: computed in the kernel from the query and
+ *     key positions (causal / window bounds and ragged-length padding), the
+ *     alternative of "Pallas Kernels and Splash Attention" §6.6 (no pattern
+ *     reads; the results are identical).  Only for tables built without
+ *     segment IDs (else SPLASH_ERR_UNSUPPORTED).
+ * The setting stays with the handle across rebuilds (a rebuild with segment
+ * IDs makes the forward use the stored patterns).  The backward always reads
+ * the stored patterns.  Errors: INVALID_ARG (NULL handle, unknown source).
+ */
+#define SPLASH_PATTERNS_STORED 0
+#define SPLASH_PATTERNS_FROM_POSITIONS 1
+splash_status splash_mask_info_set_pattern_source(splash_mask_info *mi, int32_t source);
+
 /* Frees the handle and its device memory (NULL is a no-op).  Work queued on
  * other streams that still reads the table must be complete first. */
 void splash_mask_info_destroy(splash_mask_info *mi);

@@ -89,6 +89,7 @@ def test_invalid_arguments_are_rejected_before_any_launch(splash):
     assert lib.splash_attention_bwd_workspace_size(2, 4, 1024, 128, ctypes.byref(n)) == 0
     assert n.value == 2 * 4 * 1024 * 128 * 4 + 2 * 4 * 1024 * 4   # fp32 dq accumulator + D
     assert lib.splash_attention_bwd_workspace_size(2, 4, 1024, 128, None) == 1
+    assert lib.splash_mask_info_set_pattern_source(None, 0) == 1
     # counts / shape / to_host on a NULL handle
     assert lib.splash_mask_info_counts(None, None, None, None, None) == 1
     assert lib.splash_mask_info_shape(None, None, None, None, None, None) == 1
