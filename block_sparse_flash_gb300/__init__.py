@@ -84,6 +84,8 @@ def lib():
     L.splash_attention_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i64, i64, i32, i32, vp, vp, vp,
                                        f32, f32, vp, vp, vp, vp, ctypes.c_size_t, vp]
     L.splash_mask_info_set_pattern_source.argtypes = [vp, i32]
+    L.splash_attention_fwd_host.argtypes = [vp, vp, vp, i32, i32, i32, i64, i64, i32, i32, vp, vp, vp, f32, f32,
+                                            vp, vp, vp, vp, vp, vp, vp, vp]
     L.splash_attention_merge.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp]
     L.splash_last_device_error.argtypes = [vp]
     L.splash_debug_wait_selftest.argtypes = [ctypes.c_uint64, vp]
@@ -273,6 +275,36 @@ def attention_fwd(q, k, v, mask_info: MaskInfo, scale: float, softcap: float = 0
                                       float(scale), float(softcap), _ptr(out), _ptr(lse), _stream(stream)),
            "splash_attention_fwd")
     return out, lse
+
+
+def attention_fwd_host(q_host, k_host, v_host, mask_info: MaskInfo, scale: float, softcap: float = 0.0,
+                       out_host=None, lse_host=None, q=None, k=None, v=None, out=None, lse=None,
+                       q_segment_ids=None, kv_segment_ids=None, stream=None):
+    """attention_fwd for CPU tensors (pinned for overlap): copies in, computes
+    and copies out, pipelined in chunks.  Device buffers q, k, v, out, lse are
+    allocated on the current device when not given.  Returns (out_host,
+    lse_host); they are complete once the stream has reached this point."""
+    for t in (q_host, k_host, v_host):
+        if t.dtype != torch.bfloat16 or t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError("q_host, k_host, v_host must be contiguous 4-D bf16 CPU tensors")
+    B, Hq, Lq, dqk = q_host.shape
+    Hkv, Lk, dv = k_host.shape[1], k_host.shape[2], v_host.shape[3]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if out_host is None:
+        out_host = torch.empty((B, Hq, Lq, dv), dtype=torch.bfloat16).pin_memory()
+    if lse_host is None:
+        lse_host = torch.empty((B, Hq, Lq), dtype=torch.float32).pin_memory()
+    q = torch.empty_like(q_host, device=dev) if q is None else q
+    k = torch.empty_like(k_host, device=dev) if k is None else k
+    v = torch.empty_like(v_host, device=dev) if v is None else v
+    out = torch.empty((B, Hq, Lq, dv), dtype=torch.bfloat16, device=dev) if out is None else out
+    lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=dev) if lse is None else lse
+    _check(lib().splash_attention_fwd_host(_ptr(q_host), _ptr(k_host), _ptr(v_host), B, Hq, Hkv, Lq, Lk, dqk, dv,
+                                           _ptr(q_segment_ids), _ptr(kv_segment_ids), mask_info.handle,
+                                           float(scale), float(softcap), _ptr(out_host), _ptr(lse_host), _ptr(q),
+                                           _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _stream(stream)),
+           "splash_attention_fwd_host")
+    return out_host, lse_host
 
 
 def attention_fwd_split(q, k, v, mask_info: MaskInfo, scale: float, softcap: float, num_splits: int,

@@ -246,6 +246,25 @@ splash_status splash_attention_fwd_mle(const void *q, const void *k, const void 
                                      lse, 1, nullptr, nullptr, static_cast<cudaStream_t>(cuda_stream), err);
 }
 
+splash_status splash_attention_fwd_host(const void *q_host, const void *k_host, const void *v_host, int32_t B,
+                                        int32_t Hq, int32_t Hkv, int64_t Lq, int64_t Lk, int32_t dqk, int32_t dv,
+                                        const int32_t *q_segment_ids, const int32_t *kv_segment_ids,
+                                        const splash_mask_info *mi, float scale, float softcap, void *out_host,
+                                        float *lse_host, void *q_dev, void *k_dev, void *v_dev, void *out_dev,
+                                        float *lse_dev, void *cuda_stream) {
+  (void)q_segment_ids;
+  (void)kv_segment_ids;
+  if (q_host == nullptr || k_host == nullptr || v_host == nullptr || out_host == nullptr || lse_host == nullptr)
+    return SPLASH_ERR_INVALID_ARG;
+  uint32_t *err = nullptr;
+  splash_status st =
+      check_attention(q_dev, k_dev, v_dev, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, out_dev, lse_dev, &err);
+  if (st != SPLASH_OK) return st;
+  return splash_attention_fwd_host_launch(q_host, k_host, v_host, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap,
+                                          out_host, lse_host, q_dev, k_dev, v_dev, out_dev, lse_dev, 8,
+                                          static_cast<cudaStream_t>(cuda_stream), err);
+}
+
 splash_status splash_attention_bwd_workspace_size(int32_t B, int32_t Hq, int64_t Lq, int32_t dqk, size_t *bytes) {
   if (bytes == nullptr || B <= 0 || Hq <= 0 || Lq <= 0 || dqk <= 0) return SPLASH_ERR_INVALID_ARG;
   *bytes = splash_attention_bwd_workspace_bytes(B, Hq, Lq, dqk);

@@ -115,6 +115,13 @@ splash_status splash_attention_bwd_launch(const void *q, const void *k, const vo
                                           int64_t Lq, int64_t Lk, int32_t d, splash_mask_info *mi, float scale,
                                           float softcap, void *dq, void *dk, void *dv, void *workspace,
                                           cudaStream_t stream, uint32_t *err_word);
+// host_pipeline.cu
+splash_status splash_attention_fwd_host_launch(const void *q_h, const void *k_h, const void *v_h, int32_t B,
+                                               int32_t Hq, int32_t Hkv, int64_t Lq, int64_t Lk, int32_t dqk,
+                                               int32_t dv, const splash_mask_info *mi, float scale, float softcap,
+                                               void *out_h, float *lse_h, void *q_d, void *k_d, void *v_d,
+                                               void *out_d, float *lse_d, int32_t target_chunks,
+                                               cudaStream_t stream, uint32_t *err);
 splash_status splash_wait_selftest_launch(uint64_t timeout_ns, cudaStream_t stream,
                                           uint32_t *err_word);
 

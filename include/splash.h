@@ -243,6 +243,33 @@ splash_status splash_attention_fwd_mle(const void *q, const void *k, const void 
                                        float scale, float softcap, float max_logit, void *out,
                                        float *lse, void *cuda_stream);
 
+/*
+ * splash_attention_fwd_host -- splash_attention_fwd for tensors in host
+ * memory: copies q, k, v to the caller's device buffers, runs the forward and
+ * copies out and lse back, overlapping the three.  The work is cut into
+ * contiguous chunks (whole GQA groups of one batch row when the MaskInfo is
+ * shared by the batch; the whole batch at once for a per-batch table) and
+ * pipelined on library-owned streams: host -> device copies of one chunk,
+ * the attention of the previous one and device -> host copies of the one
+ * before run at the same time.  Ordered after prior work on cuda_stream;
+ * work queued on cuda_stream afterwards waits for the last copy back.
+ *
+ *   q_host, k_host, v_host   host bf16, layouts as splash_attention_fwd
+ *   out_host, lse_host       host bf16 [B][Hq][Lq][dv] and fp32 [B][Hq][Lq]
+ *   q_dev .. lse_dev         device buffers of the full sizes (caller-owned,
+ *                            overwritten; alignment as splash_attention_fwd)
+ * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister):
+ * copies from pageable memory are correct but do not overlap.  Other
+ * arguments, supported shapes and errors as for splash_attention_fwd.
+ */
+splash_status splash_attention_fwd_host(const void *q_host, const void *k_host, const void *v_host,
+                                        int32_t B, int32_t Hq, int32_t Hkv, int64_t Lq, int64_t Lk,
+                                        int32_t dqk, int32_t dv, const int32_t *q_segment_ids,
+                                        const int32_t *kv_segment_ids, const splash_mask_info *mi,
+                                        float scale, float softcap, void *out_host, float *lse_host,
+                                        void *q_dev, void *k_dev, void *v_dev, void *out_dev,
+                                        float *lse_dev, void *cuda_stream);
+
 /* Largest num_splits accepted by the split-KV entry points. */
 #define SPLASH_MAX_SPLITS 256
 
