@@ -100,6 +100,7 @@ struct BwdCfg {
 struct BwdParams {
   int32_t B, Hq, Hkv, G;
   int64_t Lq, Lk;
+  int64_t Lq_pad;               // nq * 128: row stride of the padded workspace arrays
   int32_t nq, nk, nbm;
   int64_t num_items;            // B * Hkv * nk
   const int32_t *col_ptr;       // [nbm*nk + 1]
@@ -108,9 +109,9 @@ struct BwdParams {
   const uint32_t *pattern_t;    // [P][128 keys][4 words]: bit i%32 of word i/32 = (query i, key) allowed
   const unsigned long long *counters;  // device totals of the MaskInfo build ([2] = patterns)
   int64_t cap_patterns;
-  const float *lse;             // [B*Hq*Lq]
-  const float *delta;           // [B*Hq*Lq]
-  float *dq_acc;                // [B*Hq*Lq][D] fp32
+  const float *lse;             // [B*Hq*Lq_pad] (copied from the forward's, padding rows 0)
+  const float *delta;           // [B*Hq*Lq_pad]
+  float *dq_acc;                // [B*Hq*Lq_pad][D] fp32
   __nv_bfloat16 *dk, *dv;       // [B*Hkv*Lk][D]
   float scale, scale_log2, cap_inner, cap_log2;
   uint32_t *err;
@@ -245,12 +246,16 @@ __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const C
       bwd_step(p, it, t, h, i, mn);
       const int st = n & 1;
       if (n >= 2 && !(ok = mbar_wait(bar.q_empty(st), ((n >> 1) - 1) & 1u, abort, p.timeout_ns))) break;
+      // tiles from the caller's tensors (rows past a ragged Lq read the next
+      // head's rows or the zero fill, all masked); LSE and D from the padded
+      // workspace (whole blocks, always in bounds)
       const int64_t row = ((int64_t)it.b * p.Hq + h) * p.Lq + (int64_t)i * 128;
+      const int64_t prow = ((int64_t)it.b * p.Hq + h) * p.Lq_pad + (int64_t)i * 128;
       mbar_arrive_expect_tx(bar.q_full(st), C::TILE + 1024);
       for (int ch = 0; ch < C::CH; ++ch)
         tma_load_2d(s0 + C::OFF_Q + st * C::TILE + ch * C::CHUNK, tmQ, ch * 64, (int32_t)row, bar.q_full(st));
-      bulk_load(s0 + C::OFF_LD + st * 1024, p.lse + row, 512, bar.q_full(st));
-      bulk_load(s0 + C::OFF_LD + st * 1024 + 512, p.delta + row, 512, bar.q_full(st));
+      bulk_load(s0 + C::OFF_LD + st * 1024, p.lse + prow, 512, bar.q_full(st));
+      bulk_load(s0 + C::OFF_LD + st * 1024 + 512, p.delta + prow, 512, bar.q_full(st));
       if (n >= 1 && !(ok = mbar_wait(bar.do_empty(), (n - 1) & 1u, abort, p.timeout_ns))) break;
       mbar_arrive_expect_tx(bar.do_full(), C::TILE);
       for (int ch = 0; ch < C::CH; ++ch)
@@ -452,7 +457,9 @@ __device__ void bwd_work(const BwdParams &p, const CUtensorMap *tmDQ, uint32_t t
     const int64_t krow = ((int64_t)it.b * p.Hkv + it.kvh) * p.Lk + (int64_t)it.j * 128 + jj;
     __nv_bfloat16 *dk_row = p.dk + krow * D + wg * (D / 2);
     __nv_bfloat16 *dv_row = p.dv + krow * D + wg * (D / 2);
+    const bool key_out = (int64_t)it.j * 128 + jj < p.Lk;  // padding keys of a ragged Lk are never stored
     if (N == 0) {  // no query sees this key block: zero gradients
+      if (!key_out) continue;
       for (int x = 0; x < D / 2; x += 8) {
         *reinterpret_cast<uint4 *>(dk_row + x) = make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4 *>(dv_row + x) = make_uint4(0, 0, 0, 0);
@@ -552,7 +559,7 @@ __device__ void bwd_work(const BwdParams &p, const CUtensorMap *tmDQ, uint32_t t
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.ds_ready());
-      prev_row = (int32_t)(((int64_t)it.b * p.Hq + h) * p.Lq + (int64_t)i * 128 + wq * 32);
+      prev_row = (int32_t)(((int64_t)it.b * p.Hq + h) * p.Lq_pad + (int64_t)i * 128 + wq * 32);
     }
     if (!ok) break;
     // ---- the item's last dQ, then dK, dV (complete once that dQ has landed)
@@ -578,8 +585,10 @@ __device__ void bwd_work(const BwdParams &p, const CUtensorMap *tmDQ, uint32_t t
         b.y = pack_bf16x2(__uint_as_float(rv[x + 2]), __uint_as_float(rv[x + 3]));
         b.z = pack_bf16x2(__uint_as_float(rv[x + 4]), __uint_as_float(rv[x + 5]));
         b.w = pack_bf16x2(__uint_as_float(rv[x + 6]), __uint_as_float(rv[x + 7]));
-        *reinterpret_cast<uint4 *>(dk_row + 32 * c + x) = a;
-        *reinterpret_cast<uint4 *>(dv_row + 32 * c + x) = b;
+        if (key_out) {
+          *reinterpret_cast<uint4 *>(dk_row + 32 * c + x) = a;
+          *reinterpret_cast<uint4 *>(dv_row + 32 * c + x) = b;
+        }
       }
     }
     tc_fence_before();
@@ -660,24 +669,30 @@ splash_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
 }
 
 // ------------------------------------------------------------ small kernels
-// D_r = sum_x dout[r][x] * out[r][x] (fp32), one 16-lane half-warp per row
-// (a warp takes two consecutive rows, so its shuffles always see all 32
-// lanes); the dq accumulator rows are cleared at the same time.
+// Padded workspace rows r = bh * Lq_pad + i (whole 128-row blocks per head):
+// D_r = sum_x dout[bh*Lq + i][x] * out[...][x] (fp32) and a copy of the
+// forward's LSE for i < Lq, 0 on padding rows; the dq accumulator rows are
+// cleared.  One 16-lane half-warp per row (a warp takes two consecutive rows,
+// so its shuffles always see all 32 lanes).
 template <int D>
-__global__ void bwd_prep_kernel(const __nv_bfloat16 *out, const __nv_bfloat16 *dout, float *delta, float *dq_acc,
-                                int64_t rows) {
+__global__ void bwd_prep_kernel(const __nv_bfloat16 *out, const __nv_bfloat16 *dout, const float *lse_in,
+                                float *delta, float *lse_pad, float *dq_acc, int64_t rows_pad, int64_t Lq,
+                                int64_t Lq_pad) {
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int half = (threadIdx.x >> 4) & 1, sub = threadIdx.x & 15;
-  for (int64_t base = 2 * warp; base < rows; base += 2 * nwarps) {
+  for (int64_t base = 2 * warp; base < rows_pad; base += 2 * nwarps) {
     const int64_t r = base + half;
-    const bool valid = r < rows;
+    const bool valid = r < rows_pad;
+    const int64_t bh = r / Lq_pad, i = r - bh * Lq_pad;
+    const bool real = valid && i < Lq;
+    const int64_t src = bh * Lq + i;
     float acc = 0.f;
-    if (valid) {
+    if (real) {
 #pragma unroll
       for (int x = sub * 8; x < D; x += 128) {
-        const uint4 a = *reinterpret_cast<const uint4 *>(out + r * D + x);
-        const uint4 b = *reinterpret_cast<const uint4 *>(dout + r * D + x);
+        const uint4 a = *reinterpret_cast<const uint4 *>(out + src * D + x);
+        const uint4 b = *reinterpret_cast<const uint4 *>(dout + src * D + x);
         const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
         const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
 #pragma unroll
@@ -691,7 +706,10 @@ __global__ void bwd_prep_kernel(const __nv_bfloat16 *out, const __nv_bfloat16 *d
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (valid) {
-      if (sub == 0) delta[r] = acc;
+      if (sub == 0) {
+        delta[r] = acc;
+        lse_pad[r] = real ? lse_in[src] : 0.f;
+      }
 #pragma unroll
       for (int x = sub * 4; x < D; x += 64)
         *reinterpret_cast<float4 *>(dq_acc + r * D + x) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -699,10 +717,14 @@ __global__ void bwd_prep_kernel(const __nv_bfloat16 *out, const __nv_bfloat16 *d
   }
 }
 
-// dq = bf16(dq_acc * scale)
-__global__ void bwd_dq_convert_kernel(const float *dq_acc, __nv_bfloat16 *dq, int64_t n4, float scale) {
+// dq[bh][i] = bf16(dq_acc[bh * Lq_pad + i] * scale) for the real rows i < Lq
+// (x counts groups of 4 columns of dq).
+__global__ void bwd_dq_convert_kernel(const float *dq_acc, __nv_bfloat16 *dq, int64_t n4, int32_t d4, int64_t Lq,
+                                      int64_t Lq_pad, float scale) {
   for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n4; x += (int64_t)gridDim.x * blockDim.x) {
-    const float4 v = reinterpret_cast<const float4 *>(dq_acc)[x];
+    const int64_t row = x / d4, c = x - row * d4;
+    const int64_t bh = row / Lq, i = row - bh * Lq;
+    const float4 v = reinterpret_cast<const float4 *>(dq_acc)[(bh * Lq_pad + i) * d4 + c];
     uint2 o;
     o.x = pack_bf16x2(v.x * scale, v.y * scale);
     o.y = pack_bf16x2(v.z * scale, v.w * scale);
@@ -848,7 +870,7 @@ splash_status launch_bwd(const void *q, const void *k, const void *v, const void
       !make_bwd_map(&tk, k, D, (uint64_t)prm.B * prm.Hkv * prm.Lk) ||
       !make_bwd_map(&tv, v, D, (uint64_t)prm.B * prm.Hkv * prm.Lk) ||
       !make_bwd_map(&tdo, dout, D, (uint64_t)prm.B * prm.Hq * prm.Lq) ||
-      !make_bwd_map_f32(&tdq, prm.dq_acc, D, (uint64_t)prm.B * prm.Hq * prm.Lq))
+      !make_bwd_map_f32(&tdq, prm.dq_acc, D, (uint64_t)prm.B * prm.Hq * prm.Lq_pad))
     return SPLASH_ERR_CUDA;
   static int configured_device = -1;
   int dev = 0;
@@ -871,9 +893,11 @@ splash_status launch_bwd(const void *q, const void *k, const void *v, const void
 
 using namespace splash;
 
+// fp32 dq accumulator, D and a copy of LSE, each over whole 128-row blocks
+// per head (rows past a ragged Lq are padding)
 size_t splash_attention_bwd_workspace_bytes(int32_t B, int32_t Hq, int64_t Lq, int32_t dqk) {
-  const size_t rows = (size_t)B * Hq * Lq;
-  return ((rows * dqk * 4 + 255) & ~(size_t)255) + ((rows * 4 + 255) & ~(size_t)255);
+  const size_t rows = (size_t)B * Hq * (size_t)((Lq + 127) / 128 * 128);
+  return ((rows * dqk * 4 + 255) & ~(size_t)255) + 2 * ((rows * 4 + 255) & ~(size_t)255);
 }
 
 splash_status splash_attention_bwd_launch(const void *q, const void *k, const void *v, const void *out,
@@ -918,16 +942,20 @@ splash_status splash_attention_bwd_launch(const void *q, const void *k, const vo
   splash_count_launches(4);
 
   const int64_t rows = (int64_t)B * Hq * Lq;
+  const int64_t Lq_pad = (Lq + 127) / 128 * 128, rows_pad = (int64_t)B * Hq * Lq_pad;
   float *dq_acc = static_cast<float *>(workspace);
   float *delta = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                           ((rows * d * 4 + 255) & ~(int64_t)255));
-  const unsigned pgrid = (unsigned)std::max<int64_t>(1, std::min<int64_t>((rows * 16 + 255) / 256, sms * 16));
+                                           ((rows_pad * d * 4 + 255) & ~(int64_t)255));
+  float *lse_pad = reinterpret_cast<float *>(reinterpret_cast<char *>(delta) + ((rows_pad * 4 + 255) & ~(int64_t)255));
+  const unsigned pgrid = (unsigned)std::max<int64_t>(1, std::min<int64_t>((rows_pad * 16 + 255) / 256, sms * 16));
   if (d == 128)
     bwd_prep_kernel<128><<<pgrid, 256, 0, stream>>>(static_cast<const __nv_bfloat16 *>(out),
-                                                     static_cast<const __nv_bfloat16 *>(dout), delta, dq_acc, rows);
+                                                     static_cast<const __nv_bfloat16 *>(dout), lse, delta, lse_pad,
+                                                     dq_acc, rows_pad, Lq, Lq_pad);
   else
     bwd_prep_kernel<64><<<pgrid, 256, 0, stream>>>(static_cast<const __nv_bfloat16 *>(out),
-                                                    static_cast<const __nv_bfloat16 *>(dout), delta, dq_acc, rows);
+                                                    static_cast<const __nv_bfloat16 *>(dout), lse, delta, lse_pad,
+                                                    dq_acc, rows_pad, Lq, Lq_pad);
   SPLASH_CUDA_TRY(cudaGetLastError());
   splash_count_launches(1);
 
@@ -937,6 +965,7 @@ splash_status splash_attention_bwd_launch(const void *q, const void *k, const vo
   prm.Hkv = Hkv;
   prm.G = Hq / Hkv;
   prm.Lq = Lq;
+  prm.Lq_pad = Lq_pad;
   prm.Lk = Lk;
   prm.nq = (int32_t)mi->nq;
   prm.nk = (int32_t)mi->nk;
@@ -948,7 +977,7 @@ splash_status splash_attention_bwd_launch(const void *q, const void *k, const vo
   prm.pattern_t = mi->t_pattern_bits;
   prm.counters = mi->counters;
   prm.cap_patterns = mi->cap_patterns;
-  prm.lse = lse;
+  prm.lse = lse_pad;
   prm.delta = delta;
   prm.dq_acc = dq_acc;
   prm.dk = static_cast<__nv_bfloat16 *>(dk);
@@ -970,7 +999,8 @@ splash_status splash_attention_bwd_launch(const void *q, const void *k, const vo
 
   const int64_t n4 = rows * d / 4;
   const unsigned vgrid = (unsigned)std::max<int64_t>(1, std::min<int64_t>((n4 + 255) / 256, sms * 16));
-  bwd_dq_convert_kernel<<<vgrid, 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16 *>(dq), n4, scale);
+  bwd_dq_convert_kernel<<<vgrid, 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16 *>(dq), n4, d / 4, Lq, Lq_pad,
+                                                   scale);
   SPLASH_CUDA_TRY(cudaGetLastError());
   splash_count_launches(1);
   return SPLASH_OK;

@@ -340,8 +340,9 @@ splash_status splash_attention_merge(const float *o_part, const float *lse_part,
  *              splash_attention_bwd_workspace_size(B, Hq, Lq, dqk) bytes
  *              (an fp32 dq accumulator and D); caller-owned, overwritten.
  * All device pointers 16-byte aligned.  Supported: dqk == dv in {64, 128}
- * and MaskInfo blocks bq = bk = 128 (other valid shapes return
- * SPLASH_ERR_UNSUPPORTED).  dq is accumulated with fp32 atomic additions, so
+ * and MaskInfo blocks bq = bk = 128, any Lq / Lk (ragged lengths as in the
+ * forward; the workspace covers whole 128-row blocks per head); other valid
+ * shapes return SPLASH_ERR_UNSUPPORTED.  dq is accumulated with fp32 atomic additions, so
  * its last bits may differ between runs; dk and dv are deterministic.
  * Errors as for splash_attention_fwd.
  */

@@ -87,7 +87,10 @@ def test_invalid_arguments_are_rejected_before_any_launch(splash):
               fake, fake, fake, fake, 1 << 20, null) == 1
     n = ctypes.c_size_t(0)
     assert lib.splash_attention_bwd_workspace_size(2, 4, 1024, 128, ctypes.byref(n)) == 0
-    assert n.value == 2 * 4 * 1024 * 128 * 4 + 2 * 4 * 1024 * 4   # fp32 dq accumulator + D
+    assert n.value == 2 * 4 * 1024 * 128 * 4 + 2 * (2 * 4 * 1024 * 4)   # fp32 dq accumulator, D, LSE copy
+    # a ragged Lq is padded to whole 128-row blocks per head
+    assert lib.splash_attention_bwd_workspace_size(1, 2, 1000, 64, ctypes.byref(n)) == 0
+    assert n.value == 2 * 1024 * 64 * 4 + 2 * (2 * 1024 * 4)
     assert lib.splash_attention_bwd_workspace_size(2, 4, 1024, 128, None) == 1
     assert lib.splash_mask_info_set_pattern_source(None, 0) == 1
     # counts / shape / to_host on a NULL handle

@@ -3,8 +3,8 @@
 The grid is padded to whole blocks and the padding is masked ("Pallas
 Kernels and Splash Attention" §2.3).  The GPU MaskInfo must equal the
 oracle's padded-grid table bit for bit; the forward (one pass, split-KV and
-the Max Logit Estimate) must match the f64 oracle on every real row and
-must not write past the output tensors."""
+the Max Logit Estimate) and the backward must match the f64 oracle on every
+real row and must not write past their output tensors."""
 import math
 
 import numpy as np
@@ -116,10 +116,33 @@ def test_ragged_forward_matches_the_oracle(bsf, case):
     mi.close()
 
 
-def test_ragged_backward_is_rejected(bsf):
-    q, k, v, mi, _ = make(bsf, 1, 2, 2, 1000, 1000, 128, 128, 128)
-    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
-    out, lse = bsf.attention_fwd(qd, kd, vd, mi, 0.1, 0.0)
-    with pytest.raises(bsf.SplashError):
-        bsf.attention_bwd(qd, kd, vd, out, lse, torch.zeros_like(out), mi, 0.1, 0.0)
+RAGGED_BWD = [
+    # label, B, Hq, Hkv, Lq, Lk, d, softcap, mask kwargs
+    ("causal GQA 1000", 1, 4, 2, 1000, 1000, 128, 0.0, dict(causal=True)),
+    ("no mask 700 x 900, cap, batch 2", 2, 2, 1, 700, 900, 64, 20.0, dict(causal=False)),
+    ("window + causal 1090", 1, 2, 2, 1090, 1090, 128, 0.0, dict(causal=True, wl=300)),
+]
+
+
+@pytest.mark.parametrize("case", RAGGED_BWD, ids=[c[0] for c in RAGGED_BWD])
+def test_ragged_backward_matches_the_oracle(bsf, case):
+    from tests.test_gpu_backward import compare_grad, d_term_allowance
+    label, B, Hq, Hkv, Lq, Lk, d, cap, kw = case
+    q, k, v, mi, ospec = make(bsf, B, Hq, Hkv, Lq, Lk, d, d, 128, seed=23 * RAGGED_BWD.index(case), **kw)
+    g = workloads.normal_bf16((B, Hq, Lq, d), 500 + RAGGED_BWD.index(case))
+    scale = 1.0 / math.sqrt(d)
+    qd, kd, vd, gd = q.cuda(), k.cuda(), v.cuda(), g.cuda()
+    out, lse = bsf.attention_fwd(qd, kd, vd, mi, scale, cap)
+    # guard tails after dk / dv: padding keys must never be stored
+    kbuf, dk = guarded(tuple(k.shape), torch.bfloat16, 7.0)
+    vbuf, dv = guarded(tuple(v.shape), torch.bfloat16, 7.0)
+    dq, dk, dv = bsf.attention_bwd(qd, kd, vd, out, lse, gd, mi, scale, cap, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert bsf.last_device_error() == 0, label
+    assert torch.all(kbuf[dk.numel():] == 7.0) and torch.all(vbuf[dv.numel():] == 7.0), f"{label}: wrote past"
+    ref = oracle.attention_bwd(q, k, v, g, ospec, scale, cap)
+    extra = d_term_allowance(q, k, v, g, ospec, scale, cap)
+    compare_grad(dq, ref["dq"], f"{label}: dq", extra)
+    compare_grad(dk, ref["dk"], f"{label}: dk")
+    compare_grad(dv, ref["dv"], f"{label}: dv")
     mi.close()
