@@ -338,7 +338,8 @@ splash_status splash_attention_merge(const float *o_part, const float *lse_part,
  *   dv_out device bf16 [B][Hkv][Lk][dv]   (all fully overwritten)
  *   workspace  device, 16-byte aligned, at least
  *              splash_attention_bwd_workspace_size(B, Hq, Lq, dqk) bytes
- *              (an fp32 dq accumulator and D); caller-owned, overwritten.
+ *              (an fp32 dq accumulator, D and a copy of lse, over whole
+ *              128-row blocks per head); caller-owned, overwritten.
  * All device pointers 16-byte aligned.  Supported: dqk == dv in {64, 128}
  * and MaskInfo blocks bq = bk = 128, any Lq / Lk (ragged lengths as in the
  * forward; the workspace covers whole 128-row blocks per head); other valid
