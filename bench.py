@@ -98,6 +98,32 @@ def recorded_traffic(workload_index):
     return rec.get("bytes_per_launch") if kernel_source_sha() == rec.get("kernel_sha256_prefix") else None
 
 
+def percentiles(xs, qs=(10, 50, 90)):
+    """Nearest-rank percentiles of a list of times."""
+    ys = sorted(xs)
+    return [ys[min(len(ys) - 1, max(0, int(math.ceil(q / 100 * len(ys))) - 1))] for q in qs]
+
+
+def mask_info_rate(w, counts, shape, build_ms, peaks):
+    """The MaskInfo build against HBM: algorithmic bytes = segment IDs read
+    (4 (Lq + Lk) per table batch row, with segment IDs), block_mask (1 byte
+    per block), row_ptr (4 (R + 1)), the active lists (3 int32 + 2 flag bytes
+    per active block) and the patterns (bq*bk bytes plus their bit-packed
+    copy) written; divided by the median build time."""
+    R = shape["batch_rows"] * shape["nq"]
+    nk = shape["nk"]
+    seg = 4 * (w.q_len + w.L) * shape["batch_rows"] if w.documents else 0
+    P = counts["num_patterns"]
+    nbytes = (seg + R * nk + 4 * (R + 1) + counts["num_active"] * (3 * 4 + 2) + P * w.bq * w.bk
+              + P * w.bq * w.bk // 8)
+    med = percentiles(build_ms)[1]
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    gbs = nbytes / (med * 1e-3) / 1e9
+    return {"ms_p50": round(med, 5), "bytes": int(nbytes), "gbs": round(gbs, 2), "hbm_peak_gbs": hbm,
+            "frac_of_hbm": round(gbs / hbm, 5),
+            "note": "launch- and latency-bound at these sizes: the table is KB to a few MB"}
+
+
 def reduce_max(value, world, device=None):
     """Max of a float over ranks (identity for one rank)."""
     if world <= 1:
@@ -304,6 +330,7 @@ def run_ours(args):
     bsf.check_device_error()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     attn_ms = [a.elapsed_time(b) for a, b in ea]
+    build_ms = [a[0].elapsed_time(b[0]) for a, b in zip(ev, ea)]  # step start -> attention start
     ms_step = reduce_max(statistics.mean(step_ms), world, dev)
     ms_attn = reduce_max(statistics.mean(attn_ms), world, dev)
     value = whole_job_throughput(useful, world, ms_step)
@@ -333,6 +360,8 @@ def run_ours(args):
                    "patterns": counts["num_patterns"], "parallelism": f"replicas x{world}"},
         "attention_ms": round(ms_attn, 5),
         "mask_build_ms": round(ms_step - ms_attn, 5),
+        "attention_ms_p10_p50_p90": [round(x, 5) for x in percentiles(attn_ms)],
+        "mask_info": mask_info_rate(w, counts, mi.shape(), build_ms, peaks),
         "attention_useful_tflops": round(useful / (ms_attn * 1e-3) / 1e12, 2),
         "attention_executed_tflops": round(achieved, 2),
         "pct_of_bf16_peak_useful": round(100 * useful / (ms_attn * 1e-3) / 1e12 / peak, 2),
