@@ -61,7 +61,7 @@ struct splash_mask_info {
   int32_t *part_pidx = nullptr;    // [cap_active] pattern index (valid for representatives)
   int32_t *rep_list = nullptr;     // [cap_active] partial index of pattern u
   int32_t *row_hist = nullptr;     // [nk+1] counting-sort bins
-  unsigned long long *counters = nullptr;  // [8]: A, A_p, P, allowed, max_row
+  unsigned long long *counters = nullptr;  // [8]: A, A_p, P, allowed, max_row, deferred blocks
   // host staging
   unsigned long long *h_counters = nullptr;  // pinned [8]
   // counts of an asynchronous build: h_counters is valid once `counts_ready`

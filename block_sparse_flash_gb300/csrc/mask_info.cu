@@ -143,9 +143,13 @@ __global__ void seg_summary_kernel(DevMask m, int32_t *qsum, int32_t *kvsum) {
 // One thread per block (bm, r, c); a CTA covers 128 blocks of one row.
 constexpr int kClassifyThreads = 128;
 
+// Blocks the segment summaries cannot decide (both a shared and a differing
+// segment id possible) are either counted here element by element (deferred
+// == nullptr) or appended to `deferred` (block index row * nk + c, count in
+// counters[5]) for count_deferred_kernel, which counts each with a whole CTA.
 __global__ void __launch_bounds__(kClassifyThreads)
 classify_kernel(DevMask m, const int32_t *qsum, const int32_t *kvsum, int8_t *block_mask,
-                int32_t *row_cnt, int32_t *row_pcnt, unsigned long long *counters) {
+                int32_t *row_cnt, int32_t *row_pcnt, unsigned long long *counters, int32_t *deferred) {
   const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t r = blockIdx.y;
   const int32_t bm = blockIdx.z;
@@ -174,6 +178,11 @@ classify_kernel(DevMask m, const int32_t *qsum, const int32_t *kvsum, int8_t *bl
       const int32_t kmn = kvsum[((int64_t)bm * m.nk + c) * 2], kmx = kvsum[((int64_t)bm * m.nk + c) * 2 + 1];
       if (qmx < kmn || kmx < qmn) {
         cnt = 0;  // no segment id in common
+      } else if (!(qmn == qmx && kmn == kmx && qmn == kmn) && deferred != nullptr) {
+        // undecided by the summaries: counted by count_deferred_kernel
+        const unsigned long long slot = atomicAdd(&counters[5], 1ull);
+        deferred[slot] = (int32_t)(row * m.nk + c);
+        cnt = -1;
       } else if (!(qmn == qmx && kmn == kmx && qmn == kmn)) {
         // undecided by the summaries: count element by element
         const int32_t *kv = m.kvseg + (int64_t)bm * m.Lk;
@@ -188,8 +197,13 @@ classify_kernel(DevMask m, const int32_t *qsum, const int32_t *kvsum, int8_t *bl
       }
       // (both constant and equal: the band count stands)
     }
-    cls = cnt == 0 ? 0 : (cnt == (int64_t)m.bq * m.bk ? 2 : 1);
-    block_mask[row * m.nk + c] = (int8_t)cls;
+    if (cnt < 0) {
+      cnt = 0;  // deferred: class and counts come from count_deferred_kernel
+      cls = 0;
+    } else {
+      cls = cnt == 0 ? 0 : (cnt == (int64_t)m.bq * m.bk ? 2 : 1);
+      block_mask[row * m.nk + c] = (int8_t)cls;
+    }
   }
   // reduce within the CTA (all threads share the row)
   int na = cls != 0, np = cls == 1;
@@ -219,6 +233,48 @@ classify_kernel(DevMask m, const int32_t *qsum, const int32_t *kvsum, int8_t *bl
     if (ta) atomicAdd(&row_cnt[row], ta);
     if (tp) atomicAdd(&row_pcnt[row], tp);
     if (ts) atomicAdd(&counters[3], ts);
+  }
+}
+
+// One CTA (kClassifyThreads threads, one per query row of the block) per
+// deferred block: the allowed pairs of row i are the keys of the row's band
+// range with i's segment id; the block's class and its row / total counts are
+// then added like classify_kernel's.
+__global__ void __launch_bounds__(kClassifyThreads)
+count_deferred_kernel(DevMask m, const int32_t *deferred, int8_t *block_mask, int32_t *row_cnt, int32_t *row_pcnt,
+                      unsigned long long *counters) {
+  __shared__ unsigned long long part[kClassifyThreads / 32];
+  const int64_t n = (int64_t)counters[5];
+  const int di = threadIdx.x, lane = di & 31;
+  for (int64_t x = blockIdx.x; x < n; x += gridDim.x) {
+    const int64_t idx = deferred[x];
+    const int64_t row = idx / m.nk, c = idx - row * m.nk;
+    const int32_t bm = (int32_t)(row / m.nq);
+    const int64_t r = row - (int64_t)bm * m.nq;
+    unsigned long long cnt = 0;
+    if (di < m.bq) {
+      const int64_t i = r * m.bq + di;
+      int64_t lo, hi;
+      band_range(m, i, c * m.bk, c * m.bk + m.bk - 1, lo, hi);
+      if (hi >= lo) {
+        const int32_t sq = q_segment(m, bm, i);
+        const int32_t *kv = m.kvseg + (int64_t)bm * m.Lk;
+        for (int64_t j = lo; j <= hi; ++j) cnt += (kv[j] == sq);
+      }
+    }
+    for (int off = 16; off; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+    if (lane == 0) part[di >> 5] = cnt;
+    __syncthreads();
+    if (di == 0) {
+      unsigned long long t = 0;
+      for (int w = 0; w < kClassifyThreads / 32; ++w) t += part[w];
+      const int cls = t == 0 ? 0 : (t == (unsigned long long)m.bq * m.bk ? 2 : 1);
+      block_mask[idx] = (int8_t)cls;
+      if (cls != 0) atomicAdd(&row_cnt[row], 1);
+      if (cls == 1) atomicAdd(&row_pcnt[row], 1);
+      if (t) atomicAdd(&counters[3], t);
+    }
+    __syncthreads();
   }
 }
 
@@ -988,7 +1044,12 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
   {
     dim3 grid((unsigned)((nk + kClassifyThreads - 1) / kClassifyThreads), (unsigned)nq, (unsigned)nbm);
     classify_kernel<<<grid, kClassifyThreads, 0, stream>>>(m, qsum, kvsum, mi->block_mask, mi->row_cnt,
-                                                          mi->row_pcnt, mi->counters);
+                                                          mi->row_pcnt, mi->counters, seg ? mi->rep_list : nullptr);
+  }
+  if (seg) {
+    // the deferred list lives in rep_list, which finalize_kernel fills later
+    count_deferred_kernel<<<sms * 4, kClassifyThreads, 0, stream>>>(m, mi->rep_list, mi->block_mask, mi->row_cnt,
+                                                                   mi->row_pcnt, mi->counters);
   }
   scan_rows_kernel<<<1, 1024, 0, stream>>>(R, mi->row_cnt, mi->row_pcnt, mi->row_ptr, mi->prow_ptr,
                                            mi->counters);
@@ -1004,7 +1065,7 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
   finalize_kernel<<<sms * 4, 256, 0, stream>>>(mi->counters, mi->part_g, mi->part_rep,
                                                mi->part_pidx, mi->mask_next, mi->rep_list);
   SPLASH_CUDA_TRY(cudaGetLastError());
-  splash_count_launches(seg ? 10 : 9);
+  splash_count_launches(seg ? 11 : 9);
 
   int64_t P_cap;
   if (async) {
@@ -1173,7 +1234,7 @@ splash_status splash_classify_blocks_noalloc_impl(const splash_mask_spec *spec, 
   {
     dim3 grid((unsigned)((nk + kClassifyThreads - 1) / kClassifyThreads), (unsigned)nq, (unsigned)nbm);
     classify_kernel<<<grid, kClassifyThreads, 0, stream>>>(m, s->qsum, s->kvsum, block_mask, s->row_cnt,
-                                                          s->row_pcnt, s->counters);
+                                                          s->row_pcnt, s->counters, nullptr);
   }
   noalloc_totals_kernel<<<1, 256, 0, stream>>>(R, s);
   SPLASH_CUDA_TRY(cudaGetLastError());
