@@ -655,10 +655,10 @@ __device__ __forceinline__ f32x2 tanh_series2(f32x2 s, f32x2 k) {
 // of the mask: causal and window bounds, and the padding of ragged lengths --
 // "Pallas Kernels and Splash Attention" §6.6: masks can be computed in the
 // kernel from q / kv positions instead of stored patterns).
-template <int BK>
+template <int BK, bool BAND>
 __device__ __forceinline__ void partial_bits(const FwdParams &p, int32_t mn, int row, int64_t qpos, int32_t g_idx,
                                              uint32_t (&bits)[BK / 32]) {
-  if (p.band_bits) {
+  if constexpr (BAND) {
     const int64_t c0 = (int64_t)__ldg(p.active_cols + g_idx) * BK;
     int64_t lo = c0, hi = min(c0 + BK - 1, p.Lk - 1);
     if (p.band_causal) hi = min(hi, qpos);
@@ -695,7 +695,9 @@ __device__ __forceinline__ float exp2_block(float (&s)[N], float mul, float sub)
   return t.x + t.y;
 }
 
-template <int DQK, int DV, int BK>
+// BAND: partial blocks' masks computed from positions (a separate
+// instantiation, so that the default stored-pattern loop is unchanged).
+template <int DQK, int DV, int BK, bool BAND>
 __global__ void __launch_bounds__(kThreads, 1)
 splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -798,7 +800,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         const bool need_mask = partial || !row_valid;
         uint32_t bits[BK / 32];
         if (partial && row_valid) {
-          partial_bits<BK>(p, mn, row, (int64_t)it.qrow * p.bq + row, it.g0 + g, bits);
+          partial_bits<BK, BAND>(p, mn, row, (int64_t)it.qrow * p.bq + row, it.g0 + g, bits);
         } else {
 #pragma unroll
           for (int x = 0; x < BK / 32; ++x) bits[x] = row_valid ? 0xffffffffu : 0u;
@@ -891,17 +893,27 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             for (int j = 0; j < BK; ++j) s[j] = tanh_identity(s[j] * p.cap_inner);
           }
           if (need_mask) {
-            uint32_t rb[BK / 32];
-            if (partial && row_valid) {
-              partial_bits<BK>(p, mn, row, (int64_t)it.qrow * p.bq + row, it.g0 + g, rb);
+            if constexpr (BAND) {
+              uint32_t rb[BK / 32];
+              if (partial && row_valid) {
+                partial_bits<BK, BAND>(p, mn, row, (int64_t)it.qrow * p.bq + row, it.g0 + g, rb);
+              } else {
+#pragma unroll
+                for (int x = 0; x < BK / 32; ++x) rb[x] = row_valid ? 0xffffffffu : 0u;
+              }
+#pragma unroll
+              for (int x = 0; x < BK / 32; ++x) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) s[x * 32 + j] = ((rb[x] >> j) & 1u) ? s[x * 32 + j] : -INFINITY;
+              }
             } else {
+              const uint32_t *src = p.pattern_bits + ((int64_t)mn * p.bq + row) * (BK / 32);
 #pragma unroll
-              for (int x = 0; x < BK / 32; ++x) rb[x] = row_valid ? 0xffffffffu : 0u;
-            }
+              for (int x = 0; x < BK / 32; ++x) {
+                const uint32_t b = (partial && row_valid) ? __ldg(src + x) : (row_valid ? 0xffffffffu : 0u);
 #pragma unroll
-            for (int x = 0; x < BK / 32; ++x) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) s[x * 32 + j] = ((rb[x] >> j) & 1u) ? s[x * 32 + j] : -INFINITY;
+                for (int j = 0; j < 32; ++j) s[x * 32 + j] = ((b >> j) & 1u) ? s[x * 32 + j] : -INFINITY;
+              }
             }
           }
           if (redo) {
@@ -1119,7 +1131,7 @@ bool make_map_3d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t row
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int DQK, int DV, int BK>
+template <int DQK, int DV, int BK, bool BAND>
 splash_status launch(const void *q, const void *k, const void *v, const FwdParams &prm, cudaStream_t stream) {
   using C = Cfg<DQK, DV, BK>;
   CUtensorMap tq, tk, tv, to;
@@ -1136,16 +1148,27 @@ splash_status launch(const void *q, const void *k, const void *v, const FwdParam
   int sms = 148;
   SPLASH_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   if (configured_device != dev) {
-    SPLASH_CUDA_TRY(cudaFuncSetAttribute(splash_fwd_kernel<DQK, DV, BK>,
+    SPLASH_CUDA_TRY(cudaFuncSetAttribute(splash_fwd_kernel<DQK, DV, BK, BAND>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
     configured_device = dev;
   }
   const int64_t grid = prm.num_items < sms ? prm.num_items : sms;
   if (grid <= 0) return SPLASH_OK;
-  splash_fwd_kernel<DQK, DV, BK><<<(unsigned)grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, to, prm);
+  splash_fwd_kernel<DQK, DV, BK, BAND><<<(unsigned)grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, to, prm);
   SPLASH_CUDA_TRY(cudaGetLastError());
   splash_count_launches(1);
   return SPLASH_OK;
+}
+
+template <bool BAND>
+splash_status launch_shape(const void *q, const void *k, const void *v, const FwdParams &prm, int32_t dqk,
+                           int32_t dv, int32_t bk, cudaStream_t stream) {
+  if (dqk == 128 && dv == 128 && bk == 128) return launch<128, 128, 128, BAND>(q, k, v, prm, stream);
+  if (dqk == 192 && dv == 128 && bk == 128) return launch<192, 128, 128, BAND>(q, k, v, prm, stream);
+  if (dqk == 64 && dv == 64 && bk == 64) return launch<64, 64, 64, BAND>(q, k, v, prm, stream);
+  if (dqk == 64 && dv == 64 && bk == 128) return launch<64, 64, 128, BAND>(q, k, v, prm, stream);
+  if (dqk == 128 && dv == 128 && bk == 64) return launch<128, 128, 64, BAND>(q, k, v, prm, stream);
+  return SPLASH_ERR_UNSUPPORTED;
 }
 
 }  // namespace
@@ -1203,12 +1226,8 @@ splash_status splash_attention_fwd_launch(const void *q, const void *k, const vo
   prm.err = err_word;
   prm.timeout_ns = 1000000000ull;  // 1 s per wait
   const int bk = mi->bk;
-  if (dqk == 128 && dv == 128 && bk == 128) return launch<128, 128, 128>(q, k, v, prm, stream);
-  if (dqk == 192 && dv == 128 && bk == 128) return launch<192, 128, 128>(q, k, v, prm, stream);
-  if (dqk == 64 && dv == 64 && bk == 64) return launch<64, 64, 64>(q, k, v, prm, stream);
-  if (dqk == 64 && dv == 64 && bk == 128) return launch<64, 64, 128>(q, k, v, prm, stream);
-  if (dqk == 128 && dv == 128 && bk == 64) return launch<128, 128, 64>(q, k, v, prm, stream);
-  return SPLASH_ERR_UNSUPPORTED;
+  if (prm.band_bits) return launch_shape<true>(q, k, v, prm, dqk, dv, bk, stream);
+  return launch_shape<false>(q, k, v, prm, dqk, dv, bk, stream);
 }
 
 splash_status splash_wait_selftest_launch(uint64_t timeout_ns, cudaStream_t stream, uint32_t *err_word) {
