@@ -66,6 +66,9 @@ ATTN = [
     ("documents, 900, batch 2", 2, 2, 2, 900, 900, 128, 128, 128, 0.0, dict(causal=True, docs=True)),
     ("d192/128 MHA, 650 x 700", 1, 2, 2, 650, 700, 192, 128, 128, 0.0, dict(causal=False)),
     ("one real row past a block, 129", 1, 2, 1, 129, 129, 128, 128, 128, 0.0, dict(causal=True)),
+    ("a single query against 4096 keys (decode)", 2, 4, 1, 1, 4096, 128, 128, 128, 0.0, dict(causal=False)),
+    ("keys shorter than a block, 300 x 50", 1, 2, 2, 300, 50, 64, 64, 64, 10.0, dict(causal=False)),
+    ("a single query, causal (sees key 0 only)", 1, 2, 2, 1, 777, 128, 128, 128, 0.0, dict(causal=True)),
 ]
 
 
