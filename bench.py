@@ -49,10 +49,20 @@ def parse_args(argv=None):
                     help="time the backward pass (MaskInfo rebuild + gradients) instead of the forward")
     ap.add_argument("--pattern-source", choices=["stored", "positions"], default="stored",
                     help="partial-block masks from the stored patterns or computed from positions")
+    ap.add_argument("--bq", type=int, default=None,
+                    help="override the workload's query block (e.g. 256: two 128-row tiles of one head "
+                         "share each K / V tile)")
     ap.add_argument("--max-logit", type=float, default=None,
                     help="Max Logit Estimate: fix every row's softmax reference at this constant "
                          "(e.g. the workload's soft cap)")
     return ap.parse_args(argv)
+
+
+def bench_workload(args):
+    import dataclasses
+    import workloads
+    w = workloads.workload(args.workload)
+    return dataclasses.replace(w, bq=args.bq) if args.bq else w
 
 
 # --------------------------------------------------------------------- accounting
@@ -263,7 +273,7 @@ def run_ours(args):
         dist.barrier()
     bsf.lib()
 
-    w = workloads.workload(args.workload)
+    w = bench_workload(args)
     inp = workloads.make_inputs(w)
     q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
     seg = inp.segment_ids.to(dev) if inp.segment_ids is not None else None
@@ -343,7 +353,7 @@ def run_ours(args):
                 "frac": round(achieved / peak, 4), "traffic": None,
                 "kernel": "splash_fwd_kernel", "peak_source": f"{peak_src} bf16 burst (cuBLAS)",
                 "achieved_is": "executed FLOPs of the active blocks per launch / mean launch time (CUDA events)"}
-    roofline["traffic"] = recorded_traffic(args.workload)
+    roofline["traffic"] = recorded_traffic(args.workload) if args.bq is None else None
 
     e2e = None
     if not args.no_e2e:
@@ -448,7 +458,7 @@ def run_reference(args):
     if rank != 0:
         return
     import workloads
-    w = workloads.workload(args.workload)
+    w = bench_workload(args)
     inp = workloads.make_inputs(w)
     _, dt, nth, n = oracle_sample_rate(w, inp, 128, 3)
     rate = n / max(dt, 1e-6)
@@ -496,7 +506,7 @@ def run_backward(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     libbuild.build()
-    w = workloads.workload(args.workload)
+    w = bench_workload(args)
     inp = workloads.make_inputs(w)
     q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
     dout = workloads.normal_bf16((w.B, w.Hq, w.q_len, w.dv), 1000 * w.index + 5).to(dev)

@@ -22,6 +22,8 @@ uint32_t *g_error_addr[kMaxDevices];
 std::mutex g_error_mu;
 
 bool valid_block(int32_t b) { return b == 64 || b == 128; }
+// query blocks may also be 256 rows tall (two 128-row tiles of one head)
+bool valid_q_block(int32_t b) { return valid_block(b) || b == 256; }
 
 splash_status check_spec(const splash_mask_spec *spec, int64_t Lq, int64_t Lk) {
   if (spec == nullptr) return SPLASH_ERR_INVALID_ARG;
@@ -38,7 +40,7 @@ splash_status check_spec(const splash_mask_spec *spec, int64_t Lq, int64_t Lk) {
 
 splash_status check_geometry(int64_t Lq, int64_t Lk, int32_t bq, int32_t bk) {
   if (Lq <= 0 || Lk <= 0 || bq <= 0 || bk <= 0) return SPLASH_ERR_INVALID_ARG;
-  if (!valid_block(bq) || !valid_block(bk)) return SPLASH_ERR_UNSUPPORTED;
+  if (!valid_q_block(bq) || !valid_block(bk)) return SPLASH_ERR_UNSUPPORTED;
   // ragged lengths are padded to whole blocks (the padding is masked)
   if ((Lq + bq - 1) / bq > 65535 || Lk > (int64_t)1 << 30 || Lq > (int64_t)1 << 30) return SPLASH_ERR_UNSUPPORTED;
   return SPLASH_OK;
@@ -202,7 +204,7 @@ splash_status check_attention(const void *q, const void *k, const void *v, int32
                         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
   if (mis & 15u) return SPLASH_ERR_INVALID_ARG;
   const bool shape_ok = ((dqk == 128 && dv == 128) || (dqk == 192 && dv == 128) || (dqk == 64 && dv == 64)) &&
-                        mi->bq == mi->bk;
+                        (mi->bq == mi->bk || (mi->bq == 256 && mi->bk == 128));
   if (!shape_ok) return SPLASH_ERR_UNSUPPORTED;
   if (mi->bk == 64 && dqk == 192) return SPLASH_ERR_UNSUPPORTED;
   if ((int64_t)B * Hq * Lq >= ((int64_t)1 << 31) || (int64_t)B * Hkv * Lk >= ((int64_t)1 << 31))

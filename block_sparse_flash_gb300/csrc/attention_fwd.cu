@@ -101,7 +101,11 @@ struct FwdParams {
   int32_t B, Hq, Hkv, G;
   int64_t Lq, Lk;
   int32_t bq, nq, nk, nbm;
-  int32_t npairs;
+  // an item's two 128-row query tiles: two heads of one q-block (t1_off = 0,
+  // bq <= 128), or the two halves of one 256-row q-block of one head
+  // (t1_off = 128; the tiles then share every K / V tile)
+  int32_t t1_off;
+  int32_t npairs;  // head pairs (t1_off = 0) or heads (t1_off = 128) per row
   int64_t num_items;
   const int32_t *row_ptr;
   const int32_t *active_cols;
@@ -146,6 +150,9 @@ struct Item {
 // each row expands into B batches; each (row, batch) into npairs head pairs;
 // each of those into nsplit consecutive ranges of the row's active blocks
 // (split s of nb blocks: [nb*s/nsplit, nb*(s+1)/nsplit)).
+// TALL: 256-row q-blocks (p.t1_off = 128), a compile-time flag so that the
+// head-pair items of the other instantiations carry no extra branch.
+template <bool TALL>
 __device__ __forceinline__ Item decode_item(const FwdParams &p, int64_t w) {
   Item it;
   int64_t k;
@@ -178,9 +185,14 @@ __device__ __forceinline__ Item decode_item(const FwdParams &p, int64_t w) {
     it.g0 += lo;
     it.nb = hi - lo;
   }
-  it.h0 = 2 * pair;
-  it.h1 = 2 * pair + 1;
-  it.act1 = it.h1 < p.Hq;
+  if constexpr (TALL) {
+    it.h0 = it.h1 = pair;
+    it.act1 = (int64_t)it.qrow * p.bq + p.t1_off < p.Lq;  // the lower half holds a real row
+  } else {
+    it.h0 = 2 * pair;
+    it.h1 = 2 * pair + 1;
+    it.act1 = it.h1 < p.Hq;
+  }
   it.kvh0 = it.h0 / p.G;
   it.kvh1 = it.act1 ? it.h1 / p.G : it.kvh0;
   it.shared = (it.kvh0 == it.kvh1);
@@ -279,7 +291,7 @@ __device__ __forceinline__ int32_t checked_col(const FwdParams &p, int32_t g) {
 // tiles in exactly the order the MMA issuer consumes them:
 //   K0(0) [K1(0)], then per block g: V0(g) K0(g+1) [V1(g) K1(g+1)]
 // (the bracketed loads only when the two query heads use different KV heads).
-template <class C, int BK>
+template <class C, int BK, bool TALL>
 __device__ __noinline__ void run_producer(const FwdParams &p, const CUtensorMap *tmQ, const CUtensorMap *tmK,
                                           const CUtensorMap *tmV, uint32_t sQ, uint32_t sK, uint32_t sV,
                                           const Bars<C> bar, volatile int *abort) {
@@ -288,7 +300,7 @@ __device__ __noinline__ void run_producer(const FwdParams &p, const CUtensorMap 
   for (int64_t k = 0; ok; ++k) {
     const int64_t w = item_of_round(p, k);
     if (w < 0) break;
-    const Item it = decode_item(p, w);
+    const Item it = decode_item<TALL>(p, w);
     if (it.nb <= 0) continue;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
@@ -299,7 +311,8 @@ __device__ __noinline__ void run_producer(const FwdParams &p, const CUtensorMap 
         break;
       }
       mbar_arrive_expect_tx(bar.q_full(t), C::Q_BYTES);
-      const int32_t y = (int32_t)(((int64_t)it.b * p.Hq + (t ? it.h1 : it.h0)) * p.Lq + (int64_t)it.qrow * p.bq);
+      const int32_t y = (int32_t)(((int64_t)it.b * p.Hq + (t ? it.h1 : it.h0)) * p.Lq + (int64_t)it.qrow * p.bq +
+                                  ((TALL && t) ? 128 : 0));
 #pragma unroll
       for (int ch = 0; ch < C::QCH; ++ch)
         tma_load_2d(sQ + t * C::Q_BYTES + ch * C::Q_CHUNK, tmQ, ch * 64, y, bar.q_full(t));
@@ -448,7 +461,7 @@ __device__ __forceinline__ void ring_step_release(RingState &r, uint32_t empty0,
 // s_full after each S, o_done after the last PV, q_empty after the tile's
 // last S.  Two issuers keep one tile's MMA burst from waiting behind the
 // other's in the tensor pipe's queue.
-template <class C, int BK>
+template <class C, int BK, bool TALL>
 __device__ __noinline__ void run_mma(const FwdParams &p, uint32_t tmem, uint32_t sQ, uint32_t sK, uint32_t sV,
                                      const Bars<C> bar, volatile int *abort, const int t) {
   RingState kr{0u, 0u, false}, vr{0u, 0u, false};
@@ -459,7 +472,7 @@ __device__ __noinline__ void run_mma(const FwdParams &p, uint32_t tmem, uint32_t
   for (int64_t k = 0; ok; ++k) {
     const int64_t w = item_of_round(p, k);
     if (w < 0) break;
-    const Item it = decode_item(p, w);
+    const Item it = decode_item<TALL>(p, w);
     if (it.nb <= 0) continue;
     const bool mine = (t == 0) || it.act1;
     const bool two_kv = it.act1 && !it.shared;
@@ -550,7 +563,7 @@ __device__ __forceinline__ bool wait_ready(uint32_t pb, uint32_t pph, bool need_
 //   wait P_1(g): O_1 += P_1 V(g); S_1(g+1) = Q_1 K(g+1)^T.
 // Commits: s_full after each S, o_done after the last PV, slot releases
 // after the last MMA that reads a slot, q_empty after a tile's last S.
-template <class C, int BK>
+template <class C, int BK, bool TALL>
 __device__ __forceinline__ void run_mma_pair(const FwdParams &p, uint32_t tmem, uint32_t sQ, uint32_t sK, uint32_t sV,
                                      const Bars<C> bar, volatile int *abort, const uint32_t leader) {
   const uint64_t tmo = p.timeout_ns;
@@ -560,7 +573,7 @@ __device__ __forceinline__ void run_mma_pair(const FwdParams &p, uint32_t tmem, 
   for (int64_t k = 0; ok; ++k) {
     const int64_t w = item_of_round(p, k);
     if (w < 0) break;
-    const Item it = decode_item(p, w);
+    const Item it = decode_item<TALL>(p, w);
     if (it.nb <= 0) continue;
     const bool two = it.act1;
     const bool two_kv = it.act1 && !it.shared;
@@ -697,7 +710,7 @@ __device__ __forceinline__ float exp2_block(float (&s)[N], float mul, float sub)
 
 // BAND: partial blocks' masks computed from positions (a separate
 // instantiation, so that the default stored-pattern loop is unchanged).
-template <int DQK, int DV, int BK, bool BAND>
+template <int DQK, int DV, int BK, bool BAND, bool TALL>
 __global__ void __launch_bounds__(kThreads, 1)
 splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -757,12 +770,12 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   // ============================================================ warpgroup 2
   regs_decrease<kControlRegs>();
   if (warp == kProducerWarp) {
-    if (lane == 0) run_producer<C, BK>(p, &tmQ, &tmK, &tmV, sQ, sK, sV, bar, abort);
+    if (lane == 0) run_producer<C, BK, TALL>(p, &tmQ, &tmK, &tmV, sQ, sK, sV, bar, abort);
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     if (p.dual_issuer) {
-      if (lane == 0) run_mma<C, BK>(p, tmem, sQ, sK, sV, bar, abort, warp - kMmaWarp);
+      if (lane == 0) run_mma<C, BK, TALL>(p, tmem, sQ, sK, sV, bar, abort, warp - kMmaWarp);
     } else if (warp == kMmaWarp) {
-      run_mma_pair<C, BK>(p, tmem, sQ, sK, sV, bar, abort, elect_one_sync());
+      run_mma_pair<C, BK, TALL>(p, tmem, sQ, sK, sV, bar, abort, elect_one_sync());
     }
   }
   } else {
@@ -776,18 +789,16 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + 128u * t + lane_off;
     const uint32_t tO = tmem + 256u + 128u * t + lane_off;
-    const bool row_valid = row < p.bq;
+    const int prow = (TALL && t) ? 128 + row : row;  // row within the q-block (pattern row)
+    const bool row_valid = prow < p.bq;
     uint32_t scnt = 0, ocnt = 0;
     bool ok = true;
     for (int64_t k = 0; ok; ++k) {
       const int64_t w = item_of_round(p, k);
       if (w < 0) break;
-      const Item it = decode_item(p, w);
+      const Item it = decode_item<TALL>(p, w);
       if (t == 1 && !it.act1) continue;
-      const int32_t h = t ? it.h1 : it.h0;
-      const int64_t orow = ((int64_t)it.b * p.Hq + h) * p.Lq + (int64_t)it.qrow * p.bq + row;
-      // rows past a ragged Lq are padding: computed (all masked), never stored
-      const bool row_out = row_valid && (int64_t)it.qrow * p.bq + row < p.Lq;
+      const int32_t qpos = it.qrow * p.bq + prow;  // < 2^31: nq * bq <= 65535 * 256
       float m_ref = p.use_mle ? p.mle_ref : -INFINITY;  // running reference (log2 units)
       float l = 0.f;
       for (int32_t g = 0; g < it.nb && ok; ++g) {
@@ -800,7 +811,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         const bool need_mask = partial || !row_valid;
         uint32_t bits[BK / 32];
         if (partial && row_valid) {
-          partial_bits<BK, BAND>(p, mn, row, (int64_t)it.qrow * p.bq + row, it.g0 + g, bits);
+          partial_bits<BK, BAND>(p, mn, prow, qpos, it.g0 + g, bits);
         } else {
 #pragma unroll
           for (int x = 0; x < BK / 32; ++x) bits[x] = row_valid ? 0xffffffffu : 0u;
@@ -896,7 +907,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             if constexpr (BAND) {
               uint32_t rb[BK / 32];
               if (partial && row_valid) {
-                partial_bits<BK, BAND>(p, mn, row, (int64_t)it.qrow * p.bq + row, it.g0 + g, rb);
+                partial_bits<BK, BAND>(p, mn, prow, qpos, it.g0 + g, rb);
               } else {
 #pragma unroll
                 for (int x = 0; x < BK / 32; ++x) rb[x] = row_valid ? 0xffffffffu : 0u;
@@ -907,7 +918,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 for (int j = 0; j < 32; ++j) s[x * 32 + j] = ((rb[x] >> j) & 1u) ? s[x * 32 + j] : -INFINITY;
               }
             } else {
-              const uint32_t *src = p.pattern_bits + ((int64_t)mn * p.bq + row) * (BK / 32);
+              const uint32_t *src = p.pattern_bits + ((int64_t)mn * p.bq + prow) * (BK / 32);
 #pragma unroll
               for (int x = 0; x < BK / 32; ++x) {
                 const uint32_t b = (partial && row_valid) ? __ldg(src + x) : (row_valid ? 0xffffffffu : 0u);
@@ -953,6 +964,10 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       }
       if (!ok) break;
       // ---- epilogue: O / l and the LSE
+      const int32_t h = t ? it.h1 : it.h0;
+      const int64_t orow = ((int64_t)it.b * p.Hq + h) * p.Lq + qpos;
+      // rows past a ragged Lq are padding: computed (all masked), never stored
+      const bool row_out = row_valid && qpos < p.Lq;
       if (it.nb > 0) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar.o_done(t), ocnt & 1, abort, p.timeout_ns));
         if (!ok) break;
@@ -988,7 +1003,8 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         // columns), one TMA store per box: whole-line global writes instead
         // of 32 rows' scattered pieces per store instruction
         const uint32_t stage = sStage + (uint32_t)warp * C::STAGE_WARP;
-        const bool warp_rows = wq * 32 < p.bq;  // rows beyond bq belong to no output
+        const int wrow = ((TALL && t) ? 128 : 0) + wq * 32;  // the warp's first row within the q-block
+        const bool warp_rows = wrow < p.bq;             // rows beyond bq belong to no output
 #pragma unroll
         for (int hh = 0; hh < DV / 64; ++hh) {
           uint32_t r0[32], r1[32];
@@ -1022,7 +1038,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             if (lane == 0) {
               // O viewed as [B*Hq][Lq][DV]: rows past a ragged Lq fall outside
               // the tensor and the store clips them
-              tma_store_3d(&tmO, stage, 64 * hh, it.qrow * p.bq + wq * 32, it.b * p.Hq + h);
+              tma_store_3d(&tmO, stage, 64 * hh, it.qrow * p.bq + wrow, it.b * p.Hq + h);
               bulk_commit_group();
             }
           }
@@ -1131,7 +1147,7 @@ bool make_map_3d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t row
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int DQK, int DV, int BK, bool BAND>
+template <int DQK, int DV, int BK, bool BAND, bool TALL>
 splash_status launch(const void *q, const void *k, const void *v, const FwdParams &prm, cudaStream_t stream) {
   using C = Cfg<DQK, DV, BK>;
   CUtensorMap tq, tk, tv, to;
@@ -1148,13 +1164,13 @@ splash_status launch(const void *q, const void *k, const void *v, const FwdParam
   int sms = 148;
   SPLASH_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   if (configured_device != dev) {
-    SPLASH_CUDA_TRY(cudaFuncSetAttribute(splash_fwd_kernel<DQK, DV, BK, BAND>,
+    SPLASH_CUDA_TRY(cudaFuncSetAttribute(splash_fwd_kernel<DQK, DV, BK, BAND, TALL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
     configured_device = dev;
   }
   const int64_t grid = prm.num_items < sms ? prm.num_items : sms;
   if (grid <= 0) return SPLASH_OK;
-  splash_fwd_kernel<DQK, DV, BK, BAND><<<(unsigned)grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, to, prm);
+  splash_fwd_kernel<DQK, DV, BK, BAND, TALL><<<(unsigned)grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, to, prm);
   SPLASH_CUDA_TRY(cudaGetLastError());
   splash_count_launches(1);
   return SPLASH_OK;
@@ -1163,11 +1179,17 @@ splash_status launch(const void *q, const void *k, const void *v, const FwdParam
 template <bool BAND>
 splash_status launch_shape(const void *q, const void *k, const void *v, const FwdParams &prm, int32_t dqk,
                            int32_t dv, int32_t bk, cudaStream_t stream) {
-  if (dqk == 128 && dv == 128 && bk == 128) return launch<128, 128, 128, BAND>(q, k, v, prm, stream);
-  if (dqk == 192 && dv == 128 && bk == 128) return launch<192, 128, 128, BAND>(q, k, v, prm, stream);
-  if (dqk == 64 && dv == 64 && bk == 64) return launch<64, 64, 64, BAND>(q, k, v, prm, stream);
-  if (dqk == 64 && dv == 64 && bk == 128) return launch<64, 64, 128, BAND>(q, k, v, prm, stream);
-  if (dqk == 128 && dv == 128 && bk == 64) return launch<128, 128, 64, BAND>(q, k, v, prm, stream);
+  if (prm.t1_off) {  // 256-row q-blocks: two halves of one head per item (bk = 128)
+    if (dqk == 128 && dv == 128 && bk == 128) return launch<128, 128, 128, BAND, true>(q, k, v, prm, stream);
+    if (dqk == 192 && dv == 128 && bk == 128) return launch<192, 128, 128, BAND, true>(q, k, v, prm, stream);
+    if (dqk == 64 && dv == 64 && bk == 128) return launch<64, 64, 128, BAND, true>(q, k, v, prm, stream);
+    return SPLASH_ERR_UNSUPPORTED;
+  }
+  if (dqk == 128 && dv == 128 && bk == 128) return launch<128, 128, 128, BAND, false>(q, k, v, prm, stream);
+  if (dqk == 192 && dv == 128 && bk == 128) return launch<192, 128, 128, BAND, false>(q, k, v, prm, stream);
+  if (dqk == 64 && dv == 64 && bk == 64) return launch<64, 64, 64, BAND, false>(q, k, v, prm, stream);
+  if (dqk == 64 && dv == 64 && bk == 128) return launch<64, 64, 128, BAND, false>(q, k, v, prm, stream);
+  if (dqk == 128 && dv == 128 && bk == 64) return launch<128, 128, 64, BAND, false>(q, k, v, prm, stream);
   return SPLASH_ERR_UNSUPPORTED;
 }
 
@@ -1193,7 +1215,8 @@ splash_status splash_attention_fwd_launch(const void *q, const void *k, const vo
   prm.nq = (int32_t)mi->nq;
   prm.nk = (int32_t)mi->nk;
   prm.nbm = mi->batch_rows;
-  prm.npairs = (Hq + 1) / 2;
+  prm.t1_off = mi->bq == 256 ? 128 : 0;
+  prm.npairs = prm.t1_off ? Hq : (Hq + 1) / 2;
   const int64_t rows = (int64_t)mi->batch_rows * mi->nq;
   prm.nsplit = nsplit > 1 ? nsplit : 1;
   prm.num_items = (mi->batch_rows == 1 ? rows * B : rows) * prm.npairs * prm.nsplit;
@@ -1217,8 +1240,9 @@ splash_status splash_attention_fwd_launch(const void *q, const void *k, const vo
   prm.use_mle = std::isnan(max_logit) ? 0 : 1;  // NaN: off
   prm.mle_ref = prm.use_mle ? max_logit * kLog2e : 0.f;
   // one issuer per tile only when the two query heads of an item read
-  // different KV heads (MHA); shared K/V keeps one issuer for both tiles
-  prm.dual_issuer = (prm.G == 1) ? 1 : 0;
+  // different KV heads (MHA with two heads per item); shared K/V (GQA heads,
+  // or the two halves of a 256-row q-block) keeps one issuer for both tiles
+  prm.dual_issuer = (prm.G == 1 && !prm.t1_off) ? 1 : 0;
   prm.cap_inner = softcap > 0.f ? scale / softcap : 0.f;
   prm.cap_log2 = softcap > 0.f ? softcap * kLog2e : 0.f;
   prm.out = reinterpret_cast<__nv_bfloat16 *>(out);

@@ -165,7 +165,8 @@ classify_kernel(DevMask m, const int32_t *qsum, const int32_t *kvsum, int8_t *bl
       cls = band_block_class(m, A, W, r, c);
       block_mask[row * m.nk + c] = (int8_t)cls;
     }
-    if (blockIdx.x == 0 && (int)threadIdx.x < m.bq) cnt = band_row_count(m, A, W, r * m.bq + threadIdx.x);
+    if (blockIdx.x == 0)
+      for (int32_t di = threadIdx.x; di < m.bq; di += blockDim.x) cnt += band_row_count(m, A, W, r * m.bq + di);
   } else if (c < m.nk) {
     const int64_t c0 = c * m.bk, c1 = c0 + m.bk - 1;
     for (int32_t di = 0; di < m.bq; ++di) {
@@ -252,8 +253,8 @@ count_deferred_kernel(DevMask m, const int32_t *deferred, int8_t *block_mask, in
     const int32_t bm = (int32_t)(row / m.nq);
     const int64_t r = row - (int64_t)bm * m.nq;
     unsigned long long cnt = 0;
-    if (di < m.bq) {
-      const int64_t i = r * m.bq + di;
+    for (int32_t d = di; d < m.bq; d += kClassifyThreads) {
+      const int64_t i = r * m.bq + d;
       int64_t lo, hi;
       band_range(m, i, c * m.bk, c * m.bk + m.bk - 1, lo, hi);
       if (hi >= lo) {
@@ -410,7 +411,7 @@ __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
 __global__ void partial_hash_kernel(DevMask m, const unsigned long long *counters,
                                     const int32_t *part_row, const int32_t *part_col,
                                     uint64_t *part_hash) {
-  __shared__ uint64_t wsum[4];
+  __shared__ uint64_t wsum[8];  // bq <= 256 threads
   const int64_t Ap = (int64_t)counters[1];
   const int di = threadIdx.x;
   for (int64_t k = blockIdx.x; k < Ap; k += gridDim.x) {

@@ -101,7 +101,9 @@ typedef struct splash_mask_info splash_mask_info;
  *               nk = ceil(Lk/bk) whole blocks and the padding positions are
  *               masked (§2.3: ragged edges are padded so that every block has
  *               the same size); a block holding padding is never full.
- *   bq, bk      block sizes; this build supports bq, bk in {64, 128}.
+ *   bq, bk      block sizes; this build supports bk in {64, 128} and
+ *               bq in {64, 128, 256} (the worked example of "Pallas Kernels
+ *               and Splash Attention" §6.2 already uses bq != bk).
  *   cuda_stream stream for the build kernels.
  *   out         receives a new handle (set to NULL on error).
  *
@@ -202,10 +204,15 @@ void splash_mask_info_destroy(splash_mask_info *mi);
  *   softcap <= 0 disables the cap (NaN or +inf is rejected).
  *   out  device bf16 [B][Hq][Lq][dv]       lse device fp32 [B][Hq][Lq]
  *
- * Supported in this build: dqk in {64, 128, 192}, dv in {64, 128}, dv <= dqk
- * when dqk = 192 is used with dv = 128, Hq % Hkv == 0, and the MaskInfo's
- * blocks bq, bk in {64, 128} with bq == bk.  Other valid shapes return
- * SPLASH_ERR_UNSUPPORTED.
+ * Supported in this build: (dqk, dv) in {(64, 64), (128, 128), (192, 128)},
+ * Hq % Hkv == 0, and the MaskInfo's blocks bq == bk in {64, 128} (bk = 128
+ * for dqk = 192), or bq = 256 with bk = 128.  The kernel computes in query
+ * tiles of 128 rows, two per work item: with bq <= 128 the two tiles are
+ * two query heads of one q-block (sharing K / V within a GQA group), with
+ * bq = 256 they are the two halves of one q-block of one head and share
+ * every K / V tile (this halves the K / V traffic of MHA; blocks of the
+ * union that are masked for one half are computed and contribute nothing).
+ * Other valid shapes return SPLASH_ERR_UNSUPPORTED.
  * Errors are returned before any launch; kernel-side bounded waits and table
  * checks are reported by splash_last_device_error.
  */

@@ -60,6 +60,9 @@ def test_invalid_arguments_are_rejected_before_any_launch(splash):
     assert lib.splash_build_mask_info(ctypes.byref(spec), 0, 256, 64, 64, null, ctypes.byref(out)) == 1
     assert lib.splash_build_mask_info(ctypes.byref(spec), 256, 256, 32, 32, null, ctypes.byref(out)) == 3
     assert lib.splash_build_mask_info(ctypes.byref(spec), 256, 256, 64, 96, null, ctypes.byref(out)) == 3
+    # query blocks may be 256 rows tall, key blocks may not
+    assert lib.splash_build_mask_info(ctypes.byref(spec), 512, 512, 128, 256, null, ctypes.byref(out)) == 3
+    assert lib.splash_build_mask_info(ctypes.byref(spec), 512, 512, 512, 128, null, ctypes.byref(out)) == 3
     bad = splash._Spec(2, -1, -1, None, None, 0)
     assert lib.splash_build_mask_info(ctypes.byref(bad), 256, 256, 64, 64, null, ctypes.byref(out)) == 1
     bad = splash._Spec(1, -5, -1, None, None, 0)

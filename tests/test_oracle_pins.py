@@ -225,7 +225,8 @@ def test_causal_closed_form_square_blocks(L, b):
     assert mi.allowed_pairs == L * (L + 1) // 2
 
 
-@pytest.mark.parametrize("L,bq,bk", [(1024, 64, 128), (1024, 128, 64), (768, 32, 96), (4096, 1024, 2048)])
+@pytest.mark.parametrize("L,bq,bk", [(1024, 64, 128), (1024, 128, 64), (768, 32, 96), (4096, 1024, 2048),
+                                     (4096, 256, 128)])
 def test_causal_closed_form_rectangular_blocks(L, bq, bk):
     nq, nk = L // bq, L // bk
     mi = oracle.mask_info(MaskSpec(causal=True), L, L, bq, bk)
@@ -236,6 +237,22 @@ def test_causal_closed_form_rectangular_blocks(L, bq, bk):
         assert int(np.count_nonzero(row)) == active
         assert int(np.count_nonzero(row == 2)) == full
     assert mi.allowed_pairs == L * (L + 1) // 2
+
+
+def test_causal_tall_blocks_two_patterns():
+    # bq = 2 bk, causal: row i holds 2i + 2 active blocks, of which the last
+    # two are partial -- block 2i (the upper half on the diagonal, the lower
+    # half full) and block 2i + 1 (the upper half empty, the lower half on
+    # the diagonal) -- and every row repeats the same two patterns
+    L, bq, bk = 4096, 256, 128
+    mi = oracle.mask_info(MaskSpec(causal=True), L, L, bq, bk)
+    n = L // bq
+    assert mi.num_active == sum(2 * i + 2 for i in range(n)) == 272
+    assert mi.num_partial == 2 * n and mi.num_patterns == 2
+    tri = np.tril(np.ones((bk, bk), dtype=np.uint8))
+    np.testing.assert_array_equal(mi.partial_mask_blocks[0], np.vstack([tri, np.ones((bk, bk), np.uint8)]))
+    np.testing.assert_array_equal(mi.partial_mask_blocks[1], np.vstack([np.zeros((bk, bk), np.uint8), tri]))
+    assert list(mi.mask_next[:2]) == [0, 1] and list(mi.mask_next[2:6]) == [-1, -1, 0, 1]
 
 
 @pytest.mark.parametrize("L,b,w", [(4096, 128, 8), (8192, 128, 8), (2048, 64, 5), (65536, 1024, 4)])

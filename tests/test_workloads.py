@@ -37,4 +37,5 @@ def test_workload_table():
     assert [w.index for w in workloads.WORKLOADS] == [1, 2, 3, 4, 5]
     w5 = workloads.workload(5)
     assert (w5.window_left, w5.softcap, w5.L) == (4095, 30.0, 65536)
-    assert workloads.workload(3).dqk == 192 and workloads.workload(3).dv == 128
+    w3 = workloads.workload(3)
+    assert (w3.dqk, w3.dv, w3.bq, w3.bk) == (192, 128, 256, 128)

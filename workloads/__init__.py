@@ -71,7 +71,9 @@ class Workload:
 WORKLOADS: List[Workload] = [
     Workload(1, "tiny causal MHA", 1, 2, 2, 256, 64, 64, 64, 64),
     Workload(2, "dense causal GQA", 2, 32, 8, 4096, 128, 128, 128, 128),
-    Workload(3, "wide-head causal MHA", 1, 128, 128, 4096, 192, 128, 128, 128),
+    # the configuration leaves the blocks open: 256-row q-blocks let the
+    # kernel's two 128-row tiles of one head share each K / V tile
+    Workload(3, "wide-head causal MHA", 1, 128, 128, 4096, 192, 128, 256, 128),
     Workload(4, "document + causal GQA", 1, 16, 8, 32768, 128, 128, 128, 128, documents=True),
     Workload(5, "local window 4096 + causal + softcap 30", 1, 32, 8, 65536, 128, 128, 128, 128,
              window_left=4095, window_right=0, softcap=30.0),
