@@ -89,9 +89,17 @@ struct Cfg {
   static constexpr int STAGE_WARP = 32 * 128;
   static constexpr bool STAGE = TILES + 8 * STAGE_WARP <= TILE_BUDGET;
   static constexpr int STAGE_BYTES = STAGE ? 8 * STAGE_WARP : 0;
+  // At dqk = 192 (one 32 KB V slot next to two 48 KB K slots) the items of
+  // 256-row q-blocks stream K and V instead through a ring of NCH chunk
+  // slots of one 64-column box each (the same bytes), so that V tiles are no
+  // longer limited to one slot.
+  static constexpr int NCH = (DQK >= 192 && BK == 128) ? (NK * K_BYTES + NV * V_BYTES) / KV_CHUNK : 0;
+  static_assert(NCH == 0 || NCH * KV_CHUNK == NK * K_BYTES + NV * V_BYTES, "chunk ring covers the K/V region");
+  static_assert(NCH <= 32, "chunk-slot bit masks");
+  static_assert(NCH == 0 || (QCH <= 3 && VCH <= 3), "release_chunks covers at most three chunks per tile");
   // barriers: q_full[2] q_empty[2] k_full[NK] k_empty[NK] v_full[NV] v_empty[NV]
-  //           s_full[2] p_full[2] o_done[2] drain
-  static constexpr int NBAR = 2 + 2 + 2 * NK + 2 * NV + 2 + 2 + 2 + 1;
+  //           s_full[2] p_full[2] o_done[2] drain ch_full[NCH] ch_empty[NCH]
+  static constexpr int NBAR = 2 + 2 + 2 * NK + 2 * NV + 2 + 2 + 2 + 1 + 2 * NCH;
   static constexpr int SMEM = 1024 + TILES + STAGE_BYTES + NBAR * 8 + 16;
   static constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, BK, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, DV, true);
@@ -245,7 +253,7 @@ __device__ __forceinline__ float tanh_identity(float t) {
 
 // Shared-memory addresses of the CTA's mbarriers:
 //   q_full[2] q_empty[2] k_full[NK] k_empty[NK] v_full[NV] v_empty[NV]
-//   s_full[2] p_full[2] o_done[2] drain
+//   s_full[2] p_full[2] o_done[2] drain ch_full[NCH] ch_empty[NCH]
 template <class C>
 struct Bars {
   uint32_t base;
@@ -259,6 +267,10 @@ struct Bars {
   __device__ __forceinline__ uint32_t p_full(int t) const { return base + 8u * (6 + 2 * C::NK + 2 * C::NV + t); }
   __device__ __forceinline__ uint32_t o_done(int t) const { return base + 8u * (8 + 2 * C::NK + 2 * C::NV + t); }
   __device__ __forceinline__ uint32_t drain() const { return base + 8u * (10 + 2 * C::NK + 2 * C::NV); }
+  __device__ __forceinline__ uint32_t ch_full(uint32_t s) const { return base + 8u * (11 + 2 * C::NK + 2 * C::NV + s); }
+  __device__ __forceinline__ uint32_t ch_empty(uint32_t s) const {
+    return base + 8u * (11 + 2 * C::NK + 2 * C::NV + C::NCH + s);
+  }
 };
 
 // Loads one K or V tile (CH boxes of 64 columns x BK rows) into the next slot
@@ -653,6 +665,231 @@ __device__ __forceinline__ void run_mma_pair(const FwdParams &p, uint32_t tmem, 
   if (!mbar_wait_drain(bar.drain(), 0, tmo) && leader) atomicOr(p.err, SPLASH_DEV_TIMEOUT_DRAIN);
 }
 
+// ---------------------------------------------------------------- chunk ring
+// Items of 256-row q-blocks at dqk = 192: both tiles read every K / V tile,
+// and the K / V region is a ring of NCH chunk slots (one 64-column x BK-row
+// box each).  Chunk n of the stream goes to slot n % NCH; a K tile is QCH
+// consecutive chunks, a V tile VCH, in the issuer's order
+//   K(0), then per block g: V(g), K(g+1)
+// and a tile's chunks need not be adjacent in shared memory.  Each chunk is
+// released on its own barrier (ch_empty, one commit per use) as soon as the
+// MMAs that read it have completed, so the loads of the next tiles start
+// chunk by chunk instead of waiting for a whole slot.  A tile completes on
+// the full barrier of its first chunk's slot (armed with the whole tile's
+// bytes), so the issuer waits once per tile; since which slots start a tile
+// varies, both sides track those barriers' phases per slot (bit masks).
+//
+// Phase safety: the producer arms ch_full(s) only after waiting for
+// ch_empty(s), i.e. after the issuer has released the chunk that last used
+// slot s; the issuer consumes tiles in stream order, so by then it has
+// waited for every earlier tile, including the last one armed on ch_full(s).
+
+// One K or V tile of `nch` chunks at global row y, streamed into the ring.
+template <class C>
+__device__ __forceinline__ bool produce_tile_chunked(const FwdParams &p, const CUtensorMap *tm, uint32_t ring,
+                                                     const Bars<C> &bar, uint32_t &n, uint32_t &armed,
+                                                     uint32_t &arm_par, int nch, int32_t y, volatile int *abort) {
+  const uint32_t first = n % C::NCH;
+  for (int ch = 0; ch < nch; ++ch, ++n) {
+    const uint32_t s = n % C::NCH;
+    if (n >= (uint32_t)C::NCH && !mbar_wait(bar.ch_empty(s), ((n / C::NCH) - 1u) & 1u, abort, p.timeout_ns))
+      return false;
+    if (ch == 0) {
+      mbar_arrive_expect_tx(bar.ch_full(first), (uint32_t)(nch * C::KV_CHUNK));
+      armed |= 1u << first;
+      arm_par ^= 1u << first;  // bit = number of armings of the slot, mod 2
+    }
+    tma_load_2d(ring + s * C::KV_CHUNK, tm, ch * 64, y, bar.ch_full(first));
+  }
+  return true;
+}
+
+template <class C, int BK>
+__device__ __noinline__ void run_producer_chunked(const FwdParams &p, const CUtensorMap *tmQ, const CUtensorMap *tmK,
+                                                  const CUtensorMap *tmV, uint32_t sQ, uint32_t ring,
+                                                  const Bars<C> bar, volatile int *abort) {
+  uint32_t n = 0, armed = 0, arm_par = 0, q0 = 0, q1 = 0;
+  bool ok = true;
+  for (int64_t k = 0; ok; ++k) {
+    const int64_t w = item_of_round(p, k);
+    if (w < 0) break;
+    const Item it = decode_item<true>(p, w);
+    if (it.nb <= 0) continue;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if (t == 1 && !it.act1) break;
+      uint32_t &qc = t ? q1 : q0;
+      if (qc > 0 && !mbar_wait(bar.q_empty(t), (qc - 1) & 1, abort, p.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(bar.q_full(t), C::Q_BYTES);
+      const int32_t y = (int32_t)(((int64_t)it.b * p.Hq + it.h0) * p.Lq + (int64_t)it.qrow * p.bq + 128 * t);
+#pragma unroll
+      for (int ch = 0; ch < C::QCH; ++ch)
+        tma_load_2d(sQ + t * C::Q_BYTES + ch * C::Q_CHUNK, tmQ, ch * 64, y, bar.q_full(t));
+      ++qc;
+    }
+    if (!ok) break;
+    const int64_t kv0 = ((int64_t)it.b * p.Hkv + it.kvh0) * p.Lk;
+    int32_t c = checked_col(p, it.g0);
+    ok = produce_tile_chunked<C>(p, tmK, ring, bar, n, armed, arm_par, C::QCH, (int32_t)(kv0 + (int64_t)c * BK),
+                                 abort);
+    for (int32_t g = 0; g < it.nb && ok; ++g) {
+      const bool more = g + 1 < it.nb;
+      const int32_t cn = more ? checked_col(p, it.g0 + g + 1) : 0;
+      ok = produce_tile_chunked<C>(p, tmV, ring, bar, n, armed, arm_par, C::VCH, (int32_t)(kv0 + (int64_t)c * BK),
+                                   abort);
+      if (ok && more)
+        ok = produce_tile_chunked<C>(p, tmK, ring, bar, n, armed, arm_par, C::QCH,
+                                     (int32_t)(kv0 + (int64_t)cn * BK), abort);
+      c = cn;
+    }
+  }
+  if (!ok) raise_error(p, abort, SPLASH_DEV_TIMEOUT_PRODUCER);
+  // drain: the last tile armed on every slot has landed (its phase parity is
+  // the number of armings minus one, mod 2)
+  bool drained = true;
+  for (int s = 0; s < C::NCH; ++s)
+    if ((armed >> s) & 1u) drained &= mbar_wait_drain(bar.ch_full(s), ((arm_par >> s) & 1u) ^ 1u, p.timeout_ns);
+  if (q0 > 0) drained &= mbar_wait_drain(bar.q_full(0), (q0 - 1) & 1, p.timeout_ns);
+  if (q1 > 0) drained &= mbar_wait_drain(bar.q_full(1), (q1 - 1) & 1, p.timeout_ns);
+  if (!drained) atomicOr(p.err, SPLASH_DEV_TIMEOUT_DRAIN);
+}
+
+// S_t = Q_t K^T with the K tile's chunk ch in ring slot (first + ch) % NCH.
+template <class C>
+__device__ __forceinline__ void issue_qk_chunked(uint32_t d_tmem, uint32_t q_addr, uint32_t ring, uint32_t first,
+                                                 uint32_t leader) {
+  constexpr uint32_t HI = sdesc_hi_sw128(1024);
+  const uint32_t qd = sdesc_lo(q_addr, 16);
+#pragma unroll
+  for (int ch = 0; ch < C::QCH; ++ch) {
+    const uint32_t kd = sdesc_lo(ring + ((first + ch) % C::NCH) * C::KV_CHUNK, 16);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_ss_lhp(leader, d_tmem, qd + (uint32_t)((ch * C::Q_CHUNK + kk * 32) >> 4), HI,
+                 kd + (uint32_t)((kk * 32) >> 4), HI, C::IDESC_QK, (ch | kk) != 0);
+  }
+}
+
+// O_t (+)= P_t V, one N = 64 MMA chain per V chunk (the chunks need not be
+// adjacent, so each is its own MN-major operand): output columns 64h..64h+63
+// of O_t from chunk h.
+template <class C, int BK>
+__device__ __forceinline__ void issue_pv_chunked(uint32_t d_tmem, uint32_t p_tmem, uint32_t ring, uint32_t first,
+                                                 bool first_block, uint32_t leader) {
+  constexpr uint32_t HI = sdesc_hi_sw128(1024);
+  constexpr uint32_t IDESC_PV64 = idesc_bf16_f32(128, 64, true);  // N = one 64-column V chunk
+#pragma unroll
+  for (int h = 0; h < C::VCH; ++h) {
+    const uint32_t vd = sdesc_lo(ring + ((first + h) % C::NCH) * C::KV_CHUNK, C::KV_CHUNK);
+#pragma unroll
+    for (int j = 0; j < BK / 16; ++j)
+      mma_ts_lhp(leader, d_tmem + 64u * h, p_tmem + 8u * j, vd + (uint32_t)((j * 2048) >> 4), HI, IDESC_PV64,
+                 (!first_block || j > 0) ? 1u : 0u);
+  }
+}
+
+// Releases chunks first .. first+nch-1 when the MMAs issued so far complete.
+template <class C>
+__device__ __forceinline__ void release_chunks(const Bars<C> &bar, uint32_t first, int nch, uint32_t leader) {
+#pragma unroll
+  for (int ch = 0; ch < 3; ++ch)
+    if (ch < nch) tc_commit_p(leader, bar.ch_empty((first + ch) % C::NCH));
+}
+
+// The single MMA issuer for items of 256-row q-blocks on the chunk ring (the
+// run_mma_pair schedule with shared K / V):
+//   S_0(0), S_1(0); then per block g:
+//   wait P_0(g): O_0 += P_0 V(g); S_0(g+1) = Q_0 K(g+1)^T;
+//   wait P_1(g): O_1 += P_1 V(g); S_1(g+1) = Q_1 K(g+1)^T.
+// A tile's chunks are released after the last MMA that reads them (tile 1's,
+// or tile 0's when the lower half of the block is all padding).
+template <class C, int BK>
+__device__ __forceinline__ void run_mma_pair_chunked(const FwdParams &p, uint32_t tmem, uint32_t sQ, uint32_t ring,
+                                                     const Bars<C> bar, volatile int *abort, const uint32_t leader) {
+  const uint64_t tmo = p.timeout_ns;
+  uint32_t n = 0, fwait = 0, q0 = 0, q1 = 0, p0 = 0, p1 = 0;
+  bool ok = true;
+  const uint32_t tS0 = tmem, tS1 = tmem + 128u, tO0 = tmem + 256u, tO1 = tmem + 384u;
+  for (int64_t k = 0; ok; ++k) {
+    const int64_t w = item_of_round(p, k);
+    if (w < 0) break;
+    const Item it = decode_item<true>(p, w);
+    if (it.nb <= 0) continue;
+    const bool two = it.act1;
+    // S_0(0) [and S_1(0)]: Q tiles and the first K tile
+    const uint32_t kf0 = n, ks0 = kf0 % C::NCH;
+    if (!(ok = wait_ready(bar.q_full(0), q0 & 1u, two, bar.q_full(1), q1 & 1u, true, bar.ch_full(ks0),
+                          (fwait >> ks0) & 1u, abort, tmo)))
+      break;
+    fwait ^= 1u << ks0;
+    n += C::QCH;
+    ++q0;
+    if (two) ++q1;
+    tc_fence_after();
+    issue_qk_chunked<C>(tS0, sQ, ring, kf0, leader);
+    tc_commit_p(leader, bar.s_full(0));
+    if (two) {
+      issue_qk_chunked<C>(tS1, sQ + C::Q_BYTES, ring, kf0, leader);
+      tc_commit_p(leader, bar.s_full(1));
+    }
+    release_chunks<C>(bar, kf0, C::QCH, leader);
+    if (it.nb == 1) {
+      tc_commit_p(leader, bar.q_empty(0));
+      if (two) tc_commit_p(leader, bar.q_empty(1));
+    }
+    for (int32_t g = 0; g < it.nb && ok; ++g) {
+      const bool more = g + 1 < it.nb;
+      // the stream: V(g), then K(g+1)
+      const uint32_t vf = n, vs = vf % C::NCH;
+      n += C::VCH;
+      const uint32_t kf = n, ks = kf % C::NCH;
+      if (more) n += C::QCH;
+      // ---- tile 0: P_0(g) and V(g); then K(g+1), which is waited for
+      // separately: its chunks reuse the slots of the previous block's V
+      // (released last), so it tends to land after V(g)
+      if (!(ok = wait_ready(bar.p_full(0), p0 & 1u, true, bar.ch_full(vs), (fwait >> vs) & 1u, false, 0u, 0u,
+                            abort, tmo)))
+        break;
+      fwait ^= 1u << vs;
+      ++p0;
+      tc_fence_after();
+      issue_pv_chunked<C, BK>(tO0, tS0, ring, vf, g == 0, leader);
+      if (!more) tc_commit_p(leader, bar.o_done(0));
+      if (!two) release_chunks<C>(bar, vf, C::VCH, leader);
+      if (more) {
+        if (!(ok = mbar_wait(bar.ch_full(ks), (fwait >> ks) & 1u, abort, tmo))) break;
+        fwait ^= 1u << ks;
+        tc_fence_after();
+        issue_qk_chunked<C>(tS0, sQ, ring, kf, leader);
+        tc_commit_p(leader, bar.s_full(0));
+        if (!two) release_chunks<C>(bar, kf, C::QCH, leader);
+        if (g + 2 == it.nb) tc_commit_p(leader, bar.q_empty(0));
+      }
+      if (!two) continue;
+      // ---- tile 1: P_1(g); V(g) and K(g+1) are resident
+      if (!(ok = mbar_wait(bar.p_full(1), p1 & 1u, abort, tmo))) break;
+      ++p1;
+      tc_fence_after();
+      issue_pv_chunked<C, BK>(tO1, tS1, ring, vf, g == 0, leader);
+      if (!more) tc_commit_p(leader, bar.o_done(1));
+      release_chunks<C>(bar, vf, C::VCH, leader);
+      if (more) {
+        issue_qk_chunked<C>(tS1, sQ + C::Q_BYTES, ring, kf, leader);
+        tc_commit_p(leader, bar.s_full(1));
+        release_chunks<C>(bar, kf, C::QCH, leader);
+        if (g + 2 == it.nb) tc_commit_p(leader, bar.q_empty(1));
+      }
+    }
+  }
+  if (!ok && leader) raise_error(p, abort, SPLASH_DEV_TIMEOUT_MMA);
+  // drain: every MMA issued by this warp has completed
+  tc_commit_p(leader, bar.drain());
+  if (!mbar_wait_drain(bar.drain(), 0, tmo) && leader) atomicOr(p.err, SPLASH_DEV_TIMEOUT_DRAIN);
+}
+
 // tanh(s*k) for two scores by the series (|s*k| <= 0.25), packed fp32x2:
 // a = s*k, then a + a*u*(c1 + c2*u) with u = a*a.
 __device__ __forceinline__ f32x2 tanh_series2(f32x2 s, f32x2 k) {
@@ -752,6 +989,10 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       mbar_init(bar.v_empty(s), p.dual_issuer ? 2 : 1);
     }
     mbar_init(bar.drain(), p.dual_issuer ? 2 : 1);
+    for (int s = 0; s < C::NCH; ++s) {
+      mbar_init(bar.ch_full(s), 1);   // the producer's arm of the tile whose first chunk is here
+      mbar_init(bar.ch_empty(s), 1);  // the (single) issuer's release of the chunk
+    }
     *abort = 0;
     mbar_fence_init();
   }
@@ -770,9 +1011,15 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   // ============================================================ warpgroup 2
   regs_decrease<kControlRegs>();
   if (warp == kProducerWarp) {
-    if (lane == 0) run_producer<C, BK, TALL>(p, &tmQ, &tmK, &tmV, sQ, sK, sV, bar, abort);
+    if constexpr (TALL && C::NCH > 0) {
+      if (lane == 0) run_producer_chunked<C, BK>(p, &tmQ, &tmK, &tmV, sQ, sK, bar, abort);
+    } else {
+      if (lane == 0) run_producer<C, BK, TALL>(p, &tmQ, &tmK, &tmV, sQ, sK, sV, bar, abort);
+    }
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-    if (p.dual_issuer) {
+    if constexpr (TALL && C::NCH > 0) {
+      if (warp == kMmaWarp) run_mma_pair_chunked<C, BK>(p, tmem, sQ, sK, bar, abort, elect_one_sync());
+    } else if (p.dual_issuer) {
       if (lane == 0) run_mma<C, BK, TALL>(p, tmem, sQ, sK, sV, bar, abort, warp - kMmaWarp);
     } else if (warp == kMmaWarp) {
       run_mma_pair<C, BK, TALL>(p, tmem, sQ, sK, sV, bar, abort, elect_one_sync());

@@ -67,6 +67,9 @@ FWD = [
     ("ragged 300, lower half all padding", 1, 3, 3, 300, 300, 128, 128, 0.0, 1.0, dict(causal=True)),
     ("a single short block, 100", 1, 2, 2, 100, 100, 64, 64, 0.0, 1.0, dict(causal=True)),
     ("huge logits (reference jumps)", 1, 2, 2, 768, 768, 128, 128, 0.0, 40.0, dict(causal=True)),
+    ("window 500 + causal + cap 30, d192 GQA", 1, 4, 2, 1536, 1536, 192, 128, 30.0, 2.0, dict(causal=True, wl=499)),
+    ("documents, d192/128 MHA", 1, 3, 3, 1280, 1280, 192, 128, 0.0, 1.0, dict(causal=True, docs=True)),
+    ("no mask d192, 384 x 2000 (many blocks per row)", 1, 2, 2, 384, 2000, 192, 128, 0.0, 1.0, dict(causal=False)),
 ]
 
 
