@@ -347,7 +347,7 @@ splash_status splash_last_device_error(void *cuda_stream) {
   if (word & (SPLASH_DEV_TIMEOUT_PRODUCER | SPLASH_DEV_TIMEOUT_MMA | SPLASH_DEV_TIMEOUT_SOFTMAX |
               SPLASH_DEV_TIMEOUT_DRAIN | SPLASH_DEV_TIMEOUT_SELFTEST))
     return SPLASH_ERR_DEVICE_TIMEOUT;
-  if (word & SPLASH_DEV_BAD_TABLE) return SPLASH_ERR_DEVICE_CHECK;
+  if (word & (SPLASH_DEV_BAD_TABLE | SPLASH_DEV_SMEM_ALIGN)) return SPLASH_ERR_DEVICE_CHECK;
   return SPLASH_OK;
 }
 

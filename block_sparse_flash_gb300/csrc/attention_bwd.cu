@@ -72,17 +72,28 @@ struct BwdCfg {
   static constexpr int CHUNK = 128 * 128;      // bytes of a 128-row x 64-column bf16 box
   static constexpr int TILE = CH * CHUNK;      // a 128-row x D tile
   static constexpr int DS_BYTES = 2 * CHUNK;   // dS^T: 128 keys x 128 queries
-  // shared memory: K, V, Q[2], dO, dS, LSE/D[2], barriers, TMEM holder, abort flag
+  // shared memory: K, V, Q[2], dO, dS, LSE/D[2], second dQ staging, barriers,
+  // TMEM holder, abort flag
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = TILE;
   static constexpr int OFF_Q = 2 * TILE;
   static constexpr int OFF_DO = 4 * TILE;
   static constexpr int OFF_DS = 5 * TILE;
   static constexpr int OFF_LD = 5 * TILE + DS_BYTES;  // [2][LSE 128 floats, D 128 floats]
-  static constexpr int OFF_BAR = OFF_LD + 2 * 1024;
+  // dQ readout: a warp reduces D / 64 pieces of 32 x 32 fp32 per iteration;
+  // the first is staged in the warp's own rows of the dS^T buffer, the second
+  // (D = 128) in a 4 KB slot of its own, so that the two reductions overlap
+  static constexpr int NPIECE = D / 64;
+  static constexpr int OFF_ST2 = OFF_LD + 2 * 1024;
+  static constexpr int ST2_BYTES = NPIECE > 1 ? 8 * 4096 : 0;
+  static constexpr int OFF_BAR = OFF_ST2 + ST2_BYTES;
   static constexpr int NBAR = 15;
-  static constexpr int SMEM = 1024 + OFF_BAR + NBAR * 8 + 16;
+  // no alignment slack: the dynamic shared memory starts 1024-byte aligned on
+  // this GPU (checked by the kernel, which does nothing and reports
+  // SPLASH_DEV_SMEM_ALIGN otherwise)
+  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(OFF_ST2 % 1024 == 0, "128B-swizzled staging needs 1024-byte alignment");
   // TMEM columns: S^T / P^T, dP^T / dQ, dV, dK
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
   // instruction descriptors (bits: 4-5 D f32, 7-9 A bf16, 10-12 B bf16,
@@ -395,15 +406,32 @@ __device__ void bwd_mma(const BwdParams &p, uint32_t tmem, uint32_t s0, const Bw
 // released as soon as the pieces are in registers; a later staging (or dS
 // store) into the same 4 KB first waits until the reduction has read it.
 // row0: accumulator row of the warp's first query.
+// The warp's bulk groups are committed in order piece 0 (slot A, the dS^T
+// rows), piece 1 (slot B, D = 128 only), and the dS^T rows are written
+// between readouts.  So before writing slot A (piece 0 or dS^T) only the
+// most recent group may still be reading when it is piece 1's (slot B), and
+// before writing slot B only the just-committed piece 0: bwd_wait_slot
+// waits for all groups but the latest one when D = 128, for all of them
+// when there is a single piece per readout.
+template <int D>
+__device__ __forceinline__ void bwd_wait_slot() {
+  if constexpr (D / 64 > 1)
+    bulk_wait_read_1();
+  else
+    bulk_wait_read_all();
+}
+
 template <int D>
 __device__ __forceinline__ bool bwd_readout(const BwdParams &p, const CUtensorMap *tmDQ, uint32_t tDQ, uint32_t m,
-                                            int32_t row0, int32_t col0, uint32_t stage, volatile int *abort,
-                                            uint32_t bars_dq_full, uint32_t bars_dq_empty, int lane) {
+                                            int32_t row0, int32_t col0, uint32_t stage, uint32_t stage2,
+                                            volatile int *abort, uint32_t bars_dq_full, uint32_t bars_dq_empty,
+                                            int lane) {
   if (!__all_sync(0xffffffffu, mbar_wait(bars_dq_full, m & 1u, abort, p.timeout_ns))) return false;
   tc_fence_after();
-  const uint32_t wrow = stage + (uint32_t)lane * 128u;
 #pragma unroll
   for (int c = 0; c < D / 64; ++c) {
+    const uint32_t slot = c == 0 ? stage : stage2;
+    const uint32_t wrow = slot + (uint32_t)lane * 128u;
     uint32_t r[32];
     tmem_ld32(tDQ + 32u * c, r);
     tmem_wait_ld();
@@ -413,7 +441,7 @@ __device__ __forceinline__ bool bwd_readout(const BwdParams &p, const CUtensorMa
       __syncwarp();
       if (lane == 0) mbar_arrive(bars_dq_empty);
     }
-    if (lane == 0) bulk_wait_read_all();  // the previous reduction has read the staging
+    if (lane == 0) bwd_wait_slot<D>();  // the slot's previous reduction has read it
     __syncwarp();
 #pragma unroll
     for (int y = 0; y < 8; ++y)
@@ -421,7 +449,7 @@ __device__ __forceinline__ bool bwd_readout(const BwdParams &p, const CUtensorMa
     fence_proxy_async_shared();
     __syncwarp();
     if (lane == 0) {
-      tma_reduce_add_2d(tmDQ, stage, col0 + 32 * c, row0);
+      tma_reduce_add_2d(tmDQ, slot, col0 + 32 * c, row0);
       bulk_commit_group();
     }
   }
@@ -448,6 +476,7 @@ __device__ void bwd_work(const BwdParams &p, const CUtensorMap *tmDQ, uint32_t t
   const int32_t col0 = wg * (D / 2);
   // this warp's 32 rows of its half of the dS^T buffer (staging for the dQ readout)
   const uint32_t stage = s0 + C::OFF_DS + wg * C::CHUNK + (uint32_t)(wq * 32) * 128u;
+  const uint32_t stage2 = s0 + C::OFF_ST2 + (uint32_t)warp * 4096u;  // D = 128 only
   for (int64_t k = 0; ok; ++k) {
     const int64_t w = bwd_item_of_round(p, k);
     if (w == -1) break;
@@ -517,8 +546,8 @@ __device__ void bwd_work(const BwdParams &p, const CUtensorMap *tmDQ, uint32_t t
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.p_ready());
       // ---- dQ(n-1) out of TMEM (its MMAs ran while P(n) was formed)
-      if (t > 0 && !(ok = bwd_readout<D>(p, tmDQ, tDQ, n - 1, prev_row, col0, stage, abort, bar.dq_full(),
-                                         bar.dq_empty(), lane)))
+      if (t > 0 && !(ok = bwd_readout<D>(p, tmDQ, tDQ, n - 1, prev_row, col0, stage, stage2, abort,
+                                         bar.dq_full(), bar.dq_empty(), lane)))
         break;
       // ---- dS^T(n) = P^T (dP^T - D) [(1 - t^2)], bf16 into the swizzled dS^T buffer
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar.dp_full(), n & 1u, abort, p.timeout_ns)))) break;
@@ -530,7 +559,7 @@ __device__ void bwd_work(const BwdParams &p, const CUtensorMap *tmDQ, uint32_t t
         tmem_wait_ld();
         reg_fence32(r0);
         reg_fence32(r1);
-        if (lane == 0) bulk_wait_read_all();  // dQ staging in these rows has been read
+        if (lane == 0) bwd_wait_slot<D>();  // dQ staging in these rows has been read
         __syncwarp();
         const uint32_t row = s0 + C::OFF_DS + wg * C::CHUNK + jj * 128;
 #pragma unroll
@@ -563,8 +592,8 @@ __device__ void bwd_work(const BwdParams &p, const CUtensorMap *tmDQ, uint32_t t
     }
     if (!ok) break;
     // ---- the item's last dQ, then dK, dV (complete once that dQ has landed)
-    if (!(ok = bwd_readout<D>(p, tmDQ, tDQ, n - 1, prev_row, col0, stage, abort, bar.dq_full(), bar.dq_empty(),
-                              lane)))
+    if (!(ok = bwd_readout<D>(p, tmDQ, tDQ, n - 1, prev_row, col0, stage, stage2, abort, bar.dq_full(),
+                              bar.dq_empty(), lane)))
       break;
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) {
@@ -603,9 +632,12 @@ splash_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                   const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using C = BwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {  // uniform over the CTA: nothing has started yet
+    if (threadIdx.x == 0) atomicOr(p.err, SPLASH_DEV_SMEM_ALIGN);
+    return;
+  }
+  uint8_t *smem = smem_raw;
   const uint32_t s0 = smem_u32(smem);
   const BwdBars bar{s0 + C::OFF_BAR};
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::OFF_BAR + C::NBAR * 8);

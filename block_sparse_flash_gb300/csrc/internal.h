@@ -15,6 +15,7 @@ enum : uint32_t {
   SPLASH_DEV_TIMEOUT_DRAIN = 1u << 3,
   SPLASH_DEV_TIMEOUT_SELFTEST = 1u << 4,
   SPLASH_DEV_BAD_TABLE = 1u << 8,
+  SPLASH_DEV_SMEM_ALIGN = 1u << 9,  // dynamic shared memory not 1024-byte aligned: the kernel did nothing
 };
 
 // The library-owned sparse execution table ("Pallas Kernels and Splash
