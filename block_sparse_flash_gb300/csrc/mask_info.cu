@@ -169,10 +169,19 @@ classify_kernel(DevMask m, const int32_t *qsum, const int32_t *kvsum, int8_t *bl
       for (int32_t di = threadIdx.x; di < m.bq; di += blockDim.x) cnt += band_row_count(m, A, W, r * m.bq + di);
   } else if (c < m.nk) {
     const int64_t c0 = c * m.bk, c1 = c0 + m.bk - 1;
-    for (int32_t di = 0; di < m.bq; ++di) {
-      int64_t lo, hi;
-      band_range(m, r * m.bq + di, c0, c1, lo, hi);
-      if (hi >= lo) cnt += hi - lo + 1;
+    // the band's allowed pairs of the block: none or all of them in closed
+    // form, counted row by row only for a band-partial block
+    int64_t A, W;
+    band_limits(m, A, W);
+    const int bcls = band_block_class(m, A, W, r, c);
+    if (bcls == 2) {
+      cnt = (int64_t)m.bq * m.bk;
+    } else if (bcls == 1) {
+      for (int32_t di = 0; di < m.bq; ++di) {
+        int64_t lo, hi;
+        band_range(m, r * m.bq + di, c0, c1, lo, hi);
+        if (hi >= lo) cnt += hi - lo + 1;
+      }
     }
     if (cnt > 0 && m.qseg != nullptr) {
       const int32_t qmn = qsum[row * 2], qmx = qsum[row * 2 + 1];
@@ -440,49 +449,56 @@ __global__ void partial_hash_kernel(DevMask m, const unsigned long long *counter
   }
 }
 
-// Warp-cooperative exact comparison of two partial blocks' patterns.
+// CTA-wide exact comparison of two partial blocks' patterns: each thread
+// compares (row, 32-key word) pieces of both blocks; every thread of the CTA
+// must call it and gets the same result.
 __device__ bool patterns_equal(const DevMask &m, const int32_t *part_row, const int32_t *part_col,
                                int64_t ka, int64_t kb) {
-  const int lane = threadIdx.x & 31;
   const int64_t rowa = part_row[ka], rowb = part_row[kb];
   const int32_t bma = (int32_t)(rowa / m.nq), bmb = (int32_t)(rowb / m.nq);
   const int64_t ra = rowa % m.nq, rb = rowb % m.nq, ca = part_col[ka], cb = part_col[kb];
+  const int32_t words = m.bk / 32;
   bool same = true;
-  for (int32_t di = lane; di < m.bq; di += 32) {
+  for (int32_t x = threadIdx.x; x < m.bq * words && same; x += blockDim.x) {
+    const int32_t di = x / words, w = x - di * words;
     const int64_t ia = ra * m.bq + di, ib = rb * m.bq + di;
-    const int32_t sa = q_segment(m, bma, ia), sb = q_segment(m, bmb, ib);
-    for (int32_t w = 0; w < m.bk / 32 && same; ++w)
-      same = row_word(m, bma, ia, sa, ca * m.bk + w * 32) == row_word(m, bmb, ib, sb, cb * m.bk + w * 32);
+    same = row_word(m, bma, ia, q_segment(m, bma, ia), ca * m.bk + w * 32) ==
+           row_word(m, bmb, ib, q_segment(m, bmb, ib), cb * m.bk + w * 32);
   }
-  return __all_sync(0xffffffffu, same);
+  return __syncthreads_and(same) != 0;
 }
 
-// One warp per partial block k: rep[k] = the first k' <= k with identical content.
-__global__ void dedup_kernel(DevMask m, const unsigned long long *counters, const int32_t *part_row,
-                             const int32_t *part_col, const uint64_t *part_hash, int32_t *part_rep) {
+// One CTA per partial block k (grid-stride): rep[k] = the first k' <= k with
+// identical content.  Earlier blocks of equal hash are the candidates, tried
+// in ascending order; each exact comparison uses the whole CTA.
+constexpr int kDedupThreads = 256;
+__global__ void __launch_bounds__(kDedupThreads)
+dedup_kernel(DevMask m, const unsigned long long *counters, const int32_t *part_row, const int32_t *part_col,
+             const uint64_t *part_hash, int32_t *part_rep) {
+  __shared__ uint32_t s_ball[kDedupThreads / 32];
   const int64_t Ap = (int64_t)counters[1];
-  const int lane = threadIdx.x & 31;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t k = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; k < Ap; k += nwarps) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // band-only whole blocks: equal diagonal offsets (the "hash") mean equal content
+  const bool by_offset = m.qseg == nullptr && !m.ragged;
+  for (int64_t k = blockIdx.x; k < Ap; k += gridDim.x) {
     const uint64_t h = part_hash[k];
-    int64_t rep = k;
-    for (int64_t base = 0; base < k && rep == k; base += 32) {
-      const int64_t kp = base + lane;
-      unsigned cand = __ballot_sync(0xffffffffu, kp < k && part_hash[kp] == h);
-      if (cand && m.qseg == nullptr && !m.ragged) {
-        rep = base + __ffs(cand) - 1;  // equal diagonal offsets: equal content
-        break;
-      }
-      while (cand) {
-        const int t = __ffs(cand) - 1;
-        cand &= cand - 1u;
-        if (patterns_equal(m, part_row, part_col, k, base + t)) {
-          rep = base + t;
-          break;
+    int64_t rep = k;  // uniform over the CTA
+    for (int64_t base = 0; base < k && rep == k; base += kDedupThreads) {
+      const int64_t kp = base + tid;
+      const unsigned b = __ballot_sync(0xffffffffu, kp < k && part_hash[kp] == h);
+      if (lane == 0) s_ball[warp] = b;
+      __syncthreads();
+      for (int w = 0; w < kDedupThreads / 32 && rep == k; ++w) {
+        unsigned cand = s_ball[w];
+        while (cand && rep == k) {
+          const int64_t kc = base + 32 * w + (__ffs(cand) - 1);
+          cand &= cand - 1u;
+          if (by_offset || patterns_equal(m, part_row, part_col, k, kc)) rep = kc;
         }
       }
+      __syncthreads();  // s_ball is rewritten by the next chunk
     }
-    if (lane == 0) part_rep[k] = (int32_t)rep;
+    if (tid == 0) part_rep[k] = (int32_t)rep;
   }
 }
 
@@ -1060,7 +1076,7 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
       mi->mask_next, mi->bounds_start, mi->bounds_end, mi->part_row, mi->part_col, mi->part_g);
   partial_hash_kernel<<<sms * 4, bq, 0, stream>>>(m, mi->counters, mi->part_row, mi->part_col,
                                                   mi->part_hash);
-  dedup_kernel<<<sms * 4, 256, 0, stream>>>(m, mi->counters, mi->part_row, mi->part_col,
+  dedup_kernel<<<sms * 4, kDedupThreads, 0, stream>>>(m, mi->counters, mi->part_row, mi->part_col,
                                             mi->part_hash, mi->part_rep);
   scan_reps_kernel<<<1, 1024, 0, stream>>>(mi->counters, mi->part_rep, mi->part_pidx);
   finalize_kernel<<<sms * 4, 256, 0, stream>>>(mi->counters, mi->part_g, mi->part_rep,
