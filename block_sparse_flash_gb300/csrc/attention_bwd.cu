@@ -413,6 +413,12 @@ __device__ void bwd_mma(const BwdParams &p, uint32_t tmem, uint32_t s0, const Bw
 // before writing slot B only the just-committed piece 0: bwd_wait_slot
 // waits for all groups but the latest one when D = 128, for all of them
 // when there is a single piece per readout.
+// all but this thread's most recent bulk group have finished reading their
+// shared-memory source
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 template <int D>
 __device__ __forceinline__ void bwd_wait_slot() {
   if constexpr (D / 64 > 1)
