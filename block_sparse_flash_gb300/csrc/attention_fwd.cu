@@ -20,8 +20,16 @@
 //   * one persistent CTA per SM; each work item is (batch, two query heads,
 //     one q-block row); the two heads are two 128-row query tiles that share
 //     the row's active list, and share K/V tiles when they are in the same
-//     GQA group; items are sorted longest row first and dealt to the CTAs in
-//     serpentine order;
+//     GQA group.  With 256-row q-blocks an item is (batch, one head, one
+//     q-block row) and its tiles are the block's two halves, which share
+//     every K/V tile (the MHA analogue of the GQA pairing);
+//   * items are sorted longest row first and dealt to the CTAs in serpentine
+//     order; when rows span all keys and all heads' K/V exceeds what L2 can
+//     keep, the items are first grouped by heads whose K/V fits
+//     (choose_head_group);
+//   * K/V staging: rings of whole K and V tiles; at dqk = 192 with 256-row
+//     q-blocks one ring of 64-column chunks shared by K and V, released
+//     chunk by chunk;
 //   * warp roles (384 threads): warps 0-3 / 4-7 run the softmax of tile 0 /
 //     tile 1 (one thread per query row = one TMEM lane), warp 8 issues TMA
 //     loads; warp 9 (as a whole warp, one elected lane issuing) issues the
