@@ -170,6 +170,12 @@ class ClockSampler:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                                           "-i", str(self.device_index), "-lms", "50"], stdout=self.fh,
                                          stderr=subprocess.DEVNULL)
+            # the timed region starts only once sampling runs (nvidia-smi takes
+            # a few hundred ms to start; a short region would otherwise see at
+            # most the sample taken after it)
+            t0 = time.time()
+            while time.time() - t0 < 3.0 and self.proc.poll() is None and os.path.getsize(self.path) == 0:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
 
