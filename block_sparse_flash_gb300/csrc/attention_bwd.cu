@@ -22,8 +22,9 @@
 //
 // GB300 design:
 //   * kernels per call: the transposed table (column counts, scan, fill,
-//     pattern transpose), a prep kernel (D, dq accumulator cleared), the main
-//     kernel and a conversion of the fp32 dq accumulator to bf16;
+//     pattern transpose; only on the first call after each build of the
+//     MaskInfo, which keeps it), a prep kernel (D, dq accumulator cleared),
+//     the main kernel and a conversion of the fp32 dq accumulator to bf16;
 //   * main kernel: one persistent CTA per SM, items dealt longest column
 //     first in serpentine order; 384 threads; warps 0-7 (two
 //     warpgroups) do the elementwise work: a thread owns one key (TMEM lane)
@@ -943,9 +944,12 @@ splash_status splash_attention_bwd_launch(const void *q, const void *k, const vo
                                           int64_t Lq, int64_t Lk, int32_t d, splash_mask_info *mi, float scale,
                                           float softcap, void *dq, void *dk, void *dv, void *workspace,
                                           cudaStream_t stream, uint32_t *err_word) {
-  // the transposed table, owned by the MaskInfo (allocated on first use)
+  // the transposed table, owned by the MaskInfo (allocated on first use),
+  // made once per build of the table and reused by later calls
   const int64_t ncols = (int64_t)mi->batch_rows * mi->nk;
-  if (mi->t_cap_cols < ncols || mi->t_cap_active < mi->cap_blocks || mi->t_cap_patterns < mi->cap_patterns) {
+  const bool fresh = mi->t_gen != 0 && mi->t_gen == mi->build_gen && mi->t_ready != nullptr;
+  if (!fresh &&
+      (mi->t_cap_cols < ncols || mi->t_cap_active < mi->cap_blocks || mi->t_cap_patterns < mi->cap_patterns)) {
     splash_mask_info_free_transposed(mi);
     if (cudaMalloc(&mi->t_col_cnt, sizeof(int32_t) * ncols) != cudaSuccess ||
         cudaMalloc(&mi->t_col_ptr, sizeof(int32_t) * (ncols + 1)) != cudaSuccess ||
@@ -965,6 +969,10 @@ splash_status splash_attention_bwd_launch(const void *q, const void *k, const vo
   SPLASH_CUDA_TRY(cudaGetDevice(&dev));
   int sms = 148;
   SPLASH_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  if (fresh) {
+    // made by an earlier call, possibly on another stream
+    SPLASH_CUDA_TRY(cudaStreamWaitEvent(stream, mi->t_ready, 0));
+  } else {
   const unsigned cgrid = (unsigned)((ncols * 32 + 255) / 256);
   col_count_kernel<<<cgrid, 256, 0, stream>>>(mi->block_mask, (int32_t)mi->nq, (int32_t)mi->nk, ncols,
                                               mi->t_col_cnt);
@@ -978,6 +986,10 @@ splash_status splash_attention_bwd_launch(const void *q, const void *k, const vo
                                                mi->t_pattern_bits);
   SPLASH_CUDA_TRY(cudaGetLastError());
   splash_count_launches(4);
+  if (mi->t_ready == nullptr) SPLASH_CUDA_TRY(cudaEventCreateWithFlags(&mi->t_ready, cudaEventDisableTiming));
+  SPLASH_CUDA_TRY(cudaEventRecord(mi->t_ready, stream));
+  mi->t_gen = mi->build_gen;
+  }
 
   const int64_t rows = (int64_t)B * Hq * Lq;
   const int64_t Lq_pad = (Lq + 127) / 128 * 128, rows_pad = (int64_t)B * Hq * Lq_pad;

@@ -73,14 +73,20 @@ struct splash_mask_info {
   // capacities (elements)
   int64_t cap_rows = 0, cap_blocks = 0, cap_seg = 0, cap_patterns = 0, cap_hist = 0;
 
-  // --- column-major (transposed) table for the backward pass, rebuilt by
-  // each backward call; allocated on first use ---
+  // incremented by every build of the table
+  uint64_t build_gen = 0;
+
+  // --- column-major (transposed) table for the backward pass, made by the
+  // first backward call after each build and reused while build_gen is
+  // unchanged; allocated on first use ---
   int32_t *t_col_cnt = nullptr;       // [B_mask*nk]
   int32_t *t_col_ptr = nullptr;       // [B_mask*nk + 1]
   int32_t *t_col_rows = nullptr;      // [cap_blocks] q-block of each active block, by column
   int32_t *t_col_next = nullptr;      // [cap_blocks] its pattern index or -1
   uint32_t *t_pattern_bits = nullptr; // [cap_patterns][bk][bq/32], bit of (query, key) by key row
   int64_t t_cap_cols = 0, t_cap_active = 0, t_cap_patterns = 0;
+  uint64_t t_gen = 0;             // build_gen the copy was made from (0: none)
+  cudaEvent_t t_ready = nullptr;  // recorded on the stream that made it
 };
 
 // mask_info.cu

@@ -891,6 +891,7 @@ void splash_mask_info_free_transposed(splash_mask_info *mi) {
   mi->t_col_cnt = mi->t_col_ptr = mi->t_col_rows = mi->t_col_next = nullptr;
   mi->t_pattern_bits = nullptr;
   mi->t_cap_cols = mi->t_cap_active = mi->t_cap_patterns = 0;
+  mi->t_gen = 0;
 }
 
 void splash_mask_info_free_buffers(splash_mask_info *mi) {
@@ -906,6 +907,7 @@ void splash_mask_info_free_buffers(splash_mask_info *mi) {
   for (void *p : host)
     if (p) cudaFreeHost(p);
   if (mi->counts_ready) cudaEventDestroy(mi->counts_ready);
+  if (mi->t_ready) cudaEventDestroy(mi->t_ready);
   const int device = mi->device;
   *mi = splash_mask_info();
   mi->device = device;
@@ -918,6 +920,7 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
   const int32_t nbm = seg ? spec->batch : 1;
   const int64_t nq = (Lq + bq - 1) / bq, nk = (Lk + bk - 1) / bk, R = (int64_t)nbm * nq, NB = R * nk;
   const bool ragged = (Lq % bq) != 0 || (Lk % bk) != 0;
+  ++mi->build_gen;  // any column-major copy of the previous table is stale
 
   // -- buffers (reused when large enough) --
   splash_status st;

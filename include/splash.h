@@ -335,8 +335,10 @@ splash_status splash_attention_merge(const float *o_part, const float *lse_part,
  *   dq[b,h,i,:] = scale * sum over allowed j: dS_ij k[b,g,j,:]
  * (masked pairs contribute nothing; a key no query sees gets dk = dv = 0).
  * Only the MaskInfo's active blocks are computed, visited column by column:
- * the call rebuilds a column-major copy of the table inside the MaskInfo
- * (device memory it allocates on first use, hence the non-const handle).
+ * the first call after each build (or rebuild) of the MaskInfo makes a
+ * column-major copy of the table inside it (device memory allocated on
+ * first use, hence the non-const handle), and later calls reuse it; a call
+ * on another stream waits for the copy's completion.
  *
  *   q, k, v, mi, scale, softcap   exactly as given to the forward
  *   out  device bf16 [B][Hq][Lq][dv], lse device fp32 [B][Hq][Lq]: the forward's outputs

@@ -149,6 +149,35 @@ def test_dk_dv_are_deterministic_and_dq_nearly(bsf):
     mi.close()
 
 
+def test_column_table_follows_rebuilds(bsf):
+    # the backward keeps the MaskInfo's column-major copy between calls and
+    # must make a new one after the table is rebuilt with another mask
+    B, Hq, Hkv, L, d = 1, 2, 1, 640, 128
+    q = workloads.normal_bf16((B, Hq, L, d), 61)
+    k = workloads.normal_bf16((B, Hkv, L, d), 62)
+    v = workloads.normal_bf16((B, Hkv, L, d), 63)
+    g = workloads.normal_bf16((B, Hq, L, d), 64)
+    qd, kd, vd, gd = q.cuda(), k.cuda(), v.cuda(), g.cuda()
+    mi = bsf.build_mask_info(bsf.MaskSpec(True), L, L, 128, 128)
+    out, lse = bsf.attention_fwd(qd, kd, vd, mi, d ** -0.5)
+    first = bsf.attention_bwd(qd, kd, vd, out, lse, gd, mi, d ** -0.5)
+    again = bsf.attention_bwd(qd, kd, vd, out, lse, gd, mi, d ** -0.5)
+    torch.cuda.synchronize()
+    assert torch.equal(first[1], again[1]) and torch.equal(first[2], again[2])
+    for spec, ospec in ((bsf.MaskSpec(True, 199, -1), oracle.MaskSpec(True, 199, -1)),
+                        (bsf.MaskSpec(False, 100, 300), oracle.MaskSpec(False, 100, 300))):
+        mi.rebuild(spec, L, L, 128, 128)
+        out, lse = bsf.attention_fwd(qd, kd, vd, mi, d ** -0.5)
+        dq, dk, dv = bsf.attention_bwd(qd, kd, vd, out, lse, gd, mi, d ** -0.5)
+        torch.cuda.synchronize()
+        assert bsf.last_device_error() == 0
+        ref = oracle.attention_bwd(q, k, v, g, ospec, d ** -0.5, 0.0)
+        compare_grad(dq, ref["dq"], "dq after rebuild", d_term_allowance(q, k, v, g, ospec, d ** -0.5, 0.0))
+        compare_grad(dk, ref["dk"], "dk after rebuild")
+        compare_grad(dv, ref["dv"], "dv after rebuild")
+    mi.close()
+
+
 def test_backward_rejects_unsupported_shapes(bsf):
     q, k, v, g, mi, _ = make(bsf, 1, 2, 2, 256, 128)
     qd, kd, vd, gd = q.cuda(), k.cuda(), v.cuda(), g.cuda()
