@@ -176,3 +176,37 @@ def test_tall_rejected_with_64_key_blocks(bsf):
     with pytest.raises(bsf.SplashError):
         bsf.attention_fwd(q, q, q, mi, 0.125)
     mi.close()
+
+
+GROUPED = [
+    # label, B, Hq, Hkv, L, dqk, dv, bq: all heads' K / V exceeds 64 MB and the
+    # rows span the keys, so the items are ordered by head groups, the last
+    # group smaller than the others
+    ("40 heads MHA d192, 256-row blocks", 1, 40, 40, 4096, 192, 128, 256),
+    ("68 heads GQA (G=2) d128, head pairs", 1, 68, 34, 4096, 128, 128, 128),
+]
+
+
+@pytest.mark.parametrize("case", GROUPED, ids=[c[0] for c in GROUPED])
+def test_head_grouped_order_sampled_rows(bsf, case):
+    from tests.parity import gather_rows, sample_rows
+    label, B, Hq, Hkv, L, dqk, dv, bq = case
+    q = workloads.normal_bf16((B, Hq, L, dqk), 71)
+    k = workloads.normal_bf16((B, Hkv, L, dqk), 72)
+    v = workloads.normal_bf16((B, Hkv, L, dv), 73)
+    assert B * Hkv * L * (dqk + dv) * 2 > 64 << 20
+    mi = bsf.build_mask_info(bsf.MaskSpec(True), L, L, bq, 128)
+    scale = 1.0 / math.sqrt(dqk)
+    out, lse = bsf.attention_fwd(q.cuda(), k.cuda(), v.cuda(), mi, scale)
+    torch.cuda.synchronize()
+    assert bsf.last_device_error() == 0, label
+    nq = L // bq
+    # whole blocks of the first head, the last head (last, smaller group) and
+    # a head in between, plus random rows
+    extra = [(0, 0, nq - 1), (0, Hq - 1, 0), (0, Hq - 1, nq - 1), (0, Hq // 2, nq // 2)]
+    rows = sample_rows(B, Hq, L, bq, 256, 4242, extra)
+    O, Lref = oracle.attention(q, k, v, oracle.MaskSpec(True), scale, 0.0, rows=rows)
+    o, l = gather_rows(out, lse, rows)
+    compare_rows(o, l, O, Lref, label)
+    assert torch.isfinite(lse).all() and torch.isfinite(out.float()).all()
+    mi.close()
