@@ -139,6 +139,10 @@ struct FwdParams {
   float scale_log2;   // scale * log2(e)             (no soft cap)
   float cap_inner;    // scale / cap                 (soft cap)
   float cap_log2;     // cap * log2(e)               (soft cap)
+  // cap*log2(e) * tanh(s*scale/cap) by the series, as an odd polynomial in
+  // the raw score s: s * (scale_log2 + u (cap_c1 + u cap_c2)), u = s^2
+  float cap_c1;       // kTanhC1 * scale^3 * log2(e) / cap^2
+  float cap_c2;       // kTanhC2 * scale^5 * log2(e) / cap^4
   int32_t use_softcap;
   // Max Logit Estimate: every row's reference starts at this constant (log2
   // units, c * log2(e)) instead of its first allowed keys' maximum
@@ -907,6 +911,30 @@ __device__ __forceinline__ void run_mma_pair_chunked(const FwdParams &p, uint32_
   if (!mbar_wait_drain(bar.drain(), 0, tmo) && leader) atomicOr(p.err, SPLASH_DEV_TIMEOUT_DRAIN);
 }
 
+// A full soft-capped block's exponentials in one pass when the series holds
+// and the row's reference m is known: 2^(cap*log2(e)*tanh(s*scale/cap) - m)
+// with the series written as an odd polynomial in s (three packed FMA-pipe
+// operations per pair, the last one also subtracting m).  Returns the row
+// sum like exp2_block.
+template <int N>
+__device__ __forceinline__ float exp2_capped_series(float (&s)[N], const FwdParams &p, float m) {
+  const f32x2 c2{p.cap_c2, p.cap_c2}, c1{p.cap_c1, p.cap_c1}, ck{p.scale_log2, p.scale_log2}, nm{-m, -m};
+  f32x2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+  for (int j = 0; j < N; j += 2) {
+    const f32x2 x{s[j], s[j + 1]};
+    const f32x2 u = fmul2(x, x);
+    f32x2 q = ffma2(u, c2, c1);
+    q = ffma2(u, q, ck);
+    const f32x2 a = ffma2(x, q, nm);
+    s[j] = ex2_approx(a.x);
+    s[j + 1] = ex2_approx(a.y);
+    acc[(j >> 1) & 3] = fadd2(acc[(j >> 1) & 3], f32x2{s[j], s[j + 1]});
+  }
+  const f32x2 t = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+  return t.x + t.y;
+}
+
 // tanh(s*k) for two scores by the series (|s*k| <= 0.25), packed fp32x2:
 // a = s*k, then a + a*u*(c1 + c2*u) with u = a*a.
 __device__ __forceinline__ f32x2 tanh_series2(f32x2 s, f32x2 k) {
@@ -964,7 +992,10 @@ __device__ __forceinline__ float exp2_block(float (&s)[N], float mul, float sub)
 
 // BAND: partial blocks' masks computed from positions (a separate
 // instantiation, so that the default stored-pattern loop is unchanged).
-template <int DQK, int DV, int BK, bool BAND, bool TALL>
+// CAP: the tanh soft cap, a compile-time flag so that the kernels without
+// it carry none of its code (the fused cap + exponent loop changes their
+// register allocation).
+template <int DQK, int DV, int BK, bool BAND, bool TALL, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
 splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -1102,8 +1133,11 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         // Scores in log2 units are s*mul: mul = scale*log2e, or with the soft
         // cap s <- tanh(s*scale/cap) here and mul = cap*log2e (the exponent's
         // FFMA applies it).  Masked entries become -inf.
-        const float mul = p.use_softcap ? p.cap_log2 : p.scale_log2;
-        if (p.use_softcap) {
+        const float mul = CAP ? p.cap_log2 : p.scale_log2;
+        float alpha = 1.f;
+        float sum = 0.f;
+        bool fused = false;  // exponentials already taken by exp2_capped_series
+        if constexpr (CAP) {
           float am[4];
 #pragma unroll
           for (int x = 0; x < 4; ++x) am[x] = fmaxf(fabsf(s[2 * x]), fabsf(s[2 * x + 1]));
@@ -1113,6 +1147,10 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
           if (__any_sync(0xffffffffu, amax > kTanhSeriesLimit)) {
 #pragma unroll
             for (int j = 0; j < BK; ++j) s[j] = tanh_identity(s[j] * p.cap_inner);
+          } else if (!need_mask && !__any_sync(0xffffffffu, m_ref == -INFINITY)) {
+            // the steady state of a full block: the cap and the exponent in one pass
+            sum = exp2_capped_series<BK>(s, p, m_ref);
+            fused = true;
           } else {
             const f32x2 k2{p.cap_inner, p.cap_inner};
 #pragma unroll
@@ -1123,26 +1161,27 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             }
           }
         }
-        if (need_mask) {
+        if (!fused) {
+          if (need_mask) {
 #pragma unroll
-          for (int j = 0; j < BK; ++j) s[j] = ((bits[j >> 5] >> (j & 31)) & 1u) ? s[j] : -INFINITY;
-        }
-        // Exponentials against the row's running reference m_ref, which
-        // moves only (i) to the first allowed keys' maximum and (ii) when a
-        // block's sum of exponentials would reach 2^64 (then the block is
-        // recomputed against its own maximum): between those events the max
-        // is not needed at all.  P, l and O stay far from overflow (P < 2^64),
-        // and O / l is independent of the reference.
-        float alpha = 1.f;
-        if (__any_sync(0xffffffffu, m_ref == -INFINITY)) {
-          // a row's first block with allowed keys: its reference is their max
-          const float mx = max_tree<BK>(s) * mul;  // scale > 0
-          if (m_ref == -INFINITY && mx != -INFINITY) {
-            alpha = 0.f;
-            m_ref = mx;
+            for (int j = 0; j < BK; ++j) s[j] = ((bits[j >> 5] >> (j & 31)) & 1u) ? s[j] : -INFINITY;
           }
+          // Exponentials against the row's running reference m_ref, which
+          // moves only (i) to the first allowed keys' maximum and (ii) when a
+          // block's sum of exponentials would reach 2^64 (then the block is
+          // recomputed against its own maximum): between those events the max
+          // is not needed at all.  P, l and O stay far from overflow (P < 2^64),
+          // and O / l is independent of the reference.
+          if (__any_sync(0xffffffffu, m_ref == -INFINITY)) {
+            // a row's first block with allowed keys: its reference is their max
+            const float mx = max_tree<BK>(s) * mul;  // scale > 0
+            if (m_ref == -INFINITY && mx != -INFINITY) {
+              alpha = 0.f;
+              m_ref = mx;
+            }
+          }
+          sum = exp2_block<BK>(s, mul, m_ref == -INFINITY ? 0.f : m_ref);
         }
-        float sum = exp2_block<BK>(s, mul, m_ref == -INFINITY ? 0.f : m_ref);
         const bool redo = !(sum < kPMax);
         if (__any_sync(0xffffffffu, redo)) {
           // rare: exponentials above 2^64 for some lane.  The warp reloads S
@@ -1163,7 +1202,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
               for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(r[c][x]);
             }
           }
-          if (p.use_softcap) {
+          if constexpr (CAP) {
 #pragma unroll
             for (int j = 0; j < BK; ++j) s[j] = tanh_identity(s[j] * p.cap_inner);
           }
@@ -1443,7 +1482,7 @@ int32_t choose_head_group(bool dense_rows, int64_t items_per_head, int32_t npair
   return best;
 }
 
-template <int DQK, int DV, int BK, bool BAND, bool TALL>
+template <int DQK, int DV, int BK, bool BAND, bool TALL, bool CAP>
 splash_status launch(const void *q, const void *k, const void *v, const FwdParams &prm, cudaStream_t stream) {
   using C = Cfg<DQK, DV, BK>;
   CUtensorMap tq, tk, tv, to;
@@ -1460,7 +1499,7 @@ splash_status launch(const void *q, const void *k, const void *v, const FwdParam
   int sms = 148;
   SPLASH_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   if (configured_device != dev) {
-    SPLASH_CUDA_TRY(cudaFuncSetAttribute(splash_fwd_kernel<DQK, DV, BK, BAND, TALL>,
+    SPLASH_CUDA_TRY(cudaFuncSetAttribute(splash_fwd_kernel<DQK, DV, BK, BAND, TALL, CAP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
     configured_device = dev;
   }
@@ -1469,26 +1508,26 @@ splash_status launch(const void *q, const void *k, const void *v, const FwdParam
   FwdParams run = prm;
   run.head_group = choose_head_group(prm.dense_rows != 0, (int64_t)prm.nbm * prm.nq * (prm.nbm == 1 ? prm.B : 1) * prm.nsplit, prm.npairs,
                                      (int64_t)prm.B * prm.Hkv * prm.Lk * (DQK + DV) * 2, grid);
-  splash_fwd_kernel<DQK, DV, BK, BAND, TALL><<<(unsigned)grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, to, run);
+  splash_fwd_kernel<DQK, DV, BK, BAND, TALL, CAP><<<(unsigned)grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, to, run);
   SPLASH_CUDA_TRY(cudaGetLastError());
   splash_count_launches(1);
   return SPLASH_OK;
 }
 
-template <bool BAND>
+template <bool BAND, bool CAP>
 splash_status launch_shape(const void *q, const void *k, const void *v, const FwdParams &prm, int32_t dqk,
                            int32_t dv, int32_t bk, cudaStream_t stream) {
   if (prm.t1_off) {  // 256-row q-blocks: two halves of one head per item (bk = 128)
-    if (dqk == 128 && dv == 128 && bk == 128) return launch<128, 128, 128, BAND, true>(q, k, v, prm, stream);
-    if (dqk == 192 && dv == 128 && bk == 128) return launch<192, 128, 128, BAND, true>(q, k, v, prm, stream);
-    if (dqk == 64 && dv == 64 && bk == 128) return launch<64, 64, 128, BAND, true>(q, k, v, prm, stream);
+    if (dqk == 128 && dv == 128 && bk == 128) return launch<128, 128, 128, BAND, true, CAP>(q, k, v, prm, stream);
+    if (dqk == 192 && dv == 128 && bk == 128) return launch<192, 128, 128, BAND, true, CAP>(q, k, v, prm, stream);
+    if (dqk == 64 && dv == 64 && bk == 128) return launch<64, 64, 128, BAND, true, CAP>(q, k, v, prm, stream);
     return SPLASH_ERR_UNSUPPORTED;
   }
-  if (dqk == 128 && dv == 128 && bk == 128) return launch<128, 128, 128, BAND, false>(q, k, v, prm, stream);
-  if (dqk == 192 && dv == 128 && bk == 128) return launch<192, 128, 128, BAND, false>(q, k, v, prm, stream);
-  if (dqk == 64 && dv == 64 && bk == 64) return launch<64, 64, 64, BAND, false>(q, k, v, prm, stream);
-  if (dqk == 64 && dv == 64 && bk == 128) return launch<64, 64, 128, BAND, false>(q, k, v, prm, stream);
-  if (dqk == 128 && dv == 128 && bk == 64) return launch<128, 128, 64, BAND, false>(q, k, v, prm, stream);
+  if (dqk == 128 && dv == 128 && bk == 128) return launch<128, 128, 128, BAND, false, CAP>(q, k, v, prm, stream);
+  if (dqk == 192 && dv == 128 && bk == 128) return launch<192, 128, 128, BAND, false, CAP>(q, k, v, prm, stream);
+  if (dqk == 64 && dv == 64 && bk == 64) return launch<64, 64, 64, BAND, false, CAP>(q, k, v, prm, stream);
+  if (dqk == 64 && dv == 64 && bk == 128) return launch<64, 64, 128, BAND, false, CAP>(q, k, v, prm, stream);
+  if (dqk == 128 && dv == 128 && bk == 64) return launch<128, 128, 64, BAND, false, CAP>(q, k, v, prm, stream);
   return SPLASH_ERR_UNSUPPORTED;
 }
 
@@ -1546,13 +1585,22 @@ splash_status splash_attention_fwd_launch(const void *q, const void *k, const vo
   prm.dual_issuer = (prm.G == 1 && !prm.t1_off) ? 1 : 0;
   prm.cap_inner = softcap > 0.f ? scale / softcap : 0.f;
   prm.cap_log2 = softcap > 0.f ? softcap * kLog2e : 0.f;
+  {
+    const double sc = scale, cp = softcap > 0.f ? softcap : 1.0, l2e = 1.4426950408889634;
+    prm.cap_c1 = softcap > 0.f ? (float)(kTanhC1 * sc * sc * sc * l2e / (cp * cp)) : 0.f;
+    prm.cap_c2 = softcap > 0.f ? (float)(kTanhC2 * sc * sc * sc * sc * sc * l2e / (cp * cp * cp * cp)) : 0.f;
+  }
   prm.out = reinterpret_cast<__nv_bfloat16 *>(out);
   prm.lse = lse;
   prm.err = err_word;
   prm.timeout_ns = 1000000000ull;  // 1 s per wait
   const int bk = mi->bk;
-  if (prm.band_bits) return launch_shape<true>(q, k, v, prm, dqk, dv, bk, stream);
-  return launch_shape<false>(q, k, v, prm, dqk, dv, bk, stream);
+  if (prm.use_softcap) {
+    if (prm.band_bits) return launch_shape<true, true>(q, k, v, prm, dqk, dv, bk, stream);
+    return launch_shape<false, true>(q, k, v, prm, dqk, dv, bk, stream);
+  }
+  if (prm.band_bits) return launch_shape<true, false>(q, k, v, prm, dqk, dv, bk, stream);
+  return launch_shape<false, false>(q, k, v, prm, dqk, dv, bk, stream);
 }
 
 splash_status splash_wait_selftest_launch(uint64_t timeout_ns, cudaStream_t stream, uint32_t *err_word) {
