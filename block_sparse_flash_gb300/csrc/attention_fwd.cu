@@ -26,7 +26,7 @@
 //   * items are sorted longest row first and dealt to the CTAs in serpentine
 //     order; when rows span all keys and all heads' K/V exceeds what L2 can
 //     keep, the items are first grouped by heads whose K/V fits
-//     (choose_head_group);
+//     (splash_choose_head_group, csrc/api.cu);
 //   * K/V staging: rings of whole K and V tiles; at dqk = 192 with 256-row
 //     q-blocks one ring of 64-column chunks shared by K and V, released
 //     chunk by chunk;
@@ -53,7 +53,6 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
-#include <climits>
 #include <cmath>
 #include <mutex>
 
@@ -1450,38 +1449,6 @@ bool make_map_3d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t row
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Item order across heads.  The static schedule deals the items in rounds of
-// `grid` (one per CTA), rows longest first, every head (pair) of a row
-// together.  When rows reach across the keys (no window, no segments) and the
-// K / V of all heads is larger than L2 can keep (budget 64 MB, about half of
-// the 129 MB: each die has its own half), the CTAs of a round would stream it
-// from DRAM for every row.  Then the items are ordered
-// by groups of head_group heads whose K / V fits the budget, and among the
-// group sizes from half that bound up to it, the one whose group fills whole
-// rounds best (the fewest items left in a partial round; a group that ends
-// mid-round leaves that round unbalanced).  Measured on the wide-head causal
-// MHA workload (128 heads, K / V 335 MB): 19 heads per group (two whole
-// rounds of 152) 0.468 ms, 32 heads 0.489 ms, all 128 heads 0.556 ms.
-// (Windowed and document rows read short, overlapping key ranges; there the
-// row-major order already keeps the K / V in L2, and grouping was measured a
-// few per cent slower.)
-int32_t choose_head_group(bool dense_rows, int64_t items_per_head, int32_t npairs, int64_t kv_bytes, int64_t grid) {
-  constexpr int64_t kBudget = 64ll << 20;
-  if (!dense_rows || npairs <= 1 || kv_bytes <= kBudget) return npairs;
-  const int32_t cap = std::max<int32_t>(1, (int32_t)((int64_t)npairs * kBudget / kv_bytes));
-  int32_t best = cap;
-  int64_t best_rem = LLONG_MAX;
-  for (int32_t h = cap; h >= std::max<int32_t>(1, cap / 2); --h) {
-    const int64_t rem = (items_per_head * h) % grid;
-    if (rem < best_rem) {
-      best_rem = rem;
-      best = h;
-      if (rem == 0) break;
-    }
-  }
-  return best;
-}
-
 template <int DQK, int DV, int BK, bool BAND, bool TALL, bool CAP>
 splash_status launch(const void *q, const void *k, const void *v, const FwdParams &prm, cudaStream_t stream) {
   using C = Cfg<DQK, DV, BK>;
@@ -1506,8 +1473,9 @@ splash_status launch(const void *q, const void *k, const void *v, const FwdParam
   const int64_t grid = prm.num_items < sms ? prm.num_items : sms;
   if (grid <= 0) return SPLASH_OK;
   FwdParams run = prm;
-  run.head_group = choose_head_group(prm.dense_rows != 0, (int64_t)prm.nbm * prm.nq * (prm.nbm == 1 ? prm.B : 1) * prm.nsplit, prm.npairs,
-                                     (int64_t)prm.B * prm.Hkv * prm.Lk * (DQK + DV) * 2, grid);
+  const int64_t items_per_head = (int64_t)prm.nbm * prm.nq * (prm.nbm == 1 ? prm.B : 1) * prm.nsplit;
+  run.head_group = splash_choose_head_group(prm.dense_rows != 0, items_per_head, prm.npairs,
+                                            (int64_t)prm.B * prm.Hkv * prm.Lk * (DQK + DV) * 2, grid);
   splash_fwd_kernel<DQK, DV, BK, BAND, TALL, CAP><<<(unsigned)grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, to, run);
   SPLASH_CUDA_TRY(cudaGetLastError());
   splash_count_launches(1);
@@ -1555,7 +1523,7 @@ splash_status splash_attention_fwd_launch(const void *q, const void *k, const vo
   prm.nbm = mi->batch_rows;
   prm.t1_off = mi->bq == 256 ? 128 : 0;
   prm.npairs = prm.t1_off ? Hq : (Hq + 1) / 2;
-  prm.head_group = prm.npairs;  // chosen per launch (choose_head_group)
+  prm.head_group = prm.npairs;  // chosen per launch (splash_choose_head_group)
   prm.dense_rows = (!mi->has_segments && mi->window_left < 0 && mi->window_right < 0) ? 1 : 0;
   const int64_t rows = (int64_t)mi->batch_rows * mi->nq;
   prm.nsplit = nsplit > 1 ? nsplit : 1;

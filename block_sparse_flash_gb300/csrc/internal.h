@@ -95,6 +95,9 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
                                           cudaStream_t stream);
 void splash_mask_info_free_buffers(splash_mask_info *mi);
 void splash_mask_info_free_transposed(splash_mask_info *mi);
+// attention_fwd.cu: the forward's head-group choice (see splash_schedule_head_group)
+int32_t splash_choose_head_group(bool dense_rows, int64_t items_per_head, int32_t npairs, int64_t kv_bytes,
+                                 int64_t grid);
 // Makes the host totals current (waits for an asynchronous build's copy).
 splash_status splash_mask_info_sync_counts(splash_mask_info *mi);
 splash_status splash_classify_blocks_noalloc_impl(const splash_mask_spec *spec, int64_t Lq, int64_t Lk,

@@ -422,6 +422,28 @@ splash_status splash_debug_wait_selftest(uint64_t timeout_ns, void *cuda_stream)
  */
 uint64_t splash_kernel_launches(void);
 
+/*
+ * splash_schedule_head_group -- the forward's item order across heads, as
+ * the attention call chooses it (host logic, no device work): the number of
+ * heads (256-row q-blocks) or head pairs whose items are dealt together.
+ * The kernel deals its items in rounds of `grid` (one per CTA), rows longest
+ * first, all heads of a row together; when the rows reach across the keys
+ * (dense_rows: no window, no segment IDs) and the K / V of all heads
+ * (kv_bytes) exceeds 64 MB, the items are ordered by groups of heads whose
+ * K / V fits that budget, and among the group sizes from half the largest
+ * such size up to it, the one whose items (items_per_head per head) leave
+ * the fewest in a partial round.  Returns npairs when no grouping applies.
+ *   dense_rows      1 if the mask has neither a window nor segment IDs
+ *   items_per_head  work items per head (pair): q-block rows x batch x splits
+ *   npairs          heads (256-row q-blocks) or head pairs
+ *   kv_bytes        bytes of all heads' K and V
+ *   grid            CTAs of the launch (min(items, SMs))
+ * Invalid arguments (npairs < 1, items_per_head < 1, grid < 1, kv_bytes < 0)
+ * return 0.
+ */
+int32_t splash_schedule_head_group(int32_t dense_rows, int64_t items_per_head, int32_t npairs, int64_t kv_bytes,
+                                   int64_t grid);
+
 /* Static description of a status code (never NULL). */
 const char *splash_status_string(splash_status status);
 

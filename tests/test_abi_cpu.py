@@ -109,3 +109,36 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, splash):
     monkeypatch.setattr(splash, "LIB_PATH", "/nonexistent/libsplash.so")
     with pytest.raises(splash.SplashLibraryMissing):
         splash.lib()
+
+
+def test_head_group_schedule(splash):
+    """The forward's item order across heads (host logic, no device work)."""
+    f = splash.lib().splash_schedule_head_group
+    f.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64]
+    f.restype = ctypes.c_int32
+    MB = 1 << 20
+    # wide-head causal MHA, 256-row q-blocks: 128 heads, 16 rows each, K / V 335 MB,
+    # 152 CTAs -> 19 heads per group (two whole rounds)
+    assert f(1, 16, 128, 128 * 4096 * 320 * 2, 152) == 19
+    # dense causal GQA (33.5 MB of K / V) and anything that fits: no grouping
+    assert f(1, 64, 16, 2 * 8 * 4096 * 256 * 2, 152) == 16
+    assert f(1, 16, 128, 64 * MB, 152) == 128
+    # windows / segment IDs: rows read short key ranges, no grouping
+    assert f(0, 16, 128, 128 * 4096 * 320 * 2, 152) == 128
+    assert f(1, 16, 1, 1 << 40, 152) == 1
+    # invalid arguments
+    assert f(1, 0, 8, MB, 152) == 0 and f(1, 16, 0, MB, 152) == 0 and f(1, 16, 8, MB, 0) == 0
+    assert f(1, 16, 8, -1, 152) == 0
+    # in general: between half the L2-sized bound and the bound, and no size
+    # in that range leaves fewer items in a partial round
+    import random
+    rng = random.Random(7)
+    for _ in range(200):
+        npairs = rng.randint(2, 256)
+        items = rng.randint(1, 200)
+        grid = rng.choice([16, 132, 148, 152])
+        kv = rng.randint(65 * MB, 4000 * MB)
+        h = f(1, items, npairs, kv, grid)
+        cap = max(1, npairs * (64 * MB) // kv)
+        assert max(1, cap // 2) <= h <= cap
+        assert all((items * h) % grid <= (items * x) % grid for x in range(max(1, cap // 2), cap + 1))
