@@ -439,7 +439,9 @@ uint64_t splash_kernel_launches(void);
  *   kv_bytes        bytes of all heads' K and V
  *   grid            CTAs of the launch (min(items, SMs))
  * Invalid arguments (npairs < 1, items_per_head < 1, grid < 1, kv_bytes < 0)
- * return 0.
+ * return 0.  The pages have no counterpart (their grid is scheduled by the
+ * TPU compiler); this is the GB300 kernel's own work order, exposed so that
+ * it can be checked without a GPU.  Thread-safe, no side effects.
  */
 int32_t splash_schedule_head_group(int32_t dense_rows, int64_t items_per_head, int32_t npairs, int64_t kv_bytes,
                                    int64_t grid);
