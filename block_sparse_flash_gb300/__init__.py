@@ -228,6 +228,11 @@ class MaskInfo:
 
 
 def build_mask_info(spec: MaskSpec, Lq: int, Lk: int, bq: int, bk: int, stream=None) -> MaskInfo:
+    """The sparse execution table of `spec` on a (Lq, Lk) grid of bq x bk
+    blocks (splash_build_mask_info): bk in {64, 128}, bq in {64, 128, 256}.
+    The forward takes bq == bk, or bq = 256 with bk = 128 (each 256-row
+    q-block computed as two 128-row tiles of one head sharing every K/V tile,
+    the faster choice for MHA); the backward takes 128 x 128."""
     h = ctypes.c_void_p()
     s = spec._c()
     _check(lib().splash_build_mask_info(ctypes.byref(s), Lq, Lk, bq, bk, _stream(stream), ctypes.byref(h)),
