@@ -17,6 +17,7 @@ implementation) on the host cores, on bounded samples of the same workload.
 Prints one JSON line on rank 0.
 """
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -43,6 +44,16 @@ def parse_args(argv=None):
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the sparse workloads timed beside the headline one")
+    ap.add_argument("--sustain-s", type=float, default=2.0,
+                    help="seconds of back-to-back attention calls for the clock-normalised figures (0: skip)")
+    ap.add_argument("--shard", choices=["replicas", "heads"], default="replicas",
+                    help="N > 1: every rank runs the whole workload (replicas, weak scaling) or its own range "
+                         "of (batch, KV head) groups of one workload (heads, strong scaling)")
+    ap.add_argument("--gather", action="store_true",
+                    help="with --shard heads: gather every rank's O / LSE slice to rank 0 after timing and "
+                         "check that they tile the whole output")
     ap.add_argument("--splits", type=int, default=1,
                     help="split-KV forward with this many splits per row, then the LSE merge")
     ap.add_argument("--backward", action="store_true",
@@ -148,6 +159,33 @@ def reduce_max(value, world, device=None):
 def whole_job_throughput(flop_per_step_per_rank, world, ms_per_step_max):
     """Aggregate over ranks: every rank processes its own copy of the workload."""
     return world * flop_per_step_per_rank / (ms_per_step_max * 1e-3) / 1e12
+
+
+def sum_over_ranks(value, world, device=None):
+    """Sum of a float over ranks (identity for one rank)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def gather_shards(pieces, B, Hq, Hkv, Lq, dv):
+    """Assembles the ranks' (begin, end, out, lse) slices of (batch, KV head)
+    groups into out [B, Hq, Lq, dv] and lse [B, Hq, Lq] (host tensors), and a
+    coverage count per (batch, query head) that must be 1 everywhere."""
+    import torch
+    G = Hq // Hkv
+    out = torch.zeros((B, Hq, Lq, dv), dtype=pieces[0][2].dtype)
+    lse = torch.zeros((B, Hq, Lq), dtype=torch.float32)
+    cover = torch.zeros((B * Hkv, G), dtype=torch.int32)
+    for b0, b1, o, l in pieces:
+        out.view(B * Hkv, G, Lq, dv)[b0:b1] = o.reshape(b1 - b0, G, Lq, dv)
+        lse.view(B * Hkv, G, Lq)[b0:b1] = l.reshape(b1 - b0, G, Lq)
+        cover[b0:b1] += 1
+    return out, lse, cover.view(B, Hq)
 
 
 # --------------------------------------------------------------------- clocks
@@ -257,6 +295,123 @@ def cpu_baseline(w, inp, target_s=12.0):
                       f"{dt:.1f} s wall; useful FLOPs of those rows / time"}
 
 
+
+# --------------------------------------------------------------------- sparse workloads and sustained load
+# bf16 dense FLOPs one SM's tensor unit retires per clock: a 128x128x16 MMA
+# (65,536 FLOPs) executes in 64 cycles when the pipe is kept full (single-CTA
+# clock64 microbenchmark on this GPU).
+TENSOR_FLOP_PER_CLK_PER_SM = 2 * 128 * 128 * 16 / 64
+
+
+def tile_units(w, counts, batch_rows):
+    """Active (batch, query head, 128x128 tile) units of one forward pass."""
+    rep = w.Hq * (w.B if batch_rows == 1 else 1)
+    return counts["num_active"] * rep * (w.bq // 128 if w.bq >= 128 else 1) * (w.bk // 128 if w.bk >= 128 else 1)
+
+
+def time_forward_steps(bsf, w, inp, dev, K, warmup, flush):
+    """The headline step (MaskInfo rebuild + attention) on workload w, timed
+    like the headline: L2 flushed between steps outside the events.  Returns
+    (attention ms list, build ms list, counts, batch_rows)."""
+    import torch
+    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    seg = inp.segment_ids.to(dev) if inp.segment_ids is not None else None
+    spec = bsf.MaskSpec(w.causal, w.window_left, w.window_right, seg, seg)
+    mi = bsf.build_mask_info(spec, w.q_len, w.L, w.bq, w.bk)
+    counts, batch_rows = mi.counts(), mi.shape()["batch_rows"]
+    out = torch.empty((w.B, w.Hq, w.q_len, w.dv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Hq, w.q_len), dtype=torch.float32, device=dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for i in range(warmup + K):
+        flush.zero_()
+        e = ev[i - warmup] if i >= warmup else None
+        if e:
+            e[0].record()
+        mi.rebuild(spec, w.q_len, w.L, w.bq, w.bk)
+        if e:
+            e[1].record()
+        bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, out=out, lse=lse)
+        if e:
+            e[2].record()
+    torch.cuda.synchronize()
+    bsf.check_device_error()
+    mi.close()
+    attn = [e[1].elapsed_time(e[2]) for e in ev]
+    build = [e[0].elapsed_time(e[1]) for e in ev]
+    return attn, build, counts, batch_rows
+
+
+def per_workload(bsf, dev, K, warmup, flush, peak, indices=(3, 4, 5)):
+    """Attention time against active tile units on the sparse and wide-head
+    workloads, to show time proportional to the active blocks."""
+    import workloads
+    res = {}
+    for idx in indices:
+        w = workloads.workload(idx)
+        inp = workloads.make_inputs(w)
+        attn, build, counts, batch_rows = time_forward_steps(bsf, w, inp, dev, K, warmup, flush)
+        useful, executed = flop_counts(w, counts, batch_rows)
+        units = tile_units(w, counts, batch_rows)
+        p50 = percentiles(attn)[1]
+        res[f"workload{idx}"] = {
+            "workload": w.describe(), "attention_ms_p50": round(p50, 5),
+            "mask_build_ms_p50": round(percentiles(build)[1], 5),
+            "active_blocks": counts["num_active"], "active_tile_units": int(units),
+            "ns_per_unit": round(p50 * 1e6 / units, 3),
+            "ns_per_unit_d128_equiv": round(p50 * 1e6 / (executed / (2 * 128 * 128 * 256)), 3),
+            "executed_frac_of_burst": round(executed / (p50 * 1e-3) / 1e12 / peak, 4),
+            "useful_frac_of_burst": round(useful / (p50 * 1e-3) / 1e12 / peak, 4)}
+        del inp
+    return res
+
+
+def sustained_figures(bsf, w, q, k, v, mi, out, lse, dev, seconds, peaks, local):
+    """Back-to-back attention calls for `seconds` (no flush, no rebuild) with
+    the clock sampler running: executed TFLOP/s against the sustained cuBLAS
+    peak, the median SM clock of the samples, and the tensor fraction at that
+    clock (executed FLOPs / (time x clock x FLOP per clock per SM x SMs))."""
+    import torch
+    counts = mi.counts()
+    _, executed = flop_counts(w, counts, mi.shape()["batch_rows"])
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    # calls per chunk from one timed call
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, out=out, lse=lse)
+    b.record()
+    torch.cuda.synchronize()
+    per_chunk = max(1, int(50.0 / max(a.elapsed_time(b), 1e-3)))  # ~50 ms chunks
+    clocks = ClockSampler(local)
+    clocks.start()
+    chunks, calls, total_ms = [], 0, 0.0
+    t0 = time.time()
+    while time.time() - t0 < seconds:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(per_chunk):
+            bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, out=out, lse=lse)
+        b.record()
+        chunks.append((a, b))
+        calls += per_chunk
+        b.synchronize()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    bsf.check_device_error()
+    total_ms = sum(x.elapsed_time(y) for x, y in chunks)
+    tflops = executed * calls / (total_ms * 1e-3) / 1e12
+    res = {"seconds": round(total_ms * 1e-3, 3), "calls": calls, "ms_per_call": round(total_ms / calls, 5),
+           "executed_tflops": round(tflops, 2),
+           "peak_sustained": float(peaks.get("bf16_tflops_sustained", 1700.0)),
+           "frac_of_sustained": round(tflops / float(peaks.get("bf16_tflops_sustained", 1700.0)), 4),
+           "clocks": clk}
+    if clk.get("sm_mhz"):
+        clock_peak = clk["sm_mhz"] * 1e6 * TENSOR_FLOP_PER_CLK_PER_SM * sms / 1e12
+        res["tensor_peak_at_median_clock_tflops"] = round(clock_peak, 1)
+        res["clock_normalised_tensor_frac"] = round(tflops / clock_peak, 4)
+        res["clock_normalised_note"] = (f"{TENSOR_FLOP_PER_CLK_PER_SM:.0f} bf16 FLOP per clock per SM x {sms} SMs "
+                                        "x median SM clock of the samples")
+    return res
+
 # --------------------------------------------------------------------- our arm
 def run_ours(args):
     import torch
@@ -279,8 +434,20 @@ def run_ours(args):
         dist.barrier()
     bsf.lib()
 
-    w = bench_workload(args)
-    inp = workloads.make_inputs(w)
+    w_full = bench_workload(args)
+    inp_full = workloads.make_inputs(w_full)
+    w, inp, shard = w_full, inp_full, None
+    if args.shard == "heads":
+        # this rank's (batch, KV head) groups of the one workload, as a problem
+        # of (end - begin) batch rows with Hq / Hkv query heads and one KV head
+        if world > w_full.B * w_full.Hkv:
+            raise SystemExit("--shard heads needs at least one (batch, KV head) group per rank")
+        shard = bsf.shard_items(w_full.B, w_full.Hkv, world, rank)
+        sv = bsf.shard_views(inp_full.q, inp_full.k, inp_full.v, shard[0], shard[1],
+                             segment_ids=inp_full.segment_ids)
+        w = dataclasses.replace(w_full, B=shard[1] - shard[0], Hq=w_full.Hq // w_full.Hkv, Hkv=1)
+        inp = workloads.Inputs(sv["q"].contiguous(), sv["k"].contiguous(), sv["v"].contiguous(),
+                               sv.get("segment_ids"))
     q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
     seg = inp.segment_ids.to(dev) if inp.segment_ids is not None else None
     spec = bsf.MaskSpec(w.causal, w.window_left, w.window_right, seg, seg)
@@ -290,6 +457,9 @@ def run_ours(args):
     counts = mi.counts()
     batch_rows = mi.shape()["batch_rows"]
     useful, executed = flop_counts(w, counts, batch_rows)
+    # FLOPs of one step of the whole job: every rank's own copy (replicas), or
+    # the sum of the ranks' shares of one workload (heads)
+    job_useful = sum_over_ranks(useful, world, dev) if shard else world * useful
     out = torch.empty((w.B, w.Hq, w.q_len, w.dv), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.Hq, w.q_len), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -349,7 +519,7 @@ def run_ours(args):
     build_ms = [a[0].elapsed_time(b[0]) for a, b in zip(ev, ea)]  # step start -> attention start
     ms_step = reduce_max(statistics.mean(step_ms), world, dev)
     ms_attn = reduce_max(statistics.mean(attn_ms), world, dev)
-    value = whole_job_throughput(useful, world, ms_step)
+    value = job_useful / (ms_step * 1e-3) / 1e12
 
     peaks, peak_src = measured_peaks()
     peak = float(peaks["bf16_tflops"])
@@ -363,17 +533,20 @@ def run_ours(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(bsf, w, inp, spec, mi, dev, K=max(3, min(K, 20)), world=world, useful=useful,
+        e2e = run_e2e(bsf, w, inp, spec, mi, dev, K=max(3, min(K, 20)), world=world, job_useful=job_useful,
                       max_logit=args.max_logit)
 
     result = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "strong" if shard else "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, see workloads/)",
-        "config": {"workload": w.describe(), "step": "MaskInfo rebuild + attention forward",
+        "config": {"workload": w_full.describe(), "step": "MaskInfo rebuild + attention forward",
                    "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
                    "active_blocks": counts["num_active"], "partial_blocks": counts["num_partial"],
-                   "patterns": counts["num_patterns"], "parallelism": f"replicas x{world}"},
+                   "patterns": counts["num_patterns"],
+                   "parallelism": (f"(batch, KV head) groups split over {world} ranks" if shard
+                                   else f"replicas x{world}")},
         "attention_ms": round(ms_attn, 5),
         "mask_build_ms": round(ms_step - ms_attn, 5),
         "attention_ms_p10_p50_p90": [round(x, 5) for x in percentiles(attn_ms)],
@@ -402,8 +575,35 @@ def run_ours(args):
         result["config"]["pattern_source"] = args.pattern_source
     if e2e:
         result["e2e"] = e2e
+    if world == 1 and S == 1 and args.max_logit is None and args.sustain_s > 0:
+        result["sustained"] = sustained_figures(bsf, w, q, k, v, mi, out, lse, dev, args.sustain_s, peaks, local)
+    if world == 1 and not shard and args.workload == 2 and S == 1 and args.bq is None \
+            and args.max_logit is None and args.pattern_source == "stored" and not args.no_per_workload:
+        pw = per_workload(bsf, dev, K, args.warmup, flush, peak)
+        pw["workload2"] = {
+            "workload": w.describe(), "attention_ms_p50": round(percentiles(attn_ms)[1], 5),
+            "mask_build_ms_p50": round(percentiles(build_ms)[1], 5), "active_blocks": counts["num_active"],
+            "active_tile_units": int(tile_units(w, counts, batch_rows)),
+            "ns_per_unit": round(percentiles(attn_ms)[1] * 1e6 / tile_units(w, counts, batch_rows), 3),
+            "ns_per_unit_d128_equiv": round(percentiles(attn_ms)[1] * 1e6 / (executed / (2 * 128 * 128 * 256)), 3),
+            "executed_frac_of_burst": round(executed / (percentiles(attn_ms)[1] * 1e-3) / 1e12 / peak, 4),
+            "useful_frac_of_burst": round(useful / (percentiles(attn_ms)[1] * 1e-3) / 1e12 / peak, 4)}
+        result["per_workload"] = dict(sorted(pw.items()))
+        result["per_workload_note"] = ("same step, events and L2 flush as the headline; unit = one active "
+                                       "(batch, query head, 128x128 tile); d128_equiv divides by the executed "
+                                       "FLOPs of a d=128 tile (2*128*128*256)")
+    if shard:
+        result["config"]["rank0_groups"] = list(shard)
+        if args.gather and world > 1:
+            # host gather of every rank's slice (outside the timed region)
+            pieces = [None] * world
+            dist.all_gather_object(pieces, (shard[0], shard[1], out.cpu(), lse.cpu()))
+            full_out, full_lse, cover = gather_shards(pieces, w_full.B, w_full.Hq, w_full.Hkv, w_full.q_len,
+                                                      w_full.dv)
+            result["gather"] = {"tiles_exactly": bool((cover == 1).all()),
+                                "finite": bool(torch.isfinite(full_lse).all())}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w, inp)
+        result["cpu_baseline"] = cpu_baseline(w_full, inp_full)
     if rank == 0:
         print(json.dumps(result), flush=True)
     mi.close()
@@ -411,7 +611,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(bsf, w, inp, spec, mi, dev, K, world, useful, max_logit=None):
+def run_e2e(bsf, w, inp, spec, mi, dev, K, world, job_useful, max_logit=None):
     """Same metric through the public API with host buffers: pinned host ->
     device copies of the inputs, the step, device -> host copies of O and LSE,
     all inside the timed region (splash_attention_fwd_host, which pipelines
@@ -453,7 +653,7 @@ def run_e2e(bsf, w, inp, spec, mi, dev, K, world, useful, max_logit=None):
         if i >= 2:
             times.append(a.elapsed_time(b))
     ms = reduce_max(statistics.mean(times), world, dev)
-    return {"value": round(whole_job_throughput(useful, world, ms), 3), "unit": "TFLOP/s",
+    return {"value": round(job_useful / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 

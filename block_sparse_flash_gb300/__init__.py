@@ -93,12 +93,13 @@ def lib():
     L.splash_status_string.restype = ctypes.c_char_p
     L.splash_version.argtypes = []
     L.splash_version.restype = ctypes.c_char_p
+    L.splash_shard_items.argtypes = [i32, i32, i32, i32, P(i64), P(i64)]
     L.splash_kernel_launches.argtypes = []
     L.splash_kernel_launches.restype = ctypes.c_uint64
     for f in (L.splash_build_mask_info, L.splash_mask_info_rebuild, L.splash_mask_info_shape,
               L.splash_mask_info_counts, L.splash_mask_info_to_host, L.splash_attention_fwd,
               L.splash_attention_fwd_split, L.splash_attention_merge,
-              L.splash_last_device_error, L.splash_debug_wait_selftest):
+              L.splash_last_device_error, L.splash_debug_wait_selftest, L.splash_shard_items):
         f.restype = ctypes.c_int
     _lib = L
     return L
@@ -379,6 +380,38 @@ def attention_bwd_workspace_size(B: int, Hq: int, Lq: int, dqk: int) -> int:
     _check(lib().splash_attention_bwd_workspace_size(int(B), int(Hq), int(Lq), int(dqk), ctypes.byref(n)),
            "splash_attention_bwd_workspace_size")
     return int(n.value)
+
+
+def shard_items(B: int, Hkv: int, world: int, rank: int):
+    """This rank's half-open range [begin, end) of the B * Hkv (batch, KV
+    head) groups when a workload is split across `world` GPUs
+    (splash_shard_items)."""
+    b, e = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().splash_shard_items(int(B), int(Hkv), int(world), int(rank), ctypes.byref(b), ctypes.byref(e)),
+           "splash_shard_items")
+    return b.value, e.value
+
+
+def shard_views(q, k, v, begin: int, end: int, out=None, lse=None, segment_ids=None):
+    """Sub-tensors of groups [begin, end) as a problem of (end - begin) batch
+    rows, Hq / Hkv query heads and one KV head: views of q [B, Hq, L, dqk],
+    k, v, out and lse (no copy), and with segment IDs [B, L] a per-group copy
+    of the rows they read (row g // Hkv for group g).  Returns a dict with
+    the same keys."""
+    B, Hq, Lq, dqk = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    r = dict(q=q.view(B * Hkv, G, Lq, dqk)[begin:end],
+             k=k.view(B * Hkv, 1, k.shape[2], k.shape[3])[begin:end],
+             v=v.view(B * Hkv, 1, v.shape[2], v.shape[3])[begin:end])
+    if out is not None:
+        r["out"] = out.view(B * Hkv, G, Lq, out.shape[3])[begin:end]
+    if lse is not None:
+        r["lse"] = lse.view(B * Hkv, G, Lq)[begin:end]
+    if segment_ids is not None:
+        idx = torch.arange(begin, end, device=segment_ids.device) // Hkv
+        r["segment_ids"] = segment_ids.index_select(0, idx).contiguous()
+    return r
 
 
 def last_device_error(stream=None) -> int:

@@ -126,6 +126,17 @@ int32_t splash_schedule_head_group(int32_t dense_rows, int64_t items_per_head, i
   return splash_choose_head_group(dense_rows != 0, items_per_head, npairs, kv_bytes, grid);
 }
 
+splash_status splash_shard_items(int32_t B, int32_t Hkv, int32_t world, int32_t rank, int64_t *begin,
+                                int64_t *end) {
+  if (begin == nullptr || end == nullptr) return SPLASH_ERR_INVALID_ARG;
+  if (B <= 0 || Hkv <= 0 || world <= 0 || rank < 0 || rank >= world) return SPLASH_ERR_INVALID_ARG;
+  // balanced contiguous ranges: rank r takes [floor(n r / G), floor(n (r+1) / G))
+  const int64_t n = (int64_t)B * Hkv;
+  *begin = n * rank / world;
+  *end = n * (rank + 1) / world;
+  return SPLASH_OK;
+}
+
 splash_status splash_mask_info_rebuild(splash_mask_info *mi, const splash_mask_spec *spec, int64_t Lq,
                                        int64_t Lk, int32_t bq, int32_t bk, void *cuda_stream) {
   if (mi == nullptr) return SPLASH_ERR_INVALID_ARG;

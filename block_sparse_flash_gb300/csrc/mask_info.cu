@@ -27,6 +27,7 @@
 // pipeline as one single-CTA kernel (build_small_kernel).
 #include <algorithm>
 #include <climits>
+#include <mutex>
 
 #include "internal.h"
 
@@ -144,12 +145,14 @@ __global__ void seg_summary_kernel(DevMask m, int32_t *qsum, int32_t *kvsum) {
 constexpr int kClassifyThreads = 128;
 
 // Blocks the segment summaries cannot decide (both a shared and a differing
-// segment id possible) are either counted here element by element (deferred
-// == nullptr) or appended to `deferred` (block index row * nk + c, count in
-// counters[5]) for count_deferred_kernel, which counts each with a whole CTA.
+// segment id possible) are appended to `deferred` (block index row * nk + c;
+// counters[5] counts the appends) for count_deferred_kernel, which counts each
+// with a whole CTA.  Blocks beyond the list's capacity `defer_cap` (or all of
+// them, with deferred == nullptr) are counted here, element by element.
 __global__ void __launch_bounds__(kClassifyThreads)
 classify_kernel(DevMask m, const int32_t *qsum, const int32_t *kvsum, int8_t *block_mask,
-                int32_t *row_cnt, int32_t *row_pcnt, unsigned long long *counters, int32_t *deferred) {
+                int32_t *row_cnt, int32_t *row_pcnt, unsigned long long *counters, int32_t *deferred,
+                int64_t defer_cap) {
   const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t r = blockIdx.y;
   const int32_t bm = blockIdx.z;
@@ -188,21 +191,24 @@ classify_kernel(DevMask m, const int32_t *qsum, const int32_t *kvsum, int8_t *bl
       const int32_t kmn = kvsum[((int64_t)bm * m.nk + c) * 2], kmx = kvsum[((int64_t)bm * m.nk + c) * 2 + 1];
       if (qmx < kmn || kmx < qmn) {
         cnt = 0;  // no segment id in common
-      } else if (!(qmn == qmx && kmn == kmx && qmn == kmn) && deferred != nullptr) {
-        // undecided by the summaries: counted by count_deferred_kernel
-        const unsigned long long slot = atomicAdd(&counters[5], 1ull);
-        deferred[slot] = (int32_t)(row * m.nk + c);
-        cnt = -1;
       } else if (!(qmn == qmx && kmn == kmx && qmn == kmn)) {
-        // undecided by the summaries: count element by element
-        const int32_t *kv = m.kvseg + (int64_t)bm * m.Lk;
-        cnt = 0;
-        for (int32_t di = 0; di < m.bq; ++di) {
-          const int64_t i = r * m.bq + di;
-          const int32_t sq = q_segment(m, bm, i);
-          int64_t lo, hi;
-          band_range(m, i, c0, c1, lo, hi);
-          for (int64_t j = lo; j <= hi; ++j) cnt += (kv[j] == sq);
+        // undecided by the summaries: counted by count_deferred_kernel while
+        // the list has room, else here element by element
+        unsigned long long slot = ~0ull;
+        if (deferred != nullptr) slot = atomicAdd(&counters[5], 1ull);
+        if (slot < (unsigned long long)defer_cap) {
+          deferred[slot] = (int32_t)(row * m.nk + c);
+          cnt = -1;
+        } else {
+          const int32_t *kv = m.kvseg + (int64_t)bm * m.Lk;
+          cnt = 0;
+          for (int32_t di = 0; di < m.bq; ++di) {
+            const int64_t i = r * m.bq + di;
+            const int32_t sq = q_segment(m, bm, i);
+            int64_t lo, hi;
+            band_range(m, i, c0, c1, lo, hi);
+            for (int64_t j = lo; j <= hi; ++j) cnt += (kv[j] == sq);
+          }
         }
       }
       // (both constant and equal: the band count stands)
@@ -251,10 +257,10 @@ classify_kernel(DevMask m, const int32_t *qsum, const int32_t *kvsum, int8_t *bl
 // range with i's segment id; the block's class and its row / total counts are
 // then added like classify_kernel's.
 __global__ void __launch_bounds__(kClassifyThreads)
-count_deferred_kernel(DevMask m, const int32_t *deferred, int8_t *block_mask, int32_t *row_cnt, int32_t *row_pcnt,
-                      unsigned long long *counters) {
+count_deferred_kernel(DevMask m, const int32_t *deferred, int64_t defer_cap, int8_t *block_mask, int32_t *row_cnt,
+                      int32_t *row_pcnt, unsigned long long *counters) {
   __shared__ unsigned long long part[kClassifyThreads / 32];
-  const int64_t n = (int64_t)counters[5];
+  const int64_t n = min((int64_t)counters[5], defer_cap);
   const int di = threadIdx.x, lane = di & 31;
   for (int64_t x = blockIdx.x; x < n; x += gridDim.x) {
     const int64_t idx = deferred[x];
@@ -1064,12 +1070,13 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
   {
     dim3 grid((unsigned)((nk + kClassifyThreads - 1) / kClassifyThreads), (unsigned)nq, (unsigned)nbm);
     classify_kernel<<<grid, kClassifyThreads, 0, stream>>>(m, qsum, kvsum, mi->block_mask, mi->row_cnt,
-                                                          mi->row_pcnt, mi->counters, seg ? mi->rep_list : nullptr);
+                                                          mi->row_pcnt, mi->counters, seg ? mi->rep_list : nullptr,
+                                                          NB);
   }
   if (seg) {
     // the deferred list lives in rep_list, which finalize_kernel fills later
-    count_deferred_kernel<<<sms * 4, kClassifyThreads, 0, stream>>>(m, mi->rep_list, mi->block_mask, mi->row_cnt,
-                                                                   mi->row_pcnt, mi->counters);
+    count_deferred_kernel<<<sms * 4, kClassifyThreads, 0, stream>>>(m, mi->rep_list, NB, mi->block_mask,
+                                                                   mi->row_cnt, mi->row_pcnt, mi->counters);
   }
   scan_rows_kernel<<<1, 1024, 0, stream>>>(R, mi->row_cnt, mi->row_pcnt, mi->row_ptr, mi->prow_ptr,
                                            mi->counters);
@@ -1139,17 +1146,21 @@ splash_status splash_mask_info_sync_counts(splash_mask_info *mi) {
 // library holds it until the process exits.
 //
 // Limits: B_mask * nq <= kNoAllocMaxRows and B_mask * nk <= kNoAllocMaxCols.
-// All calls share the array (it keeps the last call's contents; the counters
+// Blocks that the segment summaries cannot decide are counted one CTA per
+// block while the fixed list has room (kNoAllocMaxDeferred), the rest one
+// thread per block.  All calls share the array (it keeps the last call's contents; the counters
 // are cleared at the start of every call), so calls that overlap on the GPU
 // -- on different streams, or from different host threads -- race.
 namespace {
 constexpr int64_t kNoAllocMaxRows = 16384;
 constexpr int64_t kNoAllocMaxCols = 16384;
+constexpr int64_t kNoAllocMaxDeferred = 65536;  // undecided blocks counted one CTA each
 struct NoAllocScratch {
   int32_t row_cnt[kNoAllocMaxRows];
   int32_t row_pcnt[kNoAllocMaxRows];
   int32_t qsum[2 * kNoAllocMaxRows];
   int32_t kvsum[2 * kNoAllocMaxCols];
+  int32_t deferred[kNoAllocMaxDeferred];
   unsigned long long counters[8];
   unsigned long long totals[4];
 };
@@ -1161,13 +1172,16 @@ namespace {
 
 constexpr int kMaxNoAllocDevices = 64;
 NoAllocScratch *g_noalloc_addr[kMaxNoAllocDevices];
+std::mutex g_noalloc_mu;
 
 // Device address of the scratch array on the current device; resolved once
-// per device (the first call on a device does it).
+// per device (the first call on a device does it), under a lock so that
+// host threads making their first calls at the same time are safe.
 splash_status noalloc_scratch(NoAllocScratch **out) {
   int dev = 0;
   SPLASH_CUDA_TRY(cudaGetDevice(&dev));
   if (dev < 0 || dev >= kMaxNoAllocDevices) return SPLASH_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (g_noalloc_addr[dev] == nullptr) {
     void *ptr = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
@@ -1254,11 +1268,19 @@ splash_status splash_classify_blocks_noalloc_impl(const splash_mask_spec *spec, 
   {
     dim3 grid((unsigned)((nk + kClassifyThreads - 1) / kClassifyThreads), (unsigned)nq, (unsigned)nbm);
     classify_kernel<<<grid, kClassifyThreads, 0, stream>>>(m, s->qsum, s->kvsum, block_mask, s->row_cnt,
-                                                          s->row_pcnt, s->counters, nullptr);
+                                                          s->row_pcnt, s->counters, seg ? s->deferred : nullptr,
+                                                          kNoAllocMaxDeferred);
+  }
+  if (seg) {
+    int dev = 0, sms = 148;
+    SPLASH_CUDA_TRY(cudaGetDevice(&dev));
+    SPLASH_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    count_deferred_kernel<<<sms * 4, kClassifyThreads, 0, stream>>>(m, s->deferred, kNoAllocMaxDeferred, block_mask,
+                                                                   s->row_cnt, s->row_pcnt, s->counters);
   }
   noalloc_totals_kernel<<<1, 256, 0, stream>>>(R, s);
   SPLASH_CUDA_TRY(cudaGetLastError());
-  splash_count_launches(seg ? 3 : 2);
+  splash_count_launches(seg ? 4 : 2);
   unsigned long long t[4];
   SPLASH_CUDA_TRY(cudaMemcpyAsync(t, s->totals, sizeof t, cudaMemcpyDeviceToHost, stream));
   SPLASH_CUDA_TRY(cudaStreamSynchronize(stream));

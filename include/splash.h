@@ -375,10 +375,13 @@ splash_status splash_attention_bwd(const void *q, const void *k, const void *v, 
  * or break the pool's accounting.
  *
  * It runs the same classification as splash_build_mask_info, but its working
- * memory (per-row counters, segment summaries, totals) is a fixed array inside
- * the library's module, present on every GPU that loads the library until the
+ * memory (per-row counters, segment summaries, the list of blocks the
+ * summaries cannot decide, totals; about 640 KiB) is a fixed array inside the
+ * library's module, present on every GPU that loads the library until the
  * process exits.  The first call on a device looks that array up (once per
- * device), so make the first call on each device before any stream capture.
+ * device, under a lock).  Every call ends by copying the totals to the host
+ * and synchronising `cuda_stream`, so it cannot be called while that stream
+ * is being captured into a CUDA graph.
  *
  *   spec, Lq, Lk, bq, bk  as for splash_build_mask_info.
  *   block_mask  device int8 [B_mask][nq][nk], caller-allocated: 0 empty,
@@ -387,10 +390,10 @@ splash_status splash_attention_bwd(const void *q, const void *k, const void *v, 
  *               (query, key) pairs, and the largest active-block count of a
  *               q-block row.
  * Limits: B_mask * nq <= 16384 and B_mask * nk <= 16384; larger masks return
- * SPLASH_ERR_UNSUPPORTED.  The call waits on `cuda_stream` for the totals.
- * All calls share the one array (its counters are cleared at the start of each
- * call), so calls that overlap on the GPU -- other streams or other host
- * threads -- race and must be serialised by the caller.
+ * SPLASH_ERR_UNSUPPORTED before any launch.  All calls share the one array
+ * (its counters are cleared at the start of each call), so calls that
+ * overlap on the GPU -- other streams or other host threads -- race and must
+ * be serialised by the caller.
  */
 splash_status splash_classify_blocks_noalloc(const splash_mask_spec *spec, int64_t Lq, int64_t Lk,
                                              int32_t bq, int32_t bk, int8_t *block_mask,
@@ -421,6 +424,30 @@ splash_status splash_debug_wait_selftest(uint64_t timeout_ns, void *cuda_stream)
  * thread-safe; for accounting in benchmarks.
  */
 uint64_t splash_kernel_launches(void);
+
+/*
+ * splash_shard_items -- the share of one rank when a workload is split
+ * across `world` GPUs by (batch, KV head) groups (host logic, no device
+ * work).  "Pallas Kernels and Splash Attention" §5.2: heads are independent,
+ * and the query heads of a GQA group read the same K / V, so a group is
+ * never split: the n = B * Hkv groups, in (batch, KV head) row-major order,
+ * are dealt in balanced contiguous ranges, rank r taking groups
+ * [floor(n r / world), floor(n (r + 1) / world)).  Group g covers batch
+ * g / Hkv and query heads (g % Hkv) * (Hq / Hkv) ... + Hq / Hkv - 1, which
+ * in the [B][H][L][d] layouts of q, k, v, out and lse is one contiguous
+ * range of memory per tensor, so a rank passes sub-tensors of the caller's
+ * tensors as a problem of (end - begin) batch rows with Hq / Hkv query heads
+ * and one KV head (with segment IDs, row g / Hkv of the segment array for
+ * each group).  The ranges of ranks 0 .. world-1 tile [0, n) with no gap or
+ * overlap; a rank may get an empty range when world > n.
+ *   B, Hkv        batch size and KV heads of the whole workload (> 0)
+ *   world, rank   number of ranks (> 0) and this rank (0 <= rank < world)
+ *   begin, end    out: this rank's half-open range of groups
+ * Errors: SPLASH_ERR_INVALID_ARG for null outputs or values out of range.
+ * Thread-safe, no side effects.
+ */
+splash_status splash_shard_items(int32_t B, int32_t Hkv, int32_t world, int32_t rank, int64_t *begin,
+                                 int64_t *end);
 
 /*
  * splash_schedule_head_group -- the forward's item order across heads, as

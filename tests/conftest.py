@@ -15,6 +15,18 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "slow: long-running CPU test")
 
 
+def pytest_terminal_summary(terminalreporter):
+    """Prints the error margins that the full-size parity checks recorded."""
+    mod = sys.modules.get("tests.parity")
+    margins = getattr(mod, "MARGINS", None) if mod else None
+    if not margins:
+        return
+    terminalreporter.write_line("parity margins vs the f64 oracle (limits: O abs 2e-2, O row rel 2e-2, LSE abs 1e-3):")
+    for label, m in margins.items():
+        terminalreporter.write_line(f"  {label}: rows={m['rows']} o_max_abs={m['o_max_abs']:.3e} "
+                                    f"o_row_rel={m['o_row_rel']:.3e} lse_max_abs={m['lse_max_abs']:.3e}")
+
+
 def read_golden(name):
     """Parses a `key = value` fixture under tests/golden (lines starting with #
     are the citation)."""

@@ -14,6 +14,10 @@ O_ABS_TOL = 2e-2
 O_REL_TOL = 2e-2
 LSE_ABS_TOL = 1e-3
 
+# Error triples of the full-size workload checks, by label, printed in the
+# test session's summary so that a run's record shows the margins.
+MARGINS = {}
+
 
 def oracle_spec(w_or_spec_kwargs, seg=None):
     import oracle

@@ -142,3 +142,19 @@ def test_head_group_schedule(splash):
         cap = max(1, npairs * (64 * MB) // kv)
         assert max(1, cap // 2) <= h <= cap
         assert all((items * h) % grid <= (items * x) % grid for x in range(max(1, cap // 2), cap + 1))
+
+
+def test_shard_items_tile_the_groups(splash):
+    for B, Hkv in ((1, 1), (2, 8), (1, 7), (3, 5), (5, 3)):
+        n = B * Hkv
+        for world in (1, 2, 3, 4, 8, 9):
+            ranges = [splash.shard_items(B, Hkv, world, r) for r in range(world)]
+            assert ranges[0][0] == 0 and ranges[-1][1] == n
+            assert all(ranges[r][1] == ranges[r + 1][0] for r in range(world - 1))
+            sizes = [e - b for b, e in ranges]
+            assert max(sizes) - min(sizes) <= 1 and min(sizes) >= 0
+    lib = splash.lib()
+    b, e = ctypes.c_int64(), ctypes.c_int64()
+    for args in ((0, 1, 1, 0), (1, 0, 1, 0), (1, 1, 0, 0), (1, 1, 2, 2), (1, 1, 2, -1)):
+        assert lib.splash_shard_items(*args, ctypes.byref(b), ctypes.byref(e)) == 1
+    assert lib.splash_shard_items(1, 1, 1, 0, None, ctypes.byref(e)) == 1

@@ -32,7 +32,8 @@ def noalloc(bsf, spec, Lq, Lk, bq, bk):
                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     f.restype = ctypes.c_int
     rows = 1 if spec.q_segment_ids is None else spec.q_segment_ids.shape[0]
-    block_mask = torch.full((rows, Lq // bq, Lk // bk), -1, dtype=torch.int8, device="cuda")
+    # ragged lengths are padded to whole blocks
+    block_mask = torch.full((rows, -(-Lq // bq), -(-Lk // bk)), -1, dtype=torch.int8, device="cuda")
     totals = np.zeros(4, dtype=np.int64)
     s = spec._c()
     status = f(ctypes.byref(s), Lq, Lk, bq, bk, ctypes.c_void_p(block_mask.data_ptr()),
@@ -64,6 +65,23 @@ def test_noalloc_matches_regular_build_on_consecutive_calls(bsf):
         assert got_tot.tolist() == ref_tot
 
 
+def test_noalloc_ragged_segments_and_tall_query_blocks(bsf):
+    # ragged lengths (padded grid) with document segments, then 256-row
+    # q-blocks under a plain causal mask, back to back
+    lens = workloads.document_lengths(8000, 4343, mean=500, lo=64, hi=2000, batch_rows=2)
+    seg = workloads.segment_ids_from_lengths(lens).cuda()
+    cases = [
+        (bsf.MaskSpec(True, -1, -1, seg, seg), 8000, 8000, 128, 128),
+        (bsf.MaskSpec(True), 4096, 4096, 256, 128),
+        (bsf.MaskSpec(True, 700, 0, seg, seg), 8000, 8000, 64, 64),
+    ]
+    for spec, Lq, Lk, bq, bk in cases:
+        got_mask, got_tot = noalloc(bsf, spec, Lq, Lk, bq, bk)
+        ref_mask, ref_tot = regular(bsf, spec, Lq, Lk, bq, bk)
+        np.testing.assert_array_equal(got_mask, ref_mask)
+        assert got_tot.tolist() == ref_tot
+
+
 def test_noalloc_rejects_masks_beyond_its_limit(bsf):
     lib = bsf.lib()
     f = lib.splash_classify_blocks_noalloc
@@ -75,5 +93,24 @@ def test_noalloc_rejects_masks_beyond_its_limit(bsf):
     L = 64 * 16385  # 16385 q-blocks of 64: one more than the scratch holds
     dummy = torch.empty(1, dtype=torch.int8, device="cuda")
     status = f(ctypes.byref(s), L, L, 64, 64, ctypes.c_void_p(dummy.data_ptr()),
+               ctypes.c_void_p(totals.ctypes.data), ctypes.c_void_p(0))
+    assert status == 3  # SPLASH_ERR_UNSUPPORTED, before any launch
+
+
+def test_noalloc_rejects_too_many_key_blocks(bsf):
+    # two batch rows of 8193 key blocks: 16386 columns against a limit of
+    # 16384, with a single q-block row
+    lib = bsf.lib()
+    f = lib.splash_classify_blocks_noalloc
+    f.argtypes = [ctypes.POINTER(bsf._Spec), ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    Lq, Lk = 64, 64 * 8193
+    sq = torch.zeros((2, Lq), dtype=torch.int32, device="cuda")
+    skv = torch.zeros((2, Lk), dtype=torch.int32, device="cuda")
+    s = bsf.MaskSpec(False, -1, -1, sq, skv)._c()
+    totals = np.zeros(4, dtype=np.int64)
+    dummy = torch.empty(1, dtype=torch.int8, device="cuda")
+    status = f(ctypes.byref(s), Lq, Lk, 64, 64, ctypes.c_void_p(dummy.data_ptr()),
                ctypes.c_void_p(totals.ctypes.data), ctypes.c_void_p(0))
     assert status == 3  # SPLASH_ERR_UNSUPPORTED, before any launch
