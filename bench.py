@@ -129,14 +129,13 @@ def mask_info_rate(w, counts, shape, build_ms, peaks):
     """The MaskInfo build against HBM: algorithmic bytes = segment IDs read
     (4 (Lq + Lk) per table batch row, with segment IDs), block_mask (1 byte
     per block), row_ptr (4 (R + 1)), the active lists (3 int32 + 2 flag bytes
-    per active block) and the patterns (bq*bk bytes plus their bit-packed
-    copy) written; divided by the median build time."""
+    per active block) and the bit-packed patterns (bq*bk/8 bytes each)
+    written; divided by the median build time."""
     R = shape["batch_rows"] * shape["nq"]
     nk = shape["nk"]
     seg = 4 * (w.q_len + w.L) * shape["batch_rows"] if w.documents else 0
     P = counts["num_patterns"]
-    nbytes = (seg + R * nk + 4 * (R + 1) + counts["num_active"] * (3 * 4 + 2) + P * w.bq * w.bk
-              + P * w.bq * w.bk // 8)
+    nbytes = seg + R * nk + 4 * (R + 1) + counts["num_active"] * (3 * 4 + 2) + P * w.bq * w.bk // 8
     med = percentiles(build_ms)[1]
     hbm = float(peaks.get("hbm_gbs", 6800.0))
     gbs = nbytes / (med * 1e-3) / 1e9

@@ -9,6 +9,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include "internal.h"
 
@@ -223,9 +224,15 @@ splash_status splash_mask_info_to_host(const splash_mask_info *mi, int8_t *block
     if (bounds_start) SPLASH_CUDA_TRY(cudaMemcpy(bounds_start, mi->bounds_start, A, cudaMemcpyDeviceToHost));
     if (bounds_end) SPLASH_CUDA_TRY(cudaMemcpy(bounds_end, mi->bounds_end, A, cudaMemcpyDeviceToHost));
   }
-  if (P > 0 && partial_mask_blocks)
-    SPLASH_CUDA_TRY(cudaMemcpy(partial_mask_blocks, mi->patterns, (size_t)P * mi->bq * mi->bk,
-                               cudaMemcpyDeviceToHost));
+  if (P > 0 && partial_mask_blocks) {
+    // the device keeps the patterns bit-packed; expand them to one byte per element
+    const int64_t words = mi->bk / 32, per = (int64_t)mi->bq * words;
+    std::vector<uint32_t> bits((size_t)(P * per));
+    SPLASH_CUDA_TRY(cudaMemcpy(bits.data(), mi->pattern_bits, bits.size() * sizeof(uint32_t), cudaMemcpyDeviceToHost));
+    for (int64_t x = 0; x < P * mi->bq; ++x)
+      for (int64_t j = 0; j < mi->bk; ++j)
+        partial_mask_blocks[x * mi->bk + j] = (uint8_t)((bits[(size_t)(x * words + j / 32)] >> (j % 32)) & 1u);
+  }
   return SPLASH_OK;
 }
 

@@ -45,8 +45,9 @@ struct splash_mask_info {
   int32_t *mask_next = nullptr;    // [cap_active]
   uint8_t *bounds_start = nullptr; // [cap_active]
   uint8_t *bounds_end = nullptr;   // [cap_active]
-  uint8_t *patterns = nullptr;     // [cap_patterns][bq][bk]
   // --- derived arrays used by the attention kernel ---
+  // the partial patterns, bit-packed (partial_mask_blocks in byte form is
+  // expanded from these when the table is copied to the host)
   uint32_t *pattern_bits = nullptr;  // [cap_patterns][bq][bk/32], bit dj of word dj/32 = allowed
   int32_t *row_order = nullptr;      // [R] rows by descending active count (longest first)
   // --- build scratch ---
@@ -65,8 +66,8 @@ struct splash_mask_info {
   unsigned long long *counters = nullptr;  // [8]: A, A_p, P, allowed, max_row, deferred blocks
   // host staging
   unsigned long long *h_counters = nullptr;  // pinned [8]
-  // counts of an asynchronous build: h_counters is valid once `counts_ready`
-  // (recorded after its copy) has completed
+  // counts of an asynchronous build: `counts_ready` is recorded after its last
+  // kernel; splash_mask_info_sync_counts waits for it and copies the totals
   cudaEvent_t counts_ready = nullptr;
   bool counts_pending = false;
 

@@ -7,24 +7,28 @@
 //         partial patterns and mask_next, bounds_start / bounds_end;
 //   §6.4  segment IDs (q_id == kv_id) joined with causal / local by AND.
 //
-// Pipeline (all kernels on the caller's stream, one host wait):
-//   K1 seg_summary   per q-block / kv-block min and max segment id
+// Pipeline (all kernels on the caller's stream):
+//   K1 seg_summary   per q-block / kv-block min and max segment id (and the
+//                    counters cleared)
 //   K2 classify      exact allowed-element count of every block -> class,
-//                    per-row active / partial counts, allowed pairs
-//   K3 scan_rows     row_ptr (CSR) and partial offsets
+//                    per-row active / partial counts, allowed pairs; blocks
+//                    the summaries cannot decide go to count_deferred (one
+//                    CTA per block, the key block's IDs staged in shared memory)
+//   K3 scan_order    row_ptr (CSR), partial offsets, and the rows by
+//                    descending active count (the attention's work order)
 //      compact       active lists in row-major, kv-ascending order, bounds
 //   K4 partial_hash  a content hash of each partial block's element pattern
 //      dedup         first partial with identical content (hash prefilter,
 //                    exact word-by-word comparison)
-//      scan_reps     pattern index of each first occurrence
-//      finalize      mask_next
-//      row_order     rows by descending active count (work order of the
-//                    attention kernel)
-//      (host wait: read A, A_p, P)
-//      materialize   partial_mask_blocks (bytes) and their bit-packed copy
-// Band-only masks (no segment IDs) take the classes in closed form, need no
-// host wait (the pattern count has a bound), and small tables run the whole
-// pipeline as one single-CTA kernel (build_small_kernel).
+//      scan_finalize pattern index of each first occurrence, mask_next
+//      materialize   the patterns, bit-packed (the byte form of
+//                    partial_mask_blocks is expanded on the host when the
+//                    table is copied there)
+// The pattern buffer is sized from a bound known before the build (no host
+// wait) unless that bound exceeds kPatternBudgetBytes; then the build waits
+// once for the exact pattern count.  Band-only masks (no segment IDs) take
+// the classes in closed form, and small tables run the whole pipeline as one
+// single-CTA kernel (build_small_kernel).
 #include <algorithm>
 #include <climits>
 #include <mutex>
@@ -111,13 +115,41 @@ __device__ __forceinline__ int64_t band_row_count(const DevMask &m, int64_t A, i
   return max((int64_t)0, min(m.Lk - 1, i + A) - max((int64_t)0, i - W) + 1);
 }
 
+// Segment IDs of key block c of batch row bm, staged in shared memory by the
+// whole CTA (keys past Lk are never read: band_range clips them).
+__device__ __forceinline__ void stage_kv_ids(const DevMask &m, int32_t bm, int64_t c, int32_t *s_kv) {
+  for (int32_t t = threadIdx.x; t < m.bk; t += blockDim.x) {
+    const int64_t j = c * m.bk + t;
+    s_kv[t] = j < m.Lk ? m.kvseg[(int64_t)bm * m.Lk + j] : 0;
+  }
+}
+
+// row_word with the key block's segment IDs staged in shared memory (its
+// first key is c0): 32 mask bits of query i (segment id sq) against keys
+// j0 .. j0+31.
+__device__ __forceinline__ uint32_t row_word_staged(const DevMask &m, int64_t i, int32_t sq, int64_t c0, int64_t j0,
+                                                    const int32_t *s_kv) {
+  int64_t lo, hi;
+  band_range(m, i, j0, j0 + 31, lo, hi);
+  uint32_t bits = 0u;
+  for (int64_t j = lo; j <= hi; ++j) bits |= (uint32_t)(s_kv[j - c0] == sq) << (j - j0);
+  return bits;
+}
+
 // ---------------------------------------------------------------- K1
-__global__ void seg_summary_kernel(DevMask m, int32_t *qsum, int32_t *kvsum) {
+// Also clears the per-row counters and the totals that classify_kernel adds to.
+__global__ void seg_summary_kernel(DevMask m, int32_t *qsum, int32_t *kvsum, int32_t *row_cnt, int32_t *row_pcnt,
+                                   unsigned long long *counters) {
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int32_t bm = blockIdx.y;
+  if (blockIdx.x == 0 && bm == 0 && threadIdx.x < 8) counters[threadIdx.x] = 0ull;
   if (warp >= m.nq + m.nk) return;
   const bool isq = warp < m.nq;
+  if (isq && lane == 0) {
+    row_cnt[(int64_t)bm * m.nq + warp] = 0;
+    row_pcnt[(int64_t)bm * m.nq + warp] = 0;
+  }
   const int64_t blk = isq ? warp : warp - m.nq;
   // the last block of a ragged sequence holds fewer positions
   const int32_t n = (int32_t)(isq ? min((int64_t)m.bq, m.Lq - blk * m.bq) : min((int64_t)m.bk, m.Lk - blk * m.bk));
@@ -260,6 +292,7 @@ __global__ void __launch_bounds__(kClassifyThreads)
 count_deferred_kernel(DevMask m, const int32_t *deferred, int64_t defer_cap, int8_t *block_mask, int32_t *row_cnt,
                       int32_t *row_pcnt, unsigned long long *counters) {
   __shared__ unsigned long long part[kClassifyThreads / 32];
+  __shared__ int32_t s_kv[128];  // the block's key segment IDs (bk <= 128)
   const int64_t n = min((int64_t)counters[5], defer_cap);
   const int di = threadIdx.x, lane = di & 31;
   for (int64_t x = blockIdx.x; x < n; x += gridDim.x) {
@@ -267,6 +300,8 @@ count_deferred_kernel(DevMask m, const int32_t *deferred, int64_t defer_cap, int
     const int64_t row = idx / m.nk, c = idx - row * m.nk;
     const int32_t bm = (int32_t)(row / m.nq);
     const int64_t r = row - (int64_t)bm * m.nq;
+    stage_kv_ids(m, bm, c, s_kv);
+    __syncthreads();
     unsigned long long cnt = 0;
     for (int32_t d = di; d < m.bq; d += kClassifyThreads) {
       const int64_t i = r * m.bq + d;
@@ -274,8 +309,7 @@ count_deferred_kernel(DevMask m, const int32_t *deferred, int64_t defer_cap, int
       band_range(m, i, c * m.bk, c * m.bk + m.bk - 1, lo, hi);
       if (hi >= lo) {
         const int32_t sq = q_segment(m, bm, i);
-        const int32_t *kv = m.kvseg + (int64_t)bm * m.Lk;
-        for (int64_t j = lo; j <= hi; ++j) cnt += (kv[j] == sq);
+        for (int64_t j = lo; j <= hi; ++j) cnt += (s_kv[j - c * m.bk] == sq);
       }
     }
     for (int off = 16; off; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
@@ -325,9 +359,39 @@ __device__ __forceinline__ int block_excl_scan(int x, int &total, int *warp_buf)
   return ex;
 }
 
-__global__ void __launch_bounds__(1024)
-scan_rows_kernel(int64_t R, const int32_t *row_cnt, const int32_t *row_pcnt, int32_t *row_ptr,
-                 int32_t *prow_ptr, unsigned long long *counters) {
+// Exclusive prefix within the CTA of 64-bit values (two 32-bit counts packed
+// in one word: their sums never carry into each other) and the CTA total.
+__device__ __forceinline__ unsigned long long block_excl_scan64(unsigned long long x, unsigned long long &total,
+                                                                unsigned long long *warp_buf) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  unsigned long long incl = x;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) warp_buf[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    const unsigned long long v = lane < nw ? warp_buf[lane] : 0ull;
+    unsigned long long vi = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, vi, off);
+      if (lane >= off) vi += y;
+    }
+    if (lane < nw) warp_buf[lane] = vi - v;
+    if (lane == 31) warp_buf[32] = vi;
+  }
+  __syncthreads();
+  const unsigned long long ex = warp_buf[w] + incl - x;
+  total = warp_buf[32];
+  __syncthreads();
+  return ex;
+}
+
+__device__ __forceinline__ void scan_rows_body(int64_t R, const int32_t *row_cnt, const int32_t *row_pcnt,
+                                               int32_t *row_ptr, int32_t *prow_ptr, unsigned long long *counters) {
   __shared__ int buf_a[33], buf_p[33];
   int carry_a = 0, carry_p = 0, mx = 0;
   for (int64_t base = 0; base < R; base += blockDim.x) {
@@ -427,6 +491,7 @@ __global__ void partial_hash_kernel(DevMask m, const unsigned long long *counter
                                     const int32_t *part_row, const int32_t *part_col,
                                     uint64_t *part_hash) {
   __shared__ uint64_t wsum[8];  // bq <= 256 threads
+  __shared__ int32_t s_kv[128];  // the block's key segment IDs (bk <= 128)
   const int64_t Ap = (int64_t)counters[1];
   const int di = threadIdx.x;
   for (int64_t k = blockIdx.x; k < Ap; k += gridDim.x) {
@@ -439,10 +504,16 @@ __global__ void partial_hash_kernel(DevMask m, const unsigned long long *counter
       if (di == 0) part_hash[k] = (uint64_t)(c * m.bk - r * m.bq);
       continue;
     }
+    if (m.qseg != nullptr) {
+      stage_kv_ids(m, bm, c, s_kv);
+      __syncthreads();
+    }
     const int64_t i = r * m.bq + di;
     const int32_t sq = q_segment(m, bm, i);
     uint64_t h = kHashBasis;
-    for (int32_t w = 0; w < m.bk / 32; ++w) h = hash_step(h, row_word(m, bm, i, sq, c * m.bk + w * 32));
+    for (int32_t w = 0; w < m.bk / 32; ++w)
+      h = hash_step(h, m.qseg != nullptr ? row_word_staged(m, i, sq, c * m.bk, c * m.bk + w * 32, s_kv)
+                                         : row_word(m, bm, i, sq, c * m.bk + w * 32));
     const uint64_t t = warp_sum_u64(row_hash_term(h, di));
     if ((di & 31) == 0) wsum[di >> 5] = t;
     __syncthreads();
@@ -457,9 +528,10 @@ __global__ void partial_hash_kernel(DevMask m, const unsigned long long *counter
 
 // CTA-wide exact comparison of two partial blocks' patterns: each thread
 // compares (row, 32-key word) pieces of both blocks; every thread of the CTA
-// must call it and gets the same result.
-__device__ bool patterns_equal(const DevMask &m, const int32_t *part_row, const int32_t *part_col,
-                               int64_t ka, int64_t kb) {
+// must call it and gets the same result.  With segment IDs, s_kv_a / s_kv_b
+// hold the two blocks' key IDs (staged by the caller).
+__device__ bool patterns_equal(const DevMask &m, const int32_t *part_row, const int32_t *part_col, int64_t ka,
+                               int64_t kb, const int32_t *s_kv_a, const int32_t *s_kv_b) {
   const int64_t rowa = part_row[ka], rowb = part_row[kb];
   const int32_t bma = (int32_t)(rowa / m.nq), bmb = (int32_t)(rowb / m.nq);
   const int64_t ra = rowa % m.nq, rb = rowb % m.nq, ca = part_col[ka], cb = part_col[kb];
@@ -468,8 +540,11 @@ __device__ bool patterns_equal(const DevMask &m, const int32_t *part_row, const 
   for (int32_t x = threadIdx.x; x < m.bq * words && same; x += blockDim.x) {
     const int32_t di = x / words, w = x - di * words;
     const int64_t ia = ra * m.bq + di, ib = rb * m.bq + di;
-    same = row_word(m, bma, ia, q_segment(m, bma, ia), ca * m.bk + w * 32) ==
-           row_word(m, bmb, ib, q_segment(m, bmb, ib), cb * m.bk + w * 32);
+    if (m.qseg != nullptr)
+      same = row_word_staged(m, ia, q_segment(m, bma, ia), ca * m.bk, ca * m.bk + w * 32, s_kv_a) ==
+             row_word_staged(m, ib, q_segment(m, bmb, ib), cb * m.bk, cb * m.bk + w * 32, s_kv_b);
+    else
+      same = row_word(m, bma, ia, 0, ca * m.bk + w * 32) == row_word(m, bmb, ib, 0, cb * m.bk + w * 32);
   }
   return __syncthreads_and(same) != 0;
 }
@@ -482,6 +557,7 @@ __global__ void __launch_bounds__(kDedupThreads)
 dedup_kernel(DevMask m, const unsigned long long *counters, const int32_t *part_row, const int32_t *part_col,
              const uint64_t *part_hash, int32_t *part_rep) {
   __shared__ uint32_t s_ball[kDedupThreads / 32];
+  __shared__ int32_t s_kv_a[128], s_kv_b[128];  // key segment IDs of block k and of the candidate
   const int64_t Ap = (int64_t)counters[1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // band-only whole blocks: equal diagonal offsets (the "hash") mean equal content
@@ -489,6 +565,7 @@ dedup_kernel(DevMask m, const unsigned long long *counters, const int32_t *part_
   for (int64_t k = blockIdx.x; k < Ap; k += gridDim.x) {
     const uint64_t h = part_hash[k];
     int64_t rep = k;  // uniform over the CTA
+    bool staged_a = false;
     for (int64_t base = 0; base < k && rep == k; base += kDedupThreads) {
       const int64_t kp = base + tid;
       const unsigned b = __ballot_sync(0xffffffffu, kp < k && part_hash[kp] == h);
@@ -499,7 +576,22 @@ dedup_kernel(DevMask m, const unsigned long long *counters, const int32_t *part_
         while (cand && rep == k) {
           const int64_t kc = base + 32 * w + (__ffs(cand) - 1);
           cand &= cand - 1u;
-          if (by_offset || patterns_equal(m, part_row, part_col, k, kc)) rep = kc;
+          if (by_offset) {
+            rep = kc;
+            continue;
+          }
+          if (m.qseg != nullptr) {
+            // (patterns_equal ends with a CTA barrier, so the previous
+            // comparison has finished reading the staged IDs)
+            if (!staged_a) {
+              const int64_t row = part_row[k];
+              stage_kv_ids(m, (int32_t)(row / m.nq), part_col[k], s_kv_a);
+              staged_a = true;
+            }
+            stage_kv_ids(m, (int32_t)(part_row[kc] / m.nq), part_col[kc], s_kv_b);
+            __syncthreads();
+          }
+          if (patterns_equal(m, part_row, part_col, k, kc, s_kv_a, s_kv_b)) rep = kc;
         }
       }
       __syncthreads();  // s_ball is rewritten by the next chunk
@@ -508,8 +600,13 @@ dedup_kernel(DevMask m, const unsigned long long *counters, const int32_t *part_
   }
 }
 
+// Pattern indices (one CTA): an exclusive scan of the first-occurrence flags
+// in partial order gives each representative its pattern index (P = the
+// total); then every partial block's mask_next and the pattern list
+// (partial index of pattern u).
 __global__ void __launch_bounds__(1024)
-scan_reps_kernel(unsigned long long *counters, const int32_t *part_rep, int32_t *part_pidx) {
+scan_finalize_kernel(unsigned long long *counters, const int32_t *part_g, const int32_t *part_rep,
+                     int32_t *part_pidx, int32_t *mask_next, int32_t *rep_list) {
   __shared__ int buf[33];
   const int64_t Ap = (int64_t)counters[1];
   int carry = 0;
@@ -522,14 +619,8 @@ scan_reps_kernel(unsigned long long *counters, const int32_t *part_rep, int32_t 
     carry += tot;
   }
   if (threadIdx.x == 0) counters[2] = (unsigned long long)carry;
-}
-
-__global__ void finalize_kernel(const unsigned long long *counters, const int32_t *part_g,
-                                const int32_t *part_rep, const int32_t *part_pidx,
-                                int32_t *mask_next, int32_t *rep_list) {
-  const int64_t Ap = (int64_t)counters[1];
-  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < Ap;
-       k += (int64_t)gridDim.x * blockDim.x) {
+  __syncthreads();  // part_pidx is complete
+  for (int64_t k = threadIdx.x; k < Ap; k += blockDim.x) {
     const int32_t rep = part_rep[k];
     const int32_t u = part_pidx[rep];
     mask_next[part_g[k]] = u;
@@ -537,13 +628,14 @@ __global__ void finalize_kernel(const unsigned long long *counters, const int32_
   }
 }
 
-// One CTA (bq threads) per pattern: the bit-packed rows and the byte pattern.
-// The pattern count is read on the device (counters[2]) and never exceeds the
-// buffer capacity `cap` (a count above it is reported and clipped).
+// One CTA (bq threads) per pattern: its bit-packed rows (word w of row di
+// holds keys 32w .. 32w+31).  The pattern count is read on the device
+// (counters[2]) and never exceeds the buffer capacity `cap` (a count above
+// it is reported and clipped).
 __global__ void materialize_kernel(DevMask m, const unsigned long long *counters, int64_t cap,
                                    const int32_t *rep_list, const int32_t *part_row,
-                                   const int32_t *part_col, uint32_t *pattern_bits, uint8_t *patterns,
-                                   uint32_t *err) {
+                                   const int32_t *part_col, uint32_t *pattern_bits, uint32_t *err) {
+  __shared__ int32_t s_kv[128];  // the block's key segment IDs (bk <= 128)
   const int di = threadIdx.x;
   const int32_t words = m.bk / 32;
   int64_t P = (int64_t)counters[2];
@@ -556,19 +648,17 @@ __global__ void materialize_kernel(DevMask m, const unsigned long long *counters
     const int64_t row = part_row[k];
     const int32_t bm = (int32_t)(row / m.nq);
     const int64_t r = row % m.nq, c = part_col[k];
+    if (m.qseg != nullptr) {
+      stage_kv_ids(m, bm, c, s_kv);
+      __syncthreads();
+    }
     const int64_t i = r * m.bq + di;
     const int32_t sq = q_segment(m, bm, i);
     uint32_t *bits = pattern_bits + (u * m.bq + di) * words;
-    uchar4 *bytes = reinterpret_cast<uchar4 *>(patterns + (u * m.bq + di) * m.bk);
-    for (int32_t w = 0; w < words; ++w) {
-      const uint32_t word = row_word(m, bm, i, sq, c * m.bk + w * 32);
-      bits[w] = word;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const uint32_t nib = word >> (4 * t);
-        bytes[w * 8 + t] = make_uchar4(nib & 1u, (nib >> 1) & 1u, (nib >> 2) & 1u, (nib >> 3) & 1u);
-      }
-    }
+    for (int32_t w = 0; w < words; ++w)
+      bits[w] = m.qseg != nullptr ? row_word_staged(m, i, sq, c * m.bk, c * m.bk + w * 32, s_kv)
+                                  : row_word(m, bm, i, sq, c * m.bk + w * 32);
+    if (m.qseg != nullptr) __syncthreads();  // s_kv is restaged for the next pattern
   }
 }
 
@@ -576,8 +666,8 @@ __global__ void materialize_kernel(DevMask m, const unsigned long long *counters
 // Rows sorted by descending active-block count, ties in ascending row order
 // (a stable counting sort): the attention kernel takes its work longest row
 // first.  One CTA; `hist` is a global scratch array of nk+1 counters.
-__global__ void __launch_bounds__(1024)
-row_order_kernel(int64_t R, int64_t nk, const int32_t *row_cnt, int32_t *hist, int32_t *row_order) {
+__device__ __forceinline__ void row_order_body(int64_t R, int64_t nk, const int32_t *row_cnt, int32_t *hist,
+                                               int32_t *row_order) {
   __shared__ int buf[33];
   for (int64_t b = threadIdx.x; b <= nk; b += blockDim.x) hist[b] = 0;
   __syncthreads();
@@ -614,6 +704,16 @@ row_order_kernel(int64_t R, int64_t nk, const int32_t *row_cnt, int32_t *hist, i
   }
 }
 
+// row_ptr and the partial offsets, then the row order, in one CTA (both need
+// only the per-row counts).
+__global__ void __launch_bounds__(1024)
+scan_order_kernel(int64_t R, int64_t nk, const int32_t *row_cnt, const int32_t *row_pcnt, int32_t *row_ptr,
+                  int32_t *prow_ptr, unsigned long long *counters, int32_t *hist, int32_t *row_order) {
+  scan_rows_body(R, row_cnt, row_pcnt, row_ptr, prow_ptr, counters);
+  __syncthreads();
+  row_order_body(R, nk, row_cnt, hist, row_order);
+}
+
 // ---------------------------------------------------------------- fused build
 // The whole pipeline above in one CTA, for band-only masks (no segment IDs)
 // with a small table.  Every phase is a loop over the CTA's 1024 threads with
@@ -639,7 +739,6 @@ struct SmallOut {
   uint8_t *bounds_start, *bounds_end;
   unsigned long long *counters;
   uint32_t *pattern_bits;
-  uint8_t *patterns;
   int64_t cap_patterns;
   uint32_t *err;
   int32_t max_partials;  // capacity of the shared partial arrays
@@ -666,50 +765,55 @@ __global__ void __launch_bounds__(kSmallThreads) build_small_kernel(DevMask m, S
   int32_t *s_pg = s_pcol + PM;                                             // [PM]
   int32_t *s_prep = s_pg + PM;                                             // [PM]
   int32_t *s_ppidx = s_prep + PM;                                          // [PM]
-  __shared__ int buf_a[33], buf_p[33], s_mx[32];
+  __shared__ int buf_a[33], s_mx[32];
+  __shared__ unsigned long long buf_ap[33];
   __shared__ unsigned long long s_allowed;
   __shared__ int64_t s_tot[3];  // A, A_p, P
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int64_t A, W;
   band_limits(m, A, W);
 
-  // classes, per-row counts, allowed pairs
-  for (int64_t x = tid; x < R; x += kSmallThreads) {
-    s_cnt[x] = 0;
-    s_pcnt[x] = 0;
-  }
+  // classes and per-row counts (one warp per row: ballots, no shared-memory
+  // atomics on a row's counters), allowed pairs
   if (tid == 0) s_allowed = 0;
-  __syncthreads();
-  const int32_t nk32 = (int32_t)nk, nb32 = (int32_t)(R * nk);
-  for (int32_t idx = tid; idx < nb32; idx += kSmallThreads) {
-    const int32_t r = idx / nk32, c = idx - r * nk32;
-    const int cls = band_block_class(m, A, W, r, c);
-    o.block_mask[idx] = (int8_t)cls;
-    if (cls != 0) atomicAdd(&s_cnt[r], 1);
-    if (cls == 1) atomicAdd(&s_pcnt[r], 1);
+  for (int64_t r = warp; r < R; r += kSmallThreads / 32) {
+    int na = 0, np = 0;
+    for (int64_t cb = 0; cb < nk; cb += 32) {
+      const int64_t c = cb + lane;
+      const int cls = c < nk ? band_block_class(m, A, W, r, c) : 0;
+      if (c < nk) o.block_mask[r * nk + c] = (int8_t)cls;
+      na += __popc(__ballot_sync(0xffffffffu, cls != 0));
+      np += __popc(__ballot_sync(0xffffffffu, cls == 1));
+    }
+    if (lane == 0) {
+      s_cnt[r] = na;
+      s_pcnt[r] = np;
+    }
   }
+  __syncthreads();
   unsigned long long allowed = 0;
   for (int64_t i = tid; i < m.Lq; i += kSmallThreads) allowed += (unsigned long long)band_row_count(m, A, W, i);
   for (int off = 16; off; off >>= 1) allowed += __shfl_xor_sync(0xffffffffu, allowed, off);
   if (lane == 0 && allowed) atomicAdd(&s_allowed, allowed);
   __syncthreads();
 
-  // row_ptr (CSR), partial offsets and the longest row
+  // row_ptr (CSR), partial offsets and the longest row: one scan of the two
+  // counts packed in 64 bits (each total is at most R * nk <= 2^16)
   int carry_a = 0, carry_p = 0, mx = 0;
   for (int64_t base = 0; base < R; base += kSmallThreads) {
     const int64_t x = base + tid;
     const int a = x < R ? s_cnt[x] : 0, pc = x < R ? s_pcnt[x] : 0;
     mx = max(mx, a);
-    int ta, tp;
-    const int ea = block_excl_scan(a, ta, buf_a);
-    const int ep = block_excl_scan(pc, tp, buf_p);
+    unsigned long long tot;
+    const unsigned long long ex =
+        block_excl_scan64((unsigned long long)a | ((unsigned long long)pc << 32), tot, buf_ap);
     if (x < R) {
-      s_rp[x] = carry_a + ea;
-      s_prp[x] = carry_p + ep;
-      o.row_ptr[x] = carry_a + ea;
+      s_rp[x] = carry_a + (int)(ex & 0xffffffffull);
+      s_prp[x] = carry_p + (int)(ex >> 32);
+      o.row_ptr[x] = s_rp[x];
     }
-    carry_a += ta;
-    carry_p += tp;
+    carry_a += (int)(tot & 0xffffffffull);
+    carry_p += (int)(tot >> 32);
   }
   for (int off = 16; off; off >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   if (lane == 0) s_mx[warp] = mx;
@@ -838,30 +942,19 @@ __global__ void __launch_bounds__(kSmallThreads) build_small_kernel(DevMask m, S
   for (int64_t k = tid; k < Ap; k += kSmallThreads)
     if (s_prep[k] == k) s_pg[s_ppidx[k]] = (int32_t)k;  // s_pg becomes the pattern list
   __syncthreads();
-  // partial_mask_blocks and their bit-packed copy (groups of bq threads)
+  // the patterns, bit-packed (word w of row di of pattern u holds keys
+  // 32w .. 32w+31): one word per thread, consecutive threads on consecutive words
   int64_t P = s_tot[2];
   if (P > o.cap_patterns) {
     if (tid == 0 && o.err) atomicOr(o.err, SPLASH_DEV_BAD_TABLE);
     P = o.cap_patterns;
   }
-  const int32_t words = m.bk / 32;
-  const int G = kSmallThreads / m.bq, grp = tid / m.bq, di = tid - grp * m.bq;
-  for (int64_t u0 = 0; u0 < P; u0 += G) {
-    const int64_t u = u0 + grp;
-    if (u >= P) break;
+  const int32_t words = m.bk / 32, per_pattern = m.bq * words;
+  for (int64_t x = tid; x < P * per_pattern; x += kSmallThreads) {
+    const int64_t u = x / per_pattern;
+    const int32_t rem = (int32_t)(x - u * per_pattern), di = rem / words, w = rem - di * words;
     const int64_t k = s_pg[u];
-    const int64_t i = (int64_t)s_prow[k] * m.bq + di, c = s_pcol[k];
-    uint32_t *bits = o.pattern_bits + (u * m.bq + di) * words;
-    uchar4 *bytes = reinterpret_cast<uchar4 *>(o.patterns + (u * m.bq + di) * m.bk);
-    for (int32_t w = 0; w < words; ++w) {
-      const uint32_t word = row_word(m, 0, i, 0, c * m.bk + w * 32);
-      bits[w] = word;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const uint32_t nib = word >> (4 * t);
-        bytes[w * 8 + t] = make_uchar4(nib & 1u, (nib >> 1) & 1u, (nib >> 2) & 1u, (nib >> 3) & 1u);
-      }
-    }
+    o.pattern_bits[x] = row_word(m, 0, (int64_t)s_prow[k] * m.bq + di, 0, (int64_t)s_pcol[k] * m.bk + w * 32);
   }
 }
 
@@ -880,6 +973,34 @@ cudaError_t grow_host(T *&p, int64_t have, int64_t need) {
   if (p) cudaFreeHost(p);
   p = nullptr;
   return cudaMallocHost(&p, sizeof(T) * (size_t)std::max<int64_t>(need, 1));
+}
+
+// Largest pattern buffer the build reserves from a bound instead of waiting
+// for the exact pattern count.
+constexpr int64_t kPatternBudgetBytes = (int64_t)256 << 20;
+
+// Blocks of one table batch row that the band part of the mask (causal and
+// window bounds, and the padding of a ragged grid) leaves non-empty; the
+// same closed form as band_block_class, one row at a time: for the rows
+// r0 .. r1 (clipped to Lq) the non-empty key blocks are those with
+// c0 <= r1 + A and c1 >= r0 - W, a contiguous range.
+int64_t band_active_blocks(const splash_mask_spec *spec, int64_t Lq, int64_t Lk, int32_t bq, int32_t bk, int64_t nq,
+                           int64_t nk) {
+  const int64_t kInf = (int64_t)1 << 60;
+  int64_t A = kInf, W = spec->window_left >= 0 ? spec->window_left : kInf;
+  if (spec->causal) A = 0;
+  if (spec->window_right >= 0) A = std::min(A, spec->window_right);
+  int64_t total = 0;
+  for (int64_t r = 0; r < nq; ++r) {
+    const int64_t r0 = r * bq, r1 = std::min(r0 + bq - 1, Lq - 1);
+    // c * bk <= r1 + A  and  min(c * bk + bk - 1, Lk - 1) >= r0 - W
+    const int64_t hi = A >= kInf ? nk - 1 : std::min(nk - 1, (r1 + A) / bk);
+    int64_t lo = 0;
+    if (W < kInf && r0 - W > 0) lo = (r0 - W) / bk;  // block c holds key r0 - W when c = floor((r0 - W) / bk)
+    if (r0 - W > Lk - 1 && W < kInf) lo = nk;         // every key is left of the window
+    if (hi >= lo) total += hi - lo + 1;
+  }
+  return std::max<int64_t>(total, 1);
 }
 
 splash_status map_alloc(cudaError_t e) {
@@ -903,7 +1024,7 @@ void splash_mask_info_free_transposed(splash_mask_info *mi) {
 void splash_mask_info_free_buffers(splash_mask_info *mi) {
   splash_mask_info_free_transposed(mi);
   void *dev[] = {mi->block_mask, mi->row_ptr, mi->active_rows, mi->active_cols, mi->mask_next,
-                 mi->bounds_start, mi->bounds_end, mi->patterns, mi->pattern_bits, mi->row_order,
+                 mi->bounds_start, mi->bounds_end, mi->pattern_bits, mi->row_order,
                  mi->row_cnt, mi->row_pcnt, mi->prow_ptr, mi->seg_summary, mi->part_row,
                  mi->part_col, mi->part_g, mi->part_hash, mi->part_rep, mi->part_pidx,
                  mi->rep_list, mi->counters, mi->row_hist};
@@ -990,37 +1111,39 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
   SPLASH_CUDA_TRY(cudaGetDevice(&dev));
   SPLASH_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
 
-  // a previous asynchronous build (possibly on another stream) copies its
-  // totals into h_counters: keep that copy ordered before this build's
+  // a previous asynchronous build, possibly on another stream, may still be
+  // running on the same buffers: keep it ordered before this one
   if (mi->counts_pending && mi->counts_ready) SPLASH_CUDA_TRY(cudaStreamWaitEvent(stream, mi->counts_ready, 0));
 
   uint32_t *err = splash_device_error_word(mi->device);
-  // -- pattern buffer.  Without segment IDs a q-block row has at most
-  // 2 * (ceil((bq-1)/bk) + 1) partial blocks (a block is partial only if one of
-  // the two band edges sweeps through it), so P has a bound known here and the
-  // build runs without a host wait; the totals are read lazily.  With segment
-  // IDs the build waits once for P.  A ragged grid adds at most the last
-  // column's block of every row and the whole last row.
+  // -- pattern buffer (bit-packed patterns, bq * bk / 8 bytes each).  Without
+  // segment IDs a q-block row has at most 2 * (ceil((bq-1)/bk) + 1) partial
+  // blocks (a block is partial only if one of the two band edges sweeps
+  // through it); a ragged grid adds at most the last column's block of every
+  // row and the whole last row.  With segment IDs every pattern belongs to an
+  // active block, and segments only remove pairs, so P is at most the number
+  // of blocks the band alone leaves non-empty (counted here in closed form).
+  // When that bound fits the budget the build runs without a host wait and
+  // the totals are read when asked for; otherwise it waits once for P.
   const int64_t per_row = 2 * ((bq - 1 + bk - 1) / bk + 1);
-  const int64_t p_bound = std::min<int64_t>(R * per_row + (ragged ? R + nk : 0), NB);
-  const bool async = !seg && p_bound * (int64_t)bq * bk <= ((int64_t)256 << 20);
+  const int64_t p_bound =
+      seg ? (int64_t)nbm * band_active_blocks(spec, Lq, Lk, bq, bk, nq, nk)
+          : std::min<int64_t>(R * per_row + (ragged ? R + nk : 0), NB);
+  const int64_t pattern_bytes = (int64_t)bq * bk / 8;
+  const bool async = p_bound * pattern_bytes <= kPatternBudgetBytes;
   auto reserve_patterns = [&](int64_t P_cap) -> splash_status {
     if (P_cap <= 0 || mi->cap_patterns >= P_cap) return SPLASH_OK;
-    if (mi->patterns) cudaFree(mi->patterns);
     if (mi->pattern_bits) cudaFree(mi->pattern_bits);
-    mi->patterns = nullptr;
     mi->pattern_bits = nullptr;
     mi->cap_patterns = 0;
     splash_status s2;
-    if ((s2 = map_alloc(cudaMalloc(&mi->patterns, (size_t)P_cap * bq * bk))) != SPLASH_OK) return s2;
-    if ((s2 = map_alloc(cudaMalloc(&mi->pattern_bits, (size_t)P_cap * bq * (bk / 32) * 4))) != SPLASH_OK)
-      return s2;
+    if ((s2 = map_alloc(cudaMalloc(&mi->pattern_bits, (size_t)P_cap * pattern_bytes))) != SPLASH_OK) return s2;
     mi->cap_patterns = P_cap;
     return SPLASH_OK;
   };
+  // the totals stay on the device; splash_mask_info_sync_counts copies them
+  // once this event has completed
   auto finish_async = [&]() -> splash_status {
-    SPLASH_CUDA_TRY(cudaMemcpyAsync(mi->h_counters, mi->counters, sizeof(unsigned long long) * 8,
-                                    cudaMemcpyDeviceToHost, stream));
     if (mi->counts_ready == nullptr)
       SPLASH_CUDA_TRY(cudaEventCreateWithFlags(&mi->counts_ready, cudaEventDisableTiming));
     SPLASH_CUDA_TRY(cudaEventRecord(mi->counts_ready, stream));
@@ -1028,7 +1151,7 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
     return SPLASH_OK;
   };
 
-  if (async && !ragged && R <= kSmallMaxRows && nk <= kSmallMaxCols && NB <= kSmallMaxBlocks &&
+  if (async && !seg && !ragged && R <= kSmallMaxRows && nk <= kSmallMaxCols && NB <= kSmallMaxBlocks &&
       p_bound <= kSmallMaxPartials) {
     // small band-only table on whole blocks: the whole build is one
     // single-CTA kernel (its diagonal-offset dedup needs whole blocks)
@@ -1044,7 +1167,6 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
     o.bounds_end = mi->bounds_end;
     o.counters = mi->counters;
     o.pattern_bits = mi->pattern_bits;
-    o.patterns = mi->patterns;
     o.cap_patterns = mi->cap_patterns;
     o.err = err;
     o.max_partials = (int32_t)p_bound;
@@ -1058,14 +1180,15 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
     return finish_async();
   }
 
-  SPLASH_CUDA_TRY(cudaMemsetAsync(mi->row_cnt, 0, sizeof(int32_t) * R, stream));
-  SPLASH_CUDA_TRY(cudaMemsetAsync(mi->row_pcnt, 0, sizeof(int32_t) * R, stream));
-  SPLASH_CUDA_TRY(cudaMemsetAsync(mi->counters, 0, sizeof(unsigned long long) * 8, stream));
-
   int32_t *qsum = mi->seg_summary, *kvsum = mi->seg_summary + 2 * R;
   if (seg) {
+    // (the summary kernel also clears the row counters and the totals)
     dim3 grid((unsigned)((nq + nk + 7) / 8), (unsigned)nbm);
-    seg_summary_kernel<<<grid, 256, 0, stream>>>(m, qsum, kvsum);
+    seg_summary_kernel<<<grid, 256, 0, stream>>>(m, qsum, kvsum, mi->row_cnt, mi->row_pcnt, mi->counters);
+  } else {
+    SPLASH_CUDA_TRY(cudaMemsetAsync(mi->row_cnt, 0, sizeof(int32_t) * R, stream));
+    SPLASH_CUDA_TRY(cudaMemsetAsync(mi->row_pcnt, 0, sizeof(int32_t) * R, stream));
+    SPLASH_CUDA_TRY(cudaMemsetAsync(mi->counters, 0, sizeof(unsigned long long) * 8, stream));
   }
   {
     dim3 grid((unsigned)((nk + kClassifyThreads - 1) / kClassifyThreads), (unsigned)nq, (unsigned)nbm);
@@ -1074,13 +1197,12 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
                                                           NB);
   }
   if (seg) {
-    // the deferred list lives in rep_list, which finalize_kernel fills later
+    // the deferred list lives in rep_list, which scan_finalize_kernel fills later
     count_deferred_kernel<<<sms * 4, kClassifyThreads, 0, stream>>>(m, mi->rep_list, NB, mi->block_mask,
                                                                    mi->row_cnt, mi->row_pcnt, mi->counters);
   }
-  scan_rows_kernel<<<1, 1024, 0, stream>>>(R, mi->row_cnt, mi->row_pcnt, mi->row_ptr, mi->prow_ptr,
-                                           mi->counters);
-  row_order_kernel<<<1, 1024, 0, stream>>>(R, nk, mi->row_cnt, mi->row_hist, mi->row_order);
+  scan_order_kernel<<<1, 1024, 0, stream>>>(R, nk, mi->row_cnt, mi->row_pcnt, mi->row_ptr, mi->prow_ptr, mi->counters,
+                                            mi->row_hist, mi->row_order);
   compact_kernel<<<(unsigned)((R + 7) / 8), 256, 0, stream>>>(
       m, R, mi->block_mask, mi->row_ptr, mi->prow_ptr, mi->active_rows, mi->active_cols,
       mi->mask_next, mi->bounds_start, mi->bounds_end, mi->part_row, mi->part_col, mi->part_g);
@@ -1088,11 +1210,10 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
                                                   mi->part_hash);
   dedup_kernel<<<sms * 4, kDedupThreads, 0, stream>>>(m, mi->counters, mi->part_row, mi->part_col,
                                             mi->part_hash, mi->part_rep);
-  scan_reps_kernel<<<1, 1024, 0, stream>>>(mi->counters, mi->part_rep, mi->part_pidx);
-  finalize_kernel<<<sms * 4, 256, 0, stream>>>(mi->counters, mi->part_g, mi->part_rep,
-                                               mi->part_pidx, mi->mask_next, mi->rep_list);
+  scan_finalize_kernel<<<1, 1024, 0, stream>>>(mi->counters, mi->part_g, mi->part_rep, mi->part_pidx, mi->mask_next,
+                                               mi->rep_list);
   SPLASH_CUDA_TRY(cudaGetLastError());
-  splash_count_launches(seg ? 11 : 9);
+  splash_count_launches(seg ? 8 : 6);
 
   int64_t P_cap;
   if (async) {
@@ -1107,7 +1228,7 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
   if (P_cap > 0) {
     const unsigned grid = (unsigned)std::min<int64_t>(P_cap, async ? sms * 4 : 65535);
     materialize_kernel<<<grid, bq, 0, stream>>>(m, mi->counters, mi->cap_patterns, mi->rep_list, mi->part_row,
-                                                mi->part_col, mi->pattern_bits, mi->patterns, err);
+                                                mi->part_col, mi->pattern_bits, err);
     SPLASH_CUDA_TRY(cudaGetLastError());
     splash_count_launches(1);
   }
@@ -1127,6 +1248,7 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
 splash_status splash_mask_info_sync_counts(splash_mask_info *mi) {
   if (!mi->counts_pending) return SPLASH_OK;
   SPLASH_CUDA_TRY(cudaEventSynchronize(mi->counts_ready));
+  SPLASH_CUDA_TRY(cudaMemcpy(mi->h_counters, mi->counters, sizeof(unsigned long long) * 8, cudaMemcpyDeviceToHost));
   mi->num_active = (int64_t)mi->h_counters[0];
   mi->num_partial = (int64_t)mi->h_counters[1];
   mi->num_patterns = (int64_t)mi->h_counters[2];
@@ -1263,7 +1385,7 @@ splash_status splash_classify_blocks_noalloc_impl(const splash_mask_spec *spec, 
   SPLASH_CUDA_TRY(cudaMemsetAsync(s->counters, 0, sizeof(s->counters), stream));
   if (seg) {
     dim3 grid((unsigned)((nq + nk + 7) / 8), (unsigned)nbm);
-    seg_summary_kernel<<<grid, 256, 0, stream>>>(m, s->qsum, s->kvsum);
+    seg_summary_kernel<<<grid, 256, 0, stream>>>(m, s->qsum, s->kvsum, s->row_cnt, s->row_pcnt, s->counters);
   }
   {
     dim3 grid((unsigned)((nk + kClassifyThreads - 1) / kClassifyThreads), (unsigned)nq, (unsigned)nbm);

@@ -59,7 +59,7 @@ def test_bench_percentiles_and_mask_info_rate():
     # dense causal, 128 x 128 blocks: 32 x 32 grid, 528 active blocks, 1 pattern
     r = bench.mask_info_rate(w, {"num_active": 528, "num_patterns": 1},
                              {"batch_rows": 1, "nq": 32, "nk": 32}, [0.02, 0.01, 0.03], {"hbm_gbs": 1000.0})
-    expect = 32 * 32 + 4 * 33 + 528 * 14 + 128 * 128 + 128 * 128 // 8
+    expect = 32 * 32 + 4 * 33 + 528 * 14 + 128 * 128 // 8
     assert r["bytes"] == expect and r["ms_p50"] == 0.02
     assert abs(r["gbs"] - expect / 0.02e-3 / 1e9) < 1e-2 and abs(r["frac_of_hbm"] - r["gbs"] / 1000.0) < 1e-4
 
