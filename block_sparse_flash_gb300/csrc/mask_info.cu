@@ -116,24 +116,61 @@ __device__ __forceinline__ int64_t band_row_count(const DevMask &m, int64_t A, i
 }
 
 // Segment IDs of key block c of batch row bm, staged in shared memory by the
-// whole CTA (keys past Lk are never read: band_range clips them).
-__device__ __forceinline__ void stage_kv_ids(const DevMask &m, int32_t bm, int64_t c, int32_t *s_kv) {
+// whole CTA (keys past Lk are never read: band_range clips them).  Returns,
+// to every thread, whether the block's IDs are non-decreasing (then the keys
+// with a given ID form one run, found by binary search).
+__device__ __forceinline__ bool stage_kv_ids(const DevMask &m, int32_t bm, int64_t c, int32_t *s_kv) {
+  const int64_t n = min((int64_t)m.bk, m.Lk - c * m.bk);  // real keys of the block
   for (int32_t t = threadIdx.x; t < m.bk; t += blockDim.x) {
     const int64_t j = c * m.bk + t;
     s_kv[t] = j < m.Lk ? m.kvseg[(int64_t)bm * m.Lk + j] : 0;
   }
+  __syncthreads();
+  bool sorted = true;
+  for (int32_t t = threadIdx.x; t + 1 < n; t += blockDim.x) sorted &= s_kv[t] <= s_kv[t + 1];
+  return __syncthreads_and(sorted) != 0;
+}
+
+// The run [a, b] (block offsets) of keys with ID sq in a sorted staged block
+// of n real keys (empty: a > b).
+__device__ __forceinline__ void sorted_run(const int32_t *s_kv, int32_t n, int32_t sq, int32_t &a, int32_t &b) {
+  int32_t lo = 0, hi = n;  // first index with s_kv >= sq
+  while (lo < hi) {
+    const int32_t mid = (lo + hi) >> 1;
+    if (s_kv[mid] < sq) lo = mid + 1; else hi = mid;
+  }
+  a = lo;
+  hi = n;  // first index with s_kv > sq
+  while (lo < hi) {
+    const int32_t mid = (lo + hi) >> 1;
+    if (s_kv[mid] <= sq) lo = mid + 1; else hi = mid;
+  }
+  b = lo - 1;
 }
 
 // row_word with the key block's segment IDs staged in shared memory (its
 // first key is c0): 32 mask bits of query i (segment id sq) against keys
-// j0 .. j0+31.
+// j0 .. j0+31.  For a sorted block, run = [ra, rb] is the row's run of keys
+// with ID sq (block offsets, from sorted_run) and the word is one range of bits.
 __device__ __forceinline__ uint32_t row_word_staged(const DevMask &m, int64_t i, int32_t sq, int64_t c0, int64_t j0,
-                                                    const int32_t *s_kv) {
+                                                    const int32_t *s_kv, bool sorted, int32_t ra, int32_t rb) {
   int64_t lo, hi;
   band_range(m, i, j0, j0 + 31, lo, hi);
+  if (sorted) {
+    lo = max(lo, c0 + ra);
+    hi = min(hi, c0 + rb);
+    if (hi < lo) return 0u;
+    const int64_t n = hi - lo + 1;
+    return (n >= 32 ? 0xffffffffu : ((1u << n) - 1u)) << (lo - j0);
+  }
   uint32_t bits = 0u;
   for (int64_t j = lo; j <= hi; ++j) bits |= (uint32_t)(s_kv[j - c0] == sq) << (j - j0);
   return bits;
+}
+
+// Real keys of key block c (fewer than bk only in the last block of a ragged Lk).
+__device__ __forceinline__ int32_t block_keys(const DevMask &m, int64_t c) {
+  return (int32_t)min((int64_t)m.bk, m.Lk - c * m.bk);
 }
 
 // ---------------------------------------------------------------- K1
@@ -191,6 +228,7 @@ classify_kernel(DevMask m, const int32_t *qsum, const int32_t *kvsum, int8_t *bl
   const int64_t row = (int64_t)bm * m.nq + r;
   int64_t cnt = 0;
   int cls = 0;
+  bool undecided = false;  // segment summaries leave the block's class open
   if (m.qseg == nullptr) {
     // band only: classes in closed form; the allowed pairs are counted per
     // query row by the first CTA of the row (cnt is then a row count)
@@ -224,31 +262,44 @@ classify_kernel(DevMask m, const int32_t *qsum, const int32_t *kvsum, int8_t *bl
       if (qmx < kmn || kmx < qmn) {
         cnt = 0;  // no segment id in common
       } else if (!(qmn == qmx && kmn == kmx && qmn == kmn)) {
-        // undecided by the summaries: counted by count_deferred_kernel while
-        // the list has room, else here element by element
-        unsigned long long slot = ~0ull;
-        if (deferred != nullptr) slot = atomicAdd(&counters[5], 1ull);
-        if (slot < (unsigned long long)defer_cap) {
-          deferred[slot] = (int32_t)(row * m.nk + c);
-          cnt = -1;
-        } else {
-          const int32_t *kv = m.kvseg + (int64_t)bm * m.Lk;
-          cnt = 0;
-          for (int32_t di = 0; di < m.bq; ++di) {
-            const int64_t i = r * m.bq + di;
-            const int32_t sq = q_segment(m, bm, i);
-            int64_t lo, hi;
-            band_range(m, i, c0, c1, lo, hi);
-            for (int64_t j = lo; j <= hi; ++j) cnt += (kv[j] == sq);
-          }
-        }
+        undecided = true;  // handled below, with the whole warp
       }
       // (both constant and equal: the band count stands)
+    }
+  }
+  if (m.qseg != nullptr) {
+    // undecided blocks: counted by count_deferred_kernel while the list has
+    // room (slots reserved with one atomic per warp), else here element by element
+    const unsigned um = __ballot_sync(0xffffffffu, undecided && deferred != nullptr);
+    unsigned long long base = 0;
+    if (um) {
+      const int leader = __ffs(um) - 1;
+      if ((int)(threadIdx.x & 31) == leader) base = atomicAdd(&counters[5], (unsigned long long)__popc(um));
+      base = __shfl_sync(0xffffffffu, base, leader);
+    }
+    if (undecided) {
+      const unsigned long long slot =
+          deferred != nullptr ? base + __popc(um & ((1u << (threadIdx.x & 31)) - 1u)) : ~0ull;
+      if (slot < (unsigned long long)defer_cap) {
+        deferred[slot] = (int32_t)(row * m.nk + c);
+        cnt = -1;
+      } else {
+        const int64_t c0 = c * m.bk, c1 = c0 + m.bk - 1;
+        const int32_t *kv = m.kvseg + (int64_t)bm * m.Lk;
+        cnt = 0;
+        for (int32_t di = 0; di < m.bq; ++di) {
+          const int64_t i = r * m.bq + di;
+          const int32_t sq = q_segment(m, bm, i);
+          int64_t lo, hi;
+          band_range(m, i, c0, c1, lo, hi);
+          for (int64_t j = lo; j <= hi; ++j) cnt += (kv[j] == sq);
+        }
+      }
     }
     if (cnt < 0) {
       cnt = 0;  // deferred: class and counts come from count_deferred_kernel
       cls = 0;
-    } else {
+    } else if (c < m.nk) {
       cls = cnt == 0 ? 0 : (cnt == (int64_t)m.bq * m.bk ? 2 : 1);
       block_mask[row * m.nk + c] = (int8_t)cls;
     }
@@ -300,8 +351,7 @@ count_deferred_kernel(DevMask m, const int32_t *deferred, int64_t defer_cap, int
     const int64_t row = idx / m.nk, c = idx - row * m.nk;
     const int32_t bm = (int32_t)(row / m.nq);
     const int64_t r = row - (int64_t)bm * m.nq;
-    stage_kv_ids(m, bm, c, s_kv);
-    __syncthreads();
+    const bool sorted = stage_kv_ids(m, bm, c, s_kv);
     unsigned long long cnt = 0;
     for (int32_t d = di; d < m.bq; d += kClassifyThreads) {
       const int64_t i = r * m.bq + d;
@@ -309,7 +359,13 @@ count_deferred_kernel(DevMask m, const int32_t *deferred, int64_t defer_cap, int
       band_range(m, i, c * m.bk, c * m.bk + m.bk - 1, lo, hi);
       if (hi >= lo) {
         const int32_t sq = q_segment(m, bm, i);
-        for (int64_t j = lo; j <= hi; ++j) cnt += (s_kv[j - c * m.bk] == sq);
+        if (sorted) {
+          int32_t a, b;
+          sorted_run(s_kv, block_keys(m, c), sq, a, b);
+          cnt += (unsigned long long)max((int64_t)0, min(hi, c * m.bk + b) - max(lo, c * m.bk + a) + 1);
+        } else {
+          for (int64_t j = lo; j <= hi; ++j) cnt += (s_kv[j - c * m.bk] == sq);
+        }
       }
     }
     for (int off = 16; off; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
@@ -504,15 +560,14 @@ __global__ void partial_hash_kernel(DevMask m, const unsigned long long *counter
       if (di == 0) part_hash[k] = (uint64_t)(c * m.bk - r * m.bq);
       continue;
     }
-    if (m.qseg != nullptr) {
-      stage_kv_ids(m, bm, c, s_kv);
-      __syncthreads();
-    }
+    const bool sorted = m.qseg != nullptr ? stage_kv_ids(m, bm, c, s_kv) : false;
     const int64_t i = r * m.bq + di;
     const int32_t sq = q_segment(m, bm, i);
+    int32_t ra = 0, rb = -1;
+    if (sorted) sorted_run(s_kv, block_keys(m, c), sq, ra, rb);
     uint64_t h = kHashBasis;
     for (int32_t w = 0; w < m.bk / 32; ++w)
-      h = hash_step(h, m.qseg != nullptr ? row_word_staged(m, i, sq, c * m.bk, c * m.bk + w * 32, s_kv)
+      h = hash_step(h, m.qseg != nullptr ? row_word_staged(m, i, sq, c * m.bk, c * m.bk + w * 32, s_kv, sorted, ra, rb)
                                          : row_word(m, bm, i, sq, c * m.bk + w * 32));
     const uint64_t t = warp_sum_u64(row_hash_term(h, di));
     if ((di & 31) == 0) wsum[di >> 5] = t;
@@ -531,7 +586,8 @@ __global__ void partial_hash_kernel(DevMask m, const unsigned long long *counter
 // must call it and gets the same result.  With segment IDs, s_kv_a / s_kv_b
 // hold the two blocks' key IDs (staged by the caller).
 __device__ bool patterns_equal(const DevMask &m, const int32_t *part_row, const int32_t *part_col, int64_t ka,
-                               int64_t kb, const int32_t *s_kv_a, const int32_t *s_kv_b) {
+                               int64_t kb, const int32_t *s_kv_a, const int32_t *s_kv_b, bool sorted_a,
+                               bool sorted_b) {
   const int64_t rowa = part_row[ka], rowb = part_row[kb];
   const int32_t bma = (int32_t)(rowa / m.nq), bmb = (int32_t)(rowb / m.nq);
   const int64_t ra = rowa % m.nq, rb = rowb % m.nq, ca = part_col[ka], cb = part_col[kb];
@@ -540,10 +596,14 @@ __device__ bool patterns_equal(const DevMask &m, const int32_t *part_row, const 
   for (int32_t x = threadIdx.x; x < m.bq * words && same; x += blockDim.x) {
     const int32_t di = x / words, w = x - di * words;
     const int64_t ia = ra * m.bq + di, ib = rb * m.bq + di;
-    if (m.qseg != nullptr)
-      same = row_word_staged(m, ia, q_segment(m, bma, ia), ca * m.bk, ca * m.bk + w * 32, s_kv_a) ==
-             row_word_staged(m, ib, q_segment(m, bmb, ib), cb * m.bk, cb * m.bk + w * 32, s_kv_b);
-    else
+    if (m.qseg != nullptr) {
+      const int32_t sa = q_segment(m, bma, ia), sb = q_segment(m, bmb, ib);
+      int32_t a0 = 0, a1 = -1, b0 = 0, b1 = -1;
+      if (sorted_a) sorted_run(s_kv_a, block_keys(m, ca), sa, a0, a1);
+      if (sorted_b) sorted_run(s_kv_b, block_keys(m, cb), sb, b0, b1);
+      same = row_word_staged(m, ia, sa, ca * m.bk, ca * m.bk + w * 32, s_kv_a, sorted_a, a0, a1) ==
+             row_word_staged(m, ib, sb, cb * m.bk, cb * m.bk + w * 32, s_kv_b, sorted_b, b0, b1);
+    } else
       same = row_word(m, bma, ia, 0, ca * m.bk + w * 32) == row_word(m, bmb, ib, 0, cb * m.bk + w * 32);
   }
   return __syncthreads_and(same) != 0;
@@ -565,7 +625,7 @@ dedup_kernel(DevMask m, const unsigned long long *counters, const int32_t *part_
   for (int64_t k = blockIdx.x; k < Ap; k += gridDim.x) {
     const uint64_t h = part_hash[k];
     int64_t rep = k;  // uniform over the CTA
-    bool staged_a = false;
+    bool staged_a = false, sorted_a = false, sorted_b = false;
     for (int64_t base = 0; base < k && rep == k; base += kDedupThreads) {
       const int64_t kp = base + tid;
       const unsigned b = __ballot_sync(0xffffffffu, kp < k && part_hash[kp] == h);
@@ -585,13 +645,12 @@ dedup_kernel(DevMask m, const unsigned long long *counters, const int32_t *part_
             // comparison has finished reading the staged IDs)
             if (!staged_a) {
               const int64_t row = part_row[k];
-              stage_kv_ids(m, (int32_t)(row / m.nq), part_col[k], s_kv_a);
+              sorted_a = stage_kv_ids(m, (int32_t)(row / m.nq), part_col[k], s_kv_a);
               staged_a = true;
             }
-            stage_kv_ids(m, (int32_t)(part_row[kc] / m.nq), part_col[kc], s_kv_b);
-            __syncthreads();
+            sorted_b = stage_kv_ids(m, (int32_t)(part_row[kc] / m.nq), part_col[kc], s_kv_b);
           }
-          if (patterns_equal(m, part_row, part_col, k, kc, s_kv_a, s_kv_b)) rep = kc;
+          if (patterns_equal(m, part_row, part_col, k, kc, s_kv_a, s_kv_b, sorted_a, sorted_b)) rep = kc;
         }
       }
       __syncthreads();  // s_ball is rewritten by the next chunk
@@ -648,15 +707,14 @@ __global__ void materialize_kernel(DevMask m, const unsigned long long *counters
     const int64_t row = part_row[k];
     const int32_t bm = (int32_t)(row / m.nq);
     const int64_t r = row % m.nq, c = part_col[k];
-    if (m.qseg != nullptr) {
-      stage_kv_ids(m, bm, c, s_kv);
-      __syncthreads();
-    }
+    const bool sorted = m.qseg != nullptr ? stage_kv_ids(m, bm, c, s_kv) : false;
     const int64_t i = r * m.bq + di;
     const int32_t sq = q_segment(m, bm, i);
+    int32_t ra = 0, rb = -1;
+    if (sorted) sorted_run(s_kv, block_keys(m, c), sq, ra, rb);
     uint32_t *bits = pattern_bits + (u * m.bq + di) * words;
     for (int32_t w = 0; w < words; ++w)
-      bits[w] = m.qseg != nullptr ? row_word_staged(m, i, sq, c * m.bk, c * m.bk + w * 32, s_kv)
+      bits[w] = m.qseg != nullptr ? row_word_staged(m, i, sq, c * m.bk, c * m.bk + w * 32, s_kv, sorted, ra, rb)
                                   : row_word(m, bm, i, sq, c * m.bk + w * 32);
     if (m.qseg != nullptr) __syncthreads();  // s_kv is restaged for the next pattern
   }
@@ -666,10 +724,19 @@ __global__ void materialize_kernel(DevMask m, const unsigned long long *counters
 // Rows sorted by descending active-block count, ties in ascending row order
 // (a stable counting sort): the attention kernel takes its work longest row
 // first.  One CTA; `hist` is a global scratch array of nk+1 counters.
-__device__ __forceinline__ void row_order_body(int64_t R, int64_t nk, const int32_t *row_cnt, int32_t *hist,
+constexpr int kOrderSmem = 4096;  // bins and rows the row order keeps in shared memory
+
+__device__ __forceinline__ void row_order_body(int64_t R, int64_t nk, const int32_t *row_cnt_g, int32_t *hist_g,
                                                int32_t *row_order) {
   __shared__ int buf[33];
+  __shared__ int s_hist[kOrderSmem], s_rows[kOrderSmem];
+  // bins and counts in shared memory when they fit (the global scratch otherwise)
+  const bool in_smem = nk + 1 <= kOrderSmem && R <= kOrderSmem;
+  int32_t *hist = in_smem ? s_hist : hist_g;
+  const int32_t *row_cnt = in_smem ? s_rows : row_cnt_g;
   for (int64_t b = threadIdx.x; b <= nk; b += blockDim.x) hist[b] = 0;
+  if (in_smem)
+    for (int64_t x = threadIdx.x; x < R; x += blockDim.x) s_rows[x] = row_cnt_g[x];
   __syncthreads();
   for (int64_t x = threadIdx.x; x < R; x += blockDim.x) atomicAdd(&hist[row_cnt[x]], 1);
   __syncthreads();
