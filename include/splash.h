@@ -107,9 +107,19 @@ typedef struct splash_mask_info splash_mask_info;
  *   cuda_stream stream for the build kernels.
  *   out         receives a new handle (set to NULL on error).
  *
- * Synchronisation: the call waits once on `cuda_stream` to read the number of
- * distinct patterns (it sizes the pattern buffer), so it is not capturable in
- * a CUDA graph.  The returned table is complete when the call returns.
+ * Synchronisation: the build kernels are queued on `cuda_stream` and the
+ * call returns without waiting, in the usual case: the pattern buffer is
+ * sized from a bound known before the build (band-only masks: at most
+ * 2 * (ceil((bq-1)/bk) + 1) partial blocks per q-block row, plus one block per
+ * row and the last row on a ragged grid; with segment IDs: the number of
+ * blocks the causal / window part alone leaves non-empty, since segments only
+ * remove pairs).  Only when that bound's bit-packed patterns would exceed
+ * 256 MB does the call wait once on `cuda_stream` for the exact pattern
+ * count; that path is not capturable in a CUDA graph.  The table may be used
+ * by later work on `cuda_stream` at once (work on another stream must wait
+ * for it); the totals reach the host only when splash_mask_info_counts or
+ * splash_mask_info_to_host asks for them.  A first build allocates the
+ * table's device memory (cudaMalloc, which synchronises the device).
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA, OOM; *out is NULL then.
  */
 splash_status splash_build_mask_info(const splash_mask_spec *spec, int64_t Lq, int64_t Lk,
@@ -135,12 +145,16 @@ splash_status splash_mask_info_shape(const splash_mask_info *mi, int32_t *batch_
                                      int64_t *nk, int32_t *bq, int32_t *bk);
 
 /*
- * splash_mask_info_counts -- totals of the table (host values, no sync):
+ * splash_mask_info_counts -- totals of the table:
  *   num_active    active blocks A (over all batch rows),
  *   num_partial   partial blocks,
  *   num_patterns  distinct partial patterns P,
  *   allowed_pairs allowed (query, key) pairs summed over the batch rows (the
- *                 "useful" entries of the score matrix).
+ *                 "useful" entries of the score matrix).  This output is an
+ *                 extension of the table the pages describe: the FLOP counts
+ *                 of the benchmark are taken from it.
+ * After an asynchronous build the first call waits for the build's kernels
+ * and copies the totals from the device (later calls read the host copy).
  * Any output may be NULL.
  */
 splash_status splash_mask_info_counts(const splash_mask_info *mi, int64_t *num_active,
@@ -151,7 +165,9 @@ splash_status splash_mask_info_counts(const splash_mask_info *mi, int64_t *num_a
  * splash_mask_info_to_host -- copy the table into caller-allocated HOST arrays
  * (synchronous).  Sizes: block_mask [B_mask*nq*nk], row_ptr [B_mask*nq + 1],
  * active_rows / active_cols / mask_next / bounds_start / bounds_end [A],
- * partial_mask_blocks [P*bq*bk].  Any pointer may be NULL to skip that array.
+ * partial_mask_blocks [P*bq*bk] (one byte per element, 1 = allowed; the
+ * device keeps the patterns bit-packed and they are expanded here).  Any
+ * pointer may be NULL to skip that array.
  */
 splash_status splash_mask_info_to_host(const splash_mask_info *mi, int8_t *block_mask,
                                        int32_t *row_ptr, int32_t *active_rows,
