@@ -1265,7 +1265,7 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
   }
   if (seg) {
     // the deferred list lives in rep_list, which scan_finalize_kernel fills later
-    count_deferred_kernel<<<sms * 4, kClassifyThreads, 0, stream>>>(m, mi->rep_list, NB, mi->block_mask,
+    count_deferred_kernel<<<sms * 8, kClassifyThreads, 0, stream>>>(m, mi->rep_list, NB, mi->block_mask,
                                                                    mi->row_cnt, mi->row_pcnt, mi->counters);
   }
   scan_order_kernel<<<1, 1024, 0, stream>>>(R, nk, mi->row_cnt, mi->row_pcnt, mi->row_ptr, mi->prow_ptr, mi->counters,
@@ -1273,10 +1273,12 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
   compact_kernel<<<(unsigned)((R + 7) / 8), 256, 0, stream>>>(
       m, R, mi->block_mask, mi->row_ptr, mi->prow_ptr, mi->active_rows, mi->active_cols,
       mi->mask_next, mi->bounds_start, mi->bounds_end, mi->part_row, mi->part_col, mi->part_g);
-  partial_hash_kernel<<<sms * 4, bq, 0, stream>>>(m, mi->counters, mi->part_row, mi->part_col,
-                                                  mi->part_hash);
-  dedup_kernel<<<sms * 4, kDedupThreads, 0, stream>>>(m, mi->counters, mi->part_row, mi->part_col,
-                                            mi->part_hash, mi->part_rep);
+  // one CTA per partial block up to eight per SM (the partial count is a
+  // device value; p_bound bounds it from the host)
+  const unsigned pgrid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(p_bound, (int64_t)sms * 8));
+  partial_hash_kernel<<<pgrid, bq, 0, stream>>>(m, mi->counters, mi->part_row, mi->part_col, mi->part_hash);
+  dedup_kernel<<<pgrid, kDedupThreads, 0, stream>>>(m, mi->counters, mi->part_row, mi->part_col, mi->part_hash,
+                                                    mi->part_rep);
   scan_finalize_kernel<<<1, 1024, 0, stream>>>(mi->counters, mi->part_g, mi->part_rep, mi->part_pidx, mi->mask_next,
                                                mi->rep_list);
   SPLASH_CUDA_TRY(cudaGetLastError());
@@ -1293,7 +1295,7 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
   }
   if ((st = reserve_patterns(P_cap)) != SPLASH_OK) return st;
   if (P_cap > 0) {
-    const unsigned grid = (unsigned)std::min<int64_t>(P_cap, async ? sms * 4 : 65535);
+    const unsigned grid = (unsigned)std::min<int64_t>(P_cap, async ? sms * 8 : 65535);
     materialize_kernel<<<grid, bq, 0, stream>>>(m, mi->counters, mi->cap_patterns, mi->rep_list, mi->part_row,
                                                 mi->part_col, mi->pattern_bits, err);
     SPLASH_CUDA_TRY(cudaGetLastError());
