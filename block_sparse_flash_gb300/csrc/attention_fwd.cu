@@ -35,7 +35,8 @@
 //     loads; warp 9 (as a whole warp, one elected lane issuing) issues the
 //     tcgen05 MMAs of both tiles when they share K/V (GQA), or lane 0 of
 //     warps 9 / 10 issues those of tile 0 / tile 1 (MHA);
-//     warp 11 only hands its registers to the softmax warpgroups;
+//     warp 11 decodes the CTA's work items ahead into a ring in shared
+//     memory (an item start costs the other roles a shared-memory read);
 //   * TMEM (512 columns): S_t / P_t at column 128t (P, bf16 pairs, overwrites
 //     the first half of S after it is read), O_t at 256 + 128t;
 //   * the exponent is base 2 (log2 e folded into the scale); a row's
@@ -53,6 +54,8 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
+#include <cstddef>
 #include <cmath>
 #include <mutex>
 
@@ -76,6 +79,11 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Upper bound on a block row's sum of exponentials (2^64): reaching it moves
 // the row's reference (no overflow in P, l or O).
 constexpr float kPMax = 1.8446744e19f;
+// Decoded work items handed from the decoder warp to the other roles through
+// a ring in shared memory (slots, and bytes per slot).
+constexpr int kItemRing = 8;
+constexpr int kItemBytes = 48;
+constexpr int kDecoderWarp = 11;
 
 template <int DQK, int DV, int BK>
 struct Cfg {
@@ -107,8 +115,11 @@ struct Cfg {
   static_assert(NCH == 0 || (QCH <= 3 && VCH <= 3), "release_chunks covers at most three chunks per tile");
   // barriers: q_full[2] q_empty[2] k_full[NK] k_empty[NK] v_full[NV] v_empty[NV]
   //           s_full[2] p_full[2] o_done[2] drain ch_full[NCH] ch_empty[NCH]
-  static constexpr int NBAR = 2 + 2 + 2 * NK + 2 * NV + 2 + 2 + 2 + 1 + 2 * NCH;
-  static constexpr int SMEM = 1024 + TILES + STAGE_BYTES + NBAR * 8 + 16;
+  //           item_full[kItemRing] item_empty[kItemRing]
+  static constexpr int NBAR = 2 + 2 + 2 * NK + 2 * NV + 2 + 2 + 2 + 1 + 2 * NCH + 2 * kItemRing;
+  // tiles, O staging, barriers, TMEM address + abort flag (16), item ring
+  static constexpr int SMEM = 1024 + TILES + STAGE_BYTES + NBAR * 8 + 16 + kItemRing * kItemBytes;
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, BK, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, DV, true);
 };
@@ -167,6 +178,9 @@ struct Item {
   int32_t split;
   bool act1, shared;
 };
+static_assert(sizeof(Item) <= kItemBytes, "item ring slot");
+// nb of the item after the CTA's last one
+constexpr int32_t kItemEnd = INT_MIN;
 
 // Work item w: rows in longest-first order; for a table shared by the batch,
 // each row expands into B batches; each (row, batch) into npairs head pairs;
@@ -291,7 +305,110 @@ struct Bars {
   __device__ __forceinline__ uint32_t ch_empty(uint32_t s) const {
     return base + 8u * (11 + 2 * C::NK + 2 * C::NV + C::NCH + s);
   }
+  __device__ __forceinline__ uint32_t item_full(uint32_t s) const {
+    return base + 8u * (11 + 2 * C::NK + 2 * C::NV + 2 * C::NCH + s);
+  }
+  __device__ __forceinline__ uint32_t item_empty(uint32_t s) const {
+    return base + 8u * (11 + 2 * C::NK + 2 * C::NV + 2 * C::NCH + kItemRing + s);
+  }
 };
+
+// The decoded work items of this CTA, in shared memory: an array of
+// kItemRing Item slots after the barriers (and the TMEM address / abort
+// words).  The decoder warp (one thread) writes item k into slot
+// k % kItemRing once every role has released the slot's previous item
+// (item_empty), then arrives on item_full; each role waits for item k, reads
+// the fields it uses (item_i32: volatile shared loads, so that only those stay
+// in registers) and releases the slot.
+template <class C>
+__device__ __forceinline__ uint32_t item_slot(const Bars<C> &bar, int64_t k) {
+  return bar.base + (uint32_t)(C::NBAR * 8 + 16) + (uint32_t)(k % kItemRing) * (uint32_t)sizeof(Item);
+}
+
+// A 32-bit field of an item slot (offsetof(Item, field)).
+__device__ __forceinline__ int32_t item_i32(uint32_t addr, size_t offset) {
+  int32_t v;
+  asm volatile("ld.volatile.shared.s32 %0, [%1];" : "=r"(v) : "r"(addr + (uint32_t)offset));
+  return v;
+}
+
+// The two flag bytes of an item (act1, shared), from one 32-bit load.
+__device__ __forceinline__ void item_flags(uint32_t addr, bool &act1, bool &shared) {
+  static_assert(offsetof(Item, shared) == offsetof(Item, act1) + 1 && offsetof(Item, act1) % 4 == 0, "flag bytes");
+  const int32_t w = item_i32(addr, offsetof(Item, act1));
+  act1 = (w & 0xff) != 0;
+  shared = ((w >> 8) & 0xff) != 0;
+}
+
+// Waits for item k (one thread).  Returns its slot address, or 0 after the
+// CTA's last item (the slot is then released) or with ok = false; the caller
+// releases the slot with release_item once it has read the fields.
+template <class C>
+__device__ __forceinline__ uint32_t hold_item(const Bars<C> &bar, int64_t k, bool &ok, volatile int *abort,
+                                              uint64_t timeout_ns) {
+  const uint32_t s = (uint32_t)(k % kItemRing);
+  ok = mbar_wait(bar.item_full(s), (uint32_t)(k / kItemRing) & 1u, abort, timeout_ns);
+  if (!ok) return 0u;
+  const uint32_t addr = item_slot(bar, k);
+  if (item_i32(addr, offsetof(Item, nb)) == kItemEnd) {
+    mbar_arrive(bar.item_empty(s));
+    return 0u;
+  }
+  return addr;
+}
+
+template <class C>
+__device__ __forceinline__ void release_item(const Bars<C> &bar, int64_t k) {
+  mbar_arrive(bar.item_empty((uint32_t)(k % kItemRing)));
+}
+
+// The same for a whole, converged warp (one arrival per warp).
+template <class C>
+__device__ __forceinline__ uint32_t hold_item_warp(const Bars<C> &bar, int64_t k, bool &ok, volatile int *abort,
+                                                   uint64_t timeout_ns) {
+  const uint32_t s = (uint32_t)(k % kItemRing);
+  ok = __all_sync(0xffffffffu, mbar_wait(bar.item_full(s), (uint32_t)(k / kItemRing) & 1u, abort, timeout_ns));
+  if (!ok) return 0u;
+  const uint32_t addr = item_slot(bar, k);
+  if (item_i32(addr, offsetof(Item, nb)) == kItemEnd) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar.item_empty(s));
+    return 0u;
+  }
+  return addr;
+}
+
+template <class C>
+__device__ __forceinline__ void release_item_warp(const Bars<C> &bar, int64_t k) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar.item_empty((uint32_t)(k % kItemRing)));
+}
+
+// The decoder (one thread of warp kDecoderWarp): decodes this CTA's items
+// ahead of the roles that use them, so that an item start costs them a few
+// shared-memory reads instead of the table loads and index arithmetic.
+template <class C, bool TALL>
+__device__ __noinline__ void run_decoder(const FwdParams &p, const Bars<C> bar, Item *items, volatile int *abort) {
+  bool ok = true;
+  for (int64_t k = 0;; ++k) {
+    const uint32_t s = (uint32_t)(k % kItemRing);
+    if (k >= kItemRing &&
+        !(ok = mbar_wait(bar.item_empty(s), (uint32_t)((k / kItemRing) - 1) & 1u, abort, p.timeout_ns)))
+      break;
+    const int64_t w = item_of_round(p, k);
+    Item it;
+    if (w < 0) {
+      it = Item{};
+      it.nb = kItemEnd;
+    } else {
+      it = decode_item<TALL>(p, w);
+    }
+    items[s] = it;
+    mbar_arrive(bar.item_full(s));  // release: the item's stores come first
+    if (w < 0) break;
+  }
+  if (!ok) raise_error(p, abort, SPLASH_DEV_TIMEOUT_PRODUCER);
+}
 
 // Loads one K or V tile (CH boxes of 64 columns x BK rows) into the next slot
 // of a ring of NS slots of BYTES bytes; waits (bounded) for the slot to be
@@ -330,9 +447,19 @@ __device__ __noinline__ void run_producer(const FwdParams &p, const CUtensorMap 
   uint32_t kcnt = 0, vcnt = 0, q0 = 0, q1 = 0;
   bool ok = true;
   for (int64_t k = 0; ok; ++k) {
-    const int64_t w = item_of_round(p, k);
-    if (w < 0) break;
-    const Item it = decode_item<TALL>(p, w);
+    const uint32_t ia = hold_item(bar, k, ok, abort, p.timeout_ns);
+    if (ia == 0u) break;
+    Item it;
+    it.nb = item_i32(ia, offsetof(Item, nb));
+    it.g0 = item_i32(ia, offsetof(Item, g0));
+    it.b = item_i32(ia, offsetof(Item, b));
+    it.h0 = item_i32(ia, offsetof(Item, h0));
+    it.h1 = item_i32(ia, offsetof(Item, h1));
+    it.kvh0 = item_i32(ia, offsetof(Item, kvh0));
+    it.kvh1 = item_i32(ia, offsetof(Item, kvh1));
+    it.qrow = item_i32(ia, offsetof(Item, qrow));
+    item_flags(ia, it.act1, it.shared);
+    release_item(bar, k);
     if (it.nb <= 0) continue;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
@@ -502,9 +629,12 @@ __device__ __noinline__ void run_mma(const FwdParams &p, uint32_t tmem, uint32_t
   const uint32_t tS = tmem + 128u * t, tO = tmem + 256u + 128u * t;
   const uint32_t sQt = sQ + t * C::Q_BYTES;
   for (int64_t k = 0; ok; ++k) {
-    const int64_t w = item_of_round(p, k);
-    if (w < 0) break;
-    const Item it = decode_item<TALL>(p, w);
+    const uint32_t ia = hold_item(bar, k, ok, abort, p.timeout_ns);
+    if (ia == 0u) break;
+    Item it;
+    it.nb = item_i32(ia, offsetof(Item, nb));
+    item_flags(ia, it.act1, it.shared);
+    release_item(bar, k);
     if (it.nb <= 0) continue;
     const bool mine = (t == 0) || it.act1;
     const bool two_kv = it.act1 && !it.shared;
@@ -603,9 +733,12 @@ __device__ __forceinline__ void run_mma_pair(const FwdParams &p, uint32_t tmem, 
   bool ok = true;
   const uint32_t tS0 = tmem, tS1 = tmem + 128u, tO0 = tmem + 256u, tO1 = tmem + 384u;
   for (int64_t k = 0; ok; ++k) {
-    const int64_t w = item_of_round(p, k);
-    if (w < 0) break;
-    const Item it = decode_item<TALL>(p, w);
+    const uint32_t ia = hold_item_warp(bar, k, ok, abort, p.timeout_ns);
+    if (ia == 0u) break;
+    Item it;
+    it.nb = item_i32(ia, offsetof(Item, nb));
+    item_flags(ia, it.act1, it.shared);
+    release_item_warp(bar, k);
     if (it.nb <= 0) continue;
     const bool two = it.act1;
     const bool two_kv = it.act1 && !it.shared;
@@ -731,9 +864,19 @@ __device__ __noinline__ void run_producer_chunked(const FwdParams &p, const CUte
   uint32_t n = 0, armed = 0, arm_par = 0, q0 = 0, q1 = 0;
   bool ok = true;
   for (int64_t k = 0; ok; ++k) {
-    const int64_t w = item_of_round(p, k);
-    if (w < 0) break;
-    const Item it = decode_item<true>(p, w);
+    const uint32_t ia = hold_item(bar, k, ok, abort, p.timeout_ns);
+    if (ia == 0u) break;
+    Item it;
+    it.nb = item_i32(ia, offsetof(Item, nb));
+    it.g0 = item_i32(ia, offsetof(Item, g0));
+    it.b = item_i32(ia, offsetof(Item, b));
+    it.h0 = item_i32(ia, offsetof(Item, h0));
+    it.h1 = item_i32(ia, offsetof(Item, h1));
+    it.kvh0 = item_i32(ia, offsetof(Item, kvh0));
+    it.kvh1 = item_i32(ia, offsetof(Item, kvh1));
+    it.qrow = item_i32(ia, offsetof(Item, qrow));
+    item_flags(ia, it.act1, it.shared);
+    release_item(bar, k);
     if (it.nb <= 0) continue;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
@@ -828,15 +971,19 @@ __device__ __forceinline__ void release_chunks(const Bars<C> &bar, uint32_t firs
 // or tile 0's when the lower half of the block is all padding).
 template <class C, int BK>
 __device__ __forceinline__ void run_mma_pair_chunked(const FwdParams &p, uint32_t tmem, uint32_t sQ, uint32_t ring,
-                                                     const Bars<C> bar, volatile int *abort, const uint32_t leader) {
+                                                     const Bars<C> bar, volatile int *abort,
+                                                     const uint32_t leader) {
   const uint64_t tmo = p.timeout_ns;
   uint32_t n = 0, fwait = 0, q0 = 0, q1 = 0, p0 = 0, p1 = 0;
   bool ok = true;
   const uint32_t tS0 = tmem, tS1 = tmem + 128u, tO0 = tmem + 256u, tO1 = tmem + 384u;
   for (int64_t k = 0; ok; ++k) {
-    const int64_t w = item_of_round(p, k);
-    if (w < 0) break;
-    const Item it = decode_item<true>(p, w);
+    const uint32_t ia = hold_item_warp(bar, k, ok, abort, p.timeout_ns);
+    if (ia == 0u) break;
+    Item it;
+    it.nb = item_i32(ia, offsetof(Item, nb));
+    item_flags(ia, it.act1, it.shared);
+    release_item_warp(bar, k);
     if (it.nb <= 0) continue;
     const bool two = it.act1;
     // S_0(0) [and S_1(0)]: Q tiles and the first K tile
@@ -1011,6 +1158,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   const Bars<C> bar{smem_u32(bars)};
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::TILES + C::STAGE_BYTES + C::NBAR * 8);
   volatile int *abort = reinterpret_cast<volatile int *>(smem + C::TILES + C::STAGE_BYTES + C::NBAR * 8 + 4);
+  Item *items = reinterpret_cast<Item *>(smem + C::TILES + C::STAGE_BYTES + C::NBAR * 8 + 16);  // the item ring
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -1039,6 +1187,11 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     for (int s = 0; s < C::NCH; ++s) {
       mbar_init(bar.ch_full(s), 1);   // the producer's arm of the tile whose first chunk is here
       mbar_init(bar.ch_empty(s), 1);  // the (single) issuer's release of the chunk
+    }
+    for (int s = 0; s < kItemRing; ++s) {
+      mbar_init(bar.item_full(s), 1);  // the decoder
+      // released by the producer, the MMA issuer(s) and the eight softmax warps
+      mbar_init(bar.item_empty(s), 1 + (p.dual_issuer ? 2 : 1) + 8);
     }
     *abort = 0;
     mbar_fence_init();
@@ -1071,6 +1224,8 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     } else if (warp == kMmaWarp) {
       run_mma_pair<C, BK, TALL>(p, tmem, sQ, sK, sV, bar, abort, elect_one_sync());
     }
+  } else if (warp == kDecoderWarp) {
+    if (lane == 0) run_decoder<C, TALL>(p, bar, items, abort);
   }
   } else {
   // ============================================================ warpgroups 0, 1
@@ -1088,15 +1243,21 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     uint32_t scnt = 0, ocnt = 0;
     bool ok = true;
     for (int64_t k = 0; ok; ++k) {
-      const int64_t w = item_of_round(p, k);
-      if (w < 0) break;
-      const Item it = decode_item<TALL>(p, w);
-      if (t == 1 && !it.act1) continue;
-      const int32_t qpos = it.qrow * p.bq + prow;  // < 2^31: nq * bq <= 65535 * 256
+      // the fields this warp needs, read from the ring slot, which is then released
+      const uint32_t ia = hold_item_warp(bar, k, ok, abort, p.timeout_ns);
+      if (ia == 0u) break;
+      const bool it_act1 = (item_i32(ia, offsetof(Item, act1) & ~(size_t)3) >> (8 * (offsetof(Item, act1) & 3))) & 0xff;
+      const int32_t it_g0 = item_i32(ia, offsetof(Item, g0)), it_nb = item_i32(ia, offsetof(Item, nb));
+      const int32_t it_qrow = item_i32(ia, offsetof(Item, qrow)), it_b = item_i32(ia, offsetof(Item, b));
+      const int32_t it_h = item_i32(ia, t ? offsetof(Item, h1) : offsetof(Item, h0));
+      const int32_t it_split = item_i32(ia, offsetof(Item, split));
+      release_item_warp(bar, k);
+      if (t == 1 && !it_act1) continue;
+      const int32_t qpos = it_qrow * p.bq + prow;  // < 2^31: nq * bq <= 65535 * 256
       float m_ref = p.use_mle ? p.mle_ref : -INFINITY;  // running reference (log2 units)
       float l = 0.f;
-      for (int32_t g = 0; g < it.nb && ok; ++g) {
-        int32_t mn = p.mask_next[it.g0 + g];
+      for (int32_t g = 0; g < it_nb && ok; ++g) {
+        int32_t mn = p.mask_next[it_g0 + g];
         if (mn >= p.num_patterns) {
           atomicOr(p.err, SPLASH_DEV_BAD_TABLE);
           mn = -1;
@@ -1105,7 +1266,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         const bool need_mask = partial || !row_valid;
         uint32_t bits[BK / 32];
         if (partial && row_valid) {
-          partial_bits<BK, BAND>(p, mn, prow, qpos, it.g0 + g, bits);
+          partial_bits<BK, BAND>(p, mn, prow, qpos, it_g0 + g, bits);
         } else {
 #pragma unroll
           for (int x = 0; x < BK / 32; ++x) bits[x] = row_valid ? 0xffffffffu : 0u;
@@ -1209,7 +1370,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             if constexpr (BAND) {
               uint32_t rb[BK / 32];
               if (partial && row_valid) {
-                partial_bits<BK, BAND>(p, mn, prow, qpos, it.g0 + g, rb);
+                partial_bits<BK, BAND>(p, mn, prow, qpos, it_g0 + g, rb);
               } else {
 #pragma unroll
                 for (int x = 0; x < BK / 32; ++x) rb[x] = row_valid ? 0xffffffffu : 0u;
@@ -1266,11 +1427,11 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       }
       if (!ok) break;
       // ---- epilogue: O / l and the LSE
-      const int32_t h = t ? it.h1 : it.h0;
-      const int64_t orow = ((int64_t)it.b * p.Hq + h) * p.Lq + qpos;
+      const int32_t h = it_h;
+      const int64_t orow = ((int64_t)it_b * p.Hq + h) * p.Lq + qpos;
       // rows past a ragged Lq are padding: computed (all masked), never stored
       const bool row_out = row_valid && qpos < p.Lq;
-      if (it.nb > 0) {
+      if (it_nb > 0) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar.o_done(t), ocnt & 1, abort, p.timeout_ns));
         if (!ok) break;
         ++ocnt;
@@ -1279,11 +1440,11 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       const float inv = l > 0.f ? 1.f / l : 0.f;
       if (p.o_part != nullptr) {
         // split-KV partial: the split's normalized O in fp32 (32-byte stores)
-        float *dst = p.o_part + ((int64_t)it.split * p.part_rows + orow) * DV;
+        float *dst = p.o_part + ((int64_t)it_split * p.part_rows + orow) * DV;
 #pragma unroll
         for (int c = 0; c < DV / 32; ++c) {
           uint32_t r[32];
-          if (it.nb > 0) {
+          if (it_nb > 0) {
             tmem_ld32(tO + 32u * c, r);
             tmem_wait_ld();
             reg_fence32(r);
@@ -1310,7 +1471,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
 #pragma unroll
         for (int hh = 0; hh < DV / 64; ++hh) {
           uint32_t r0[32], r1[32];
-          if (it.nb > 0) {
+          if (it_nb > 0) {
             tmem_ld32(tO + 64u * hh, r0);
             tmem_ld32(tO + 64u * hh + 32u, r1);
             tmem_wait_ld();
@@ -1340,7 +1501,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             if (lane == 0) {
               // O viewed as [B*Hq][Lq][DV]: rows past a ragged Lq fall outside
               // the tensor and the store clips them
-              tma_store_3d(&tmO, stage, 64 * hh, it.qrow * p.bq + wrow, it.b * p.Hq + h);
+              tma_store_3d(&tmO, stage, 64 * hh, it_qrow * p.bq + wrow, it_b * p.Hq + h);
               bulk_commit_group();
             }
           }
@@ -1350,7 +1511,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
 #pragma unroll
       for (int c = 0; c < DV / 32; ++c) {
         uint32_t r[32];
-        if (it.nb > 0) {
+        if (it_nb > 0) {
           tmem_ld32(tO + 32u * c, r);
           tmem_wait_ld();
           reg_fence32(r);
@@ -1374,7 +1535,7 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       if (row_out) {
         const float lse_v = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
         if (p.o_part != nullptr)
-          p.lse_part[(int64_t)it.split * p.part_rows + orow] = lse_v;
+          p.lse_part[(int64_t)it_split * p.part_rows + orow] = lse_v;
         else
           p.lse[orow] = lse_v;
       }
