@@ -329,7 +329,7 @@ def time_forward_steps(bsf, w, inp, dev, K, warmup, flush):
         mi.rebuild(spec, w.q_len, w.L, w.bq, w.bk)
         if e:
             e[1].record()
-        bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, out=out, lse=lse)
+        bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, seg, seg, out=out, lse=lse)
         if e:
             e[2].record()
     torch.cuda.synchronize()
@@ -364,7 +364,7 @@ def per_workload(bsf, dev, K, warmup, flush, peak, indices=(3, 4, 5)):
     return res
 
 
-def sustained_figures(bsf, w, q, k, v, mi, out, lse, dev, seconds, peaks, local):
+def sustained_figures(bsf, w, q, k, v, mi, out, lse, dev, seconds, peaks, local, seg=None):
     """Back-to-back attention calls for `seconds` (no flush, no rebuild) with
     the clock sampler running: executed TFLOP/s against the sustained cuBLAS
     peak, the median SM clock of the samples, and the tensor fraction at that
@@ -376,7 +376,7 @@ def sustained_figures(bsf, w, q, k, v, mi, out, lse, dev, seconds, peaks, local)
     # calls per chunk from one timed call
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
-    bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, out=out, lse=lse)
+    bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, seg, seg, out=out, lse=lse)
     b.record()
     torch.cuda.synchronize()
     per_chunk = max(1, int(50.0 / max(a.elapsed_time(b), 1e-3)))  # ~50 ms chunks
@@ -388,7 +388,7 @@ def sustained_figures(bsf, w, q, k, v, mi, out, lse, dev, seconds, peaks, local)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         for _ in range(per_chunk):
-            bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, out=out, lse=lse)
+            bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, seg, seg, out=out, lse=lse)
         b.record()
         chunks.append((a, b))
         calls += per_chunk
@@ -475,14 +475,15 @@ def run_ours(args):
         if attn_events:
             attn_events[0].record()
         if S > 1:
-            bsf.attention_fwd_split(q, k, v, mi, w.scale, w.softcap, S, o_part=o_part, lse_part=lse_part)
+            bsf.attention_fwd_split(q, k, v, mi, w.scale, w.softcap, S, seg, seg, o_part=o_part, lse_part=lse_part)
             if merge_events:
                 merge_events[0].record()
             bsf.attention_merge(o_part, lse_part, out=out, lse=lse)
             if merge_events:
                 merge_events[1].record()
         else:
-            bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, out=out, lse=lse, max_logit=args.max_logit)
+            bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, seg, seg, out=out, lse=lse,
+                              max_logit=args.max_logit)
         if attn_events:
             attn_events[1].record()
 
@@ -575,7 +576,8 @@ def run_ours(args):
     if e2e:
         result["e2e"] = e2e
     if world == 1 and S == 1 and args.max_logit is None and args.sustain_s > 0:
-        result["sustained"] = sustained_figures(bsf, w, q, k, v, mi, out, lse, dev, args.sustain_s, peaks, local)
+        result["sustained"] = sustained_figures(bsf, w, q, k, v, mi, out, lse, dev, args.sustain_s, peaks, local,
+                                                seg)
     if world == 1 and not shard and args.workload == 2 and S == 1 and args.bq is None \
             and args.max_logit is None and args.pattern_source == "stored" and not args.no_per_workload:
         pw = per_workload(bsf, dev, K, args.warmup, flush, peak)
@@ -639,12 +641,12 @@ def run_e2e(bsf, w, inp, spec, mi, dev, K, world, job_useful, max_logit=None):
         if max_logit is None:
             # the library's host-buffer entry: copies and attention pipelined in chunks
             bsf.attention_fwd_host(qh, kh, vh, mi, w.scale, w.softcap, out_host=outh, lse_host=lseh,
-                                   q=q, k=k, v=v, out=out, lse=lse)
+                                   q=q, k=k, v=v, out=out, lse=lse, q_segment_ids=seg, kv_segment_ids=seg)
         else:
             q.copy_(qh, non_blocking=True)
             k.copy_(kh, non_blocking=True)
             v.copy_(vh, non_blocking=True)
-            bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, out=out, lse=lse, max_logit=max_logit)
+            bsf.attention_fwd(q, k, v, mi, w.scale, w.softcap, seg, seg, out=out, lse=lse, max_logit=max_logit)
             outh.copy_(out, non_blocking=True)
             lseh.copy_(lse, non_blocking=True)
         b.record()

@@ -192,7 +192,8 @@ class MaskInfo:
 
     def set_pattern_source(self, source: str):
         """'stored' (default) or 'positions': the forward computes partial
-        blocks' masks from positions (tables without segment IDs)."""
+        blocks' masks from positions, and for a table built with segment IDs
+        from the segment arrays, which every forward call must then pass."""
         code = {"stored": 0, "positions": 1}[source]
         _check(lib().splash_mask_info_set_pattern_source(self.handle, code), "splash_mask_info_set_pattern_source")
 

@@ -201,7 +201,6 @@ splash_status splash_mask_info_counts(const splash_mask_info *mi, int64_t *num_a
 splash_status splash_mask_info_set_pattern_source(splash_mask_info *mi, int32_t source) {
   if (mi == nullptr || (source != SPLASH_PATTERNS_STORED && source != SPLASH_PATTERNS_FROM_POSITIONS))
     return SPLASH_ERR_INVALID_ARG;
-  if (source == SPLASH_PATTERNS_FROM_POSITIONS && mi->has_segments) return SPLASH_ERR_UNSUPPORTED;
   mi->patterns_from_positions = source == SPLASH_PATTERNS_FROM_POSITIONS ? 1 : 0;
   return SPLASH_OK;
 }
@@ -282,13 +281,12 @@ splash_status splash_attention_fwd(const void *q, const void *k, const void *v, 
                                    const int32_t *q_segment_ids, const int32_t *kv_segment_ids,
                                    const splash_mask_info *mi, float scale, float softcap, void *out,
                                    float *lse, void *cuda_stream) {
-  (void)q_segment_ids;
-  (void)kv_segment_ids;
   uint32_t *err = nullptr;
   splash_status st = check_attention(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, out, lse, &err);
   if (st != SPLASH_OK) return st;
-  return splash_attention_fwd_launch(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, NAN, out, lse,
-                                     1, nullptr, nullptr, static_cast<cudaStream_t>(cuda_stream), err);
+  return splash_attention_fwd_launch(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, q_segment_ids, kv_segment_ids, mi, scale,
+                                     softcap, NAN, out, lse, 1, nullptr, nullptr,
+                                     static_cast<cudaStream_t>(cuda_stream), err);
 }
 
 splash_status splash_attention_fwd_mle(const void *q, const void *k, const void *v, int32_t B, int32_t Hq,
@@ -296,14 +294,13 @@ splash_status splash_attention_fwd_mle(const void *q, const void *k, const void 
                                        const int32_t *q_segment_ids, const int32_t *kv_segment_ids,
                                        const splash_mask_info *mi, float scale, float softcap, float max_logit,
                                        void *out, float *lse, void *cuda_stream) {
-  (void)q_segment_ids;
-  (void)kv_segment_ids;
   if (!std::isfinite(max_logit)) return SPLASH_ERR_INVALID_ARG;
   uint32_t *err = nullptr;
   splash_status st = check_attention(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, out, lse, &err);
   if (st != SPLASH_OK) return st;
-  return splash_attention_fwd_launch(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, max_logit, out,
-                                     lse, 1, nullptr, nullptr, static_cast<cudaStream_t>(cuda_stream), err);
+  return splash_attention_fwd_launch(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, q_segment_ids, kv_segment_ids, mi, scale,
+                                     softcap, max_logit, out, lse, 1, nullptr, nullptr,
+                                     static_cast<cudaStream_t>(cuda_stream), err);
 }
 
 splash_status splash_attention_fwd_host(const void *q_host, const void *k_host, const void *v_host, int32_t B,
@@ -312,15 +309,14 @@ splash_status splash_attention_fwd_host(const void *q_host, const void *k_host, 
                                         const splash_mask_info *mi, float scale, float softcap, void *out_host,
                                         float *lse_host, void *q_dev, void *k_dev, void *v_dev, void *out_dev,
                                         float *lse_dev, void *cuda_stream) {
-  (void)q_segment_ids;
-  (void)kv_segment_ids;
   if (q_host == nullptr || k_host == nullptr || v_host == nullptr || out_host == nullptr || lse_host == nullptr)
     return SPLASH_ERR_INVALID_ARG;
   uint32_t *err = nullptr;
   splash_status st =
       check_attention(q_dev, k_dev, v_dev, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, out_dev, lse_dev, &err);
   if (st != SPLASH_OK) return st;
-  return splash_attention_fwd_host_launch(q_host, k_host, v_host, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap,
+  return splash_attention_fwd_host_launch(q_host, k_host, v_host, B, Hq, Hkv, Lq, Lk, dqk, dv, q_segment_ids,
+                                          kv_segment_ids, mi, scale, softcap,
                                           out_host, lse_host, q_dev, k_dev, v_dev, out_dev, lse_dev, 8,
                                           static_cast<cudaStream_t>(cuda_stream), err);
 }
@@ -359,17 +355,15 @@ splash_status splash_attention_fwd_split(const void *q, const void *k, const voi
                                          const int32_t *q_segment_ids, const int32_t *kv_segment_ids,
                                          const splash_mask_info *mi, float scale, float softcap,
                                          int32_t num_splits, float *o_part, float *lse_part, void *cuda_stream) {
-  (void)q_segment_ids;
-  (void)kv_segment_ids;
   if (num_splits < 1 || num_splits > SPLASH_MAX_SPLITS) return SPLASH_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(o_part) & 31u) != 0) return SPLASH_ERR_INVALID_ARG;
   uint32_t *err = nullptr;
   splash_status st =
       check_attention(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, o_part, lse_part, &err);
   if (st != SPLASH_OK) return st;
-  return splash_attention_fwd_launch(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, mi, scale, softcap, NAN, nullptr,
-                                     nullptr, num_splits, o_part, lse_part, static_cast<cudaStream_t>(cuda_stream),
-                                     err);
+  return splash_attention_fwd_launch(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, q_segment_ids, kv_segment_ids, mi, scale,
+                                     softcap, NAN, nullptr, nullptr, num_splits, o_part, lse_part,
+                                     static_cast<cudaStream_t>(cuda_stream), err);
 }
 
 splash_status splash_attention_merge(const float *o_part, const float *lse_part, int32_t num_splits, int64_t rows,

@@ -142,9 +142,11 @@ struct FwdParams {
   const uint32_t *pattern_bits;
   const int32_t *row_order;
   // partial blocks' element masks computed from positions instead of read
-  // from pattern_bits (masks without segment IDs): causal / window bounds
+  // from pattern_bits: causal / window bounds, and with segment IDs the
+  // arrays [nbm][Lq] and [nbm][Lk] the table was built from
   int32_t band_bits, band_causal;
   int64_t band_wl, band_wr;
+  const int32_t *seg_q, *seg_kv;
   int64_t num_patterns;
   float scale_log2;   // scale * log2(e)             (no soft cap)
   float cap_inner;    // scale / cap                 (soft cap)
@@ -1096,10 +1098,14 @@ __device__ __forceinline__ f32x2 tanh_series2(f32x2 s, f32x2 k) {
 // of the mask: causal and window bounds, and the padding of ragged lengths --
 // "Pallas Kernels and Splash Attention" §6.6: masks can be computed in the
 // kernel from q / kv positions instead of stored patterns).
-template <int BK, bool BAND>
+// Where a partial block's element mask comes from: the stored pattern, or
+// positions (the band part), or positions and segment IDs.
+constexpr int kPatStored = 0, kPatBand = 1, kPatBandSeg = 2;
+
+template <int BK, int PM>
 __device__ __forceinline__ void partial_bits(const FwdParams &p, int32_t mn, int row, int64_t qpos, int32_t g_idx,
                                              uint32_t (&bits)[BK / 32]) {
-  if constexpr (BAND) {
+  if constexpr (PM != kPatStored) {
     const int64_t c0 = (int64_t)__ldg(p.active_cols + g_idx) * BK;
     int64_t lo = c0, hi = min(c0 + BK - 1, p.Lk - 1);
     if (p.band_causal) hi = min(hi, qpos);
@@ -1119,6 +1125,57 @@ __device__ __forceinline__ void partial_bits(const FwdParams &p, int32_t mn, int
   }
 }
 
+// Segment part of a partial block's mask ("Pallas Kernels and Splash
+// Attention" §6.4, §6.6): key j is allowed for the query only if their
+// segment IDs are equal.  Lane l holds kid[x], the ID of key 32x + l of the
+// block, so a warp ballot on "ID == the query's ID" is word x of the row's
+// mask for every lane that has that query ID.  The usual case, all 32 rows of
+// the warp in one segment, takes one ballot per word; a warp whose rows span
+// several segments takes one more pass per further query ID.  Warp-collective:
+// every lane of the warp calls it with the same control flow.
+// The key IDs of active block g_idx (kid) and the query's own ID (returned)
+// for batch row b; rows past Lq and keys past Lk read nothing (the band part
+// masks them).
+template <int BK>
+__device__ __forceinline__ int32_t seg_kids(const FwdParams &p, int32_t b, int32_t qpos, int32_t g_idx, int lane,
+                                            int32_t (&kid)[BK / 32]) {
+  const int64_t sr = p.nbm > 1 ? b : 0;  // segment-array row
+  const int64_t c0 = (int64_t)__ldg(p.active_cols + g_idx) * BK;
+#pragma unroll
+  for (int x = 0; x < BK / 32; ++x) {
+    const int64_t kp = c0 + 32 * x + lane;
+    kid[x] = kp < p.Lk ? __ldg(p.seg_kv + sr * p.Lk + kp) : 0;
+  }
+  return qpos < p.Lq ? __ldg(p.seg_q + sr * p.Lq + qpos) : 0;
+}
+
+template <int BK>
+__device__ __forceinline__ void seg_and(uint32_t (&bits)[BK / 32], const int32_t (&kid)[BK / 32], int32_t qseg) {
+  const int32_t q0 = __shfl_sync(0xffffffffu, qseg, 0);
+  if (__all_sync(0xffffffffu, qseg == q0)) {
+#pragma unroll
+    for (int x = 0; x < BK / 32; ++x) bits[x] &= __ballot_sync(0xffffffffu, kid[x] == q0);
+    return;
+  }
+  // rows of several segments (a warp at a segment boundary): one ballot per
+  // word for each distinct query ID, lane 0's first
+  uint32_t w[BK / 32];
+#pragma unroll
+  for (int x = 0; x < BK / 32; ++x) w[x] = __ballot_sync(0xffffffffu, kid[x] == q0);
+  uint32_t done = __ballot_sync(0xffffffffu, qseg == q0);
+  while (done != 0xffffffffu) {  // warp-uniform
+    const int32_t qv = __shfl_sync(0xffffffffu, qseg, __ffs(~done) - 1);
+#pragma unroll
+    for (int x = 0; x < BK / 32; ++x) {
+      const uint32_t b = __ballot_sync(0xffffffffu, kid[x] == qv);
+      w[x] = qseg == qv ? b : w[x];
+    }
+    done |= __ballot_sync(0xffffffffu, qseg == qv);
+  }
+#pragma unroll
+  for (int x = 0; x < BK / 32; ++x) bits[x] &= w[x];
+}
+
 // s_j <- 2^(s_j * mul - sub) in place (packed argument), returns the row sum
 // (eight independent partial sums).
 template <int N>
@@ -1136,12 +1193,13 @@ __device__ __forceinline__ float exp2_block(float (&s)[N], float mul, float sub)
   return t.x + t.y;
 }
 
-// BAND: partial blocks' masks computed from positions (a separate
-// instantiation, so that the default stored-pattern loop is unchanged).
+// PM: partial blocks' masks from the stored patterns, or computed from
+// positions (and segment IDs) -- separate instantiations, so that the default
+// stored-pattern loop is unchanged.
 // CAP: the tanh soft cap, a compile-time flag so that the kernels without
 // it carry none of its code (the fused cap + exponent loop changes their
 // register allocation).
-template <int DQK, int DV, int BK, bool BAND, bool TALL, bool CAP>
+template <int DQK, int DV, int BK, int PM, bool TALL, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
 splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -1266,10 +1324,19 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         const bool need_mask = partial || !row_valid;
         uint32_t bits[BK / 32];
         if (partial && row_valid) {
-          partial_bits<BK, BAND>(p, mn, prow, qpos, it_g0 + g, bits);
+          partial_bits<BK, PM>(p, mn, prow, qpos, it_g0 + g, bits);
         } else {
 #pragma unroll
           for (int x = 0; x < BK / 32; ++x) bits[x] = row_valid ? 0xffffffffu : 0u;
+        }
+        // the segment part, before the wait for S (whose latency hides the
+        // key IDs' loads); partial is the same for every lane of the warp
+        if constexpr (PM == kPatBandSeg) {
+          if (partial) {
+            int32_t kid[BK / 32];
+            const int32_t qseg = seg_kids<BK>(p, it_b, qpos, it_g0 + g, lane, kid);
+            seg_and<BK>(bits, kid, qseg);
+          }
         }
         // all lanes wait; the outcome is made warp-uniform before the
         // warp-collective TMEM accesses
@@ -1349,7 +1416,23 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
           // their reference to the block's maximum, and every lane
           // recomputes its row (for the others this gives the values they
           // already have, up to rounding); nothing from the main path stays
-          // live across this branch but the references.
+          // live across this branch but the references.  (With segment IDs
+          // the row's mask words are formed again first, before S occupies
+          // the registers.)
+          [[maybe_unused]] uint32_t rs[PM == kPatBandSeg ? BK / 32 : 1];
+          if constexpr (PM == kPatBandSeg) {
+            if (partial && row_valid) {
+              partial_bits<BK, PM>(p, mn, prow, qpos, it_g0 + g, rs);
+            } else {
+#pragma unroll
+              for (int x = 0; x < BK / 32; ++x) rs[x] = row_valid ? 0xffffffffu : 0u;
+            }
+            if (partial) {
+              int32_t kr[BK / 32];
+              const int32_t qseg = seg_kids<BK>(p, it_b, qpos, it_g0 + g, lane, kr);
+              seg_and<BK>(rs, kr, qseg);
+            }
+          }
           {
             uint32_t r[BK / 32][32];
 #pragma unroll
@@ -1367,10 +1450,16 @@ splash_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             for (int j = 0; j < BK; ++j) s[j] = tanh_identity(s[j] * p.cap_inner);
           }
           if (need_mask) {
-            if constexpr (BAND) {
+            if constexpr (PM == kPatBandSeg) {
+#pragma unroll
+              for (int x = 0; x < BK / 32; ++x) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) s[x * 32 + j] = ((rs[x] >> j) & 1u) ? s[x * 32 + j] : -INFINITY;
+              }
+            } else if constexpr (PM == kPatBand) {
               uint32_t rb[BK / 32];
               if (partial && row_valid) {
-                partial_bits<BK, BAND>(p, mn, prow, qpos, it_g0 + g, rb);
+                partial_bits<BK, PM>(p, mn, prow, qpos, it_g0 + g, rb);
               } else {
 #pragma unroll
                 for (int x = 0; x < BK / 32; ++x) rb[x] = row_valid ? 0xffffffffu : 0u;
@@ -1610,7 +1699,7 @@ bool make_map_3d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t row
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int DQK, int DV, int BK, bool BAND, bool TALL, bool CAP>
+template <int DQK, int DV, int BK, int PM, bool TALL, bool CAP>
 splash_status launch(const void *q, const void *k, const void *v, const FwdParams &prm, cudaStream_t stream) {
   using C = Cfg<DQK, DV, BK>;
   CUtensorMap tq, tk, tv, to;
@@ -1627,7 +1716,7 @@ splash_status launch(const void *q, const void *k, const void *v, const FwdParam
   int sms = 148;
   SPLASH_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   if (configured_device != dev) {
-    SPLASH_CUDA_TRY(cudaFuncSetAttribute(splash_fwd_kernel<DQK, DV, BK, BAND, TALL, CAP>,
+    SPLASH_CUDA_TRY(cudaFuncSetAttribute(splash_fwd_kernel<DQK, DV, BK, PM, TALL, CAP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
     configured_device = dev;
   }
@@ -1637,26 +1726,26 @@ splash_status launch(const void *q, const void *k, const void *v, const FwdParam
   const int64_t items_per_head = (int64_t)prm.nbm * prm.nq * (prm.nbm == 1 ? prm.B : 1) * prm.nsplit;
   run.head_group = splash_choose_head_group(prm.dense_rows != 0, items_per_head, prm.npairs,
                                             (int64_t)prm.B * prm.Hkv * prm.Lk * (DQK + DV) * 2, grid);
-  splash_fwd_kernel<DQK, DV, BK, BAND, TALL, CAP><<<(unsigned)grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, to, run);
+  splash_fwd_kernel<DQK, DV, BK, PM, TALL, CAP><<<(unsigned)grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, to, run);
   SPLASH_CUDA_TRY(cudaGetLastError());
   splash_count_launches(1);
   return SPLASH_OK;
 }
 
-template <bool BAND, bool CAP>
+template <int PM, bool CAP>
 splash_status launch_shape(const void *q, const void *k, const void *v, const FwdParams &prm, int32_t dqk,
                            int32_t dv, int32_t bk, cudaStream_t stream) {
   if (prm.t1_off) {  // 256-row q-blocks: two halves of one head per item (bk = 128)
-    if (dqk == 128 && dv == 128 && bk == 128) return launch<128, 128, 128, BAND, true, CAP>(q, k, v, prm, stream);
-    if (dqk == 192 && dv == 128 && bk == 128) return launch<192, 128, 128, BAND, true, CAP>(q, k, v, prm, stream);
-    if (dqk == 64 && dv == 64 && bk == 128) return launch<64, 64, 128, BAND, true, CAP>(q, k, v, prm, stream);
+    if (dqk == 128 && dv == 128 && bk == 128) return launch<128, 128, 128, PM, true, CAP>(q, k, v, prm, stream);
+    if (dqk == 192 && dv == 128 && bk == 128) return launch<192, 128, 128, PM, true, CAP>(q, k, v, prm, stream);
+    if (dqk == 64 && dv == 64 && bk == 128) return launch<64, 64, 128, PM, true, CAP>(q, k, v, prm, stream);
     return SPLASH_ERR_UNSUPPORTED;
   }
-  if (dqk == 128 && dv == 128 && bk == 128) return launch<128, 128, 128, BAND, false, CAP>(q, k, v, prm, stream);
-  if (dqk == 192 && dv == 128 && bk == 128) return launch<192, 128, 128, BAND, false, CAP>(q, k, v, prm, stream);
-  if (dqk == 64 && dv == 64 && bk == 64) return launch<64, 64, 64, BAND, false, CAP>(q, k, v, prm, stream);
-  if (dqk == 64 && dv == 64 && bk == 128) return launch<64, 64, 128, BAND, false, CAP>(q, k, v, prm, stream);
-  if (dqk == 128 && dv == 128 && bk == 64) return launch<128, 128, 64, BAND, false, CAP>(q, k, v, prm, stream);
+  if (dqk == 128 && dv == 128 && bk == 128) return launch<128, 128, 128, PM, false, CAP>(q, k, v, prm, stream);
+  if (dqk == 192 && dv == 128 && bk == 128) return launch<192, 128, 128, PM, false, CAP>(q, k, v, prm, stream);
+  if (dqk == 64 && dv == 64 && bk == 64) return launch<64, 64, 64, PM, false, CAP>(q, k, v, prm, stream);
+  if (dqk == 64 && dv == 64 && bk == 128) return launch<64, 64, 128, PM, false, CAP>(q, k, v, prm, stream);
+  if (dqk == 128 && dv == 128 && bk == 64) return launch<128, 128, 64, PM, false, CAP>(q, k, v, prm, stream);
   return SPLASH_ERR_UNSUPPORTED;
 }
 
@@ -1667,7 +1756,8 @@ using namespace splash;
 
 splash_status splash_attention_fwd_launch(const void *q, const void *k, const void *v, int32_t B,
                                           int32_t Hq, int32_t Hkv, int64_t Lq, int64_t Lk,
-                                          int32_t dqk, int32_t dv, const splash_mask_info *mi,
+                                          int32_t dqk, int32_t dv, const int32_t *q_segment_ids,
+                                          const int32_t *kv_segment_ids, const splash_mask_info *mi,
                                           float scale, float softcap, float max_logit, void *out,
                                           float *lse, int32_t nsplit, float *o_part, float *lse_part,
                                           cudaStream_t stream, uint32_t *err_word) {
@@ -1696,7 +1786,13 @@ splash_status splash_attention_fwd_launch(const void *q, const void *k, const vo
   prm.active_cols = mi->active_cols;
   prm.mask_next = mi->mask_next;
   prm.pattern_bits = mi->pattern_bits;
-  prm.band_bits = (mi->patterns_from_positions && !mi->has_segments) ? 1 : 0;
+  // pattern source: stored, or from positions (with segment IDs when the
+  // table has them; the caller passes the arrays it was built from)
+  const int pm = !mi->patterns_from_positions ? kPatStored : (mi->has_segments ? kPatBandSeg : kPatBand);
+  if (pm == kPatBandSeg && q_segment_ids == nullptr) return SPLASH_ERR_INVALID_ARG;
+  prm.band_bits = pm != kPatStored ? 1 : 0;
+  prm.seg_q = q_segment_ids;
+  prm.seg_kv = kv_segment_ids != nullptr ? kv_segment_ids : q_segment_ids;
   prm.band_causal = mi->causal;
   prm.band_wl = mi->window_left;
   prm.band_wr = mi->window_right;
@@ -1725,11 +1821,13 @@ splash_status splash_attention_fwd_launch(const void *q, const void *k, const vo
   prm.timeout_ns = 1000000000ull;  // 1 s per wait
   const int bk = mi->bk;
   if (prm.use_softcap) {
-    if (prm.band_bits) return launch_shape<true, true>(q, k, v, prm, dqk, dv, bk, stream);
-    return launch_shape<false, true>(q, k, v, prm, dqk, dv, bk, stream);
+    if (pm == kPatBandSeg) return launch_shape<kPatBandSeg, true>(q, k, v, prm, dqk, dv, bk, stream);
+    if (pm == kPatBand) return launch_shape<kPatBand, true>(q, k, v, prm, dqk, dv, bk, stream);
+    return launch_shape<kPatStored, true>(q, k, v, prm, dqk, dv, bk, stream);
   }
-  if (prm.band_bits) return launch_shape<true, false>(q, k, v, prm, dqk, dv, bk, stream);
-  return launch_shape<false, false>(q, k, v, prm, dqk, dv, bk, stream);
+  if (pm == kPatBandSeg) return launch_shape<kPatBandSeg, false>(q, k, v, prm, dqk, dv, bk, stream);
+  if (pm == kPatBand) return launch_shape<kPatBand, false>(q, k, v, prm, dqk, dv, bk, stream);
+  return launch_shape<kPatStored, false>(q, k, v, prm, dqk, dv, bk, stream);
 }
 
 splash_status splash_wait_selftest_launch(uint64_t timeout_ns, cudaStream_t stream, uint32_t *err_word) {

@@ -53,8 +53,9 @@ splash_status context_for(int dev, PipelineContext **out) {
 
 splash_status splash_attention_fwd_host_launch(const void *q_h, const void *k_h, const void *v_h, int32_t B,
                                                int32_t Hq, int32_t Hkv, int64_t Lq, int64_t Lk, int32_t dqk,
-                                               int32_t dv, const splash_mask_info *mi, float scale, float softcap,
-                                               void *out_h, float *lse_h, void *q_d, void *k_d, void *v_d,
+                                               int32_t dv, const int32_t *q_segment_ids,
+                                               const int32_t *kv_segment_ids, const splash_mask_info *mi,
+                                               float scale, float softcap, void *out_h, float *lse_h, void *q_d, void *k_d, void *v_d,
                                                void *out_d, float *lse_d, int32_t target_chunks,
                                                cudaStream_t stream, uint32_t *err) {
   int dev = 0;
@@ -114,8 +115,11 @@ splash_status splash_attention_fwd_host_launch(const void *q_h, const void *k_h,
                                     cudaMemcpyHostToDevice, c->s_in));
     SPLASH_CUDA_TRY(cudaEventRecord(c->in_done[x], c->s_in));
     SPLASH_CUDA_TRY(cudaStreamWaitEvent(c->s_comp, c->in_done[x], 0));
-    st = splash_attention_fwd_launch(qd, kd, vd, ch.nb, ch.nkv * G, ch.nkv, Lq, Lk, dqk, dv, mi, scale, softcap,
-                                     NAN, od, ld, 1, nullptr, nullptr, c->s_comp, err);
+    // segment arrays: their rows follow the table's batch rows (one row
+    // when B_mask = 1; the whole batch is one chunk when B_mask = B)
+    st = splash_attention_fwd_launch(qd, kd, vd, ch.nb, ch.nkv * G, ch.nkv, Lq, Lk, dqk, dv, q_segment_ids,
+                                     kv_segment_ids, mi, scale, softcap, NAN, od, ld, 1, nullptr, nullptr, c->s_comp,
+                                     err);
     if (st != SPLASH_OK) return st;
     SPLASH_CUDA_TRY(cudaEventRecord(c->comp_done[x], c->s_comp));
     SPLASH_CUDA_TRY(cudaStreamWaitEvent(c->s_out, c->comp_done[x], 0));

@@ -30,8 +30,9 @@ struct splash_mask_info {
   int32_t causal = 0;
   int64_t window_left = -1, window_right = -1;
   int32_t has_segments = 0;
-  // the forward computes partial blocks' masks from positions instead of
-  // reading the stored patterns (masks without segment IDs only)
+  // the forward computes partial blocks' masks from positions (and, for a
+  // table with segment IDs, from the arrays the caller passes to it) instead
+  // of reading the stored patterns
   int32_t patterns_from_positions = 0;
   // totals (host copies)
   int64_t num_active = 0, num_partial = 0, num_patterns = 0, allowed_pairs = 0;
@@ -112,7 +113,8 @@ uint32_t *splash_device_error_word(int device);  // device address of the error 
 // nsplit > 1: split-KV partials into o_part / lse_part (out / lse unused).
 splash_status splash_attention_fwd_launch(const void *q, const void *k, const void *v, int32_t B,
                                           int32_t Hq, int32_t Hkv, int64_t Lq, int64_t Lk,
-                                          int32_t dqk, int32_t dv, const splash_mask_info *mi,
+                                          int32_t dqk, int32_t dv, const int32_t *q_segment_ids,
+                                          const int32_t *kv_segment_ids, const splash_mask_info *mi,
                                           float scale, float softcap, float max_logit, void *out,
                                           float *lse, int32_t nsplit, float *o_part, float *lse_part,
                                           cudaStream_t stream, uint32_t *err_word);
@@ -129,8 +131,9 @@ splash_status splash_attention_bwd_launch(const void *q, const void *k, const vo
 // host_pipeline.cu
 splash_status splash_attention_fwd_host_launch(const void *q_h, const void *k_h, const void *v_h, int32_t B,
                                                int32_t Hq, int32_t Hkv, int64_t Lq, int64_t Lk, int32_t dqk,
-                                               int32_t dv, const splash_mask_info *mi, float scale, float softcap,
-                                               void *out_h, float *lse_h, void *q_d, void *k_d, void *v_d,
+                                               int32_t dv, const int32_t *q_segment_ids,
+                                               const int32_t *kv_segment_ids, const splash_mask_info *mi,
+                                               float scale, float softcap, void *out_h, float *lse_h, void *q_d, void *k_d, void *v_d,
                                                void *out_d, float *lse_d, int32_t target_chunks,
                                                cudaStream_t stream, uint32_t *err);
 splash_status splash_wait_selftest_launch(uint64_t timeout_ns, cudaStream_t stream,

@@ -180,13 +180,16 @@ splash_status splash_mask_info_to_host(const splash_mask_info *mi, int8_t *block
  * element masks of partial blocks from:
  *   SPLASH_PATTERNS_STORED (default): the deduplicated partial_mask_blocks;
  *   SPLASH_PATTERNS_FROM_POSITIONS: computed in the kernel from the query and
- *     key positions (causal / window bounds and ragged-length padding), the
+ *     key positions (causal / window bounds and ragged-length padding) and,
+ *     for a table built with segment IDs, from the segment arrays, the
  *     alternative of "Pallas Kernels and Splash Attention" §6.6 (no pattern
- *     reads; the results are identical).  Only for tables built without
- *     segment IDs (else SPLASH_ERR_UNSUPPORTED).
- * The setting stays with the handle across rebuilds (a rebuild with segment
- * IDs makes the forward use the stored patterns).  The backward always reads
- * the stored patterns.  Errors: INVALID_ARG (NULL handle, unknown source).
+ *     reads; the results are identical).  With segment IDs every forward
+ *     call (splash_attention_fwd, _fwd_mle, _fwd_split, _fwd_host) must pass
+ *     the arrays the table was built from (same values; device memory, read
+ *     by the kernel); a NULL q_segment_ids there returns INVALID_ARG.
+ * The setting stays with the handle across rebuilds.  The backward always
+ * reads the stored patterns.  Errors: INVALID_ARG (NULL handle, unknown
+ * source).
  */
 #define SPLASH_PATTERNS_STORED 0
 #define SPLASH_PATTERNS_FROM_POSITIONS 1
@@ -208,13 +211,16 @@ void splash_mask_info_destroy(splash_mask_info *mi);
  *   lse[b,h,i]   = m + ln(sum_j exp(s_j - m))            (natural log)
  * Rows with no allowed key get out = 0 and lse = -inf.  Only the MaskInfo's
  * active blocks are loaded or computed; partial blocks are masked element by
- * element from partial_mask_blocks.
+ * element from partial_mask_blocks (or from positions and segment IDs, see
+ * splash_mask_info_set_pattern_source).
  *
  *   q    device bf16 [B][Hq][Lq][dqk]      k  device bf16 [B][Hkv][Lk][dqk]
  *   v    device bf16 [B][Hkv][Lk][dv]      (all 16-byte aligned)
  *   q_segment_ids, kv_segment_ids  the device arrays the MaskInfo was built
- *        from, or NULL; accepted for interface symmetry (the stored patterns
- *        already encode them).
+ *        from, or NULL.  Read only when the table has segment IDs and its
+ *        pattern source is SPLASH_PATTERNS_FROM_POSITIONS (then q_segment_ids
+ *        is required; kv_segment_ids NULL means q_segment_ids); the stored
+ *        patterns already encode them otherwise.
  *   mi   a MaskInfo built for (Lq, Lk) with B_mask == 1 or B_mask == B.
  *   scale  multiplies q.k (e.g. 1/sqrt(dqk)); must be positive and finite.
  *   softcap <= 0 disables the cap (NaN or +inf is rejected).

@@ -1,8 +1,8 @@
-"""Partial-block masks computed from positions in the kernel ("Pallas Kernels
-and Splash Attention" §6.6) against the stored patterns: for masks without
-segment IDs the two sources give the same element masks, so every output of
-the forward (one pass, split-KV, Max Logit Estimate) must be identical bit
-for bit, and equal to the f64 oracle within tolerance."""
+"""Partial-block masks computed in the kernel from positions and segment IDs
+("Pallas Kernels and Splash Attention" §6.6) against the stored patterns: the
+two sources give the same element masks, so every output of the forward (one
+pass, split-KV, Max Logit Estimate, host buffers) must be identical bit for
+bit, and equal to the f64 oracle within tolerance."""
 import math
 
 import pytest
@@ -61,10 +61,69 @@ def test_positions_equal_stored_patterns(bsf, case):
     mi.close()
 
 
-def test_positions_need_a_mask_without_segment_ids(bsf):
+SEG_CASES = [
+    # label, B, Hq, Hkv, L, d, bq, bk, softcap, causal, wl, wr, max_id, sorted, B_mask
+    ("documents + causal GQA", 2, 4, 2, 2048, 128, 128, 128, 0.0, True, -1, -1, 6, True, 2),
+    ("documents, no band, blocks 64", 1, 2, 2, 1024, 64, 64, 64, 0.0, False, -1, -1, 9, True, 1),
+    ("non-monotone IDs + causal + cap", 1, 4, 4, 1024, 128, 128, 128, 30.0, True, -1, -1, 3, False, 1),
+    ("many short documents + window", 2, 2, 1, 1536, 128, 128, 128, 0.0, True, 200, 0, 40, True, 2),
+    ("ragged 1000, documents + causal", 1, 2, 1, 1000, 128, 128, 128, 0.0, True, -1, -1, 5, True, 1),
+    ("256-row q-blocks, documents + causal", 1, 2, 2, 1024, 128, 256, 128, 0.0, True, -1, -1, 4, True, 1),
+    ("d192/128, documents", 1, 2, 2, 768, 192, 128, 128, 0.0, True, -1, -1, 5, True, 1),
+]
+
+
+@pytest.mark.parametrize("case", SEG_CASES, ids=[c[0] for c in SEG_CASES])
+def test_positions_with_segment_ids_equal_stored_patterns(bsf, case):
+    """Masks with segment IDs: the kernel forms partial blocks' masks from the
+    positions and the segment arrays ("Pallas Kernels and Splash Attention"
+    §6.4, §6.6); the outputs equal those from the stored patterns bit for bit
+    (one pass, split-KV, Max Logit Estimate, host buffers), and the oracle
+    within tolerance.  Non-monotone and short-document IDs put several
+    segments in one warp's rows (the key-by-key path)."""
+    label, B, Hq, Hkv, L, d, bq, bk, cap, causal, wl, wr, max_id, srt, bm = case
+    dv = 128 if d == 192 else d
+    seed = 31 * SEG_CASES.index(case) + 7
+    q = workloads.normal_bf16((B, Hq, L, d), seed + 1).cuda()
+    k = workloads.normal_bf16((B, Hkv, L, d), seed + 2).cuda()
+    v = workloads.normal_bf16((B, Hkv, L, dv), seed + 3).cuda()
+    seg = workloads.random_segment_ids(bm, L, seed, max_id, srt).cuda()
+    mi = bsf.build_mask_info(bsf.MaskSpec(causal, wl, wr, seg, seg), L, L, bq, bk)
+    assert mi.counts()["num_partial"] > 0, label
+    scale = 1.0 / math.sqrt(d)
+    runs = {}
+    for source in ("stored", "positions"):
+        mi.set_pattern_source(source)
+        runs[source] = (bsf.attention_fwd(q, k, v, mi, scale, cap, seg, seg),
+                        bsf.attention_fwd(q, k, v, mi, scale, cap, seg, None, num_splits=3),
+                        bsf.attention_fwd(q, k, v, mi, scale, cap, seg, seg, max_logit=cap if cap > 0 else 8.0),
+                        bsf.attention_fwd_host(q.cpu(), k.cpu(), v.cpu(), mi, scale, cap,
+                                               q_segment_ids=seg, kv_segment_ids=seg))
+    torch.cuda.synchronize()
+    assert bsf.last_device_error() == 0, label
+    for (a_out, a_lse), (b_out, b_lse) in zip(runs["stored"], runs["positions"]):
+        assert torch.equal(a_out, b_out) and torch.equal(a_lse, b_lse), label
+    seg_c = seg.cpu().numpy()  # one row serves every batch row (B_mask = 1), as in the library
+    O, Lse = oracle.attention(q.cpu(), k.cpu(), v.cpu(), oracle.MaskSpec(causal, wl, wr, seg_c, seg_c), scale, cap)
+    out, lse = runs["positions"][0]
+    compare_rows(out.float().cpu().numpy().reshape(-1, dv), lse.cpu().numpy().reshape(-1),
+                 O.reshape(-1, dv), Lse.reshape(-1), label)
+    mi.close()
+
+
+def test_positions_with_segment_ids_need_the_arrays(bsf):
+    """A table with segment IDs whose pattern source is positions needs the
+    segment arrays in the forward call: without them the call is refused
+    before any launch."""
     seg = workloads.random_segment_ids(1, 512, 5, 3, True).cuda()
     mi = bsf.build_mask_info(bsf.MaskSpec(True, -1, -1, seg, seg), 512, 512, 128, 128)
+    mi.set_pattern_source("positions")
+    q = workloads.normal_bf16((1, 2, 512, 128), 1).cuda()
+    k = workloads.normal_bf16((1, 2, 512, 128), 2).cuda()
     with pytest.raises(bsf.SplashError):
-        mi.set_pattern_source("positions")
+        bsf.attention_fwd(q, k, k, mi, 0.1, 0.0)
     mi.set_pattern_source("stored")
+    bsf.attention_fwd(q, k, k, mi, 0.1, 0.0)
+    torch.cuda.synchronize()
+    assert bsf.last_device_error() == 0
     mi.close()
