@@ -397,7 +397,7 @@ splash_status splash_last_device_error(void *cuda_stream) {
   SPLASH_CUDA_TRY(cudaMemcpy(&word, addr, sizeof word, cudaMemcpyDeviceToHost));
   if (word != 0) SPLASH_CUDA_TRY(cudaMemset(addr, 0, sizeof word));
   if (word & (SPLASH_DEV_TIMEOUT_PRODUCER | SPLASH_DEV_TIMEOUT_MMA | SPLASH_DEV_TIMEOUT_SOFTMAX |
-              SPLASH_DEV_TIMEOUT_DRAIN | SPLASH_DEV_TIMEOUT_SELFTEST))
+              SPLASH_DEV_TIMEOUT_DRAIN | SPLASH_DEV_TIMEOUT_SELFTEST | SPLASH_DEV_TIMEOUT_BUILD))
     return SPLASH_ERR_DEVICE_TIMEOUT;
   if (word & (SPLASH_DEV_BAD_TABLE | SPLASH_DEV_SMEM_ALIGN)) return SPLASH_ERR_DEVICE_CHECK;
   return SPLASH_OK;

@@ -14,6 +14,7 @@ enum : uint32_t {
   SPLASH_DEV_TIMEOUT_SOFTMAX = 1u << 2,
   SPLASH_DEV_TIMEOUT_DRAIN = 1u << 3,
   SPLASH_DEV_TIMEOUT_SELFTEST = 1u << 4,
+  SPLASH_DEV_TIMEOUT_BUILD = 1u << 5,  // the one-launch MaskInfo build gave up at a grid barrier
   SPLASH_DEV_BAD_TABLE = 1u << 8,
   SPLASH_DEV_SMEM_ALIGN = 1u << 9,  // dynamic shared memory not 1024-byte aligned: the kernel did nothing
 };
@@ -65,6 +66,11 @@ struct splash_mask_info {
   int32_t *rep_list = nullptr;     // [cap_active] partial index of pattern u
   int32_t *row_hist = nullptr;     // [nk+1] counting-sort bins
   unsigned long long *counters = nullptr;  // [8]: A, A_p, P, allowed, max_row, deferred blocks
+  unsigned int *grid_sync = nullptr;       // [2]: the one-launch build's barrier (arrivals, generation)
+  uint32_t *part_bits = nullptr;           // [cap_part_bits] one-launch build: each partial block's words
+  unsigned long long *ht_key = nullptr;    // [cap_ht] one-launch build: content hash table (keys)
+  int32_t *ht_val = nullptr;               // [cap_ht] smallest partial index per key
+  int64_t cap_part_bits = 0, cap_ht = 0;
   // host staging
   unsigned long long *h_counters = nullptr;  // pinned [8]
   // counts of an asynchronous build: `counts_ready` is recorded after its last

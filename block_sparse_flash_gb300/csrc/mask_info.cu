@@ -174,14 +174,11 @@ __device__ __forceinline__ int32_t block_keys(const DevMask &m, int64_t c) {
 }
 
 // ---------------------------------------------------------------- K1
-// Also clears the per-row counters and the totals that classify_kernel adds to.
-__global__ void seg_summary_kernel(DevMask m, int32_t *qsum, int32_t *kvsum, int32_t *row_cnt, int32_t *row_pcnt,
-                                   unsigned long long *counters) {
-  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+// One warp per q-block or kv-block of batch row bm (warp index `warp` within
+// the row).  Also clears the per-row counters.
+__device__ __forceinline__ void seg_summary_warp(const DevMask &m, int64_t warp, int32_t bm, int32_t *qsum,
+                                                 int32_t *kvsum, int32_t *row_cnt, int32_t *row_pcnt) {
   const int lane = threadIdx.x & 31;
-  const int32_t bm = blockIdx.y;
-  if (blockIdx.x == 0 && bm == 0 && threadIdx.x < 8) counters[threadIdx.x] = 0ull;
-  if (warp >= m.nq + m.nk) return;
   const bool isq = warp < m.nq;
   if (isq && lane == 0) {
     row_cnt[(int64_t)bm * m.nq + warp] = 0;
@@ -209,6 +206,15 @@ __global__ void seg_summary_kernel(DevMask m, int32_t *qsum, int32_t *kvsum, int
   }
 }
 
+// Also clears the totals that classify_kernel adds to.
+__global__ void seg_summary_kernel(DevMask m, int32_t *qsum, int32_t *kvsum, int32_t *row_cnt, int32_t *row_pcnt,
+                                   unsigned long long *counters) {
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 8) counters[threadIdx.x] = 0ull;
+  if (warp >= m.nq + m.nk) return;
+  seg_summary_warp(m, warp, (int32_t)blockIdx.y, qsum, kvsum, row_cnt, row_pcnt);
+}
+
 // ---------------------------------------------------------------- K2
 // One thread per block (bm, r, c); a CTA covers 128 blocks of one row.
 constexpr int kClassifyThreads = 128;
@@ -218,13 +224,12 @@ constexpr int kClassifyThreads = 128;
 // counters[5] counts the appends) for count_deferred_kernel, which counts each
 // with a whole CTA.  Blocks beyond the list's capacity `defer_cap` (or all of
 // them, with deferred == nullptr) are counted here, element by element.
-__global__ void __launch_bounds__(kClassifyThreads)
-classify_kernel(DevMask m, const int32_t *qsum, const int32_t *kvsum, int8_t *block_mask,
-                int32_t *row_cnt, int32_t *row_pcnt, unsigned long long *counters, int32_t *deferred,
-                int64_t defer_cap) {
-  const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t r = blockIdx.y;
-  const int32_t bm = blockIdx.z;
+// The CTA (any multiple of 32 threads up to 1024) classifies blocks
+// xc*blockDim .. of row r of batch row bm, one thread per block.
+__device__ void classify_body(const DevMask &m, int64_t xc, int64_t r, int32_t bm, const int32_t *qsum,
+                              const int32_t *kvsum, int8_t *block_mask, int32_t *row_cnt, int32_t *row_pcnt,
+                              unsigned long long *counters, int32_t *deferred, int64_t defer_cap) {
+  const int64_t c = xc * blockDim.x + threadIdx.x;
   const int64_t row = (int64_t)bm * m.nq + r;
   int64_t cnt = 0;
   int cls = 0;
@@ -238,7 +243,7 @@ classify_kernel(DevMask m, const int32_t *qsum, const int32_t *kvsum, int8_t *bl
       cls = band_block_class(m, A, W, r, c);
       block_mask[row * m.nk + c] = (int8_t)cls;
     }
-    if (blockIdx.x == 0)
+    if (xc == 0)
       for (int32_t di = threadIdx.x; di < m.bq; di += blockDim.x) cnt += band_row_count(m, A, W, r * m.bq + di);
   } else if (c < m.nk) {
     const int64_t c0 = c * m.bk, c1 = c0 + m.bk - 1;
@@ -312,8 +317,8 @@ classify_kernel(DevMask m, const int32_t *qsum, const int32_t *kvsum, int8_t *bl
     np += __shfl_xor_sync(0xffffffffu, np, off);
     ns += __shfl_xor_sync(0xffffffffu, ns, off);
   }
-  __shared__ int sa[kClassifyThreads / 32], sp[kClassifyThreads / 32];
-  __shared__ unsigned long long ss[kClassifyThreads / 32];
+  __shared__ int sa[32], sp[32];
+  __shared__ unsigned long long ss[32];
   const int w = threadIdx.x >> 5;
   if ((threadIdx.x & 31) == 0) {
     sa[w] = na;
@@ -324,7 +329,7 @@ classify_kernel(DevMask m, const int32_t *qsum, const int32_t *kvsum, int8_t *bl
   if (threadIdx.x == 0) {
     int ta = 0, tp = 0;
     unsigned long long ts = 0;
-    for (int x = 0; x < kClassifyThreads / 32; ++x) {
+    for (int x = 0; x < (int)(blockDim.x >> 5); ++x) {
       ta += sa[x];
       tp += sp[x];
       ts += ss[x];
@@ -333,27 +338,36 @@ classify_kernel(DevMask m, const int32_t *qsum, const int32_t *kvsum, int8_t *bl
     if (tp) atomicAdd(&row_pcnt[row], tp);
     if (ts) atomicAdd(&counters[3], ts);
   }
+  __syncthreads();  // sa / sp / ss are rewritten by the CTA's next call
+}
+
+__global__ void __launch_bounds__(kClassifyThreads)
+classify_kernel(DevMask m, const int32_t *qsum, const int32_t *kvsum, int8_t *block_mask,
+                int32_t *row_cnt, int32_t *row_pcnt, unsigned long long *counters, int32_t *deferred,
+                int64_t defer_cap) {
+  classify_body(m, blockIdx.x, blockIdx.y, (int32_t)blockIdx.z, qsum, kvsum, block_mask, row_cnt, row_pcnt,
+                counters, deferred, defer_cap);
 }
 
 // One CTA (kClassifyThreads threads, one per query row of the block) per
 // deferred block: the allowed pairs of row i are the keys of the row's band
 // range with i's segment id; the block's class and its row / total counts are
 // then added like classify_kernel's.
-__global__ void __launch_bounds__(kClassifyThreads)
-count_deferred_kernel(DevMask m, const int32_t *deferred, int64_t defer_cap, int8_t *block_mask, int32_t *row_cnt,
-                      int32_t *row_pcnt, unsigned long long *counters) {
-  __shared__ unsigned long long part[kClassifyThreads / 32];
+__device__ void count_deferred_body(const DevMask &m, const int32_t *deferred, int64_t defer_cap, int8_t *block_mask,
+                                    int32_t *row_cnt, int32_t *row_pcnt, unsigned long long *counters, int64_t bid,
+                                    int64_t nb) {
+  __shared__ unsigned long long part[32];
   __shared__ int32_t s_kv[128];  // the block's key segment IDs (bk <= 128)
   const int64_t n = min((int64_t)counters[5], defer_cap);
   const int di = threadIdx.x, lane = di & 31;
-  for (int64_t x = blockIdx.x; x < n; x += gridDim.x) {
+  for (int64_t x = bid; x < n; x += nb) {
     const int64_t idx = deferred[x];
     const int64_t row = idx / m.nk, c = idx - row * m.nk;
     const int32_t bm = (int32_t)(row / m.nq);
     const int64_t r = row - (int64_t)bm * m.nq;
     const bool sorted = stage_kv_ids(m, bm, c, s_kv);
     unsigned long long cnt = 0;
-    for (int32_t d = di; d < m.bq; d += kClassifyThreads) {
+    for (int32_t d = di; d < m.bq; d += blockDim.x) {
       const int64_t i = r * m.bq + d;
       int64_t lo, hi;
       band_range(m, i, c * m.bk, c * m.bk + m.bk - 1, lo, hi);
@@ -373,7 +387,7 @@ count_deferred_kernel(DevMask m, const int32_t *deferred, int64_t defer_cap, int
     __syncthreads();
     if (di == 0) {
       unsigned long long t = 0;
-      for (int w = 0; w < kClassifyThreads / 32; ++w) t += part[w];
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += part[w];
       const int cls = t == 0 ? 0 : (t == (unsigned long long)m.bq * m.bk ? 2 : 1);
       block_mask[idx] = (int8_t)cls;
       if (cls != 0) atomicAdd(&row_cnt[row], 1);
@@ -382,6 +396,12 @@ count_deferred_kernel(DevMask m, const int32_t *deferred, int64_t defer_cap, int
     }
     __syncthreads();
   }
+}
+
+__global__ void __launch_bounds__(kClassifyThreads)
+count_deferred_kernel(DevMask m, const int32_t *deferred, int64_t defer_cap, int8_t *block_mask, int32_t *row_cnt,
+                      int32_t *row_pcnt, unsigned long long *counters) {
+  count_deferred_body(m, deferred, defer_cap, block_mask, row_cnt, row_pcnt, counters, blockIdx.x, gridDim.x);
 }
 
 // ---------------------------------------------------------------- scans
@@ -483,14 +503,12 @@ __device__ __forceinline__ void scan_rows_body(int64_t R, const int32_t *row_cnt
 // ---------------------------------------------------------------- K3 compact
 // One warp per row (b_mask, r): columns in chunks of 32, ballots give each
 // active block its position.
-__global__ void compact_kernel(DevMask m, int64_t R, const int8_t *block_mask,
-                               const int32_t *row_ptr, const int32_t *prow_ptr,
-                               int32_t *active_rows, int32_t *active_cols, int32_t *mask_next,
-                               uint8_t *bounds_start, uint8_t *bounds_end, int32_t *part_row,
-                               int32_t *part_col, int32_t *part_g) {
-  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+__device__ __forceinline__ void compact_warp(const DevMask &m, int64_t row, const int8_t *block_mask,
+                                             const int32_t *row_ptr, const int32_t *prow_ptr, int32_t *active_rows,
+                                             int32_t *active_cols, int32_t *mask_next, uint8_t *bounds_start,
+                                             uint8_t *bounds_end, int32_t *part_row, int32_t *part_col,
+                                             int32_t *part_g) {
   const int lane = threadIdx.x & 31;
-  if (row >= R) return;
   const int32_t r = (int32_t)(row % m.nq);
   const int32_t g0 = row_ptr[row], gend = row_ptr[row + 1];
   int32_t g = g0, k = prow_ptr[row];
@@ -519,6 +537,17 @@ __global__ void compact_kernel(DevMask m, int64_t R, const int8_t *block_mask,
   }
 }
 
+__global__ void compact_kernel(DevMask m, int64_t R, const int8_t *block_mask,
+                               const int32_t *row_ptr, const int32_t *prow_ptr,
+                               int32_t *active_rows, int32_t *active_cols, int32_t *mask_next,
+                               uint8_t *bounds_start, uint8_t *bounds_end, int32_t *part_row,
+                               int32_t *part_col, int32_t *part_g) {
+  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (row >= R) return;
+  compact_warp(m, row, block_mask, row_ptr, prow_ptr, active_rows, active_cols, mask_next, bounds_start, bounds_end,
+               part_row, part_col, part_g);
+}
+
 // ---------------------------------------------------------------- K4 patterns
 constexpr uint64_t kHashBasis = 0xcbf29ce484222325ull;
 constexpr uint64_t kHashPrime = 0x100000001b3ull;
@@ -542,15 +571,16 @@ __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
   return v;
 }
 
-// One CTA (bq threads, one per query row) per partial block, grid-stride.
-__global__ void partial_hash_kernel(DevMask m, const unsigned long long *counters,
-                                    const int32_t *part_row, const int32_t *part_col,
-                                    uint64_t *part_hash) {
+// One CTA per partial block, grid-stride; thread di < bq takes query row di
+// (a CTA of more threads leaves the others idle).
+__device__ void partial_hash_body(const DevMask &m, const unsigned long long *counters, const int32_t *part_row,
+                                  const int32_t *part_col, uint64_t *part_hash, int64_t bid, int64_t nb) {
   __shared__ uint64_t wsum[8];  // bq <= 256 threads
   __shared__ int32_t s_kv[128];  // the block's key segment IDs (bk <= 128)
   const int64_t Ap = (int64_t)counters[1];
   const int di = threadIdx.x;
-  for (int64_t k = blockIdx.x; k < Ap; k += gridDim.x) {
+  const bool act = di < m.bq;
+  for (int64_t k = bid; k < Ap; k += nb) {
     const int64_t row = part_row[k];
     const int32_t bm = (int32_t)(row / m.nq);
     const int64_t r = row % m.nq, c = part_col[k];
@@ -561,16 +591,20 @@ __global__ void partial_hash_kernel(DevMask m, const unsigned long long *counter
       continue;
     }
     const bool sorted = m.qseg != nullptr ? stage_kv_ids(m, bm, c, s_kv) : false;
-    const int64_t i = r * m.bq + di;
-    const int32_t sq = q_segment(m, bm, i);
-    int32_t ra = 0, rb = -1;
-    if (sorted) sorted_run(s_kv, block_keys(m, c), sq, ra, rb);
-    uint64_t h = kHashBasis;
-    for (int32_t w = 0; w < m.bk / 32; ++w)
-      h = hash_step(h, m.qseg != nullptr ? row_word_staged(m, i, sq, c * m.bk, c * m.bk + w * 32, s_kv, sorted, ra, rb)
-                                         : row_word(m, bm, i, sq, c * m.bk + w * 32));
-    const uint64_t t = warp_sum_u64(row_hash_term(h, di));
-    if ((di & 31) == 0) wsum[di >> 5] = t;
+    uint64_t t = 0;
+    if (act) {  // whole warps (bq is a multiple of 32)
+      const int64_t i = r * m.bq + di;
+      const int32_t sq = q_segment(m, bm, i);
+      int32_t ra = 0, rb = -1;
+      if (sorted) sorted_run(s_kv, block_keys(m, c), sq, ra, rb);
+      uint64_t h = kHashBasis;
+      for (int32_t w = 0; w < m.bk / 32; ++w)
+        h = hash_step(h, m.qseg != nullptr
+                             ? row_word_staged(m, i, sq, c * m.bk, c * m.bk + w * 32, s_kv, sorted, ra, rb)
+                             : row_word(m, bm, i, sq, c * m.bk + w * 32));
+      t = warp_sum_u64(row_hash_term(h, di));
+    }
+    if (act && (di & 31) == 0) wsum[di >> 5] = t;
     __syncthreads();
     if (di == 0) {
       uint64_t H = 0;
@@ -579,6 +613,11 @@ __global__ void partial_hash_kernel(DevMask m, const unsigned long long *counter
     }
     __syncthreads();
   }
+}
+
+__global__ void partial_hash_kernel(DevMask m, const unsigned long long *counters, const int32_t *part_row,
+                                    const int32_t *part_col, uint64_t *part_hash) {
+  partial_hash_body(m, counters, part_row, part_col, part_hash, blockIdx.x, gridDim.x);
 }
 
 // CTA-wide exact comparison of two partial blocks' patterns: each thread
@@ -613,16 +652,16 @@ __device__ bool patterns_equal(const DevMask &m, const int32_t *part_row, const 
 // identical content.  Earlier blocks of equal hash are the candidates, tried
 // in ascending order; each exact comparison uses the whole CTA.
 constexpr int kDedupThreads = 256;
-__global__ void __launch_bounds__(kDedupThreads)
-dedup_kernel(DevMask m, const unsigned long long *counters, const int32_t *part_row, const int32_t *part_col,
-             const uint64_t *part_hash, int32_t *part_rep) {
+__device__ void dedup_body(const DevMask &m, const unsigned long long *counters, const int32_t *part_row,
+                           const int32_t *part_col, const uint64_t *part_hash, int32_t *part_rep, int64_t bid,
+                           int64_t nb) {
   __shared__ uint32_t s_ball[kDedupThreads / 32];
   __shared__ int32_t s_kv_a[128], s_kv_b[128];  // key segment IDs of block k and of the candidate
   const int64_t Ap = (int64_t)counters[1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // band-only whole blocks: equal diagonal offsets (the "hash") mean equal content
   const bool by_offset = m.qseg == nullptr && !m.ragged;
-  for (int64_t k = blockIdx.x; k < Ap; k += gridDim.x) {
+  for (int64_t k = bid; k < Ap; k += nb) {
     const uint64_t h = part_hash[k];
     int64_t rep = k;  // uniform over the CTA
     bool staged_a = false, sorted_a = false, sorted_b = false;
@@ -659,13 +698,18 @@ dedup_kernel(DevMask m, const unsigned long long *counters, const int32_t *part_
   }
 }
 
+__global__ void __launch_bounds__(kDedupThreads)
+dedup_kernel(DevMask m, const unsigned long long *counters, const int32_t *part_row, const int32_t *part_col,
+             const uint64_t *part_hash, int32_t *part_rep) {
+  dedup_body(m, counters, part_row, part_col, part_hash, part_rep, blockIdx.x, gridDim.x);
+}
+
 // Pattern indices (one CTA): an exclusive scan of the first-occurrence flags
 // in partial order gives each representative its pattern index (P = the
 // total); then every partial block's mask_next and the pattern list
 // (partial index of pattern u).
-__global__ void __launch_bounds__(1024)
-scan_finalize_kernel(unsigned long long *counters, const int32_t *part_g, const int32_t *part_rep,
-                     int32_t *part_pidx, int32_t *mask_next, int32_t *rep_list) {
+__device__ void scan_finalize_body(unsigned long long *counters, const int32_t *part_g, const int32_t *part_rep,
+                                   int32_t *part_pidx, int32_t *mask_next, int32_t *rep_list) {
   __shared__ int buf[33];
   const int64_t Ap = (int64_t)counters[1];
   int carry = 0;
@@ -687,37 +731,52 @@ scan_finalize_kernel(unsigned long long *counters, const int32_t *part_g, const 
   }
 }
 
+__global__ void __launch_bounds__(1024)
+scan_finalize_kernel(unsigned long long *counters, const int32_t *part_g, const int32_t *part_rep,
+                     int32_t *part_pidx, int32_t *mask_next, int32_t *rep_list) {
+  scan_finalize_body(counters, part_g, part_rep, part_pidx, mask_next, rep_list);
+}
+
 // One CTA (bq threads) per pattern: its bit-packed rows (word w of row di
 // holds keys 32w .. 32w+31).  The pattern count is read on the device
 // (counters[2]) and never exceeds the buffer capacity `cap` (a count above
 // it is reported and clipped).
-__global__ void materialize_kernel(DevMask m, const unsigned long long *counters, int64_t cap,
-                                   const int32_t *rep_list, const int32_t *part_row,
-                                   const int32_t *part_col, uint32_t *pattern_bits, uint32_t *err) {
+__device__ void materialize_body(const DevMask &m, const unsigned long long *counters, int64_t cap,
+                                 const int32_t *rep_list, const int32_t *part_row, const int32_t *part_col,
+                                 uint32_t *pattern_bits, uint32_t *err, int64_t bid, int64_t nb) {
   __shared__ int32_t s_kv[128];  // the block's key segment IDs (bk <= 128)
   const int di = threadIdx.x;
+  const bool act = di < m.bq;  // thread di takes row di (others idle)
   const int32_t words = m.bk / 32;
   int64_t P = (int64_t)counters[2];
   if (P > cap) {
-    if (blockIdx.x == 0 && di == 0 && err) atomicOr(err, SPLASH_DEV_BAD_TABLE);
+    if (bid == 0 && di == 0 && err) atomicOr(err, SPLASH_DEV_BAD_TABLE);
     P = cap;
   }
-  for (int64_t u = blockIdx.x; u < P; u += gridDim.x) {
+  for (int64_t u = bid; u < P; u += nb) {
     const int64_t k = rep_list[u];
     const int64_t row = part_row[k];
     const int32_t bm = (int32_t)(row / m.nq);
     const int64_t r = row % m.nq, c = part_col[k];
     const bool sorted = m.qseg != nullptr ? stage_kv_ids(m, bm, c, s_kv) : false;
-    const int64_t i = r * m.bq + di;
-    const int32_t sq = q_segment(m, bm, i);
-    int32_t ra = 0, rb = -1;
-    if (sorted) sorted_run(s_kv, block_keys(m, c), sq, ra, rb);
-    uint32_t *bits = pattern_bits + (u * m.bq + di) * words;
-    for (int32_t w = 0; w < words; ++w)
-      bits[w] = m.qseg != nullptr ? row_word_staged(m, i, sq, c * m.bk, c * m.bk + w * 32, s_kv, sorted, ra, rb)
-                                  : row_word(m, bm, i, sq, c * m.bk + w * 32);
+    if (act) {
+      const int64_t i = r * m.bq + di;
+      const int32_t sq = q_segment(m, bm, i);
+      int32_t ra = 0, rb = -1;
+      if (sorted) sorted_run(s_kv, block_keys(m, c), sq, ra, rb);
+      uint32_t *bits = pattern_bits + (u * m.bq + di) * words;
+      for (int32_t w = 0; w < words; ++w)
+        bits[w] = m.qseg != nullptr ? row_word_staged(m, i, sq, c * m.bk, c * m.bk + w * 32, s_kv, sorted, ra, rb)
+                                    : row_word(m, bm, i, sq, c * m.bk + w * 32);
+    }
     if (m.qseg != nullptr) __syncthreads();  // s_kv is restaged for the next pattern
   }
+}
+
+__global__ void materialize_kernel(DevMask m, const unsigned long long *counters, int64_t cap,
+                                   const int32_t *rep_list, const int32_t *part_row,
+                                   const int32_t *part_col, uint32_t *pattern_bits, uint32_t *err) {
+  materialize_body(m, counters, cap, rep_list, part_row, part_col, pattern_bits, err, blockIdx.x, gridDim.x);
 }
 
 // ---------------------------------------------------------------- row order
@@ -779,6 +838,275 @@ scan_order_kernel(int64_t R, int64_t nk, const int32_t *row_cnt, const int32_t *
   scan_rows_body(R, row_cnt, row_pcnt, row_ptr, prow_ptr, counters);
   __syncthreads();
   row_order_body(R, nk, row_cnt, hist, row_order);
+}
+
+// ---------------------------------------------------------------- one-launch build
+// The pipeline K1 .. materialize as one persistent kernel: every CTA runs each
+// phase on its share of the work (the bodies above with a grid stride; the
+// two scans on CTA 0), and a grid-wide barrier separates the phases.  It
+// replaces nine dependent launches, each of which costs a few microseconds of
+// launch and drain latency at these sizes.  The launch is cooperative, so
+// that every CTA is resident and the barrier can complete; the barrier itself
+// is this file's own, with a bounded wait: a CTA that waits longer than
+// kGridBarrierNs sets SPLASH_DEV_TIMEOUT_BUILD and stops (the others then
+// time out at their next barrier too), so the kernel always ends.
+constexpr int kGridThreads = 256;
+constexpr uint64_t kGridBarrierNs = 2000000000ull;  // 2 s
+constexpr int64_t kGridMaxBlocks = (int64_t)1 << 22;  // larger tables take the launch chain
+constexpr int64_t kGridMaxPartials = 65536;
+
+struct GridArgs {
+  int32_t *qsum, *kvsum;
+  int8_t *block_mask;
+  int32_t *row_cnt, *row_pcnt, *row_ptr, *prow_ptr, *row_hist, *row_order;
+  int32_t *active_rows, *active_cols, *mask_next;
+  uint8_t *bounds_start, *bounds_end;
+  int32_t *part_row, *part_col, *part_g, *part_rep, *part_pidx, *rep_list;
+  uint64_t *part_hash;
+  unsigned long long *counters;
+  uint32_t *pattern_bits;
+  int64_t cap_patterns, NB;
+  // each partial block's mask words (the layout of pattern_bits, indexed by
+  // partial block), and a hash table: key = content hash (0 = empty slot),
+  // value = the smallest partial index with that hash
+  uint32_t *part_bits;
+  unsigned long long *ht_key;
+  int32_t *ht_val;
+  int64_t ht_mask;  // table size - 1 (a power of two, at least twice the partial blocks)
+  unsigned int *sync;  // [2]: arrivals, generation (arrivals 0 at launch)
+  uint32_t *err;
+};
+
+// Warp-level K4 phases of the one-launch build.  hash: the warp computes the
+// mask words of partial block k once (into part_bits), their content hash,
+// and enters the hash in the table with the block's index (the table keeps
+// the smallest).  dedup: the smallest index c with the same hash is the first
+// block of identical content whenever the two blocks' words are equal (all
+// blocks of equal content have equal hashes); otherwise (a hash collision)
+// the earlier blocks of equal hash are compared in ascending order.  So the
+// result is exact, and the usual cost is one comparison per block.
+__device__ __forceinline__ void stage_kv_ids_warp(const DevMask &m, int32_t bm, int64_t c, int32_t *s_kv, bool &sorted) {
+  const int lane = threadIdx.x & 31;
+  const int64_t n = min((int64_t)m.bk, m.Lk - c * m.bk);
+  for (int32_t t = lane; t < m.bk; t += 32) {
+    const int64_t j = c * m.bk + t;
+    s_kv[t] = j < m.Lk ? m.kvseg[(int64_t)bm * m.Lk + j] : 0;
+  }
+  __syncwarp();
+  bool ok = true;
+  for (int32_t t = lane; t + 1 < n; t += 32) ok &= s_kv[t] <= s_kv[t + 1];
+  sorted = __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ unsigned long long table_key(uint64_t h) { return h != 0 ? h : 1ull; }
+
+__device__ void hash_warp(const DevMask &m, const GridArgs &a, int64_t k, int32_t *s_kv) {
+  const int lane = threadIdx.x & 31;
+  const int32_t words = m.bk / 32;
+  const int64_t row = a.part_row[k];
+  const int32_t bm = (int32_t)(row / m.nq);
+  const int64_t r = row % m.nq, c = a.part_col[k];
+  // band-only whole blocks: the diagonal offset identifies the content
+  // exactly (no words are stored; materialize computes them)
+  const bool by_offset = m.qseg == nullptr && !m.ragged;
+  bool sorted = false;
+  if (m.qseg != nullptr) stage_kv_ids_warp(m, bm, c, s_kv, sorted);
+  uint32_t *dst = a.part_bits + k * m.bq * words;
+  uint64_t t = 0;
+  for (int32_t di = lane; di < m.bq && !by_offset; di += 32) {
+    const int64_t i = r * m.bq + di;
+    const int32_t sq = q_segment(m, bm, i);
+    int32_t ra = 0, rb = -1;
+    if (sorted) sorted_run(s_kv, block_keys(m, c), sq, ra, rb);
+    uint64_t h = kHashBasis;
+    for (int32_t w = 0; w < words; ++w) {
+      const uint32_t x = m.qseg != nullptr
+                             ? row_word_staged(m, i, sq, c * m.bk, c * m.bk + w * 32, s_kv, sorted, ra, rb)
+                             : row_word(m, bm, i, sq, c * m.bk + w * 32);
+      dst[di * words + w] = x;
+      h = hash_step(h, x);
+    }
+    t += row_hash_term(h, di);
+  }
+  t = warp_sum_u64(t);
+  const unsigned long long key =
+      by_offset ? ((unsigned long long)(c * m.bk - r * m.bq) ^ 0x8000000000000000ull) : table_key(t);
+  if (lane == 0) {
+    a.part_hash[k] = key;
+    int64_t slot = (int64_t)(key & (unsigned long long)a.ht_mask);
+    for (int64_t probe = 0; probe <= a.ht_mask; ++probe) {  // the table is at most half full
+      const unsigned long long prev = atomicCAS(&a.ht_key[slot], 0ull, key);
+      if (prev == 0ull || prev == key) {
+        atomicMin(&a.ht_val[slot], (int32_t)k);
+        break;
+      }
+      slot = (slot + 1) & a.ht_mask;
+    }
+  }
+  __syncwarp();  // s_kv is restaged for the warp's next block
+}
+
+// Whether partial blocks ka and kb have equal words (warp-wide result).
+__device__ __forceinline__ bool words_equal(const DevMask &m, const GridArgs &a, int64_t ka, int64_t kb) {
+  const int64_t n = (int64_t)m.bq * (m.bk / 32);
+  const uint32_t *pa = a.part_bits + ka * n, *pb = a.part_bits + kb * n;
+  bool same = true;
+  for (int64_t x = threadIdx.x & 31; x < n; x += 32) same &= pa[x] == pb[x];
+  return __all_sync(0xffffffffu, same);
+}
+
+__device__ void dedup_warp(const DevMask &m, const GridArgs &a, int64_t k) {
+  const int lane = threadIdx.x & 31;
+  const unsigned long long key = a.part_hash[k];
+  const bool by_offset = m.qseg == nullptr && !m.ragged;
+  int64_t slot = (int64_t)(key & (unsigned long long)a.ht_mask);
+  int64_t c = k;
+  for (int64_t probe = 0; probe <= a.ht_mask; ++probe) {
+    if (a.ht_key[slot] == key) {
+      c = a.ht_val[slot];
+      break;
+    }
+    slot = (slot + 1) & a.ht_mask;
+  }
+  int64_t rep = k;
+  if (c < k && (by_offset || words_equal(m, a, k, c))) {
+    rep = c;
+  } else if (c < k) {
+    // a hash collision: earlier blocks of equal hash, ascending
+    for (int64_t base = 0; base < k && rep == k; base += 32) {
+      const int64_t kp = base + lane;
+      unsigned cand = __ballot_sync(0xffffffffu, kp < k && a.part_hash[kp] == key);
+      while (cand && rep == k) {
+        const int64_t kc = base + (__ffs(cand) - 1);
+        cand &= cand - 1u;
+        if (words_equal(m, a, k, kc)) rep = kc;
+      }
+    }
+  }
+  if (lane == 0) a.part_rep[k] = (int32_t)rep;
+}
+
+__device__ __forceinline__ uint64_t build_clock_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Grid-wide barrier with a bounded wait; returns false (to every thread of
+// the CTA) when it gave up.  Writes of every CTA before it are visible to
+// every CTA after it (fences around the arrival and the release).
+__device__ bool grid_barrier(unsigned int *sync, uint32_t *err) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile unsigned int *gen = sync + 1;
+    const unsigned int g = *gen;
+    __threadfence();
+    bool ok = true;
+    if (atomicAdd(sync, 1u) == gridDim.x - 1) {
+      atomicExch(sync, 0u);
+      __threadfence();
+      atomicAdd(sync + 1, 1u);
+    } else {
+      const uint64_t t0 = build_clock_ns();
+      while (*gen == g) {
+        if (build_clock_ns() - t0 > kGridBarrierNs) {
+          ok = false;
+          atomicOr(err, SPLASH_DEV_TIMEOUT_BUILD);
+          break;
+        }
+        __nanosleep(32);
+      }
+    }
+    __threadfence();
+    s_ok = ok ? 1 : 0;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+__global__ void __launch_bounds__(kGridThreads) build_grid_kernel(DevMask m, GridArgs a) {
+  const int64_t bid = blockIdx.x, nb = gridDim.x;
+  const int64_t R = (int64_t)m.nbm * m.nq;
+  const int64_t warps = nb * (kGridThreads / 32), gw = bid * (kGridThreads / 32) + (threadIdx.x >> 5);
+  const bool seg = m.qseg != nullptr;
+  // K1: totals and row counters cleared; segment summaries
+  if (bid == 0 && threadIdx.x < 8) a.counters[threadIdx.x] = 0ull;
+  if (seg) {
+    for (int64_t w = gw; w < (m.nq + m.nk) * m.nbm; w += warps)
+      seg_summary_warp(m, w % (m.nq + m.nk), (int32_t)(w / (m.nq + m.nk)), a.qsum, a.kvsum, a.row_cnt, a.row_pcnt);
+  } else {
+    for (int64_t x = bid * kGridThreads + threadIdx.x; x < R; x += nb * kGridThreads) {
+      a.row_cnt[x] = 0;
+      a.row_pcnt[x] = 0;
+    }
+  }
+  for (int64_t x = bid * kGridThreads + threadIdx.x; x <= a.ht_mask; x += nb * kGridThreads) {
+    a.ht_key[x] = 0ull;
+    a.ht_val[x] = INT_MAX;
+  }
+  if (!grid_barrier(a.sync, a.err)) return;
+  // K2: classes, row counts, allowed pairs; undecided blocks to the deferred list
+  {
+    const int64_t xcs = (m.nk + kGridThreads - 1) / kGridThreads;
+    for (int64_t v = bid; v < xcs * R; v += nb) {
+      const int64_t row = v / xcs, xc = v - row * xcs;
+      classify_body(m, xc, row % m.nq, (int32_t)(row / m.nq), a.qsum, a.kvsum, a.block_mask, a.row_cnt, a.row_pcnt,
+                    a.counters, seg ? a.rep_list : nullptr, a.NB);
+    }
+  }
+  if (!grid_barrier(a.sync, a.err)) return;
+  if (seg) {
+    // the deferred list lives in rep_list, which scan_finalize fills later
+    count_deferred_body(m, a.rep_list, a.NB, a.block_mask, a.row_cnt, a.row_pcnt, a.counters, bid, nb);
+    if (!grid_barrier(a.sync, a.err)) return;
+  }
+  // K3: row_ptr, partial offsets and row order (CTA 0), then the active lists
+  if (bid == 0) {
+    scan_rows_body(R, a.row_cnt, a.row_pcnt, a.row_ptr, a.prow_ptr, a.counters);
+    __syncthreads();
+    row_order_body(R, m.nk, a.row_cnt, a.row_hist, a.row_order);
+  }
+  if (!grid_barrier(a.sync, a.err)) return;
+  for (int64_t row = gw; row < R; row += warps)
+    compact_warp(m, row, a.block_mask, a.row_ptr, a.prow_ptr, a.active_rows, a.active_cols, a.mask_next,
+                 a.bounds_start, a.bounds_end, a.part_row, a.part_col, a.part_g);
+  if (!grid_barrier(a.sync, a.err)) return;
+  // K4: words and hashes, first occurrences, pattern indices, patterns (one
+  // warp per partial block / pattern)
+  {
+    __shared__ int32_t s_kv[kGridThreads / 32][128];  // a warp's key segment IDs (bk <= 128)
+    const int64_t Ap = (int64_t)a.counters[1];
+    for (int64_t k = gw; k < Ap; k += warps) hash_warp(m, a, k, s_kv[threadIdx.x >> 5]);
+    if (!grid_barrier(a.sync, a.err)) return;
+    for (int64_t k = gw; k < Ap; k += warps) dedup_warp(m, a, k);
+  }
+  if (!grid_barrier(a.sync, a.err)) return;
+  if (bid == 0) scan_finalize_body(a.counters, a.part_g, a.part_rep, a.part_pidx, a.mask_next, a.rep_list);
+  if (!grid_barrier(a.sync, a.err)) return;
+  {
+    int64_t P = (int64_t)a.counters[2];
+    if (P > a.cap_patterns) {
+      if (bid == 0 && threadIdx.x == 0) atomicOr(a.err, SPLASH_DEV_BAD_TABLE);
+      P = a.cap_patterns;
+    }
+    const int32_t words = m.bk / 32;
+    const int64_t n = (int64_t)m.bq * words;
+    const bool by_offset = m.qseg == nullptr && !m.ragged;
+    for (int64_t u = gw; u < P; u += warps) {
+      const int64_t k = a.rep_list[u];
+      uint32_t *dst = a.pattern_bits + u * n;
+      if (by_offset) {  // band only: the words in closed form
+        const int64_t row = a.part_row[k], c = a.part_col[k];
+        const int64_t r = row % m.nq;
+        for (int64_t x = threadIdx.x & 31; x < n; x += 32)
+          dst[x] = row_word(m, 0, r * m.bq + x / words, 0, c * m.bk + (x % words) * 32);
+      } else {
+        const uint32_t *src = a.part_bits + k * n;
+        for (int64_t x = threadIdx.x & 31; x < n; x += 32) dst[x] = src[x];
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------- fused build
@@ -1094,7 +1422,8 @@ void splash_mask_info_free_buffers(splash_mask_info *mi) {
                  mi->bounds_start, mi->bounds_end, mi->pattern_bits, mi->row_order,
                  mi->row_cnt, mi->row_pcnt, mi->prow_ptr, mi->seg_summary, mi->part_row,
                  mi->part_col, mi->part_g, mi->part_hash, mi->part_rep, mi->part_pidx,
-                 mi->rep_list, mi->counters, mi->row_hist};
+                 mi->rep_list, mi->counters, mi->row_hist, mi->grid_sync, mi->part_bits,
+                 mi->ht_key, mi->ht_val};
   for (void *p : dev)
     if (p) cudaFree(p);
   void *host[] = {mi->h_counters};
@@ -1248,6 +1577,68 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
   }
 
   int32_t *qsum = mi->seg_summary, *kvsum = mi->seg_summary + 2 * R;
+  if (async && NB <= kGridMaxBlocks && p_bound <= kGridMaxPartials) {
+    // the whole pipeline as one persistent kernel (cooperative launch: every
+    // CTA resident; its grid barrier state starts cleared)
+    if ((st = reserve_patterns(p_bound)) != SPLASH_OK) return st;
+    if (mi->grid_sync == nullptr && (st = map_alloc(cudaMalloc(&mi->grid_sync, 2 * sizeof(unsigned int)))) != SPLASH_OK)
+      return st;
+    // per-partial words (p_bound bounds the partial blocks too) and the hash
+    // table, at least twice as large
+    const int64_t words_per = (int64_t)bq * (bk / 32);
+    if ((st = map_alloc(grow(mi->part_bits, mi->cap_part_bits, p_bound * words_per))) != SPLASH_OK) return st;
+    mi->cap_part_bits = std::max(mi->cap_part_bits, p_bound * words_per);
+    int64_t ht = 64;
+    while (ht < 2 * p_bound) ht <<= 1;
+    if ((st = map_alloc(grow(mi->ht_key, mi->cap_ht, ht))) != SPLASH_OK) return st;
+    if ((st = map_alloc(grow(mi->ht_val, mi->cap_ht, ht))) != SPLASH_OK) return st;
+    mi->cap_ht = std::max(mi->cap_ht, ht);
+    static int per_sm[64] = {0};
+    if (dev < 64 && per_sm[dev] == 0) {
+      int n = 0;
+      SPLASH_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, build_grid_kernel, kGridThreads, 0));
+      per_sm[dev] = std::max(1, std::min(n, 2));
+    }
+    const unsigned grid = (unsigned)(sms * (dev < 64 ? per_sm[dev] : 1));
+    GridArgs a;
+    a.qsum = qsum;
+    a.kvsum = kvsum;
+    a.block_mask = mi->block_mask;
+    a.row_cnt = mi->row_cnt;
+    a.row_pcnt = mi->row_pcnt;
+    a.row_ptr = mi->row_ptr;
+    a.prow_ptr = mi->prow_ptr;
+    a.row_hist = mi->row_hist;
+    a.row_order = mi->row_order;
+    a.active_rows = mi->active_rows;
+    a.active_cols = mi->active_cols;
+    a.mask_next = mi->mask_next;
+    a.bounds_start = mi->bounds_start;
+    a.bounds_end = mi->bounds_end;
+    a.part_row = mi->part_row;
+    a.part_col = mi->part_col;
+    a.part_g = mi->part_g;
+    a.part_rep = mi->part_rep;
+    a.part_pidx = mi->part_pidx;
+    a.rep_list = mi->rep_list;
+    a.part_hash = mi->part_hash;
+    a.counters = mi->counters;
+    a.pattern_bits = mi->pattern_bits;
+    a.cap_patterns = mi->cap_patterns;
+    a.NB = NB;
+    a.part_bits = mi->part_bits;
+    a.ht_key = mi->ht_key;
+    a.ht_val = mi->ht_val;
+    a.ht_mask = ht - 1;
+    a.sync = mi->grid_sync;
+    a.err = err;
+    SPLASH_CUDA_TRY(cudaMemsetAsync(mi->grid_sync, 0, 2 * sizeof(unsigned int), stream));
+    void *args[] = {&m, &a};
+    SPLASH_CUDA_TRY(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(build_grid_kernel), dim3(grid),
+                                                dim3(kGridThreads), args, 0, stream));
+    splash_count_launches(1);
+    return finish_async();
+  }
   if (seg) {
     // (the summary kernel also clears the row counters and the totals)
     dim3 grid((unsigned)((nq + nk + 7) / 8), (unsigned)nbm);
