@@ -503,15 +503,14 @@ __device__ __forceinline__ void scan_rows_body(int64_t R, const int32_t *row_cnt
 // ---------------------------------------------------------------- K3 compact
 // One warp per row (b_mask, r): columns in chunks of 32, ballots give each
 // active block its position.
-__device__ __forceinline__ void compact_warp(const DevMask &m, int64_t row, const int8_t *block_mask,
-                                             const int32_t *row_ptr, const int32_t *prow_ptr, int32_t *active_rows,
-                                             int32_t *active_cols, int32_t *mask_next, uint8_t *bounds_start,
-                                             uint8_t *bounds_end, int32_t *part_row, int32_t *part_col,
-                                             int32_t *part_g) {
+// g0 .. gend: the row's range of the active lists; k0: its first partial index
+__device__ __forceinline__ void compact_warp(const DevMask &m, int64_t row, int32_t g0, int32_t gend, int32_t k0,
+                                             const int8_t *block_mask, int32_t *active_rows, int32_t *active_cols,
+                                             int32_t *mask_next, uint8_t *bounds_start, uint8_t *bounds_end,
+                                             int32_t *part_row, int32_t *part_col, int32_t *part_g) {
   const int lane = threadIdx.x & 31;
   const int32_t r = (int32_t)(row % m.nq);
-  const int32_t g0 = row_ptr[row], gend = row_ptr[row + 1];
-  int32_t g = g0, k = prow_ptr[row];
+  int32_t g = g0, k = k0;
   const unsigned lt = (1u << lane) - 1u;
   for (int64_t cb = 0; cb < m.nk; cb += 32) {
     const int64_t c = cb + lane;
@@ -544,8 +543,8 @@ __global__ void compact_kernel(DevMask m, int64_t R, const int8_t *block_mask,
                                int32_t *part_col, int32_t *part_g) {
   const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (row >= R) return;
-  compact_warp(m, row, block_mask, row_ptr, prow_ptr, active_rows, active_cols, mask_next, bounds_start, bounds_end,
-               part_row, part_col, part_g);
+  compact_warp(m, row, row_ptr[row], row_ptr[row + 1], prow_ptr[row], block_mask, active_rows, active_cols,
+               mask_next, bounds_start, bounds_end, part_row, part_col, part_g);
 }
 
 // ---------------------------------------------------------------- K4 patterns
@@ -854,6 +853,7 @@ constexpr int kGridThreads = 256;
 constexpr uint64_t kGridBarrierNs = 2000000000ull;  // 2 s
 constexpr int64_t kGridMaxBlocks = (int64_t)1 << 22;  // larger tables take the launch chain
 constexpr int64_t kGridMaxPartials = 65536;
+constexpr int64_t kGridRowwiseMaxRows = 2048;  // rows a warp scans to place its own row
 
 struct GridArgs {
   int32_t *qsum, *kvsum;
@@ -1061,24 +1061,63 @@ __global__ void __launch_bounds__(kGridThreads) build_grid_kernel(DevMask m, Gri
     count_deferred_body(m, a.rep_list, a.NB, a.block_mask, a.row_cnt, a.row_pcnt, a.counters, bid, nb);
     if (!grid_barrier(a.sync, a.err)) return;
   }
-  // K3: row_ptr, partial offsets and row order (CTA 0), then the active lists
-  if (bid == 0) {
-    scan_rows_body(R, a.row_cnt, a.row_pcnt, a.row_ptr, a.prow_ptr, a.counters);
-    __syncthreads();
-    row_order_body(R, m.nk, a.row_cnt, a.row_hist, a.row_order);
-  }
-  if (!grid_barrier(a.sync, a.err)) return;
-  for (int64_t row = gw; row < R; row += warps)
-    compact_warp(m, row, a.block_mask, a.row_ptr, a.prow_ptr, a.active_rows, a.active_cols, a.mask_next,
-                 a.bounds_start, a.bounds_end, a.part_row, a.part_col, a.part_g);
-  if (!grid_barrier(a.sync, a.err)) return;
-  // K4: words and hashes, first occurrences, pattern indices, patterns (one
-  // warp per partial block / pattern)
+  // K3: row_ptr, partial offsets, row order and the active lists
   {
     __shared__ int32_t s_kv[kGridThreads / 32][128];  // a warp's key segment IDs (bk <= 128)
-    const int64_t Ap = (int64_t)a.counters[1];
-    for (int64_t k = gw; k < Ap; k += warps) hash_warp(m, a, k, s_kv[threadIdx.x >> 5]);
+    int32_t *kv = s_kv[threadIdx.x >> 5];
+    if (R <= kGridRowwiseMaxRows) {
+      // one warp per row: its offsets are the sums over the rows before it,
+      // its place in the row order the number of rows with more active
+      // blocks or as many and a smaller index (a stable sort by count)
+      const int lane = threadIdx.x & 31;
+      for (int64_t row = gw; row < R; row += warps) {
+        const int32_t my = a.row_cnt[row], myp = a.row_pcnt[row];
+        int32_t ga = 0, gp = 0, ahead = 0;
+        for (int64_t x = lane; x < R; x += 32) {
+          const int32_t cx = a.row_cnt[x];
+          if (x < row) {
+            ga += cx;
+            gp += a.row_pcnt[x];
+          }
+          ahead += (cx > my || (cx == my && x < row)) ? 1 : 0;
+        }
+        for (int off = 16; off; off >>= 1) {
+          ga += __shfl_xor_sync(0xffffffffu, ga, off);
+          gp += __shfl_xor_sync(0xffffffffu, gp, off);
+          ahead += __shfl_xor_sync(0xffffffffu, ahead, off);
+        }
+        if (lane == 0) {
+          a.row_ptr[row] = ga;
+          a.prow_ptr[row] = gp;
+          a.row_order[ahead] = (int32_t)row;
+          if (my > 0) atomicMax(&a.counters[4], (unsigned long long)my);
+          if (row == R - 1) {
+            a.row_ptr[R] = ga + my;
+            a.prow_ptr[R] = gp + myp;
+            a.counters[0] = (unsigned long long)(ga + my);
+            a.counters[1] = (unsigned long long)(gp + myp);
+          }
+        }
+        compact_warp(m, row, ga, ga + my, gp, a.block_mask, a.active_rows, a.active_cols, a.mask_next,
+                     a.bounds_start, a.bounds_end, a.part_row, a.part_col, a.part_g);
+      }
+    } else {
+      if (bid == 0) {
+        scan_rows_body(R, a.row_cnt, a.row_pcnt, a.row_ptr, a.prow_ptr, a.counters);
+        __syncthreads();
+        row_order_body(R, m.nk, a.row_cnt, a.row_hist, a.row_order);
+      }
+      if (!grid_barrier(a.sync, a.err)) return;
+      for (int64_t row = gw; row < R; row += warps)
+        compact_warp(m, row, a.row_ptr[row], a.row_ptr[row + 1], a.prow_ptr[row], a.block_mask, a.active_rows,
+                     a.active_cols, a.mask_next, a.bounds_start, a.bounds_end, a.part_row, a.part_col, a.part_g);
+    }
     if (!grid_barrier(a.sync, a.err)) return;
+    // words and hashes (one warp per partial block)
+    for (int64_t k = gw; k < (int64_t)a.counters[1]; k += warps) hash_warp(m, a, k, kv);
+    if (!grid_barrier(a.sync, a.err)) return;
+    // first occurrences (one warp per partial block)
+    const int64_t Ap = (int64_t)a.counters[1];
     for (int64_t k = gw; k < Ap; k += warps) dedup_warp(m, a, k);
   }
   if (!grid_barrier(a.sync, a.err)) return;
