@@ -345,7 +345,8 @@ splash_status splash_attention_bwd(const void *q, const void *k, const void *v, 
                         reinterpret_cast<uintptr_t>(lse) | reinterpret_cast<uintptr_t>(workspace);
   if (mis & 15u) return SPLASH_ERR_INVALID_ARG;
   if (workspace_bytes < splash_attention_bwd_workspace_bytes(B, Hq, Lq, dqk)) return SPLASH_ERR_INVALID_ARG;
-  if (dqk != dv || (dqk != 64 && dqk != 128) || mi->bq != 128 || mi->bk != 128) return SPLASH_ERR_UNSUPPORTED;
+  if (dqk != dv || (dqk != 64 && dqk != 128) || (mi->bq != 128 && mi->bq != 256) || mi->bk != 128)
+    return SPLASH_ERR_UNSUPPORTED;
   return splash_attention_bwd_launch(q, k, v, out, lse, dout, B, Hq, Hkv, Lq, Lk, dqk, mi, scale, softcap, dq, dk,
                                      dv_out, workspace, static_cast<cudaStream_t>(cuda_stream), err);
 }

@@ -112,13 +112,16 @@ struct BwdCfg {
 struct BwdParams {
   int32_t B, Hq, Hkv, G;
   int64_t Lq, Lk;
-  int64_t Lq_pad;               // nq * 128: row stride of the padded workspace arrays
+  int64_t Lq_pad;               // nq * bq: row stride of the padded workspace arrays
   int32_t nq, nk, nbm;
+  // q-blocks of 128 or 256 rows; an iteration takes 128 query rows (one half
+  // of a 256-row q-block), so a block's active entry is visited `halves` times
+  int32_t bq, halves;
   int64_t num_items;            // B * Hkv * nk
   const int32_t *col_ptr;       // [nbm*nk + 1]
   const int32_t *col_rows;      // q-block of each active block, column-major
   const int32_t *col_next;      // its pattern index, -1 for full blocks
-  const uint32_t *pattern_t;    // [P][128 keys][4 words]: bit i%32 of word i/32 = (query i, key) allowed
+  const uint32_t *pattern_t;    // [P][128 keys][bq/32 words]: bit i%32 of word i/32 = (query i, key) allowed
   const unsigned long long *counters;  // device totals of the MaskInfo build ([2] = patterns)
   int64_t cap_patterns;
   const float *lse;             // [B*Hq*Lq_pad] (copied from the forward's, padding rows 0)
@@ -159,10 +162,13 @@ __device__ __forceinline__ int64_t bwd_item_of_round(const BwdParams &p, int64_t
   return w < p.num_items ? w : -2;
 }
 
-// (query head, q-block, pattern) of the item's iteration t: heads outermost
+// (query head, q-block, its 128-row half, pattern) of the item's iteration t:
+// heads outermost, halves innermost
 __device__ __forceinline__ void bwd_step(const BwdParams &p, const BwdItem &it, int32_t t, int32_t &h,
-                                         int32_t &i, int32_t &mn) {
-  const int32_t hh = t / it.cnt, e = it.e0 + t % it.cnt;
+                                         int32_t &i, int32_t &half, int32_t &mn) {
+  const int32_t u = t / p.halves;
+  half = t - u * p.halves;
+  const int32_t hh = u / it.cnt, e = it.e0 + u % it.cnt;
   h = it.kvh * p.G + hh;
   i = p.col_rows[e];
   mn = p.col_next[e];
@@ -172,6 +178,11 @@ __device__ __forceinline__ void bwd_step(const BwdParams &p, const BwdItem &it, 
     i = 0;
     mn = -1;
   }
+}
+
+// first query row (within the head) of iteration (q-block i, half)
+__device__ __forceinline__ int64_t bwd_q0(const BwdParams &p, int32_t i, int32_t half) {
+  return (int64_t)i * p.bq + (int64_t)half * 128;
 }
 
 struct BwdBars {
@@ -243,7 +254,7 @@ __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const C
     if (w == -1) break;
     if (w < 0) continue;
     const BwdItem it = bwd_item(p, w);
-    const int32_t N = p.G * it.cnt;
+    const int32_t N = p.G * it.cnt * p.halves;
     if (N == 0) continue;
     if (kv > 0 && !(ok = mbar_wait(bar.kv_empty(), (kv - 1) & 1u, abort, p.timeout_ns))) break;
     const int32_t ykv = (int32_t)(((int64_t)it.b * p.Hkv + it.kvh) * p.Lk + (int64_t)it.j * 128);
@@ -254,15 +265,15 @@ __device__ void bwd_producer(const BwdParams &p, const CUtensorMap *tmQ, const C
     }
     ++kv;
     for (int32_t t = 0; t < N; ++t, ++n) {
-      int32_t h, i, mn;
-      bwd_step(p, it, t, h, i, mn);
+      int32_t h, i, half, mn;
+      bwd_step(p, it, t, h, i, half, mn);
       const int st = n & 1;
       if (n >= 2 && !(ok = mbar_wait(bar.q_empty(st), ((n >> 1) - 1) & 1u, abort, p.timeout_ns))) break;
       // tiles from the caller's tensors (rows past a ragged Lq read the next
       // head's rows or the zero fill, all masked); LSE and D from the padded
       // workspace (whole blocks, always in bounds)
-      const int64_t row = ((int64_t)it.b * p.Hq + h) * p.Lq + (int64_t)i * 128;
-      const int64_t prow = ((int64_t)it.b * p.Hq + h) * p.Lq_pad + (int64_t)i * 128;
+      const int64_t row = ((int64_t)it.b * p.Hq + h) * p.Lq + bwd_q0(p, i, half);
+      const int64_t prow = ((int64_t)it.b * p.Hq + h) * p.Lq_pad + bwd_q0(p, i, half);
       mbar_arrive_expect_tx(bar.q_full(st), C::TILE + 1024);
       for (int ch = 0; ch < C::CH; ++ch)
         tma_load_2d(s0 + C::OFF_Q + st * C::TILE + ch * C::CHUNK, tmQ, ch * 64, (int32_t)row, bar.q_full(st));
@@ -355,7 +366,7 @@ __device__ void bwd_mma(const BwdParams &p, uint32_t tmem, uint32_t s0, const Bw
     if (w == -1) break;
     if (w < 0) continue;
     const BwdItem it = bwd_item(p, w);
-    const int32_t N = p.G * it.cnt;
+    const int32_t N = p.G * it.cnt * p.halves;
     if (N == 0) continue;
     if (!(ok = mbar_wait(bar.kv_full(), kv & 1u, abort, p.timeout_ns))) break;
     ++kv;
@@ -489,7 +500,7 @@ __device__ void bwd_work(const BwdParams &p, const CUtensorMap *tmDQ, uint32_t t
     if (w == -1) break;
     if (w < 0) continue;
     const BwdItem it = bwd_item(p, w);
-    const int32_t N = p.G * it.cnt;
+    const int32_t N = p.G * it.cnt * p.halves;
     const int64_t krow = ((int64_t)it.b * p.Hkv + it.kvh) * p.Lk + (int64_t)it.j * 128 + jj;
     __nv_bfloat16 *dk_row = p.dk + krow * D + wg * (D / 2);
     __nv_bfloat16 *dv_row = p.dv + krow * D + wg * (D / 2);
@@ -503,8 +514,8 @@ __device__ void bwd_work(const BwdParams &p, const CUtensorMap *tmDQ, uint32_t t
       continue;
     }
     for (int32_t t = 0; t < N && ok; ++t, ++n) {
-      int32_t h, i, mn;
-      bwd_step(p, it, t, h, i, mn);
+      int32_t h, i, half, mn;
+      bwd_step(p, it, t, h, i, half, mn);
       const int st = n & 1;
       const uint32_t ld = s0 + C::OFF_LD + st * 1024 + 256u * wg;  // this half's LSE; D at +512
       // ---- P^T(n) = exp(S^T - LSE): S^T lane = key jj, columns = queries 64wg + x
@@ -520,7 +531,7 @@ __device__ void bwd_work(const BwdParams &p, const CUtensorMap *tmDQ, uint32_t t
         tmem_ld32(tS + 32u, r1);
         uint32_t bits0 = 0xffffffffu, bits1 = 0xffffffffu;
         if (mn >= 0) {
-          const uint32_t *src = p.pattern_t + ((int64_t)mn * 128 + jj) * 4 + 2 * wg;
+          const uint32_t *src = p.pattern_t + ((int64_t)mn * 128 + jj) * (p.bq / 32) + 4 * half + 2 * wg;
           bits0 = __ldg(src);
           bits1 = __ldg(src + 1);
         }
@@ -595,7 +606,7 @@ __device__ void bwd_work(const BwdParams &p, const CUtensorMap *tmDQ, uint32_t t
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.ds_ready());
-      prev_row = (int32_t)(((int64_t)it.b * p.Hq + h) * p.Lq_pad + (int64_t)i * 128 + wq * 32);
+      prev_row = (int32_t)(((int64_t)it.b * p.Hq + h) * p.Lq_pad + bwd_q0(p, i, half) + wq * 32);
     }
     if (!ok) break;
     // ---- the item's last dQ, then dK, dV (complete once that dQ has landed)
@@ -708,7 +719,7 @@ splash_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
 }
 
 // ------------------------------------------------------------ small kernels
-// Padded workspace rows r = bh * Lq_pad + i (whole 128-row blocks per head):
+// Padded workspace rows r = bh * Lq_pad + i (whole q-blocks per head):
 // D_r = sum_x dout[bh*Lq + i][x] * out[...][x] (fp32) and a copy of the
 // forward's LSE for i < Lq, 0 on padding rows; the dq accumulator rows are
 // cleared.  One 16-lane half-warp per row (a warp takes two consecutive rows,
@@ -842,16 +853,18 @@ __global__ void col_fill_kernel(const int8_t *block_mask, const int32_t *row_ptr
 }
 
 // Transposed pattern bits: word (p, key j, w) holds, at bit b, whether query
-// 32w + b may see key j.  Source: pattern_bits [p][query][4 words over keys].
+// 32w + b may see key j (bq / 32 words per key).  Source: pattern_bits
+// [p][query][4 words over the 128 keys].
 __global__ void pattern_transpose_kernel(const uint32_t *pattern_bits, const unsigned long long *counters,
-                                         int64_t cap_patterns, uint32_t *pattern_t) {
+                                         int64_t cap_patterns, int32_t bq, uint32_t *pattern_t) {
   const int64_t np = min((int64_t)counters[2], cap_patterns);
-  const int64_t total = np * 128 * 4;
+  const int32_t qw = bq / 32;
+  const int64_t total = np * 128 * qw;
   for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < total;
        x += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t pidx = x / 512;
-    const int32_t j = (int32_t)((x / 4) % 128), w = (int32_t)(x % 4);
-    const uint32_t *src = pattern_bits + pidx * 128 * 4;
+    const int64_t pidx = x / (128 * qw);
+    const int32_t j = (int32_t)((x / qw) % 128), w = (int32_t)(x % qw);
+    const uint32_t *src = pattern_bits + pidx * bq * 4;
     uint32_t v = 0;
 #pragma unroll 8
     for (int b = 0; b < 32; ++b) v |= ((src[(32 * w + b) * 4 + (j >> 5)] >> (j & 31)) & 1u) << b;
@@ -932,10 +945,11 @@ splash_status launch_bwd(const void *q, const void *k, const void *v, const void
 
 using namespace splash;
 
-// fp32 dq accumulator, D and a copy of LSE, each over whole 128-row blocks
-// per head (rows past a ragged Lq are padding)
+// fp32 dq accumulator, D and a copy of LSE, each over whole q-blocks per
+// head (rows past a ragged Lq are padding); sized for 256-row blocks, which
+// covers 128-row ones
 size_t splash_attention_bwd_workspace_bytes(int32_t B, int32_t Hq, int64_t Lq, int32_t dqk) {
-  const size_t rows = (size_t)B * Hq * (size_t)((Lq + 127) / 128 * 128);
+  const size_t rows = (size_t)B * Hq * (size_t)((Lq + 255) / 256 * 256);
   return ((rows * dqk * 4 + 255) & ~(size_t)255) + 2 * ((rows * 4 + 255) & ~(size_t)255);
 }
 
@@ -948,14 +962,15 @@ splash_status splash_attention_bwd_launch(const void *q, const void *k, const vo
   // made once per build of the table and reused by later calls
   const int64_t ncols = (int64_t)mi->batch_rows * mi->nk;
   const bool fresh = mi->t_gen != 0 && mi->t_gen == mi->build_gen && mi->t_ready != nullptr;
-  if (!fresh &&
-      (mi->t_cap_cols < ncols || mi->t_cap_active < mi->cap_blocks || mi->t_cap_patterns < mi->cap_patterns)) {
+  const int64_t pwords = 128 * (mi->bq / 32);  // transposed words per pattern
+  if (!fresh && (mi->t_cap_cols < ncols || mi->t_cap_active < mi->cap_blocks ||
+                 mi->t_cap_patterns < mi->cap_patterns * pwords)) {
     splash_mask_info_free_transposed(mi);
     if (cudaMalloc(&mi->t_col_cnt, sizeof(int32_t) * ncols) != cudaSuccess ||
         cudaMalloc(&mi->t_col_ptr, sizeof(int32_t) * (ncols + 1)) != cudaSuccess ||
         cudaMalloc(&mi->t_col_rows, sizeof(int32_t) * std::max<int64_t>(mi->cap_blocks, 1)) != cudaSuccess ||
         cudaMalloc(&mi->t_col_next, sizeof(int32_t) * std::max<int64_t>(mi->cap_blocks, 1)) != cudaSuccess ||
-        cudaMalloc(&mi->t_pattern_bits, sizeof(uint32_t) * 512 * std::max<int64_t>(mi->cap_patterns, 1)) !=
+        cudaMalloc(&mi->t_pattern_bits, sizeof(uint32_t) * pwords * std::max<int64_t>(mi->cap_patterns, 1)) !=
             cudaSuccess) {
       splash_mask_info_free_transposed(mi);
       cudaGetLastError();
@@ -963,7 +978,7 @@ splash_status splash_attention_bwd_launch(const void *q, const void *k, const vo
     }
     mi->t_cap_cols = ncols;
     mi->t_cap_active = mi->cap_blocks;
-    mi->t_cap_patterns = mi->cap_patterns;
+    mi->t_cap_patterns = mi->cap_patterns * pwords;
   }
   int dev = 0;
   SPLASH_CUDA_TRY(cudaGetDevice(&dev));
@@ -981,8 +996,8 @@ splash_status splash_attention_bwd_launch(const void *q, const void *k, const vo
                                              (int32_t)mi->nq, (int32_t)mi->nk, ncols, mi->t_col_ptr,
                                              mi->t_col_rows, mi->t_col_next);
   pattern_transpose_kernel<<<(unsigned)std::max<int64_t>(1, std::min<int64_t>(
-                                 (512 * std::max<int64_t>(mi->cap_patterns, 1) + 255) / 256, sms * 8)),
-                             256, 0, stream>>>(mi->pattern_bits, mi->counters, mi->cap_patterns,
+                                 (pwords * std::max<int64_t>(mi->cap_patterns, 1) + 255) / 256, sms * 8)),
+                             256, 0, stream>>>(mi->pattern_bits, mi->counters, mi->cap_patterns, mi->bq,
                                                mi->t_pattern_bits);
   SPLASH_CUDA_TRY(cudaGetLastError());
   splash_count_launches(4);
@@ -992,7 +1007,7 @@ splash_status splash_attention_bwd_launch(const void *q, const void *k, const vo
   }
 
   const int64_t rows = (int64_t)B * Hq * Lq;
-  const int64_t Lq_pad = (Lq + 127) / 128 * 128, rows_pad = (int64_t)B * Hq * Lq_pad;
+  const int64_t Lq_pad = mi->nq * mi->bq, rows_pad = (int64_t)B * Hq * Lq_pad;
   float *dq_acc = static_cast<float *>(workspace);
   float *delta = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                            ((rows_pad * d * 4 + 255) & ~(int64_t)255));
@@ -1020,6 +1035,8 @@ splash_status splash_attention_bwd_launch(const void *q, const void *k, const vo
   prm.nq = (int32_t)mi->nq;
   prm.nk = (int32_t)mi->nk;
   prm.nbm = mi->batch_rows;
+  prm.bq = mi->bq;
+  prm.halves = mi->bq / 128;
   prm.num_items = (int64_t)B * Hkv * mi->nk;
   prm.col_ptr = mi->t_col_ptr;
   prm.col_rows = mi->t_col_rows;

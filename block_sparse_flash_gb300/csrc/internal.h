@@ -92,7 +92,7 @@ struct splash_mask_info {
   int32_t *t_col_rows = nullptr;      // [cap_blocks] q-block of each active block, by column
   int32_t *t_col_next = nullptr;      // [cap_blocks] its pattern index or -1
   uint32_t *t_pattern_bits = nullptr; // [cap_patterns][bk][bq/32], bit of (query, key) by key row
-  int64_t t_cap_cols = 0, t_cap_active = 0, t_cap_patterns = 0;
+  int64_t t_cap_cols = 0, t_cap_active = 0, t_cap_patterns = 0;  // (t_cap_patterns counts words)
   uint64_t t_gen = 0;             // build_gen the copy was made from (0: none)
   cudaEvent_t t_ready = nullptr;  // recorded on the stream that made it
 };

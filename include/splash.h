@@ -370,11 +370,11 @@ splash_status splash_attention_merge(const float *o_part, const float *lse_part,
  *   workspace  device, 16-byte aligned, at least
  *              splash_attention_bwd_workspace_size(B, Hq, Lq, dqk) bytes
  *              (an fp32 dq accumulator, D and a copy of lse, over whole
- *              128-row blocks per head); caller-owned, overwritten.
+ *              256-row blocks per head); caller-owned, overwritten.
  * All device pointers 16-byte aligned.  Supported: dqk == dv in {64, 128}
- * and MaskInfo blocks bq = bk = 128, any Lq / Lk (ragged lengths as in the
- * forward; the workspace covers whole 128-row blocks per head); other valid
- * shapes return SPLASH_ERR_UNSUPPORTED.  dq is accumulated with fp32 atomic additions, so
+ * and MaskInfo blocks bk = 128 with bq = 128 or 256 (a 256-row q-block is
+ * taken as two 128-row halves), any Lq / Lk (ragged lengths as in the
+ * forward); other valid shapes return SPLASH_ERR_UNSUPPORTED.  dq is accumulated with fp32 atomic additions, so
  * its last bits may differ between runs; dk and dv are deterministic.
  * Errors as for splash_attention_fwd.
  */

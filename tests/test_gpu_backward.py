@@ -60,7 +60,7 @@ CASES = [
 ]
 
 
-def make(bsf, B, Hq, Hkv, L, d, causal=True, wl=-1, wr=-1, docs=False, seed=0, kv_seg=None):
+def make(bsf, B, Hq, Hkv, L, d, causal=True, wl=-1, wr=-1, docs=False, seed=0, kv_seg=None, bq=128):
     q = workloads.normal_bf16((B, Hq, L, d), seed + 1)
     k = workloads.normal_bf16((B, Hkv, L, d), seed + 2)
     v = workloads.normal_bf16((B, Hkv, L, d), seed + 3)
@@ -68,7 +68,7 @@ def make(bsf, B, Hq, Hkv, L, d, causal=True, wl=-1, wr=-1, docs=False, seed=0, k
     qs = workloads.random_segment_ids(B, L, seed + 4, 4, True) if docs else None
     ks = kv_seg if kv_seg is not None else qs
     mi = bsf.build_mask_info(bsf.MaskSpec(causal, wl, wr, qs.cuda() if qs is not None else None,
-                                          ks.cuda() if ks is not None else None), L, L, 128, 128)
+                                          ks.cuda() if ks is not None else None), L, L, bq, 128)
     ospec = oracle.MaskSpec(causal, wl, wr, qs.numpy() if qs is not None else None,
                             ks.numpy() if ks is not None else None)
     return q, k, v, g, mi, ospec
@@ -113,6 +113,53 @@ def test_backward_matches_the_oracle(bsf, case):
             compare_grad(dv, ref["dv"], f"{label}: dv")]
     print(label, errs)
     mi.close()
+
+
+TALL_CASES = [
+    # label, B, Hq, Hkv, L, d, softcap, mask kwargs -- tables of 256-row q-blocks
+    ("256-row blocks, causal MHA d128", 1, 2, 2, 1024, 128, 0.0, dict(causal=True)),
+    ("256-row blocks, documents + causal GQA, batch 2", 2, 4, 2, 768, 128, 0.0, dict(causal=True, docs=True)),
+    ("256-row blocks, ragged causal 1000", 1, 2, 1, 1000, 128, 0.0, dict(causal=True)),
+    ("256-row blocks, window 300 + causal d64 cap 30", 1, 2, 2, 896, 64, 30.0, dict(causal=True, wl=299)),
+]
+
+
+@pytest.mark.parametrize("case", TALL_CASES, ids=[c[0] for c in TALL_CASES])
+def test_backward_with_256_row_blocks_matches_the_oracle(bsf, case):
+    """A table of 256-row q-blocks: the backward takes each as two 128-row
+    halves (the half's rows of Q, dO, LSE, D and its words of the transposed
+    pattern); a half the mask leaves empty for a key block contributes
+    nothing."""
+    label, B, Hq, Hkv, L, d, cap, kw = case
+    q, k, v, g, mi, ospec = make(bsf, B, Hq, Hkv, L, d, seed=17 * TALL_CASES.index(case) + 3, bq=256, **kw)
+    assert mi.shape()["bq"] == 256
+    scale = 1.0 / math.sqrt(d)
+    (dq, dk, dv), ref = run_both(bsf, q, k, v, g, mi, ospec, scale, cap)
+    extra = d_term_allowance(q, k, v, g, ospec, scale, cap)
+    errs = [compare_grad(dq, ref["dq"], f"{label}: dq", extra), compare_grad(dk, ref["dk"], f"{label}: dk"),
+            compare_grad(dv, ref["dv"], f"{label}: dv")]
+    print(label, errs)
+    mi.close()
+
+
+def test_256_row_blocks_give_the_same_key_gradients(bsf):
+    """dk and dv of a 256-row table equal those of the 128-row table bit for
+    bit: both visit the same 128-row pieces of a key block's column in the
+    same order, and a half that the mask leaves empty adds exact zeros."""
+    B, Hq, Hkv, L, d = 1, 4, 2, 1024, 128
+    grads = []
+    for bq in (128, 256):
+        q, k, v, g, mi, ospec = make(bsf, B, Hq, Hkv, L, d, seed=5, bq=bq)
+        qd, kd, vd, gd = q.cuda(), k.cuda(), v.cuda(), g.cuda()
+        mi128 = bsf.build_mask_info(bsf.MaskSpec(True), L, L, 128, 128)
+        out, lse = bsf.attention_fwd(qd, kd, vd, mi128, d ** -0.5)  # same forward for both
+        grads.append(bsf.attention_bwd(qd, kd, vd, out, lse, gd, mi, d ** -0.5))
+        torch.cuda.synchronize()
+        assert bsf.last_device_error() == 0
+        mi.close()
+        mi128.close()
+    assert torch.equal(grads[0][1], grads[1][1]) and torch.equal(grads[0][2], grads[1][2])
+    assert (grads[0][0].float() - grads[1][0].float()).abs().max().item() <= 2e-2 * grads[0][0].float().abs().max().item()
 
 
 def test_keys_no_query_sees_get_zero_gradients(bsf):
