@@ -77,6 +77,7 @@ struct splash_mask_info {
   // kernel; splash_mask_info_sync_counts waits for it and copies the totals
   cudaEvent_t counts_ready = nullptr;
   bool counts_pending = false;
+  bool counts_captured = false;  // the last build was captured into a graph (no event recorded)
 
   // capacities (elements)
   int64_t cap_rows = 0, cap_blocks = 0, cap_seg = 0, cap_patterns = 0, cap_hist = 0;

@@ -1548,7 +1548,12 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
 
   // a previous asynchronous build, possibly on another stream, may still be
   // running on the same buffers: keep it ordered before this one
-  if (mi->counts_pending && mi->counts_ready) SPLASH_CUDA_TRY(cudaStreamWaitEvent(stream, mi->counts_ready, 0));
+  // (not while the stream is being captured: a graph cannot wait on work
+  // outside it, and its own nodes already order a captured rebuild)
+  cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+  SPLASH_CUDA_TRY(cudaStreamIsCapturing(stream, &capturing));
+  if (capturing == cudaStreamCaptureStatusNone && mi->counts_pending && !mi->counts_captured && mi->counts_ready)
+    SPLASH_CUDA_TRY(cudaStreamWaitEvent(stream, mi->counts_ready, 0));
 
   uint32_t *err = splash_device_error_word(mi->device);
   // -- pattern buffer (bit-packed patterns, bq * bk / 8 bytes each).  Without
@@ -1579,10 +1584,12 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
   // the totals stay on the device; splash_mask_info_sync_counts copies them
   // once this event has completed
   auto finish_async = [&]() -> splash_status {
+    mi->counts_pending = true;
+    mi->counts_captured = capturing != cudaStreamCaptureStatusNone;
+    if (mi->counts_captured) return SPLASH_OK;  // replays are ordered by the caller
     if (mi->counts_ready == nullptr)
       SPLASH_CUDA_TRY(cudaEventCreateWithFlags(&mi->counts_ready, cudaEventDisableTiming));
     SPLASH_CUDA_TRY(cudaEventRecord(mi->counts_ready, stream));
-    mi->counts_pending = true;
     return SPLASH_OK;
   };
 
@@ -1746,7 +1753,11 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
 
 splash_status splash_mask_info_sync_counts(splash_mask_info *mi) {
   if (!mi->counts_pending) return SPLASH_OK;
-  SPLASH_CUDA_TRY(cudaEventSynchronize(mi->counts_ready));
+  // a rebuild captured into a graph recorded no event: wait for the device
+  if (mi->counts_captured)
+    SPLASH_CUDA_TRY(cudaDeviceSynchronize());
+  else
+    SPLASH_CUDA_TRY(cudaEventSynchronize(mi->counts_ready));
   SPLASH_CUDA_TRY(cudaMemcpy(mi->h_counters, mi->counters, sizeof(unsigned long long) * 8, cudaMemcpyDeviceToHost));
   mi->num_active = (int64_t)mi->h_counters[0];
   mi->num_partial = (int64_t)mi->h_counters[1];

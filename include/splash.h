@@ -119,7 +119,10 @@ typedef struct splash_mask_info splash_mask_info;
  * by later work on `cuda_stream` at once (work on another stream must wait
  * for it); the totals reach the host only when splash_mask_info_counts or
  * splash_mask_info_to_host asks for them.  A first build allocates the
- * table's device memory (cudaMalloc, which synchronises the device).
+ * table's device memory (cudaMalloc, which synchronises the device); a
+ * rebuild into a handle whose buffers are large enough can then be captured
+ * into a CUDA graph on `cuda_stream` (with the attention calls that use it);
+ * after a replay, synchronise the stream before asking for the totals.
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA, OOM; *out is NULL then.
  */
 splash_status splash_build_mask_info(const splash_mask_spec *spec, int64_t Lq, int64_t Lk,
