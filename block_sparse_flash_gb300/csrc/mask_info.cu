@@ -83,6 +83,16 @@ __device__ __forceinline__ int32_t q_segment(const DevMask &m, int32_t bm, int64
   return (m.qseg && i < m.Lq) ? m.qseg[(int64_t)bm * m.Lq + i] : 0;  // padding rows: unused
 }
 
+// q_segment issued as a volatile load of the read-only segment array, so
+// that a batch of them stays where it is written (the compiler would
+// otherwise sink each load to its first use, one memory latency per row)
+__device__ __forceinline__ int32_t q_segment_early(const DevMask &m, int32_t bm, int64_t i) {
+  if (!(m.qseg && i < m.Lq)) return 0;
+  int32_t v;
+  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(m.qseg + (int64_t)bm * m.Lq + i));
+  return v;
+}
+
 // The band part in closed form: key j is allowed for query i iff
 // i - W <= j <= i + A, with A = 0 for causal (and min with the right window)
 // and W the left window; an unbounded side is kBandInf.
@@ -146,6 +156,36 @@ __device__ __forceinline__ void sorted_run(const int32_t *s_kv, int32_t n, int32
     if (s_kv[mid] <= sq) lo = mid + 1; else hi = mid;
   }
   b = lo - 1;
+}
+
+// For a block whose n real keys have non-decreasing IDs (s_kv, staged), the
+// run [ra, rb] of keys with ID sq (the caller's query ID; each lane its own)
+// is ra = #(IDs < sq), rb = #(IDs <= sq) - 1: counted by ballots over the
+// keys lane, lane+32, .. (bk <= 128), one pass per distinct sq in the warp.
+// Warp-collective; it replaces two binary searches of dependent shared-memory
+// loads per row.
+__device__ __forceinline__ void sorted_run_warp(const int32_t *s_kv, int32_t n, int32_t sq, int32_t &ra,
+                                                int32_t &rb) {
+  const int lane = threadIdx.x & 31;
+  int32_t kid[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) kid[j] = s_kv[lane + 32 * j];
+  unsigned todo = 0xffffffffu;
+  while (todo != 0u) {  // warp-uniform
+    const int32_t v = __shfl_sync(0xffffffffu, sq, __ffs(todo) - 1);
+    int32_t lt = 0, le = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const bool valid = lane + 32 * j < n;
+      lt += __popc(__ballot_sync(0xffffffffu, valid && kid[j] < v));
+      le += __popc(__ballot_sync(0xffffffffu, valid && kid[j] <= v));
+    }
+    if (sq == v) {
+      ra = lt;
+      rb = le - 1;
+    }
+    todo &= ~__ballot_sync(0xffffffffu, sq == v);
+  }
 }
 
 // row_word with the key block's segment IDs staged in shared memory (its
@@ -246,31 +286,43 @@ __device__ void classify_body(const DevMask &m, int64_t xc, int64_t r, int32_t b
     if (xc == 0)
       for (int32_t di = threadIdx.x; di < m.bq; di += blockDim.x) cnt += band_row_count(m, A, W, r * m.bq + di);
   } else if (c < m.nk) {
-    const int64_t c0 = c * m.bk, c1 = c0 + m.bk - 1;
     // the band's allowed pairs of the block: none or all of them in closed
-    // form, counted row by row only for a band-partial block
+    // form; a band-partial block's are summed row by row below, by its warp
     int64_t A, W;
     band_limits(m, A, W);
-    const int bcls = band_block_class(m, A, W, r, c);
-    if (bcls == 2) {
-      cnt = (int64_t)m.bq * m.bk;
-    } else if (bcls == 1) {
-      for (int32_t di = 0; di < m.bq; ++di) {
+    if (band_block_class(m, A, W, r, c) == 2) cnt = (int64_t)m.bq * m.bk;
+  }
+  if (m.qseg != nullptr) {
+    // band-partial blocks: their rows' band counts summed by the whole warp
+    // (one such block per lane at a time; lanes take rows lane, lane+32, ...)
+    int64_t A, W;
+    band_limits(m, A, W);
+    const bool bpart = c < m.nk && band_block_class(m, A, W, r, c) == 1;
+    unsigned need = __ballot_sync(0xffffffffu, bpart);
+    const int lane = threadIdx.x & 31;
+    while (need != 0u) {
+      const int src = __ffs(need) - 1;
+      need &= need - 1u;
+      const int64_t cc = __shfl_sync(0xffffffffu, c, src);
+      int64_t part = 0;
+      for (int32_t di = lane; di < m.bq; di += 32) {
         int64_t lo, hi;
-        band_range(m, r * m.bq + di, c0, c1, lo, hi);
-        if (hi >= lo) cnt += hi - lo + 1;
+        band_range(m, r * m.bq + di, cc * m.bk, cc * m.bk + m.bk - 1, lo, hi);
+        if (hi >= lo) part += hi - lo + 1;
       }
+      for (int off = 16; off; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+      if (lane == src) cnt = part;
     }
-    if (cnt > 0 && m.qseg != nullptr) {
-      const int32_t qmn = qsum[row * 2], qmx = qsum[row * 2 + 1];
-      const int32_t kmn = kvsum[((int64_t)bm * m.nk + c) * 2], kmx = kvsum[((int64_t)bm * m.nk + c) * 2 + 1];
-      if (qmx < kmn || kmx < qmn) {
-        cnt = 0;  // no segment id in common
-      } else if (!(qmn == qmx && kmn == kmx && qmn == kmn)) {
-        undecided = true;  // handled below, with the whole warp
-      }
-      // (both constant and equal: the band count stands)
+  }
+  if (m.qseg != nullptr && c < m.nk && cnt > 0) {
+    const int32_t qmn = qsum[row * 2], qmx = qsum[row * 2 + 1];
+    const int32_t kmn = kvsum[((int64_t)bm * m.nk + c) * 2], kmx = kvsum[((int64_t)bm * m.nk + c) * 2 + 1];
+    if (qmx < kmn || kmx < qmn) {
+      cnt = 0;  // no segment id in common
+    } else if (!(qmn == qmx && kmn == kmx && qmn == kmn)) {
+      undecided = true;  // handled below, with the whole warp
     }
+    // (both constant and equal: the band count stands)
   }
   if (m.qseg != nullptr) {
     // undecided blocks: counted by count_deferred_kernel while the list has
@@ -365,21 +417,24 @@ __device__ void count_deferred_body(const DevMask &m, const int32_t *deferred, i
     const int64_t row = idx / m.nk, c = idx - row * m.nk;
     const int32_t bm = (int32_t)(row / m.nq);
     const int64_t r = row - (int64_t)bm * m.nq;
+    // (the first row's query ID is loaded beside the key IDs)
+    const int32_t sq0 = di < m.bq ? q_segment_early(m, bm, r * m.bq + di) : 0;
     const bool sorted = stage_kv_ids(m, bm, c, s_kv);
     unsigned long long cnt = 0;
+    // (bq and the block's thread count are multiples of 32: the loop's trip
+    // count is the same for every lane of a warp, as sorted_run_warp needs)
     for (int32_t d = di; d < m.bq; d += blockDim.x) {
       const int64_t i = r * m.bq + d;
       int64_t lo, hi;
       band_range(m, i, c * m.bk, c * m.bk + m.bk - 1, lo, hi);
+      const int32_t sq = d == di ? sq0 : q_segment(m, bm, i);
+      int32_t a = 0, b = -1;
+      if (sorted) sorted_run_warp(s_kv, block_keys(m, c), sq, a, b);
       if (hi >= lo) {
-        const int32_t sq = q_segment(m, bm, i);
-        if (sorted) {
-          int32_t a, b;
-          sorted_run(s_kv, block_keys(m, c), sq, a, b);
+        if (sorted)
           cnt += (unsigned long long)max((int64_t)0, min(hi, c * m.bk + b) - max(lo, c * m.bk + a) + 1);
-        } else {
+        else
           for (int64_t j = lo; j <= hi; ++j) cnt += (s_kv[j - c * m.bk] == sq);
-        }
       }
     }
     for (int off = 16; off; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
@@ -512,27 +567,39 @@ __device__ __forceinline__ void compact_warp(const DevMask &m, int64_t row, int3
   const int32_t r = (int32_t)(row % m.nq);
   int32_t g = g0, k = k0;
   const unsigned lt = (1u << lane) - 1u;
-  for (int64_t cb = 0; cb < m.nk; cb += 32) {
-    const int64_t c = cb + lane;
-    const int cls = c < m.nk ? block_mask[row * m.nk + c] : 0;
-    const unsigned act = __ballot_sync(0xffffffffu, cls != 0);
-    const unsigned par = __ballot_sync(0xffffffffu, cls == 1);
-    if (cls != 0) {
-      const int32_t pos = g + __popc(act & lt);
-      active_rows[pos] = r;
-      active_cols[pos] = (int32_t)c;
-      mask_next[pos] = -1;
-      bounds_start[pos] = (uint8_t)(pos == g0);
-      bounds_end[pos] = (uint8_t)(pos == gend - 1);
-      if (cls == 1) {
-        const int32_t kk = k + __popc(par & lt);
-        part_row[kk] = (int32_t)row;
-        part_col[kk] = (int32_t)c;
-        part_g[kk] = pos;
-      }
+  // the row's classes are loaded 256 columns (8 chunks) at a time, then placed
+  for (int64_t cb0 = 0; cb0 < m.nk; cb0 += 256) {
+    int cl[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const int64_t c = cb0 + 32 * t + lane;
+      cl[t] = c < m.nk ? block_mask[row * m.nk + c] : 0;
     }
-    g += __popc(act);
-    k += __popc(par);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const int64_t cb = cb0 + 32 * t;
+      if (cb >= m.nk) break;
+      const int64_t c = cb + lane;
+      const int cls = cl[t];
+      const unsigned act = __ballot_sync(0xffffffffu, cls != 0);
+      const unsigned par = __ballot_sync(0xffffffffu, cls == 1);
+      if (cls != 0) {
+        const int32_t pos = g + __popc(act & lt);
+        active_rows[pos] = r;
+        active_cols[pos] = (int32_t)c;
+        mask_next[pos] = -1;
+        bounds_start[pos] = (uint8_t)(pos == g0);
+        bounds_end[pos] = (uint8_t)(pos == gend - 1);
+        if (cls == 1) {
+          const int32_t kk = k + __popc(par & lt);
+          part_row[kk] = (int32_t)row;
+          part_col[kk] = (int32_t)c;
+          part_g[kk] = pos;
+        }
+      }
+      g += __popc(act);
+      k += __popc(par);
+    }
   }
 }
 
@@ -873,7 +940,7 @@ struct GridArgs {
   unsigned long long *ht_key;
   int32_t *ht_val;
   int64_t ht_mask;  // table size - 1 (a power of two, at least twice the partial blocks)
-  unsigned int *sync;  // [2]: arrivals, generation (arrivals 0 at launch)
+  unsigned int *sync;  // [2]: the grid barrier's arrival counter (0 at launch), spare
   uint32_t *err;
 };
 
@@ -900,6 +967,7 @@ __device__ __forceinline__ void stage_kv_ids_warp(const DevMask &m, int32_t bm, 
 
 __device__ __forceinline__ unsigned long long table_key(uint64_t h) { return h != 0 ? h : 1ull; }
 
+
 __device__ void hash_warp(const DevMask &m, const GridArgs &a, int64_t k, int32_t *s_kv) {
   const int lane = threadIdx.x & 31;
   const int32_t words = m.bk / 32;
@@ -909,22 +977,30 @@ __device__ void hash_warp(const DevMask &m, const GridArgs &a, int64_t k, int32_
   // band-only whole blocks: the diagonal offset identifies the content
   // exactly (no words are stored; materialize computes them)
   const bool by_offset = m.qseg == nullptr && !m.ragged;
+  // the query IDs of this lane's rows (di = lane + 32 x, bq <= 256) are
+  // loaded together, beside the key IDs, instead of one per row
+  int32_t sqr[8];
+#pragma unroll
+  for (int x = 0; x < 8; ++x) sqr[x] = (lane + 32 * x < m.bq) ? q_segment_early(m, bm, r * m.bq + lane + 32 * x) : 0;
   bool sorted = false;
   if (m.qseg != nullptr) stage_kv_ids_warp(m, bm, c, s_kv, sorted);
   uint32_t *dst = a.part_bits + k * m.bq * words;
   uint64_t t = 0;
-  for (int32_t di = lane; di < m.bq && !by_offset; di += 32) {
+#pragma unroll
+  for (int x = 0; x < 8; ++x) {
+    const int32_t di = lane + 32 * x;
+    if (di >= m.bq || by_offset) break;
     const int64_t i = r * m.bq + di;
-    const int32_t sq = q_segment(m, bm, i);
+    const int32_t sq = sqr[x];
     int32_t ra = 0, rb = -1;
-    if (sorted) sorted_run(s_kv, block_keys(m, c), sq, ra, rb);
+    if (sorted) sorted_run_warp(s_kv, block_keys(m, c), sq, ra, rb);  // warp-uniform
     uint64_t h = kHashBasis;
     for (int32_t w = 0; w < words; ++w) {
-      const uint32_t x = m.qseg != nullptr
-                             ? row_word_staged(m, i, sq, c * m.bk, c * m.bk + w * 32, s_kv, sorted, ra, rb)
-                             : row_word(m, bm, i, sq, c * m.bk + w * 32);
-      dst[di * words + w] = x;
-      h = hash_step(h, x);
+      const uint32_t wv = m.qseg != nullptr
+                              ? row_word_staged(m, i, sq, c * m.bk, c * m.bk + w * 32, s_kv, sorted, ra, rb)
+                              : row_word(m, bm, i, sq, c * m.bk + w * 32);
+      dst[di * words + w] = wv;
+      h = hash_step(h, wv);
     }
     t += row_hash_term(h, di);
   }
@@ -993,43 +1069,51 @@ __device__ __forceinline__ uint64_t build_clock_ns() {
 }
 
 // Grid-wide barrier with a bounded wait; returns false (to every thread of
-// the CTA) when it gave up.  Writes of every CTA before it are visible to
-// every CTA after it (fences around the arrival and the release).
-__device__ bool grid_barrier(unsigned int *sync, uint32_t *err) {
+// the CTA) when it gave up.  One arrival counter that only grows during the
+// launch (cleared before it): barrier number n of the launch completes when
+// the counter reaches n * gridDim.x.  Thread 0 arrives with a release
+// reduction after the CTA's barrier (so the CTA's writes before it are
+// released) and polls with acquire loads (so every write released before the
+// last arrival is visible to the CTA after it).
+__device__ __forceinline__ void grid_arrive_release(unsigned int *counter) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(counter) : "memory");
+}
+__device__ __forceinline__ unsigned int grid_load_acquire(const unsigned int *counter) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+  return v;
+}
+
+__device__ bool grid_barrier(unsigned int *sync, uint32_t *err, unsigned int &nbar) {
   __shared__ int s_ok;
+  ++nbar;
   __syncthreads();
   if (threadIdx.x == 0) {
-    volatile unsigned int *gen = sync + 1;
-    const unsigned int g = *gen;
-    __threadfence();
+    const unsigned int target = nbar * gridDim.x;
+    grid_arrive_release(sync);
     bool ok = true;
-    if (atomicAdd(sync, 1u) == gridDim.x - 1) {
-      atomicExch(sync, 0u);
-      __threadfence();
-      atomicAdd(sync + 1, 1u);
-    } else {
-      const uint64_t t0 = build_clock_ns();
-      while (*gen == g) {
-        if (build_clock_ns() - t0 > kGridBarrierNs) {
-          ok = false;
-          atomicOr(err, SPLASH_DEV_TIMEOUT_BUILD);
-          break;
-        }
-        __nanosleep(32);
+    const uint64_t t0 = build_clock_ns();
+    while (grid_load_acquire(sync) < target) {
+      if (build_clock_ns() - t0 > kGridBarrierNs) {
+        ok = false;
+        atomicOr(err, SPLASH_DEV_TIMEOUT_BUILD);
+        break;
       }
     }
-    __threadfence();
     s_ok = ok ? 1 : 0;
   }
   __syncthreads();
   return s_ok != 0;
 }
 
-__global__ void __launch_bounds__(kGridThreads) build_grid_kernel(DevMask m, GridArgs a) {
+__global__ void __launch_bounds__(kGridThreads, 2) build_grid_kernel(DevMask m, GridArgs a) {
   const int64_t bid = blockIdx.x, nb = gridDim.x;
   const int64_t R = (int64_t)m.nbm * m.nq;
-  const int64_t warps = nb * (kGridThreads / 32), gw = bid * (kGridThreads / 32) + (threadIdx.x >> 5);
+  // warp index for the per-warp loops, CTA-minor: consecutive work units go
+  // to different CTAs (so to every SM) before a CTA's second warp takes one
+  const int64_t warps = nb * (kGridThreads / 32), gw = (int64_t)(threadIdx.x >> 5) * nb + bid;
   const bool seg = m.qseg != nullptr;
+  unsigned int nbar = 0;  // grid barriers passed
   // K1: totals and row counters cleared; segment summaries
   if (bid == 0 && threadIdx.x < 8) a.counters[threadIdx.x] = 0ull;
   if (seg) {
@@ -1045,7 +1129,7 @@ __global__ void __launch_bounds__(kGridThreads) build_grid_kernel(DevMask m, Gri
     a.ht_key[x] = 0ull;
     a.ht_val[x] = INT_MAX;
   }
-  if (!grid_barrier(a.sync, a.err)) return;
+  if (!grid_barrier(a.sync, a.err, nbar)) return;
   // K2: classes, row counts, allowed pairs; undecided blocks to the deferred list
   {
     const int64_t xcs = (m.nk + kGridThreads - 1) / kGridThreads;
@@ -1055,11 +1139,11 @@ __global__ void __launch_bounds__(kGridThreads) build_grid_kernel(DevMask m, Gri
                     a.counters, seg ? a.rep_list : nullptr, a.NB);
     }
   }
-  if (!grid_barrier(a.sync, a.err)) return;
+  if (!grid_barrier(a.sync, a.err, nbar)) return;
   if (seg) {
     // the deferred list lives in rep_list, which scan_finalize fills later
     count_deferred_body(m, a.rep_list, a.NB, a.block_mask, a.row_cnt, a.row_pcnt, a.counters, bid, nb);
-    if (!grid_barrier(a.sync, a.err)) return;
+    if (!grid_barrier(a.sync, a.err, nbar)) return;
   }
   // K3: row_ptr, partial offsets, row order and the active lists
   {
@@ -1107,22 +1191,22 @@ __global__ void __launch_bounds__(kGridThreads) build_grid_kernel(DevMask m, Gri
         __syncthreads();
         row_order_body(R, m.nk, a.row_cnt, a.row_hist, a.row_order);
       }
-      if (!grid_barrier(a.sync, a.err)) return;
+      if (!grid_barrier(a.sync, a.err, nbar)) return;
       for (int64_t row = gw; row < R; row += warps)
         compact_warp(m, row, a.row_ptr[row], a.row_ptr[row + 1], a.prow_ptr[row], a.block_mask, a.active_rows,
                      a.active_cols, a.mask_next, a.bounds_start, a.bounds_end, a.part_row, a.part_col, a.part_g);
     }
-    if (!grid_barrier(a.sync, a.err)) return;
+    if (!grid_barrier(a.sync, a.err, nbar)) return;
     // words and hashes (one warp per partial block)
     for (int64_t k = gw; k < (int64_t)a.counters[1]; k += warps) hash_warp(m, a, k, kv);
-    if (!grid_barrier(a.sync, a.err)) return;
+    if (!grid_barrier(a.sync, a.err, nbar)) return;
     // first occurrences (one warp per partial block)
     const int64_t Ap = (int64_t)a.counters[1];
     for (int64_t k = gw; k < Ap; k += warps) dedup_warp(m, a, k);
   }
-  if (!grid_barrier(a.sync, a.err)) return;
+  if (!grid_barrier(a.sync, a.err, nbar)) return;
   if (bid == 0) scan_finalize_body(a.counters, a.part_g, a.part_rep, a.part_pidx, a.mask_next, a.rep_list);
-  if (!grid_barrier(a.sync, a.err)) return;
+  if (!grid_barrier(a.sync, a.err, nbar)) return;
   {
     int64_t P = (int64_t)a.counters[2];
     if (P > a.cap_patterns) {
