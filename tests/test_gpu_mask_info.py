@@ -85,17 +85,17 @@ def test_fuzzed_masks_bit_exact(bsf, n, L, bq, bk, causal, wl, wr, kind, seed):
 
 # Band-only masks (no segment IDs) are built either by one single-CTA kernel
 # (tables up to 2048 q-block rows, 2048 kv-blocks and 65536 blocks) or by the
-# multi-kernel pipeline; both take the block classes in closed form.  Shapes on
-# both sides of each limit, square and rectangular.
+# one-launch persistent build; both take the block classes in closed form.
+# Shapes on both sides of each limit, square and rectangular.
 BAND_CASES = [
     # Lq, Lk, bq, bk, causal, wl, wr
     (131072, 2048, 64, 64, True, -1, -1),      # single CTA: 2048 rows x 32 (row limit)
     (2048, 131072, 128, 64, False, 700, 3000),  # single CTA: 16 rows x 2048 (column limit)
     (16384, 16384, 64, 64, True, 4095, 0),      # single CTA: 256 x 256 = 65536 blocks
     (16384, 16384, 64, 128, False, 100, 100),   # single CTA, bq != bk
-    (20480, 20480, 64, 64, True, -1, -1),       # multi-kernel: 320 x 320 blocks
-    (8192, 139264, 64, 64, True, 2000, -1),     # multi-kernel: 2176 kv-blocks
-    (3000 * 64, 128, 64, 64, False, 10, 10),    # multi-kernel: 3000 rows
+    (20480, 20480, 64, 64, True, -1, -1),       # one launch: 320 x 320 blocks
+    (8192, 139264, 64, 64, True, 2000, -1),     # one launch: 2176 kv-blocks
+    (3000 * 64, 128, 64, 64, False, 10, 10),    # one launch, 3000 rows (single-CTA scan)
 ]
 
 
@@ -103,6 +103,34 @@ BAND_CASES = [
 def test_band_masks_both_build_paths(bsf, Lq, Lk, bq, bk, causal, wl, wr):
     got, ref = gpu_and_oracle(bsf, causal, wl, wr, None, None, Lq, Lk, bq, bk)
     assert_same(got, ref, f"{Lq}x{Lk} {bq}x{bk} causal={causal} window=({wl},{wr})")
+
+
+# The build is one persistent launch up to 4M blocks and a bound of 65,536
+# partial blocks (the blocks the band part alone leaves non-empty with segment
+# IDs; 2 * (ceil((bq-1)/bk) + 1) per q-block row without them); past that it
+# is the chain of nine kernels.  Inside the one launch, tables of more than
+# 2048 q-block rows place their rows with a single-CTA scan.  Each path is
+# compared bit for bit with the oracle.
+PATH_CASES = [
+    # label, Lq, Lk, bq, bk, causal, wl, wr, segments (0 none, 1 documents, 2 q and kv IDs of their own)
+    ("chain: documents + causal, 512 x 512 blocks of 64", 32768, 32768, 64, 64, True, -1, -1, 1),
+    ("chain: band only, 20000 rows x 8 columns", 20000 * 64, 512, 64, 64, False, 60, 100, 0),
+    ("one launch, 2100 rows (single-CTA scan): q / kv IDs of their own", 2100 * 64, 256, 64, 64, False, -1, -1, 2),
+]
+
+
+@pytest.mark.parametrize("case", PATH_CASES, ids=[c[0] for c in PATH_CASES])
+def test_build_paths_beyond_the_one_launch_limits(bsf, case):
+    label, Lq, Lk, bq, bk, causal, wl, wr, segs = case
+    seg_q = seg_kv = None
+    if segs == 1:
+        lens = workloads.document_lengths(Lq, 77, mean=1500, lo=64, hi=6000)
+        seg_q = seg_kv = workloads.segment_ids_from_lengths(lens)
+    elif segs == 2:
+        seg_q = workloads.random_segment_ids(1, Lq, 78, 5, True)
+        seg_kv = workloads.random_segment_ids(1, Lk, 79, 5, True)
+    got, ref = gpu_and_oracle(bsf, causal, wl, wr, seg_q, seg_kv, Lq, Lk, bq, bk)
+    assert_same(got, ref, label)
 
 
 def test_rebuild_reuses_the_handle(bsf):
