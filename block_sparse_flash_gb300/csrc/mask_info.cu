@@ -774,8 +774,9 @@ dedup_kernel(DevMask m, const unsigned long long *counters, const int32_t *part_
 // in partial order gives each representative its pattern index (P = the
 // total); then every partial block's mask_next and the pattern list
 // (partial index of pattern u).
-__device__ void scan_finalize_body(unsigned long long *counters, const int32_t *part_g, const int32_t *part_rep,
-                                   int32_t *part_pidx, int32_t *mask_next, int32_t *rep_list) {
+// The pattern indices (one CTA): part_pidx[k] = the first occurrences among
+// partial blocks 0 .. k-1, and their total P in counters[2].
+__device__ void scan_reps_body(unsigned long long *counters, const int32_t *part_rep, int32_t *part_pidx) {
   __shared__ int buf[33];
   const int64_t Ap = (int64_t)counters[1];
   int carry = 0;
@@ -788,6 +789,12 @@ __device__ void scan_finalize_body(unsigned long long *counters, const int32_t *
     carry += tot;
   }
   if (threadIdx.x == 0) counters[2] = (unsigned long long)carry;
+}
+
+__device__ void scan_finalize_body(unsigned long long *counters, const int32_t *part_g, const int32_t *part_rep,
+                                   int32_t *part_pidx, int32_t *mask_next, int32_t *rep_list) {
+  const int64_t Ap = (int64_t)counters[1];
+  scan_reps_body(counters, part_rep, part_pidx);
   __syncthreads();  // part_pidx is complete
   for (int64_t k = threadIdx.x; k < Ap; k += blockDim.x) {
     const int32_t rep = part_rep[k];
@@ -1205,19 +1212,25 @@ __global__ void __launch_bounds__(kGridThreads, 2) build_grid_kernel(DevMask m, 
     for (int64_t k = gw; k < Ap; k += warps) dedup_warp(m, a, k);
   }
   if (!grid_barrier(a.sync, a.err, nbar)) return;
-  if (bid == 0) scan_finalize_body(a.counters, a.part_g, a.part_rep, a.part_pidx, a.mask_next, a.rep_list);
+  if (bid == 0) scan_reps_body(a.counters, a.part_rep, a.part_pidx);
   if (!grid_barrier(a.sync, a.err, nbar)) return;
   {
-    int64_t P = (int64_t)a.counters[2];
-    if (P > a.cap_patterns) {
-      if (bid == 0 && threadIdx.x == 0) atomicOr(a.err, SPLASH_DEV_BAD_TABLE);
-      P = a.cap_patterns;
-    }
+    // one warp per partial block: its mask_next entry, and for a first
+    // occurrence its place in the pattern list and its pattern
+    const int64_t P = (int64_t)a.counters[2];
+    if (P > a.cap_patterns && bid == 0 && threadIdx.x == 0) atomicOr(a.err, SPLASH_DEV_BAD_TABLE);
+    const int64_t Ap = (int64_t)a.counters[1];
     const int32_t words = m.bk / 32;
     const int64_t n = (int64_t)m.bq * words;
     const bool by_offset = m.qseg == nullptr && !m.ragged;
-    for (int64_t u = gw; u < P; u += warps) {
-      const int64_t k = a.rep_list[u];
+    for (int64_t k = gw; k < Ap; k += warps) {
+      const int32_t rep = a.part_rep[k];
+      const int64_t u = a.part_pidx[rep];
+      if ((threadIdx.x & 31) == 0) {
+        a.mask_next[a.part_g[k]] = (int32_t)u;
+        if (rep == k) a.rep_list[u] = (int32_t)k;
+      }
+      if (rep != k || u >= a.cap_patterns) continue;
       uint32_t *dst = a.pattern_bits + u * n;
       if (by_offset) {  // band only: the words in closed form
         const int64_t row = a.part_row[k], c = a.part_col[k];
