@@ -12,7 +12,13 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libsplash.so")
-SOURCES = ["api.cu", "mask_info.cu", "attention_fwd.cu", "attention_bwd.cu", "host_pipeline.cu"]
+# (source, object, defines): attention_fwd.cu is compiled once per pattern
+# mode, so that its kernel instantiations build in parallel
+SOURCES = [("api.cu", "api", []), ("mask_info.cu", "mask_info", []),
+           ("attention_fwd.cu", "attention_fwd", ["-DSPLASH_FWD_PM=0"]),
+           ("attention_fwd.cu", "attention_fwd_band", ["-DSPLASH_FWD_PM=1"]),
+           ("attention_fwd.cu", "attention_fwd_band_seg", ["-DSPLASH_FWD_PM=2"]),
+           ("attention_bwd.cu", "attention_bwd", []), ("host_pipeline.cu", "host_pipeline", [])]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 
@@ -35,9 +41,10 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
         return LIB
     nvcc = _nvcc()
 
-    def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.splitext(src)[0] + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
+    def compile_one(entry):
+        src, name, defines = entry
+        obj = os.path.join(OUT_DIR, name + ".o")
+        cmd = [nvcc, *ARCH, *FLAGS, *defines, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")

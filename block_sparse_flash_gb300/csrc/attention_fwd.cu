@@ -1754,14 +1754,20 @@ splash_status launch_shape(const void *q, const void *k, const void *v, const Fw
 
 using namespace splash;
 
-splash_status splash_attention_fwd_launch(const void *q, const void *k, const void *v, int32_t B,
-                                          int32_t Hq, int32_t Hkv, int64_t Lq, int64_t Lk,
-                                          int32_t dqk, int32_t dv, const int32_t *q_segment_ids,
-                                          const int32_t *kv_segment_ids, const splash_mask_info *mi,
-                                          float scale, float softcap, float max_logit, void *out,
-                                          float *lse, int32_t nsplit, float *o_part, float *lse_part,
-                                          cudaStream_t stream, uint32_t *err_word) {
-  FwdParams prm;
+namespace {
+
+// The pattern source of a MaskInfo: stored, or from positions (with segment
+// IDs when the table has them).
+int pattern_mode(const splash_mask_info *mi) {
+  return !mi->patterns_from_positions ? kPatStored : (mi->has_segments ? kPatBandSeg : kPatBand);
+}
+
+// The kernel parameters of a forward call (SPLASH_OK) or the argument error.
+splash_status make_fwd_params(int32_t B, int32_t Hq, int32_t Hkv, int64_t Lq, int64_t Lk,
+                              const int32_t *q_segment_ids, const int32_t *kv_segment_ids,
+                              const splash_mask_info *mi, float scale, float softcap, float max_logit, void *out,
+                              float *lse, int32_t nsplit, float *o_part, float *lse_part, uint32_t *err_word,
+                              FwdParams &prm) {
   prm.B = B;
   prm.Hq = Hq;
   prm.Hkv = Hkv;
@@ -1788,7 +1794,7 @@ splash_status splash_attention_fwd_launch(const void *q, const void *k, const vo
   prm.pattern_bits = mi->pattern_bits;
   // pattern source: stored, or from positions (with segment IDs when the
   // table has them; the caller passes the arrays it was built from)
-  const int pm = !mi->patterns_from_positions ? kPatStored : (mi->has_segments ? kPatBandSeg : kPatBand);
+  const int pm = pattern_mode(mi);
   if (pm == kPatBandSeg && q_segment_ids == nullptr) return SPLASH_ERR_INVALID_ARG;
   prm.band_bits = pm != kPatStored ? 1 : 0;
   prm.seg_q = q_segment_ids;
@@ -1819,15 +1825,50 @@ splash_status splash_attention_fwd_launch(const void *q, const void *k, const vo
   prm.lse = lse;
   prm.err = err_word;
   prm.timeout_ns = 1000000000ull;  // 1 s per wait
-  const int bk = mi->bk;
-  if (prm.use_softcap) {
-    if (pm == kPatBandSeg) return launch_shape<kPatBandSeg, true>(q, k, v, prm, dqk, dv, bk, stream);
-    if (pm == kPatBand) return launch_shape<kPatBand, true>(q, k, v, prm, dqk, dv, bk, stream);
-    return launch_shape<kPatStored, true>(q, k, v, prm, dqk, dv, bk, stream);
+  return SPLASH_OK;
+}
+
+}  // namespace
+
+// The launcher of one pattern mode (its kernels only are compiled here).
+#define SPLASH_FWD_MODE_LAUNCHER(PM, NAME)                                                                        \
+  splash_status NAME(const void *q, const void *k, const void *v, int32_t B, int32_t Hq, int32_t Hkv, int64_t Lq, \
+                     int64_t Lk, int32_t dqk, int32_t dv, const int32_t *q_segment_ids,                          \
+                     const int32_t *kv_segment_ids, const splash_mask_info *mi, float scale, float softcap,     \
+                     float max_logit, void *out, float *lse, int32_t nsplit, float *o_part, float *lse_part,    \
+                     cudaStream_t stream, uint32_t *err_word) {                                                  \
+    FwdParams prm;                                                                                               \
+    const splash_status st = make_fwd_params(B, Hq, Hkv, Lq, Lk, q_segment_ids, kv_segment_ids, mi, scale,       \
+                                             softcap, max_logit, out, lse, nsplit, o_part, lse_part, err_word,   \
+                                             prm);                                                               \
+    if (st != SPLASH_OK) return st;                                                                              \
+    if (prm.use_softcap) return launch_shape<PM, true>(q, k, v, prm, dqk, dv, mi->bk, stream);                 \
+    return launch_shape<PM, false>(q, k, v, prm, dqk, dv, mi->bk, stream);                                      \
   }
-  if (pm == kPatBandSeg) return launch_shape<kPatBandSeg, false>(q, k, v, prm, dqk, dv, bk, stream);
-  if (pm == kPatBand) return launch_shape<kPatBand, false>(q, k, v, prm, dqk, dv, bk, stream);
-  return launch_shape<kPatStored, false>(q, k, v, prm, dqk, dv, bk, stream);
+
+#if !defined(SPLASH_FWD_PM) || SPLASH_FWD_PM == 0
+SPLASH_FWD_MODE_LAUNCHER(kPatStored, splash_fwd_launch_stored)
+#endif
+#if !defined(SPLASH_FWD_PM) || SPLASH_FWD_PM == 1
+SPLASH_FWD_MODE_LAUNCHER(kPatBand, splash_fwd_launch_band)
+#endif
+#if !defined(SPLASH_FWD_PM) || SPLASH_FWD_PM == 2
+SPLASH_FWD_MODE_LAUNCHER(kPatBandSeg, splash_fwd_launch_band_seg)
+#endif
+
+#if !defined(SPLASH_FWD_PM) || SPLASH_FWD_PM == 0
+splash_status splash_attention_fwd_launch(const void *q, const void *k, const void *v, int32_t B,
+                                          int32_t Hq, int32_t Hkv, int64_t Lq, int64_t Lk,
+                                          int32_t dqk, int32_t dv, const int32_t *q_segment_ids,
+                                          const int32_t *kv_segment_ids, const splash_mask_info *mi,
+                                          float scale, float softcap, float max_logit, void *out,
+                                          float *lse, int32_t nsplit, float *o_part, float *lse_part,
+                                          cudaStream_t stream, uint32_t *err_word) {
+  const int pm = pattern_mode(mi);
+  auto launcher = pm == kPatBandSeg ? splash_fwd_launch_band_seg
+                                    : (pm == kPatBand ? splash_fwd_launch_band : splash_fwd_launch_stored);
+  return launcher(q, k, v, B, Hq, Hkv, Lq, Lk, dqk, dv, q_segment_ids, kv_segment_ids, mi, scale, softcap,
+                  max_logit, out, lse, nsplit, o_part, lse_part, stream, err_word);
 }
 
 splash_status splash_wait_selftest_launch(uint64_t timeout_ns, cudaStream_t stream, uint32_t *err_word) {
@@ -1915,3 +1956,4 @@ splash_status splash_attention_merge_launch(const float *o_part, const float *ls
   splash_count_launches(1);
   return SPLASH_OK;
 }
+#endif  // the entry point, the self test and the merge: the compilation for the stored patterns

@@ -125,6 +125,18 @@ splash_status splash_attention_fwd_launch(const void *q, const void *k, const vo
                                           float scale, float softcap, float max_logit, void *out,
                                           float *lse, int32_t nsplit, float *o_part, float *lse_part,
                                           cudaStream_t stream, uint32_t *err_word);
+// attention_fwd.cu, compiled once per pattern mode (stored, band, band and
+// segment IDs) so that the three sets of kernel instantiations build in
+// parallel: the launchers of each mode (same arguments as
+// splash_attention_fwd_launch, which picks one)
+#define SPLASH_FWD_LAUNCHER_ARGS                                                                                 \
+  const void *q, const void *k, const void *v, int32_t B, int32_t Hq, int32_t Hkv, int64_t Lq, int64_t Lk,      \
+      int32_t dqk, int32_t dv, const int32_t *q_segment_ids, const int32_t *kv_segment_ids,                       \
+      const splash_mask_info *mi, float scale, float softcap, float max_logit, void *out, float *lse,             \
+      int32_t nsplit, float *o_part, float *lse_part, cudaStream_t stream, uint32_t *err_word
+splash_status splash_fwd_launch_stored(SPLASH_FWD_LAUNCHER_ARGS);
+splash_status splash_fwd_launch_band(SPLASH_FWD_LAUNCHER_ARGS);
+splash_status splash_fwd_launch_band_seg(SPLASH_FWD_LAUNCHER_ARGS);
 splash_status splash_attention_merge_launch(const float *o_part, const float *lse_part, int32_t nsplit,
                                             int64_t rows, int32_t dv, void *out, float *lse,
                                             cudaStream_t stream);
