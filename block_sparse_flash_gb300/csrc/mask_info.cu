@@ -27,9 +27,12 @@
 // The pattern buffer is sized from a bound known before the build (no host
 // wait) unless that bound exceeds kPatternBudgetBytes; then the build waits
 // once for the exact pattern count.  Band-only masks (no segment IDs) take
-// the classes in closed form, and small tables run the whole pipeline as one
-// single-CTA kernel (build_small_kernel).
+// the classes in closed form.  Small band tables run the whole pipeline as
+// one single-CTA kernel (build_small_kernel); other tables up to 4M blocks
+// as one persistent cooperative kernel whose phases are separated by a grid
+// barrier (build_grid_kernel); larger ones as the chain of kernels above.
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <mutex>
 
@@ -1736,13 +1739,17 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
     if ((st = map_alloc(grow(mi->ht_key, mi->cap_ht, ht))) != SPLASH_OK) return st;
     if ((st = map_alloc(grow(mi->ht_val, mi->cap_ht, ht))) != SPLASH_OK) return st;
     mi->cap_ht = std::max(mi->cap_ht, ht);
-    static int per_sm[64] = {0};
-    if (dev < 64 && per_sm[dev] == 0) {
+    // CTAs per SM (at most 2), asked once per device; concurrent first
+    // builds on several host threads store the same value
+    static std::atomic<int> per_sm[64] = {};
+    int cps = dev < 64 ? per_sm[dev].load(std::memory_order_relaxed) : 0;
+    if (cps == 0) {
       int n = 0;
       SPLASH_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, build_grid_kernel, kGridThreads, 0));
-      per_sm[dev] = std::max(1, std::min(n, 2));
+      cps = std::max(1, std::min(n, 2));
+      if (dev < 64) per_sm[dev].store(cps, std::memory_order_relaxed);
     }
-    const unsigned grid = (unsigned)(sms * (dev < 64 ? per_sm[dev] : 1));
+    const unsigned grid = (unsigned)(sms * cps);
     GridArgs a;
     a.qsum = qsum;
     a.kvsum = kvsum;
