@@ -667,9 +667,11 @@ def run_reference(args):
     import workloads
     w = bench_workload(args)
     inp = workloads.make_inputs(w)
-    _, dt, nth, n = oracle_sample_rate(w, inp, 128, 3)
+    # the rate from a sample large enough that thread start-up is small
+    # against it; each step's sample is at least 512 rows for the same reason
+    _, dt, nth, n = oracle_sample_rate(w, inp, 1024, 3)
     rate = n / max(dt, 1e-6)
-    per_step = int(min(8192, max(64, rate * 90.0 / max(1, args.steps + args.warmup))))
+    per_step = int(min(8192, max(512, rate * 90.0 / max(1, args.steps + args.warmup))))
     for i in range(args.warmup):
         oracle_sample_rate(w, inp, per_step, 100 + i)
     flops, secs = 0.0, 0.0
