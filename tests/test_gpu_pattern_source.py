@@ -127,3 +127,41 @@ def test_positions_with_segment_ids_need_the_arrays(bsf):
     torch.cuda.synchronize()
     assert bsf.last_device_error() == 0
     mi.close()
+
+
+RECT_CASES = [
+    # label, B_mask, Hq, Hkv, Lq, Lk, d, blk, causal, wl, wr
+    ("700 x 1300, own q / kv IDs, no band", 1, 2, 1, 700, 1300, 128, 128, False, -1, -1),
+    ("1300 x 700, own q / kv IDs, two-sided window, batch 2", 2, 2, 2, 1300, 700, 64, 64, False, 150, 90),
+]
+
+
+@pytest.mark.parametrize("case", RECT_CASES, ids=[c[0] for c in RECT_CASES])
+def test_positions_with_different_q_and_kv_segment_ids(bsf, case):
+    """Lq != Lk with query and key segment arrays of their own (the key IDs
+    indexed by key position, the query IDs by query position): masks from
+    positions and segment IDs equal the stored patterns bit for bit, and the
+    oracle within tolerance."""
+    label, bm, Hq, Hkv, Lq, Lk, d, blk, causal, wl, wr = case
+    seed = 53 * RECT_CASES.index(case) + 11
+    q = workloads.normal_bf16((bm, Hq, Lq, d), seed + 1).cuda()
+    k = workloads.normal_bf16((bm, Hkv, Lk, d), seed + 2).cuda()
+    v = workloads.normal_bf16((bm, Hkv, Lk, d), seed + 3).cuda()
+    sq = workloads.random_segment_ids(bm, Lq, seed + 4, 4, True).cuda()
+    skv = workloads.random_segment_ids(bm, Lk, seed + 5, 4, True).cuda()
+    mi = bsf.build_mask_info(bsf.MaskSpec(causal, wl, wr, sq, skv), Lq, Lk, blk, blk)
+    scale = 1.0 / math.sqrt(d)
+    runs = {}
+    for source in ("stored", "positions"):
+        mi.set_pattern_source(source)
+        runs[source] = bsf.attention_fwd(q, k, v, mi, scale, 0.0, sq, skv)
+    torch.cuda.synchronize()
+    assert bsf.last_device_error() == 0, label
+    assert torch.equal(runs["stored"][0], runs["positions"][0]), label
+    assert torch.equal(runs["stored"][1], runs["positions"][1]), label
+    O, Lse = oracle.attention(q.cpu(), k.cpu(), v.cpu(),
+                              oracle.MaskSpec(causal, wl, wr, sq.cpu().numpy(), skv.cpu().numpy()), scale, 0.0)
+    out, lse = runs["positions"]
+    compare_rows(out.float().cpu().numpy().reshape(-1, d), lse.cpu().numpy().reshape(-1),
+                 O.reshape(-1, d), Lse.reshape(-1), label)
+    mi.close()
