@@ -1151,7 +1151,7 @@ __global__ void __launch_bounds__(kGridThreads, 2) build_grid_kernel(DevMask m, 
   }
   if (!grid_barrier(a.sync, a.err, nbar)) return;
   if (seg) {
-    // the deferred list lives in rep_list, which scan_finalize fills later
+    // the deferred list lives in rep_list, which the last phase fills later
     count_deferred_body(m, a.rep_list, a.NB, a.block_mask, a.row_cnt, a.row_pcnt, a.counters, bid, nb);
     if (!grid_barrier(a.sync, a.err, nbar)) return;
   }
