@@ -66,7 +66,7 @@ struct splash_mask_info {
   int32_t *rep_list = nullptr;     // [cap_active] partial index of pattern u
   int32_t *row_hist = nullptr;     // [nk+1] counting-sort bins
   unsigned long long *counters = nullptr;  // [8]: A, A_p, P, allowed, max_row, deferred blocks
-  unsigned int *grid_sync = nullptr;       // [2]: the one-launch build's barrier (arrivals, generation)
+  unsigned int *grid_sync = nullptr;       // the one-launch build: barrier counter, spare, first-occurrence bitmap
   uint32_t *part_bits = nullptr;           // [cap_part_bits] one-launch build: each partial block's words
   unsigned long long *ht_key = nullptr;    // [cap_ht] one-launch build: content hash table (keys)
   int32_t *ht_val = nullptr;               // [cap_ht] smallest partial index per key

@@ -931,6 +931,11 @@ constexpr uint64_t kGridBarrierNs = 2000000000ull;  // 2 s
 constexpr int64_t kGridMaxBlocks = (int64_t)1 << 22;  // larger tables take the launch chain
 constexpr int64_t kGridMaxPartials = 65536;
 constexpr int64_t kGridRowwiseMaxRows = 2048;  // rows a warp scans to place its own row
+// Up to this many partial blocks the first occurrences are also marked in a
+// bitmap (after the barrier's two words), from which each warp counts its
+// block's pattern index itself; larger tables take the single-CTA scan.
+constexpr int64_t kGridWarpScanMaxPartials = 2048;
+constexpr int kGridSyncWords = 2 + (int)(kGridWarpScanMaxPartials / 32);
 
 struct GridArgs {
   int32_t *qsum, *kvsum;
@@ -950,7 +955,10 @@ struct GridArgs {
   unsigned long long *ht_key;
   int32_t *ht_val;
   int64_t ht_mask;  // table size - 1 (a power of two, at least twice the partial blocks)
-  unsigned int *sync;  // [2]: the grid barrier's arrival counter (0 at launch), spare
+  // [kGridSyncWords], zero at launch: the grid barrier's arrival counter, a
+  // spare word, and the first-occurrence bitmap (bit k: partial block k is
+  // the first of its content, for k < kGridWarpScanMaxPartials)
+  unsigned int *sync;
   uint32_t *err;
 };
 
@@ -1069,7 +1077,10 @@ __device__ void dedup_warp(const DevMask &m, const GridArgs &a, int64_t k) {
       }
     }
   }
-  if (lane == 0) a.part_rep[k] = (int32_t)rep;
+  if (lane == 0) {
+    a.part_rep[k] = (int32_t)rep;
+    if (rep == k && k < kGridWarpScanMaxPartials) atomicOr(a.sync + 2 + (k >> 5), 1u << (k & 31));
+  }
 }
 
 __device__ __forceinline__ uint64_t build_clock_ns() {
@@ -1215,20 +1226,45 @@ __global__ void __launch_bounds__(kGridThreads, 2) build_grid_kernel(DevMask m, 
     for (int64_t k = gw; k < Ap; k += warps) dedup_warp(m, a, k);
   }
   if (!grid_barrier(a.sync, a.err, nbar)) return;
-  if (bid == 0) scan_reps_body(a.counters, a.part_rep, a.part_pidx);
-  if (!grid_barrier(a.sync, a.err, nbar)) return;
+  // Pattern indices: the number of first occurrences before each one, and
+  // their total P.  Up to kGridWarpScanMaxPartials partial blocks every warp
+  // counts them in the bitmap itself (two words per lane), so neither a
+  // single-CTA scan nor a grid barrier comes before the last phase.
+  const int64_t Ap = (int64_t)a.counters[1];
+  const bool bitmap = Ap <= kGridWarpScanMaxPartials;
+  const unsigned int *first = a.sync + 2;
+  const int lane = threadIdx.x & 31;
+  if (!bitmap) {
+    if (bid == 0) scan_reps_body(a.counters, a.part_rep, a.part_pidx);
+    if (!grid_barrier(a.sync, a.err, nbar)) return;
+    if (bid == 0 && threadIdx.x == 0 && (int64_t)a.counters[2] > a.cap_patterns) atomicOr(a.err, SPLASH_DEV_BAD_TABLE);
+  } else if (gw == 0) {
+    const int tot = __reduce_add_sync(0xffffffffu, __popc(first[lane]) + __popc(first[lane + 32]));
+    if (lane == 0) {
+      a.counters[2] = (unsigned long long)tot;
+      if (tot > a.cap_patterns) atomicOr(a.err, SPLASH_DEV_BAD_TABLE);
+    }
+  }
   {
     // one warp per partial block: its mask_next entry, and for a first
     // occurrence its place in the pattern list and its pattern
-    const int64_t P = (int64_t)a.counters[2];
-    if (P > a.cap_patterns && bid == 0 && threadIdx.x == 0) atomicOr(a.err, SPLASH_DEV_BAD_TABLE);
-    const int64_t Ap = (int64_t)a.counters[1];
     const int32_t words = m.bk / 32;
     const int64_t n = (int64_t)m.bq * words;
     const bool by_offset = m.qseg == nullptr && !m.ragged;
     for (int64_t k = gw; k < Ap; k += warps) {
       const int32_t rep = a.part_rep[k];
-      const int64_t u = a.part_pidx[rep];
+      int64_t u;
+      if (bitmap) {
+        // bits below rep: whole words before word rep / 32, then that word's low bits
+        const int wr = rep >> 5;
+        const unsigned int lo = first[lane], hi = first[lane + 32];
+        const unsigned int below = (1u << (rep & 31)) - 1u;
+        const int cnt = (lane < wr ? __popc(lo) : (lane == wr ? __popc(lo & below) : 0)) +
+                        (lane + 32 < wr ? __popc(hi) : (lane + 32 == wr ? __popc(hi & below) : 0));
+        u = __reduce_add_sync(0xffffffffu, cnt);
+      } else {
+        u = a.part_pidx[rep];
+      }
       if ((threadIdx.x & 31) == 0) {
         a.mask_next[a.part_g[k]] = (int32_t)u;
         if (rep == k) a.rep_list[u] = (int32_t)k;
@@ -1727,7 +1763,8 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
     // the whole pipeline as one persistent kernel (cooperative launch: every
     // CTA resident; its grid barrier state starts cleared)
     if ((st = reserve_patterns(p_bound)) != SPLASH_OK) return st;
-    if (mi->grid_sync == nullptr && (st = map_alloc(cudaMalloc(&mi->grid_sync, 2 * sizeof(unsigned int)))) != SPLASH_OK)
+    if (mi->grid_sync == nullptr &&
+        (st = map_alloc(cudaMalloc(&mi->grid_sync, kGridSyncWords * sizeof(unsigned int)))) != SPLASH_OK)
       return st;
     // per-partial words (p_bound bounds the partial blocks too) and the hash
     // table, at least twice as large
@@ -1782,7 +1819,7 @@ splash_status splash_mask_info_build_into(splash_mask_info *mi, const splash_mas
     a.ht_mask = ht - 1;
     a.sync = mi->grid_sync;
     a.err = err;
-    SPLASH_CUDA_TRY(cudaMemsetAsync(mi->grid_sync, 0, 2 * sizeof(unsigned int), stream));
+    SPLASH_CUDA_TRY(cudaMemsetAsync(mi->grid_sync, 0, kGridSyncWords * sizeof(unsigned int), stream));
     void *args[] = {&m, &a};
     SPLASH_CUDA_TRY(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(build_grid_kernel), dim3(grid),
                                                 dim3(kGridThreads), args, 0, stream));

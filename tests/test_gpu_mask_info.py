@@ -115,6 +115,8 @@ PATH_CASES = [
     # label, Lq, Lk, bq, bk, causal, wl, wr, segments (0 none, 1 documents, 2 q and kv IDs of their own)
     ("chain: documents + causal, 512 x 512 blocks of 64", 32768, 32768, 64, 64, True, -1, -1, 1),
     ("chain: band only, 20000 rows x 8 columns", 20000 * 64, 512, 64, 64, False, 60, 100, 0),
+    # (3,359 partial blocks: the pattern indices also come from the single-CTA
+    # scan, where smaller tables count them in the first-occurrence bitmap)
     ("one launch, 2100 rows (single-CTA scan): q / kv IDs of their own", 2100 * 64, 256, 64, 64, False, -1, -1, 2),
 ]
 
