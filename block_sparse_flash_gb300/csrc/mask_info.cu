@@ -1337,15 +1337,16 @@ __global__ void __launch_bounds__(kSmallThreads) build_small_kernel(DevMask m, S
   int32_t *s_ppidx = s_prep + PM;                                          // [PM]
   __shared__ int buf_a[33], s_mx[32];
   __shared__ unsigned long long buf_ap[33];
-  __shared__ unsigned long long s_allowed;
+  __shared__ unsigned long long s_allow[32];  // allowed pairs, per warp
+  __shared__ unsigned int s_first[kSmallMaxPartials / 32];  // bit k: partial k is a first occurrence
   __shared__ int64_t s_tot[3];  // A, A_p, P
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int64_t A, W;
   band_limits(m, A, W);
 
   // classes and per-row counts (one warp per row: ballots, no shared-memory
-  // atomics on a row's counters), allowed pairs
-  if (tid == 0) s_allowed = 0;
+  // atomics on a row's counters), allowed pairs (per warp, summed below)
+  for (int x = tid; x < (int)(kSmallMaxPartials / 32); x += kSmallThreads) s_first[x] = 0u;
   for (int64_t r = warp; r < R; r += kSmallThreads / 32) {
     int na = 0, np = 0;
     for (int64_t cb = 0; cb < nk; cb += 32) {
@@ -1360,11 +1361,10 @@ __global__ void __launch_bounds__(kSmallThreads) build_small_kernel(DevMask m, S
       s_pcnt[r] = np;
     }
   }
-  __syncthreads();
   unsigned long long allowed = 0;
   for (int64_t i = tid; i < m.Lq; i += kSmallThreads) allowed += (unsigned long long)band_row_count(m, A, W, i);
   for (int off = 16; off; off >>= 1) allowed += __shfl_xor_sync(0xffffffffu, allowed, off);
-  if (lane == 0 && allowed) atomicAdd(&s_allowed, allowed);
+  if (lane == 0) s_allow[warp] = allowed;
   __syncthreads();
 
   // row_ptr (CSR), partial offsets and the longest row: one scan of the two
@@ -1391,13 +1391,17 @@ __global__ void __launch_bounds__(kSmallThreads) build_small_kernel(DevMask m, S
   __syncthreads();
   if (tid == 0) {
     int t = 0;
-    for (int x = 0; x < kSmallThreads / 32; ++x) t = max(t, s_mx[x]);
+    unsigned long long allowed_all = 0;
+    for (int x = 0; x < kSmallThreads / 32; ++x) {
+      t = max(t, s_mx[x]);
+      allowed_all += s_allow[x];
+    }
     s_rp[R] = carry_a;
     s_prp[R] = carry_p;
     o.row_ptr[R] = carry_a;
     o.counters[0] = (unsigned long long)carry_a;
     o.counters[1] = (unsigned long long)carry_p;
-    o.counters[3] = s_allowed;
+    o.counters[3] = allowed_all;
     o.counters[4] = (unsigned long long)t;
     s_tot[0] = carry_a;
     s_tot[1] = carry_p;
@@ -1484,33 +1488,29 @@ __global__ void __launch_bounds__(kSmallThreads) build_small_kernel(DevMask m, S
         break;
       }
     }
-    if (lane == 0) s_prep[k] = rep;
+    if (lane == 0) {
+      s_prep[k] = rep;
+      if (rep == k) atomicOr(&s_first[k >> 5], 1u << (k & 31));
+    }
   }
   __syncthreads();
-  // pattern indices of the first occurrences
-  carry = 0;
-  for (int64_t base = 0; base < Ap; base += kSmallThreads) {
-    const int64_t k = base + tid;
-    const int f = (k < Ap && s_prep[k] == k) ? 1 : 0;
-    int tot;
-    const int ex = block_excl_scan(f, tot, buf_a);
-    if (k < Ap) s_ppidx[k] = carry + ex;
-    carry += tot;
-  }
-  if (tid == 0) {
-    o.counters[2] = (unsigned long long)carry;
-    s_tot[2] = carry;
-  }
-  __syncthreads();
-  // mask_next of the partial blocks, then the pattern list (partial index of
-  // pattern u) in the place of s_pg, which is not read again
+  // pattern index of partial k's content: the first occurrences before its
+  // representative, counted in the bitmap; the mask_next entry, and for a
+  // first occurrence its place in the pattern list (s_ppidx: partial index
+  // of pattern u)
   for (int64_t k = tid; k < Ap; k += kSmallThreads) {
     const int32_t rep = s_prep[k];
-    o.mask_next[s_pg[k]] = s_ppidx[rep];
+    int32_t u = __popc(s_first[rep >> 5] & ((1u << (rep & 31)) - 1u));
+    for (int32_t w = 0; w < (rep >> 5); ++w) u += __popc(s_first[w]);
+    o.mask_next[s_pg[k]] = u;
+    if (rep == k) s_ppidx[u] = (int32_t)k;
   }
-  __syncthreads();
-  for (int64_t k = tid; k < Ap; k += kSmallThreads)
-    if (s_prep[k] == k) s_pg[s_ppidx[k]] = (int32_t)k;  // s_pg becomes the pattern list
+  if (tid == 0) {
+    int32_t P = 0;
+    for (int32_t w = 0; w < (int32_t)((Ap + 31) >> 5); ++w) P += __popc(s_first[w]);
+    o.counters[2] = (unsigned long long)P;
+    s_tot[2] = P;
+  }
   __syncthreads();
   // the patterns, bit-packed (word w of row di of pattern u holds keys
   // 32w .. 32w+31): one word per thread, consecutive threads on consecutive words
@@ -1523,7 +1523,7 @@ __global__ void __launch_bounds__(kSmallThreads) build_small_kernel(DevMask m, S
   for (int64_t x = tid; x < P * per_pattern; x += kSmallThreads) {
     const int64_t u = x / per_pattern;
     const int32_t rem = (int32_t)(x - u * per_pattern), di = rem / words, w = rem - di * words;
-    const int64_t k = s_pg[u];
+    const int64_t k = s_ppidx[u];
     o.pattern_bits[x] = row_word(m, 0, (int64_t)s_prow[k] * m.bq + di, 0, (int64_t)s_pcol[k] * m.bk + w * 32);
   }
 }
