@@ -919,7 +919,9 @@ scan_order_kernel(int64_t R, int64_t nk, const int32_t *row_cnt, const int32_t *
 // ---------------------------------------------------------------- one-launch build
 // The pipeline K1 .. materialize as one persistent kernel: every CTA runs each
 // phase on its share of the work (the bodies above with a grid stride; the
-// two scans on CTA 0), and a grid-wide barrier separates the phases.  It
+// row and pattern-index scans are counted per warp up to the limits below,
+// and beyond them run on CTA 0), and a grid-wide barrier separates the
+// phases.  It
 // replaces nine dependent launches, each of which costs a few microseconds of
 // launch and drain latency at these sizes.  The launch is cooperative, so
 // that every CTA is resident and the barrier can complete; the barrier itself
