@@ -921,9 +921,8 @@ scan_order_kernel(int64_t R, int64_t nk, const int32_t *row_cnt, const int32_t *
 // phase on its share of the work (the bodies above with a grid stride; the
 // row and pattern-index scans are counted per warp up to the limits below,
 // and beyond them run on CTA 0), and a grid-wide barrier separates the
-// phases.  It
-// replaces nine dependent launches, each of which costs a few microseconds of
-// launch and drain latency at these sizes.  The launch is cooperative, so
+// phases.  It replaces nine dependent launches, each of which costs a few
+// microseconds of launch and drain latency at these sizes.  The launch is cooperative, so
 // that every CTA is resident and the barrier can complete; the barrier itself
 // is this file's own, with a bounded wait: a CTA that waits longer than
 // kGridBarrierNs sets SPLASH_DEV_TIMEOUT_BUILD and stops (the others then
@@ -1239,7 +1238,8 @@ __global__ void __launch_bounds__(kGridThreads, 2) build_grid_kernel(DevMask m, 
   if (!bitmap) {
     if (bid == 0) scan_reps_body(a.counters, a.part_rep, a.part_pidx);
     if (!grid_barrier(a.sync, a.err, nbar)) return;
-    if (bid == 0 && threadIdx.x == 0 && (int64_t)a.counters[2] > a.cap_patterns) atomicOr(a.err, SPLASH_DEV_BAD_TABLE);
+    if (bid == 0 && threadIdx.x == 0 && (int64_t)a.counters[2] > a.cap_patterns)
+      atomicOr(a.err, SPLASH_DEV_BAD_TABLE);
   } else if (gw == 0) {
     const int tot = __reduce_add_sync(0xffffffffu, __popc(first[lane]) + __popc(first[lane + 32]));
     if (lane == 0) {
@@ -1291,8 +1291,9 @@ __global__ void __launch_bounds__(kGridThreads, 2) build_grid_kernel(DevMask m, 
 // with a small table.  Every phase is a loop over the CTA's 1024 threads with
 // __syncthreads between phases; the block classes come from the closed form,
 // and every intermediate (row counts and offsets, row-order bins, the partial
-// blocks' coordinates, hashes, representatives and pattern indices) stays in
-// shared memory (global memory is only written: the table itself).  Partial
+// blocks' coordinates and diagonal offsets, their representatives, the
+// first-occurrence bitmap and the pattern list) stays in shared memory
+// (global memory is only written: the table itself).  Partial
 // blocks are deduplicated by their diagonal offset d = c*bk - r*bq: under a
 // band mask the pattern of a block is {(i', j'): L <= j' - i' <= U} with L, U
 // shifted by -d, and for partial blocks (neither empty nor full) the clipped
@@ -1336,7 +1337,7 @@ __global__ void __launch_bounds__(kSmallThreads) build_small_kernel(DevMask m, S
   int32_t *s_pcol = s_prow + PM;                                           // [PM]
   int32_t *s_pg = s_pcol + PM;                                             // [PM]
   int32_t *s_prep = s_pg + PM;                                             // [PM]
-  int32_t *s_ppidx = s_prep + PM;                                          // [PM]
+  int32_t *s_ppidx = s_prep + PM;                                          // [PM] pattern list
   __shared__ int buf_a[33], s_mx[32];
   __shared__ unsigned long long buf_ap[33];
   __shared__ unsigned long long s_allow[32];  // allowed pairs, per warp
